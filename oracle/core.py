@@ -1,0 +1,238 @@
+"""ctypes wrappers around the C oracle, plus the whole-layer forward chain.
+
+Arrays are numpy.  Values that are bf16 in the layer may be passed either as
+uint16 bit patterns (widened exactly) or as float32 values.  Outputs rounded to
+bf16 come back as float32 arrays holding bf16 values.
+"""
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "libmoe_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ACT = {"relu": 0, "gelu": 1, "swiglu": 2}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP when available).  Returns the .so path."""
+    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
+        return _SO
+    os.makedirs(_BUILD, exist_ok=True)
+    tmp = _SO + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+            "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _SO)
+    return _SO
+
+
+def _L():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P, I64, I32, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
+            sig = {
+                "orc_gate_logits": [P, P, P, I64, I32, I32, P],
+                "orc_topk": [P, I64, I32, I32, P],
+                "orc_gates": [P, P, I64, I32, I32, I32, P],
+                "orc_locations": [P, I64, I32, I32, P, P],
+                "orc_capacity": [D, I64, I32, I32, P],
+                "orc_encode": [P, P, P, I64, I64, I32, I32, I32, I64, P],
+                "orc_decode": [P, P, P, P, I64, I64, I32, I32, I32, I64, I32, P],
+                "orc_decode_bwd": [P, P, P, P, P, I64, I64, I32, I32, I32, I64, I32, P, P],
+                "orc_encode_bwd": [P, P, P, I64, I64, I32, I32, I32, I64, I32, P],
+                "orc_ffn_rows": [P, P, P, P, P, P, I32, I32, I64, I32, I32, I32, P, P, I64, P],
+                "orc_round_bf16": [D],
+                "orc_set_threads": [I32],
+                "orc_get_threads": [],
+            }
+            for name, args in sig.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = None
+            lib.orc_capacity.restype = I64
+            lib.orc_round_bf16.restype = ctypes.c_float
+            lib.orc_get_threads.restype = I32
+            _lib = lib
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def to_f32(a):
+    """float32 contiguous view of a tensor given as fp32 values or bf16 bits."""
+    if a is None:
+        return None
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def set_threads(n: int):
+    _L().orc_set_threads(int(n))
+
+
+def get_threads() -> int:
+    return int(_L().orc_get_threads())
+
+
+def round_bf16(v: float) -> float:
+    return float(_L().orc_round_bf16(float(v)))
+
+
+def gate_logits(x, wg, bias=None):
+    """fp32 logits [s, e]; ascending-i fmaf order, then + bias."""
+    x, wg, bias = to_f32(x), to_f32(wg), to_f32(bias)
+    s, m = x.shape
+    e = wg.shape[1]
+    out = np.empty((s, e), np.float32)
+    _L().orc_gate_logits(_p(x), _p(wg), _p(bias), s, m, e, _p(out))
+    return out
+
+
+def topk(logits, k):
+    logits = to_f32(logits)
+    s, e = logits.shape
+    idx = np.empty((k, s), np.int32)
+    _L().orc_topk(_p(logits), s, e, k, _p(idx))
+    return idx
+
+
+def gates(logits, idx, normalize):
+    logits = to_f32(logits)
+    idx = np.ascontiguousarray(idx, np.int32)
+    s, e = logits.shape
+    k = idx.shape[0]
+    g = np.empty((k, s), np.float32)
+    _L().orc_gates(_p(logits), _p(idx), s, e, k, int(bool(normalize)), _p(g))
+    return g
+
+
+def locations(idx, e):
+    idx = np.ascontiguousarray(idx, np.int32)
+    k, s = idx.shape
+    loc = np.empty((k, s), np.int32)
+    needed = np.zeros(e, np.int64)
+    _L().orc_locations(_p(idx), s, e, k, _p(loc), _p(needed))
+    return loc, needed
+
+
+def capacity(f, s, e, k, needed):
+    needed = np.ascontiguousarray(needed, np.int64)
+    return int(_L().orc_capacity(float(np.float32(f)), s, e, k, _p(needed)))
+
+
+def kept_rows(needed, c):
+    return np.minimum(np.asarray(needed, np.int64), c)
+
+
+def encode(x, idx, loc, c, e, cmax, buf=None):
+    x = to_f32(x)
+    idx = np.ascontiguousarray(idx, np.int32)
+    loc = np.ascontiguousarray(loc, np.int32)
+    s, m = x.shape
+    k = idx.shape[0]
+    if buf is None:
+        buf = np.zeros((e, cmax, m), np.float32)
+    _L().orc_encode(_p(x), _p(idx), _p(loc), c, s, m, e, k, cmax, _p(buf))
+    return buf
+
+
+def decode(out, idx, loc, g, c, bf16):
+    out = to_f32(out)
+    e, cmax, m = out.shape
+    idx = np.ascontiguousarray(idx, np.int32)
+    loc = np.ascontiguousarray(loc, np.int32)
+    g = np.ascontiguousarray(g, np.float32)
+    k, s = idx.shape
+    y = np.empty((s, m), np.float32)
+    _L().orc_decode(_p(out), _p(idx), _p(loc), _p(g), c, s, m, e, k, cmax, int(bf16), _p(y))
+    return y
+
+
+def decode_bwd(dy, out, idx, loc, g, c, bf16):
+    dy, out = to_f32(dy), to_f32(out)
+    e, cmax, m = out.shape
+    idx = np.ascontiguousarray(idx, np.int32)
+    loc = np.ascontiguousarray(loc, np.int32)
+    g = np.ascontiguousarray(g, np.float32)
+    k, s = idx.shape
+    d_out = np.zeros((e, cmax, m), np.float32)
+    d_g = np.empty((k, s), np.float32)
+    _L().orc_decode_bwd(_p(dy), _p(out), _p(idx), _p(loc), _p(g), c, s, m, e, k, cmax,
+                        int(bf16), _p(d_out), _p(d_g))
+    return d_out, d_g
+
+
+def encode_bwd(d_buf, idx, loc, c, bf16):
+    d_buf = to_f32(d_buf)
+    e, cmax, m = d_buf.shape
+    idx = np.ascontiguousarray(idx, np.int32)
+    loc = np.ascontiguousarray(loc, np.int32)
+    k, s = idx.shape
+    dx = np.empty((s, m), np.float32)
+    _L().orc_encode_bwd(_p(d_buf), _p(idx), _p(loc), c, s, m, e, k, cmax, int(bf16), _p(dx))
+    return dx
+
+
+def ffn_rows(buf, w1, b1, w3, w2, b2, act, rows_e, rows_j, bf16):
+    """Expert MLP outputs for the listed (expert, row) pairs -> [len(rows), m]."""
+    buf, w1, b1, w3, w2, b2 = (to_f32(a) for a in (buf, w1, b1, w3, w2, b2))
+    e, cmax, m = buf.shape
+    h = w1.shape[1]
+    re = np.ascontiguousarray(rows_e, np.int32)
+    rj = np.ascontiguousarray(rows_j, np.int64)
+    out = np.empty((len(re), m), np.float32)
+    _L().orc_ffn_rows(_p(buf), _p(w1), _p(b1), _p(w3), _p(w2), _p(b2), ACT[act], e, cmax, m, h,
+                      int(bf16), _p(re), _p(rj), len(re), _p(out))
+    return out
+
+
+def layer_forward(w, inp, cmax=None, rows=None):
+    """The full forward chain on the CPU for workload `w` with inputs `inp`.
+
+    Returns a dict with logits, idx, gates, loc, needed, c, buf, out (expert
+    outputs at kept rows; other rows 0) and y.  `rows`, if given, restricts the
+    FFN to those (expert, row) pairs (the rest of `out` stays 0) and y is then
+    not computed.
+    """
+    bf16 = w.dtype == "bf16"
+    lg = gate_logits(inp["x"], inp["wg"], inp.get("bias"))
+    idx = topk(lg, w.k)
+    g = gates(lg, idx, w.normalize_gates and w.k >= 2)
+    loc, needed = locations(idx, w.e)
+    c = capacity(w.capacity_factor, w.s, w.e, w.k, needed)
+    cmax = c if cmax is None else cmax
+    buf = encode(inp["x"], idx, loc, c, w.e, cmax)
+    kept = kept_rows(needed, c)
+    res = dict(logits=lg, idx=idx, gates=g, loc=loc, needed=needed, c=c, buf=buf, kept=kept)
+    full = rows is None
+    if full:
+        re = np.concatenate([np.full(int(kept[j]), j, np.int32) for j in range(w.e)])
+        rj = np.concatenate([np.arange(int(kept[j]), dtype=np.int64) for j in range(w.e)])
+    else:
+        re, rj = rows
+    o = ffn_rows(buf, inp["w1"], inp.get("b1"), inp.get("w3"), inp["w2"], inp.get("b2"),
+                 w.act, re, rj, bf16)
+    out = np.zeros_like(buf)
+    out[np.asarray(re, np.int64), np.asarray(rj, np.int64)] = o
+    res["out"] = out
+    if full:
+        res["y"] = decode(out, idx, loc, g, c, bf16)
+    return res

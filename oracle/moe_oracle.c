@@ -1,0 +1,322 @@
+/*
+ * CPU oracle for the top-k MoE layer: gate, capacity/locations, encode, expert
+ * FFN, decode, and the backward of encode/decode.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the package's smoke check and the
+ * bench's CPU-baseline leg may load this library.  It shares no code, header,
+ * table or constant with the CUDA library, and the CUDA library never calls it.
+ *
+ * Plain loops, no blocking or fusion.  Arithmetic is in double unless a
+ * function states the precision the method fixes:
+ *   - gate logits are fp32 (the decision top-k takes is made in fp32; see
+ *     orc_gate_logits for the exact summation order);
+ *   - combine (decode) and its K0 twin (encode backward) accumulate in fp32,
+ *     as the DeepSpeed index-dispatch change requires (PR #8195, change 3:
+ *     "combine accumulates in fp32").
+ * Values that are bf16 in the layer are passed in as fp32 (exact widening);
+ * functions with a `bf16` flag round their outputs to bf16 (round to nearest,
+ * ties to even) and return them stored in fp32.
+ *
+ * Sources (the pages this oracle restates):
+ *   [Tutel]   "Tutel" project profile, FAQ on gate_type k and capacity_factor,
+ *             and the key-configuration table (MOELayer gate_type / experts).
+ *   [Blog]    "MoE training systems: DeepSpeed-MoE vs Tutel", section 1.4
+ *             (kernel optimisation: dense mapping table, fused top-k + cumsum)
+ *             and section 3.5 (fast encode/decode; dynamic capacity factor).
+ *   [PR8195]  DeepSpeed PR #8195 (follow-up to #8174), changes 1 and 3.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_ACT_RELU 0
+#define ORC_ACT_GELU 1
+#define ORC_ACT_SWIGLU 2
+
+/* ---------------------------------------------------------------- helpers */
+
+/* Round a double to the nearest bf16 value (ties to even), returned as float.
+ * bf16 keeps 8 significant bits; its smallest subnormal step is 2^-133. */
+static float round_bf16(double v)
+{
+    if (v == 0.0 || !isfinite(v)) return (float)v;
+    int ex;
+    frexp(v, &ex);               /* |v| in [2^(ex-1), 2^ex) */
+    int lsb = ex - 8;            /* weight of the last kept bit */
+    if (lsb < -133) lsb = -133;
+    double r = nearbyint(ldexp(v, -lsb));   /* default mode: ties to even */
+    double res = ldexp(r, lsb);
+    if (fabs(res) > 3.3895313892515355e38) return (float)copysign(INFINITY, v);
+    return (float)res;           /* exact: res has at most 8 significant bits */
+}
+
+static float round_to(double v, int bf16) { return bf16 ? round_bf16(v) : (float)v; }
+
+float orc_round_bf16(double v) { return round_bf16(v); }
+
+void orc_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+int orc_get_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ------------------------------------------------------------------- gate */
+
+/* Gate logits l[t,j] = x[t,:] . wg[:,j] + bias[j]   ([Tutel] gate_type 'top').
+ *
+ * Precision and order (the reading this build fixes so that top-k is
+ * reproducible bit for bit): fp32, one accumulator per (t, j) starting from
+ * +0, updated acc = fmaf(x[t,i], wg[i,j], acc) for i = 0, 1, ..., m-1 in
+ * ascending order, then one fp32 add of bias[j] (skipped when bias is NULL).
+ * x is [s, m] row-major, wg is [m, e] row-major, logits is [s, e]. */
+void orc_gate_logits(const float *x, const float *wg, const float *bias,
+                     int64_t s, int m, int e, float *logits)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < s; t++) {
+        for (int j = 0; j < e; j++) {
+            float acc = 0.0f;
+            for (int i = 0; i < m; i++)
+                acc = fmaf(x[t * m + i], wg[(int64_t)i * e + j], acc);
+            if (bias) acc = acc + bias[j];
+            logits[t * e + j] = acc;
+        }
+    }
+}
+
+typedef struct { float v; int j; } orc_vj;
+
+/* Larger logit first; equal logits: lower expert index first. */
+static int cmp_logit_desc(const void *a, const void *b)
+{
+    const orc_vj *p = (const orc_vj *)a, *q = (const orc_vj *)b;
+    if (p->v > q->v) return -1;
+    if (p->v < q->v) return 1;
+    return (p->j > q->j) - (p->j < q->j);
+}
+
+/* Top-k routing: route r of token t is the expert in position r when all e
+ * experts are ordered by (logit descending, index ascending).  Selecting on
+ * logits equals selecting on softmax probabilities (softmax is monotone).
+ * idx is route-major [k, s]: idx[r*s + t]. */
+void orc_topk(const float *logits, int64_t s, int e, int k, int32_t *idx)
+{
+    orc_vj *a = (orc_vj *)malloc(sizeof(orc_vj) * (size_t)e);
+    for (int64_t t = 0; t < s; t++) {
+        for (int j = 0; j < e; j++) { a[j].v = logits[t * e + j]; a[j].j = j; }
+        qsort(a, (size_t)e, sizeof(orc_vj), cmp_logit_desc);
+        for (int r = 0; r < k; r++) idx[(int64_t)r * s + t] = a[r].j;
+    }
+    free(a);
+}
+
+/* Gate values (double, rounded once to fp32): p = softmax over all e logits;
+ * route r's gate is p[idx[r,t]], divided by the sum of the k selected p's when
+ * `normalize` is set.  Normalisation happens before any capacity drop and is
+ * not redone after drops. */
+void orc_gates(const float *logits, const int32_t *idx, int64_t s, int e, int k,
+               int normalize, float *gates)
+{
+    for (int64_t t = 0; t < s; t++) {
+        const float *l = logits + t * e;
+        double mx = l[0];
+        for (int j = 1; j < e; j++) if (l[j] > mx) mx = l[j];
+        double z = 0.0;
+        for (int j = 0; j < e; j++) z += exp((double)l[j] - mx);
+        double sel = 0.0;
+        for (int r = 0; r < k; r++) sel += exp((double)l[idx[(int64_t)r * s + t]] - mx) / z;
+        for (int r = 0; r < k; r++) {
+            double p = exp((double)l[idx[(int64_t)r * s + t]] - mx) / z;
+            gates[(int64_t)r * s + t] = (float)(normalize ? p / sel : p);
+        }
+    }
+}
+
+/* --------------------------------------------------------------- capacity */
+
+/* Slot assignment as a sequential queue ([Blog] 1.4: the cumsum over the
+ * token-to-expert table; route-priority order): for r = 0..k-1, for
+ * t = 0..s-1, loc[r,t] = fill[idx[r,t]]++.  needed[e] = routes sent to e
+ * before any drop.  Locations are returned un-clipped. */
+void orc_locations(const int32_t *idx, int64_t s, int e, int k, int32_t *loc, int64_t *needed)
+{
+    for (int j = 0; j < e; j++) needed[j] = 0;
+    for (int r = 0; r < k; r++)
+        for (int64_t t = 0; t < s; t++) {
+            int32_t x = idx[(int64_t)r * s + t];
+            loc[(int64_t)r * s + t] = (int32_t)needed[x]++;
+        }
+}
+
+/* ceil(x / e) for a non-negative double x that is exact (f*k*s with f a float
+ * and k*s < 2^29 is exact in double). */
+static int64_t ceil_div_exact(double x, int e)
+{
+    int64_t c = (int64_t)ceil(x / (double)e);
+    while (c > 0 && (double)(c - 1) * (double)e >= x) c--;
+    while ((double)c * (double)e < x) c++;
+    return c;
+}
+
+/* Capacity c from capacity_factor f ([Tutel] FAQ; [Blog] 3.5 "dynamic capacity
+ * factor"):
+ *   f > 0: fixed factor, c = ceil(f*k*s/e);
+ *   f = 0: just enough that nothing is dropped, c = max_e needed[e];
+ *   f < 0: -f is an upper bound, c = min(ceil(-f*k*s/e), max_e needed[e]). */
+int64_t orc_capacity(double f, int64_t s, int e, int k, const int64_t *needed)
+{
+    int64_t mx = 0;
+    for (int j = 0; j < e; j++) if (needed[j] > mx) mx = needed[j];
+    if (f > 0) return ceil_div_exact(f * (double)k * (double)s, e);
+    if (f == 0) return mx;
+    int64_t bound = ceil_div_exact(-f * (double)k * (double)s, e);
+    return bound < mx ? bound : mx;
+}
+
+/* --------------------------------------------------- encode / decode (sparse) */
+
+/* Fast encode ([Blog] 3.5, kernel K1 forward): for each kept route (r,t)
+ * (loc < c), buf[idx, loc, :] = x[t, :].  Unweighted copy.  buf is the
+ * physical [e, cmax, m] buffer; rows not written are left untouched. */
+void orc_encode(const float *x, const int32_t *idx, const int32_t *loc, int64_t c,
+                int64_t s, int m, int e, int k, int64_t cmax, float *buf)
+{
+    (void)e;
+    for (int r = 0; r < k; r++)
+        for (int64_t t = 0; t < s; t++) {
+            int64_t o = (int64_t)r * s + t;
+            if (loc[o] >= c) continue;
+            memcpy(buf + ((int64_t)idx[o] * cmax + loc[o]) * m, x + t * m, sizeof(float) * (size_t)m);
+        }
+}
+
+/* Fast decode ([Blog] 3.5, K0 forward; [PR8195] change 3): y[t,:] =
+ * sum over kept routes r of gates[r,t] * out[idx, loc, :], accumulated in fp32
+ * in ascending r with acc = fmaf(g, v, acc) from +0, rounded once to the
+ * output dtype.  A token whose routes were all dropped gets 0. */
+void orc_decode(const float *out, const int32_t *idx, const int32_t *loc, const float *gates,
+                int64_t c, int64_t s, int m, int e, int k, int64_t cmax, int bf16, float *y)
+{
+    (void)e;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < s; t++) {
+        for (int i = 0; i < m; i++) {
+            float acc = 0.0f;
+            for (int r = 0; r < k; r++) {
+                int64_t o = (int64_t)r * s + t;
+                if (loc[o] >= c) continue;
+                acc = fmaf(gates[o], out[((int64_t)idx[o] * cmax + loc[o]) * m + i], acc);
+            }
+            y[t * m + i] = round_to(acc, bf16);
+        }
+    }
+}
+
+/* Backward of decode ([Blog] 3.5: K1 is combine's backward, K2 the cross
+ * term).  For kept (r,t): d_out[idx, loc, :] = gates[r,t] * dy[t,:] (exact
+ * product rounded once to the dtype) and d_gates[r,t] = sum_i dy[t,i] *
+ * out[idx, loc, i] (double, rounded to fp32).  Dropped routes: d_gates = 0. */
+void orc_decode_bwd(const float *dy, const float *out, const int32_t *idx, const int32_t *loc,
+                    const float *gates, int64_t c, int64_t s, int m, int e, int k, int64_t cmax,
+                    int bf16, float *d_out, float *d_gates)
+{
+    (void)e;
+    for (int r = 0; r < k; r++)
+        for (int64_t t = 0; t < s; t++) {
+            int64_t o = (int64_t)r * s + t;
+            if (loc[o] >= c) { d_gates[o] = 0.0f; continue; }
+            int64_t row = ((int64_t)idx[o] * cmax + loc[o]) * m;
+            double dot = 0.0;
+            for (int i = 0; i < m; i++) {
+                d_out[row + i] = round_to((double)gates[o] * (double)dy[t * m + i], bf16);
+                dot += (double)dy[t * m + i] * (double)out[row + i];
+            }
+            d_gates[o] = (float)dot;
+        }
+}
+
+/* Backward of encode ([Blog] 3.5: K0 with unit weights): dx[t,:] = sum over
+ * kept routes of d_buf[idx, loc, :], fp32 accumulation in ascending r from +0,
+ * rounded once to the dtype. */
+void orc_encode_bwd(const float *d_buf, const int32_t *idx, const int32_t *loc, int64_t c,
+                    int64_t s, int m, int e, int k, int64_t cmax, int bf16, float *dx)
+{
+    (void)e;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < s; t++) {
+        for (int i = 0; i < m; i++) {
+            float acc = 0.0f;
+            for (int r = 0; r < k; r++) {
+                int64_t o = (int64_t)r * s + t;
+                if (loc[o] >= c) continue;
+                acc = acc + d_buf[((int64_t)idx[o] * cmax + loc[o]) * m + i];
+            }
+            dx[t * m + i] = round_to(acc, bf16);
+        }
+    }
+}
+
+/* ------------------------------------------------------------- expert FFN */
+
+/* One expert MLP row ([Tutel] experts {'type': 'ffn', hidden_size_per_expert,
+ * has_fc1_bias, has_fc2_bias}).  For the requested (expert, row) pairs:
+ *   ReLU/GELU: hid = act(x . w1[e]^T + b1[e]),  out = hid . w2[e]^T + b2[e]
+ *   SwiGLU:    hid = silu(x . w1[e]^T) * (x . w3[e]^T), out = hid . w2[e]^T
+ * Layouts: buf [e, cmax, m]; w1, w3 [e, h, m]; w2 [e, m, h]; b1 [e, h];
+ * b2 [e, m].  Sums in double; the hidden activation is rounded to the layer
+ * dtype (bf16 or fp32) before fc2, and each output once more.  GELU is the
+ * exact erf form; biases may be NULL. */
+void orc_ffn_rows(const float *buf, const float *w1, const float *b1, const float *w3,
+                  const float *w2, const float *b2, int act, int e, int64_t cmax, int m, int h,
+                  int bf16, const int32_t *row_e, const int64_t *row_j, int64_t nrows,
+                  float *out_rows)
+{
+    (void)e;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t q = 0; q < nrows; q++) {
+        int64_t ex = row_e[q];
+        const float *xr = buf + (ex * cmax + row_j[q]) * m;
+        float *hid = (float *)malloc(sizeof(float) * (size_t)h);
+        for (int u = 0; u < h; u++) {
+            const float *w1r = w1 + (ex * h + u) * (int64_t)m;
+            double a = 0.0;
+            for (int i = 0; i < m; i++) a += (double)xr[i] * (double)w1r[i];
+            double v;
+            if (act == ORC_ACT_SWIGLU) {
+                const float *w3r = w3 + (ex * h + u) * (int64_t)m;
+                double b = 0.0;
+                for (int i = 0; i < m; i++) b += (double)xr[i] * (double)w3r[i];
+                v = a / (1.0 + exp(-a)) * b;
+            } else {
+                if (b1) a += (double)b1[ex * h + u];
+                v = act == ORC_ACT_RELU ? (a > 0.0 ? a : 0.0)
+                                        : 0.5 * a * (1.0 + erf(a / sqrt(2.0)));
+            }
+            hid[u] = round_to(v, bf16);
+        }
+        for (int i = 0; i < m; i++) {
+            const float *w2r = w2 + (ex * m + i) * (int64_t)h;
+            double o = 0.0;
+            for (int u = 0; u < h; u++) o += (double)hid[u] * (double)w2r[u];
+            if (b2 && act != ORC_ACT_SWIGLU) o += (double)b2[ex * m + i];
+            out_rows[q * m + i] = round_to(o, bf16);
+        }
+        free(hid);
+    }
+}
