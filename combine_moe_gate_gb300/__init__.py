@@ -1,0 +1,218 @@
+"""GB300-native top-k MoE layer hot path: Python binding of libmoe_gate.so.
+
+Every step runs in the CUDA library (include/moe_gate.h); this module only
+marshals torch tensors into the C ABI: data pointers, sizes taken from the
+tensor shapes, the current CUDA stream.  There is no fallback: if the library
+is missing, importing the entry points raises.
+
+Functions keep the C names:
+    moe_gate_topk, moe_capacity_locations, moe_encode, moe_expert_ffn,
+    moe_decode, moe_decode_bwd, moe_encode_bwd, moe_layer_forward
+plus the size queries and `MoEError`.
+"""
+
+import ctypes
+import os
+import re
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libmoe_gate.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "moe_gate.h")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_CAPACITY, MOE_ERR_TIMEOUT = range(6)
+MOE_F32, MOE_BF16 = 0, 1
+ACT = {"relu": 0, "gelu": 1, "swiglu": 2}
+MOE_FLAG_NORMALIZE_GATES = 1
+MOE_FLAG_ZERO_FILL = 2
+
+_lib = None
+
+
+class MoEError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__(f"{where}: {status_str(code)} ({code})")
+
+
+def load():
+    """Load libmoe_gate.so (build it first with combine_moe_gate_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                           "(run `python -m combine_moe_gate_gb300.build`)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, I64, U, F, SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint,
+                           ctypes.c_float, ctypes.c_size_t)
+    sigs = {
+        "moe_gate_topk": (I, [P, I, P, P, I64, I, I, I, U, P, P, P, P]),
+        "moe_capacity_bound": (I64, [F, I64, I, I]),
+        "moe_capacity_workspace_size": (SZ, [I64, I, I]),
+        "moe_capacity_locations": (I, [P, I64, I, I, F, I64, P, SZ, P, P, P, P, P]),
+        "moe_encode": (I, [P, I, P, P, P, P, I64, I, I, I, I64, U, P, P, P]),
+        "moe_expert_ffn_workspace_size": (SZ, [I, I, I, I64, I, I]),
+        "moe_expert_ffn": (I, [P, I, P, P, P, P, P, P, P, I, I, I64, I, I, P, SZ, P, P, P]),
+        "moe_decode": (I, [P, I, P, P, P, P, I64, I, I, I, I64, P, P, P]),
+        "moe_decode_bwd": (I, [P, P, I, P, P, P, P, P, I64, I, I, I, I64, U, P, P, P, P]),
+        "moe_encode_bwd": (I, [P, I, P, P, P, I64, I, I, I, I64, P, P, P]),
+        "moe_layer_workspace_size": (SZ, [I, I, I64, I, I, I, I64, I]),
+        "moe_layer_forward": (I, [P, I, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, I64, U,
+                                  P, P, P, P, P, P, P, P, P, SZ, P, P]),
+        "moe_status_str": (ctypes.c_char_p, [I]),
+        "moe_launch_count": (ctypes.c_uint64, []),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def declared_symbols():
+    """Names of the functions include/moe_gate.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(moe_\w+)\s*\(", text, re.M)))
+
+
+def status_str(code) -> str:
+    return load().moe_status_str(int(code)).decode()
+
+
+def launch_count() -> int:
+    return int(load().moe_launch_count())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dt(t):
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return MOE_BF16
+    if t.dtype == torch.float32:
+        return MOE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(code, where):
+    if code != MOE_OK:
+        raise MoEError(code, where)
+
+
+def _act(act):
+    return ACT[act] if isinstance(act, str) else int(act)
+
+
+# ------------------------------------------------------------------ sizes
+def moe_capacity_bound(capacity_factor, s, e, k) -> int:
+    return int(load().moe_capacity_bound(float(capacity_factor), int(s), int(e), int(k)))
+
+
+def moe_capacity_workspace_size(s, e, k) -> int:
+    return int(load().moe_capacity_workspace_size(int(s), int(e), int(k)))
+
+
+def moe_expert_ffn_workspace_size(dtype, act, e, c_max, m, h) -> int:
+    return int(load().moe_expert_ffn_workspace_size(int(dtype), _act(act), int(e), int(c_max),
+                                                    int(m), int(h)))
+
+
+def moe_layer_workspace_size(dtype, act, s, m, e, k, c_max, h) -> int:
+    return int(load().moe_layer_workspace_size(int(dtype), _act(act), int(s), int(m), int(e),
+                                               int(k), int(c_max), int(h)))
+
+
+# ------------------------------------------------------------ entry points
+def moe_gate_topk(x, wg, bias, k, idx, gates, dev_status, flags=0, stream=None):
+    """x [s, m]; wg [m, e] fp32; bias [e] fp32 or None -> idx [k, s] int32, gates [k, s] fp32."""
+    s, m = x.shape
+    e = wg.shape[1]
+    _check(load().moe_gate_topk(_ptr(x), _dt(x), _ptr(wg), _ptr(bias), s, m, e, int(k),
+                                int(flags), _ptr(idx), _ptr(gates), _ptr(dev_status),
+                                _stream(stream)), "moe_gate_topk")
+
+
+def moe_capacity_locations(idx, e, capacity_factor, c_max, workspace, loc, counts, c_dev,
+                           dev_status, stream=None):
+    k, s = idx.shape
+    _check(load().moe_capacity_locations(
+        _ptr(idx), s, int(e), k, float(capacity_factor), int(c_max), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(loc), _ptr(counts), _ptr(c_dev),
+        _ptr(dev_status), _stream(stream)), "moe_capacity_locations")
+
+
+def moe_encode(x, idx, loc, counts, c_dev, buf, dev_status, flags=0, stream=None):
+    """buf is [e, c_max, m]."""
+    s, m = x.shape
+    k = idx.shape[0]
+    e, c_max, _ = buf.shape
+    _check(load().moe_encode(_ptr(x), _dt(x), _ptr(idx), _ptr(loc), _ptr(counts), _ptr(c_dev),
+                             s, m, e, k, c_max, int(flags), _ptr(buf), _ptr(dev_status),
+                             _stream(stream)), "moe_encode")
+
+
+def moe_expert_ffn(buf, counts, c_dev, w1, b1, w3, w2, b2, act, workspace, out, dev_status,
+                   stream=None):
+    e, c_max, m = buf.shape
+    h = w1.shape[1]
+    _check(load().moe_expert_ffn(
+        _ptr(buf), _dt(buf), _ptr(counts), _ptr(c_dev), _ptr(w1), _ptr(b1), _ptr(w3), _ptr(w2),
+        _ptr(b2), _act(act), e, c_max, m, h, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _ptr(dev_status),
+        _stream(stream)), "moe_expert_ffn")
+
+
+def moe_decode(out, idx, loc, gates, c_dev, y, dev_status, stream=None):
+    e, c_max, m = out.shape
+    k, s = idx.shape
+    _check(load().moe_decode(_ptr(out), _dt(out), _ptr(idx), _ptr(loc), _ptr(gates), _ptr(c_dev),
+                             s, m, e, k, c_max, _ptr(y), _ptr(dev_status), _stream(stream)),
+           "moe_decode")
+
+
+def moe_decode_bwd(dy, out, idx, loc, gates, counts, c_dev, d_out, d_gates, dev_status, flags=0,
+                   stream=None):
+    e, c_max, m = out.shape
+    k, s = idx.shape
+    _check(load().moe_decode_bwd(
+        _ptr(dy), _ptr(out), _dt(out), _ptr(idx), _ptr(loc), _ptr(gates), _ptr(counts),
+        _ptr(c_dev), s, m, e, k, c_max, int(flags), _ptr(d_out), _ptr(d_gates), _ptr(dev_status),
+        _stream(stream)), "moe_decode_bwd")
+
+
+def moe_encode_bwd(d_buf, idx, loc, c_dev, dx, dev_status, stream=None):
+    e, c_max, m = d_buf.shape
+    k, s = idx.shape
+    _check(load().moe_encode_bwd(_ptr(d_buf), _dt(d_buf), _ptr(idx), _ptr(loc), _ptr(c_dev), s, m,
+                                 e, k, c_max, _ptr(dx), _ptr(dev_status), _stream(stream)),
+           "moe_encode_bwd")
+
+
+def moe_layer_forward(x, wg, gate_bias, w1, b1, w3, w2, b2, act, k, capacity_factor, flags,
+                      idx, gates, loc, counts, c_dev, buf, out, y, workspace, dev_status,
+                      stream=None):
+    s, m = x.shape
+    e, c_max, _ = buf.shape
+    h = w1.shape[1]
+    _check(load().moe_layer_forward(
+        _ptr(x), _dt(x), _ptr(wg), _ptr(gate_bias), _ptr(w1), _ptr(b1), _ptr(w3), _ptr(w2),
+        _ptr(b2), _act(act), s, m, e, int(k), h, float(capacity_factor), c_max, int(flags),
+        _ptr(idx), _ptr(gates), _ptr(loc), _ptr(counts), _ptr(c_dev), _ptr(buf), _ptr(out),
+        _ptr(y), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status),
+        _stream(stream)), "moe_layer_forward")
+
+
+from .layer import MoELayerBuffers, alloc_layer, run_layer  # noqa: E402,F401

@@ -1,0 +1,224 @@
+// C ABI entry points: synchronous argument checks, then kernel launches.
+#include <atomic>
+
+#include "common.cuh"
+
+namespace moe {
+
+static std::atomic<uint64_t> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+// kernels (one translation unit each)
+moe_status gate_topk_launch(const void *x, moe_dtype xdt, const float *wg, const float *bias,
+                            int64_t s, int m, int e, int k, unsigned flags, int32_t *idx,
+                            float *gates, int32_t *st, cudaStream_t stream);
+int64_t capacity_bound_host(float f, int64_t s, int e, int k);
+size_t capacity_workspace_bytes(int64_t s, int e, int k);
+moe_status capacity_launch(const int32_t *idx, int64_t s, int e, int k, float f, int64_t c_max,
+                           void *ws, int32_t *loc, int32_t *counts, int32_t *c_dev, int32_t *st,
+                           cudaStream_t stream);
+moe_status encode_launch(const void *x, moe_dtype dt, const int32_t *idx, const int32_t *loc,
+                         const int32_t *counts, const int32_t *c_dev, int64_t s, int m, int e,
+                         int k, int64_t c_max, unsigned flags, void *buf, int32_t *st,
+                         cudaStream_t stream);
+moe_status combine_launch(const void *src, moe_dtype dt, const int32_t *idx, const int32_t *loc,
+                          const float *gates, const int32_t *c_dev, int64_t s, int m, int e, int k,
+                          int64_t c_max, void *y, int32_t *st, cudaStream_t stream);
+moe_status decode_bwd_launch(const void *dy, const void *out, moe_dtype dt, const int32_t *idx,
+                             const int32_t *loc, const float *gates, const int32_t *counts,
+                             const int32_t *c_dev, int64_t s, int m, int e, int k, int64_t c_max,
+                             unsigned flags, void *d_out, float *d_gates, int32_t *st,
+                             cudaStream_t stream);
+moe_status ffn_simt_launch(const void *buf, moe_dtype dt, const int32_t *counts,
+                           const int32_t *c_dev, const void *w1, const void *b1, const void *w3,
+                           const void *w2, const void *b2, moe_act act, int e, int64_t c_max,
+                           int m, int h, void *hid, void *out, int32_t *st, cudaStream_t stream);
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+
+inline bool ok16(const void *p) { return p != nullptr && aligned16(p); }
+inline bool ok4(const void *p) { return p != nullptr && ((uintptr_t)p & 3u) == 0; }
+inline bool opt16(const void *p) { return p == nullptr || aligned16(p); }
+inline bool valid_dt(moe_dtype dt) { return dt == MOE_F32 || dt == MOE_BF16; }
+inline int vec_of(moe_dtype dt) { return dt == MOE_BF16 ? 8 : 4; }
+inline size_t esize(moe_dtype dt) { return dt == MOE_BF16 ? 2 : 4; }
+inline size_t up256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+bool routing_shape_ok(int64_t s, int e, int k) {
+    return s >= 1 && s <= (int64_t)1 << 30 && e >= 1 && e <= kMaxE && k >= 1 && k <= e &&
+           k <= kMaxK && s * (int64_t)k < ((int64_t)1 << 31);
+}
+
+bool rows_ok(moe_dtype dt, int m) { return valid_dt(dt) && m >= 1 && m % vec_of(dt) == 0; }
+
+cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_status_str(moe_status st) {
+    switch (st) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported combination";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_CAPACITY: return "capacity exceeds c_max";
+        case MOE_ERR_TIMEOUT: return "bounded wait timed out";
+    }
+    return "unknown status";
+}
+
+uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+moe_status moe_gate_topk(const void *x, moe_dtype xdt, const float *wg, const float *bias,
+                         int64_t s, int m, int e, int k, unsigned flags, int32_t *idx,
+                         float *gates, int32_t *dev_status, void *stream) {
+    if (!routing_shape_ok(s, e, k) || !rows_ok(xdt, m) || !ok16(x) || !ok16(wg) || !opt16(bias) ||
+        !ok4(idx) || !ok4(gates) || !ok4(dev_status) || (flags & ~3u))
+        return MOE_ERR_INVALID_ARG;
+    if (e > 256) return MOE_ERR_UNSUPPORTED;
+    return gate_topk_launch(x, xdt, wg, bias, s, m, e, k, flags, idx, gates, dev_status,
+                            as_stream(stream));
+}
+
+int64_t moe_capacity_bound(float capacity_factor, int64_t s, int e, int k) {
+    if (!routing_shape_ok(s, e, k) || capacity_factor != capacity_factor) return -1;
+    return capacity_bound_host(capacity_factor, s, e, k);
+}
+
+size_t moe_capacity_workspace_size(int64_t s, int e, int k) {
+    if (!routing_shape_ok(s, e, k)) return 0;
+    return capacity_workspace_bytes(s, e, k);
+}
+
+moe_status moe_capacity_locations(const int32_t *idx, int64_t s, int e, int k,
+                                  float capacity_factor, int64_t c_max, void *workspace,
+                                  size_t workspace_bytes, int32_t *loc, int32_t *counts,
+                                  int32_t *c_dev, int32_t *dev_status, void *stream) {
+    if (!routing_shape_ok(s, e, k) || c_max < 1 || c_max > 0x7fffffff ||
+        capacity_factor != capacity_factor || !ok4(idx) || !ok4(loc) || !ok4(counts) ||
+        !ok4(c_dev) || !ok4(dev_status) || !ok16(workspace) ||
+        workspace_bytes < capacity_workspace_bytes(s, e, k))
+        return MOE_ERR_INVALID_ARG;
+    return capacity_launch(idx, s, e, k, capacity_factor, c_max, workspace, loc, counts, c_dev,
+                           dev_status, as_stream(stream));
+}
+
+moe_status moe_encode(const void *x, moe_dtype dt, const int32_t *idx, const int32_t *loc,
+                      const int32_t *counts, const int32_t *c_dev, int64_t s, int m, int e, int k,
+                      int64_t c_max, unsigned flags, void *buf, int32_t *dev_status,
+                      void *stream) {
+    if (!routing_shape_ok(s, e, k) || !rows_ok(dt, m) || c_max < 1 || c_max > 0x7fffffff ||
+        !ok16(x) || !ok4(idx) || !ok4(loc) || !ok4(c_dev) || !ok16(buf) || !ok4(dev_status) ||
+        (flags & ~3u) || ((flags & MOE_FLAG_ZERO_FILL) && !ok4(counts)))
+        return MOE_ERR_INVALID_ARG;
+    return encode_launch(x, dt, idx, loc, counts, c_dev, s, m, e, k, c_max, flags, buf, dev_status,
+                         as_stream(stream));
+}
+
+size_t moe_expert_ffn_workspace_size(moe_dtype dt, moe_act act, int e, int64_t c_max, int m,
+                                     int h) {
+    (void)act;
+    (void)m;
+    if (!valid_dt(dt) || e < 1 || c_max < 1 || h < 1) return 0;
+    return up256((size_t)e * (size_t)c_max * (size_t)h * esize(dt));
+}
+
+moe_status moe_expert_ffn(const void *buf, moe_dtype dt, const int32_t *counts,
+                          const int32_t *c_dev, const void *w1, const void *b1, const void *w3,
+                          const void *w2, const void *b2, moe_act act, int e, int64_t c_max, int m,
+                          int h, void *workspace, size_t workspace_bytes, void *out,
+                          int32_t *dev_status, void *stream) {
+    if (!rows_ok(dt, m) || !rows_ok(dt, h) || e < 1 || e > kMaxE || c_max < 1 ||
+        c_max > 0x7fffffff || !ok16(buf) || !ok4(counts) || !ok4(c_dev) || !ok16(w1) ||
+        !ok16(w2) || !opt16(b1) || !opt16(b2) || !ok16(out) || !ok4(dev_status) ||
+        !ok16(workspace) ||
+        workspace_bytes < moe_expert_ffn_workspace_size(dt, act, e, c_max, m, h))
+        return MOE_ERR_INVALID_ARG;
+    if (act != MOE_ACT_RELU && act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU)
+        return MOE_ERR_INVALID_ARG;
+    if (act == MOE_ACT_SWIGLU && (!ok16(w3) || b1 != nullptr || b2 != nullptr))
+        return MOE_ERR_INVALID_ARG;
+    return ffn_simt_launch(buf, dt, counts, c_dev, w1, b1, w3, w2, b2, act, e, c_max, m, h,
+                           workspace, out, dev_status, as_stream(stream));
+}
+
+moe_status moe_decode(const void *out, moe_dtype dt, const int32_t *idx, const int32_t *loc,
+                      const float *gates, const int32_t *c_dev, int64_t s, int m, int e, int k,
+                      int64_t c_max, void *y, int32_t *dev_status, void *stream) {
+    if (!routing_shape_ok(s, e, k) || !rows_ok(dt, m) || c_max < 1 || c_max > 0x7fffffff ||
+        !ok16(out) || !ok4(idx) || !ok4(loc) || !ok4(gates) || !ok4(c_dev) || !ok16(y) ||
+        !ok4(dev_status))
+        return MOE_ERR_INVALID_ARG;
+    return combine_launch(out, dt, idx, loc, gates, c_dev, s, m, e, k, c_max, y, dev_status,
+                          as_stream(stream));
+}
+
+moe_status moe_decode_bwd(const void *dy, const void *out, moe_dtype dt, const int32_t *idx,
+                          const int32_t *loc, const float *gates, const int32_t *counts,
+                          const int32_t *c_dev, int64_t s, int m, int e, int k, int64_t c_max,
+                          unsigned flags, void *d_out, float *d_gates, int32_t *dev_status,
+                          void *stream) {
+    if (!routing_shape_ok(s, e, k) || !rows_ok(dt, m) || c_max < 1 || c_max > 0x7fffffff ||
+        !ok16(dy) || !ok16(out) || !ok4(idx) || !ok4(loc) || !ok4(gates) || !ok4(c_dev) ||
+        !ok16(d_out) || !ok4(d_gates) || !ok4(dev_status) || (flags & ~3u) ||
+        ((flags & MOE_FLAG_ZERO_FILL) && !ok4(counts)))
+        return MOE_ERR_INVALID_ARG;
+    return decode_bwd_launch(dy, out, dt, idx, loc, gates, counts, c_dev, s, m, e, k, c_max, flags,
+                             d_out, d_gates, dev_status, as_stream(stream));
+}
+
+moe_status moe_encode_bwd(const void *d_buf, moe_dtype dt, const int32_t *idx, const int32_t *loc,
+                          const int32_t *c_dev, int64_t s, int m, int e, int k, int64_t c_max,
+                          void *dx, int32_t *dev_status, void *stream) {
+    if (!routing_shape_ok(s, e, k) || !rows_ok(dt, m) || c_max < 1 || c_max > 0x7fffffff ||
+        !ok16(d_buf) || !ok4(idx) || !ok4(loc) || !ok4(c_dev) || !ok16(dx) || !ok4(dev_status))
+        return MOE_ERR_INVALID_ARG;
+    return combine_launch(d_buf, dt, idx, loc, nullptr, c_dev, s, m, e, k, c_max, dx, dev_status,
+                          as_stream(stream));
+}
+
+size_t moe_layer_workspace_size(moe_dtype dt, moe_act act, int64_t s, int m, int e, int k,
+                                int64_t c_max, int h) {
+    size_t a = moe_capacity_workspace_size(s, e, k);
+    size_t b = moe_expert_ffn_workspace_size(dt, act, e, c_max, m, h);
+    if (a == 0 || b == 0) return 0;
+    return up256(a) + up256(b);
+}
+
+moe_status moe_layer_forward(const void *x, moe_dtype dt, const float *wg, const float *gate_bias,
+                             const void *w1, const void *b1, const void *w3, const void *w2,
+                             const void *b2, moe_act act, int64_t s, int m, int e, int k, int h,
+                             float capacity_factor, int64_t c_max, unsigned flags, int32_t *idx,
+                             float *gates, int32_t *loc, int32_t *counts, int32_t *c_dev,
+                             void *buf, void *out, void *y, void *workspace,
+                             size_t workspace_bytes, int32_t *dev_status, void *stream) {
+    size_t need = moe_layer_workspace_size(dt, act, s, m, e, k, c_max, h);
+    if (need == 0 || workspace_bytes < need || !ok16(workspace)) return MOE_ERR_INVALID_ARG;
+    size_t cap_b = up256(moe_capacity_workspace_size(s, e, k));
+    char *ws = (char *)workspace;
+    moe_status st;
+    st = moe_gate_topk(x, dt, wg, gate_bias, s, m, e, k, flags & MOE_FLAG_NORMALIZE_GATES, idx,
+                       gates, dev_status, stream);
+    if (st != MOE_OK) return st;
+    st = moe_capacity_locations(idx, s, e, k, capacity_factor, c_max, ws, cap_b, loc, counts, c_dev,
+                                dev_status, stream);
+    if (st != MOE_OK) return st;
+    st = moe_encode(x, dt, idx, loc, counts, c_dev, s, m, e, k, c_max, flags & MOE_FLAG_ZERO_FILL,
+                    buf, dev_status, stream);
+    if (st != MOE_OK) return st;
+    st = moe_expert_ffn(buf, dt, counts, c_dev, w1, b1, w3, w2, b2, act, e, c_max, m, h,
+                        ws + cap_b, workspace_bytes - cap_b, out, dev_status, stream);
+    if (st != MOE_OK) return st;
+    return moe_decode(out, dt, idx, loc, gates, c_dev, s, m, e, k, c_max, y, dev_status, stream);
+}
+
+}  // extern "C"

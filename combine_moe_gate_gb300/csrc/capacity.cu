@@ -1,0 +1,173 @@
+// Capacity and slot locations.
+//
+// Method: the DeepSpeed-MoE vs Tutel blog, section 1.4 (slot assignment is a
+// cumsum over the token-to-expert table, parallelised as a scan) and section
+// 3.5 (dynamic capacity factor: fixed / adaptive no-drop / capped adaptive),
+// with the Tutel profile's FAQ on capacity_factor.  Priority order: all
+// tokens' route 0 in token order, then route 1, and so on; the location of a
+// route is its rank among the routes that chose the same expert, so the flat
+// route-major table [k, s] is ranked in its natural order.
+//
+// Two launches, no inter-CTA waiting:
+//   1. cap_hist: CTA b counts the experts of its chunk of CH routes -> hist[b][e].
+//   2. cap_assign: CTA b sums hist[0..b-1][j] for its base offsets, ranks its
+//      chunk stably (warps take consecutive segments; inside a warp
+//      __match_any_sync groups equal experts and popc of the lower lanes gives
+//      the rank), then adds the per-warp prefix.  CTA 0 also forms counts[],
+//      the capacity c and the overflow check.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int CAP_NT = 256;            // threads per CTA
+constexpr int CAP_NW = CAP_NT / 32;    // warps per CTA
+constexpr int CAP_CH = 4096;           // routes per chunk (per CTA)
+constexpr int CAP_SEG = CAP_CH / CAP_NW;  // routes per warp
+constexpr int CAP_ROUNDS = CAP_SEG / 32;
+
+__global__ void __launch_bounds__(CAP_NT)
+cap_hist_kernel(const int32_t *__restrict__ idx, int64_t n, int e, int32_t *__restrict__ hist,
+                int32_t *status) {
+    if (status_bad(status)) return;
+    extern __shared__ int32_t h[];
+    for (int j = threadIdx.x; j < e; j += CAP_NT) h[j] = 0;
+    __syncthreads();
+    const int64_t base = (int64_t)blockIdx.x * CAP_CH;
+    for (int q = threadIdx.x; q < CAP_CH; q += CAP_NT) {
+        int64_t j = base + q;
+        if (j >= n) break;
+        int v = idx[j];
+        if ((unsigned)v < (unsigned)e) atomicAdd(&h[v], 1);
+        else set_status(status, MOE_ERR_INVALID_ARG);
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < e; j += CAP_NT) hist[(int64_t)blockIdx.x * e + j] = h[j];
+}
+
+// c_fixed >= 0: capacity fixed on the host (capacity_factor > 0).
+// Otherwise c = min(c_cap, max_j counts[j]) (c_cap = INT_MAX for factor 0).
+__global__ void __launch_bounds__(CAP_NT)
+cap_assign_kernel(const int32_t *__restrict__ idx, int64_t n, int e, int nblk,
+                  const int32_t *__restrict__ hist, int c_fixed, int c_cap, int64_t c_max,
+                  int32_t *__restrict__ loc, int32_t *__restrict__ counts,
+                  int32_t *__restrict__ c_dev, int32_t *status) {
+    if (status_bad(status)) return;
+    extern __shared__ int32_t sm[];
+    int32_t *wcnt = sm;                 // [NW][e]: per-warp counts, then per-warp offsets
+    int32_t *base = sm + CAP_NW * e;    // [e]
+    __shared__ int32_t s_max;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) s_max = 0;
+    for (int j = tid; j < CAP_NW * e; j += CAP_NT) wcnt[j] = 0;
+    for (int j = tid; j < e; j += CAP_NT) {
+        int32_t b = 0;
+        for (int q = 0; q < (int)blockIdx.x; q++) b += hist[(int64_t)q * e + j];
+        base[j] = b;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int j = tid; j < e; j += CAP_NT) {
+            int32_t tot = 0;
+            for (int q = 0; q < nblk; q++) tot += hist[(int64_t)q * e + j];
+            counts[j] = tot;
+            atomicMax(&s_max, tot);
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int c = c_fixed >= 0 ? c_fixed : min(c_cap, s_max);
+            c_dev[0] = c;
+            if ((int64_t)c > c_max) set_status(status, MOE_ERR_CAPACITY);
+        }
+    }
+
+    // stable rank inside this warp's segment
+    const int64_t seg0 = (int64_t)blockIdx.x * CAP_CH + (int64_t)warp * CAP_SEG;
+    int32_t rank[CAP_ROUNDS];
+    int32_t val[CAP_ROUNDS];
+    const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int rd = 0; rd < CAP_ROUNDS; rd++) {
+        int64_t j = seg0 + rd * 32 + lane;
+        int v = j < n ? idx[j] : -1;
+        if ((unsigned)v >= (unsigned)e) v = -1;
+        unsigned peers = __match_any_sync(0xffffffffu, v);
+        int prev = v >= 0 ? wcnt[warp * e + v] : 0;
+        __syncwarp();
+        if (v >= 0 && (peers & lt) == 0) wcnt[warp * e + v] = prev + __popc(peers);
+        __syncwarp();
+        rank[rd] = prev + __popc(peers & lt);
+        val[rd] = v;
+    }
+    __syncthreads();
+    // exclusive prefix over warps, seeded with the chunk's base offset
+    for (int j = tid; j < e; j += CAP_NT) {
+        int32_t run = base[j];
+        for (int w = 0; w < CAP_NW; w++) {
+            int32_t t = wcnt[w * e + j];
+            wcnt[w * e + j] = run;
+            run += t;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int rd = 0; rd < CAP_ROUNDS; rd++) {
+        int64_t j = seg0 + rd * 32 + lane;
+        if (j < n && val[rd] >= 0) loc[j] = wcnt[warp * e + val[rd]] + rank[rd];
+    }
+}
+
+int64_t ceil_div_exact(double x, int e) {
+    int64_t c = (int64_t)ceil(x / (double)e);
+    while (c > 0 && (double)(c - 1) * (double)e >= x) c--;
+    while ((double)c * (double)e < x) c++;
+    return c;
+}
+
+}  // namespace
+
+int64_t capacity_bound_host(float f, int64_t s, int e, int k) {
+    if (f > 0.0f) return ceil_div_exact((double)f * (double)k * (double)s, e);
+    if (f == 0.0f) return s;
+    int64_t b = ceil_div_exact(-(double)f * (double)k * (double)s, e);
+    return b < s ? b : s;
+}
+
+size_t capacity_workspace_bytes(int64_t s, int e, int k) {
+    int64_t n = s * (int64_t)k;
+    int64_t nblk = (n + CAP_CH - 1) / CAP_CH;
+    size_t b = (size_t)nblk * (size_t)e * sizeof(int32_t);
+    return (b + 255) & ~(size_t)255;
+}
+
+moe_status capacity_launch(const int32_t *idx, int64_t s, int e, int k, float f, int64_t c_max,
+                           void *ws, int32_t *loc, int32_t *counts, int32_t *c_dev, int32_t *st,
+                           cudaStream_t stream) {
+    const int64_t n = s * (int64_t)k;
+    const int64_t nblk = (n + CAP_CH - 1) / CAP_CH;
+    if (nblk > 0x7fffffff) return MOE_ERR_UNSUPPORTED;
+    int c_fixed = -1, c_cap = 0x7fffffff;
+    if (f > 0.0f) {
+        int64_t c = capacity_bound_host(f, s, e, k);
+        c_fixed = (int)(c < 0x7fffffff ? c : 0x7fffffff);
+    } else if (f < 0.0f) {
+        int64_t c = capacity_bound_host(f, s, e, k);
+        c_cap = (int)c;
+    }
+    int32_t *hist = (int32_t *)ws;
+    cap_hist_kernel<<<(unsigned)nblk, CAP_NT, e * sizeof(int32_t), stream>>>(idx, n, e, hist, st);
+    note_launch();
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    size_t smem = (size_t)(CAP_NW + 1) * e * sizeof(int32_t);
+    auto kern = cap_assign_kernel;
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+        return MOE_ERR_CUDA;
+    kern<<<(unsigned)nblk, CAP_NT, smem, stream>>>(idx, n, e, (int)nblk, hist, c_fixed, c_cap, c_max,
+                                                   loc, counts, c_dev, st);
+    note_launch();
+    return launch_status();
+}
+
+}  // namespace moe

@@ -1,0 +1,108 @@
+// Shared device/host helpers of the MoE layer kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "moe_gate.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- launches
+
+// Count of kernels launched by this library (exported by moe_launch_count).
+void note_launch();
+
+inline moe_status launch_status() {
+    cudaError_t err = cudaGetLastError();
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// ------------------------------------------------------------ device status
+
+// First error wins; later errors are dropped.
+__device__ __forceinline__ void set_status(int32_t *st, int32_t code) {
+    if (st) atomicCAS(st, 0, code);
+}
+
+__device__ __forceinline__ bool status_bad(const int32_t *st) {
+    return st && *(volatile const int32_t *)st != 0;
+}
+
+// ----------------------------------------------------------------- vectors
+
+struct alignas(16) V16 { uint32_t w[4]; };  // 16 bytes: 8 bf16 or 4 fp32
+
+__device__ __forceinline__ V16 ld_stream(const void *p) {
+    V16 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ V16 ld_v16(const void *p) {
+    V16 v;
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_v16(void *p, const V16 &v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]) : "memory");
+}
+
+// Streaming store (evict-first): for outputs nobody reads back soon.
+__device__ __forceinline__ void st_v16_cs(void *p, const V16 &v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]) : "memory");
+}
+
+// bf16 <-> fp32.  Widening is exact (bit shift).
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// fp32 -> bf16 bits, round to nearest even (finite inputs; NaN stays NaN).
+__device__ __forceinline__ uint32_t f2bf(float f) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    return f2bf(lo) | (f2bf(hi) << 16);
+}
+
+// Element-type traits: 16-byte chunk = VEC elements.
+template <typename T> struct Elt;
+template <> struct Elt<float> {
+    static constexpr int VEC = 4;
+    static constexpr int BYTES = 4;
+    __device__ __forceinline__ static void unpack(const V16 &v, float *f) {
+#pragma unroll
+        for (int i = 0; i < 4; i++) f[i] = __uint_as_float(v.w[i]);
+    }
+    __device__ __forceinline__ static V16 pack(const float *f) {
+        V16 v;
+#pragma unroll
+        for (int i = 0; i < 4; i++) v.w[i] = __float_as_uint(f[i]);
+        return v;
+    }
+};
+template <> struct Elt<__nv_bfloat16> {
+    static constexpr int VEC = 8;
+    static constexpr int BYTES = 2;
+    __device__ __forceinline__ static void unpack(const V16 &v, float *f) {
+#pragma unroll
+        for (int i = 0; i < 4; i++) { f[2 * i] = bf16lo(v.w[i]); f[2 * i + 1] = bf16hi(v.w[i]); }
+    }
+    __device__ __forceinline__ static V16 pack(const float *f) {
+        V16 v;
+#pragma unroll
+        for (int i = 0; i < 4; i++) v.w[i] = pack_bf16(f[2 * i], f[2 * i + 1]);
+        return v;
+    }
+};
+
+inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace moe

@@ -1,0 +1,335 @@
+// Index-based encode / decode and their backward.
+//
+// Method: the DeepSpeed-MoE vs Tutel blog, section 3.5 (fast encode/decode:
+// act only on the k non-zero entries of the token-to-expert map, O(T*k*D)
+// instead of the O(T*E*C*D) einsum; K0 = encode backward = combine forward,
+// K1 = encode forward = combine backward, K2 = the cross term) and DeepSpeed
+// PR #8195 change 3 (dispatch and combine become a gather each; combine
+// accumulates in fp32).
+//
+// One warp per token.  Lanes r < k hold route r's (expert, slot, gate); the
+// warp then streams the token's row in 16-byte chunks (8 bf16 / 4 fp32 per
+// lane per access), UNR chunks per lane in flight.  Every row access is a full
+// coalesced 512-byte warp transaction.  Combine accumulates each element in
+// fp32 in ascending route order, as the C ABI specifies, so results are
+// deterministic and independent of the launch shape.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int DNT = 256;  // threads per CTA (8 token-warps)
+constexpr int UNR = 4;    // 16-byte chunks per lane per batch
+
+struct Routes {
+    unsigned kept;   // bit r: route r of this token is kept
+    int64_t row;     // lane r: element offset of route r's slot row
+    float g;         // lane r: route r's gate
+};
+
+__device__ __forceinline__ Routes load_routes(const int32_t *idx, const int32_t *loc,
+                                              const float *gates, int64_t s, int64_t t, int m,
+                                              int e, int k, int c_eff, int64_t c_max,
+                                              int32_t *status) {
+    const int lane = threadIdx.x & 31;
+    Routes R{0u, 0, 0.0f};
+    bool kept = false;
+    if (lane < k) {
+        int ex = idx[(int64_t)lane * s + t];
+        int l = loc[(int64_t)lane * s + t];
+        if ((unsigned)ex >= (unsigned)e || l < 0) {
+            set_status(status, MOE_ERR_INVALID_ARG);
+        } else if (l < c_eff) {
+            kept = true;
+            R.row = ((int64_t)ex * c_max + l) * m;
+            if (gates) R.g = gates[(int64_t)lane * s + t];
+        }
+    }
+    R.kept = __ballot_sync(0xffffffffu, kept);
+    return R;
+}
+
+__device__ __forceinline__ int read_c(const int32_t *c_dev, int64_t c_max) {
+    int c = *c_dev;
+    return (int)min((int64_t)c, c_max);
+}
+
+// ---------------------------------------------------------------- encode (K1)
+template <typename T>
+__global__ void __launch_bounds__(DNT)
+encode_kernel(const T *__restrict__ x, const int32_t *__restrict__ idx,
+              const int32_t *__restrict__ loc, const int32_t *__restrict__ c_dev, int64_t s,
+              int m, int e, int k, int64_t c_max, T *__restrict__ buf, int32_t *status) {
+    if (status_bad(status)) return;
+    const int c_eff = read_c(c_dev, c_max);
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = (int64_t)gridDim.x * (DNT / 32);
+    const int nch = m / Elt<T>::VEC;
+    for (int64_t t = blockIdx.x * (DNT / 32) + (threadIdx.x >> 5); t < s; t += nw) {
+        Routes R = load_routes(idx, loc, nullptr, s, t, m, e, k, c_eff, c_max, status);
+        if (!R.kept) continue;
+        const V16 *src = reinterpret_cast<const V16 *>(x + t * m);
+        for (int base = 0; base < nch; base += 32 * UNR) {  // warp-uniform trip count
+            const int q0 = base + lane;
+            V16 v[UNR];
+#pragma unroll
+            for (int u = 0; u < UNR; u++)
+                if (q0 + 32 * u < nch) v[u] = ld_stream(src + q0 + 32 * u);
+            for (unsigned km = R.kept; km; km &= km - 1) {
+                int r = __ffs(km) - 1;
+                int64_t row = __shfl_sync(0xffffffffu, R.row, r);
+                V16 *dst = reinterpret_cast<V16 *>(buf + row);
+#pragma unroll
+                for (int u = 0; u < UNR; u++)
+                    if (q0 + 32 * u < nch) st_v16(dst + q0 + 32 * u, v[u]);
+            }
+        }
+    }
+}
+
+// Zero rows min(counts[j], c) .. c-1 of every expert j (one warp per row).
+template <typename T>
+__global__ void __launch_bounds__(DNT)
+zero_fill_kernel(const int32_t *__restrict__ counts, const int32_t *__restrict__ c_dev, int e,
+                 int64_t c_max, int m, T *__restrict__ buf, int32_t *status) {
+    if (status_bad(status)) return;
+    const int c_eff = read_c(c_dev, c_max);
+    const int j = blockIdx.y;
+    const int kept = min(counts[j], c_eff);
+    const int lane = threadIdx.x & 31;
+    const int nch = m / Elt<T>::VEC;
+    V16 z;
+    z.w[0] = z.w[1] = z.w[2] = z.w[3] = 0u;
+    for (int64_t row = kept + (int64_t)blockIdx.x * (DNT / 32) + (threadIdx.x >> 5); row < c_eff;
+         row += (int64_t)gridDim.x * (DNT / 32)) {
+        V16 *dst = reinterpret_cast<V16 *>(buf + ((int64_t)j * c_max + row) * m);
+        for (int q = lane; q < nch; q += 32) st_v16(dst + q, z);
+    }
+}
+
+// ------------------------------------------------ combine: decode (K0) and
+// encode backward (K0 with unit weights)
+template <typename T, bool WEIGHTED>
+__global__ void __launch_bounds__(DNT)
+combine_kernel(const T *__restrict__ src, const int32_t *__restrict__ idx,
+               const int32_t *__restrict__ loc, const float *__restrict__ gates,
+               const int32_t *__restrict__ c_dev, int64_t s, int m, int e, int k, int64_t c_max,
+               T *__restrict__ y, int32_t *status) {
+    if (status_bad(status)) return;
+    constexpr int VEC = Elt<T>::VEC;
+    const int c_eff = read_c(c_dev, c_max);
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = (int64_t)gridDim.x * (DNT / 32);
+    const int nch = m / VEC;
+    for (int64_t t = blockIdx.x * (DNT / 32) + (threadIdx.x >> 5); t < s; t += nw) {
+        Routes R = load_routes(idx, loc, WEIGHTED ? gates : nullptr, s, t, m, e, k, c_eff, c_max,
+                               status);
+        V16 *dst = reinterpret_cast<V16 *>(y + t * m);
+        for (int base = 0; base < nch; base += 32 * UNR) {  // warp-uniform trip count
+            const int q0 = base + lane;
+            float acc[UNR][VEC];
+#pragma unroll
+            for (int u = 0; u < UNR; u++)
+#pragma unroll
+                for (int i = 0; i < VEC; i++) acc[u][i] = 0.0f;
+            for (unsigned km = R.kept; km; km &= km - 1) {  // ascending route order
+                int r = __ffs(km) - 1;
+                int64_t row = __shfl_sync(0xffffffffu, R.row, r);
+                float g = WEIGHTED ? __shfl_sync(0xffffffffu, R.g, r) : 1.0f;
+                const V16 *sp = reinterpret_cast<const V16 *>(src + row);
+                V16 v[UNR];
+#pragma unroll
+                for (int u = 0; u < UNR; u++)
+                    if (q0 + 32 * u < nch) v[u] = ld_stream(sp + q0 + 32 * u);
+#pragma unroll
+                for (int u = 0; u < UNR; u++) {
+                    float f[VEC];
+                    Elt<T>::unpack(v[u], f);
+#pragma unroll
+                    for (int i = 0; i < VEC; i++)
+                        acc[u][i] = WEIGHTED ? __fmaf_rn(g, f[i], acc[u][i]) : __fadd_rn(acc[u][i], f[i]);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < UNR; u++)
+                if (q0 + 32 * u < nch) st_v16_cs(dst + q0 + 32 * u, Elt<T>::pack(acc[u]));
+        }
+    }
+}
+
+// g * d correctly rounded to bf16 (one rounding of the exact product): the
+// fp32 product p is exact to within the error term err = fma(g, d, -p); only
+// when p sits exactly halfway between two bf16 values does err decide.
+__device__ __forceinline__ uint32_t mul_round_bf16(float g, float d) {
+    float p = __fmul_rn(g, d);
+    float err = __fmaf_rn(g, d, -p);
+    uint32_t u = __float_as_uint(p);
+    if ((u & 0xFFFFu) == 0x8000u && err != 0.0f && (u & 0x7F800000u) != 0x7F800000u) {
+        bool away = (err > 0.0f) == (p > 0.0f);
+        return (u >> 16) + (away ? 1u : 0u);
+    }
+    return f2bf(p);
+}
+
+template <typename T> struct ScaleRound;
+template <> struct ScaleRound<float> {
+    __device__ __forceinline__ static V16 apply(float g, const V16 &d) {
+        V16 o;
+#pragma unroll
+        for (int i = 0; i < 4; i++) o.w[i] = __float_as_uint(__fmul_rn(g, __uint_as_float(d.w[i])));
+        return o;
+    }
+};
+template <> struct ScaleRound<__nv_bfloat16> {
+    __device__ __forceinline__ static V16 apply(float g, const V16 &d) {
+        V16 o;
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+            o.w[i] = mul_round_bf16(g, bf16lo(d.w[i])) | (mul_round_bf16(g, bf16hi(d.w[i])) << 16);
+        return o;
+    }
+};
+
+// -------------------------------------------- decode backward (K1 bwd + K2)
+template <typename T>
+__global__ void __launch_bounds__(DNT)
+decode_bwd_kernel(const T *__restrict__ dy, const T *__restrict__ out,
+                  const int32_t *__restrict__ idx, const int32_t *__restrict__ loc,
+                  const float *__restrict__ gates, const int32_t *__restrict__ c_dev, int64_t s,
+                  int m, int e, int k, int64_t c_max, T *__restrict__ d_out,
+                  float *__restrict__ d_gates, int32_t *status) {
+    if (status_bad(status)) return;
+    constexpr int VEC = Elt<T>::VEC;
+    const int c_eff = read_c(c_dev, c_max);
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = (int64_t)gridDim.x * (DNT / 32);
+    const int nch = m / VEC;
+    for (int64_t t = blockIdx.x * (DNT / 32) + (threadIdx.x >> 5); t < s; t += nw) {
+        Routes R = load_routes(idx, loc, gates, s, t, m, e, k, c_eff, c_max, status);
+        if (lane < k && !((R.kept >> lane) & 1u)) d_gates[(int64_t)lane * s + t] = 0.0f;
+        if (!R.kept) continue;
+        const V16 *dyp = reinterpret_cast<const V16 *>(dy + t * m);
+        for (unsigned km = R.kept; km; km &= km - 1) {
+            int r = __ffs(km) - 1;
+            int64_t row = __shfl_sync(0xffffffffu, R.row, r);
+            float g = __shfl_sync(0xffffffffu, R.g, r);
+            const V16 *op = reinterpret_cast<const V16 *>(out + row);
+            V16 *dp = reinterpret_cast<V16 *>(d_out + row);
+            float part = 0.0f;
+            for (int base = 0; base < nch; base += 32 * UNR) {
+                const int q0 = base + lane;
+                V16 dv[UNR], ov[UNR];
+#pragma unroll
+                for (int u = 0; u < UNR; u++)
+                    if (q0 + 32 * u < nch) {
+                        dv[u] = ld_v16(dyp + q0 + 32 * u);  // re-read per route: keep in L1
+                        ov[u] = ld_stream(op + q0 + 32 * u);
+                    }
+#pragma unroll
+                for (int u = 0; u < UNR; u++)
+                    if (q0 + 32 * u < nch) {
+                        float a[VEC], b[VEC];
+                        Elt<T>::unpack(dv[u], a);
+                        Elt<T>::unpack(ov[u], b);
+#pragma unroll
+                        for (int i = 0; i < VEC; i++) part = __fmaf_rn(a[i], b[i], part);
+                        st_v16(dp + q0 + 32 * u, ScaleRound<T>::apply(g, dv[u]));
+                    }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            if (lane == 0) d_gates[(int64_t)r * s + t] = part;
+        }
+    }
+}
+
+int grid_for_tokens(int64_t s) {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int64_t want = (s + (DNT / 32) - 1) / (DNT / 32);
+    int64_t cap = (int64_t)sms * 8;  // 8 CTAs x 8 warps per SM: 64 warps resident
+    return (int)(want < cap ? want : cap);
+}
+
+}  // namespace
+
+moe_status encode_launch(const void *x, moe_dtype dt, const int32_t *idx, const int32_t *loc,
+                         const int32_t *counts, const int32_t *c_dev, int64_t s, int m, int e,
+                         int k, int64_t c_max, unsigned flags, void *buf, int32_t *st,
+                         cudaStream_t stream) {
+    const int grid = grid_for_tokens(s);
+    if (dt == MOE_BF16)
+        encode_kernel<__nv_bfloat16><<<grid, DNT, 0, stream>>>(
+            (const __nv_bfloat16 *)x, idx, loc, c_dev, s, m, e, k, c_max, (__nv_bfloat16 *)buf, st);
+    else
+        encode_kernel<float><<<grid, DNT, 0, stream>>>((const float *)x, idx, loc, c_dev, s, m, e, k,
+                                                       c_max, (float *)buf, st);
+    note_launch();
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (flags & MOE_FLAG_ZERO_FILL) {
+        int64_t gx = (c_max + (DNT / 32) - 1) / (DNT / 32);
+        dim3 g((unsigned)(gx < 1024 ? gx : 1024), (unsigned)e);
+        if (dt == MOE_BF16)
+            zero_fill_kernel<__nv_bfloat16><<<g, DNT, 0, stream>>>(counts, c_dev, e, c_max, m,
+                                                                  (__nv_bfloat16 *)buf, st);
+        else
+            zero_fill_kernel<float><<<g, DNT, 0, stream>>>(counts, c_dev, e, c_max, m, (float *)buf,
+                                                          st);
+        note_launch();
+        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+moe_status combine_launch(const void *src, moe_dtype dt, const int32_t *idx, const int32_t *loc,
+                          const float *gates, const int32_t *c_dev, int64_t s, int m, int e, int k,
+                          int64_t c_max, void *y, int32_t *st, cudaStream_t stream) {
+    const int grid = grid_for_tokens(s);
+    const bool w = gates != nullptr;
+    if (dt == MOE_BF16) {
+        auto *sp = (const __nv_bfloat16 *)src;
+        auto *yp = (__nv_bfloat16 *)y;
+        if (w) combine_kernel<__nv_bfloat16, true><<<grid, DNT, 0, stream>>>(sp, idx, loc, gates, c_dev, s, m, e, k, c_max, yp, st);
+        else combine_kernel<__nv_bfloat16, false><<<grid, DNT, 0, stream>>>(sp, idx, loc, nullptr, c_dev, s, m, e, k, c_max, yp, st);
+    } else {
+        auto *sp = (const float *)src;
+        auto *yp = (float *)y;
+        if (w) combine_kernel<float, true><<<grid, DNT, 0, stream>>>(sp, idx, loc, gates, c_dev, s, m, e, k, c_max, yp, st);
+        else combine_kernel<float, false><<<grid, DNT, 0, stream>>>(sp, idx, loc, nullptr, c_dev, s, m, e, k, c_max, yp, st);
+    }
+    note_launch();
+    return launch_status();
+}
+
+moe_status decode_bwd_launch(const void *dy, const void *out, moe_dtype dt, const int32_t *idx,
+                             const int32_t *loc, const float *gates, const int32_t *counts,
+                             const int32_t *c_dev, int64_t s, int m, int e, int k, int64_t c_max,
+                             unsigned flags, void *d_out, float *d_gates, int32_t *st,
+                             cudaStream_t stream) {
+    if (flags & MOE_FLAG_ZERO_FILL) {
+        int64_t gx = (c_max + (DNT / 32) - 1) / (DNT / 32);
+        dim3 g((unsigned)(gx < 1024 ? gx : 1024), (unsigned)e);
+        if (dt == MOE_BF16)
+            zero_fill_kernel<__nv_bfloat16><<<g, DNT, 0, stream>>>(counts, c_dev, e, c_max, m,
+                                                                  (__nv_bfloat16 *)d_out, st);
+        else
+            zero_fill_kernel<float><<<g, DNT, 0, stream>>>(counts, c_dev, e, c_max, m,
+                                                          (float *)d_out, st);
+        note_launch();
+        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    }
+    const int grid = grid_for_tokens(s);
+    if (dt == MOE_BF16)
+        decode_bwd_kernel<__nv_bfloat16><<<grid, DNT, 0, stream>>>(
+            (const __nv_bfloat16 *)dy, (const __nv_bfloat16 *)out, idx, loc, gates, c_dev, s, m, e,
+            k, c_max, (__nv_bfloat16 *)d_out, d_gates, st);
+    else
+        decode_bwd_kernel<float><<<grid, DNT, 0, stream>>>((const float *)dy, (const float *)out,
+                                                           idx, loc, gates, c_dev, s, m, e, k, c_max,
+                                                           (float *)d_out, d_gates, st);
+    note_launch();
+    return launch_status();
+}
+
+}  // namespace moe

@@ -1,0 +1,222 @@
+/*
+ * moe_gate.h -- C ABI of the single-GPU top-k Mixture-of-Experts layer hot path
+ * (gate -> capacity/locations -> encode -> expert FFN -> decode, plus the
+ * backward of encode and decode), built for NVIDIA GB300 (sm_103a).
+ *
+ * Sources restated (web pages, cited by title and section):
+ *   [Tutel]  "Tutel" project profile: key-configuration table (MOELayer
+ *            gate_type {'type': 'top', 'k', 'capacity_factor'}, experts
+ *            {'type': 'ffn', hidden_size_per_expert, has_fc1_bias,
+ *            has_fc2_bias}) and the FAQ on capacity_factor.
+ *   [Blog]   "MoE training systems: DeepSpeed-MoE vs Tutel", section 1.4
+ *            (dense token-to-expert mapping table; fused top-k + cumsum +
+ *            scatter; data-layout transform instead of einsum) and section 3.5
+ *            (fast encode/decode kernels K0, K1, K2; dynamic capacity factor).
+ *   [PR8195] DeepSpeed PR #8195 (follow-up to #8174): change 1 (per-route
+ *            int32 index/location/gate, capacity resolved once without a
+ *            device-to-host sync), change 2 (the [e, c, m] vs flat [e*c, m]
+ *            buffer hazard), change 3 (index dispatch, fp32 combine).
+ *
+ * Conventions shared by every call:
+ *   - Every pointer argument is caller-owned memory.  Device pointers must be
+ *     16-byte aligned.  Tensors are dense row-major with the shapes given.
+ *   - No call allocates, frees or synchronises.  Work is enqueued on `stream`
+ *     (a cudaStream_t passed as void*; NULL = the legacy default stream).
+ *   - Routing tables are route-major [k, s]: entry (r, t) is at r*s + t.
+ *     Route r of token t is its r-th best expert.
+ *   - Expert buffers are physically [e, c_max, m] (row stride c_max*m per
+ *     expert).  The logical [e, c, m] view is rows 0..c-1 of each expert.
+ *     c_max is fixed by the caller; the data-dependent c lives in device
+ *     memory (`c_dev`) and is never read back by the library.
+ *   - A route is kept iff loc < c.  Dropped routes keep their un-clipped loc.
+ *   - dev_status: caller-owned device int32, zeroed by the caller.  A kernel
+ *     that detects a data-dependent error (c > c_max, an index out of range,
+ *     a bounded wait that gave up) stores the first error code there.  Every
+ *     kernel reads it on entry and does nothing if it is non-zero.  The caller
+ *     reads it after its own synchronisation.
+ *   - Host-side validation is synchronous: a bad shape, NULL or misaligned
+ *     pointer returns MOE_ERR_INVALID_ARG and nothing is launched.  A launch
+ *     failure returns MOE_ERR_CUDA.
+ *   - Shapes: s >= 1, 1 <= k <= min(e, 32), 1 <= e <= 1024, m, h >= 1.
+ *     Rows must be 16-byte multiples: m and h multiples of 8 (bf16) or 4 (fp32).
+ */
+#ifndef MOE_GATE_H
+#define MOE_GATE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* bad shape / pointer (host) or bad index (device) */
+    MOE_ERR_UNSUPPORTED = 2,  /* valid but not implemented combination */
+    MOE_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+    MOE_ERR_CAPACITY = 4,     /* device: capacity c exceeds c_max */
+    MOE_ERR_TIMEOUT = 5       /* device: a bounded wait gave up */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef enum {
+    MOE_ACT_RELU = 0,   /* y = relu(x W1^T + b1) W2^T + b2 */
+    MOE_ACT_GELU = 1,   /* y = gelu_erf(x W1^T + b1) W2^T + b2 */
+    MOE_ACT_SWIGLU = 2  /* y = (silu(x W1^T) * (x W3^T)) W2^T, no biases */
+} moe_act;
+
+#define MOE_FLAG_NORMALIZE_GATES 1u /* divide the k selected gates by their sum */
+#define MOE_FLAG_ZERO_FILL 2u       /* zero the unoccupied rows 0..c-1 of each expert */
+
+/*
+ * Gate ([Tutel] gate_type 'top'; [Blog] 1.4 fused top-k).
+ *   logits[t, j] = fp32 dot(x[t, :], wg[:, j]) + bias[j], with one accumulator
+ *   from +0 updated by fused multiply-add in ascending feature index, then one
+ *   fp32 add of the bias.  This fixed order makes idx reproducible bit for bit.
+ *   idx[r, t]: expert at position r when experts are ordered by (logit
+ *   descending, index ascending).  gates[r, t]: softmax probability of that
+ *   expert over all e logits; with MOE_FLAG_NORMALIZE_GATES divided by the sum
+ *   of the k selected probabilities.
+ * x [s, m] in `xdt`; wg [m, e] fp32; bias [e] fp32 or NULL.
+ * idx [k, s] int32 and gates [k, s] fp32 are written.  e <= 256 here.
+ */
+moe_status moe_gate_topk(const void *x, moe_dtype xdt, const float *wg, const float *bias,
+                         int64_t s, int m, int e, int k, unsigned flags,
+                         int32_t *idx, float *gates, int32_t *dev_status, void *stream);
+
+/*
+ * Capacity bound on the host ([Tutel] FAQ capacity_factor; [Blog] 3.5).
+ *   f > 0: exactly c = ceil(f*k*s/e)  (evaluated exactly on the float value f);
+ *   f = 0: s  (the largest c the no-drop rule can produce);
+ *   f < 0: min(ceil(-f*k*s/e), s).
+ * A c_max at least this large never triggers MOE_ERR_CAPACITY.
+ */
+int64_t moe_capacity_bound(float capacity_factor, int64_t s, int e, int k);
+
+/* Bytes of device workspace moe_capacity_locations needs. */
+size_t moe_capacity_workspace_size(int64_t s, int e, int k);
+
+/*
+ * Capacity and slot locations ([Blog] 1.4 cumsum; [Blog] 3.5 dynamic capacity).
+ *   counts[j] = number of routes that chose expert j (before any drop).
+ *   c = ceil(f*k*s/e) for f > 0; max_j counts[j] for f = 0;
+ *       min(ceil(-f*k*s/e), max_j counts[j]) for f < 0.   Written to c_dev[0].
+ *   loc[r, t] = number of routes ahead of (r, t) in route-priority order
+ *   (all tokens' route 0 in token order, then route 1, ...) that chose the
+ *   same expert.  Kept iff loc < c.
+ *   c > c_max stores MOE_ERR_CAPACITY in dev_status (loc/counts still valid).
+ * idx [k, s] int32 in; loc [k, s] int32, counts [e] int32, c_dev [1] int32 out.
+ * workspace: device memory of moe_capacity_workspace_size() bytes, contents
+ * ignored on entry (scratch).
+ */
+moe_status moe_capacity_locations(const int32_t *idx, int64_t s, int e, int k,
+                                  float capacity_factor, int64_t c_max,
+                                  void *workspace, size_t workspace_bytes,
+                                  int32_t *loc, int32_t *counts, int32_t *c_dev,
+                                  int32_t *dev_status, void *stream);
+
+/*
+ * Fast encode ([Blog] 3.5, kernel K1 forward; [PR8195] change 3).
+ *   buf[idx[r,t], loc[r,t], :] = x[t, :] for every kept route (unweighted copy).
+ *   With MOE_FLAG_ZERO_FILL, rows min(counts[j], c)..c-1 of every expert j are
+ *   set to zero as well (counts required then, else it may be NULL).  Other
+ *   rows of buf are left untouched.
+ * x [s, m]; buf [e, c_max, m], both in `dt`.
+ */
+moe_status moe_encode(const void *x, moe_dtype dt, const int32_t *idx, const int32_t *loc,
+                      const int32_t *counts, const int32_t *c_dev, int64_t s, int m, int e,
+                      int k, int64_t c_max, unsigned flags, void *buf, int32_t *dev_status,
+                      void *stream);
+
+/* Bytes of device workspace moe_expert_ffn needs (the hidden activations). */
+size_t moe_expert_ffn_workspace_size(moe_dtype dt, moe_act act, int e, int64_t c_max, int m,
+                                     int h);
+
+/*
+ * Per-expert FFN ([Tutel] experts 'ffn'; [Blog] 3.5 batched expert matmul over
+ * (E, C, D)).  For every expert j and row i < min(counts[j], c):
+ *   hid = act(buf[j,i,:] W1[j]^T + b1[j])        (ReLU / GELU, exact erf form)
+ *   hid = silu(buf[j,i,:] W1[j]^T) * (buf[j,i,:] W3[j]^T)      (SwiGLU)
+ *   out[j,i,:] = hid W2[j]^T + b2[j]
+ * Accumulation in fp32; the hidden activation is rounded to `dt` before the
+ * second product; each output is rounded once to `dt`.  Rows >= the kept
+ * count are not written.
+ * buf, out [e, c_max, m]; w1, w3 [e, h, m]; w2 [e, m, h]; b1 [e, h]; b2 [e, m];
+ * all in `dt`.  b1/b2 may be NULL (no bias); w3 only for SwiGLU, which takes
+ * no biases.  workspace: moe_expert_ffn_workspace_size() bytes, scratch.
+ * bf16 runs on the tensor cores (tcgen05, fp32 accumulation in TMEM); fp32
+ * runs on the SIMT cores with fp32 fused multiply-add.
+ */
+moe_status moe_expert_ffn(const void *buf, moe_dtype dt, const int32_t *counts,
+                          const int32_t *c_dev, const void *w1, const void *b1, const void *w3,
+                          const void *w2, const void *b2, moe_act act, int e, int64_t c_max,
+                          int m, int h, void *workspace, size_t workspace_bytes, void *out,
+                          int32_t *dev_status, void *stream);
+
+/*
+ * Fast decode ([Blog] 3.5, K0 forward; [PR8195] change 3, fp32 combine).
+ *   y[t, :] = sum over kept routes r of gates[r,t] * out[idx[r,t], loc[r,t], :],
+ *   accumulated in fp32 with fused multiply-add in ascending r from +0 and
+ *   rounded once to `dt`.  Tokens with every route dropped get 0.
+ * out [e, c_max, m], y [s, m] in `dt`; gates [k, s] fp32.
+ */
+moe_status moe_decode(const void *out, moe_dtype dt, const int32_t *idx, const int32_t *loc,
+                      const float *gates, const int32_t *c_dev, int64_t s, int m, int e, int k,
+                      int64_t c_max, void *y, int32_t *dev_status, void *stream);
+
+/*
+ * Backward of decode ([Blog] 3.5: K1 is combine's backward, K2 the cross term).
+ *   d_out[idx, loc, :] = gates[r,t] * dy[t, :]  (exact product rounded once)
+ *   d_gates[r, t] = sum_i dy[t,i] * out[idx, loc, i]  (fp32), 0 if dropped.
+ *   With MOE_FLAG_ZERO_FILL (counts required) unoccupied rows < c of d_out
+ *   are zeroed; otherwise they are left untouched.
+ * dy [s, m], out and d_out [e, c_max, m] in `dt`; gates, d_gates [k, s] fp32.
+ */
+moe_status moe_decode_bwd(const void *dy, const void *out, moe_dtype dt, const int32_t *idx,
+                          const int32_t *loc, const float *gates, const int32_t *counts,
+                          const int32_t *c_dev, int64_t s, int m, int e, int k, int64_t c_max,
+                          unsigned flags, void *d_out, float *d_gates, int32_t *dev_status,
+                          void *stream);
+
+/*
+ * Backward of encode ([Blog] 3.5: K0 with unit weights).
+ *   dx[t, :] = sum over kept routes of d_buf[idx, loc, :], fp32 accumulation
+ *   in ascending r from +0, rounded once to `dt`.  All-dropped tokens get 0.
+ * d_buf [e, c_max, m], dx [s, m] in `dt`.
+ */
+moe_status moe_encode_bwd(const void *d_buf, moe_dtype dt, const int32_t *idx,
+                          const int32_t *loc, const int32_t *c_dev, int64_t s, int m, int e,
+                          int k, int64_t c_max, void *dx, int32_t *dev_status, void *stream);
+
+/* Bytes of device workspace moe_layer_forward needs. */
+size_t moe_layer_workspace_size(moe_dtype dt, moe_act act, int64_t s, int m, int e, int k,
+                                int64_t c_max, int h);
+
+/*
+ * The whole forward layer in one call: moe_gate_topk, moe_capacity_locations,
+ * moe_encode, moe_expert_ffn and moe_decode enqueued back to back on `stream`
+ * with no host synchronisation.  Intermediate tensors the caller may inspect
+ * (idx, gates, loc, counts, c_dev, buf, out) are caller-owned outputs; the
+ * rest lives in `workspace` (moe_layer_workspace_size() bytes).
+ */
+moe_status moe_layer_forward(const void *x, moe_dtype dt, const float *wg, const float *gate_bias,
+                             const void *w1, const void *b1, const void *w3, const void *w2,
+                             const void *b2, moe_act act, int64_t s, int m, int e, int k, int h,
+                             float capacity_factor, int64_t c_max, unsigned flags,
+                             int32_t *idx, float *gates, int32_t *loc, int32_t *counts,
+                             int32_t *c_dev, void *buf, void *out, void *y,
+                             void *workspace, size_t workspace_bytes,
+                             int32_t *dev_status, void *stream);
+
+/* Human-readable name of a status code (static string). */
+const char *moe_status_str(moe_status st);
+
+/* Number of kernels this library has launched in this process (monotonic). */
+uint64_t moe_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GATE_H */

@@ -90,13 +90,17 @@ void orc_gate_logits(const float *x, const float *wg, const float *bias,
 {
 #pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < s; t++) {
-        for (int j = 0; j < e; j++) {
-            float acc = 0.0f;
-            for (int i = 0; i < m; i++)
-                acc = fmaf(x[t * m + i], wg[(int64_t)i * e + j], acc);
-            if (bias) acc = acc + bias[j];
-            logits[t * e + j] = acc;
+        /* acc[j] is logit (t, j)'s single accumulator; the loops visit i in
+         * ascending order for every j (walking wg row by row). */
+        float *acc = logits + t * e;
+        for (int j = 0; j < e; j++) acc[j] = 0.0f;
+        for (int i = 0; i < m; i++) {
+            const float xi = x[t * m + i];
+            const float *wr = wg + (int64_t)i * e;
+            for (int j = 0; j < e; j++) acc[j] = fmaf(xi, wr[j], acc[j]);
         }
+        if (bias)
+            for (int j = 0; j < e; j++) acc[j] = acc[j] + bias[j];
     }
 }
 

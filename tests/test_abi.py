@@ -1,0 +1,100 @@
+"""The C ABI on the host: the library loads and exports every symbol the header
+declares; host-side logic (capacity bound, workspace sizes, argument checks)
+behaves as documented.  No call here reaches a kernel launch."""
+
+import ctypes
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import combine_moe_gate_gb300 as M
+import oracle
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def test_library_exports_every_declared_symbol():
+    lib = M.load()
+    names = M.declared_symbols()
+    assert len(names) >= 14
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    # exported with C linkage: visible to a plain dlsym by the unmangled name
+    raw = ctypes.CDLL(M.LIB_PATH)
+    for n in names:
+        ctypes.cast(getattr(raw, n), ctypes.c_void_p)
+
+
+def test_status_strings():
+    assert M.status_str(M.MOE_OK) == "ok"
+    assert "c_max" in M.status_str(M.MOE_ERR_CAPACITY)
+    assert M.status_str(99) == "unknown status"
+
+
+def test_capacity_bound_matches_closed_forms():
+    with open(os.path.join(GOLD, "capacity.json")) as f:
+        cap = json.load(f)
+    for c in cap["fixed"]:
+        assert M.moe_capacity_bound(c["f"], c["s"], c["e"], c["k"]) == c["c"]
+    for c in cap["capped_bound"]:
+        assert M.moe_capacity_bound(c["f"], c["s"], c["e"], c["k"]) == c["bound"]
+    assert M.moe_capacity_bound(0.0, 8192, 16, 3) == 8192       # no-drop: at most s per expert
+    assert M.moe_capacity_bound(-100.0, 50, 2, 2) == 50          # capped by s
+    assert M.moe_capacity_bound(1.0, 10, 4, 5) == -1             # k > e: invalid
+
+
+@pytest.mark.parametrize("f", [0.3, 1.0, 1.25, 1.7, 2.0, 3.3])
+def test_capacity_bound_agrees_with_oracle(f):
+    rng = np.random.default_rng(int(f * 10))
+    for _ in range(50):
+        e = int(rng.integers(1, 300))
+        k = int(rng.integers(1, min(e, 32) + 1))
+        s = int(rng.integers(1, 100000))
+        want = oracle.capacity(f, s, e, k, np.zeros(e, np.int64))
+        assert M.moe_capacity_bound(f, s, e, k) == want
+
+
+def test_workspace_sizes():
+    ws = M.moe_capacity_workspace_size(16384, 256, 8)
+    assert ws >= 32 * 256 * 4 and ws % 256 == 0
+    h = M.moe_expert_ffn_workspace_size(M.MOE_BF16, "gelu", 8, 1280, 1024, 4096)
+    assert h == 8 * 1280 * 4096 * 2
+    assert M.moe_layer_workspace_size(M.MOE_BF16, "gelu", 4096, 1024, 8, 2, 1280, 4096) >= h + 256
+    assert M.moe_expert_ffn_workspace_size(7, "gelu", 8, 1280, 1024, 4096) == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake device pointers are only safe without a GPU")
+def test_invalid_arguments_are_rejected_before_launch():
+    lib = M.load()
+    before = M.launch_count()
+    A = ctypes.c_void_p(0x10000)      # 16-byte aligned fake addresses (never dereferenced)
+    B = ctypes.c_void_p(0x20000)
+    odd = ctypes.c_void_p(0x30004)
+    INV = M.MOE_ERR_INVALID_ARG
+    gate = lib.moe_gate_topk
+    # k > e, k = 0, s = 0, m not a multiple of 8 for bf16, NULL / misaligned x
+    assert gate(A, M.MOE_BF16, B, None, 10, 64, 4, 5, 0, A, B, A, None) == INV
+    assert gate(A, M.MOE_BF16, B, None, 10, 64, 4, 0, 0, A, B, A, None) == INV
+    assert gate(A, M.MOE_BF16, B, None, 0, 64, 4, 1, 0, A, B, A, None) == INV
+    assert gate(A, M.MOE_BF16, B, None, 10, 60, 4, 1, 0, A, B, A, None) == INV
+    assert gate(None, M.MOE_BF16, B, None, 10, 64, 4, 1, 0, A, B, A, None) == INV
+    assert gate(odd, M.MOE_BF16, B, None, 10, 64, 4, 1, 0, A, B, A, None) == INV
+    assert gate(A, 5, B, None, 10, 64, 4, 1, 0, A, B, A, None) == INV
+    assert gate(A, M.MOE_BF16, B, None, 10, 64, 4, 1, 8, A, B, A, None) == INV  # unknown flag
+    cap = lib.moe_capacity_locations
+    assert cap(A, 100, 4, 2, 1.0, 0, A, 1 << 20, A, A, A, A, None) == INV        # c_max = 0
+    assert cap(A, 100, 4, 2, 1.0, 50, A, 0, A, A, A, A, None) == INV             # workspace too small
+    assert cap(A, 100, 4, 2, float("nan"), 50, A, 1 << 20, A, A, A, A, None) == INV
+    ffn = lib.moe_expert_ffn
+    # SwiGLU takes no biases and needs w3
+    assert ffn(A, M.MOE_BF16, A, A, A, B, A, A, None, 2, 4, 64, 64, 64, A, 1 << 30, A, A, None) == INV
+    assert ffn(A, M.MOE_BF16, A, A, A, None, None, A, None, 2, 4, 64, 64, 64, A, 1 << 30, A, A, None) == INV
+    assert ffn(A, M.MOE_BF16, A, A, A, None, None, A, None, 7, 4, 64, 64, 64, A, 1 << 30, A, A, None) == INV
+    dec = lib.moe_decode
+    assert dec(A, M.MOE_F32, A, A, A, A, 10, 6, 4, 1, 8, A, A, None) == INV    # m % 4 != 0 (fp32)
+    enc = lib.moe_encode
+    assert enc(A, M.MOE_BF16, A, A, None, A, 10, 64, 4, 1, 8, M.MOE_FLAG_ZERO_FILL, A, A, None) == INV
+    assert M.launch_count() == before
