@@ -1,0 +1,397 @@
+"""Benchmark of the MoE layer forward hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one forward pass of the whole path (gate -> capacity/locations ->
+encode -> expert FFN -> decode) over one batch of the bf16 workload
+s=4096 m=1024 e=8 k=2 h=4096 GELU, capacity_factor 1.25.  Inputs are seeded
+synthetic tensors already resident in HBM; L2 is flushed (256 MiB write)
+before every timed step and the flush is outside the timed interval.
+
+value       whole-job forward tokens/s (device time, CUDA events, max over ranks)
+e2e         the same metric through the one-call public API (moe_layer_forward)
+            with the step's input copied from pinned host memory and the output
+            copied back inside the timed interval
+roofline    the expert FFN (the dominant stage): algorithmic bf16 FLOPs of the
+            kept rows / its measured duration, against the measured bf16 peak
+cpu_baseline the CPU oracle timed on the host cores on a bounded token sample
+
+With --gpus N > 1 (torchrun) every rank runs an independent replica of the
+layer on its own GPU ("replicas only": the layer has no cross-GPU step).
+`--impl reference` times the CPU oracle as the reference arm (rank 0 only).
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from synth.workloads import BF16_E8  # noqa: E402
+
+METRIC = "MoE-layer fwd tokens/s; encode/decode HBM GB/s and FFN TC util, 1×GB300"
+WORKLOAD = BF16_E8
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d.get("bf16_tflops_sustained"),
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [l for (ts, l) in self.lines if t0 - 0.06 <= ts <= t1 + 0.06] or [l for _, l in self.lines]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle
+def oracle_sample_inputs(w, inp, s_sample):
+    """The first s_sample tokens of the workload's batch (same weights)."""
+    ws = w.with_(s=s_sample, name=f"{w.name}_first{s_sample}")
+    sub = dict(inp)
+    sub["x"] = inp["x"][:s_sample]
+    return ws, sub
+
+
+def time_oracle(w, inp, target_s):
+    """Time the CPU oracle's full forward chain on the first s' tokens, s' sized
+    so the run takes about target_s seconds.  Returns (tokens/s, s', seconds, threads)."""
+    import oracle
+
+    s1 = 16
+    ws, sub = oracle_sample_inputs(w, inp, s1)
+    t = time.perf_counter()
+    oracle.layer_forward(ws, sub)
+    dt = time.perf_counter() - t
+    s2 = int(max(s1, min(w.s, s1 * target_s / max(dt, 1e-3))))
+    ws, sub = oracle_sample_inputs(w, inp, s2)
+    t = time.perf_counter()
+    oracle.layer_forward(ws, sub)
+    dt = time.perf_counter() - t
+    return s2 / dt, s2, dt, oracle.get_threads()
+
+
+def cpu_baseline_dict(w, inp, target_s):
+    v, s2, dt, thr = time_oracle(w, inp, target_s)
+    return {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+            "sample": f"full forward chain (gate, capacity, encode, FFN, decode) on the first {s2} "
+                      f"tokens of the batch, same weights; {dt:.1f} s on {thr} threads"}
+
+
+# ------------------------------------------------------------------- ours
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import combine_moe_gate_gb300 as M
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = WORKLOAD
+    inp = synth.make_inputs_host(w)
+
+    def D(a):
+        if a is None:
+            return None
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    x, wg, gb = D(inp["x"]), D(inp["wg"]), D(inp["bias"])
+    w1, b1, w3, w2, b2 = (D(inp[n]) for n in ("w1", "b1", "w3", "w2", "b2"))
+    bufs = M.alloc_layer(w.s, w.m, w.e, w.k, w.h, w.act, w.capacity_factor, device=dev)
+    flags = M.MOE_FLAG_NORMALIZE_GATES if w.normalize_gates and w.k >= 2 else 0
+    cap_ws = bufs.workspace[: M.moe_capacity_workspace_size(w.s, w.e, w.k)]
+    ffn_ws = torch.empty(M.moe_expert_ffn_workspace_size(M.MOE_BF16, w.act, w.e, bufs.c_max, w.m, w.h),
+                         dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def staged_step(ev):
+        """The five C-ABI calls, with an event after each stage."""
+        M.moe_gate_topk(x, wg, gb, w.k, bufs.idx, bufs.gates, bufs.status, flags=flags)
+        ev[1].record()
+        M.moe_capacity_locations(bufs.idx, w.e, w.capacity_factor, bufs.c_max, cap_ws, bufs.loc,
+                                 bufs.counts, bufs.c_dev, bufs.status)
+        ev[2].record()
+        M.moe_encode(x, bufs.idx, bufs.loc, bufs.counts, bufs.c_dev, bufs.buf, bufs.status)
+        ev[3].record()
+        M.moe_expert_ffn(bufs.buf, bufs.counts, bufs.c_dev, w1, b1, w3, w2, b2, w.act, ffn_ws,
+                         bufs.out, bufs.status)
+        ev[4].record()
+        M.moe_decode(bufs.out, bufs.idx, bufs.loc, bufs.gates, bufs.c_dev, bufs.y, bufs.status)
+
+    def mk():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        ev = mk()
+        ev[0].record()
+        staged_step(ev)
+        ev[5].record()
+    torch.cuda.synchronize()
+    if int(bufs.status.item()) != 0:
+        raise RuntimeError(f"device status {int(bufs.status.item())}")
+
+    # ---- timed: device-resident inputs
+    n_launch0 = M.launch_count()
+    events = []
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t_wall0 = clk.mark()
+        for _ in range(args.steps):
+            flush.fill_(1)
+            ev = mk()
+            ev[0].record()
+            staged_step(ev)
+            ev[5].record()
+            events.append(ev)
+        torch.cuda.synchronize()
+        t_wall1 = clk.mark()
+    if world > 1:
+        torch.distributed.barrier()
+    launches = M.launch_count() - n_launch0
+    stage_names = ["gate", "capacity", "encode", "expert_ffn", "decode"]
+    stage_ms = {n: 0.0 for n in stage_names}
+    total_ms = 0.0
+    for ev in events:
+        total_ms += ev[0].elapsed_time(ev[5])
+        for i, n in enumerate(stage_names):
+            stage_ms[n] += ev[i].elapsed_time(ev[i + 1])
+    ms_step = total_ms / args.steps
+    stage_ms = {n: v / args.steps for n, v in stage_ms.items()}
+
+    # ---- e2e: one-call public API, host input/output inside the interval
+    x_host = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_host = torch.empty((w.s, w.m), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(x)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        M.run_layer(x_dev, wg, gb, w1, b1, w3, w2, b2, w.act, w.k, w.capacity_factor, bufs,
+                    normalize_gates=bool(flags))
+        y_host.copy_(bufs.y, non_blocking=True)
+
+    for _ in range(max(3, args.warmup // 2)):
+        flush.fill_(1)
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = 0.0
+    for _ in range(args.steps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        e2e_step()
+        b.record()
+        b.synchronize()
+        e2e_ms += a.elapsed_time(b)
+    e2e_ms /= args.steps
+
+    # ---- max over ranks
+    if world > 1:
+        t = torch.tensor([ms_step, e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step, e2e_ms = float(t[0]), float(t[1])
+
+    # ---- algorithmic work of this batch (read after timing)
+    counts = bufs.counts.cpu().numpy().astype(np.int64)
+    c = int(bufs.c_dev.item())
+    kept = np.minimum(counts, c)
+    R = int(kept.sum())
+    loc = bufs.loc.cpu().numpy()
+    t1 = int(((loc < c).any(0)).sum())  # tokens with at least one kept route
+    b = 2
+    ffn_flops = 4.0 * R * w.m * w.h
+    bytes_ = {
+        "gate": w.s * w.m * b + 4 * w.m * w.e + 8 * w.s * w.k,
+        "encode": t1 * w.m * b + R * w.m * b + 8 * w.s * w.k,
+        "decode": R * w.m * b + w.s * w.m * b + 12 * w.s * w.k,
+    }
+    pk = peaks()
+    stages = {}
+    for n in stage_names:
+        d = {"ms": stage_ms[n]}
+        if n in bytes_:
+            gbs = bytes_[n] / (stage_ms[n] * 1e-3) / 1e9
+            d.update(gbs=gbs, hbm_frac=gbs / pk["hbm"])
+        if n == "expert_ffn":
+            tf = ffn_flops / (stage_ms[n] * 1e-3) / 1e12
+            d.update(tflops=tf, tc_frac=tf / pk["bf16"])
+        stages[n] = d
+    ffn_tf = ffn_flops / (stage_ms["expert_ffn"] * 1e-3) / 1e12
+    clocks = clk.summary(t_wall0, t_wall1)
+
+    res = {
+        "metric": METRIC,
+        "value": world * w.s / (ms_step * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded counter-based normal draws; no dataset)",
+        "config": {"workload": w.name, "s": w.s, "m": w.m, "e": w.e, "k": w.k, "h": w.h,
+                   "act": w.act, "capacity_factor": w.capacity_factor, "c": c, "kept_routes": R,
+                   "l2": "flushed (256 MiB write) before every timed step, outside the interval",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"kernel": "expert_ffn (tcgen05 grouped GEMM, fc1+fc2)", "bound": "tensor",
+                     "achieved": ffn_tf, "peak": pk["bf16"], "unit": "TFLOP/s",
+                     "frac": ffn_tf / pk["bf16"], "peak_source": f"{pk['src']} bf16 burst",
+                     "traffic": None},
+        "stages": stages,
+        "e2e": {"value": world * w.s / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": w.s * w.m * 2, "d2h_bytes_per_step": w.s * w.m * 2,
+                "ms_per_step": e2e_ms},
+        "clocks": clocks,
+        "gpu_launches": launches,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline_dict(w, inp, args.cpu_seconds)
+    return res
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is a bounded token sample."""
+    import oracle
+
+    w = WORKLOAD
+    inp = synth.make_inputs_host(w)
+    _, s2, dt0, thr = time_oracle(w, inp, max(0.2, 60.0 / max(1, args.steps)))
+    ws, sub = oracle_sample_inputs(w, inp, s2)
+    for _ in range(min(args.warmup, 1)):
+        oracle.layer_forward(ws, sub)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.layer_forward(ws, sub)
+    dt = (time.perf_counter() - t) / args.steps
+    v = s2 / dt
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded counter-based normal draws; no dataset)",
+        "config": {"workload": w.name, "s": w.s, "m": w.m, "e": w.e, "k": w.k, "h": w.h,
+                   "act": w.act, "capacity_factor": w.capacity_factor},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                         "sample": f"each step: the CPU oracle's forward chain on the first {s2} "
+                                   f"tokens of the batch"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+    if world > 1:
+        import torch
+
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch
+
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -29,6 +29,11 @@ moe_status decode_bwd_launch(const void *dy, const void *out, moe_dtype dt, cons
                              const int32_t *c_dev, int64_t s, int m, int e, int k, int64_t c_max,
                              unsigned flags, void *d_out, float *d_gates, int32_t *st,
                              cudaStream_t stream);
+bool ffn_tc_supported(int e, int64_t c_max, int m, int h);
+moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *c_dev,
+                         const void *w1, const void *b1, const void *w3, const void *w2,
+                         const void *b2, moe_act act, int e, int64_t c_max, int m, int h,
+                         void *hid, void *out, int32_t *st, cudaStream_t stream);
 moe_status ffn_simt_launch(const void *buf, moe_dtype dt, const int32_t *counts,
                            const int32_t *c_dev, const void *w1, const void *b1, const void *w3,
                            const void *w2, const void *b2, moe_act act, int e, int64_t c_max,
@@ -147,6 +152,11 @@ moe_status moe_expert_ffn(const void *buf, moe_dtype dt, const int32_t *counts,
         return MOE_ERR_INVALID_ARG;
     if (act == MOE_ACT_SWIGLU && (!ok16(w3) || b1 != nullptr || b2 != nullptr))
         return MOE_ERR_INVALID_ARG;
+    if (dt == MOE_BF16) {
+        if (!ffn_tc_supported(e, c_max, m, h)) return MOE_ERR_UNSUPPORTED;
+        return ffn_tc_launch(buf, counts, c_dev, w1, b1, w3, w2, b2, act, e, c_max, m, h,
+                             workspace, out, dev_status, as_stream(stream));
+    }
     return ffn_simt_launch(buf, dt, counts, c_dev, w1, b1, w3, w2, b2, act, e, c_max, m, h,
                            workspace, out, dev_status, as_stream(stream));
 }

@@ -1,4 +1,4 @@
-// Expert FFN on the SIMT cores (fp32 layers).
+// Expert FFN on the SIMT cores (fp32 layers only).
 //
 // Method: the Tutel profile's experts {'type': 'ffn', hidden_size_per_expert,
 // has_fc1_bias, has_fc2_bias} and the DeepSpeed-MoE vs Tutel blog, section 3.5
@@ -126,11 +126,9 @@ moe_status ffn_simt_launch(const void *buf, moe_dtype dt, const int32_t *counts,
                            const int32_t *c_dev, const void *w1, const void *b1, const void *w3,
                            const void *w2, const void *b2, moe_act act, int e, int64_t c_max,
                            int m, int h, void *hid, void *out, int32_t *st, cudaStream_t stream) {
-    if (dt == MOE_F32)
-        return run<float>(buf, counts, c_dev, w1, b1, w3, w2, b2, act, e, c_max, m, h, hid, out, st,
-                          stream);
-    return run<__nv_bfloat16>(buf, counts, c_dev, w1, b1, w3, w2, b2, act, e, c_max, m, h, hid, out,
-                              st, stream);
+    if (dt != MOE_F32) return MOE_ERR_UNSUPPORTED;  // bf16 layers run on the tensor cores
+    return run<float>(buf, counts, c_dev, w1, b1, w3, w2, b2, act, e, c_max, m, h, hid, out, st,
+                      stream);
 }
 
 }  // namespace moe

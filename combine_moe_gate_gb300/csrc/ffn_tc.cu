@@ -1,0 +1,514 @@
+// Expert FFN on the 5th-generation tensor cores (bf16 layers).
+//
+// Method: the Tutel profile's experts {'type': 'ffn', hidden_size_per_expert,
+// has_fc1_bias, has_fc2_bias} and the DeepSpeed-MoE vs Tutel blog, section 3.5
+// (experts run as one batched matmul over the (E, C, D) expert buffer, whose
+// shape does not depend on the routing).  Here that batched matmul is a
+// grouped GEMM over experts j, restricted on the device to the first
+// min(counts[j], c) rows of expert j: no host synchronisation is needed to
+// learn the ragged row counts.
+//
+//   fc1:  hid[j] = act(buf[j] W1[j]^T + b1[j])        (SwiGLU: silu(buf W1^T) * (buf W3^T))
+//   fc2:  out[j] = hid[j] W2[j]^T + b2[j]
+//
+// One persistent kernel per GEMM, one CTA per SM (~200 KB shared memory):
+//   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per stage, 128-byte
+//               swizzle, 4-stage ring guarded by full/empty mbarriers;
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators);
+//               one lane issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32,
+//               M=128 N=256 K=16) and tcgen05.commit to release stages and to
+//               publish a finished accumulator;
+//   warps 2-9   epilogue: tcgen05.ld 32 lanes x 32 columns, bias + activation in
+//               fp32, one rounding to bf16, 16-byte stores of the valid rows.
+// The epilogue of tile i overlaps the main loop of tile i+1 (double-buffered
+// accumulator).  Every wait is bounded: after ~1 s a role sets
+// MOE_ERR_TIMEOUT, raises a CTA-wide abort flag and leaves its loop; the CTA
+// then drains its outstanding copies and MMAs (bounded) and frees TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;                 // UMMA M (rows of A per tile)
+constexpr int BN = 256;                 // UMMA N (rows of B per tile)
+constexpr int BK = 64;                  // bf16 elements per 128-byte swizzle span
+constexpr int UK = 16;                  // K of one tcgen05.mma kind::f16
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;    // 16 KiB
+constexpr int B_BYTES = BN * BK * 2;    // 32 KiB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + EPI_WARPS * 32;
+constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
+constexpr int MAX_E = 1024;
+constexpr unsigned long long WAIT_NS = 1000000000ull;  // 1 s per wait
+
+enum Epi { EPI_GELU = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_BIAS = 3 };
+
+// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major,
+// N >> 3 at bit 17, M >> 4 at bit 24.
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                           ((uint32_t)(BM >> 4) << 24);
+
+struct Ctl {  // control block in shared memory
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int32_t abort;
+    int32_t total_tiles;
+    int32_t tile_start[MAX_E + 1];
+};
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctl);
+
+struct GemmArgs {
+    const int32_t *counts;
+    const int32_t *c_dev;
+    int32_t *status;
+    const __nv_bfloat16 *bias;  // [e, n_out] or nullptr
+    __nv_bfloat16 *out;         // [e, c_max, n_out]
+    int64_t c_max;
+    int e;
+    int K;             // contraction length
+    int n_out;         // output columns per expert
+    int b_rows;        // rows of each B tensor map per expert
+};
+
+// ------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t su32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ unsigned long long gtimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(su32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with `parity` to complete.  Returns false if the
+// CTA is aborting or the wait ran past WAIT_NS (then the abort is raised).
+__device__ __noinline__ bool mbar_wait(uint64_t *b, uint32_t parity, Ctl *ctl, int32_t *status) {
+    if (mbar_try(b, parity)) return true;
+    unsigned long long t0 = gtimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try(b, parity)) return true;
+        if ((it & 31u) == 0) {
+            if (*(volatile int32_t *)&ctl->abort) return false;
+            if (gtimer() - t0 > WAIT_NS) {
+                *(volatile int32_t *)&ctl->abort = 1;
+                set_status(status, MOE_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(su32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
+// layout TMA writes: 8-row x 128-byte atoms, atoms 1024 bytes apart (SBO);
+// the leading-byte offset is unused for this layout; bits 46-48 = 0b001;
+// swizzle mode 2 (128 B) in bits 61-63.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(IDESC), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            su32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float gelu_erf(float a) {
+    return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f));
+}
+__device__ __forceinline__ float silu(float a) { return a / (1.0f + expf(-a)); }
+
+// Tile t -> (expert j, m-tile, n-tile); m-tile varies fastest.
+struct Tile { int j, mt, nt, rows; };
+
+__device__ __forceinline__ Tile decode_tile(const Ctl *ctl, int e, int t, int ntn,
+                                            const int32_t *kept_rows) {
+    int lo = 0, hi = e;  // largest j with tile_start[j] <= t
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (ctl->tile_start[mid] <= t) lo = mid; else hi = mid;
+    }
+    Tile T;
+    T.j = lo;
+    int local = t - ctl->tile_start[lo];
+    T.rows = kept_rows[lo];
+    int mtiles = (T.rows + BM - 1) / BM;
+    T.nt = local / mtiles;
+    T.mt = local % mtiles;
+    return T;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmB3, const GemmArgs args) {
+    __shared__ int32_t s_bad;
+    if (threadIdx.x == 0) s_bad = status_bad(args.status) ? 1 : 0;
+    __syncthreads();
+    if (s_bad) return;  // uniform across the CTA: nothing allocated yet
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * A_BYTES;
+    Ctl *ctl = (Ctl *)(smem + STAGES * STAGE_BYTES);
+    __shared__ int32_t kept_rows[MAX_E];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = args.e;
+    constexpr int NOUT_TILE = EPI == EPI_SWIGLU ? BN / 2 : BN;  // output columns per tile
+    const int ntn = (args.n_out + NOUT_TILE - 1) / NOUT_TILE;
+    const int nk = (args.K + BK - 1) / BK;
+
+    // ---- setup: per-expert row counts and tile prefix (warp 0), barriers,
+    // TMEM allocation (warp 1)
+    if (warp == 0) {
+        const int c_eff = (int)min((int64_t)*args.c_dev, args.c_max);
+        int run = 0;
+        for (int base = 0; base < e; base += 32) {
+            int j = base + lane;
+            int rows = j < e ? min(max(args.counts[j], 0), c_eff) : 0;
+            if (j < e) kept_rows[j] = rows;
+            int v = ((rows + BM - 1) / BM) * ntn;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (j < e) ctl->tile_start[j] = run + v - ((rows + BM - 1) / BM) * ntn;
+            run += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) {
+            ctl->tile_start[e] = run;
+            ctl->total_tiles = run;
+            ctl->abort = 0;
+            for (int s = 0; s < STAGES; s++) { mbar_init(&ctl->full[s], 1); mbar_init(&ctl->empty[s], 1); }
+            for (int a = 0; a < 2; a++) { mbar_init(&ctl->tfull[a], 1); mbar_init(&ctl->tempty[a], EPI_WARPS); }
+            mbar_init(&ctl->drain, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+    } else if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         su32(&ctl->tmem_base)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    const int total = ctl->total_tiles;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------- TMA producer
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            Tile T = decode_tile(ctl, e, t, ntn, kept_rows);
+            const int a_row = (int)((int64_t)T.j * args.c_max + (int64_t)T.mt * BM);
+            const int b_row = T.j * args.b_rows + T.nt * (EPI == EPI_SWIGLU ? BN / 2 : BN);
+            for (int kb = 0; kb < nk; kb++) {
+                if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, ctl, args.status)) goto producer_done;
+                mbar_expect_tx(&ctl->full[stage], STAGE_BYTES);
+                tma_load_2d(sA + stage * A_BYTES, &tmA, kb * BK, a_row, &ctl->full[stage]);
+                if (EPI == EPI_SWIGLU) {
+                    tma_load_2d(sB + stage * B_BYTES, &tmB, kb * BK, b_row, &ctl->full[stage]);
+                    tma_load_2d(sB + stage * B_BYTES + B_BYTES / 2, &tmB3, kb * BK, b_row,
+                                &ctl->full[stage]);
+                } else {
+                    tma_load_2d(sB + stage * B_BYTES, &tmB, kb * BK, b_row, &ctl->full[stage]);
+                }
+                issued++;
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+    producer_done:
+        // wait (bounded) for the copies still in flight before the CTA can exit
+        for (int i = max(0, issued - STAGES); i < issued; i++) {
+            int s = i % STAGES;
+            uint32_t ph = (uint32_t)((i / STAGES) & 1);
+            unsigned long long t0 = gtimer();
+            while (!mbar_try(&ctl->full[s], ph) && gtimer() - t0 < WAIT_NS) {
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            if (!mbar_wait(&ctl->tempty[acc], acc_phase ^ 1u, ctl, args.status)) break;
+            tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(acc * BN);
+            bool ok = true;
+            for (int kb = 0; kb < nk; kb++) {
+                if (!mbar_wait(&ctl->full[stage], phase, ctl, args.status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t a0 = su32(sA + stage * A_BYTES);
+                const uint32_t b0 = su32(sB + stage * B_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < BK / UK; kk++)
+                    umma(d, sdesc(a0 + kk * UK * 2), sdesc(b0 + kk * UK * 2), (kb | kk) != 0);
+                umma_commit(&ctl->empty[stage]);  // stage reusable once these MMAs read it
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            umma_commit(&ctl->tfull[acc]);  // accumulator ready when all MMAs finish
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        // all MMAs issued by this thread complete before TMEM is released
+        umma_commit(&ctl->drain);
+        unsigned long long t0 = gtimer();
+        while (!mbar_try(&ctl->drain, 0) && gtimer() - t0 < WAIT_NS) {
+        }
+    } else if (warp >= 2) {
+        // ------------------------------------------------------------- epilogue
+        const int ew = warp - 2;
+        const int sub = warp & 3;             // TMEM lane quarter this warp may access
+        const int half = ew >> 2;             // which half of the tile's columns
+        const int row_in_tile = sub * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            Tile T = decode_tile(ctl, e, t, ntn, kept_rows);
+            if (!mbar_wait(&ctl->tfull[acc], acc_phase, ctl, args.status)) break;
+            tc_fence_after();
+            const int row = T.mt * BM + row_in_tile;
+            const bool valid = row < T.rows;
+            __nv_bfloat16 *orow =
+                args.out + ((int64_t)T.j * args.c_max + row) * (int64_t)args.n_out;
+            const __nv_bfloat16 *brow = args.bias ? args.bias + (int64_t)T.j * args.n_out : nullptr;
+            const uint32_t tbase = tmem + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * BN);
+            constexpr int COLS = NOUT_TILE / 2;   // output columns per epilogue warp
+#pragma unroll 1
+            for (int c0 = 0; c0 < COLS; c0 += 32) {
+                const int ocol = half * COLS + c0;            // column within the tile's output
+                const int gcol = T.nt * NOUT_TILE + ocol;     // column within the expert
+                float v[32];
+                uint32_t r[32];
+                tmem_ld32(tbase + (uint32_t)ocol, r);
+                tmem_wait_ld();
+                if (EPI == EPI_SWIGLU) {
+                    uint32_t u[32];
+                    tmem_ld32(tbase + (uint32_t)(BN / 2 + ocol), u);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; i++)
+                        v[i] = silu(__uint_as_float(r[i])) * __uint_as_float(u[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; i++) {
+                        float a = __uint_as_float(r[i]);
+                        if (brow) {
+                            int cc = min(gcol + i, args.n_out - 1);
+                            a += __bfloat162float(brow[cc]);
+                        }
+                        if (EPI == EPI_GELU) a = gelu_erf(a);
+                        else if (EPI == EPI_RELU) a = fmaxf(a, 0.0f);
+                        v[i] = a;
+                    }
+                }
+                if (valid) {
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        if (gcol + q * 8 < args.n_out) {
+                            V16 pk = Elt<__nv_bfloat16>::pack(v + q * 8);
+                            st_v16(orow + gcol + q * 8, pk);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->tempty[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box box_rows x 64.
+bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = v > 0 ? v : 148;
+    }
+    return cached[dev];
+}
+
+template <int EPI>
+moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &b3,
+                       const GemmArgs &args, cudaStream_t stream) {
+    auto kern = tc_group_gemm<EPI>;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)SMEM_BYTES) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    constexpr int NOUT_TILE = EPI == EPI_SWIGLU ? BN / 2 : BN;
+    int64_t ntn = (args.n_out + NOUT_TILE - 1) / NOUT_TILE;
+    int64_t upper = (int64_t)args.e * ((args.c_max + BM - 1) / BM) * ntn;
+    int64_t grid = upper < sm_count() ? upper : sm_count();
+    if (grid < 1) grid = 1;
+    kern<<<(unsigned)grid, NUM_THREADS, SMEM_BYTES, stream>>>(a, b, b3, args);
+    note_launch();
+    return launch_status();
+}
+
+}  // namespace
+
+bool ffn_tc_supported(int e, int64_t c_max, int m, int h) {
+    return e >= 1 && e <= MAX_E && (int64_t)e * c_max < ((int64_t)1 << 31) &&
+           (int64_t)e * h * 2 < ((int64_t)1 << 31) && (int64_t)e * m < ((int64_t)1 << 31) &&
+           m % 8 == 0 && h % 8 == 0;
+}
+
+moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *c_dev,
+                         const void *w1, const void *b1, const void *w3, const void *w2,
+                         const void *b2, moe_act act, int e, int64_t c_max, int m, int h,
+                         void *hid, void *out, int32_t *st, cudaStream_t stream) {
+    CUtensorMap mA1, mB1, mB3, mA2, mB2;
+    const bool swiglu = act == MOE_ACT_SWIGLU;
+    const uint32_t b1_box = swiglu ? BN / 2 : BN;
+    if (!make_map(&mA1, buf, (uint64_t)e * c_max, (uint64_t)m, BM) ||
+        !make_map(&mB1, w1, (uint64_t)e * h, (uint64_t)m, b1_box) ||
+        !make_map(&mB3, swiglu ? w3 : w1, (uint64_t)e * h, (uint64_t)m, b1_box) ||
+        !make_map(&mA2, hid, (uint64_t)e * c_max, (uint64_t)h, BM) ||
+        !make_map(&mB2, w2, (uint64_t)e * m, (uint64_t)h, BN))
+        return MOE_ERR_CUDA;
+    GemmArgs g1{counts, c_dev, st, (const __nv_bfloat16 *)b1, (__nv_bfloat16 *)hid, c_max, e, m, h, h};
+    moe_status r;
+    if (swiglu) r = launch_gemm<EPI_SWIGLU>(mA1, mB1, mB3, g1, stream);
+    else if (act == MOE_ACT_GELU) r = launch_gemm<EPI_GELU>(mA1, mB1, mB1, g1, stream);
+    else r = launch_gemm<EPI_RELU>(mA1, mB1, mB1, g1, stream);
+    if (r != MOE_OK) return r;
+    GemmArgs g2{counts, c_dev, st, (const __nv_bfloat16 *)b2, (__nv_bfloat16 *)out, c_max, e, h, m, m};
+    return launch_gemm<EPI_BIAS>(mA2, mB2, mB2, g2, stream);
+}
+
+}  // namespace moe

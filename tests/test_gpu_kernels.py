@@ -238,6 +238,8 @@ FFN_CASES = [
     _w(s=333, m=128, e=4, k=2, h=256, act="gelu", capacity_factor=1.25),
     _w(s=300, m=192, e=8, k=2, h=320, act="swiglu", capacity_factor=0.0, skew_alpha=1.0),
     _w(s=200, m=256, e=5, k=1, h=512, act="relu", capacity_factor=-2.0, skew_alpha=1.5),
+    _w(s=600, m=200, e=3, k=2, h=136, act="gelu", capacity_factor=0.0),
+    _w(s=900, m=64, e=6, k=3, h=1024, act="swiglu", capacity_factor=1.5, skew_alpha=0.7),
 ]
 
 
