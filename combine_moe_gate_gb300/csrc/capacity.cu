@@ -34,12 +34,17 @@ cap_hist_kernel(const int32_t *__restrict__ idx, int64_t n, int e, int32_t *__re
     for (int j = threadIdx.x; j < e; j += CAP_NT) h[j] = 0;
     __syncthreads();
     const int64_t base = (int64_t)blockIdx.x * CAP_CH;
-    for (int q = threadIdx.x; q < CAP_CH; q += CAP_NT) {
-        int64_t j = base + q;
-        if (j >= n) break;
-        int v = idx[j];
-        if ((unsigned)v < (unsigned)e) atomicAdd(&h[v], 1);
-        else set_status(status, MOE_ERR_INVALID_ARG);
+    constexpr int PER = CAP_CH / CAP_NT;
+    int v[PER];
+#pragma unroll
+    for (int i = 0; i < PER; i++) {  // all loads in flight before any atomic
+        int64_t j = base + threadIdx.x + (int64_t)i * CAP_NT;
+        v[i] = j < n ? __ldg(idx + j) : -2;
+    }
+#pragma unroll
+    for (int i = 0; i < PER; i++) {
+        if ((unsigned)v[i] < (unsigned)e) atomicAdd(&h[v[i]], 1);
+        else if (v[i] != -2) set_status(status, MOE_ERR_INVALID_ARG);
     }
     __syncthreads();
     for (int j = threadIdx.x; j < e; j += CAP_NT) hist[(int64_t)blockIdx.x * e + j] = h[j];
@@ -87,17 +92,20 @@ cap_assign_kernel(const int32_t *__restrict__ idx, int64_t n, int e, int nblk,
     int32_t val[CAP_ROUNDS];
     const unsigned lt = (1u << lane) - 1u;
 #pragma unroll
-    for (int rd = 0; rd < CAP_ROUNDS; rd++) {
+    for (int rd = 0; rd < CAP_ROUNDS; rd++) {  // all loads in flight first
         int64_t j = seg0 + rd * 32 + lane;
-        int v = j < n ? idx[j] : -1;
-        if ((unsigned)v >= (unsigned)e) v = -1;
+        int v = j < n ? __ldg(idx + j) : -1;
+        val[rd] = (unsigned)v < (unsigned)e ? v : -1;
+    }
+#pragma unroll
+    for (int rd = 0; rd < CAP_ROUNDS; rd++) {
+        const int v = val[rd];
         unsigned peers = __match_any_sync(0xffffffffu, v);
         int prev = v >= 0 ? wcnt[warp * e + v] : 0;
         __syncwarp();
         if (v >= 0 && (peers & lt) == 0) wcnt[warp * e + v] = prev + __popc(peers);
         __syncwarp();
         rank[rd] = prev + __popc(peers & lt);
-        val[rd] = v;
     }
     __syncthreads();
     // exclusive prefix over warps, seeded with the chunk's base offset

@@ -187,8 +187,29 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr));
 }
 
-__device__ __forceinline__ void tmem_wait_ld() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+// Wait for this thread's outstanding tcgen05.ld.  The registers of a load are
+// tied to the wait so that no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.wait::ld.sync.aligned;"
+        : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+          "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+          "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+          "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+          "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+        :
+        : "memory");
+}
+
+// Ties further registers to an already completed wait (emits nothing).
+__device__ __forceinline__ void tmem_tie(uint32_t (&r)[32]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                   "+r"(r[30]), "+r"(r[31]));
 }
 
 __device__ __forceinline__ float gelu_erf(float a) {
@@ -361,40 +382,59 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             const __nv_bfloat16 *brow = args.bias ? args.bias + (int64_t)T.j * args.n_out : nullptr;
             const uint32_t tbase = tmem + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * BN);
             constexpr int COLS = NOUT_TILE / 2;   // output columns per epilogue warp
+            if (EPI == EPI_SWIGLU) {
 #pragma unroll 1
-            for (int c0 = 0; c0 < COLS; c0 += 32) {
-                const int ocol = half * COLS + c0;            // column within the tile's output
-                const int gcol = T.nt * NOUT_TILE + ocol;     // column within the expert
-                float v[32];
-                uint32_t r[32];
-                tmem_ld32(tbase + (uint32_t)ocol, r);
-                tmem_wait_ld();
-                if (EPI == EPI_SWIGLU) {
-                    uint32_t u[32];
+                for (int c0 = 0; c0 < COLS; c0 += 32) {
+                    const int ocol = half * COLS + c0;        // column within the tile's output
+                    const int gcol = T.nt * NOUT_TILE + ocol; // column within the expert
+                    uint32_t r[32], u[32];
+                    tmem_ld32(tbase + (uint32_t)ocol, r);
                     tmem_ld32(tbase + (uint32_t)(BN / 2 + ocol), u);
-                    tmem_wait_ld();
+                    tmem_wait_ld(r);
+                    tmem_tie(u);
+                    float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; i++)
                         v[i] = silu(__uint_as_float(r[i])) * __uint_as_float(u[i]);
-                } else {
+                    if (valid) {
 #pragma unroll
-                    for (int i = 0; i < 32; i++) {
-                        float a = __uint_as_float(r[i]);
-                        if (brow) {
-                            int cc = min(gcol + i, args.n_out - 1);
-                            a += __bfloat162float(brow[cc]);
-                        }
-                        if (EPI == EPI_GELU) a = gelu_erf(a);
-                        else if (EPI == EPI_RELU) a = fmaxf(a, 0.0f);
-                        v[i] = a;
+                        for (int q = 0; q < 4; q++)
+                            if (gcol + q * 8 < args.n_out)
+                                st_v16(orow + gcol + q * 8, Elt<__nv_bfloat16>::pack(v + q * 8));
                     }
                 }
-                if (valid) {
+            } else {
+#pragma unroll 1
+                for (int c0 = 0; c0 < COLS; c0 += 64) {
+                    uint32_t r[2][32];
+                    tmem_ld32(tbase + (uint32_t)(half * COLS + c0), r[0]);
+                    tmem_ld32(tbase + (uint32_t)(half * COLS + c0 + 32), r[1]);
+                    tmem_wait_ld(r[0]);
+                    tmem_tie(r[1]);
 #pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        if (gcol + q * 8 < args.n_out) {
-                            V16 pk = Elt<__nv_bfloat16>::pack(v + q * 8);
-                            st_v16(orow + gcol + q * 8, pk);
+                    for (int h2 = 0; h2 < 2; h2++) {
+                        const int gcol = T.nt * NOUT_TILE + half * COLS + c0 + 32 * h2;
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            const int g8 = gcol + q * 8;
+                            float v[8];
+                            float bsum[8];
+                            if (brow && g8 < args.n_out) {
+                                V16 bv = *reinterpret_cast<const V16 *>(brow + g8);
+                                Elt<__nv_bfloat16>::unpack(bv, bsum);
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 8; i++) bsum[i] = 0.0f;
+                            }
+#pragma unroll
+                            for (int i = 0; i < 8; i++) {
+                                float a = __uint_as_float(r[h2][q * 8 + i]) + bsum[i];
+                                if (EPI == EPI_GELU) a = gelu_erf(a);
+                                else if (EPI == EPI_RELU) a = fmaxf(a, 0.0f);
+                                v[i] = a;
+                            }
+                            if (valid && g8 < args.n_out)
+                                st_v16(orow + g8, Elt<__nv_bfloat16>::pack(v));
                         }
                     }
                 }

@@ -16,8 +16,6 @@
 namespace moe {
 namespace {
 
-constexpr int KT = 32;  // features per shared-memory tile
-
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool valid) {
     unsigned s = (unsigned)__cvta_generic_to_shared(smem);
     int n = valid ? 16 : 0;
@@ -33,7 +31,8 @@ __device__ __forceinline__ void cp_async4(void *smem, const void *gmem, bool val
 }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // N consecutive floats from shared memory; 16-byte loads when N % 4 == 0
 // (callers pass 16-byte aligned addresses in that case).
@@ -51,8 +50,10 @@ __device__ __forceinline__ void lds_vec(float *dst, const float *src) {
     }
 }
 
-template <int EP_, int TE_, int TT_, int NT_, typename XT>
+template <int EP_, int TE_, int TT_, int NT_, int KT_, int ST_, typename XT>
 struct GateCfg {
+    static constexpr int KT = KT_;               // features per shared-memory tile
+    static constexpr int STAGES = ST_;           // cp.async pipeline depth
     static constexpr int EP = EP_;               // experts per CTA (e padded)
     static constexpr int TE = TE_;               // experts per thread
     static constexpr int TT = TT_;               // tokens per thread
@@ -65,14 +66,14 @@ struct GateCfg {
     static constexpr int XROW = KT * Elt<XT>::BYTES + 16;  // padded raw row (bytes)
     static constexpr int XFS = TOKC + 4;         // fp32 x tile row stride (floats)
     static constexpr int LGS = EP + 1;           // logits tile row stride
-    // shared memory (bytes): raw x double buffer, fp32 x tile, Wg double buffer
-    static constexpr int RAW_BYTES = 2 * TOKC * XROW;
+    // shared memory (bytes): raw x ring, fp32 x tile, Wg ring
+    static constexpr int RAW_BYTES = STAGES * TOKC * XROW;
     static constexpr int XF_BYTES = KT * XFS * 4;
-    static constexpr int WS_BYTES = 2 * KT * EP * 4;
+    static constexpr int WS_BYTES = STAGES * KT * EP * 4;
     static constexpr int MAIN_BYTES = RAW_BYTES + XF_BYTES + WS_BYTES;
     static constexpr int LG_BYTES = TOKC * LGS * 4;
     static constexpr int SMEM = MAIN_BYTES > LG_BYTES ? MAIN_BYTES : LG_BYTES;
-    static_assert(EP % TE == 0 && NT % EX == 0 && TE % 4 == 0, "layout");
+    static_assert(EP % TE == 0 && NT % EX == 0 && TE % 4 == 0 && STAGES >= 2, "layout");
 };
 
 template <class C, typename XT>
@@ -89,6 +90,7 @@ __device__ __forceinline__ void load_tile(unsigned char *raw, float *ws, const X
         cp_async16(raw + row * C::XROW + ch * 16, src, ok);
     }
     // Wg: KT rows x EP columns (zero beyond m rows / e columns)
+    constexpr int KT = C::KT;
     if (wg16) {
         for (int q = tid; q < KT * (C::EP / 4); q += C::NT) {
             int kk = q / (C::EP / 4), j = (q % (C::EP / 4)) * 4;
@@ -114,9 +116,9 @@ gate_topk_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
                  int32_t *__restrict__ idx, float *__restrict__ gates, int32_t *status) {
     if (status_bad(status)) return;
     extern __shared__ __align__(16) unsigned char smem[];
-    unsigned char *raw = smem;                                   // [2][TOKC][XROW]
+    unsigned char *raw = smem;                                   // [STAGES][TOKC][XROW]
     float *xf = (float *)(smem + C::RAW_BYTES);                  // [KT][XFS]
-    float *ws = (float *)(smem + C::RAW_BYTES + C::XF_BYTES);    // [2][KT][EP]
+    float *ws = (float *)(smem + C::RAW_BYTES + C::XF_BYTES);    // [STAGES][KT][EP]
 
     const int tid = threadIdx.x;
     const int tx = tid % C::EX, ty = tid / C::EX;
@@ -129,15 +131,29 @@ gate_topk_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
 #pragma unroll
         for (int i = 0; i < C::TE; i++) acc[j][i] = 0.0f;
 
+    constexpr int KT = C::KT, ST = C::STAGES;
     const int ntiles = (m + KT - 1) / KT;
-    load_tile<C, XT>(raw, ws, x, wg, s, m, e, t0, 0, wg16);
+    // prologue: tiles 0 .. ST-2 in flight (one commit group per tile, empty groups past the end)
+#pragma unroll
+    for (int p = 0; p < ST - 1; p++) {
+        if (p < ntiles)
+            load_tile<C, XT>(raw + p * C::TOKC * C::XROW, ws + p * KT * C::EP, x, wg, s, m, e, t0,
+                             p * KT, wg16);
+        else
+            cp_async_commit();
+    }
     for (int it = 0; it < ntiles; it++) {
-        const int cur = it & 1;
-        cp_async_wait0();
-        __syncthreads();  // tile `it` landed; everyone finished reading xf of tile it-1
-        if (it + 1 < ntiles)
-            load_tile<C, XT>(raw + (cur ^ 1) * C::TOKC * C::XROW, ws + (cur ^ 1) * KT * C::EP, x,
-                             wg, s, m, e, t0, (it + 1) * KT, wg16);
+        const int cur = it % ST;
+        cp_async_wait<ST - 2>();
+        __syncthreads();  // tile `it` landed; everyone finished reading tile it-1 and xf
+        {
+            const int nx = it + ST - 1, nb = nx % ST;
+            if (nx < ntiles)
+                load_tile<C, XT>(raw + nb * C::TOKC * C::XROW, ws + nb * KT * C::EP, x, wg, s, m, e,
+                                 t0, nx * KT, wg16);
+            else
+                cp_async_commit();
+        }
         // widen the raw x tile to fp32, transposed to [feature][token]
         const unsigned char *rc = raw + cur * C::TOKC * C::XROW;
         for (int q = tid; q < C::TOKC * C::XCH; q += C::NT) {
@@ -174,6 +190,7 @@ gate_topk_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
             }
         }
     }
+    cp_async_wait<0>();
     __syncthreads();  // all reads of the tiles done before the logits overwrite them
 
     float *lg = (float *)smem;  // [TOKC][LGS]
@@ -272,17 +289,19 @@ template <typename XT>
 moe_status gate_dispatch(const void *x, const float *wg, const float *bias, int64_t s, int m, int e,
                          int k, int normalize, int32_t *idx, float *gates, int32_t *st,
                          cudaStream_t stream) {
-#define MOE_GATE_CASE(EPV, TEV, TTV, NTV)                                                   \
+#define MOE_GATE_CASE(EPV, TEV, TTV, NTV, KTV, STV)                                        \
     if (e <= EPV)                                                                           \
-        return launch_cfg<GateCfg<EPV, TEV, TTV, NTV, XT>, XT>(x, wg, bias, s, m, e, k,     \
-                                                               normalize, idx, gates, st, stream);
-    MOE_GATE_CASE(4, 4, 1, 64)
-    MOE_GATE_CASE(8, 8, 1, 64)
-    MOE_GATE_CASE(16, 8, 2, 128)
-    MOE_GATE_CASE(32, 8, 4, 128)
-    MOE_GATE_CASE(64, 8, 8, 128)
-    MOE_GATE_CASE(128, 8, 8, 256)
-    MOE_GATE_CASE(256, 8, 8, 256)
+        return launch_cfg<GateCfg<EPV, TEV, TTV, NTV, KTV, STV, XT>, XT>(                   \
+            x, wg, bias, s, m, e, k, normalize, idx, gates, st, stream);
+    // small e: HBM/latency bound -> few tokens per CTA, long tiles, deep pipeline;
+    // large e: fp32-FMA bound -> register-blocked 8x8 micro-tiles
+    MOE_GATE_CASE(4, 4, 1, 32, 128, 4)
+    MOE_GATE_CASE(8, 8, 1, 32, 128, 4)
+    MOE_GATE_CASE(16, 8, 1, 64, 128, 4)
+    MOE_GATE_CASE(32, 8, 2, 64, 64, 4)
+    MOE_GATE_CASE(64, 8, 8, 128, 32, 3)
+    MOE_GATE_CASE(128, 8, 8, 256, 32, 2)
+    MOE_GATE_CASE(256, 8, 8, 256, 32, 2)
 #undef MOE_GATE_CASE
     return MOE_ERR_UNSUPPORTED;
 }
