@@ -205,64 +205,111 @@ gate_topk_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
         }
     __syncthreads();
 
-    // softmax + top-k: one warp per token
-    constexpr int NW = C::NT / 32;
-    constexpr int QE = (C::EP + 31) / 32;  // experts per lane
-    const int lane = tid & 31, warp = tid >> 5;
-    for (int tl = warp; tl < C::TOKC; tl += NW) {
-        const int64_t t = t0 + tl;
-        if (t >= s) break;
-        float v[QE];
-        float mx = -INFINITY;
+    if constexpr (C::EP <= 32) {
+        // softmax + top-k, one thread per token: the token's <= 32 logits are read
+        // from the tile; selection scans experts in ascending index with a strict
+        // comparison, so equal logits go to the lower index.
+        for (int tl = tid; tl < C::TOKC; tl += C::NT) {
+            const int64_t t = t0 + tl;
+            if (t >= s) break;
+            float v[C::EP];
+            float mx = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < QE; q++) {
-            int ex = lane + 32 * q;
-            v[q] = ex < e ? lg[tl * C::LGS + ex] : -INFINITY;
-            mx = fmaxf(mx, v[q]);
+            for (int q = 0; q < C::EP; q++) {
+                v[q] = q < e ? lg[tl * C::LGS + q] : -INFINITY;
+                mx = fmaxf(mx, v[q]);
+            }
+            float z = 0.0f;
+#pragma unroll
+            for (int q = 0; q < C::EP; q++)
+                if (q < e) z += expf(v[q] - mx);
+            unsigned taken = 0;
+            float psel = 0.0f;
+            float pr[C::EP];
+#pragma unroll
+            for (int r = 0; r < C::EP; r++) {
+                if (r >= k) break;
+                float bv = -INFINITY;
+                int bj = 0;
+                bool found = false;
+#pragma unroll
+                for (int q = 0; q < C::EP; q++) {
+                    bool cand = q < e && !((taken >> q) & 1u);
+                    if (cand && (!found || v[q] > bv)) { bv = v[q]; bj = q; found = true; }
+                }
+                taken |= 1u << bj;
+                pr[r] = expf(bv - mx);
+                psel += pr[r];
+                idx[(int64_t)r * s + t] = bj;
+            }
+            const float den = normalize ? psel : z;
+#pragma unroll
+            for (int r = 0; r < C::EP; r++) {
+                if (r >= k) break;
+                gates[(int64_t)r * s + t] = pr[r] / den;
+            }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        float z = 0.0f;
-#pragma unroll
-        for (int q = 0; q < QE; q++)
-            if (lane + 32 * q < e) z += expf(v[q] - mx);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-
-        unsigned taken = 0;  // bit q: expert lane+32q already selected
-        float my_v = 0.0f;   // lane r keeps route r's logit and expert
-        int my_j = 0;
-        for (int r = 0; r < k; r++) {
-            float bv = -INFINITY;
-            int bj = 0x7fffffff;
+        return;
+    } else {
+        // softmax + top-k: one warp per token
+        constexpr int NW = C::NT / 32;
+        constexpr int QE = (C::EP + 31) / 32;  // experts per lane
+        const int lane = tid & 31, warp = tid >> 5;
+        for (int tl = warp; tl < C::TOKC; tl += NW) {
+            const int64_t t = t0 + tl;
+            if (t >= s) break;
+            float v[QE];
+            float mx = -INFINITY;
 #pragma unroll
             for (int q = 0; q < QE; q++) {
                 int ex = lane + 32 * q;
-                bool cand = ex < e && !((taken >> q) & 1u);
-                if (cand && (v[q] > bv || (v[q] == bv && ex < bj))) { bv = v[q]; bj = ex; }
+                v[q] = ex < e ? lg[tl * C::LGS + ex] : -INFINITY;
+                mx = fmaxf(mx, v[q]);
             }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                int oj = __shfl_xor_sync(0xffffffffu, bj, o);
-                if (ov > bv || (ov == bv && oj < bj)) { bv = ov; bj = oj; }
-            }
-            if ((bj & 31) == lane) taken |= 1u << (bj >> 5);
-            if (lane == r) { my_v = bv; my_j = bj; }
-        }
-        float p = lane < k ? expf(my_v - mx) : 0.0f;
-        float g;
-        if (normalize) {
-            float sel = p;
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            float z = 0.0f;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) sel += __shfl_xor_sync(0xffffffffu, sel, o);
-            g = p / sel;
-        } else {
-            g = p / z;
-        }
-        if (lane < k) {
-            idx[(int64_t)lane * s + t] = my_j;
-            gates[(int64_t)lane * s + t] = g;
+            for (int q = 0; q < QE; q++)
+                if (lane + 32 * q < e) z += expf(v[q] - mx);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+
+            unsigned taken = 0;  // bit q: expert lane+32q already selected
+            float my_v = 0.0f;   // lane r keeps route r's logit and expert
+            int my_j = 0;
+            for (int r = 0; r < k; r++) {
+                float bv = -INFINITY;
+                int bj = 0x7fffffff;
+#pragma unroll
+                for (int q = 0; q < QE; q++) {
+                    int ex = lane + 32 * q;
+                    bool cand = ex < e && !((taken >> q) & 1u);
+                    if (cand && (v[q] > bv || (v[q] == bv && ex < bj))) { bv = v[q]; bj = ex; }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                    int oj = __shfl_xor_sync(0xffffffffu, bj, o);
+                    if (ov > bv || (ov == bv && oj < bj)) { bv = ov; bj = oj; }
+                }
+                if ((bj & 31) == lane) taken |= 1u << (bj >> 5);
+                if (lane == r) { my_v = bv; my_j = bj; }
+            }
+            float p = lane < k ? expf(my_v - mx) : 0.0f;
+            float g;
+            if (normalize) {
+                float sel = p;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) sel += __shfl_xor_sync(0xffffffffu, sel, o);
+                g = p / sel;
+            } else {
+                g = p / z;
+            }
+            if (lane < k) {
+                idx[(int64_t)lane * s + t] = my_j;
+                gates[(int64_t)lane * s + t] = g;
+            }
         }
     }
 }
@@ -295,10 +342,10 @@ moe_status gate_dispatch(const void *x, const float *wg, const float *bias, int6
             x, wg, bias, s, m, e, k, normalize, idx, gates, st, stream);
     // small e: HBM/latency bound -> few tokens per CTA, long tiles, deep pipeline;
     // large e: fp32-FMA bound -> register-blocked 8x8 micro-tiles
-    MOE_GATE_CASE(4, 4, 1, 32, 128, 4)
-    MOE_GATE_CASE(8, 8, 1, 32, 128, 4)
-    MOE_GATE_CASE(16, 8, 1, 64, 128, 4)
-    MOE_GATE_CASE(32, 8, 2, 64, 64, 4)
+    MOE_GATE_CASE(4, 4, 1, 64, 128, 4)
+    MOE_GATE_CASE(8, 4, 1, 64, 128, 4)
+    MOE_GATE_CASE(16, 4, 1, 128, 128, 3)
+    MOE_GATE_CASE(32, 8, 1, 128, 64, 4)
     MOE_GATE_CASE(64, 8, 8, 128, 32, 3)
     MOE_GATE_CASE(128, 8, 8, 256, 32, 2)
     MOE_GATE_CASE(256, 8, 8, 256, 32, 2)
