@@ -29,6 +29,7 @@ constexpr int CAP_ROUNDS = CAP_SEG / 32;
 __global__ void __launch_bounds__(CAP_NT)
 cap_hist_kernel(const int32_t *__restrict__ idx, int64_t n, int e, int32_t *__restrict__ hist,
                 int32_t *status) {
+    pdl_enter();
     if (status_bad(status)) return;
     extern __shared__ int32_t h[];
     for (int j = threadIdx.x; j < e; j += CAP_NT) h[j] = 0;
@@ -57,6 +58,7 @@ cap_assign_kernel(const int32_t *__restrict__ idx, int64_t n, int e, int nblk,
                   const int32_t *__restrict__ hist, int c_fixed, int c_cap, int64_t c_max,
                   int32_t *__restrict__ loc, int32_t *__restrict__ counts,
                   int32_t *__restrict__ c_dev, int32_t *status) {
+    pdl_enter();
     if (status_bad(status)) return;
     extern __shared__ int32_t sm[];
     int32_t *wcnt = sm;                 // [NW][e]: per-warp counts, then per-warp offsets
@@ -163,19 +165,17 @@ moe_status capacity_launch(const int32_t *idx, int64_t s, int e, int k, float f,
         c_cap = (int)c;
     }
     int32_t *hist = (int32_t *)ws;
-    cap_hist_kernel<<<(unsigned)nblk, CAP_NT, e * sizeof(int32_t), stream>>>(idx, n, e, hist, st);
-    note_launch();
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (launch_pdl(cap_hist_kernel, dim3((unsigned)nblk), dim3(CAP_NT), e * sizeof(int32_t), stream,
+                   idx, n, e, hist, st) != MOE_OK)
+        return MOE_ERR_CUDA;
     size_t smem = (size_t)(CAP_NW + 1) * e * sizeof(int32_t);
     auto kern = cap_assign_kernel;
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
         return MOE_ERR_CUDA;
-    kern<<<(unsigned)nblk, CAP_NT, smem, stream>>>(idx, n, e, (int)nblk, hist, c_fixed, c_cap, c_max,
-                                                   loc, counts, c_dev, st);
-    note_launch();
-    return launch_status();
+    return launch_pdl(kern, dim3((unsigned)nblk), dim3(CAP_NT), smem, stream, idx, n, e, (int)nblk,
+                      hist, c_fixed, c_cap, c_max, loc, counts, c_dev, st);
 }
 
 }  // namespace moe

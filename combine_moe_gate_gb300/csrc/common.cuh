@@ -19,6 +19,39 @@ inline moe_status launch_status() {
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// Launch with programmatic dependent launch allowed: the kernel may be
+// scheduled while its predecessor in the stream drains; it must call
+// pdl_enter() before touching anything the predecessor writes.
+template <typename... KArgs, typename... Args>
+moe_status launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t err = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+    note_launch();
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+// Wait until the previous kernel in the stream has completed and its writes
+// are visible (no-op when launched without programmatic serialization), then
+// let the next kernel start its own launch early.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------ device status
 
 // First error wins; later errors are dropped.

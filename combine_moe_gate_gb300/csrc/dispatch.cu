@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(DNT)
 encode_kernel(const T *__restrict__ x, const int32_t *__restrict__ idx,
               const int32_t *__restrict__ loc, const int32_t *__restrict__ c_dev, int64_t s,
               int m, int e, int k, int64_t c_max, T *__restrict__ buf, int32_t *status) {
+    pdl_enter();
     if (status_bad(status)) return;
     const int c_eff = read_c(c_dev, c_max);
     const int lane = threadIdx.x & 31;
@@ -92,6 +93,7 @@ template <typename T>
 __global__ void __launch_bounds__(DNT)
 zero_fill_kernel(const int32_t *__restrict__ counts, const int32_t *__restrict__ c_dev, int e,
                  int64_t c_max, int m, T *__restrict__ buf, int32_t *status) {
+    pdl_enter();
     if (status_bad(status)) return;
     const int c_eff = read_c(c_dev, c_max);
     const int j = blockIdx.y;
@@ -115,6 +117,7 @@ combine_kernel(const T *__restrict__ src, const int32_t *__restrict__ idx,
                const int32_t *__restrict__ loc, const float *__restrict__ gates,
                const int32_t *__restrict__ c_dev, int64_t s, int m, int e, int k, int64_t c_max,
                T *__restrict__ y, int32_t *status) {
+    pdl_enter();
     if (status_bad(status)) return;
     constexpr int VEC = Elt<T>::VEC;
     const int c_eff = read_c(c_dev, c_max);
@@ -198,6 +201,7 @@ decode_bwd_kernel(const T *__restrict__ dy, const T *__restrict__ out,
                   const float *__restrict__ gates, const int32_t *__restrict__ c_dev, int64_t s,
                   int m, int e, int k, int64_t c_max, T *__restrict__ d_out,
                   float *__restrict__ d_gates, int32_t *status) {
+    pdl_enter();
     if (status_bad(status)) return;
     constexpr int VEC = Elt<T>::VEC;
     const int c_eff = read_c(c_dev, c_max);
@@ -259,25 +263,25 @@ moe_status encode_launch(const void *x, moe_dtype dt, const int32_t *idx, const 
                          int k, int64_t c_max, unsigned flags, void *buf, int32_t *st,
                          cudaStream_t stream) {
     const int grid = grid_for_tokens(s);
+    moe_status r;
     if (dt == MOE_BF16)
-        encode_kernel<__nv_bfloat16><<<grid, DNT, 0, stream>>>(
-            (const __nv_bfloat16 *)x, idx, loc, c_dev, s, m, e, k, c_max, (__nv_bfloat16 *)buf, st);
+        r = launch_pdl(encode_kernel<__nv_bfloat16>, dim3(grid), dim3(DNT), 0, stream,
+                       (const __nv_bfloat16 *)x, idx, loc, c_dev, s, m, e, k, c_max,
+                       (__nv_bfloat16 *)buf, st);
     else
-        encode_kernel<float><<<grid, DNT, 0, stream>>>((const float *)x, idx, loc, c_dev, s, m, e, k,
-                                                       c_max, (float *)buf, st);
-    note_launch();
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+        r = launch_pdl(encode_kernel<float>, dim3(grid), dim3(DNT), 0, stream, (const float *)x, idx,
+                       loc, c_dev, s, m, e, k, c_max, (float *)buf, st);
+    if (r != MOE_OK) return r;
     if (flags & MOE_FLAG_ZERO_FILL) {
         int64_t gx = (c_max + (DNT / 32) - 1) / (DNT / 32);
         dim3 g((unsigned)(gx < 1024 ? gx : 1024), (unsigned)e);
         if (dt == MOE_BF16)
-            zero_fill_kernel<__nv_bfloat16><<<g, DNT, 0, stream>>>(counts, c_dev, e, c_max, m,
-                                                                  (__nv_bfloat16 *)buf, st);
+            r = launch_pdl(zero_fill_kernel<__nv_bfloat16>, g, dim3(DNT), 0, stream, counts, c_dev, e,
+                           c_max, m, (__nv_bfloat16 *)buf, st);
         else
-            zero_fill_kernel<float><<<g, DNT, 0, stream>>>(counts, c_dev, e, c_max, m, (float *)buf,
-                                                          st);
-        note_launch();
-        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+            r = launch_pdl(zero_fill_kernel<float>, g, dim3(DNT), 0, stream, counts, c_dev, e, c_max,
+                           m, (float *)buf, st);
+        if (r != MOE_OK) return r;
     }
     return MOE_OK;
 }
@@ -287,19 +291,18 @@ moe_status combine_launch(const void *src, moe_dtype dt, const int32_t *idx, con
                           int64_t c_max, void *y, int32_t *st, cudaStream_t stream) {
     const int grid = grid_for_tokens(s);
     const bool w = gates != nullptr;
+    const dim3 g(grid), b(DNT);
+    const float *gp = gates;
     if (dt == MOE_BF16) {
         auto *sp = (const __nv_bfloat16 *)src;
         auto *yp = (__nv_bfloat16 *)y;
-        if (w) combine_kernel<__nv_bfloat16, true><<<grid, DNT, 0, stream>>>(sp, idx, loc, gates, c_dev, s, m, e, k, c_max, yp, st);
-        else combine_kernel<__nv_bfloat16, false><<<grid, DNT, 0, stream>>>(sp, idx, loc, nullptr, c_dev, s, m, e, k, c_max, yp, st);
-    } else {
-        auto *sp = (const float *)src;
-        auto *yp = (float *)y;
-        if (w) combine_kernel<float, true><<<grid, DNT, 0, stream>>>(sp, idx, loc, gates, c_dev, s, m, e, k, c_max, yp, st);
-        else combine_kernel<float, false><<<grid, DNT, 0, stream>>>(sp, idx, loc, nullptr, c_dev, s, m, e, k, c_max, yp, st);
+        if (w) return launch_pdl(combine_kernel<__nv_bfloat16, true>, g, b, 0, stream, sp, idx, loc, gp, c_dev, s, m, e, k, c_max, yp, st);
+        return launch_pdl(combine_kernel<__nv_bfloat16, false>, g, b, 0, stream, sp, idx, loc, gp, c_dev, s, m, e, k, c_max, yp, st);
     }
-    note_launch();
-    return launch_status();
+    auto *sp = (const float *)src;
+    auto *yp = (float *)y;
+    if (w) return launch_pdl(combine_kernel<float, true>, g, b, 0, stream, sp, idx, loc, gp, c_dev, s, m, e, k, c_max, yp, st);
+    return launch_pdl(combine_kernel<float, false>, g, b, 0, stream, sp, idx, loc, gp, c_dev, s, m, e, k, c_max, yp, st);
 }
 
 moe_status decode_bwd_launch(const void *dy, const void *out, moe_dtype dt, const int32_t *idx,
@@ -310,26 +313,23 @@ moe_status decode_bwd_launch(const void *dy, const void *out, moe_dtype dt, cons
     if (flags & MOE_FLAG_ZERO_FILL) {
         int64_t gx = (c_max + (DNT / 32) - 1) / (DNT / 32);
         dim3 g((unsigned)(gx < 1024 ? gx : 1024), (unsigned)e);
+        moe_status r;
         if (dt == MOE_BF16)
-            zero_fill_kernel<__nv_bfloat16><<<g, DNT, 0, stream>>>(counts, c_dev, e, c_max, m,
-                                                                  (__nv_bfloat16 *)d_out, st);
+            r = launch_pdl(zero_fill_kernel<__nv_bfloat16>, g, dim3(DNT), 0, stream, counts, c_dev, e,
+                           c_max, m, (__nv_bfloat16 *)d_out, st);
         else
-            zero_fill_kernel<float><<<g, DNT, 0, stream>>>(counts, c_dev, e, c_max, m,
-                                                          (float *)d_out, st);
-        note_launch();
-        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+            r = launch_pdl(zero_fill_kernel<float>, g, dim3(DNT), 0, stream, counts, c_dev, e, c_max,
+                           m, (float *)d_out, st);
+        if (r != MOE_OK) return r;
     }
     const int grid = grid_for_tokens(s);
     if (dt == MOE_BF16)
-        decode_bwd_kernel<__nv_bfloat16><<<grid, DNT, 0, stream>>>(
-            (const __nv_bfloat16 *)dy, (const __nv_bfloat16 *)out, idx, loc, gates, c_dev, s, m, e,
-            k, c_max, (__nv_bfloat16 *)d_out, d_gates, st);
-    else
-        decode_bwd_kernel<float><<<grid, DNT, 0, stream>>>((const float *)dy, (const float *)out,
-                                                           idx, loc, gates, c_dev, s, m, e, k, c_max,
-                                                           (float *)d_out, d_gates, st);
-    note_launch();
-    return launch_status();
+        return launch_pdl(decode_bwd_kernel<__nv_bfloat16>, dim3(grid), dim3(DNT), 0, stream,
+                          (const __nv_bfloat16 *)dy, (const __nv_bfloat16 *)out, idx, loc, gates,
+                          c_dev, s, m, e, k, c_max, (__nv_bfloat16 *)d_out, d_gates, st);
+    return launch_pdl(decode_bwd_kernel<float>, dim3(grid), dim3(DNT), 0, stream, (const float *)dy,
+                      (const float *)out, idx, loc, gates, c_dev, s, m, e, k, c_max, (float *)d_out,
+                      d_gates, st);
 }
 
 }  // namespace moe

@@ -33,6 +33,7 @@ simt_group_gemm(const T *__restrict__ A, const T *__restrict__ B, const T *__res
                 const T *__restrict__ bias, const int32_t *__restrict__ counts,
                 const int32_t *__restrict__ c_dev, int64_t c_max, int N, int K, int act,
                 T *__restrict__ C, int32_t *status) {
+    pdl_enter();
     if (status_bad(status)) return;
     const int j = blockIdx.z;
     const int c_eff = (int)min((int64_t)*c_dev, c_max);
@@ -102,22 +103,21 @@ moe_status run(const void *buf, const int32_t *counts, const int32_t *c_dev, con
     int64_t gy = (c_max + BM - 1) / BM;
     if (gy > 65535 || e > 65535) return MOE_ERR_UNSUPPORTED;
     dim3 g1((h + BN - 1) / BN, (unsigned)gy, e);
+    const T *none = nullptr;
+    moe_status r;
     if (act == MOE_ACT_SWIGLU)
-        simt_group_gemm<T, EPI_SWIGLU><<<g1, SNT, 0, stream>>>(
-            (const T *)buf, (const T *)w1, (const T *)w3, nullptr, counts, c_dev, c_max, h, m, act,
-            (T *)hid, st);
+        r = launch_pdl(simt_group_gemm<T, EPI_SWIGLU>, g1, dim3(SNT), 0, stream, (const T *)buf,
+                       (const T *)w1, (const T *)w3, none, counts, c_dev, c_max, h, m, (int)act,
+                       (T *)hid, st);
     else
-        simt_group_gemm<T, EPI_ACT><<<g1, SNT, 0, stream>>>((const T *)buf, (const T *)w1, nullptr,
-                                                            (const T *)b1, counts, c_dev, c_max, h,
-                                                            m, act, (T *)hid, st);
-    note_launch();
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+        r = launch_pdl(simt_group_gemm<T, EPI_ACT>, g1, dim3(SNT), 0, stream, (const T *)buf,
+                       (const T *)w1, none, (const T *)b1, counts, c_dev, c_max, h, m, (int)act,
+                       (T *)hid, st);
+    if (r != MOE_OK) return r;
     dim3 g2((m + BN - 1) / BN, (unsigned)gy, e);
-    simt_group_gemm<T, EPI_OUT><<<g2, SNT, 0, stream>>>((const T *)hid, (const T *)w2, nullptr,
-                                                        (const T *)b2, counts, c_dev, c_max, m, h,
-                                                        act, (T *)out, st);
-    note_launch();
-    return launch_status();
+    return launch_pdl(simt_group_gemm<T, EPI_OUT>, g2, dim3(SNT), 0, stream, (const T *)hid,
+                      (const T *)w2, none, (const T *)b2, counts, c_dev, c_max, m, h, (int)act,
+                      (T *)out, st);
 }
 
 }  // namespace

@@ -212,8 +212,31 @@ __device__ __forceinline__ void tmem_tie(uint32_t (&r)[32]) {
                    "+r"(r[30]), "+r"(r[31]));
 }
 
+// erf(x) by Abramowitz & Stegun, Handbook of Mathematical Functions, formula
+// 7.1.28 (Hastings): erf(x) = 1 - (1 + a1 x + ... + a6 x^6)^-16 for x >= 0,
+// |error| <= 3e-7, odd extension for x < 0.  One reciprocal and no exponential,
+// which keeps the fc1 epilogue off the critical path; the error is three
+// orders of magnitude below the bf16 rounding that follows.
+__device__ __forceinline__ float erf_as7128(float x) {
+    const float ax = fabsf(x);
+    float p = fmaf(ax, 0.0000430638f, 0.0002765672f);
+    p = fmaf(ax, p, 0.0001520143f);
+    p = fmaf(ax, p, 0.0092705272f);
+    p = fmaf(ax, p, 0.0422820123f);
+    p = fmaf(ax, p, 0.0705230784f);
+    p = fmaf(ax, p, 1.0f);
+    float q = p * p;   // ^2
+    q = q * q;         // ^4
+    q = q * q;         // ^8
+    q = q * q;         // ^16 (overflows to inf for large x: erf -> 1)
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(q));
+    return copysignf(1.0f - r, x);
+}
+
+// GELU, exact erf form: a * Phi(a) = 0.5 a (1 + erf(a / sqrt 2)).
 __device__ __forceinline__ float gelu_erf(float a) {
-    return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f));
+    return 0.5f * a * (1.0f + erf_as7128(a * 0.70710678118654752f));
 }
 __device__ __forceinline__ float silu(float a) { return a / (1.0f + expf(-a)); }
 
@@ -242,6 +265,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmB3, const GemmArgs args) {
     __shared__ int32_t s_bad;
+    pdl_enter();
     if (threadIdx.x == 0) s_bad = status_bad(args.status) ? 1 : 0;
     __syncthreads();
     if (s_bad) return;  // uniform across the CTA: nothing allocated yet
@@ -515,9 +539,8 @@ moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtenso
     int64_t upper = (int64_t)args.e * ((args.c_max + BM - 1) / BM) * ntn;
     int64_t grid = upper < sm_count() ? upper : sm_count();
     if (grid < 1) grid = 1;
-    kern<<<(unsigned)grid, NUM_THREADS, SMEM_BYTES, stream>>>(a, b, b3, args);
-    note_launch();
-    return launch_status();
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(NUM_THREADS), SMEM_BYTES, stream, a, b, b3,
+                      args);
 }
 
 }  // namespace

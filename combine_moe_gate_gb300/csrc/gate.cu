@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(C::NT)
 gate_topk_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
                  const float *__restrict__ bias, int64_t s, int m, int e, int k, int normalize,
                  int32_t *__restrict__ idx, float *__restrict__ gates, int32_t *status) {
+    pdl_enter();
     if (status_bad(status)) return;
     extern __shared__ __align__(16) unsigned char smem[];
     unsigned char *raw = smem;                                   // [STAGES][TOKC][XROW]
@@ -326,10 +327,8 @@ moe_status launch_cfg(const void *x, const float *wg, const float *bias, int64_t
     }
     int64_t grid = (s + C::TOKC - 1) / C::TOKC;
     if (grid > 0x7fffffff) return MOE_ERR_UNSUPPORTED;
-    kern<<<(unsigned)grid, C::NT, C::SMEM, stream>>>((const XT *)x, wg, bias, s, m, e, k, normalize,
-                                                     idx, gates, st);
-    note_launch();
-    return launch_status();
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(C::NT), C::SMEM, stream, (const XT *)x, wg,
+                      bias, s, m, e, k, normalize, idx, gates, st);
 }
 
 template <typename XT>

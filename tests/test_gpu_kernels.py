@@ -309,3 +309,31 @@ def test_determinism_repeat_bitwise():
         outs.append((bits(bufs.y), bufs.idx.cpu().numpy(), bufs.loc.cpu().numpy()))
     for a, b in zip(*outs):
         assert np.array_equal(a, b)
+
+
+def test_ffn_gelu_epilogue_matches_exact_erf():
+    """Identity fc1/fc2 weights make out = bf16(GELU(x)) exactly, so the tensor-core
+    epilogue's GELU is compared with the oracle's exact double-precision erf form
+    on a dense sweep of bf16 inputs in [-6, 6]: every value within one bf16 step
+    and nearly all bit-identical."""
+    m = h = 64
+    xs = np.linspace(-6.0, 6.0, 64 * 256).astype(np.float32)
+    xb = synth.f32_to_bf16_bits(xs).reshape(256, 64)        # 256 rows of 64 values
+    rows = xb.shape[0]
+    eye = synth.f32_to_bf16_bits(np.eye(h, m, dtype=np.float32))[None]  # [1, h, m]
+    buf = xb[None]                                             # [1, rows, m]
+    counts = np.array([rows], np.int32)
+    ws = torch.empty(M.moe_expert_ffn_workspace_size(M.MOE_BF16, "gelu", 1, rows, m, h),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.empty((1, rows, m), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    M.moe_expert_ffn(to_dev(buf), to_dev(counts), to_dev(counts), to_dev(eye), None, None,
+                     to_dev(eye), None, "gelu", ws, out, st)
+    torch.cuda.synchronize()
+    status_ok(st)
+    got = to_host(out)[0]
+    want = oracle.ffn_rows(buf, eye, None, None, eye, None, "gelu", np.zeros(rows, np.int32),
+                           np.arange(rows), True)
+    ulp = np.maximum(np.abs(want), 2.0 ** -126) * 2.0 ** -7
+    assert np.all(np.abs(got - want) <= ulp * 1.01)
+    assert np.mean(got == want) > 0.995
