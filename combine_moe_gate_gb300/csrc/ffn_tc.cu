@@ -212,32 +212,35 @@ __device__ __forceinline__ void tmem_tie(uint32_t (&r)[32]) {
                    "+r"(r[30]), "+r"(r[31]));
 }
 
-// erf(x) by Abramowitz & Stegun, Handbook of Mathematical Functions, formula
-// 7.1.28 (Hastings): erf(x) = 1 - (1 + a1 x + ... + a6 x^6)^-16 for x >= 0,
-// |error| <= 3e-7, odd extension for x < 0.  One reciprocal and no exponential,
-// which keeps the fc1 epilogue off the critical path; the error is three
-// orders of magnitude below the bf16 rounding that follows.
-__device__ __forceinline__ float erf_as7128(float x) {
-    const float ax = fabsf(x);
-    float p = fmaf(ax, 0.0000430638f, 0.0002765672f);
-    p = fmaf(ax, p, 0.0001520143f);
-    p = fmaf(ax, p, 0.0092705272f);
-    p = fmaf(ax, p, 0.0422820123f);
-    p = fmaf(ax, p, 0.0705230784f);
-    p = fmaf(ax, p, 1.0f);
+// erfc(x) for x >= 0 by Abramowitz & Stegun, Handbook of Mathematical
+// Functions, formula 7.1.28 (Hastings): erf(x) = 1 - (1 + a1 x + ... + a6 x^6)^-16
+// with |error| <= 3e-7, so erfc(x) = (1 + a1 x + ... + a6 x^6)^-16.  One
+// reciprocal and no exponential, which keeps the fc1 epilogue cheap; the error
+// is three orders of magnitude below the bf16 rounding that follows.
+__device__ __forceinline__ float erfc_as7128(float x) {
+    float p = fmaf(x, 0.0000430638f, 0.0002765672f);
+    p = fmaf(x, p, 0.0001520143f);
+    p = fmaf(x, p, 0.0092705272f);
+    p = fmaf(x, p, 0.0422820123f);
+    p = fmaf(x, p, 0.0705230784f);
+    p = fmaf(x, p, 1.0f);
     float q = p * p;   // ^2
     q = q * q;         // ^4
     q = q * q;         // ^8
-    q = q * q;         // ^16 (overflows to inf for large x: erf -> 1)
+    q = q * q;         // ^16 (overflows to inf for large x: erfc -> 0)
     float r;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(q));
-    return copysignf(1.0f - r, x);
+    return r;
 }
 
-// GELU, exact erf form: a * Phi(a) = 0.5 a (1 + erf(a / sqrt 2)).
+// GELU, exact erf form: a * Phi(a) with Phi(a) = 0.5 (1 + erf(a / sqrt 2)),
+// evaluated as 1 - erfc/2 for a >= 0 and erfc(|a| / sqrt 2) / 2 for a < 0 so
+// that the negative tail does not cancel.  |GELU error| <= 5e-7.
 __device__ __forceinline__ float gelu_erf(float a) {
-    return 0.5f * a * (1.0f + erf_as7128(a * 0.70710678118654752f));
+    const float r = 0.5f * erfc_as7128(fabsf(a) * 0.70710678118654752f);
+    return a * (a >= 0.0f ? 1.0f - r : r);
 }
+
 __device__ __forceinline__ float silu(float a) { return a / (1.0f + expf(-a)); }
 
 // Tile t -> (expert j, m-tile, n-tile); m-tile varies fastest.
