@@ -29,6 +29,9 @@ moe_status decode_bwd_launch(const void *dy, const void *out, moe_dtype dt, cons
                              const int32_t *c_dev, int64_t s, int m, int e, int k, int64_t c_max,
                              unsigned flags, void *d_out, float *d_gates, int32_t *st,
                              cudaStream_t stream);
+moe_status capacity_noalloc_launch(const int32_t *idx, int64_t s, int e, int k, float f,
+                                   int64_t c_max, int32_t *loc, int32_t *counts, int32_t *c_dev,
+                                   int32_t *st, cudaStream_t stream);
 bool ffn_tc_supported(int e, int64_t c_max, int m, int h);
 moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *c_dev,
                          const void *w1, const void *b1, const void *w3, const void *w2,
@@ -115,6 +118,18 @@ moe_status moe_capacity_locations(const int32_t *idx, int64_t s, int e, int k,
         return MOE_ERR_INVALID_ARG;
     return capacity_launch(idx, s, e, k, capacity_factor, c_max, workspace, loc, counts, c_dev,
                            dev_status, as_stream(stream));
+}
+
+moe_status moe_capacity_locations_noalloc(const int32_t *idx, int64_t s, int e, int k,
+                                          float capacity_factor, int64_t c_max, int32_t *loc,
+                                          int32_t *counts, int32_t *c_dev, int32_t *dev_status,
+                                          void *stream) {
+    if (!routing_shape_ok(s, e, k) || c_max < 1 || c_max > 0x7fffffff ||
+        capacity_factor != capacity_factor || !ok4(idx) || !ok4(loc) || !ok4(counts) ||
+        !ok4(c_dev) || !ok4(dev_status))
+        return MOE_ERR_INVALID_ARG;
+    return capacity_noalloc_launch(idx, s, e, k, capacity_factor, c_max, loc, counts, c_dev,
+                                   dev_status, as_stream(stream));
 }
 
 moe_status moe_encode(const void *x, moe_dtype dt, const int32_t *idx, const int32_t *loc,

@@ -15,6 +15,8 @@
 //      __match_any_sync groups equal experts and popc of the lower lanes gives
 //      the rank), then adds the per-warp prefix.  CTA 0 also forms counts[],
 //      the capacity c and the overflow check.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -176,6 +178,52 @@ moe_status capacity_launch(const int32_t *idx, int64_t s, int e, int k, float f,
         return MOE_ERR_CUDA;
     return launch_pdl(kern, dim3((unsigned)nblk), dim3(CAP_NT), smem, stream, idx, n, e, (int)nblk,
                       hist, c_fixed, c_cap, c_max, loc, counts, c_dev, st);
+}
+
+// ------------------------------------------------------ no-allocation variant
+//
+// Scratch for moe_capacity_locations_noalloc: a fixed array in the library's
+// own device memory, so callers that cannot allocate device memory still get
+// the two-kernel capacity path.  Every GPU that loads the library holds these
+// 1 MiB until the process exits.  All calls share the array: calls whose
+// kernels overlap on the GPU (different streams, no ordering) race on it.
+// The histogram kernel writes every entry the assign kernel reads, so nothing
+// has to be cleared between calls.
+constexpr size_t NOALLOC_SCRATCH_BYTES = MOE_CAPACITY_NOALLOC_SCRATCH_BYTES;
+static_assert(NOALLOC_SCRATCH_BYTES % 256 == 0, "scratch size");
+static __device__ __align__(256) int32_t g_cap_scratch[NOALLOC_SCRATCH_BYTES / sizeof(int32_t)];
+
+namespace {
+
+// Device address of g_cap_scratch on the current device.  In host code the
+// symbol name is only a host-side stand-in, so the address is looked up once
+// per device with that device current and cached.
+int32_t *cap_scratch_on_current_device() {
+    static std::mutex mu;
+    static int32_t *addr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_cap_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        addr[dev] = static_cast<int32_t *>(p);
+    }
+    return addr[dev];
+}
+
+}  // namespace
+
+moe_status capacity_noalloc_launch(const int32_t *idx, int64_t s, int e, int k, float f,
+                                   int64_t c_max, int32_t *loc, int32_t *counts, int32_t *c_dev,
+                                   int32_t *st, cudaStream_t stream) {
+    if (capacity_workspace_bytes(s, e, k) > NOALLOC_SCRATCH_BYTES) return MOE_ERR_UNSUPPORTED;
+    int32_t *scratch = cap_scratch_on_current_device();
+    if (!scratch) return MOE_ERR_CUDA;
+    return capacity_launch(idx, s, e, k, f, c_max, scratch, loc, counts, c_dev, st, stream);
 }
 
 }  // namespace moe

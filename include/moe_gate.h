@@ -118,6 +118,33 @@ moe_status moe_capacity_locations(const int32_t *idx, int64_t s, int e, int k,
                                   int32_t *dev_status, void *stream);
 
 /*
+ * moe_capacity_locations without a workspace argument: the same results from
+ * the same kernels, with their scratch in a fixed array inside the library.
+ * The pages have no counterpart; this entry point exists for callers that
+ * cannot allocate device memory themselves -- for example a plugin running
+ * inside an inference engine that owns the device's whole memory pool, or a
+ * latency-critical path where cudaMalloc's implicit device synchronisation is
+ * not acceptable.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Scratch limit: MOE_CAPACITY_NOALLOC_SCRATCH_BYTES (1 MiB), held
+ *     on every GPU that loads the library until the process exits.  Shapes
+ *     whose moe_capacity_workspace_size() exceeds it return
+ *     MOE_ERR_UNSUPPORTED with nothing launched.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (different
+ *     streams without ordering between them) race and give wrong locations.
+ *     Calls ordered on one stream are safe; nothing needs clearing in between.
+ */
+moe_status moe_capacity_locations_noalloc(const int32_t *idx, int64_t s, int e, int k,
+                                          float capacity_factor, int64_t c_max, int32_t *loc,
+                                          int32_t *counts, int32_t *c_dev, int32_t *dev_status,
+                                          void *stream);
+
+/* Bytes of the fixed scratch array moe_capacity_locations_noalloc uses. */
+#define MOE_CAPACITY_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/*
  * Fast encode ([Blog] 3.5, kernel K1 forward; [PR8195] change 3).
  *   buf[idx[r,t], loc[r,t], :] = x[t, :] for every kept route (unweighted copy).
  *   With MOE_FLAG_ZERO_FILL, rows min(counts[j], c)..c-1 of every expert j are
