@@ -30,4 +30,4 @@ from .rng import (  # noqa: F401
     stream_key,
     uniform_host,
 )
-from .workloads import Workload, WORKLOADS, sweep_points, make_inputs_host  # noqa: F401
+from .workloads import Workload, WORKLOADS, sweep_points, make_inputs_host, make_inputs_device  # noqa: F401

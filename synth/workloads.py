@@ -144,3 +144,34 @@ def make_inputs_host(w: Workload, parts=("x", "wg", "bias", "w1", "w3", "w2", "b
     if "dy" in parts:
         out["dy"] = normal_host(sd, "dy", (w.s, w.m), 1.0, dt) if w.backward else None
     return out
+
+
+def make_inputs_device(w: Workload, device="cuda", weight_seed=None):
+    """The same recipe drawn with torch on `device` (for multi-GB workloads).
+
+    bf16 tensors come back as torch.bfloat16, fp32 as torch.float32.  Expert
+    weights use `weight_seed` when given (the sweep shares one weight set across
+    its points), otherwise the workload's seed.
+    """
+    import torch
+
+    from .rng import normal_torch
+
+    dt, sd = w.dtype, w.seed
+    wsd = sd if weight_seed is None else weight_seed
+    out = {
+        "x": normal_torch(sd, "x", (w.s, w.m), 1.0, dt, device),
+        "wg": normal_torch(sd, "wg", (w.m, w.e), 1.0 / math.sqrt(w.m), "f32", device),
+        "bias": None,
+        "w1": normal_torch(wsd, "w1", (w.e, w.h, w.m), 1.0 / math.sqrt(w.m), dt, device),
+        "w3": (normal_torch(wsd, "w3", (w.e, w.h, w.m), 1.0 / math.sqrt(w.m), dt, device)
+               if w.act == ACT_SWIGLU else None),
+        "w2": normal_torch(wsd, "w2", (w.e, w.m, w.h), 1.0 / math.sqrt(w.h), dt, device),
+        "b1": normal_torch(wsd, "b1", (w.e, w.h), 0.01, dt, device) if w.has_bias else None,
+        "b2": normal_torch(wsd, "b2", (w.e, w.m), 0.01, dt, device) if w.has_bias else None,
+        "dy": normal_torch(sd, "dy", (w.s, w.m), 1.0, dt, device) if w.backward else None,
+    }
+    b = gate_bias_host(w)
+    if b is not None:
+        out["bias"] = torch.from_numpy(b).to(device)
+    return out
