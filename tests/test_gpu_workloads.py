@@ -144,8 +144,10 @@ def run_and_check(w, weight_seed=None, n_ffn_experts=3, n_tokens=4, rng_seed=0):
     # decode alone, identity experts: decode the encoded buffer; the oracle's slot
     # rows are the host token rows they hold.  Bit-exact on sampled tokens (both
     # sides accumulate in fp32 in ascending route order).
+    # (the oracle's gates are fed to the GPU: both sides then multiply identical values)
     y2 = torch.empty((w.s, w.m), dtype=tdt, device="cuda")
-    M.moe_decode(bufs.buf, bufs.idx, bufs.loc, bufs.gates, bufs.c_dev, y2, bufs.status)
+    g_dev = torch.from_numpy(g_o).cuda()
+    M.moe_decode(bufs.buf, bufs.idx, bufs.loc, g_dev, bufs.c_dev, y2, bufs.status)
     torch.cuda.synchronize()
     status_ok(bufs.status)
     toks2 = rng.choice(w.s, size=min(64, w.s), replace=False)
@@ -202,7 +204,8 @@ def test_bf16_e16_forward_and_backward():
     d_out = torch.empty_like(out_in)
     d_g = torch.empty((w.k, w.s), dtype=torch.float32, device="cuda")
     dx = torch.empty((w.s, w.m), dtype=torch.bfloat16, device="cuda")
-    M.moe_decode_bwd(inp["dy"], out_in, bufs.idx, bufs.loc, bufs.gates, bufs.counts, bufs.c_dev,
+    g_dev = torch.from_numpy(res["g"]).cuda()    # oracle gates: identical products on both sides
+    M.moe_decode_bwd(inp["dy"], out_in, bufs.idx, bufs.loc, g_dev, bufs.counts, bufs.c_dev,
                      d_out, d_g, bufs.status)
     d_out_o, d_g_o = oracle.decode_bwd(dy_h, out_h, res["idx"], res["loc"], res["g"], c, True)
     # encode backward of the oracle's d_out (identity-expert chain: dx_t = kappa_t dy_t)
