@@ -128,6 +128,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# -------------------------------------------------------------- multi-rank
+def reduce_max(vals, device=None):
+    """Max over ranks of a list of floats (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in vals]
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_throughput(world, tokens_per_rank, ms_step):
+    """Whole-job tokens/s: every rank runs its own replica on its own tokens."""
+    return world * tokens_per_rank / (ms_step * 1e-3)
+
+
 # ------------------------------------------------------------------ oracle
 def oracle_sample_inputs(w, inp, s_sample):
     """The first s_sample tokens of the workload's batch (same weights)."""
@@ -293,10 +311,7 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms /= args.steps
 
     # ---- max over ranks
-    if world > 1:
-        t = torch.tensor([ms_step, e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step, e2e_ms = float(t[0]), float(t[1])
+    ms_step, e2e_ms = reduce_max([ms_step, e2e_ms], device=dev)
 
     # ---- algorithmic work of this batch (read after timing)
     counts = bufs.counts.cpu().numpy().astype(np.int64)
@@ -328,7 +343,7 @@ def run_ours(args, rank, world, local_rank):
 
     res = {
         "metric": METRIC,
-        "value": world * w.s / (ms_step * 1e-3),
+        "value": job_throughput(world, w.s, ms_step),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -349,7 +364,7 @@ def run_ours(args, rank, world, local_rank):
                      "frac": ffn_tf / pk["bf16"], "peak_source": f"{pk['src']} bf16 burst",
                      "traffic": None},
         "stages": stages,
-        "e2e": {"value": world * w.s / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_throughput(world, w.s, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": w.s * w.m * 2, "d2h_bytes_per_step": w.s * w.m * 2,
                 "ms_per_step": e2e_ms},
         "clocks": clocks,
