@@ -156,28 +156,53 @@ def oracle_sample_inputs(w, inp, s_sample):
 
 
 def time_oracle(w, inp, target_s):
-    """Time the CPU oracle's full forward chain on the first s' tokens, s' sized
-    so the run takes about target_s seconds.  Returns (tokens/s, s', seconds, threads)."""
+    """Time the CPU oracle's full forward chain on the first s' tokens of the
+    batch, s' sized so one pass takes about target_s seconds (at most the whole
+    batch); when the whole batch is faster than that, it is repeated until
+    target_s has passed.  Returns (tokens/s, s', passes, seconds, threads)."""
     import oracle
 
-    s1 = 16
+    s1 = min(w.s, 64)
     ws, sub = oracle_sample_inputs(w, inp, s1)
     t = time.perf_counter()
     oracle.layer_forward(ws, sub)
     dt = time.perf_counter() - t
     s2 = int(max(s1, min(w.s, s1 * target_s / max(dt, 1e-3))))
     ws, sub = oracle_sample_inputs(w, inp, s2)
-    t = time.perf_counter()
-    oracle.layer_forward(ws, sub)
-    dt = time.perf_counter() - t
-    return s2 / dt, s2, dt, oracle.get_threads()
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        oracle.layer_forward(ws, sub)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= target_s or s2 < w.s:
+            break
+    return passes * s2 / dt, s2, passes, dt, oracle.get_threads()
 
 
 def cpu_baseline_dict(w, inp, target_s):
-    v, s2, dt, thr = time_oracle(w, inp, target_s)
+    v, s2, passes, dt, thr = time_oracle(w, inp, target_s)
     return {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle",
             "sample": f"full forward chain (gate, capacity, encode, FFN, decode) on the first {s2} "
-                      f"tokens of the batch, same weights; {dt:.1f} s on {thr} threads"}
+                      f"of {w.s} tokens, same weights, {passes} pass(es): {dt:.1f} s on {thr} threads"}
+
+
+def ffn_traffic_from_profile():
+    """DRAM bytes per expert-FFN call from the committed ncu summary, or None when
+    the kernel source has changed since the counters were taken."""
+    import hashlib
+
+    prof = os.path.join(ROOT, "profiles", "expert_ffn_tcgen05_bf16_e8.md")
+    src = os.path.join(ROOT, "combine_moe_gate_gb300", "csrc", "ffn_tc.cu")
+    try:
+        text = open(prof).read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    fields = dict(line.split(":", 1) for line in text.splitlines() if line.startswith(
+        ("source_sha256_16:", "dram_bytes_per_call:")))
+    if fields.get("source_sha256_16", "").split()[0:1] != [digest]:
+        return None
+    return int(fields["dram_bytes_per_call"].split()[0])
 
 
 # ------------------------------------------------------------------- ours
@@ -362,7 +387,7 @@ def run_ours(args, rank, world, local_rank):
                                "stage-bracketed timed pass)", "bound": "tensor",
                      "achieved": ffn_tf, "peak": pk["bf16"], "unit": "TFLOP/s",
                      "frac": ffn_tf / pk["bf16"], "peak_source": f"{pk['src']} bf16 burst",
-                     "traffic": None},
+                     "traffic": ffn_traffic_from_profile(), "traffic_unit": "bytes per call"},
         "stages": stages,
         "e2e": {"value": job_throughput(world, w.s, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": w.s * w.m * 2, "d2h_bytes_per_step": w.s * w.m * 2,
@@ -381,7 +406,7 @@ def run_reference(args):
 
     w = WORKLOAD
     inp = synth.make_inputs_host(w)
-    _, s2, dt0, thr = time_oracle(w, inp, max(0.2, 60.0 / max(1, args.steps)))
+    _, s2, _, dt0, thr = time_oracle(w, inp, max(0.2, 60.0 / max(1, args.steps)))
     ws, sub = oracle_sample_inputs(w, inp, s2)
     for _ in range(min(args.warmup, 1)):
         oracle.layer_forward(ws, sub)
