@@ -12,16 +12,17 @@
 //   fc2:  out[j] = hid[j] W2[j]^T + b2[j]
 //
 // One persistent kernel per GEMM, one CTA per SM (~200 KB shared memory):
-//   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per stage, 128-byte
-//               swizzle, 4-stage ring guarded by full/empty mbarriers;
-//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators);
-//               one lane issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32,
-//               M=128 N=256 K=16) and tcgen05.commit to release stages and to
-//               publish a finished accumulator;
+//   warp 0      TMA producer: an A tile of 128 (or 256) x 64 and a 256x64 B tile
+//               per stage, 128-byte swizzle, a 4- (or 3-) stage ring guarded by
+//               full/empty mbarriers;
+//   warp 1      allocates all 512 TMEM columns; one lane issues tcgen05.mma
+//               (kind::f16, bf16 x bf16 -> fp32, M=128 N=256 K=16; two per K step
+//               for 256-row tiles, sharing the B tile) and tcgen05.commit to
+//               release stages and to publish a finished accumulator;
 //   warps 2-9   epilogue: tcgen05.ld 32 lanes x 32 columns, bias + activation in
 //               fp32, one rounding to bf16, 16-byte stores of the valid rows.
-// The epilogue of tile i overlaps the main loop of tile i+1 (double-buffered
-// accumulator).  Every wait is bounded: after ~1 s a role sets
+// With 128-row tiles the two 128x256 accumulators let the epilogue of tile i
+// overlap the main loop of tile i+1; 256-row tiles use both as one.  Every wait is bounded: after ~1 s a role sets
 // MOE_ERR_TIMEOUT, raises a CTA-wide abort flag and leaves its loop; the CTA
 // then drains its outstanding copies and MMAs (bounded) and frees TMEM.
 #include <cuda.h>
@@ -32,27 +33,39 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;                 // UMMA M (rows of A per tile)
+constexpr int UM = 128;                 // UMMA M (rows of one MMA)
 constexpr int BN = 256;                 // UMMA N (rows of B per tile)
 constexpr int BK = 64;                  // bf16 elements per 128-byte swizzle span
 constexpr int UK = 16;                  // K of one tcgen05.mma kind::f16
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;    // 16 KiB
 constexpr int B_BYTES = BN * BK * 2;    // 32 KiB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + EPI_WARPS * 32;
-constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
+constexpr uint32_t TMEM_COLS = 512;     // all of TMEM
 constexpr int MAX_E = 1024;
 constexpr unsigned long long WAIT_NS = 1000000000ull;  // 1 s per wait
 
 enum Epi { EPI_GELU = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_BIAS = 3 };
 
+// Tile shape.  TM = 1: 128 x 256 tiles, two 256-column accumulators in TMEM so
+// the epilogue of one tile overlaps the main loop of the next, 4 stages.
+// TM = 2: 256 x 256 tiles as two M=128 MMAs sharing every B tile (a third
+// fewer operand bytes per FLOP), one 512-column accumulator, 3 stages.
+template <int TM>
+struct Tiling {
+    static constexpr int BMT = UM * TM;                   // rows of A per tile
+    static constexpr int A_BYTES = BMT * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = TM == 1 ? 4 : 3;
+    static constexpr int NACC = TM == 1 ? 2 : 1;          // accumulator buffers
+    static constexpr int ACC_COLS = BN * TM;              // TMEM columns per buffer
+};
+
 // kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major,
 // N >> 3 at bit 17, M >> 4 at bit 24.
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                           ((uint32_t)(BM >> 4) << 24);
+                           ((uint32_t)(UM >> 4) << 24);
 
+template <int STAGES>
 struct Ctl {  // control block in shared memory
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
@@ -64,7 +77,12 @@ struct Ctl {  // control block in shared memory
     int32_t total_tiles;
     int32_t tile_start[MAX_E + 1];
 };
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctl);
+
+template <int TM>
+constexpr size_t smem_bytes() {
+    return 1024 + (size_t)Tiling<TM>::STAGES * Tiling<TM>::STAGE_BYTES +
+           sizeof(Ctl<Tiling<TM>::STAGES>);
+}
 
 struct GemmArgs {
     const int32_t *counts;
@@ -117,15 +135,16 @@ __device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
 
 // Bounded wait for the phase with `parity` to complete.  Returns false if the
 // CTA is aborting or the wait ran past WAIT_NS (then the abort is raised).
-__device__ __noinline__ bool mbar_wait(uint64_t *b, uint32_t parity, Ctl *ctl, int32_t *status) {
+__device__ __noinline__ bool mbar_wait(uint64_t *b, uint32_t parity, int32_t *abort_flag,
+                                       int32_t *status) {
     if (mbar_try(b, parity)) return true;
     unsigned long long t0 = gtimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try(b, parity)) return true;
         if ((it & 31u) == 0) {
-            if (*(volatile int32_t *)&ctl->abort) return false;
+            if (*(volatile int32_t *)abort_flag) return false;
             if (gtimer() - t0 > WAIT_NS) {
-                *(volatile int32_t *)&ctl->abort = 1;
+                *(volatile int32_t *)abort_flag = 1;
                 set_status(status, MOE_ERR_TIMEOUT);
                 return false;
             }
@@ -246,27 +265,29 @@ __device__ __forceinline__ float silu(float a) { return a / (1.0f + expf(-a)); }
 // Tile t -> (expert j, m-tile, n-tile); m-tile varies fastest.
 struct Tile { int j, mt, nt, rows; };
 
-__device__ __forceinline__ Tile decode_tile(const Ctl *ctl, int e, int t, int ntn,
+__device__ __forceinline__ Tile decode_tile(const int32_t *tile_start, int e, int t, int bmt,
                                             const int32_t *kept_rows) {
     int lo = 0, hi = e;  // largest j with tile_start[j] <= t
     while (hi - lo > 1) {
         int mid = (lo + hi) >> 1;
-        if (ctl->tile_start[mid] <= t) lo = mid; else hi = mid;
+        if (tile_start[mid] <= t) lo = mid; else hi = mid;
     }
     Tile T;
     T.j = lo;
-    int local = t - ctl->tile_start[lo];
+    int local = t - tile_start[lo];
     T.rows = kept_rows[lo];
-    int mtiles = (T.rows + BM - 1) / BM;
+    int mtiles = (T.rows + bmt - 1) / bmt;
     T.nt = local / mtiles;
     T.mt = local % mtiles;
     return T;
 }
 
-template <int EPI>
+template <int EPI, int TM>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmB3, const GemmArgs args) {
+    using TL = Tiling<TM>;
+    constexpr int STAGES = TL::STAGES, BMT = TL::BMT, A_BYTES = TL::A_BYTES;
     __shared__ int32_t s_bad;
     pdl_enter();
     if (threadIdx.x == 0) s_bad = status_bad(args.status) ? 1 : 0;
@@ -276,7 +297,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * A_BYTES;
-    Ctl *ctl = (Ctl *)(smem + STAGES * STAGE_BYTES);
+    Ctl<STAGES> *ctl = (Ctl<STAGES> *)(smem + STAGES * TL::STAGE_BYTES);
     __shared__ int32_t kept_rows[MAX_E];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -294,13 +315,14 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             int j = base + lane;
             int rows = j < e ? min(max(args.counts[j], 0), c_eff) : 0;
             if (j < e) kept_rows[j] = rows;
-            int v = ((rows + BM - 1) / BM) * ntn;
+            const int own = ((rows + BMT - 1) / BMT) * ntn;
+            int v = own;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 int u = __shfl_up_sync(0xffffffffu, v, o);
                 if (lane >= o) v += u;
             }
-            if (j < e) ctl->tile_start[j] = run + v - ((rows + BM - 1) / BM) * ntn;
+            if (j < e) ctl->tile_start[j] = run + v - own;
             run += __shfl_sync(0xffffffffu, v, 31);
         }
         if (lane == 0) {
@@ -324,6 +346,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     const int total = ctl->total_tiles;
+    int32_t *abort_flag = &ctl->abort;
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------- TMA producer
@@ -331,12 +354,13 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         uint32_t phase = 0;
         int issued = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            Tile T = decode_tile(ctl, e, t, ntn, kept_rows);
-            const int a_row = (int)((int64_t)T.j * args.c_max + (int64_t)T.mt * BM);
-            const int b_row = T.j * args.b_rows + T.nt * (EPI == EPI_SWIGLU ? BN / 2 : BN);
+            Tile T = decode_tile(ctl->tile_start, e, t, BMT, kept_rows);
+            const int a_row = (int)((int64_t)T.j * args.c_max + (int64_t)T.mt * BMT);
+            const int b_row = T.j * args.b_rows + T.nt * NOUT_TILE;
             for (int kb = 0; kb < nk; kb++) {
-                if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, ctl, args.status)) goto producer_done;
-                mbar_expect_tx(&ctl->full[stage], STAGE_BYTES);
+                if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag, args.status))
+                    goto producer_done;
+                mbar_expect_tx(&ctl->full[stage], TL::STAGE_BYTES);
                 tma_load_2d(sA + stage * A_BYTES, &tmA, kb * BK, a_row, &ctl->full[stage]);
                 if (EPI == EPI_SWIGLU) {
                     tma_load_2d(sB + stage * B_BYTES, &tmB, kb * BK, b_row, &ctl->full[stage]);
@@ -365,25 +389,27 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            if (!mbar_wait(&ctl->tempty[acc], acc_phase ^ 1u, ctl, args.status)) break;
+            if (!mbar_wait(&ctl->tempty[acc], acc_phase ^ 1u, abort_flag, args.status)) break;
             tc_fence_after();
-            const uint32_t d = tmem + (uint32_t)(acc * BN);
+            const uint32_t d = tmem + (uint32_t)(acc * TL::ACC_COLS);
             bool ok = true;
             for (int kb = 0; kb < nk; kb++) {
-                if (!mbar_wait(&ctl->full[stage], phase, ctl, args.status)) { ok = false; break; }
+                if (!mbar_wait(&ctl->full[stage], phase, abort_flag, args.status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t a0 = su32(sA + stage * A_BYTES);
                 const uint32_t b0 = su32(sB + stage * B_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < BK / UK; kk++)
-                    umma(d, sdesc(a0 + kk * UK * 2), sdesc(b0 + kk * UK * 2), (kb | kk) != 0);
+#pragma unroll
+                    for (int hm = 0; hm < TM; hm++)  // M halves share the B tile
+                        umma(d + (uint32_t)(hm * BN), sdesc(a0 + hm * UM * BK * 2 + kk * UK * 2),
+                             sdesc(b0 + kk * UK * 2), (kb | kk) != 0);
                 umma_commit(&ctl->empty[stage]);  // stage reusable once these MMAs read it
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
             if (!ok) break;
             umma_commit(&ctl->tfull[acc]);  // accumulator ready when all MMAs finish
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1u;
+            if (++acc == TL::NACC) { acc = 0; acc_phase ^= 1u; }
         }
         // all MMAs issued by this thread complete before TMEM is released
         umma_commit(&ctl->drain);
@@ -392,27 +418,31 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         }
     } else if (warp >= 2) {
         // ------------------------------------------------------------- epilogue
+        // TM = 1: warp (sub, half) owns rows sub*32.. and half of the columns.
+        // TM = 2: warp (sub, half) owns rows half*128 + sub*32.. and all columns.
         const int ew = warp - 2;
         const int sub = warp & 3;             // TMEM lane quarter this warp may access
-        const int half = ew >> 2;             // which half of the tile's columns
-        const int row_in_tile = sub * 32 + lane;
+        const int half = ew >> 2;
+        const int row_in_tile = (TM == 2 ? half * UM : 0) + sub * 32 + lane;
+        constexpr int COLS = TM == 2 ? NOUT_TILE : NOUT_TILE / 2;  // output columns per warp
+        const int col0 = TM == 2 ? 0 : half * COLS;                // first output column
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            Tile T = decode_tile(ctl, e, t, ntn, kept_rows);
-            if (!mbar_wait(&ctl->tfull[acc], acc_phase, ctl, args.status)) break;
+            Tile T = decode_tile(ctl->tile_start, e, t, BMT, kept_rows);
+            if (!mbar_wait(&ctl->tfull[acc], acc_phase, abort_flag, args.status)) break;
             tc_fence_after();
-            const int row = T.mt * BM + row_in_tile;
+            const int row = T.mt * BMT + row_in_tile;
             const bool valid = row < T.rows;
             __nv_bfloat16 *orow =
                 args.out + ((int64_t)T.j * args.c_max + row) * (int64_t)args.n_out;
             const __nv_bfloat16 *brow = args.bias ? args.bias + (int64_t)T.j * args.n_out : nullptr;
-            const uint32_t tbase = tmem + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * BN);
-            constexpr int COLS = NOUT_TILE / 2;   // output columns per epilogue warp
+            const uint32_t tbase = tmem + ((uint32_t)(sub * 32) << 16) +
+                                   (uint32_t)(acc * TL::ACC_COLS + (TM == 2 ? half * BN : 0));
             if (EPI == EPI_SWIGLU) {
 #pragma unroll 1
                 for (int c0 = 0; c0 < COLS; c0 += 32) {
-                    const int ocol = half * COLS + c0;        // column within the tile's output
+                    const int ocol = col0 + c0;               // column within the tile's output
                     const int gcol = T.nt * NOUT_TILE + ocol; // column within the expert
                     uint32_t r[32], u[32];
                     tmem_ld32(tbase + (uint32_t)ocol, r);
@@ -434,13 +464,13 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
 #pragma unroll 1
                 for (int c0 = 0; c0 < COLS; c0 += 64) {
                     uint32_t r[2][32];
-                    tmem_ld32(tbase + (uint32_t)(half * COLS + c0), r[0]);
-                    tmem_ld32(tbase + (uint32_t)(half * COLS + c0 + 32), r[1]);
+                    tmem_ld32(tbase + (uint32_t)(col0 + c0), r[0]);
+                    tmem_ld32(tbase + (uint32_t)(col0 + c0 + 32), r[1]);
                     tmem_wait_ld(r[0]);
                     tmem_tie(r[1]);
 #pragma unroll
                     for (int h2 = 0; h2 < 2; h2++) {
-                        const int gcol = T.nt * NOUT_TILE + half * COLS + c0 + 32 * h2;
+                        const int gcol = T.nt * NOUT_TILE + col0 + c0 + 32 * h2;
 #pragma unroll
                         for (int q = 0; q < 4; q++) {
                             const int g8 = gcol + q * 8;
@@ -469,8 +499,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->tempty[acc]);
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1u;
+            if (++acc == TL::NACC) { acc = 0; acc_phase ^= 1u; }
         }
     }
 
@@ -524,26 +553,27 @@ int sm_count() {
     return cached[dev];
 }
 
-template <int EPI>
+template <int EPI, int TM>
 moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &b3,
                        const GemmArgs &args, cudaStream_t stream) {
-    auto kern = tc_group_gemm<EPI>;
+    auto kern = tc_group_gemm<EPI, TM>;
+    constexpr size_t SMEM = smem_bytes<TM>();
     static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
     if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)SMEM_BYTES) != cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) !=
+            cudaSuccess)
             return MOE_ERR_CUDA;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
     constexpr int NOUT_TILE = EPI == EPI_SWIGLU ? BN / 2 : BN;
+    constexpr int BMT = Tiling<TM>::BMT;
     int64_t ntn = (args.n_out + NOUT_TILE - 1) / NOUT_TILE;
-    int64_t upper = (int64_t)args.e * ((args.c_max + BM - 1) / BM) * ntn;
+    int64_t upper = (int64_t)args.e * ((args.c_max + BMT - 1) / BMT) * ntn;
     int64_t grid = upper < sm_count() ? upper : sm_count();
     if (grid < 1) grid = 1;
-    return launch_pdl(kern, dim3((unsigned)grid), dim3(NUM_THREADS), SMEM_BYTES, stream, a, b, b3,
-                      args);
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(NUM_THREADS), SMEM, stream, a, b, b3, args);
 }
 
 }  // namespace
@@ -558,23 +588,26 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
                          const void *w1, const void *b1, const void *w3, const void *w2,
                          const void *b2, moe_act act, int e, int64_t c_max, int m, int h,
                          void *hid, void *out, int32_t *st, cudaStream_t stream) {
+    // fc1 keeps 128-row tiles (its activation epilogue overlaps the next tile's
+    // main loop); fc2 (bias-only epilogue, long K) uses 256-row tiles.
+    constexpr int TM1 = 1, TM2 = 2;
     CUtensorMap mA1, mB1, mB3, mA2, mB2;
     const bool swiglu = act == MOE_ACT_SWIGLU;
     const uint32_t b1_box = swiglu ? BN / 2 : BN;
-    if (!make_map(&mA1, buf, (uint64_t)e * c_max, (uint64_t)m, BM) ||
+    if (!make_map(&mA1, buf, (uint64_t)e * c_max, (uint64_t)m, Tiling<TM1>::BMT) ||
         !make_map(&mB1, w1, (uint64_t)e * h, (uint64_t)m, b1_box) ||
         !make_map(&mB3, swiglu ? w3 : w1, (uint64_t)e * h, (uint64_t)m, b1_box) ||
-        !make_map(&mA2, hid, (uint64_t)e * c_max, (uint64_t)h, BM) ||
+        !make_map(&mA2, hid, (uint64_t)e * c_max, (uint64_t)h, Tiling<TM2>::BMT) ||
         !make_map(&mB2, w2, (uint64_t)e * m, (uint64_t)h, BN))
         return MOE_ERR_CUDA;
     GemmArgs g1{counts, c_dev, st, (const __nv_bfloat16 *)b1, (__nv_bfloat16 *)hid, c_max, e, m, h, h};
     moe_status r;
-    if (swiglu) r = launch_gemm<EPI_SWIGLU>(mA1, mB1, mB3, g1, stream);
-    else if (act == MOE_ACT_GELU) r = launch_gemm<EPI_GELU>(mA1, mB1, mB1, g1, stream);
-    else r = launch_gemm<EPI_RELU>(mA1, mB1, mB1, g1, stream);
+    if (swiglu) r = launch_gemm<EPI_SWIGLU, TM1>(mA1, mB1, mB3, g1, stream);
+    else if (act == MOE_ACT_GELU) r = launch_gemm<EPI_GELU, TM1>(mA1, mB1, mB1, g1, stream);
+    else r = launch_gemm<EPI_RELU, TM1>(mA1, mB1, mB1, g1, stream);
     if (r != MOE_OK) return r;
     GemmArgs g2{counts, c_dev, st, (const __nv_bfloat16 *)b2, (__nv_bfloat16 *)out, c_max, e, h, m, m};
-    return launch_gemm<EPI_BIAS>(mA2, mB2, mB2, g2, stream);
+    return launch_gemm<EPI_BIAS, TM2>(mA2, mB2, mB2, g2, stream);
 }
 
 }  // namespace moe
