@@ -35,29 +35,36 @@ namespace {
 
 constexpr int UM = 128;                 // UMMA M (rows of one MMA)
 constexpr int BN = 256;                 // UMMA N (rows of B per tile)
-constexpr int BK = 64;                  // bf16 elements per 128-byte swizzle span
 constexpr int UK = 16;                  // K of one tcgen05.mma kind::f16
-constexpr int B_BYTES = BN * BK * 2;    // 32 KiB
 constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 512;     // all of TMEM
 constexpr int MAX_E = 1024;
 constexpr unsigned long long WAIT_NS = 1000000000ull;  // 1 s per wait
+constexpr int SMEM_RING = 192 * 1024;   // operand ring per CTA
 
 enum Epi { EPI_GELU = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_BIAS = 3 };
 
 // Tile shape.  TM = 1: 128 x 256 tiles, two 256-column accumulators in TMEM so
-// the epilogue of one tile overlaps the main loop of the next, 4 stages.
-// TM = 2: 256 x 256 tiles as two M=128 MMAs sharing every B tile (a third
-// fewer operand bytes per FLOP), one 512-column accumulator, 3 stages.
-template <int TM>
+// the epilogue of one tile overlaps the main loop of the next.  TM = 2:
+// 256 x 256 tiles as two M=128 MMAs sharing every B tile (a third fewer operand
+// bytes per FLOP), one 512-column accumulator.  BK is the K depth of one
+// pipeline stage: 64 bf16 (one 128-byte swizzle row) or 32 (64-byte swizzle);
+// the smaller stage doubles the number of stages in the same shared memory,
+// i.e. more operand bytes in flight to cover L2/HBM latency.
+template <int TM, int BK_>
 struct Tiling {
+    static constexpr int BK = BK_;
+    static constexpr int ROWB = BK * 2;                   // bytes per operand row
     static constexpr int BMT = UM * TM;                   // rows of A per tile
     static constexpr int A_BYTES = BMT * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = TM == 1 ? 4 : 3;
+    static constexpr int STAGES = SMEM_RING / STAGE_BYTES;
     static constexpr int NACC = TM == 1 ? 2 : 1;          // accumulator buffers
     static constexpr int ACC_COLS = BN * TM;              // TMEM columns per buffer
+    static_assert(BK == 64 || BK == 32, "BK");
+    static_assert(STAGES >= 3 && STAGES <= 8, "stages");
 };
 
 // kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major,
@@ -78,10 +85,9 @@ struct Ctl {  // control block in shared memory
     int32_t tile_start[MAX_E + 1];
 };
 
-template <int TM>
+template <class TL>
 constexpr size_t smem_bytes() {
-    return 1024 + (size_t)Tiling<TM>::STAGES * Tiling<TM>::STAGE_BYTES +
-           sizeof(Ctl<Tiling<TM>::STAGES>);
+    return 1024 + (size_t)TL::STAGES * TL::STAGE_BYTES + sizeof(Ctl<TL::STAGES>);
 }
 
 struct GemmArgs {
@@ -168,13 +174,15 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
-// layout TMA writes: 8-row x 128-byte atoms, atoms 1024 bytes apart (SBO);
-// the leading-byte offset is unused for this layout; bits 46-48 = 0b001;
-// swizzle mode 2 (128 B) in bits 61-63.
+// Shared-memory matrix descriptor of a K-major operand in the swizzled layout
+// TMA writes: 8-row atoms of ROWB-byte rows (128 B: swizzle mode 2, 64 B:
+// mode 4, bits 61-63), atoms ROWB*8 bytes apart (stride byte offset); the
+// leading-byte offset is unused for these layouts; bits 46-48 = 0b001.
+template <int ROWB>
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+    constexpr uint64_t mode = ROWB == 128 ? 2 : 4;
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) |
+           ((uint64_t)((ROWB * 8) >> 4) << 32) | ((uint64_t)1 << 46) | (mode << 61);
 }
 
 __device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t accumulate) {
@@ -282,12 +290,13 @@ __device__ __forceinline__ Tile decode_tile(const int32_t *tile_start, int e, in
     return T;
 }
 
-template <int EPI, int TM>
+template <int EPI, int TM, int BK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmB3, const GemmArgs args) {
-    using TL = Tiling<TM>;
+    using TL = Tiling<TM, BK>;
     constexpr int STAGES = TL::STAGES, BMT = TL::BMT, A_BYTES = TL::A_BYTES;
+    constexpr int B_BYTES = TL::B_BYTES, ROWB = TL::ROWB;
     __shared__ int32_t s_bad;
     pdl_enter();
     if (threadIdx.x == 0) s_bad = status_bad(args.status) ? 1 : 0;
@@ -402,8 +411,9 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 for (int kk = 0; kk < BK / UK; kk++)
 #pragma unroll
                     for (int hm = 0; hm < TM; hm++)  // M halves share the B tile
-                        umma(d + (uint32_t)(hm * BN), sdesc(a0 + hm * UM * BK * 2 + kk * UK * 2),
-                             sdesc(b0 + kk * UK * 2), (kb | kk) != 0);
+                        umma(d + (uint32_t)(hm * BN),
+                             sdesc<ROWB>(a0 + hm * UM * ROWB + kk * UK * 2),
+                             sdesc<ROWB>(b0 + kk * UK * 2), (kb | kk) != 0);
                 umma_commit(&ctl->empty[stage]);  // stage reusable once these MMAs read it
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
@@ -527,16 +537,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box box_rows x 64.
-bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box box_rows x bk
+// (bk = 64: 128-byte swizzle; bk = 32: 64-byte swizzle).
+bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+              int bk) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    cuuint32_t box[2] = {(cuuint32_t)bk, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -553,11 +566,12 @@ int sm_count() {
     return cached[dev];
 }
 
-template <int EPI, int TM>
+template <int EPI, int TM, int BK>
 moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &b3,
                        const GemmArgs &args, cudaStream_t stream) {
-    auto kern = tc_group_gemm<EPI, TM>;
-    constexpr size_t SMEM = smem_bytes<TM>();
+    using TL = Tiling<TM, BK>;
+    auto kern = tc_group_gemm<EPI, TM, BK>;
+    constexpr size_t SMEM = smem_bytes<TL>();
     static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
@@ -568,9 +582,8 @@ moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtenso
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
     constexpr int NOUT_TILE = EPI == EPI_SWIGLU ? BN / 2 : BN;
-    constexpr int BMT = Tiling<TM>::BMT;
     int64_t ntn = (args.n_out + NOUT_TILE - 1) / NOUT_TILE;
-    int64_t upper = (int64_t)args.e * ((args.c_max + BMT - 1) / BMT) * ntn;
+    int64_t upper = (int64_t)args.e * ((args.c_max + TL::BMT - 1) / TL::BMT) * ntn;
     int64_t grid = upper < sm_count() ? upper : sm_count();
     if (grid < 1) grid = 1;
     return launch_pdl(kern, dim3((unsigned)grid), dim3(NUM_THREADS), SMEM, stream, a, b, b3, args);
@@ -588,26 +601,26 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
                          const void *w1, const void *b1, const void *w3, const void *w2,
                          const void *b2, moe_act act, int e, int64_t c_max, int m, int h,
                          void *hid, void *out, int32_t *st, cudaStream_t stream) {
-    // fc1 keeps 128-row tiles (its activation epilogue overlaps the next tile's
-    // main loop); fc2 (bias-only epilogue, long K) uses 256-row tiles.
-    constexpr int TM1 = 1, TM2 = 2;
+    // fc1: 128-row tiles, so its activation epilogue overlaps the next tile's
+    // main loop.  fc2 (bias-only epilogue, long K): 256-row tiles, 32-deep stages.
+    constexpr int TM1 = 1, BK1 = 64, TM2 = 2, BK2 = 32;
     CUtensorMap mA1, mB1, mB3, mA2, mB2;
     const bool swiglu = act == MOE_ACT_SWIGLU;
     const uint32_t b1_box = swiglu ? BN / 2 : BN;
-    if (!make_map(&mA1, buf, (uint64_t)e * c_max, (uint64_t)m, Tiling<TM1>::BMT) ||
-        !make_map(&mB1, w1, (uint64_t)e * h, (uint64_t)m, b1_box) ||
-        !make_map(&mB3, swiglu ? w3 : w1, (uint64_t)e * h, (uint64_t)m, b1_box) ||
-        !make_map(&mA2, hid, (uint64_t)e * c_max, (uint64_t)h, Tiling<TM2>::BMT) ||
-        !make_map(&mB2, w2, (uint64_t)e * m, (uint64_t)h, BN))
+    if (!make_map(&mA1, buf, (uint64_t)e * c_max, (uint64_t)m, Tiling<TM1, BK1>::BMT, BK1) ||
+        !make_map(&mB1, w1, (uint64_t)e * h, (uint64_t)m, b1_box, BK1) ||
+        !make_map(&mB3, swiglu ? w3 : w1, (uint64_t)e * h, (uint64_t)m, b1_box, BK1) ||
+        !make_map(&mA2, hid, (uint64_t)e * c_max, (uint64_t)h, Tiling<TM2, BK2>::BMT, BK2) ||
+        !make_map(&mB2, w2, (uint64_t)e * m, (uint64_t)h, BN, BK2))
         return MOE_ERR_CUDA;
     GemmArgs g1{counts, c_dev, st, (const __nv_bfloat16 *)b1, (__nv_bfloat16 *)hid, c_max, e, m, h, h};
     moe_status r;
-    if (swiglu) r = launch_gemm<EPI_SWIGLU, TM1>(mA1, mB1, mB3, g1, stream);
-    else if (act == MOE_ACT_GELU) r = launch_gemm<EPI_GELU, TM1>(mA1, mB1, mB1, g1, stream);
-    else r = launch_gemm<EPI_RELU, TM1>(mA1, mB1, mB1, g1, stream);
+    if (swiglu) r = launch_gemm<EPI_SWIGLU, TM1, BK1>(mA1, mB1, mB3, g1, stream);
+    else if (act == MOE_ACT_GELU) r = launch_gemm<EPI_GELU, TM1, BK1>(mA1, mB1, mB1, g1, stream);
+    else r = launch_gemm<EPI_RELU, TM1, BK1>(mA1, mB1, mB1, g1, stream);
     if (r != MOE_OK) return r;
     GemmArgs g2{counts, c_dev, st, (const __nv_bfloat16 *)b2, (__nv_bfloat16 *)out, c_max, e, h, m, m};
-    return launch_gemm<EPI_BIAS, TM2>(mA2, mB2, mB2, g2, stream);
+    return launch_gemm<EPI_BIAS, TM2, BK2>(mA2, mB2, mB2, g2, stream);
 }
 
 }  // namespace moe
