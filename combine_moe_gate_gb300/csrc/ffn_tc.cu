@@ -12,9 +12,9 @@
 //   fc2:  out[j] = hid[j] W2[j]^T + b2[j]
 //
 // One persistent kernel per GEMM, one CTA per SM (~200 KB shared memory):
-//   warp 0      TMA producer: an A tile of 128 (or 256) x 64 and a 256x64 B tile
-//               per stage, 128-byte swizzle, a 4- (or 3-) stage ring guarded by
-//               full/empty mbarriers;
+//   warps 0, 10 TMA producers (A tiles, B tiles): an A tile of 128 (or 256) rows
+//               and a 256-row B tile per stage, swizzled, a ring of stages
+//               guarded by full/empty mbarriers;
 //   warp 1      allocates all 512 TMEM columns; one lane issues tcgen05.mma
 //               (kind::f16, bf16 x bf16 -> fp32, M=128 N=256 K=16; two per K step
 //               for 256-row tiles, sharing the B tile) and tcgen05.commit to
@@ -37,7 +37,8 @@ constexpr int UM = 128;                 // UMMA M (rows of one MMA)
 constexpr int BN = 256;                 // UMMA N (rows of B per tile)
 constexpr int UK = 16;                  // K of one tcgen05.mma kind::f16
 constexpr int EPI_WARPS = 8;
-constexpr int NUM_THREADS = 64 + EPI_WARPS * 32;
+constexpr int NUM_THREADS = 64 + EPI_WARPS * 32 + 32;  // + a second producer warp (B tiles)
+constexpr int B_WARP = 2 + EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;     // all of TMEM
 constexpr int MAX_E = 1024;
 constexpr unsigned long long WAIT_NS = 1000000000ull;  // 1 s per wait
@@ -338,7 +339,8 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             ctl->tile_start[e] = run;
             ctl->total_tiles = run;
             ctl->abort = 0;
-            for (int s = 0; s < STAGES; s++) { mbar_init(&ctl->full[s], 1); mbar_init(&ctl->empty[s], 1); }
+            // full: one arrival (with its transaction bytes) from each producer
+            for (int s = 0; s < STAGES; s++) { mbar_init(&ctl->full[s], 2); mbar_init(&ctl->empty[s], 1); }
             for (int a = 0; a < 2; a++) { mbar_init(&ctl->tfull[a], 1); mbar_init(&ctl->tempty[a], EPI_WARPS); }
             mbar_init(&ctl->drain, 1);
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -357,8 +359,12 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     const int total = ctl->total_tiles;
     int32_t *abort_flag = &ctl->abort;
 
-    if (warp == 0 && lane == 0) {
-        // ------------------------------------------------------- TMA producer
+    if ((warp == 0 || warp == B_WARP) && lane == 0) {
+        // ----------------------------------------------------- TMA producers
+        // Two issuing threads in different warps: TMA throughput per SM is
+        // bounded per issuing thread, so A tiles (warp 0) and B tiles (the last
+        // warp) are issued independently into the same stage.
+        const bool is_a = warp == 0;
         int stage = 0;
         uint32_t phase = 0;
         int issued = 0;
@@ -369,13 +375,16 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             for (int kb = 0; kb < nk; kb++) {
                 if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag, args.status))
                     goto producer_done;
-                mbar_expect_tx(&ctl->full[stage], TL::STAGE_BYTES);
-                tma_load_2d(sA + stage * A_BYTES, &tmA, kb * BK, a_row, &ctl->full[stage]);
-                if (EPI == EPI_SWIGLU) {
+                if (is_a) {
+                    mbar_expect_tx(&ctl->full[stage], A_BYTES);
+                    tma_load_2d(sA + stage * A_BYTES, &tmA, kb * BK, a_row, &ctl->full[stage]);
+                } else if (EPI == EPI_SWIGLU) {
+                    mbar_expect_tx(&ctl->full[stage], B_BYTES);
                     tma_load_2d(sB + stage * B_BYTES, &tmB, kb * BK, b_row, &ctl->full[stage]);
                     tma_load_2d(sB + stage * B_BYTES + B_BYTES / 2, &tmB3, kb * BK, b_row,
                                 &ctl->full[stage]);
                 } else {
+                    mbar_expect_tx(&ctl->full[stage], B_BYTES);
                     tma_load_2d(sB + stage * B_BYTES, &tmB, kb * BK, b_row, &ctl->full[stage]);
                 }
                 issued++;
@@ -426,7 +435,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         unsigned long long t0 = gtimer();
         while (!mbar_try(&ctl->drain, 0) && gtimer() - t0 < WAIT_NS) {
         }
-    } else if (warp >= 2) {
+    } else if (warp >= 2 && warp < B_WARP) {
         // ------------------------------------------------------------- epilogue
         // TM = 1: warp (sub, half) owns rows sub*32.. and half of the columns.
         // TM = 2: warp (sub, half) owns rows half*128 + sub*32.. and all columns.
