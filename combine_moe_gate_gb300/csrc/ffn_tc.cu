@@ -168,6 +168,14 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// Pull a box into L2 ahead of its TMA load (no shared memory involved).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     (uint64_t)map),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -269,6 +277,29 @@ __device__ __forceinline__ float gelu_erf(float a) {
     return a * (a >= 0.0f ? 1.0f - r : r);
 }
 
+// The same GELU on a pair of values with packed fp32x2 arithmetic.
+__device__ __forceinline__ float2 gelu_erf2(float2 a) {
+    const float2 x = __fmul2_rn(make_float2(fabsf(a.x), fabsf(a.y)),
+                                make_float2(0.70710678118654752f, 0.70710678118654752f));
+    float2 p = __ffma2_rn(x, make_float2(0.0000430638f, 0.0000430638f),
+                          make_float2(0.0002765672f, 0.0002765672f));
+    p = __ffma2_rn(x, p, make_float2(0.0001520143f, 0.0001520143f));
+    p = __ffma2_rn(x, p, make_float2(0.0092705272f, 0.0092705272f));
+    p = __ffma2_rn(x, p, make_float2(0.0422820123f, 0.0422820123f));
+    p = __ffma2_rn(x, p, make_float2(0.0705230784f, 0.0705230784f));
+    p = __ffma2_rn(x, p, make_float2(1.0f, 1.0f));
+    float2 q = __fmul2_rn(p, p);
+    q = __fmul2_rn(q, q);
+    q = __fmul2_rn(q, q);
+    q = __fmul2_rn(q, q);
+    float2 r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.x) : "f"(q.x));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.y) : "f"(q.y));
+    r = __fmul2_rn(r, make_float2(0.5f, 0.5f));
+    const float2 phi = make_float2(a.x >= 0.0f ? 1.0f - r.x : r.x, a.y >= 0.0f ? 1.0f - r.y : r.y);
+    return __fmul2_rn(a, phi);
+}
+
 __device__ __forceinline__ float silu(float a) { return a / (1.0f + expf(-a)); }
 
 // Tile t -> (expert j, m-tile, n-tile); m-tile varies fastest.
@@ -309,6 +340,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     uint8_t *sB = smem + STAGES * A_BYTES;
     Ctl<STAGES> *ctl = (Ctl<STAGES> *)(smem + STAGES * TL::STAGE_BYTES);
     __shared__ int32_t kept_rows[MAX_E];
+    __shared__ __align__(16) float epi_bias[EPI_WARPS][256];  // per epilogue warp
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = args.e;
@@ -373,6 +405,16 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             const int a_row = (int)((int64_t)T.j * args.c_max + (int64_t)T.mt * BMT);
             const int b_row = T.j * args.b_rows + T.nt * NOUT_TILE;
             for (int kb = 0; kb < nk; kb++) {
+                // L2 prefetch a ring-depth beyond the loads in flight
+                const int pk = kb + STAGES;
+                if (pk < nk) {
+                    if (is_a) {
+                        tma_prefetch_2d(&tmA, pk * BK, a_row);
+                    } else {
+                        tma_prefetch_2d(&tmB, pk * BK, b_row);
+                        if (EPI == EPI_SWIGLU) tma_prefetch_2d(&tmB3, pk * BK, b_row);
+                    }
+                }
                 if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag, args.status))
                     goto producer_done;
                 if (is_a) {
@@ -480,6 +522,21 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     }
                 }
             } else {
+                // this warp's bias columns, widened to fp32 in shared memory once per tile
+                float *bsl = epi_bias[ew];
+                if (lane * 8 < COLS) {
+                    const int g8 = T.nt * NOUT_TILE + col0 + lane * 8;
+                    float b8[8];
+                    if (brow && g8 < args.n_out) {
+                        Elt<__nv_bfloat16>::unpack(*reinterpret_cast<const V16 *>(brow + g8), b8);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; i++) b8[i] = 0.0f;
+                    }
+                    reinterpret_cast<float4 *>(bsl + lane * 8)[0] = make_float4(b8[0], b8[1], b8[2], b8[3]);
+                    reinterpret_cast<float4 *>(bsl + lane * 8)[1] = make_float4(b8[4], b8[5], b8[6], b8[7]);
+                }
+                __syncwarp();
 #pragma unroll 1
                 for (int c0 = 0; c0 < COLS; c0 += 64) {
                     uint32_t r[2][32];
@@ -493,27 +550,29 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
 #pragma unroll
                         for (int q = 0; q < 4; q++) {
                             const int g8 = gcol + q * 8;
-                            float v[8];
-                            float bsum[8];
-                            if (brow && g8 < args.n_out) {
-                                V16 bv = *reinterpret_cast<const V16 *>(brow + g8);
-                                Elt<__nv_bfloat16>::unpack(bv, bsum);
-                            } else {
+                            const float4 *bp = reinterpret_cast<const float4 *>(bsl + c0 + 32 * h2 + q * 8);
+                            const float4 bl = bp[0], bh = bp[1];
+                            const float2 bb[4] = {make_float2(bl.x, bl.y), make_float2(bl.z, bl.w),
+                                                  make_float2(bh.x, bh.y), make_float2(bh.z, bh.w)};
+                            uint32_t pk[4];
 #pragma unroll
-                                for (int i = 0; i < 8; i++) bsum[i] = 0.0f;
+                            for (int i = 0; i < 4; i++) {
+                                float2 a = __fadd2_rn(make_float2(__uint_as_float(r[h2][q * 8 + 2 * i]),
+                                                                  __uint_as_float(r[h2][q * 8 + 2 * i + 1])),
+                                                      bb[i]);
+                                if (EPI == EPI_GELU) a = gelu_erf2(a);
+                                else if (EPI == EPI_RELU) a = make_float2(fmaxf(a.x, 0.0f), fmaxf(a.y, 0.0f));
+                                pk[i] = pack_bf16(a.x, a.y);
                             }
-#pragma unroll
-                            for (int i = 0; i < 8; i++) {
-                                float a = __uint_as_float(r[h2][q * 8 + i]) + bsum[i];
-                                if (EPI == EPI_GELU) a = gelu_erf(a);
-                                else if (EPI == EPI_RELU) a = fmaxf(a, 0.0f);
-                                v[i] = a;
+                            if (valid && g8 < args.n_out) {
+                                V16 o;
+                                o.w[0] = pk[0]; o.w[1] = pk[1]; o.w[2] = pk[2]; o.w[3] = pk[3];
+                                st_v16(orow + g8, o);
                             }
-                            if (valid && g8 < args.n_out)
-                                st_v16(orow + g8, Elt<__nv_bfloat16>::pack(v));
                         }
                     }
                 }
+                __syncwarp();   // slice reused for the next tile
             }
             tc_fence_before();
             __syncwarp();
