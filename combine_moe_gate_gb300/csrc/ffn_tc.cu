@@ -102,6 +102,9 @@ struct GemmArgs {
     int K;             // contraction length
     int n_out;         // output columns per expert
     int b_rows;        // rows of each B tensor map per expert
+    const __nv_bfloat16 *a_ptr;   // the operands again, for L2 prefetch
+    const __nv_bfloat16 *b_ptr;
+    const __nv_bfloat16 *b3_ptr;
 };
 
 // ------------------------------------------------------------- PTX wrappers
@@ -169,11 +172,20 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 }
 
 // Pull a box into L2 ahead of its TMA load (no shared memory involved).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     (uint64_t)map),
-                 "r"(x), "r"(y)
-                 : "memory");
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// The whole warp pulls the rows [row0, row0 + rows) x columns [x0, x0 + bk) of a
+// row-major [nrows, ld] bf16 operand into L2 (one 128-byte line per row and
+// lane step); rows past the end are skipped.
+__device__ __forceinline__ void warp_prefetch_rows(const __nv_bfloat16 *base, int64_t nrows,
+                                                   int64_t ld, int64_t row0, int rows, int x0,
+                                                   int lane) {
+    for (int r = lane; r < rows; r += 32) {
+        const int64_t row = row0 + r;
+        if (row < nrows) prefetch_l2(base + row * ld + x0);
+    }
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -391,12 +403,16 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     const int total = ctl->total_tiles;
     int32_t *abort_flag = &ctl->abort;
 
-    if ((warp == 0 || warp == B_WARP) && lane == 0) {
+    if (warp == 0 || warp == B_WARP) {
         // ----------------------------------------------------- TMA producers
-        // Two issuing threads in different warps: TMA throughput per SM is
-        // bounded per issuing thread, so A tiles (warp 0) and B tiles (the last
-        // warp) are issued independently into the same stage.
+        // Two issuing threads in different warps (TMA throughput per SM is
+        // bounded per issuing thread): A tiles from warp 0, B tiles from the last
+        // warp.  Lane 0 issues the copies; all lanes pull the operand rows of the
+        // k-block PF ahead into L2, so that more distinct HBM lines are in flight
+        // than the shared-memory ring alone allows.
+        constexpr int PF = 512 / BK;
         const bool is_a = warp == 0;
+        const int64_t a_nrows = (int64_t)e * args.c_max, b_nrows = (int64_t)e * args.b_rows;
         int stage = 0;
         uint32_t phase = 0;
         int issued = 0;
@@ -405,29 +421,33 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             const int a_row = (int)((int64_t)T.j * args.c_max + (int64_t)T.mt * BMT);
             const int b_row = T.j * args.b_rows + T.nt * NOUT_TILE;
             for (int kb = 0; kb < nk; kb++) {
-                // L2 prefetch a ring-depth beyond the loads in flight
-                const int pk = kb + STAGES;
-                if (pk < nk) {
-                    if (is_a) {
-                        tma_prefetch_2d(&tmA, pk * BK, a_row);
-                    } else {
-                        tma_prefetch_2d(&tmB, pk * BK, b_row);
-                        if (EPI == EPI_SWIGLU) tma_prefetch_2d(&tmB3, pk * BK, b_row);
+                int ok = 1;
+                if (lane == 0) {
+                    ok = mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag, args.status);
+                    if (ok && is_a) {
+                        mbar_expect_tx(&ctl->full[stage], A_BYTES);
+                        tma_load_2d(sA + stage * A_BYTES, &tmA, kb * BK, a_row, &ctl->full[stage]);
+                    } else if (ok && EPI == EPI_SWIGLU) {
+                        mbar_expect_tx(&ctl->full[stage], B_BYTES);
+                        tma_load_2d(sB + stage * B_BYTES, &tmB, kb * BK, b_row, &ctl->full[stage]);
+                        tma_load_2d(sB + stage * B_BYTES + B_BYTES / 2, &tmB3, kb * BK, b_row,
+                                    &ctl->full[stage]);
+                    } else if (ok) {
+                        mbar_expect_tx(&ctl->full[stage], B_BYTES);
+                        tma_load_2d(sB + stage * B_BYTES, &tmB, kb * BK, b_row, &ctl->full[stage]);
                     }
                 }
-                if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag, args.status))
-                    goto producer_done;
-                if (is_a) {
-                    mbar_expect_tx(&ctl->full[stage], A_BYTES);
-                    tma_load_2d(sA + stage * A_BYTES, &tmA, kb * BK, a_row, &ctl->full[stage]);
-                } else if (EPI == EPI_SWIGLU) {
-                    mbar_expect_tx(&ctl->full[stage], B_BYTES);
-                    tma_load_2d(sB + stage * B_BYTES, &tmB, kb * BK, b_row, &ctl->full[stage]);
-                    tma_load_2d(sB + stage * B_BYTES + B_BYTES / 2, &tmB3, kb * BK, b_row,
-                                &ctl->full[stage]);
-                } else {
-                    mbar_expect_tx(&ctl->full[stage], B_BYTES);
-                    tma_load_2d(sB + stage * B_BYTES, &tmB, kb * BK, b_row, &ctl->full[stage]);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) goto producer_done;
+                const int pk = kb + PF;
+                if (pk < nk) {
+                    if (is_a) {
+                        warp_prefetch_rows(args.a_ptr, a_nrows, args.K, a_row, BMT, pk * BK, lane);
+                    } else if (EPI == EPI_SWIGLU) {
+                        warp_prefetch_rows(args.b_ptr, b_nrows, args.K, b_row, BN / 2, pk * BK, lane);
+                        warp_prefetch_rows(args.b3_ptr, b_nrows, args.K, b_row, BN / 2, pk * BK, lane);
+                    } else {
+                        warp_prefetch_rows(args.b_ptr, b_nrows, args.K, b_row, BN, pk * BK, lane);
+                    }
                 }
                 issued++;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -435,11 +455,13 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         }
     producer_done:
         // wait (bounded) for the copies still in flight before the CTA can exit
-        for (int i = max(0, issued - STAGES); i < issued; i++) {
-            int s = i % STAGES;
-            uint32_t ph = (uint32_t)((i / STAGES) & 1);
-            unsigned long long t0 = gtimer();
-            while (!mbar_try(&ctl->full[s], ph) && gtimer() - t0 < WAIT_NS) {
+        if (lane == 0) {
+            for (int i = max(0, issued - STAGES); i < issued; i++) {
+                int s = i % STAGES;
+                uint32_t ph = (uint32_t)((i / STAGES) & 1);
+                unsigned long long t0 = gtimer();
+                while (!mbar_try(&ctl->full[s], ph) && gtimer() - t0 < WAIT_NS) {
+                }
             }
         }
     } else if (warp == 1 && lane == 0) {
@@ -681,13 +703,16 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
         !make_map(&mA2, hid, (uint64_t)e * c_max, (uint64_t)h, Tiling<TM2, BK2>::BMT, BK2) ||
         !make_map(&mB2, w2, (uint64_t)e * m, (uint64_t)h, BN, BK2))
         return MOE_ERR_CUDA;
-    GemmArgs g1{counts, c_dev, st, (const __nv_bfloat16 *)b1, (__nv_bfloat16 *)hid, c_max, e, m, h, h};
+    GemmArgs g1{counts, c_dev, st, (const __nv_bfloat16 *)b1, (__nv_bfloat16 *)hid, c_max, e, m, h, h,
+                (const __nv_bfloat16 *)buf, (const __nv_bfloat16 *)w1,
+                (const __nv_bfloat16 *)(swiglu ? w3 : w1)};
     moe_status r;
     if (swiglu) r = launch_gemm<EPI_SWIGLU, TM1, BK1>(mA1, mB1, mB3, g1, stream);
     else if (act == MOE_ACT_GELU) r = launch_gemm<EPI_GELU, TM1, BK1>(mA1, mB1, mB1, g1, stream);
     else r = launch_gemm<EPI_RELU, TM1, BK1>(mA1, mB1, mB1, g1, stream);
     if (r != MOE_OK) return r;
-    GemmArgs g2{counts, c_dev, st, (const __nv_bfloat16 *)b2, (__nv_bfloat16 *)out, c_max, e, h, m, m};
+    GemmArgs g2{counts, c_dev, st, (const __nv_bfloat16 *)b2, (__nv_bfloat16 *)out, c_max, e, h, m, m,
+                (const __nv_bfloat16 *)hid, (const __nv_bfloat16 *)w2, (const __nv_bfloat16 *)w2};
     return launch_gemm<EPI_BIAS, TM2, BK2>(mA2, mB2, mB2, g2, stream);
 }
 
