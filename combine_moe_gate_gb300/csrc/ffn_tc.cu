@@ -102,9 +102,6 @@ struct GemmArgs {
     int K;             // contraction length
     int n_out;         // output columns per expert
     int b_rows;        // rows of each B tensor map per expert
-    const __nv_bfloat16 *a_ptr;   // the operands again, for L2 prefetch
-    const __nv_bfloat16 *b_ptr;
-    const __nv_bfloat16 *b3_ptr;
 };
 
 // ------------------------------------------------------------- PTX wrappers
@@ -172,22 +169,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 }
 
 // Pull a box into L2 ahead of its TMA load (no shared memory involved).
-__device__ __forceinline__ void prefetch_l2(const void *p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
-// The whole warp pulls the rows [row0, row0 + rows) x columns [x0, x0 + bk) of a
-// row-major [nrows, ld] bf16 operand into L2 (one 128-byte line per row and
-// lane step); rows past the end are skipped.
-__device__ __forceinline__ void warp_prefetch_rows(const __nv_bfloat16 *base, int64_t nrows,
-                                                   int64_t ld, int64_t row0, int rows, int x0,
-                                                   int lane) {
-    for (int r = lane; r < rows; r += 32) {
-        const int64_t row = row0 + r;
-        if (row < nrows) prefetch_l2(base + row * ld + x0);
-    }
-}
-
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -407,12 +388,8 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         // ----------------------------------------------------- TMA producers
         // Two issuing threads in different warps (TMA throughput per SM is
         // bounded per issuing thread): A tiles from warp 0, B tiles from the last
-        // warp.  Lane 0 issues the copies; all lanes pull the operand rows of the
-        // k-block PF ahead into L2, so that more distinct HBM lines are in flight
-        // than the shared-memory ring alone allows.
-        constexpr int PF = 512 / BK;
+        // warp (lane 0 of each issues).
         const bool is_a = warp == 0;
-        const int64_t a_nrows = (int64_t)e * args.c_max, b_nrows = (int64_t)e * args.b_rows;
         int stage = 0;
         uint32_t phase = 0;
         int issued = 0;
@@ -438,17 +415,6 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     }
                 }
                 if (!__shfl_sync(0xffffffffu, ok, 0)) goto producer_done;
-                const int pk = kb + PF;
-                if (pk < nk) {
-                    if (is_a) {
-                        warp_prefetch_rows(args.a_ptr, a_nrows, args.K, a_row, BMT, pk * BK, lane);
-                    } else if (EPI == EPI_SWIGLU) {
-                        warp_prefetch_rows(args.b_ptr, b_nrows, args.K, b_row, BN / 2, pk * BK, lane);
-                        warp_prefetch_rows(args.b3_ptr, b_nrows, args.K, b_row, BN / 2, pk * BK, lane);
-                    } else {
-                        warp_prefetch_rows(args.b_ptr, b_nrows, args.K, b_row, BN, pk * BK, lane);
-                    }
-                }
                 issued++;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
@@ -703,16 +669,13 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
         !make_map(&mA2, hid, (uint64_t)e * c_max, (uint64_t)h, Tiling<TM2, BK2>::BMT, BK2) ||
         !make_map(&mB2, w2, (uint64_t)e * m, (uint64_t)h, BN, BK2))
         return MOE_ERR_CUDA;
-    GemmArgs g1{counts, c_dev, st, (const __nv_bfloat16 *)b1, (__nv_bfloat16 *)hid, c_max, e, m, h, h,
-                (const __nv_bfloat16 *)buf, (const __nv_bfloat16 *)w1,
-                (const __nv_bfloat16 *)(swiglu ? w3 : w1)};
+    GemmArgs g1{counts, c_dev, st, (const __nv_bfloat16 *)b1, (__nv_bfloat16 *)hid, c_max, e, m, h, h};
     moe_status r;
     if (swiglu) r = launch_gemm<EPI_SWIGLU, TM1, BK1>(mA1, mB1, mB3, g1, stream);
     else if (act == MOE_ACT_GELU) r = launch_gemm<EPI_GELU, TM1, BK1>(mA1, mB1, mB1, g1, stream);
     else r = launch_gemm<EPI_RELU, TM1, BK1>(mA1, mB1, mB1, g1, stream);
     if (r != MOE_OK) return r;
-    GemmArgs g2{counts, c_dev, st, (const __nv_bfloat16 *)b2, (__nv_bfloat16 *)out, c_max, e, h, m, m,
-                (const __nv_bfloat16 *)hid, (const __nv_bfloat16 *)w2, (const __nv_bfloat16 *)w2};
+    GemmArgs g2{counts, c_dev, st, (const __nv_bfloat16 *)b2, (__nv_bfloat16 *)out, c_max, e, h, m, m};
     return launch_gemm<EPI_BIAS, TM2, BK2>(mA2, mB2, mB2, g2, stream);
 }
 
