@@ -142,7 +142,7 @@ __device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
 
 // Bounded wait for the phase with `parity` to complete.  Returns false if the
 // CTA is aborting or the wait ran past WAIT_NS (then the abort is raised).
-__device__ __noinline__ bool mbar_wait(uint64_t *b, uint32_t parity, int32_t *abort_flag,
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, int32_t *abort_flag,
                                        int32_t *status) {
     if (mbar_try(b, parity)) return true;
     unsigned long long t0 = gtimer();
