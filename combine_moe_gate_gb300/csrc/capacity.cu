@@ -8,7 +8,8 @@
 // route is its rank among the routes that chose the same expert, so the flat
 // route-major table [k, s] is ranked in its natural order.
 //
-// Two launches, no inter-CTA waiting:
+// Small tables (up to 16384 routes, e <= 256) take one single-CTA launch;
+// otherwise two launches, no inter-CTA waiting:
 //   1. cap_hist: CTA b counts the experts of its chunk of CH routes -> hist[b][e].
 //   2. cap_assign: CTA b sums hist[0..b-1][j] for its base offsets, ranks its
 //      chunk stably (warps take consecutive segments; inside a warp
@@ -129,6 +130,69 @@ cap_assign_kernel(const int32_t *__restrict__ idx, int64_t n, int e, int nblk,
     }
 }
 
+// Single-CTA path for small route tables (n <= 32 warps x 32 lanes x R routes,
+// e <= 256): one launch, no histogram pass.  Warp w ranks the contiguous
+// segment [w*32R, (w+1)*32R) stably; an exclusive prefix over warps per expert
+// gives the base offsets, the totals give counts[] and c.
+constexpr int CAP1_NT = 1024, CAP1_NW = 32, CAP1_MAXE = 256;
+
+template <int R>
+__global__ void __launch_bounds__(CAP1_NT)
+cap_single_kernel(const int32_t *__restrict__ idx, int64_t n, int e, int c_fixed, int c_cap,
+                  int64_t c_max, int32_t *__restrict__ loc, int32_t *__restrict__ counts,
+                  int32_t *__restrict__ c_dev, int32_t *status) {
+    pdl_enter();
+    if (status_bad(status)) return;
+    __shared__ int32_t wcnt[CAP1_NW][CAP1_MAXE];
+    __shared__ int32_t s_max;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int q = tid; q < CAP1_NW * CAP1_MAXE; q += CAP1_NT) (&wcnt[0][0])[q] = 0;
+    if (tid == 0) s_max = 0;
+    const int64_t seg0 = (int64_t)warp * 32 * R;
+    int32_t val[R], rank[R];
+#pragma unroll
+    for (int rd = 0; rd < R; rd++) {
+        const int64_t j = seg0 + rd * 32 + lane;
+        const int v = j < n ? __ldg(idx + j) : -1;
+        if (j < n && (unsigned)v >= (unsigned)e) set_status(status, MOE_ERR_INVALID_ARG);
+        val[rd] = (unsigned)v < (unsigned)e ? v : -1;
+    }
+    __syncthreads();
+    const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int rd = 0; rd < R; rd++) {
+        const int v = val[rd];
+        const unsigned peers = __match_any_sync(0xffffffffu, v);
+        const int prev = v >= 0 ? wcnt[warp][v] : 0;
+        __syncwarp();
+        if (v >= 0 && (peers & lt) == 0) wcnt[warp][v] = prev + __popc(peers);
+        __syncwarp();
+        rank[rd] = prev + __popc(peers & lt);
+    }
+    __syncthreads();
+    for (int x = tid; x < e; x += CAP1_NT) {
+        int32_t run = 0;
+        for (int w = 0; w < CAP1_NW; w++) {
+            const int32_t c = wcnt[w][x];
+            wcnt[w][x] = run;
+            run += c;
+        }
+        counts[x] = run;
+        atomicMax(&s_max, run);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const int c = c_fixed >= 0 ? c_fixed : min(c_cap, s_max);
+        c_dev[0] = c;
+        if ((int64_t)c > c_max) set_status(status, MOE_ERR_CAPACITY);
+    }
+#pragma unroll
+    for (int rd = 0; rd < R; rd++) {
+        const int64_t j = seg0 + rd * 32 + lane;
+        if (j < n && val[rd] >= 0) loc[j] = wcnt[warp][val[rd]] + rank[rd];
+    }
+}
+
 int64_t ceil_div_exact(double x, int e) {
     int64_t c = (int64_t)ceil(x / (double)e);
     while (c > 0 && (double)(c - 1) * (double)e >= x) c--;
@@ -165,6 +229,18 @@ moe_status capacity_launch(const int32_t *idx, int64_t s, int e, int k, float f,
     } else if (f < 0.0f) {
         int64_t c = capacity_bound_host(f, s, e, k);
         c_cap = (int)c;
+    }
+    if (e <= CAP1_MAXE && n <= (int64_t)CAP1_NW * 32 * 16) {
+#define MOE_CAP1(RV)                                                                               \
+        if (n <= (int64_t)CAP1_NW * 32 * RV)                                                       \
+            return launch_pdl(cap_single_kernel<RV>, dim3(1), dim3(CAP1_NT), 0, stream, idx, n, e,  \
+                              c_fixed, c_cap, c_max, loc, counts, c_dev, st);
+        MOE_CAP1(1)
+        MOE_CAP1(2)
+        MOE_CAP1(4)
+        MOE_CAP1(8)
+        MOE_CAP1(16)
+#undef MOE_CAP1
     }
     int32_t *hist = (int32_t *)ws;
     if (launch_pdl(cap_hist_kernel, dim3((unsigned)nblk), dim3(CAP_NT), e * sizeof(int32_t), stream,

@@ -20,6 +20,7 @@ namespace {
 
 constexpr int DNT = 256;  // threads per CTA (8 token-warps)
 constexpr int UNR = 4;    // 16-byte chunks per lane per batch
+constexpr int RG = 4;     // routes whose rows are in flight together in combine
 
 struct Routes {
     unsigned kept;   // bit r: route r of this token is kept
@@ -67,15 +68,21 @@ encode_kernel(const T *__restrict__ x, const int32_t *__restrict__ idx,
     const int64_t nw = (int64_t)gridDim.x * (DNT / 32);
     const int nch = m / Elt<T>::VEC;
     for (int64_t t = blockIdx.x * (DNT / 32) + (threadIdx.x >> 5); t < s; t += nw) {
+        const V16 *src = reinterpret_cast<const V16 *>(x + t * m);
+        // the first batch of the token's row is loaded together with its routes
+        V16 v[UNR];
+#pragma unroll
+        for (int u = 0; u < UNR; u++)
+            if (lane + 32 * u < nch) v[u] = ld_stream(src + lane + 32 * u);
         Routes R = load_routes(idx, loc, nullptr, s, t, m, e, k, c_eff, c_max, status);
         if (!R.kept) continue;
-        const V16 *src = reinterpret_cast<const V16 *>(x + t * m);
         for (int base = 0; base < nch; base += 32 * UNR) {  // warp-uniform trip count
             const int q0 = base + lane;
-            V16 v[UNR];
+            if (base > 0) {
 #pragma unroll
-            for (int u = 0; u < UNR; u++)
-                if (q0 + 32 * u < nch) v[u] = ld_stream(src + q0 + 32 * u);
+                for (int u = 0; u < UNR; u++)
+                    if (q0 + 32 * u < nch) v[u] = ld_stream(src + q0 + 32 * u);
+            }
             for (unsigned km = R.kept; km; km &= km - 1) {
                 int r = __ffs(km) - 1;
                 int64_t row = __shfl_sync(0xffffffffu, R.row, r);
@@ -135,22 +142,38 @@ combine_kernel(const T *__restrict__ src, const int32_t *__restrict__ idx,
             for (int u = 0; u < UNR; u++)
 #pragma unroll
                 for (int i = 0; i < VEC; i++) acc[u][i] = 0.0f;
-            for (unsigned km = R.kept; km; km &= km - 1) {  // ascending route order
-                int r = __ffs(km) - 1;
-                int64_t row = __shfl_sync(0xffffffffu, R.row, r);
-                float g = WEIGHTED ? __shfl_sync(0xffffffffu, R.g, r) : 1.0f;
-                const V16 *sp = reinterpret_cast<const V16 *>(src + row);
-                V16 v[UNR];
+            // routes in ascending order, RG at a time: every row load of a group is
+            // in flight before the group's fused multiply-adds (same order as one
+            // route at a time)
+            for (int rg = 0; rg < k; rg += RG) {
+                const unsigned gm = (R.kept >> rg) & ((1u << RG) - 1u);
+                if (!gm) continue;
+                V16 v[RG][UNR];
+                float g[RG];
 #pragma unroll
-                for (int u = 0; u < UNR; u++)
-                    if (q0 + 32 * u < nch) v[u] = ld_stream(sp + q0 + 32 * u);
+                for (int rr = 0; rr < RG; rr++) {
+                    g[rr] = 0.0f;
+                    if ((gm >> rr) & 1u) {
+                        const int64_t row = __shfl_sync(0xffffffffu, R.row, rg + rr);
+                        g[rr] = WEIGHTED ? __shfl_sync(0xffffffffu, R.g, rg + rr) : 1.0f;
+                        const V16 *sp = reinterpret_cast<const V16 *>(src + row);
 #pragma unroll
-                for (int u = 0; u < UNR; u++) {
-                    float f[VEC];
-                    Elt<T>::unpack(v[u], f);
+                        for (int u = 0; u < UNR; u++)
+                            if (q0 + 32 * u < nch) v[rr][u] = ld_stream(sp + q0 + 32 * u);
+                    }
+                }
 #pragma unroll
-                    for (int i = 0; i < VEC; i++)
-                        acc[u][i] = WEIGHTED ? __fmaf_rn(g, f[i], acc[u][i]) : __fadd_rn(acc[u][i], f[i]);
+                for (int rr = 0; rr < RG; rr++) {
+                    if (!((gm >> rr) & 1u)) continue;
+#pragma unroll
+                    for (int u = 0; u < UNR; u++) {
+                        float f[VEC];
+                        Elt<T>::unpack(v[rr][u], f);
+#pragma unroll
+                        for (int i = 0; i < VEC; i++)
+                            acc[u][i] = WEIGHTED ? __fmaf_rn(g[rr], f[i], acc[u][i])
+                                                 : __fadd_rn(acc[u][i], f[i]);
+                    }
                 }
             }
 #pragma unroll

@@ -315,6 +315,119 @@ gate_topk_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
     }
 }
 
+// ---------------------------------------------------------------- small e
+// One thread per (token, expert) for e <= 32: the logit's single accumulator
+// walks the features in ascending order (the contract above) with no blocking
+// at all, so the whole batch runs as s*e independent chains in s*e/32 warps.
+// The transposed gate weight [EP][m + 4] sits in shared memory (the +4 keeps the
+// 16-byte reads of different experts on different banks); x is streamed with
+// 16-byte loads kept PD chunks ahead.  Softmax and top-k run on the EP lanes
+// of each token with segmented shuffles.
+template <int EP, typename XT>
+__global__ void __launch_bounds__(256)
+gate_small_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
+                  const float *__restrict__ bias, int64_t s, int m, int e, int k, int normalize,
+                  int32_t *__restrict__ idx, float *__restrict__ gates, int32_t *status) {
+    pdl_enter();
+    if (status_bad(status)) return;
+    extern __shared__ __align__(16) float wt[];  // [EP][m + 4]
+    constexpr int VEC = Elt<XT>::VEC;
+    constexpr int PD = 4;
+    const int ld = m + 4;
+    for (int q = threadIdx.x; q < m * EP; q += blockDim.x) {
+        const int i = q / EP, j = q % EP;
+        wt[j * ld + i] = j < e ? wg[(int64_t)i * e + j] : 0.0f;
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int TPW = 32 / EP;
+    const int j = lane % EP;
+    const int64_t t = ((int64_t)blockIdx.x * (blockDim.x / 32) + warp) * TPW + lane / EP;
+    const bool live = t < s;
+    const XT *xr = x + (live ? t : 0) * (int64_t)m;
+    const float *wr = wt + j * ld;
+    const int nch = m / VEC;
+    float acc = 0.0f;
+    V16 cur[PD];
+#pragma unroll
+    for (int p = 0; p < PD; p++)
+        if (p < nch) cur[p] = ld_stream(xr + p * VEC);
+    for (int c0 = 0; c0 < nch; c0 += PD) {
+        V16 nxt[PD];
+#pragma unroll
+        for (int p = 0; p < PD; p++)
+            if (c0 + PD + p < nch) nxt[p] = ld_stream(xr + (c0 + PD + p) * VEC);
+#pragma unroll
+        for (int p = 0; p < PD; p++) {
+            if (c0 + p < nch) {
+                float f[VEC];
+                Elt<XT>::unpack(cur[p], f);
+                const float *w = wr + (c0 + p) * VEC;
+#pragma unroll
+                for (int u = 0; u < VEC; u += 4) {
+                    const float4 w4 = *reinterpret_cast<const float4 *>(w + u);
+                    acc = fmaf(f[u], w4.x, acc);
+                    acc = fmaf(f[u + 1], w4.y, acc);
+                    acc = fmaf(f[u + 2], w4.z, acc);
+                    acc = fmaf(f[u + 3], w4.w, acc);
+                }
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < PD; p++) cur[p] = nxt[p];
+    }
+    float v = -INFINITY;
+    if (j < e) v = bias ? acc + bias[j] : acc;
+    // segmented (EP lanes per token) softmax statistics
+    float mx = v;
+#pragma unroll
+    for (int o = EP / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float z = j < e ? expf(v - mx) : 0.0f;
+#pragma unroll
+    for (int o = EP / 2; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    // top-k: k rounds of segmented arg-max (ties -> lower expert index)
+    bool taken = j >= e;
+    float my_v = 0.0f;
+    int my_j = 0;
+    for (int r = 0; r < k; r++) {
+        float bv = taken ? -INFINITY : v;
+        int bj = taken ? 0x7fffffff : j;
+#pragma unroll
+        for (int o = EP / 2; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
+            if (ov > bv || (ov == bv && oj < bj)) { bv = ov; bj = oj; }
+        }
+        if (bj == j) taken = true;
+        if (j == r) { my_v = bv; my_j = bj; }
+    }
+    const float p = j < k ? expf(my_v - mx) : 0.0f;
+    float sel = p;
+#pragma unroll
+    for (int o = EP / 2; o > 0; o >>= 1) sel += __shfl_xor_sync(0xffffffffu, sel, o);
+    if (live && j < k) {
+        idx[(int64_t)j * s + t] = my_j;
+        gates[(int64_t)j * s + t] = p / (normalize ? sel : z);
+    }
+}
+
+template <int EP, typename XT>
+moe_status launch_small(const void *x, const float *wg, const float *bias, int64_t s, int m, int e,
+                        int k, int normalize, int32_t *idx, float *gates, int32_t *st,
+                        cudaStream_t stream) {
+    auto kern = gate_small_kernel<EP, XT>;
+    const size_t smem = (size_t)EP * (m + 4) * sizeof(float);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+        return MOE_ERR_CUDA;
+    constexpr int TPB = (256 / 32) * (32 / EP);  // tokens per CTA
+    const int64_t grid = (s + TPB - 1) / TPB;
+    if (grid > 0x7fffffff) return MOE_ERR_UNSUPPORTED;
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(256), smem, stream, (const XT *)x, wg, bias, s,
+                      m, e, k, normalize, idx, gates, st);
+}
+
 template <class C, typename XT>
 moe_status launch_cfg(const void *x, const float *wg, const float *bias, int64_t s, int m, int e,
                       int k, int normalize, int32_t *idx, float *gates, int32_t *st,
@@ -331,6 +444,9 @@ moe_status launch_cfg(const void *x, const float *wg, const float *bias, int64_t
                       bias, s, m, e, k, normalize, idx, gates, st);
 }
 
+// Shared memory the small-e kernel needs for the transposed gate weight.
+constexpr size_t SMALL_E_SMEM_MAX = 64 * 1024;
+
 template <typename XT>
 moe_status gate_dispatch(const void *x, const float *wg, const float *bias, int64_t s, int m, int e,
                          int k, int normalize, int32_t *idx, float *gates, int32_t *st,
@@ -339,7 +455,16 @@ moe_status gate_dispatch(const void *x, const float *wg, const float *bias, int6
     if (e <= EPV)                                                                           \
         return launch_cfg<GateCfg<EPV, TEV, TTV, NTV, KTV, STV, XT>, XT>(                   \
             x, wg, bias, s, m, e, k, normalize, idx, gates, st, stream);
-    // small e: HBM/latency bound -> few tokens per CTA, long tiles, deep pipeline;
+    // small e whose transposed weight fits in shared memory: one chain per thread
+#define MOE_GATE_SMALL(EPV)                                                                  \
+    if (e <= EPV && (size_t)EPV * (m + 4) * sizeof(float) <= SMALL_E_SMEM_MAX)               \
+        return launch_small<EPV, XT>(x, wg, bias, s, m, e, k, normalize, idx, gates, st, stream);
+    MOE_GATE_SMALL(4)
+    MOE_GATE_SMALL(8)
+    MOE_GATE_SMALL(16)
+    MOE_GATE_SMALL(32)
+#undef MOE_GATE_SMALL
+    // otherwise: HBM/latency bound -> few tokens per CTA, long tiles, deep pipeline;
     // large e: fp32-FMA bound -> register-blocked 8x8 micro-tiles
     MOE_GATE_CASE(4, 4, 1, 64, 128, 4)
     MOE_GATE_CASE(8, 4, 1, 64, 128, 4)
