@@ -7,10 +7,10 @@
 // PR #8195 change 3 (dispatch and combine become a gather each; combine
 // accumulates in fp32).
 //
-// One warp per token.  Lanes r < k hold route r's (expert, slot, gate); the
-// warp then streams the token's row in 16-byte chunks (8 bf16 / 4 fp32 per
-// lane per access), UNR chunks per lane in flight.  Every row access is a full
-// coalesced 512-byte warp transaction.  Combine accumulates each element in
+// One warp per (token, row slice).  Lanes r < k hold route r's (expert, slot,
+// gate); the warp streams its slice of the token's row in 16-byte chunks (8 bf16
+// / 4 fp32 per lane per access).  Every row access is a full coalesced 512-byte
+// warp transaction.  Combine accumulates each element in
 // fp32 in ascending route order, as the C ABI specifies, so results are
 // deterministic and independent of the launch shape.
 #include "common.cuh"
@@ -19,7 +19,8 @@ namespace moe {
 namespace {
 
 constexpr int DNT = 256;  // threads per CTA (8 token-warps)
-constexpr int UNR = 4;    // 16-byte chunks per lane per batch
+constexpr int UNR = 4;    // 16-byte chunks per lane per batch (decode backward)
+constexpr int SL = 64;    // 16-byte chunks of a row per warp (encode, combine): 2 per lane
 constexpr int RG = 4;     // routes whose rows are in flight together in combine
 
 struct Routes {
@@ -56,6 +57,9 @@ __device__ __forceinline__ int read_c(const int32_t *c_dev, int64_t c_max) {
 }
 
 // ---------------------------------------------------------------- encode (K1)
+// Work item = (token, slice of SL 16-byte chunks of its row): one warp per item,
+// so a token row is spread over several warps and every warp needs a single
+// row round trip (the slice is loaded together with the route entries).
 template <typename T>
 __global__ void __launch_bounds__(DNT)
 encode_kernel(const T *__restrict__ x, const int32_t *__restrict__ idx,
@@ -65,32 +69,26 @@ encode_kernel(const T *__restrict__ x, const int32_t *__restrict__ idx,
     if (status_bad(status)) return;
     const int c_eff = read_c(c_dev, c_max);
     const int lane = threadIdx.x & 31;
-    const int64_t nw = (int64_t)gridDim.x * (DNT / 32);
     const int nch = m / Elt<T>::VEC;
-    for (int64_t t = blockIdx.x * (DNT / 32) + (threadIdx.x >> 5); t < s; t += nw) {
+    const int nsl = (nch + SL - 1) / SL;
+    const int64_t items = s * nsl;
+    const int64_t nw = (int64_t)gridDim.x * (DNT / 32);
+    for (int64_t it = blockIdx.x * (DNT / 32) + (threadIdx.x >> 5); it < items; it += nw) {
+        const int64_t t = it / nsl;
+        const int c0 = (int)(it % nsl) * SL + lane;
         const V16 *src = reinterpret_cast<const V16 *>(x + t * m);
-        // the first batch of the token's row is loaded together with its routes
-        V16 v[UNR];
+        V16 v[SL / 32];
 #pragma unroll
-        for (int u = 0; u < UNR; u++)
-            if (lane + 32 * u < nch) v[u] = ld_stream(src + lane + 32 * u);
+        for (int u = 0; u < SL / 32; u++)
+            if (c0 + 32 * u < nch) v[u] = ld_stream(src + c0 + 32 * u);
         Routes R = load_routes(idx, loc, nullptr, s, t, m, e, k, c_eff, c_max, status);
-        if (!R.kept) continue;
-        for (int base = 0; base < nch; base += 32 * UNR) {  // warp-uniform trip count
-            const int q0 = base + lane;
-            if (base > 0) {
+        for (unsigned km = R.kept; km; km &= km - 1) {
+            const int r = __ffs(km) - 1;
+            const int64_t row = __shfl_sync(0xffffffffu, R.row, r);
+            V16 *dst = reinterpret_cast<V16 *>(buf + row);
 #pragma unroll
-                for (int u = 0; u < UNR; u++)
-                    if (q0 + 32 * u < nch) v[u] = ld_stream(src + q0 + 32 * u);
-            }
-            for (unsigned km = R.kept; km; km &= km - 1) {
-                int r = __ffs(km) - 1;
-                int64_t row = __shfl_sync(0xffffffffu, R.row, r);
-                V16 *dst = reinterpret_cast<V16 *>(buf + row);
-#pragma unroll
-                for (int u = 0; u < UNR; u++)
-                    if (q0 + 32 * u < nch) st_v16(dst + q0 + 32 * u, v[u]);
-            }
+            for (int u = 0; u < SL / 32; u++)
+                if (c0 + 32 * u < nch) st_v16(dst + c0 + 32 * u, v[u]);
         }
     }
 }
@@ -126,60 +124,60 @@ combine_kernel(const T *__restrict__ src, const int32_t *__restrict__ idx,
                T *__restrict__ y, int32_t *status) {
     pdl_enter();
     if (status_bad(status)) return;
-    constexpr int VEC = Elt<T>::VEC;
+    constexpr int VEC = Elt<T>::VEC, U = SL / 32;
     const int c_eff = read_c(c_dev, c_max);
     const int lane = threadIdx.x & 31;
-    const int64_t nw = (int64_t)gridDim.x * (DNT / 32);
     const int nch = m / VEC;
-    for (int64_t t = blockIdx.x * (DNT / 32) + (threadIdx.x >> 5); t < s; t += nw) {
+    const int nsl = (nch + SL - 1) / SL;
+    const int64_t items = s * nsl;
+    const int64_t nw = (int64_t)gridDim.x * (DNT / 32);
+    for (int64_t it = blockIdx.x * (DNT / 32) + (threadIdx.x >> 5); it < items; it += nw) {
+        const int64_t t = it / nsl;
+        const int c0 = (int)(it % nsl) * SL + lane;
         Routes R = load_routes(idx, loc, WEIGHTED ? gates : nullptr, s, t, m, e, k, c_eff, c_max,
                                status);
-        V16 *dst = reinterpret_cast<V16 *>(y + t * m);
-        for (int base = 0; base < nch; base += 32 * UNR) {  // warp-uniform trip count
-            const int q0 = base + lane;
-            float acc[UNR][VEC];
+        float acc[U][VEC];
 #pragma unroll
-            for (int u = 0; u < UNR; u++)
+        for (int u = 0; u < U; u++)
 #pragma unroll
-                for (int i = 0; i < VEC; i++) acc[u][i] = 0.0f;
-            // routes in ascending order, RG at a time: every row load of a group is
-            // in flight before the group's fused multiply-adds (same order as one
-            // route at a time)
-            for (int rg = 0; rg < k; rg += RG) {
-                const unsigned gm = (R.kept >> rg) & ((1u << RG) - 1u);
-                if (!gm) continue;
-                V16 v[RG][UNR];
-                float g[RG];
+            for (int i = 0; i < VEC; i++) acc[u][i] = 0.0f;
+        // routes in ascending order, RG at a time: every row load of a group is in
+        // flight before the group's fused multiply-adds (same order as one at a time)
+        for (int rg = 0; rg < k; rg += RG) {
+            const unsigned gm = (R.kept >> rg) & ((1u << RG) - 1u);
+            if (!gm) continue;
+            V16 v[RG][U];
+            float g[RG];
 #pragma unroll
-                for (int rr = 0; rr < RG; rr++) {
-                    g[rr] = 0.0f;
-                    if ((gm >> rr) & 1u) {
-                        const int64_t row = __shfl_sync(0xffffffffu, R.row, rg + rr);
-                        g[rr] = WEIGHTED ? __shfl_sync(0xffffffffu, R.g, rg + rr) : 1.0f;
-                        const V16 *sp = reinterpret_cast<const V16 *>(src + row);
+            for (int rr = 0; rr < RG; rr++) {
+                g[rr] = 0.0f;
+                if ((gm >> rr) & 1u) {
+                    const int64_t row = __shfl_sync(0xffffffffu, R.row, rg + rr);
+                    g[rr] = WEIGHTED ? __shfl_sync(0xffffffffu, R.g, rg + rr) : 1.0f;
+                    const V16 *sp = reinterpret_cast<const V16 *>(src + row);
 #pragma unroll
-                        for (int u = 0; u < UNR; u++)
-                            if (q0 + 32 * u < nch) v[rr][u] = ld_stream(sp + q0 + 32 * u);
-                    }
-                }
-#pragma unroll
-                for (int rr = 0; rr < RG; rr++) {
-                    if (!((gm >> rr) & 1u)) continue;
-#pragma unroll
-                    for (int u = 0; u < UNR; u++) {
-                        float f[VEC];
-                        Elt<T>::unpack(v[rr][u], f);
-#pragma unroll
-                        for (int i = 0; i < VEC; i++)
-                            acc[u][i] = WEIGHTED ? __fmaf_rn(g[rr], f[i], acc[u][i])
-                                                 : __fadd_rn(acc[u][i], f[i]);
-                    }
+                    for (int u = 0; u < U; u++)
+                        if (c0 + 32 * u < nch) v[rr][u] = ld_stream(sp + c0 + 32 * u);
                 }
             }
 #pragma unroll
-            for (int u = 0; u < UNR; u++)
-                if (q0 + 32 * u < nch) st_v16_cs(dst + q0 + 32 * u, Elt<T>::pack(acc[u]));
+            for (int rr = 0; rr < RG; rr++) {
+                if (!((gm >> rr) & 1u)) continue;
+#pragma unroll
+                for (int u = 0; u < U; u++) {
+                    float f[VEC];
+                    Elt<T>::unpack(v[rr][u], f);
+#pragma unroll
+                    for (int i = 0; i < VEC; i++)
+                        acc[u][i] = WEIGHTED ? __fmaf_rn(g[rr], f[i], acc[u][i])
+                                             : __fadd_rn(acc[u][i], f[i]);
+                }
+            }
         }
+        V16 *dst = reinterpret_cast<V16 *>(y + t * m);
+#pragma unroll
+        for (int u = 0; u < U; u++)
+            if (c0 + 32 * u < nch) st_v16_cs(dst + c0 + 32 * u, Elt<T>::pack(acc[u]));
     }
 }
 
@@ -270,13 +268,31 @@ decode_bwd_kernel(const T *__restrict__ dy, const T *__restrict__ out,
     }
 }
 
-int grid_for_tokens(int64_t s) {
-    int dev = 0, sms = 148;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    int64_t want = (s + (DNT / 32) - 1) / (DNT / 32);
-    int64_t cap = (int64_t)sms * 8;  // 8 CTAs x 8 warps per SM: 64 warps resident
-    return (int)(want < cap ? want : cap);
+int sm_count_cached() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = v > 0 ? v : 148;
+    }
+    return cached[dev];
+}
+
+// CTAs for `items` one-warp work items: one item per warp, at most 8 CTAs x 8
+// warps (64 warps) resident per SM; larger batches loop.
+int grid_for_items(int64_t items) {
+    int64_t want = (items + (DNT / 32) - 1) / (DNT / 32);
+    int64_t cap = (int64_t)sm_count_cached() * 8;
+    return (int)(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
+int grid_for_tokens(int64_t s) { return grid_for_items(s); }
+
+int64_t row_slices(int m, moe_dtype dt) {
+    const int nch = m / (dt == MOE_BF16 ? 8 : 4);
+    return (nch + SL - 1) / SL;
 }
 
 }  // namespace
@@ -285,7 +301,7 @@ moe_status encode_launch(const void *x, moe_dtype dt, const int32_t *idx, const 
                          const int32_t *counts, const int32_t *c_dev, int64_t s, int m, int e,
                          int k, int64_t c_max, unsigned flags, void *buf, int32_t *st,
                          cudaStream_t stream) {
-    const int grid = grid_for_tokens(s);
+    const int grid = grid_for_items(s * row_slices(m, dt));
     moe_status r;
     if (dt == MOE_BF16)
         r = launch_pdl(encode_kernel<__nv_bfloat16>, dim3(grid), dim3(DNT), 0, stream,
@@ -312,7 +328,7 @@ moe_status encode_launch(const void *x, moe_dtype dt, const int32_t *idx, const 
 moe_status combine_launch(const void *src, moe_dtype dt, const int32_t *idx, const int32_t *loc,
                           const float *gates, const int32_t *c_dev, int64_t s, int m, int e, int k,
                           int64_t c_max, void *y, int32_t *st, cudaStream_t stream) {
-    const int grid = grid_for_tokens(s);
+    const int grid = grid_for_items(s * row_slices(m, dt));
     const bool w = gates != nullptr;
     const dim3 g(grid), b(DNT);
     const float *gp = gates;

@@ -334,9 +334,22 @@ gate_small_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
     constexpr int VEC = Elt<XT>::VEC;
     constexpr int PD = 4;
     const int ld = m + 4;
-    for (int q = threadIdx.x; q < m * EP; q += blockDim.x) {
-        const int i = q / EP, j = q % EP;
-        wt[j * ld + i] = j < e ? wg[(int64_t)i * e + j] : 0.0f;
+    {   // stage the transposed weight: 8 independent loads in flight per thread
+        constexpr int B = 8;
+        const int total = m * EP;
+        for (int q0 = threadIdx.x; q0 < total; q0 += B * 256) {
+            float v[B];
+#pragma unroll
+            for (int b = 0; b < B; b++) {
+                const int q = q0 + b * 256, i = q / EP, j = q % EP;
+                v[b] = (q < total && j < e) ? __ldg(wg + (int64_t)i * e + j) : 0.0f;
+            }
+#pragma unroll
+            for (int b = 0; b < B; b++) {
+                const int q = q0 + b * 256;
+                if (q < total) wt[(q % EP) * ld + q / EP] = v[b];
+            }
+        }
     }
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
