@@ -7,7 +7,7 @@
 // PR #8195 change 3 (dispatch and combine become a gather each; combine
 // accumulates in fp32).
 //
-// One warp per (token, row slice).  Lanes r < k hold route r's (expert, slot,
+// One warp per (token, row slice of up to 2 KB).  Lanes r < k hold route r's (expert, slot,
 // gate); the warp streams its slice of the token's row in 16-byte chunks (8 bf16
 // / 4 fp32 per lane per access).  Every row access is a full coalesced 512-byte
 // warp transaction.  Combine accumulates each element in
@@ -20,8 +20,8 @@ namespace {
 
 constexpr int DNT = 256;  // threads per CTA (8 token-warps)
 constexpr int UNR = 4;    // 16-byte chunks per lane per batch (decode backward)
-constexpr int SL = 64;    // 16-byte chunks of a row per warp (encode, combine): 2 per lane
-constexpr int RG = 4;     // routes whose rows are in flight together in combine
+constexpr int SL = 128;   // 16-byte chunks of a row per warp (encode, combine): 4 per lane
+constexpr int RG = 2;     // routes whose rows are in flight together in combine
 
 struct Routes {
     unsigned kept;   // bit r: route r of this token is kept

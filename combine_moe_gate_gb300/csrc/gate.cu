@@ -317,12 +317,26 @@ gate_topk_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
 
 // ---------------------------------------------------------------- small e
 // One thread per (token, expert) for e <= 32: the logit's single accumulator
-// walks the features in ascending order (the contract above) with no blocking
-// at all, so the whole batch runs as s*e independent chains in s*e/32 warps.
-// The transposed gate weight [EP][m + 4] sits in shared memory (the +4 keeps the
-// 16-byte reads of different experts on different banks); x is streamed with
-// 16-byte loads kept PD chunks ahead.  Softmax and top-k run on the EP lanes
-// of each token with segmented shuffles.
+// walks the features in ascending order (the contract above) with no blocking,
+// so the batch runs as s*e independent chains.  The transposed gate weight
+// [EP][m + 4] sits in shared memory (the +4 keeps 16-byte reads of different
+// experts on different banks).  x reaches shared memory through a SK-deep
+// cp.async ring of KS-feature tiles of the CTA's TPB tokens, so that a whole
+// ring of x (not just a few registers per thread) is in flight against HBM
+// latency; the EP threads of a token read its features with broadcast loads.
+// (KS below: features per tile, 512 bytes of each token row.)
+// Softmax and top-k run on the EP lanes of each token with segmented shuffles.
+constexpr int SK = 4;    // x tiles in flight
+
+template <int EP, typename XT>
+struct SmallCfg {
+    static constexpr int KS = 512 / (int)sizeof(XT);             // features per x tile (512 B rows)
+    static constexpr int TPB = (256 / 32) * (32 / EP);           // tokens per CTA
+    static constexpr int XROWB = 512 + 16;                       // padded x tile row (bytes)
+    static constexpr int XBYTES = SK * TPB * XROWB;              // x ring
+    static_assert(XBYTES <= 140 * 1024, "x ring");
+};
+
 template <int EP, typename XT>
 __global__ void __launch_bounds__(256)
 gate_small_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
@@ -330,10 +344,32 @@ gate_small_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
                   int32_t *__restrict__ idx, float *__restrict__ gates, int32_t *status) {
     pdl_enter();
     if (status_bad(status)) return;
-    extern __shared__ __align__(16) float wt[];  // [EP][m + 4]
-    constexpr int VEC = Elt<XT>::VEC;
-    constexpr int PD = 4;
+    using SC = SmallCfg<EP, XT>;
+    constexpr int VEC = Elt<XT>::VEC, KS = SC::KS;
+    constexpr int CPR = KS / VEC;   // 16-byte chunks per token row per tile
+    extern __shared__ __align__(16) unsigned char smem_small[];
+    unsigned char *xs = smem_small;                          // [SK][TPB][XROWB]
+    float *wt = reinterpret_cast<float *>(smem_small + SC::XBYTES);  // [EP][m + 4]
     const int ld = m + 4;
+    const int64_t t0 = (int64_t)blockIdx.x * SC::TPB;
+    const int ntiles = (m + KS - 1) / KS;
+    auto load_x = [&](int tile) {
+        unsigned char *dst = xs + (tile % SK) * SC::TPB * SC::XROWB;
+        for (int q = threadIdx.x; q < SC::TPB * CPR; q += 256) {
+            const int row = q / CPR, ch = q % CPR;
+            const int64_t t = t0 + row;
+            const int f = tile * KS + ch * VEC;
+            const bool ok = t < s && f < m;
+            cp_async16(dst + row * SC::XROWB + ch * 16, ok ? (const void *)(x + t * m + f) : (const void *)x,
+                       ok);
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int p = 0; p < SK - 1; p++) {
+        if (p < ntiles) load_x(p);
+        else cp_async_commit();
+    }
     {   // stage the transposed weight: 8 independent loads in flight per thread
         constexpr int B = 8;
         const int total = m * EP;
@@ -351,44 +387,36 @@ gate_small_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
             }
         }
     }
-    __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int TPW = 32 / EP;
     const int j = lane % EP;
-    const int64_t t = ((int64_t)blockIdx.x * (blockDim.x / 32) + warp) * TPW + lane / EP;
+    const int tl = warp * TPW + lane / EP;       // token within the CTA
+    const int64_t t = t0 + tl;
     const bool live = t < s;
-    const XT *xr = x + (live ? t : 0) * (int64_t)m;
     const float *wr = wt + j * ld;
-    const int nch = m / VEC;
     float acc = 0.0f;
-    V16 cur[PD];
+    for (int it = 0; it < ntiles; it++) {
+        cp_async_wait<SK - 2>();
+        __syncthreads();   // tile `it` landed (and the weight staged); tile it-1 fully read
+        if (it + SK - 1 < ntiles) load_x(it + SK - 1);
+        else cp_async_commit();
+        const unsigned char *xr = xs + (it % SK) * SC::TPB * SC::XROWB + tl * SC::XROWB;
+        const int nfeat = min(KS, m - it * KS);
+        const float *w = wr + it * KS;
+        for (int c = 0; c < nfeat / VEC; c++) {
+            float f[VEC];
+            Elt<XT>::unpack(*reinterpret_cast<const V16 *>(xr + c * 16), f);
 #pragma unroll
-    for (int p = 0; p < PD; p++)
-        if (p < nch) cur[p] = ld_stream(xr + p * VEC);
-    for (int c0 = 0; c0 < nch; c0 += PD) {
-        V16 nxt[PD];
-#pragma unroll
-        for (int p = 0; p < PD; p++)
-            if (c0 + PD + p < nch) nxt[p] = ld_stream(xr + (c0 + PD + p) * VEC);
-#pragma unroll
-        for (int p = 0; p < PD; p++) {
-            if (c0 + p < nch) {
-                float f[VEC];
-                Elt<XT>::unpack(cur[p], f);
-                const float *w = wr + (c0 + p) * VEC;
-#pragma unroll
-                for (int u = 0; u < VEC; u += 4) {
-                    const float4 w4 = *reinterpret_cast<const float4 *>(w + u);
-                    acc = fmaf(f[u], w4.x, acc);
-                    acc = fmaf(f[u + 1], w4.y, acc);
-                    acc = fmaf(f[u + 2], w4.z, acc);
-                    acc = fmaf(f[u + 3], w4.w, acc);
-                }
+            for (int u = 0; u < VEC; u += 4) {
+                const float4 w4 = *reinterpret_cast<const float4 *>(w + c * VEC + u);
+                acc = fmaf(f[u], w4.x, acc);
+                acc = fmaf(f[u + 1], w4.y, acc);
+                acc = fmaf(f[u + 2], w4.z, acc);
+                acc = fmaf(f[u + 3], w4.w, acc);
             }
         }
-#pragma unroll
-        for (int p = 0; p < PD; p++) cur[p] = nxt[p];
     }
+    cp_async_wait<0>();
     float v = -INFINITY;
     if (j < e) v = bias ? acc + bias[j] : acc;
     // segmented (EP lanes per token) softmax statistics
@@ -429,12 +457,12 @@ moe_status launch_small(const void *x, const float *wg, const float *bias, int64
                         int k, int normalize, int32_t *idx, float *gates, int32_t *st,
                         cudaStream_t stream) {
     auto kern = gate_small_kernel<EP, XT>;
-    const size_t smem = (size_t)EP * (m + 4) * sizeof(float);
+    const size_t smem = SmallCfg<EP, XT>::XBYTES + (size_t)EP * (m + 4) * sizeof(float);
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
         return MOE_ERR_CUDA;
-    constexpr int TPB = (256 / 32) * (32 / EP);  // tokens per CTA
+    constexpr int TPB = SmallCfg<EP, XT>::TPB;
     const int64_t grid = (s + TPB - 1) / TPB;
     if (grid > 0x7fffffff) return MOE_ERR_UNSUPPORTED;
     return launch_pdl(kern, dim3((unsigned)grid), dim3(256), smem, stream, (const XT *)x, wg, bias, s,
@@ -457,7 +485,7 @@ moe_status launch_cfg(const void *x, const float *wg, const float *bias, int64_t
                       bias, s, m, e, k, normalize, idx, gates, st);
 }
 
-// Shared memory the small-e kernel needs for the transposed gate weight.
+// Shared memory the small-e kernel may use for the transposed gate weight.
 constexpr size_t SMALL_E_SMEM_MAX = 64 * 1024;
 
 template <typename XT>
