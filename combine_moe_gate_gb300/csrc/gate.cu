@@ -318,14 +318,13 @@ gate_topk_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
 // ---------------------------------------------------------------- small e
 // One thread per (token, expert) for e <= 32: the logit's single accumulator
 // walks the features in ascending order (the contract above) with no blocking,
-// so the batch runs as s*e independent chains.  The transposed gate weight
-// [EP][m + 4] sits in shared memory (the +4 keeps 16-byte reads of different
-// experts on different banks).  x reaches shared memory through a SK-deep
-// cp.async ring of KS-feature tiles of the CTA's TPB tokens, so that a whole
-// ring of x (not just a few registers per thread) is in flight against HBM
-// latency; the EP threads of a token read its features with broadcast loads.
-// (KS below: features per tile, 512 bytes of each token row.)
-// Softmax and top-k run on the EP lanes of each token with segmented shuffles.
+// so the batch runs as s*e independent chains.  The gate weight [m][e] is copied
+// whole into shared memory (the e threads of a token read consecutive words);
+// x reaches shared memory through a SK-deep cp.async ring of tiles of the CTA's
+// TPB tokens, so that a whole ring of x (not just a few registers per thread) is
+// in flight against HBM latency; the threads of a token read its features with
+// broadcast loads.  Softmax and top-k run on the EP lanes of each token with
+// segmented shuffles.  (KS below: features per tile, 512 bytes of each row.)
 constexpr int SK = 4;    // x tiles in flight
 
 template <int EP, typename XT>
@@ -349,8 +348,7 @@ gate_small_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
     constexpr int CPR = KS / VEC;   // 16-byte chunks per token row per tile
     extern __shared__ __align__(16) unsigned char smem_small[];
     unsigned char *xs = smem_small;                          // [SK][TPB][XROWB]
-    float *wt = reinterpret_cast<float *>(smem_small + SC::XBYTES);  // [EP][m + 4]
-    const int ld = m + 4;
+    float *wt = reinterpret_cast<float *>(smem_small + SC::XBYTES);  // [m][e]
     const int64_t t0 = (int64_t)blockIdx.x * SC::TPB;
     const int ntiles = (m + KS - 1) / KS;
     auto load_x = [&](int tile) {
@@ -370,22 +368,15 @@ gate_small_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
         if (p < ntiles) load_x(p);
         else cp_async_commit();
     }
-    {   // stage the transposed weight: 8 independent loads in flight per thread
-        constexpr int B = 8;
-        const int total = m * EP;
-        for (int q0 = threadIdx.x; q0 < total; q0 += B * 256) {
-            float v[B];
-#pragma unroll
-            for (int b = 0; b < B; b++) {
-                const int q = q0 + b * 256, i = q / EP, j = q % EP;
-                v[b] = (q < total && j < e) ? __ldg(wg + (int64_t)i * e + j) : 0.0f;
-            }
-#pragma unroll
-            for (int b = 0; b < B; b++) {
-                const int q = q0 + b * 256;
-                if (q < total) wt[(q % EP) * ld + q / EP] = v[b];
-            }
+    {   // the gate weight, [m][e] as in global memory, copied in one go
+        const int total = m * e;
+        if ((e & 3) == 0) {
+            for (int q = threadIdx.x * 4; q < total; q += 256 * 4)
+                cp_async16(wt + q, wg + q, true);
+        } else {
+            for (int q = threadIdx.x; q < total; q += 256) cp_async4(wt + q, wg + q, true);
         }
+        cp_async_commit();
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int TPW = 32 / EP;
@@ -393,27 +384,22 @@ gate_small_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
     const int tl = warp * TPW + lane / EP;       // token within the CTA
     const int64_t t = t0 + tl;
     const bool live = t < s;
-    const float *wr = wt + j * ld;
+    const float *wr = wt + (j < e ? j : 0);
     float acc = 0.0f;
     for (int it = 0; it < ntiles; it++) {
-        cp_async_wait<SK - 2>();
+        if (it == 0) cp_async_wait<0>();   // the weight (committed after the x prologue) and tile 0
+        else cp_async_wait<SK - 2>();
         __syncthreads();   // tile `it` landed (and the weight staged); tile it-1 fully read
         if (it + SK - 1 < ntiles) load_x(it + SK - 1);
         else cp_async_commit();
         const unsigned char *xr = xs + (it % SK) * SC::TPB * SC::XROWB + tl * SC::XROWB;
         const int nfeat = min(KS, m - it * KS);
-        const float *w = wr + it * KS;
+        const float *w = wr + (int64_t)it * KS * e;
         for (int c = 0; c < nfeat / VEC; c++) {
             float f[VEC];
             Elt<XT>::unpack(*reinterpret_cast<const V16 *>(xr + c * 16), f);
 #pragma unroll
-            for (int u = 0; u < VEC; u += 4) {
-                const float4 w4 = *reinterpret_cast<const float4 *>(w + c * VEC + u);
-                acc = fmaf(f[u], w4.x, acc);
-                acc = fmaf(f[u + 1], w4.y, acc);
-                acc = fmaf(f[u + 2], w4.z, acc);
-                acc = fmaf(f[u + 3], w4.w, acc);
-            }
+            for (int u = 0; u < VEC; u++) acc = fmaf(f[u], w[(c * VEC + u) * e], acc);
         }
     }
     cp_async_wait<0>();
@@ -457,7 +443,7 @@ moe_status launch_small(const void *x, const float *wg, const float *bias, int64
                         int k, int normalize, int32_t *idx, float *gates, int32_t *st,
                         cudaStream_t stream) {
     auto kern = gate_small_kernel<EP, XT>;
-    const size_t smem = SmallCfg<EP, XT>::XBYTES + (size_t)EP * (m + 4) * sizeof(float);
+    const size_t smem = SmallCfg<EP, XT>::XBYTES + (size_t)m * e * sizeof(float);
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
@@ -498,7 +484,7 @@ moe_status gate_dispatch(const void *x, const float *wg, const float *bias, int6
             x, wg, bias, s, m, e, k, normalize, idx, gates, st, stream);
     // small e whose transposed weight fits in shared memory: one chain per thread
 #define MOE_GATE_SMALL(EPV)                                                                  \
-    if (e <= EPV && (size_t)EPV * (m + 4) * sizeof(float) <= SMALL_E_SMEM_MAX)               \
+    if (e <= EPV && (size_t)m * e * sizeof(float) <= SMALL_E_SMEM_MAX)                       \
         return launch_small<EPV, XT>(x, wg, bias, s, m, e, k, normalize, idx, gates, st, stream);
     MOE_GATE_SMALL(4)
     MOE_GATE_SMALL(8)
