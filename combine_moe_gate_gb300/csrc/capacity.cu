@@ -8,8 +8,8 @@
 // route is its rank among the routes that chose the same expert, so the flat
 // route-major table [k, s] is ranked in its natural order.
 //
-// Small tables (up to 16384 routes, e <= 256) take one single-CTA launch;
-// otherwise two launches, no inter-CTA waiting:
+// Small tables (up to 16384 routes, e <= 256) take one launch of up to 16 CTAs
+// (cap_small_kernel); otherwise two launches, no inter-CTA waiting:
 //   1. cap_hist: CTA b counts the experts of its chunk of CH routes -> hist[b][e].
 //   2. cap_assign: CTA b sums hist[0..b-1][j] for its base offsets, ranks its
 //      chunk stably (warps take consecutive segments; inside a warp
@@ -130,37 +130,59 @@ cap_assign_kernel(const int32_t *__restrict__ idx, int64_t n, int e, int nblk,
     }
 }
 
-// Single-CTA path for small route tables (n <= 32 warps x 32 lanes x R routes,
-// e <= 256): one launch, no histogram pass.  Warp w ranks the contiguous
-// segment [w*32R, (w+1)*32R) stably; an exclusive prefix over warps per expert
-// gives the base offsets, the totals give counts[] and c.
-constexpr int CAP1_NT = 1024, CAP1_NW = 32, CAP1_MAXE = 256;
+// Small route tables (n <= 16 chunks of CAPS_CH routes, e <= 256): one launch
+// of ceil(n / CAPS_CH) CTAs with no inter-CTA waiting.  CTA b histograms the
+// routes of all earlier chunks itself (redundant, but at most 15 chunks) for
+// its base offsets, then ranks its own chunk stably as cap_assign does.  The
+// last CTA, which has seen every route, writes counts[], c and the overflow
+// status.
+constexpr int CAPS_NT = 256, CAPS_NW = CAPS_NT / 32, CAPS_CH = 1024, CAPS_MAXE = 256;
+constexpr int CAPS_ROUNDS = CAPS_CH / CAPS_NT;   // routes per thread (own chunk)
+constexpr int CAPS_MAXBLK = 16;
 
-template <int R>
-__global__ void __launch_bounds__(CAP1_NT)
-cap_single_kernel(const int32_t *__restrict__ idx, int64_t n, int e, int c_fixed, int c_cap,
-                  int64_t c_max, int32_t *__restrict__ loc, int32_t *__restrict__ counts,
-                  int32_t *__restrict__ c_dev, int32_t *status) {
+__global__ void __launch_bounds__(CAPS_NT)
+cap_small_kernel(const int32_t *__restrict__ idx, int64_t n, int e, int c_fixed, int c_cap,
+                 int64_t c_max, int32_t *__restrict__ loc, int32_t *__restrict__ counts,
+                 int32_t *__restrict__ c_dev, int32_t *status) {
     pdl_enter();
     if (status_bad(status)) return;
-    __shared__ int32_t wcnt[CAP1_NW][CAP1_MAXE];
-    __shared__ int32_t s_max;
+    __shared__ int32_t base[CAPS_MAXE];
+    __shared__ int32_t wcnt[CAPS_NW][CAPS_MAXE];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int q = tid; q < CAP1_NW * CAP1_MAXE; q += CAP1_NT) (&wcnt[0][0])[q] = 0;
-    if (tid == 0) s_max = 0;
-    const int64_t seg0 = (int64_t)warp * 32 * R;
-    int32_t val[R], rank[R];
+    for (int q = tid; q < CAPS_MAXE; q += CAPS_NT) base[q] = 0;
+    for (int q = tid; q < CAPS_NW * CAPS_MAXE; q += CAPS_NT) (&wcnt[0][0])[q] = 0;
+    // own chunk: warp w takes routes [w*128, (w+1)*128) of it, 4 rounds of 32
+    const int64_t seg0 = (int64_t)blockIdx.x * CAPS_CH + warp * 32 * CAPS_ROUNDS;
+    int32_t val[CAPS_ROUNDS], rank[CAPS_ROUNDS];
 #pragma unroll
-    for (int rd = 0; rd < R; rd++) {
+    for (int rd = 0; rd < CAPS_ROUNDS; rd++) {
         const int64_t j = seg0 + rd * 32 + lane;
         const int v = j < n ? __ldg(idx + j) : -1;
         if (j < n && (unsigned)v >= (unsigned)e) set_status(status, MOE_ERR_INVALID_ARG);
         val[rd] = (unsigned)v < (unsigned)e ? v : -1;
     }
     __syncthreads();
+    // earlier chunks: warp-aggregated histogram into base[]
+    const int64_t pre = (int64_t)blockIdx.x * CAPS_CH;
+    for (int64_t q0 = 0; q0 < pre; q0 += CAPS_NT * 8) {
+        int v8[8];
+#pragma unroll
+        for (int b = 0; b < 8; b++) {
+            const int64_t q = q0 + b * CAPS_NT + tid;
+            const int v = q < pre ? __ldg(idx + q) : -1;
+            v8[b] = (unsigned)v < (unsigned)e ? v : -1;
+        }
+#pragma unroll
+        for (int b = 0; b < 8; b++) {
+            const unsigned peers = __match_any_sync(0xffffffffu, v8[b]);
+            if (v8[b] >= 0 && (peers & ((1u << lane) - 1u)) == 0)
+                atomicAdd(&base[v8[b]], __popc(peers));
+        }
+    }
+    // own chunk: stable ranks inside each warp's segment
     const unsigned lt = (1u << lane) - 1u;
 #pragma unroll
-    for (int rd = 0; rd < R; rd++) {
+    for (int rd = 0; rd < CAPS_ROUNDS; rd++) {
         const int v = val[rd];
         const unsigned peers = __match_any_sync(0xffffffffu, v);
         const int prev = v >= 0 ? wcnt[warp][v] : 0;
@@ -170,24 +192,30 @@ cap_single_kernel(const int32_t *__restrict__ idx, int64_t n, int e, int c_fixed
         rank[rd] = prev + __popc(peers & lt);
     }
     __syncthreads();
-    for (int x = tid; x < e; x += CAP1_NT) {
-        int32_t run = 0;
-        for (int w = 0; w < CAP1_NW; w++) {
+    const bool last = blockIdx.x == gridDim.x - 1;
+    __shared__ int32_t s_max;
+    if (tid == 0) s_max = 0;
+    __syncthreads();
+    for (int x = tid; x < e; x += CAPS_NT) {
+        int32_t run = base[x];
+        for (int w = 0; w < CAPS_NW; w++) {
             const int32_t c = wcnt[w][x];
             wcnt[w][x] = run;
             run += c;
         }
-        counts[x] = run;
-        atomicMax(&s_max, run);
+        if (last) {
+            counts[x] = run;
+            atomicMax(&s_max, run);
+        }
     }
     __syncthreads();
-    if (tid == 0) {
+    if (last && tid == 0) {
         const int c = c_fixed >= 0 ? c_fixed : min(c_cap, s_max);
         c_dev[0] = c;
         if ((int64_t)c > c_max) set_status(status, MOE_ERR_CAPACITY);
     }
 #pragma unroll
-    for (int rd = 0; rd < R; rd++) {
+    for (int rd = 0; rd < CAPS_ROUNDS; rd++) {
         const int64_t j = seg0 + rd * 32 + lane;
         if (j < n && val[rd] >= 0) loc[j] = wcnt[warp][val[rd]] + rank[rd];
     }
@@ -230,17 +258,10 @@ moe_status capacity_launch(const int32_t *idx, int64_t s, int e, int k, float f,
         int64_t c = capacity_bound_host(f, s, e, k);
         c_cap = (int)c;
     }
-    if (e <= CAP1_MAXE && n <= (int64_t)CAP1_NW * 32 * 16) {
-#define MOE_CAP1(RV)                                                                               \
-        if (n <= (int64_t)CAP1_NW * 32 * RV)                                                       \
-            return launch_pdl(cap_single_kernel<RV>, dim3(1), dim3(CAP1_NT), 0, stream, idx, n, e,  \
-                              c_fixed, c_cap, c_max, loc, counts, c_dev, st);
-        MOE_CAP1(1)
-        MOE_CAP1(2)
-        MOE_CAP1(4)
-        MOE_CAP1(8)
-        MOE_CAP1(16)
-#undef MOE_CAP1
+    if (e <= CAPS_MAXE && n <= (int64_t)CAPS_CH * CAPS_MAXBLK) {
+        const unsigned nb = (unsigned)((n + CAPS_CH - 1) / CAPS_CH);
+        return launch_pdl(cap_small_kernel, dim3(nb), dim3(CAPS_NT), 0, stream, idx, n, e, c_fixed,
+                          c_cap, c_max, loc, counts, c_dev, st);
     }
     int32_t *hist = (int32_t *)ws;
     if (launch_pdl(cap_hist_kernel, dim3((unsigned)nblk), dim3(CAP_NT), e * sizeof(int32_t), stream,

@@ -20,8 +20,7 @@ namespace {
 
 constexpr int DNT = 256;  // threads per CTA (8 token-warps)
 constexpr int UNR = 4;    // 16-byte chunks per lane per batch (decode backward)
-constexpr int SL = 128;   // 16-byte chunks of a row per warp (encode, combine): 4 per lane
-constexpr int RG = 2;     // routes whose rows are in flight together in combine
+constexpr int SL = 128;   // 16-byte chunks of a row per warp in encode: 4 per lane
 
 struct Routes {
     unsigned kept;   // bit r: route r of this token is kept
@@ -61,7 +60,7 @@ __device__ __forceinline__ int read_c(const int32_t *c_dev, int64_t c_max) {
 // so a token row is spread over several warps and every warp needs a single
 // row round trip (the slice is loaded together with the route entries).
 template <typename T>
-__global__ void __launch_bounds__(DNT)
+__global__ void __launch_bounds__(DNT, 4)
 encode_kernel(const T *__restrict__ x, const int32_t *__restrict__ idx,
               const int32_t *__restrict__ loc, const int32_t *__restrict__ c_dev, int64_t s,
               int m, int e, int k, int64_t c_max, T *__restrict__ buf, int32_t *status) {
@@ -116,40 +115,47 @@ zero_fill_kernel(const int32_t *__restrict__ counts, const int32_t *__restrict__
 
 // ------------------------------------------------ combine: decode (K0) and
 // encode backward (K0 with unit weights)
-template <typename T, bool WEIGHTED>
-__global__ void __launch_bounds__(DNT)
+// U: 16-byte chunks per lane (slice = 32*U chunks).  RGK: routes whose row
+// loads are in flight together.  ONE: every route fits in one group (k <= RGK),
+// so each chunk is finished (all routes, ascending) before the next one and
+// only VEC accumulators are live.
+template <typename T, bool WEIGHTED, int U, int RGK, bool ONE>
+__global__ void __launch_bounds__(DNT, 4)
 combine_kernel(const T *__restrict__ src, const int32_t *__restrict__ idx,
                const int32_t *__restrict__ loc, const float *__restrict__ gates,
                const int32_t *__restrict__ c_dev, int64_t s, int m, int e, int k, int64_t c_max,
                T *__restrict__ y, int32_t *status) {
     pdl_enter();
     if (status_bad(status)) return;
-    constexpr int VEC = Elt<T>::VEC, U = SL / 32;
+    constexpr int VEC = Elt<T>::VEC, SLU = 32 * U;
     const int c_eff = read_c(c_dev, c_max);
     const int lane = threadIdx.x & 31;
     const int nch = m / VEC;
-    const int nsl = (nch + SL - 1) / SL;
+    const int nsl = (nch + SLU - 1) / SLU;
     const int64_t items = s * nsl;
     const int64_t nw = (int64_t)gridDim.x * (DNT / 32);
     for (int64_t it = blockIdx.x * (DNT / 32) + (threadIdx.x >> 5); it < items; it += nw) {
         const int64_t t = it / nsl;
-        const int c0 = (int)(it % nsl) * SL + lane;
+        const int c0 = (int)(it % nsl) * SLU + lane;
         Routes R = load_routes(idx, loc, WEIGHTED ? gates : nullptr, s, t, m, e, k, c_eff, c_max,
                                status);
-        float acc[U][VEC];
+        V16 *dst = reinterpret_cast<V16 *>(y + t * m);
+        float acc[ONE ? 1 : U][VEC];
+        if (!ONE) {
 #pragma unroll
-        for (int u = 0; u < U; u++)
+            for (int u = 0; u < (ONE ? 1 : U); u++)
 #pragma unroll
-            for (int i = 0; i < VEC; i++) acc[u][i] = 0.0f;
-        // routes in ascending order, RG at a time: every row load of a group is in
-        // flight before the group's fused multiply-adds (same order as one at a time)
-        for (int rg = 0; rg < k; rg += RG) {
-            const unsigned gm = (R.kept >> rg) & ((1u << RG) - 1u);
-            if (!gm) continue;
-            V16 v[RG][U];
-            float g[RG];
+                for (int i = 0; i < VEC; i++) acc[u][i] = 0.0f;
+        }
+        // routes in ascending order, RGK at a time: every row load of a group is
+        // in flight before the group's fused multiply-adds
+        for (int rg = 0; rg < k; rg += RGK) {
+            const unsigned gm = (R.kept >> rg) & ((1u << RGK) - 1u);
+            if (!ONE && !gm) continue;
+            V16 v[RGK][U];
+            float g[RGK];
 #pragma unroll
-            for (int rr = 0; rr < RG; rr++) {
+            for (int rr = 0; rr < RGK; rr++) {
                 g[rr] = 0.0f;
                 if ((gm >> rr) & 1u) {
                     const int64_t row = __shfl_sync(0xffffffffu, R.row, rg + rr);
@@ -161,23 +167,31 @@ combine_kernel(const T *__restrict__ src, const int32_t *__restrict__ idx,
                 }
             }
 #pragma unroll
-            for (int rr = 0; rr < RG; rr++) {
-                if (!((gm >> rr) & 1u)) continue;
+            for (int u = 0; u < U; u++) {
+                float a1[VEC];
+                float *a = ONE ? a1 : acc[ONE ? 0 : u];
+                if (ONE) {
 #pragma unroll
-                for (int u = 0; u < U; u++) {
+                    for (int i = 0; i < VEC; i++) a1[i] = 0.0f;
+                }
+#pragma unroll
+                for (int rr = 0; rr < RGK; rr++) {
+                    if (!((gm >> rr) & 1u)) continue;
                     float f[VEC];
                     Elt<T>::unpack(v[rr][u], f);
 #pragma unroll
                     for (int i = 0; i < VEC; i++)
-                        acc[u][i] = WEIGHTED ? __fmaf_rn(g[rr], f[i], acc[u][i])
-                                             : __fadd_rn(acc[u][i], f[i]);
+                        a[i] = WEIGHTED ? __fmaf_rn(g[rr], f[i], a[i]) : __fadd_rn(a[i], f[i]);
                 }
+                if (ONE && c0 + 32 * u < nch) st_v16_cs(dst + c0 + 32 * u, Elt<T>::pack(a1));
             }
+            if (ONE) break;
         }
-        V16 *dst = reinterpret_cast<V16 *>(y + t * m);
+        if (!ONE) {
 #pragma unroll
-        for (int u = 0; u < U; u++)
-            if (c0 + 32 * u < nch) st_v16_cs(dst + c0 + 32 * u, Elt<T>::pack(acc[u]));
+            for (int u = 0; u < (ONE ? 1 : U); u++)
+                if (c0 + 32 * u < nch) st_v16_cs(dst + c0 + 32 * u, Elt<T>::pack(acc[u]));
+        }
     }
 }
 
@@ -280,11 +294,12 @@ int sm_count_cached() {
     return cached[dev];
 }
 
-// CTAs for `items` one-warp work items: one item per warp, at most 8 CTAs x 8
-// warps (64 warps) resident per SM; larger batches loop.
+// CTAs for `items` one-warp work items: one item per warp, but never more CTAs
+// than are resident at once (4 per SM at the kernels' <= 64 registers), so no
+// partial second wave; larger batches loop inside each warp.
 int grid_for_items(int64_t items) {
     int64_t want = (items + (DNT / 32) - 1) / (DNT / 32);
-    int64_t cap = (int64_t)sm_count_cached() * 8;
+    int64_t cap = (int64_t)sm_count_cached() * 4;
     return (int)(want < 1 ? 1 : (want < cap ? want : cap));
 }
 
@@ -325,23 +340,34 @@ moe_status encode_launch(const void *x, moe_dtype dt, const int32_t *idx, const 
     return MOE_OK;
 }
 
+template <typename T, bool W>
+moe_status combine_typed(const void *src, const int32_t *idx, const int32_t *loc, const float *gates,
+                         const int32_t *c_dev, int64_t s, int m, int e, int k, int64_t c_max,
+                         void *y, int32_t *st, cudaStream_t stream) {
+    constexpr int VEC = Elt<T>::VEC;
+    const int nch = m / VEC;
+    const dim3 b(DNT);
+    const T *sp = (const T *)src;
+    T *yp = (T *)y;
+    if (k <= 2) {  // all routes in one group: 4 chunks per lane, 8 live accumulators
+        const int64_t items = s * ((nch + 127) / 128);
+        return launch_pdl(combine_kernel<T, W, 4, 2, true>, dim3(grid_for_items(items)), b, 0, stream,
+                          sp, idx, loc, gates, c_dev, s, m, e, k, c_max, yp, st);
+    }
+    const int64_t items = s * ((nch + 63) / 64);
+    return launch_pdl(combine_kernel<T, W, 2, 4, false>, dim3(grid_for_items(items)), b, 0, stream,
+                      sp, idx, loc, gates, c_dev, s, m, e, k, c_max, yp, st);
+}
+
 moe_status combine_launch(const void *src, moe_dtype dt, const int32_t *idx, const int32_t *loc,
                           const float *gates, const int32_t *c_dev, int64_t s, int m, int e, int k,
                           int64_t c_max, void *y, int32_t *st, cudaStream_t stream) {
-    const int grid = grid_for_items(s * row_slices(m, dt));
     const bool w = gates != nullptr;
-    const dim3 g(grid), b(DNT);
-    const float *gp = gates;
-    if (dt == MOE_BF16) {
-        auto *sp = (const __nv_bfloat16 *)src;
-        auto *yp = (__nv_bfloat16 *)y;
-        if (w) return launch_pdl(combine_kernel<__nv_bfloat16, true>, g, b, 0, stream, sp, idx, loc, gp, c_dev, s, m, e, k, c_max, yp, st);
-        return launch_pdl(combine_kernel<__nv_bfloat16, false>, g, b, 0, stream, sp, idx, loc, gp, c_dev, s, m, e, k, c_max, yp, st);
-    }
-    auto *sp = (const float *)src;
-    auto *yp = (float *)y;
-    if (w) return launch_pdl(combine_kernel<float, true>, g, b, 0, stream, sp, idx, loc, gp, c_dev, s, m, e, k, c_max, yp, st);
-    return launch_pdl(combine_kernel<float, false>, g, b, 0, stream, sp, idx, loc, gp, c_dev, s, m, e, k, c_max, yp, st);
+    if (dt == MOE_BF16)
+        return w ? combine_typed<__nv_bfloat16, true>(src, idx, loc, gates, c_dev, s, m, e, k, c_max, y, st, stream)
+                 : combine_typed<__nv_bfloat16, false>(src, idx, loc, gates, c_dev, s, m, e, k, c_max, y, st, stream);
+    return w ? combine_typed<float, true>(src, idx, loc, gates, c_dev, s, m, e, k, c_max, y, st, stream)
+             : combine_typed<float, false>(src, idx, loc, gates, c_dev, s, m, e, k, c_max, y, st, stream);
 }
 
 moe_status decode_bwd_launch(const void *dy, const void *out, moe_dtype dt, const int32_t *idx,
