@@ -49,22 +49,30 @@ enum Epi { EPI_GELU = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_BIAS = 3 };
 // Tile shape.  TM = 1: 128 x 256 tiles, two 256-column accumulators in TMEM so
 // the epilogue of one tile overlaps the main loop of the next.  TM = 2:
 // 256 x 256 tiles as two M=128 MMAs sharing every B tile (a third fewer operand
-// bytes per FLOP), one 512-column accumulator.  BK is the K depth of one
-// pipeline stage: 64 bf16 (one 128-byte swizzle row) or 32 (64-byte swizzle);
-// the smaller stage doubles the number of stages in the same shared memory,
-// i.e. more operand bytes in flight to cover L2/HBM latency.
-template <int TM, int BK_>
+// bytes per FLOP), one 512-column accumulator.  PAIR (with TM = 1): a CTA pair
+// (cluster of 2) computes a 256 x 256 tile with the 2-SM MMA (M = 256): each
+// CTA loads its 128 rows of A and one half of the B tile, so each SM moves the
+// TM = 2 operand bytes per FLOP while keeping two accumulators for overlap.
+// BK is the K depth of one pipeline stage: 64 bf16 (one 128-byte swizzle row)
+// or 32 (64-byte swizzle); the smaller stage doubles the number of stages in
+// the same shared memory, i.e. more operand bytes in flight to cover L2/HBM
+// latency.
+template <int TM, int BK_, bool PAIR_ = false>
 struct Tiling {
+    static constexpr bool PAIR = PAIR_;
     static constexpr int BK = BK_;
     static constexpr int ROWB = BK * 2;                   // bytes per operand row
-    static constexpr int BMT = UM * TM;                   // rows of A per tile
-    static constexpr int A_BYTES = BMT * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int A_ROWS = UM * TM;                // rows of A per CTA and stage
+    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;     // rows of B per CTA and stage
+    static constexpr int BMT = A_ROWS * (PAIR ? 2 : 1);   // rows of A per tile
+    static constexpr int A_BYTES = A_ROWS * BK * 2;
+    static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = SMEM_RING / STAGE_BYTES;
     static constexpr int NACC = TM == 1 ? 2 : 1;          // accumulator buffers
     static constexpr int ACC_COLS = BN * TM;              // TMEM columns per buffer
     static_assert(BK == 64 || BK == 32, "BK");
+    static_assert(!PAIR || TM == 1, "pair tiles use one M=256 MMA");
     static_assert(STAGES >= 3 && STAGES <= 8, "stages");
 };
 
@@ -72,6 +80,9 @@ struct Tiling {
 // N >> 3 at bit 17, M >> 4 at bit 24.
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                            ((uint32_t)(UM >> 4) << 24);
+// The same for the 2-SM MMA: M = 256 over the CTA pair (128 rows per CTA).
+constexpr uint32_t IDESC_PAIR = (1u << 4) | (1u << 7) | (1u << 10) |
+                                ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((2 * UM) >> 4) << 24);
 
 template <int STAGES>
 struct Ctl {  // control block in shared memory
@@ -128,26 +139,38 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *b) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
 }
 
+// CL: acquire at cluster scope (arrivals and copies from the peer CTA of a pair).
+template <bool CL = false>
 __device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(su32(b)), "r"(parity)
-        : "memory");
+    if (CL)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(su32(b)), "r"(parity)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(su32(b)), "r"(parity)
+            : "memory");
     return ok != 0;
 }
 
 // Bounded wait for the phase with `parity` to complete.  Returns false if the
 // CTA is aborting or the wait ran past WAIT_NS (then the abort is raised).
+template <bool CL = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, int32_t *abort_flag,
                                        int32_t *status) {
-    if (mbar_try(b, parity)) return true;
+    if (mbar_try<CL>(b, parity)) return true;
     unsigned long long t0 = gtimer();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try(b, parity)) return true;
+        if (mbar_try<CL>(b, parity)) return true;
         if ((it & 31u) == 0) {
             if (*(volatile int32_t *)abort_flag) return false;
             if (gtimer() - t0 > WAIT_NS) {
@@ -168,7 +191,41 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
-// Pull a box into L2 ahead of its TMA load (no shared memory involved).
+// ------------------------------------------------------- CTA-pair helpers
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is counted on an
+// mbarrier of either CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, int x, int y,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -196,10 +253,32 @@ __device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, ui
         : "memory");
 }
 
+// 2-SM MMA, issued by the pair's first CTA: A and B descriptors name the same
+// shared-memory offsets in both CTAs; each CTA's TMEM receives its 128 rows.
+__device__ __forceinline__ void umma_pair(uint32_t tmem_d, uint64_t a, uint64_t b,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(IDESC_PAIR), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             su32(bar))
+        : "memory");
+}
+
+// Arrive on the mbarrier at this offset in both CTAs of the pair once the
+// pair MMAs issued so far have completed.
+__device__ __forceinline__ void umma_commit_pair(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(su32(bar)),
+        "h"((uint16_t)3)
         : "memory");
 }
 
@@ -315,18 +394,20 @@ __device__ __forceinline__ Tile decode_tile(const int32_t *tile_start, int e, in
     return T;
 }
 
-template <int EPI, int TM, int BK>
+template <int EPI, int TM, int BK, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmB3, const GemmArgs args) {
-    using TL = Tiling<TM, BK>;
+    using TL = Tiling<TM, BK, PAIR>;
     constexpr int STAGES = TL::STAGES, BMT = TL::BMT, A_BYTES = TL::A_BYTES;
     constexpr int B_BYTES = TL::B_BYTES, ROWB = TL::ROWB;
     __shared__ int32_t s_bad;
     pdl_enter();
     if (threadIdx.x == 0) s_bad = status_bad(args.status) ? 1 : 0;
     __syncthreads();
-    if (s_bad) return;  // uniform across the CTA: nothing allocated yet
+    // A single CTA may leave now (nothing allocated yet); a pair decides
+    // together after its first cluster barrier.
+    if (!PAIR && s_bad) return;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sA = smem;
@@ -337,6 +418,10 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = args.e;
+    // CTA pairs: rank 0 issues the MMAs; tiles are dealt out per pair.
+    const uint32_t rank = PAIR ? cluster_rank() : 0;
+    const int tile0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int tile_step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
     constexpr int NOUT_TILE = EPI == EPI_SWIGLU ? BN / 2 : BN;  // output columns per tile
     const int ntn = (args.n_out + NOUT_TILE - 1) / NOUT_TILE;
     const int nk = (args.K + BK - 1) / BK;
@@ -364,44 +449,80 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             ctl->tile_start[e] = run;
             ctl->total_tiles = run;
             ctl->abort = 0;
-            // full: one arrival (with its transaction bytes) from each producer
+            // full: one arrival (with its transaction bytes, for a pair those of
+            // both CTAs) from each producer of the MMA-issuing CTA
             for (int s = 0; s < STAGES; s++) { mbar_init(&ctl->full[s], 2); mbar_init(&ctl->empty[s], 1); }
-            for (int a = 0; a < 2; a++) { mbar_init(&ctl->tfull[a], 1); mbar_init(&ctl->tempty[a], EPI_WARPS); }
+            for (int a = 0; a < 2; a++) {
+                mbar_init(&ctl->tfull[a], 1);
+                mbar_init(&ctl->tempty[a], PAIR ? 2 * EPI_WARPS : EPI_WARPS);
+            }
             mbar_init(&ctl->drain, 1);
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
     } else if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         su32(&ctl->tmem_base)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if (PAIR) {
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             su32(&ctl->tmem_base)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             su32(&ctl->tmem_base)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if (PAIR) cluster_sync();  // both CTAs' barriers initialised, TMEM allocated
+    else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
-    const int total = ctl->total_tiles;
+    int total = ctl->total_tiles;
+    if (PAIR) {
+        int peer_bad;
+        asm volatile("ld.shared::cluster.u32 %0, [%1];"
+                     : "=r"(peer_bad)
+                     : "r"(map_to_rank(su32(&s_bad), rank ^ 1u)));
+        if (s_bad | peer_bad) total = 0;  // the same decision in both CTAs
+    }
     int32_t *abort_flag = &ctl->abort;
 
     if (warp == 0 || warp == B_WARP) {
         // ----------------------------------------------------- TMA producers
         // Two issuing threads in different warps (TMA throughput per SM is
         // bounded per issuing thread): A tiles from warp 0, B tiles from the last
-        // warp (lane 0 of each issues).
+        // warp (lane 0 of each issues).  In a pair both CTAs load their own
+        // halves; the copies complete on the first CTA's full barriers, whose
+        // producers announce the bytes of both.
         const bool is_a = warp == 0;
         int stage = 0;
         uint32_t phase = 0;
         int issued = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        for (int t = tile0; t < total; t += tile_step) {
             Tile T = decode_tile(ctl->tile_start, e, t, BMT, kept_rows);
-            const int a_row = (int)((int64_t)T.j * args.c_max + (int64_t)T.mt * BMT);
-            const int b_row = T.j * args.b_rows + T.nt * NOUT_TILE;
+            const int a_row = (int)((int64_t)T.j * args.c_max + (int64_t)T.mt * BMT +
+                                    (int64_t)rank * TL::A_ROWS);
+            const int b_row = T.j * args.b_rows + T.nt * NOUT_TILE +
+                              (PAIR && EPI != EPI_SWIGLU ? (int)rank * TL::B_ROWS : 0);
             for (int kb = 0; kb < nk; kb++) {
                 int ok = 1;
                 if (lane == 0) {
-                    ok = mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag, args.status);
-                    if (ok && is_a) {
+                    ok = mbar_wait<PAIR>(&ctl->empty[stage], phase ^ 1u, abort_flag, args.status);
+                    if (ok && PAIR) {
+                        const uint32_t fb = map_to_rank(su32(&ctl->full[stage]), 0);
+                        if (is_a) {
+                            if (rank == 0) mbar_expect_tx(&ctl->full[stage], 2 * A_BYTES);
+                            tma_load_2d_pair(sA + stage * A_BYTES, &tmA, kb * BK, a_row, fb);
+                        } else {
+                            // SwiGLU: the first CTA's half of B is W1, the second's W3
+                            if (rank == 0) mbar_expect_tx(&ctl->full[stage], 2 * B_BYTES);
+                            tma_load_2d_pair(sB + stage * B_BYTES,
+                                             EPI == EPI_SWIGLU && rank ? &tmB3 : &tmB, kb * BK,
+                                             b_row, fb);
+                        }
+                    } else if (ok && is_a) {
                         mbar_expect_tx(&ctl->full[stage], A_BYTES);
                         tma_load_2d(sA + stage * A_BYTES, &tmA, kb * BK, a_row, &ctl->full[stage]);
                     } else if (ok && EPI == EPI_SWIGLU) {
@@ -421,65 +542,82 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         }
     producer_done:
         // wait (bounded) for the copies still in flight before the CTA can exit
-        if (lane == 0) {
+        // (a pair's second CTA cannot observe the first CTA's barriers: its
+        // copies are covered by the MMAs that consume them, or on an abort by
+        // the delay before the final cluster barrier)
+        if (lane == 0 && (!PAIR || rank == 0)) {
             for (int i = max(0, issued - STAGES); i < issued; i++) {
                 int s = i % STAGES;
                 uint32_t ph = (uint32_t)((i / STAGES) & 1);
                 unsigned long long t0 = gtimer();
-                while (!mbar_try(&ctl->full[s], ph) && gtimer() - t0 < WAIT_NS) {
+                while (!mbar_try<PAIR>(&ctl->full[s], ph) && gtimer() - t0 < WAIT_NS) {
                 }
             }
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------------ MMA issuer
-        int stage = 0;
-        uint32_t phase = 0;
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            if (!mbar_wait(&ctl->tempty[acc], acc_phase ^ 1u, abort_flag, args.status)) break;
-            tc_fence_after();
-            const uint32_t d = tmem + (uint32_t)(acc * TL::ACC_COLS);
-            bool ok = true;
-            for (int kb = 0; kb < nk; kb++) {
-                if (!mbar_wait(&ctl->full[stage], phase, abort_flag, args.status)) { ok = false; break; }
+        if (!PAIR || rank == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            for (int t = tile0; t < total; t += tile_step) {
+                if (!mbar_wait<PAIR>(&ctl->tempty[acc], acc_phase ^ 1u, abort_flag, args.status)) break;
                 tc_fence_after();
-                const uint32_t a0 = su32(sA + stage * A_BYTES);
-                const uint32_t b0 = su32(sB + stage * B_BYTES);
+                const uint32_t d = tmem + (uint32_t)(acc * TL::ACC_COLS);
+                bool ok = true;
+                for (int kb = 0; kb < nk; kb++) {
+                    if (!mbar_wait<PAIR>(&ctl->full[stage], phase, abort_flag, args.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a0 = su32(sA + stage * A_BYTES);
+                    const uint32_t b0 = su32(sB + stage * B_BYTES);
 #pragma unroll
-                for (int kk = 0; kk < BK / UK; kk++)
+                    for (int kk = 0; kk < BK / UK; kk++) {
+                        if (PAIR) {
+                            umma_pair(d, sdesc<ROWB>(a0 + kk * UK * 2), sdesc<ROWB>(b0 + kk * UK * 2),
+                                      (kb | kk) != 0);
+                        } else {
 #pragma unroll
-                    for (int hm = 0; hm < TM; hm++)  // M halves share the B tile
-                        umma(d + (uint32_t)(hm * BN),
-                             sdesc<ROWB>(a0 + hm * UM * ROWB + kk * UK * 2),
-                             sdesc<ROWB>(b0 + kk * UK * 2), (kb | kk) != 0);
-                umma_commit(&ctl->empty[stage]);  // stage reusable once these MMAs read it
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                            for (int hm = 0; hm < TM; hm++)  // M halves share the B tile
+                                umma(d + (uint32_t)(hm * BN),
+                                     sdesc<ROWB>(a0 + hm * UM * ROWB + kk * UK * 2),
+                                     sdesc<ROWB>(b0 + kk * UK * 2), (kb | kk) != 0);
+                        }
+                    }
+                    // stage reusable (in both CTAs of a pair) once these MMAs read it
+                    if (PAIR) umma_commit_pair(&ctl->empty[stage]);
+                    else umma_commit(&ctl->empty[stage]);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                // accumulator ready when all MMAs finish
+                if (PAIR) umma_commit_pair(&ctl->tfull[acc]);
+                else umma_commit(&ctl->tfull[acc]);
+                if (++acc == TL::NACC) { acc = 0; acc_phase ^= 1u; }
             }
-            if (!ok) break;
-            umma_commit(&ctl->tfull[acc]);  // accumulator ready when all MMAs finish
-            if (++acc == TL::NACC) { acc = 0; acc_phase ^= 1u; }
+            // all MMAs issued by this thread complete before TMEM is released
+            if (PAIR) umma_commit_pair(&ctl->drain);
+            else umma_commit(&ctl->drain);
         }
-        // all MMAs issued by this thread complete before TMEM is released
-        umma_commit(&ctl->drain);
         unsigned long long t0 = gtimer();
-        while (!mbar_try(&ctl->drain, 0) && gtimer() - t0 < WAIT_NS) {
+        while (!mbar_try<PAIR>(&ctl->drain, 0) && gtimer() - t0 < WAIT_NS) {
         }
     } else if (warp >= 2 && warp < B_WARP) {
         // ------------------------------------------------------------- epilogue
         // TM = 1: warp (sub, half) owns rows sub*32.. and half of the columns.
         // TM = 2: warp (sub, half) owns rows half*128 + sub*32.. and all columns.
+        // A pair's second CTA holds rows 128..255 of the tile.
         const int ew = warp - 2;
         const int sub = warp & 3;             // TMEM lane quarter this warp may access
         const int half = ew >> 2;
-        const int row_in_tile = (TM == 2 ? half * UM : 0) + sub * 32 + lane;
+        const int row_in_tile = (int)rank * UM + (TM == 2 ? half * UM : 0) + sub * 32 + lane;
         constexpr int COLS = TM == 2 ? NOUT_TILE : NOUT_TILE / 2;  // output columns per warp
         const int col0 = TM == 2 ? 0 : half * COLS;                // first output column
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        for (int t = tile0; t < total; t += tile_step) {
             Tile T = decode_tile(ctl->tile_start, e, t, BMT, kept_rows);
-            if (!mbar_wait(&ctl->tfull[acc], acc_phase, abort_flag, args.status)) break;
+            if (!mbar_wait<PAIR>(&ctl->tfull[acc], acc_phase, abort_flag, args.status)) break;
             tc_fence_after();
             const int row = T.mt * BMT + row_in_tile;
             const bool valid = row < T.rows;
@@ -564,18 +702,40 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->tempty[acc]);
+            if (lane == 0) {
+                // a pair's accumulators are reused by the first CTA's MMAs
+                if (PAIR) mbar_arrive_cluster(map_to_rank(su32(&ctl->tempty[acc]), 0));
+                else mbar_arrive(&ctl->tempty[acc]);
+            }
             if (++acc == TL::NACC) { acc = 0; acc_phase ^= 1u; }
         }
     }
 
     tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(TMEM_COLS)
-                     : "memory");
+    if (PAIR) {
+        // After an abort, copies issued by either CTA may still be landing in
+        // its shared memory: give them time (they finish within microseconds)
+        // before the pair leaves.
+        if (*(volatile int32_t *)abort_flag) {
+            unsigned long long t0 = gtimer();
+            while (gtimer() - t0 < 1000000ull) {
+            }
+        }
+        cluster_sync();  // no MMA, copy or remote arrival of the pair in flight
+        if (warp == 1) {
+            tc_fence_after();
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                         "r"(TMEM_COLS)
+                         : "memory");
+        }
+    } else {
+        __syncthreads();
+        if (warp == 1) {
+            tc_fence_after();
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                         "r"(TMEM_COLS)
+                         : "memory");
+        }
     }
 }
 
@@ -622,27 +782,74 @@ int sm_count() {
     return cached[dev];
 }
 
-template <int EPI, int TM, int BK>
+// Resident CTA pairs of a pair kernel with this configuration (the GPCs bound
+// how many 2-CTA clusters of ~200 KB shared memory fit at once).
+template <typename K>
+int max_pairs(K kern, size_t smem) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (const void *)kern, &cfg) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        return sm_count() / 2;
+    }
+    return n;
+}
+
+template <int EPI, int TM, int BK, bool PAIR>
 moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &b3,
                        const GemmArgs &args, cudaStream_t stream) {
-    using TL = Tiling<TM, BK>;
-    auto kern = tc_group_gemm<EPI, TM, BK>;
+    using TL = Tiling<TM, BK, PAIR>;
+    auto kern = tc_group_gemm<EPI, TM, BK, PAIR>;
     constexpr size_t SMEM = smem_bytes<TL>();
-    static bool attr_set[64] = {false};
+    static int units[64] = {0};  // resident CTAs (1-SM) or CTA pairs, per device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    int nunits = dev >= 0 && dev < 64 ? units[dev] : 0;
+    if (!nunits) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) !=
             cudaSuccess)
             return MOE_ERR_CUDA;
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+        nunits = PAIR ? max_pairs(kern, SMEM) : sm_count();
+        if (dev >= 0 && dev < 64) units[dev] = nunits;
     }
     constexpr int NOUT_TILE = EPI == EPI_SWIGLU ? BN / 2 : BN;
     int64_t ntn = (args.n_out + NOUT_TILE - 1) / NOUT_TILE;
     int64_t upper = (int64_t)args.e * ((args.c_max + TL::BMT - 1) / TL::BMT) * ntn;
-    int64_t grid = upper < sm_count() ? upper : sm_count();
+    int64_t grid = upper < nunits ? upper : nunits;
     if (grid < 1) grid = 1;
-    return launch_pdl(kern, dim3((unsigned)grid), dim3(NUM_THREADS), SMEM, stream, a, b, b3, args);
+    if (!PAIR)
+        return launch_pdl(kern, dim3((unsigned)grid), dim3(NUM_THREADS), SMEM, stream, a, b, b3, args);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * grid));
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t err = cudaLaunchKernelEx(&cfg, kern, a, b, b3, args);
+    note_launch();
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
 }
 
 }  // namespace
@@ -657,26 +864,31 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
                          const void *w1, const void *b1, const void *w3, const void *w2,
                          const void *b2, moe_act act, int e, int64_t c_max, int m, int h,
                          void *hid, void *out, int32_t *st, cudaStream_t stream) {
-    // fc1: 128-row tiles, so its activation epilogue overlaps the next tile's
-    // main loop.  fc2 (bias-only epilogue, long K): 256-row tiles, 32-deep stages.
+    // fc1: 256-row tiles on CTA pairs (2-SM MMA), two accumulators per CTA so
+    // its activation epilogue overlaps the next tile's main loop.  fc2
+    // (bias-only epilogue, long K): 256-row tiles per CTA, 32-deep stages.
     constexpr int TM1 = 1, BK1 = 64, TM2 = 2, BK2 = 32;
+    constexpr bool PAIR1 = true;
+    using T1 = Tiling<TM1, BK1, PAIR1>;
+    using T2 = Tiling<TM2, BK2, false>;
     CUtensorMap mA1, mB1, mB3, mA2, mB2;
     const bool swiglu = act == MOE_ACT_SWIGLU;
-    const uint32_t b1_box = swiglu ? BN / 2 : BN;
-    if (!make_map(&mA1, buf, (uint64_t)e * c_max, (uint64_t)m, Tiling<TM1, BK1>::BMT, BK1) ||
+    // one CTA's B box: a pair CTA's half tile, or a 1-SM SwiGLU tile's W1/W3 half
+    const uint32_t b1_box = PAIR1 || swiglu ? BN / 2 : BN;
+    if (!make_map(&mA1, buf, (uint64_t)e * c_max, (uint64_t)m, T1::A_ROWS, BK1) ||
         !make_map(&mB1, w1, (uint64_t)e * h, (uint64_t)m, b1_box, BK1) ||
         !make_map(&mB3, swiglu ? w3 : w1, (uint64_t)e * h, (uint64_t)m, b1_box, BK1) ||
-        !make_map(&mA2, hid, (uint64_t)e * c_max, (uint64_t)h, Tiling<TM2, BK2>::BMT, BK2) ||
-        !make_map(&mB2, w2, (uint64_t)e * m, (uint64_t)h, BN, BK2))
+        !make_map(&mA2, hid, (uint64_t)e * c_max, (uint64_t)h, T2::A_ROWS, BK2) ||
+        !make_map(&mB2, w2, (uint64_t)e * m, (uint64_t)h, T2::B_ROWS, BK2))
         return MOE_ERR_CUDA;
     GemmArgs g1{counts, c_dev, st, (const __nv_bfloat16 *)b1, (__nv_bfloat16 *)hid, c_max, e, m, h, h};
     moe_status r;
-    if (swiglu) r = launch_gemm<EPI_SWIGLU, TM1, BK1>(mA1, mB1, mB3, g1, stream);
-    else if (act == MOE_ACT_GELU) r = launch_gemm<EPI_GELU, TM1, BK1>(mA1, mB1, mB1, g1, stream);
-    else r = launch_gemm<EPI_RELU, TM1, BK1>(mA1, mB1, mB1, g1, stream);
+    if (swiglu) r = launch_gemm<EPI_SWIGLU, TM1, BK1, PAIR1>(mA1, mB1, mB3, g1, stream);
+    else if (act == MOE_ACT_GELU) r = launch_gemm<EPI_GELU, TM1, BK1, PAIR1>(mA1, mB1, mB1, g1, stream);
+    else r = launch_gemm<EPI_RELU, TM1, BK1, PAIR1>(mA1, mB1, mB1, g1, stream);
     if (r != MOE_OK) return r;
     GemmArgs g2{counts, c_dev, st, (const __nv_bfloat16 *)b2, (__nv_bfloat16 *)out, c_max, e, h, m, m};
-    return launch_gemm<EPI_BIAS, TM2, BK2>(mA2, mB2, mB2, g2, stream);
+    return launch_gemm<EPI_BIAS, TM2, BK2, false>(mA2, mB2, mB2, g2, stream);
 }
 
 }  // namespace moe
