@@ -97,9 +97,14 @@ struct Ctl {  // control block in shared memory
     int32_t tile_start[MAX_E + 1];
 };
 
+// Output staging per epilogue warp: 32 rows x 32 bf16 (64-byte swizzle),
+// written by the warp and stored to global memory by TMA.
+constexpr int STG_WARP_BYTES = 2048;
+
 template <class TL>
 constexpr size_t smem_bytes() {
-    return 1024 + (size_t)TL::STAGES * TL::STAGE_BYTES + sizeof(Ctl<TL::STAGES>);
+    return 1024 + (size_t)TL::STAGES * TL::STAGE_BYTES + (size_t)EPI_WARPS * STG_WARP_BYTES +
+           sizeof(Ctl<TL::STAGES>);
 }
 
 struct GemmArgs {
@@ -191,6 +196,73 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// TMA store of a box from this CTA's shared memory (bulk async-group).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int y, const void *src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     (uint64_t)map),
+                 "r"(x), "r"(y), "r"(su32(src))
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's store groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until all of this thread's store groups have completed.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint8_t *p, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(su32(p)), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// One lane's 32 output columns (pk: 16 packed bf16 pairs, column order) of a
+// warp's 32 consecutive rows starting at global row grow0, columns gcol...
+// When all 32 rows are kept: through the warp's staging buffer (row = lane,
+// 16-byte chunk c of a 64-byte row at c ^ ((row >> 1) & 3), the 64-byte
+// swizzle pattern) and one TMA store, which clips columns >= n_out.
+// Otherwise direct stores of this lane's row if it is kept.
+__device__ __forceinline__ void epi_store32(const CUtensorMap *map, uint8_t *stg,
+                                            const uint32_t (&pk)[16], bool all_kept, bool kept,
+                                            int lane, int64_t grow0, int gcol, int n_out,
+                                            __nv_bfloat16 *orow) {
+    if (all_kept) {
+        if (gcol >= n_out) return;  // warp-uniform
+        if (lane == 0) bulk_wait_read<0>();  // the previous store has read the buffer
+        __syncwarp();
+        const int sw = (lane >> 1) & 3;
+#pragma unroll
+        for (int c = 0; c < 4; c++)
+            st_shared_v4(stg + lane * 64 + ((c ^ sw) << 4), pk[c * 4 + 0], pk[c * 4 + 1],
+                         pk[c * 4 + 2], pk[c * 4 + 3]);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(map, gcol, (int)grow0, stg);
+            bulk_commit();
+        }
+    } else if (kept) {
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            if (gcol + q * 8 < n_out) {
+                V16 o;
+                o.w[0] = pk[q * 4 + 0]; o.w[1] = pk[q * 4 + 1];
+                o.w[2] = pk[q * 4 + 2]; o.w[3] = pk[q * 4 + 3];
+                st_v16(orow + gcol + q * 8, o);
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------- CTA-pair helpers
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -210,9 +282,12 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Arrive on an mbarrier of either CTA of the pair.  Release at CTA scope (the
+// default): what the waiter needs ordered are this thread's completed
+// tcgen05.ld (by tcgen05.fence::before_thread_sync), not its global stores; a
+// cluster-scope release would wait for those stores as well.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-                 : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // TMA load into this CTA's shared memory whose completion is counted on an
@@ -397,7 +472,8 @@ __device__ __forceinline__ Tile decode_tile(const int32_t *tile_start, int e, in
 template <int EPI, int TM, int BK, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              const __grid_constant__ CUtensorMap tmB3, const GemmArgs args) {
+              const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmO,
+              const GemmArgs args) {
     using TL = Tiling<TM, BK, PAIR>;
     constexpr int STAGES = TL::STAGES, BMT = TL::BMT, A_BYTES = TL::A_BYTES;
     constexpr int B_BYTES = TL::B_BYTES, ROWB = TL::ROWB;
@@ -412,7 +488,8 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * A_BYTES;
-    Ctl<STAGES> *ctl = (Ctl<STAGES> *)(smem + STAGES * TL::STAGE_BYTES);
+    uint8_t *stg_all = smem + STAGES * TL::STAGE_BYTES;  // output staging
+    Ctl<STAGES> *ctl = (Ctl<STAGES> *)(stg_all + EPI_WARPS * STG_WARP_BYTES);
     __shared__ int32_t kept_rows[MAX_E];
     __shared__ __align__(16) float epi_bias[EPI_WARPS][256];  // per epilogue warp
 
@@ -613,6 +690,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         const int row_in_tile = (int)rank * UM + (TM == 2 ? half * UM : 0) + sub * 32 + lane;
         constexpr int COLS = TM == 2 ? NOUT_TILE : NOUT_TILE / 2;  // output columns per warp
         const int col0 = TM == 2 ? 0 : half * COLS;                // first output column
+        uint8_t *stg = stg_all + ew * STG_WARP_BYTES;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = tile0; t < total; t += tile_step) {
@@ -621,6 +699,8 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             tc_fence_after();
             const int row = T.mt * BMT + row_in_tile;
             const bool valid = row < T.rows;
+            const bool all_kept = row - lane + 31 < T.rows;  // the warp's 32 rows
+            const int64_t grow0 = (int64_t)T.j * args.c_max + row - lane;
             __nv_bfloat16 *orow =
                 args.out + ((int64_t)T.j * args.c_max + row) * (int64_t)args.n_out;
             const __nv_bfloat16 *brow = args.bias ? args.bias + (int64_t)T.j * args.n_out : nullptr;
@@ -636,16 +716,14 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     tmem_ld32(tbase + (uint32_t)(BN / 2 + ocol), u);
                     tmem_wait_ld(r);
                     tmem_tie(u);
-                    float v[32];
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int i = 0; i < 32; i++)
-                        v[i] = silu(__uint_as_float(r[i])) * __uint_as_float(u[i]);
-                    if (valid) {
-#pragma unroll
-                        for (int q = 0; q < 4; q++)
-                            if (gcol + q * 8 < args.n_out)
-                                st_v16(orow + gcol + q * 8, Elt<__nv_bfloat16>::pack(v + q * 8));
-                    }
+                    for (int i = 0; i < 16; i++)
+                        pk[i] = pack_bf16(silu(__uint_as_float(r[2 * i])) * __uint_as_float(u[2 * i]),
+                                          silu(__uint_as_float(r[2 * i + 1])) *
+                                              __uint_as_float(u[2 * i + 1]));
+                    epi_store32(&tmO, stg, pk, all_kept, valid, lane, grow0, gcol, args.n_out,
+                                orow);
                 }
             } else {
                 // this warp's bias columns, widened to fp32 in shared memory once per tile
@@ -673,14 +751,13 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
 #pragma unroll
                     for (int h2 = 0; h2 < 2; h2++) {
                         const int gcol = T.nt * NOUT_TILE + col0 + c0 + 32 * h2;
+                        uint32_t pk[16];
 #pragma unroll
                         for (int q = 0; q < 4; q++) {
-                            const int g8 = gcol + q * 8;
                             const float4 *bp = reinterpret_cast<const float4 *>(bsl + c0 + 32 * h2 + q * 8);
                             const float4 bl = bp[0], bh = bp[1];
                             const float2 bb[4] = {make_float2(bl.x, bl.y), make_float2(bl.z, bl.w),
                                                   make_float2(bh.x, bh.y), make_float2(bh.z, bh.w)};
-                            uint32_t pk[4];
 #pragma unroll
                             for (int i = 0; i < 4; i++) {
                                 float2 a = __fadd2_rn(make_float2(__uint_as_float(r[h2][q * 8 + 2 * i]),
@@ -688,14 +765,11 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                                                       bb[i]);
                                 if (EPI == EPI_GELU) a = gelu_erf2(a);
                                 else if (EPI == EPI_RELU) a = make_float2(fmaxf(a.x, 0.0f), fmaxf(a.y, 0.0f));
-                                pk[i] = pack_bf16(a.x, a.y);
-                            }
-                            if (valid && g8 < args.n_out) {
-                                V16 o;
-                                o.w[0] = pk[0]; o.w[1] = pk[1]; o.w[2] = pk[2]; o.w[3] = pk[3];
-                                st_v16(orow + g8, o);
+                                pk[q * 4 + i] = pack_bf16(a.x, a.y);
                             }
                         }
+                        epi_store32(&tmO, stg, pk, all_kept, valid, lane, grow0, gcol,
+                                    args.n_out, orow);
                     }
                 }
                 __syncwarp();   // slice reused for the next tile
@@ -709,6 +783,8 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             }
             if (++acc == TL::NACC) { acc = 0; acc_phase ^= 1u; }
         }
+        if (lane == 0) bulk_wait_all();  // output stores complete before the CTA exits
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -754,7 +830,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D bf16 tensor map over a row-major [rows, cols] matrix, box box_rows x bk
-// (bk = 64: 128-byte swizzle; bk = 32: 64-byte swizzle).
+// (bk = 64: 128-byte swizzle; bk = 32: 64-byte swizzle, also the epilogue's
+// output staging; bk = 16: 32-byte swizzle).
 bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
               int bk) {
     auto fn = encode_fn();
@@ -765,7 +842,9 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, 
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                    bk == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                    : bk == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                               : CU_TENSOR_MAP_SWIZZLE_32B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -807,7 +886,7 @@ int max_pairs(K kern, size_t smem) {
 
 template <int EPI, int TM, int BK, bool PAIR>
 moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &b3,
-                       const GemmArgs &args, cudaStream_t stream) {
+                       const CUtensorMap &o, const GemmArgs &args, cudaStream_t stream) {
     using TL = Tiling<TM, BK, PAIR>;
     auto kern = tc_group_gemm<EPI, TM, BK, PAIR>;
     constexpr size_t SMEM = smem_bytes<TL>();
@@ -828,7 +907,8 @@ moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtenso
     int64_t grid = upper < nunits ? upper : nunits;
     if (grid < 1) grid = 1;
     if (!PAIR)
-        return launch_pdl(kern, dim3((unsigned)grid), dim3(NUM_THREADS), SMEM, stream, a, b, b3, args);
+        return launch_pdl(kern, dim3((unsigned)grid), dim3(NUM_THREADS), SMEM, stream, a, b, b3, o,
+                          args);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * grid));
     cfg.blockDim = dim3(NUM_THREADS);
@@ -843,7 +923,7 @@ moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtenso
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t err = cudaLaunchKernelEx(&cfg, kern, a, b, b3, args);
+    cudaError_t err = cudaLaunchKernelEx(&cfg, kern, a, b, b3, o, args);
     note_launch();
     if (err != cudaSuccess) {
         cudaGetLastError();
@@ -871,7 +951,7 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
     constexpr bool PAIR1 = true;
     using T1 = Tiling<TM1, BK1, PAIR1>;
     using T2 = Tiling<TM2, BK2, false>;
-    CUtensorMap mA1, mB1, mB3, mA2, mB2;
+    CUtensorMap mA1, mB1, mB3, mA2, mB2, mO1, mO2;
     const bool swiglu = act == MOE_ACT_SWIGLU;
     // one CTA's B box: a pair CTA's half tile, or a 1-SM SwiGLU tile's W1/W3 half
     const uint32_t b1_box = PAIR1 || swiglu ? BN / 2 : BN;
@@ -879,16 +959,19 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
         !make_map(&mB1, w1, (uint64_t)e * h, (uint64_t)m, b1_box, BK1) ||
         !make_map(&mB3, swiglu ? w3 : w1, (uint64_t)e * h, (uint64_t)m, b1_box, BK1) ||
         !make_map(&mA2, hid, (uint64_t)e * c_max, (uint64_t)h, T2::A_ROWS, BK2) ||
-        !make_map(&mB2, w2, (uint64_t)e * m, (uint64_t)h, T2::B_ROWS, BK2))
+        !make_map(&mB2, w2, (uint64_t)e * m, (uint64_t)h, T2::B_ROWS, BK2) ||
+        !make_map(&mO1, hid, (uint64_t)e * c_max, (uint64_t)h, 32, 32) ||
+        !make_map(&mO2, out, (uint64_t)e * c_max, (uint64_t)m, 32, 32))
         return MOE_ERR_CUDA;
     GemmArgs g1{counts, c_dev, st, (const __nv_bfloat16 *)b1, (__nv_bfloat16 *)hid, c_max, e, m, h, h};
     moe_status r;
-    if (swiglu) r = launch_gemm<EPI_SWIGLU, TM1, BK1, PAIR1>(mA1, mB1, mB3, g1, stream);
-    else if (act == MOE_ACT_GELU) r = launch_gemm<EPI_GELU, TM1, BK1, PAIR1>(mA1, mB1, mB1, g1, stream);
-    else r = launch_gemm<EPI_RELU, TM1, BK1, PAIR1>(mA1, mB1, mB1, g1, stream);
+    if (swiglu) r = launch_gemm<EPI_SWIGLU, TM1, BK1, PAIR1>(mA1, mB1, mB3, mO1, g1, stream);
+    else if (act == MOE_ACT_GELU)
+        r = launch_gemm<EPI_GELU, TM1, BK1, PAIR1>(mA1, mB1, mB1, mO1, g1, stream);
+    else r = launch_gemm<EPI_RELU, TM1, BK1, PAIR1>(mA1, mB1, mB1, mO1, g1, stream);
     if (r != MOE_OK) return r;
     GemmArgs g2{counts, c_dev, st, (const __nv_bfloat16 *)b2, (__nv_bfloat16 *)out, c_max, e, h, m, m};
-    return launch_gemm<EPI_BIAS, TM2, BK2, false>(mA2, mB2, mB2, g2, stream);
+    return launch_gemm<EPI_BIAS, TM2, BK2, false>(mA2, mB2, mB2, mO2, g2, stream);
 }
 
 }  // namespace moe
