@@ -37,8 +37,11 @@ constexpr int UM = 128;                 // UMMA M (rows of one MMA)
 constexpr int BN = 256;                 // UMMA N (rows of B per tile)
 constexpr int UK = 16;                  // K of one tcgen05.mma kind::f16
 constexpr int EPI_WARPS = 8;
-constexpr int NUM_THREADS = 64 + EPI_WARPS * 32 + 32;  // + a second producer warp (B tiles)
-constexpr int B_WARP = 2 + EPI_WARPS;
+// Warps: 0 producer (A, even stages), 1 MMA, 2..9 epilogue, then producers
+// (B even), (A odd), (B odd).  The TMA boxes of one issuing thread are served
+// one after another, so each operand is fed by two threads on alternate stages.
+constexpr int PROD_WARP0 = 2 + EPI_WARPS;
+constexpr int NUM_THREADS = (PROD_WARP0 + 3) * 32;
 constexpr uint32_t TMEM_COLS = 512;     // all of TMEM
 constexpr int MAX_E = 1024;
 constexpr unsigned long long WAIT_NS = 1000000000ull;  // 1 s per wait
@@ -566,64 +569,70 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     }
     int32_t *abort_flag = &ctl->abort;
 
-    if (warp == 0 || warp == B_WARP) {
+    if (warp == 0 || warp >= PROD_WARP0) {
         // ----------------------------------------------------- TMA producers
-        // Two issuing threads in different warps (TMA throughput per SM is
-        // bounded per issuing thread): A tiles from warp 0, B tiles from the last
-        // warp (lane 0 of each issues).  In a pair both CTAs load their own
-        // halves; the copies complete on the first CTA's full barriers, whose
-        // producers announce the bytes of both.
-        const bool is_a = warp == 0;
+        // Four issuing threads in different warps: prod 0/2 load A tiles, 1/3
+        // B tiles; prod 0/1 take the even ring stages, 2/3 the odd ones (lane 0
+        // of each issues).  In a pair both CTAs load their own halves; the
+        // copies complete on the first CTA's full barriers, whose producers
+        // announce the bytes of both.
+        const int prod = warp == 0 ? 0 : warp - PROD_WARP0 + 1;
+        const bool is_a = (prod & 1) == 0;
+        const int par = prod >> 1;
+        static_assert(STAGES % 2 == 0, "producers alternate stages");
         int stage = 0;
         uint32_t phase = 0;
-        int issued = 0;
+        int it = 0, last_mine = -1;
         for (int t = tile0; t < total; t += tile_step) {
             Tile T = decode_tile(ctl->tile_start, e, t, BMT, kept_rows);
             const int a_row = (int)((int64_t)T.j * args.c_max + (int64_t)T.mt * BMT +
                                     (int64_t)rank * TL::A_ROWS);
             const int b_row = T.j * args.b_rows + T.nt * NOUT_TILE +
                               (PAIR && EPI != EPI_SWIGLU ? (int)rank * TL::B_ROWS : 0);
-            for (int kb = 0; kb < nk; kb++) {
-                int ok = 1;
-                if (lane == 0) {
-                    ok = mbar_wait<PAIR>(&ctl->empty[stage], phase ^ 1u, abort_flag, args.status);
-                    if (ok && PAIR) {
-                        const uint32_t fb = map_to_rank(su32(&ctl->full[stage]), 0);
-                        if (is_a) {
-                            if (rank == 0) mbar_expect_tx(&ctl->full[stage], 2 * A_BYTES);
-                            tma_load_2d_pair(sA + stage * A_BYTES, &tmA, kb * BK, a_row, fb);
-                        } else {
-                            // SwiGLU: the first CTA's half of B is W1, the second's W3
-                            if (rank == 0) mbar_expect_tx(&ctl->full[stage], 2 * B_BYTES);
-                            tma_load_2d_pair(sB + stage * B_BYTES,
-                                             EPI == EPI_SWIGLU && rank ? &tmB3 : &tmB, kb * BK,
-                                             b_row, fb);
+            for (int kb = 0; kb < nk; kb++, it++) {
+                if ((it & 1) == par) {
+                    int ok = 1;
+                    if (lane == 0) {
+                        ok = mbar_wait<PAIR>(&ctl->empty[stage], phase ^ 1u, abort_flag, args.status);
+                        if (ok && PAIR) {
+                            const uint32_t fb = map_to_rank(su32(&ctl->full[stage]), 0);
+                            if (is_a) {
+                                if (rank == 0) mbar_expect_tx(&ctl->full[stage], 2 * A_BYTES);
+                                tma_load_2d_pair(sA + stage * A_BYTES, &tmA, kb * BK, a_row, fb);
+                            } else {
+                                // SwiGLU: the first CTA's half of B is W1, the second's W3
+                                if (rank == 0) mbar_expect_tx(&ctl->full[stage], 2 * B_BYTES);
+                                tma_load_2d_pair(sB + stage * B_BYTES,
+                                                 EPI == EPI_SWIGLU && rank ? &tmB3 : &tmB, kb * BK,
+                                                 b_row, fb);
+                            }
+                        } else if (ok && is_a) {
+                            mbar_expect_tx(&ctl->full[stage], A_BYTES);
+                            tma_load_2d(sA + stage * A_BYTES, &tmA, kb * BK, a_row, &ctl->full[stage]);
+                        } else if (ok && EPI == EPI_SWIGLU) {
+                            mbar_expect_tx(&ctl->full[stage], B_BYTES);
+                            tma_load_2d(sB + stage * B_BYTES, &tmB, kb * BK, b_row, &ctl->full[stage]);
+                            tma_load_2d(sB + stage * B_BYTES + B_BYTES / 2, &tmB3, kb * BK, b_row,
+                                        &ctl->full[stage]);
+                        } else if (ok) {
+                            mbar_expect_tx(&ctl->full[stage], B_BYTES);
+                            tma_load_2d(sB + stage * B_BYTES, &tmB, kb * BK, b_row, &ctl->full[stage]);
                         }
-                    } else if (ok && is_a) {
-                        mbar_expect_tx(&ctl->full[stage], A_BYTES);
-                        tma_load_2d(sA + stage * A_BYTES, &tmA, kb * BK, a_row, &ctl->full[stage]);
-                    } else if (ok && EPI == EPI_SWIGLU) {
-                        mbar_expect_tx(&ctl->full[stage], B_BYTES);
-                        tma_load_2d(sB + stage * B_BYTES, &tmB, kb * BK, b_row, &ctl->full[stage]);
-                        tma_load_2d(sB + stage * B_BYTES + B_BYTES / 2, &tmB3, kb * BK, b_row,
-                                    &ctl->full[stage]);
-                    } else if (ok) {
-                        mbar_expect_tx(&ctl->full[stage], B_BYTES);
-                        tma_load_2d(sB + stage * B_BYTES, &tmB, kb * BK, b_row, &ctl->full[stage]);
                     }
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) goto producer_done;
+                    last_mine = it;
                 }
-                if (!__shfl_sync(0xffffffffu, ok, 0)) goto producer_done;
-                issued++;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
     producer_done:
-        // wait (bounded) for the copies still in flight before the CTA can exit
-        // (a pair's second CTA cannot observe the first CTA's barriers: its
-        // copies are covered by the MMAs that consume them, or on an abort by
-        // the delay before the final cluster barrier)
+        // wait (bounded) for this thread's copies still in flight before the CTA
+        // can exit (a pair's second CTA cannot observe the first CTA's barriers:
+        // its copies are covered by the MMAs that consume them, or on an abort
+        // by the delay before the final cluster barrier)
         if (lane == 0 && (!PAIR || rank == 0)) {
-            for (int i = max(0, issued - STAGES); i < issued; i++) {
+            for (int i = max(0, last_mine + 1 - STAGES); i <= last_mine; i++) {
+                if ((i & 1) != par) continue;
                 int s = i % STAGES;
                 uint32_t ph = (uint32_t)((i / STAGES) & 1);
                 unsigned long long t0 = gtimer();
@@ -679,7 +688,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         unsigned long long t0 = gtimer();
         while (!mbar_try<PAIR>(&ctl->drain, 0) && gtimer() - t0 < WAIT_NS) {
         }
-    } else if (warp >= 2 && warp < B_WARP) {
+    } else if (warp >= 2 && warp < PROD_WARP0) {
         // ------------------------------------------------------------- epilogue
         // TM = 1: warp (sub, half) owns rows sub*32.. and half of the columns.
         // TM = 2: warp (sub, half) owns rows half*128 + sub*32.. and all columns.
