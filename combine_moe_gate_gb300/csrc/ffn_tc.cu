@@ -37,9 +37,10 @@ constexpr int UM = 128;                 // UMMA M (rows of one MMA)
 constexpr int BN = 256;                 // UMMA N (rows of B per tile)
 constexpr int UK = 16;                  // K of one tcgen05.mma kind::f16
 constexpr int EPI_WARPS = 8;
-// Warps: 0 producer (A, even stages), 1 MMA, 2..9 epilogue, then producers
-// (B even), (A odd), (B odd).  The TMA boxes of one issuing thread are served
-// one after another, so each operand is fed by two threads on alternate stages.
+// Warps: 0 producer (A, first half of its rows), 1 MMA, 2..9 epilogue, then
+// producers (B first half), (A second half), (B second half).  Every stage's
+// operands arrive as four boxes of half the rows, in flight side by side, so
+// a stage lands sooner than as two boxes.
 constexpr int PROD_WARP0 = 2 + EPI_WARPS;
 constexpr int NUM_THREADS = (PROD_WARP0 + 3) * 32;
 constexpr uint32_t TMEM_COLS = 512;     // all of TMEM
@@ -52,22 +53,30 @@ enum Epi { EPI_GELU = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_BIAS = 3 };
 // Tile shape.  TM = 1: 128 x 256 tiles, two 256-column accumulators in TMEM so
 // the epilogue of one tile overlaps the main loop of the next.  TM = 2:
 // 256 x 256 tiles as two M=128 MMAs sharing every B tile (a third fewer operand
-// bytes per FLOP), one 512-column accumulator.  PAIR (with TM = 1): a CTA pair
+// bytes per FLOP), one 512-column accumulator.  CL = 2 (with TM = 1): a CTA pair
 // (cluster of 2) computes a 256 x 256 tile with the 2-SM MMA (M = 256): each
 // CTA loads its 128 rows of A and one half of the B tile, so each SM moves the
 // TM = 2 operand bytes per FLOP while keeping two accumulators for overlap.
+// CL = 4: two such pairs compute the tiles (m, 2n) and (m, 2n+1), which share
+// their A rows: each CTA loads a quarter of the pair tile's A rows and
+// multicasts it to its counterpart in the other pair, a quarter fewer operand
+// bytes per SM again.
 // BK is the K depth of one pipeline stage: 64 bf16 (one 128-byte swizzle row)
 // or 32 (64-byte swizzle); the smaller stage doubles the number of stages in
 // the same shared memory, i.e. more operand bytes in flight to cover L2/HBM
 // latency.
-template <int TM, int BK_, bool PAIR_ = false>
+template <int TM, int BK_, int CL_ = 1>
 struct Tiling {
-    static constexpr bool PAIR = PAIR_;
+    static constexpr int CL = CL_;                        // CTAs per cluster: 1, 2 or 4
+    static constexpr bool PAIR = CL > 1;                  // 2-SM MMA on CTA pairs
+    static constexpr bool QUAD = CL == 4;                 // two pairs sharing A by multicast
     static constexpr int BK = BK_;
     static constexpr int ROWB = BK * 2;                   // bytes per operand row
     static constexpr int A_ROWS = UM * TM;                // rows of A per CTA and stage
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;     // rows of B per CTA and stage
     static constexpr int BMT = A_ROWS * (PAIR ? 2 : 1);   // rows of A per tile
+    static constexpr int A_BOX_ROWS = QUAD ? A_ROWS / 4 : A_ROWS / 2;  // rows of one A copy
+    static constexpr int B_BOX_ROWS = B_ROWS / 2;                    // rows of one B copy
     static constexpr int A_BYTES = A_ROWS * BK * 2;
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -75,6 +84,7 @@ struct Tiling {
     static constexpr int NACC = TM == 1 ? 2 : 1;          // accumulator buffers
     static constexpr int ACC_COLS = BN * TM;              // TMEM columns per buffer
     static_assert(BK == 64 || BK == 32, "BK");
+    static_assert(CL == 1 || CL == 2 || CL == 4, "cluster size");
     static_assert(!PAIR || TM == 1, "pair tiles use one M=256 MMA");
     static_assert(STAGES >= 3 && STAGES <= 8, "stages");
 };
@@ -293,6 +303,18 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// TMA load of one box into the same shared-memory offset of every CTA in
+// `mask`; for each destination the bytes are counted on the mbarrier at
+// bar_cluster's offset in that destination's pair-leading CTA (even rank).
+__device__ __forceinline__ void tma_load_2d_mcast(void *dst, const CUtensorMap *map, int x, int y,
+                                                  uint32_t bar_cluster, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(su32(dst)),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar_cluster), "h"(mask)
+        : "memory");
+}
+
 // TMA load into this CTA's shared memory whose completion is counted on an
 // mbarrier of either CTA of the pair (cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, int x, int y,
@@ -350,13 +372,13 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
         : "memory");
 }
 
-// Arrive on the mbarrier at this offset in both CTAs of the pair once the
-// pair MMAs issued so far have completed.
-__device__ __forceinline__ void umma_commit_pair(uint64_t *bar) {
+// Arrive on the mbarrier at this offset in every CTA of `mask` (cluster CTA
+// ranks) once the pair MMAs issued so far have completed.
+__device__ __forceinline__ void umma_commit_pair(uint64_t *bar, uint16_t mask) {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
         " [%0], %1;" ::"r"(su32(bar)),
-        "h"((uint16_t)3)
+        "h"(mask)
         : "memory");
 }
 
@@ -472,19 +494,20 @@ __device__ __forceinline__ Tile decode_tile(const int32_t *tile_start, int e, in
     return T;
 }
 
-template <int EPI, int TM, int BK, bool PAIR>
+template <int EPI, int TM, int BK, int CL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmO,
               const GemmArgs args) {
-    using TL = Tiling<TM, BK, PAIR>;
+    using TL = Tiling<TM, BK, CL>;
+    constexpr bool PAIR = TL::PAIR, QUAD = TL::QUAD;
     constexpr int STAGES = TL::STAGES, BMT = TL::BMT, A_BYTES = TL::A_BYTES;
     constexpr int B_BYTES = TL::B_BYTES, ROWB = TL::ROWB;
     __shared__ int32_t s_bad;
     pdl_enter();
     if (threadIdx.x == 0) s_bad = status_bad(args.status) ? 1 : 0;
     __syncthreads();
-    // A single CTA may leave now (nothing allocated yet); a pair decides
+    // A single CTA may leave now (nothing allocated yet); a cluster decides
     // together after its first cluster barrier.
     if (!PAIR && s_bad) return;
     extern __shared__ uint8_t smem_raw[];
@@ -498,12 +521,17 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = args.e;
-    // CTA pairs: rank 0 issues the MMAs; tiles are dealt out per pair.
+    // Clusters: the even CTA of each pair issues the pair's MMAs; tiles are
+    // dealt out per cluster (with CL = 4 a tile index covers two N tiles).
     const uint32_t rank = PAIR ? cluster_rank() : 0;
-    const int tile0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-    const int tile_step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    const uint32_t prank = rank & 1u;    // rank within the pair
+    const uint32_t cpair = rank >> 1;    // pair within a cluster of 4
+    const uint32_t lead = rank & ~1u;    // the pair's MMA-issuing CTA
+    const int tile0 = (int)(blockIdx.x / CL);
+    const int tile_step = (int)(gridDim.x / CL);
     constexpr int NOUT_TILE = EPI == EPI_SWIGLU ? BN / 2 : BN;  // output columns per tile
     const int ntn = (args.n_out + NOUT_TILE - 1) / NOUT_TILE;
+    const int ntn_t = QUAD ? (ntn + 1) / 2 : ntn;               // N entries of the tile list
     const int nk = (args.K + BK - 1) / BK;
 
     // ---- setup: per-expert row counts and tile prefix (warp 0), barriers,
@@ -515,7 +543,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             int j = base + lane;
             int rows = j < e ? min(max(args.counts[j], 0), c_eff) : 0;
             if (j < e) kept_rows[j] = rows;
-            const int own = ((rows + BMT - 1) / BMT) * ntn;
+            const int own = ((rows + BMT - 1) / BMT) * ntn_t;
             int v = own;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -530,8 +558,9 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             ctl->total_tiles = run;
             ctl->abort = 0;
             // full: one arrival (with its transaction bytes, for a pair those of
-            // both CTAs) from each producer of the MMA-issuing CTA
-            for (int s = 0; s < STAGES; s++) { mbar_init(&ctl->full[s], 2); mbar_init(&ctl->empty[s], 1); }
+            // both CTAs) from each of the four producers of the MMA-issuing CTA
+            // empty: released by the MMAs of every pair whose copies write the stage
+            for (int s = 0; s < STAGES; s++) { mbar_init(&ctl->full[s], 4); mbar_init(&ctl->empty[s], QUAD ? 2 : 1); }
             for (int a = 0; a < 2; a++) {
                 mbar_init(&ctl->tfull[a], 1);
                 mbar_init(&ctl->tempty[a], PAIR ? 2 * EPI_WARPS : EPI_WARPS);
@@ -555,73 +584,86 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         }
     }
     tc_fence_before();
-    if (PAIR) cluster_sync();  // both CTAs' barriers initialised, TMEM allocated
+    if (PAIR) cluster_sync();  // every CTA's barriers initialised, TMEM allocated
     else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     int total = ctl->total_tiles;
     if (PAIR) {
-        int peer_bad;
-        asm volatile("ld.shared::cluster.u32 %0, [%1];"
-                     : "=r"(peer_bad)
-                     : "r"(map_to_rank(su32(&s_bad), rank ^ 1u)));
-        if (s_bad | peer_bad) total = 0;  // the same decision in both CTAs
+        int any_bad = 0;
+        for (uint32_t r = 0; r < (uint32_t)CL; r++) {
+            int b;
+            asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(b) : "r"(map_to_rank(su32(&s_bad), r)));
+            any_bad |= b;
+        }
+        if (any_bad) total = 0;  // the same decision in every CTA of the cluster
     }
     int32_t *abort_flag = &ctl->abort;
 
     if (warp == 0 || warp >= PROD_WARP0) {
         // ----------------------------------------------------- TMA producers
-        // Four issuing threads in different warps: prod 0/2 load A tiles, 1/3
-        // B tiles; prod 0/1 take the even ring stages, 2/3 the odd ones (lane 0
-        // of each issues).  In a pair both CTAs load their own halves; the
-        // copies complete on the first CTA's full barriers, whose producers
-        // announce the bytes of both.
+        // Four issuing threads in different warps: prod 0/2 load the two row
+        // halves of each stage's A tile, 1/3 those of its B tile (lane 0 of each
+        // issues).  In a pair both CTAs load their own halves; the copies
+        // complete on the pair-leading CTA's full barriers, whose producers
+        // announce the bytes of both.  With CL = 4 the A copies are multicast to
+        // the same rank of the other pair, which loads the other half of them.
         const int prod = warp == 0 ? 0 : warp - PROD_WARP0 + 1;
         const bool is_a = (prod & 1) == 0;
-        const int par = prod >> 1;
-        static_assert(STAGES % 2 == 0, "producers alternate stages");
+        const int hh = prod >> 1;   // row half of this producer's boxes
+        constexpr int A_BOX_BYTES = TL::A_BOX_ROWS * ROWB, B_BOX_BYTES = TL::B_BOX_ROWS * ROWB;
+        // bytes one producer's copies put into each CTA of its pair per stage
+        constexpr int MY_BYTES_ONE = QUAD ? 2 * A_BOX_BYTES : A_BOX_BYTES;
         int stage = 0;
         uint32_t phase = 0;
-        int it = 0, last_mine = -1;
+        int issued = 0;
         for (int t = tile0; t < total; t += tile_step) {
             Tile T = decode_tile(ctl->tile_start, e, t, BMT, kept_rows);
+            if (QUAD) T.nt = 2 * T.nt + (int)cpair;
+            // A: this CTA's 128 rows; with CL = 4 split in quarters: (pair, half)
+            const int a_sub = QUAD ? (int)cpair * 2 + hh : hh;
             const int a_row = (int)((int64_t)T.j * args.c_max + (int64_t)T.mt * BMT +
-                                    (int64_t)rank * TL::A_ROWS);
+                                    (int64_t)prank * TL::A_ROWS + (int64_t)a_sub * TL::A_BOX_ROWS);
             const int b_row = T.j * args.b_rows + T.nt * NOUT_TILE +
-                              (PAIR && EPI != EPI_SWIGLU ? (int)rank * TL::B_ROWS : 0);
-            for (int kb = 0; kb < nk; kb++, it++) {
-                if ((it & 1) == par) {
-                    int ok = 1;
-                    if (lane == 0) {
-                        ok = mbar_wait<PAIR>(&ctl->empty[stage], phase ^ 1u, abort_flag, args.status);
-                        if (ok && PAIR) {
-                            const uint32_t fb = map_to_rank(su32(&ctl->full[stage]), 0);
-                            if (is_a) {
-                                if (rank == 0) mbar_expect_tx(&ctl->full[stage], 2 * A_BYTES);
-                                tma_load_2d_pair(sA + stage * A_BYTES, &tmA, kb * BK, a_row, fb);
-                            } else {
-                                // SwiGLU: the first CTA's half of B is W1, the second's W3
-                                if (rank == 0) mbar_expect_tx(&ctl->full[stage], 2 * B_BYTES);
-                                tma_load_2d_pair(sB + stage * B_BYTES,
-                                                 EPI == EPI_SWIGLU && rank ? &tmB3 : &tmB, kb * BK,
-                                                 b_row, fb);
-                            }
-                        } else if (ok && is_a) {
-                            mbar_expect_tx(&ctl->full[stage], A_BYTES);
-                            tma_load_2d(sA + stage * A_BYTES, &tmA, kb * BK, a_row, &ctl->full[stage]);
-                        } else if (ok && EPI == EPI_SWIGLU) {
-                            mbar_expect_tx(&ctl->full[stage], B_BYTES);
-                            tma_load_2d(sB + stage * B_BYTES, &tmB, kb * BK, b_row, &ctl->full[stage]);
-                            tma_load_2d(sB + stage * B_BYTES + B_BYTES / 2, &tmB3, kb * BK, b_row,
-                                        &ctl->full[stage]);
-                        } else if (ok) {
-                            mbar_expect_tx(&ctl->full[stage], B_BYTES);
-                            tma_load_2d(sB + stage * B_BYTES, &tmB, kb * BK, b_row, &ctl->full[stage]);
+                              (PAIR && EPI != EPI_SWIGLU ? (int)prank * TL::B_ROWS : 0) +
+                              hh * TL::B_BOX_ROWS;
+            for (int kb = 0; kb < nk; kb++) {
+                int ok = 1;
+                if (lane == 0) {
+                    ok = mbar_wait<PAIR>(&ctl->empty[stage], phase ^ 1u, abort_flag, args.status);
+                    if (ok && PAIR) {
+                        const uint32_t fb = map_to_rank(su32(&ctl->full[stage]), lead);
+                        if (is_a) {
+                            if (prank == 0) mbar_expect_tx(&ctl->full[stage], 2 * MY_BYTES_ONE);
+                            if (QUAD)
+                                tma_load_2d_mcast(sA + stage * A_BYTES + a_sub * A_BOX_BYTES, &tmA, kb * BK,
+                                                  a_row, fb, (uint16_t)((1u << prank) | (1u << (prank + 2))));
+                            else
+                                tma_load_2d_pair(sA + stage * A_BYTES + a_sub * A_BOX_BYTES, &tmA, kb * BK,
+                                                 a_row, fb);
+                        } else {
+                            // SwiGLU: the first CTA's half of B is W1, the second's W3
+                            if (prank == 0) mbar_expect_tx(&ctl->full[stage], 2 * B_BOX_BYTES);
+                            tma_load_2d_pair(sB + stage * B_BYTES + hh * B_BOX_BYTES,
+                                             EPI == EPI_SWIGLU && prank ? &tmB3 : &tmB, kb * BK, b_row, fb);
                         }
+                    } else if (ok && is_a) {
+                        mbar_expect_tx(&ctl->full[stage], A_BOX_BYTES);
+                        tma_load_2d(sA + stage * A_BYTES + hh * A_BOX_BYTES, &tmA, kb * BK, a_row,
+                                    &ctl->full[stage]);
+                    } else if (ok && EPI == EPI_SWIGLU) {
+                        // W1 rows in the first half of the B tile, W3 rows in the second
+                        mbar_expect_tx(&ctl->full[stage], B_BOX_BYTES);
+                        tma_load_2d(sB + stage * B_BYTES + hh * B_BOX_BYTES, hh ? &tmB3 : &tmB, kb * BK,
+                                    b_row - hh * TL::B_BOX_ROWS, &ctl->full[stage]);
+                    } else if (ok) {
+                        mbar_expect_tx(&ctl->full[stage], B_BOX_BYTES);
+                        tma_load_2d(sB + stage * B_BYTES + hh * B_BOX_BYTES, &tmB, kb * BK, b_row,
+                                    &ctl->full[stage]);
                     }
-                    if (!__shfl_sync(0xffffffffu, ok, 0)) goto producer_done;
-                    last_mine = it;
                 }
+                if (!__shfl_sync(0xffffffffu, ok, 0)) goto producer_done;
+                issued++;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
@@ -630,9 +672,8 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         // can exit (a pair's second CTA cannot observe the first CTA's barriers:
         // its copies are covered by the MMAs that consume them, or on an abort
         // by the delay before the final cluster barrier)
-        if (lane == 0 && (!PAIR || rank == 0)) {
-            for (int i = max(0, last_mine + 1 - STAGES); i <= last_mine; i++) {
-                if ((i & 1) != par) continue;
+        if (lane == 0 && (!PAIR || prank == 0)) {
+            for (int i = max(0, issued - STAGES); i < issued; i++) {
                 int s = i % STAGES;
                 uint32_t ph = (uint32_t)((i / STAGES) & 1);
                 unsigned long long t0 = gtimer();
@@ -642,7 +683,10 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------------ MMA issuer
-        if (!PAIR || rank == 0) {
+        if (!PAIR || prank == 0) {
+            // the pair's own CTAs, and every CTA whose stages its copies fill
+            const uint16_t pair_mask = (uint16_t)(3u << (2 * cpair));
+            const uint16_t stage_mask = QUAD ? (uint16_t)0xF : pair_mask;
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -671,18 +715,18 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                         }
                     }
                     // stage reusable (in both CTAs of a pair) once these MMAs read it
-                    if (PAIR) umma_commit_pair(&ctl->empty[stage]);
+                    if (PAIR) umma_commit_pair(&ctl->empty[stage], stage_mask);
                     else umma_commit(&ctl->empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
                 // accumulator ready when all MMAs finish
-                if (PAIR) umma_commit_pair(&ctl->tfull[acc]);
+                if (PAIR) umma_commit_pair(&ctl->tfull[acc], pair_mask);
                 else umma_commit(&ctl->tfull[acc]);
                 if (++acc == TL::NACC) { acc = 0; acc_phase ^= 1u; }
             }
             // all MMAs issued by this thread complete before TMEM is released
-            if (PAIR) umma_commit_pair(&ctl->drain);
+            if (PAIR) umma_commit_pair(&ctl->drain, pair_mask);
             else umma_commit(&ctl->drain);
         }
         unsigned long long t0 = gtimer();
@@ -696,7 +740,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         const int ew = warp - 2;
         const int sub = warp & 3;             // TMEM lane quarter this warp may access
         const int half = ew >> 2;
-        const int row_in_tile = (int)rank * UM + (TM == 2 ? half * UM : 0) + sub * 32 + lane;
+        const int row_in_tile = (int)prank * UM + (TM == 2 ? half * UM : 0) + sub * 32 + lane;
         constexpr int COLS = TM == 2 ? NOUT_TILE : NOUT_TILE / 2;  // output columns per warp
         const int col0 = TM == 2 ? 0 : half * COLS;                // first output column
         uint8_t *stg = stg_all + ew * STG_WARP_BYTES;
@@ -704,6 +748,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         uint32_t acc_phase = 0;
         for (int t = tile0; t < total; t += tile_step) {
             Tile T = decode_tile(ctl->tile_start, e, t, BMT, kept_rows);
+            if (QUAD) T.nt = 2 * T.nt + (int)cpair;
             if (!mbar_wait<PAIR>(&ctl->tfull[acc], acc_phase, abort_flag, args.status)) break;
             tc_fence_after();
             const int row = T.mt * BMT + row_in_tile;
@@ -787,7 +832,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             __syncwarp();
             if (lane == 0) {
                 // a pair's accumulators are reused by the first CTA's MMAs
-                if (PAIR) mbar_arrive_cluster(map_to_rank(su32(&ctl->tempty[acc]), 0));
+                if (PAIR) mbar_arrive_cluster(map_to_rank(su32(&ctl->tempty[acc]), lead));
                 else mbar_arrive(&ctl->tempty[acc]);
             }
             if (++acc == TL::NACC) { acc = 0; acc_phase ^= 1u; }
@@ -870,17 +915,17 @@ int sm_count() {
     return cached[dev];
 }
 
-// Resident CTA pairs of a pair kernel with this configuration (the GPCs bound
-// how many 2-CTA clusters of ~200 KB shared memory fit at once).
+// Resident clusters of `cl` CTAs of a kernel with this configuration (the
+// GPCs bound how many clusters of ~200 KB-shared-memory CTAs fit at once).
 template <typename K>
-int max_pairs(K kern, size_t smem) {
+int max_clusters(K kern, size_t smem, int cl) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2);
+    cfg.gridDim = dim3(cl);
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = cl;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -888,18 +933,18 @@ int max_pairs(K kern, size_t smem) {
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, (const void *)kern, &cfg) != cudaSuccess || n < 1) {
         cudaGetLastError();
-        return sm_count() / 2;
+        return sm_count() / cl;
     }
     return n;
 }
 
-template <int EPI, int TM, int BK, bool PAIR>
+template <int EPI, int TM, int BK, int CL>
 moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &b3,
                        const CUtensorMap &o, const GemmArgs &args, cudaStream_t stream) {
-    using TL = Tiling<TM, BK, PAIR>;
-    auto kern = tc_group_gemm<EPI, TM, BK, PAIR>;
+    using TL = Tiling<TM, BK, CL>;
+    auto kern = tc_group_gemm<EPI, TM, BK, CL>;
     constexpr size_t SMEM = smem_bytes<TL>();
-    static int units[64] = {0};  // resident CTAs (1-SM) or CTA pairs, per device
+    static int units[64] = {0};  // resident CTAs (CL = 1) or clusters, per device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
     int nunits = dev >= 0 && dev < 64 ? units[dev] : 0;
@@ -907,19 +952,20 @@ moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtenso
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) !=
             cudaSuccess)
             return MOE_ERR_CUDA;
-        nunits = PAIR ? max_pairs(kern, SMEM) : sm_count();
+        nunits = CL > 1 ? max_clusters(kern, SMEM, CL) : sm_count();
         if (dev >= 0 && dev < 64) units[dev] = nunits;
     }
     constexpr int NOUT_TILE = EPI == EPI_SWIGLU ? BN / 2 : BN;
     int64_t ntn = (args.n_out + NOUT_TILE - 1) / NOUT_TILE;
+    if (TL::QUAD) ntn = (ntn + 1) / 2;
     int64_t upper = (int64_t)args.e * ((args.c_max + TL::BMT - 1) / TL::BMT) * ntn;
     int64_t grid = upper < nunits ? upper : nunits;
     if (grid < 1) grid = 1;
-    if (!PAIR)
+    if (CL == 1)
         return launch_pdl(kern, dim3((unsigned)grid), dim3(NUM_THREADS), SMEM, stream, a, b, b3, o,
                           args);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(2 * grid));
+    cfg.gridDim = dim3((unsigned)(CL * grid));
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = SMEM;
     cfg.stream = stream;
@@ -927,7 +973,7 @@ moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtenso
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.x = CL;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -953,34 +999,36 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
                          const void *w1, const void *b1, const void *w3, const void *w2,
                          const void *b2, moe_act act, int e, int64_t c_max, int m, int h,
                          void *hid, void *out, int32_t *st, cudaStream_t stream) {
-    // fc1: 256-row tiles on CTA pairs (2-SM MMA), two accumulators per CTA so
-    // its activation epilogue overlaps the next tile's main loop.  fc2
-    // (bias-only epilogue, long K): 256-row tiles per CTA, 32-deep stages.
+    // fc1: 256-row tiles on CTA pairs (2-SM MMA), two pairs per cluster sharing
+    // A by multicast, two accumulators per CTA so its activation epilogue
+    // overlaps the next tile's main loop.  fc2 (bias-only epilogue, long K):
+    // 256-row tiles per CTA, 32-deep stages.
     constexpr int TM1 = 1, BK1 = 64, TM2 = 2, BK2 = 32;
-    constexpr bool PAIR1 = true;
-    using T1 = Tiling<TM1, BK1, PAIR1>;
-    using T2 = Tiling<TM2, BK2, false>;
+    constexpr int CL1 = 4;
+    using T1 = Tiling<TM1, BK1, CL1>;
+    using T2 = Tiling<TM2, BK2, 1>;
     CUtensorMap mA1, mB1, mB3, mA2, mB2, mO1, mO2;
     const bool swiglu = act == MOE_ACT_SWIGLU;
     // one CTA's B box: a pair CTA's half tile, or a 1-SM SwiGLU tile's W1/W3 half
-    const uint32_t b1_box = PAIR1 || swiglu ? BN / 2 : BN;
-    if (!make_map(&mA1, buf, (uint64_t)e * c_max, (uint64_t)m, T1::A_ROWS, BK1) ||
+    // one producer's B box: half of a CTA's B rows (1-SM SwiGLU: the W1 or W3 half)
+    const uint32_t b1_box = T1::B_BOX_ROWS;
+    if (!make_map(&mA1, buf, (uint64_t)e * c_max, (uint64_t)m, T1::A_BOX_ROWS, BK1) ||
         !make_map(&mB1, w1, (uint64_t)e * h, (uint64_t)m, b1_box, BK1) ||
         !make_map(&mB3, swiglu ? w3 : w1, (uint64_t)e * h, (uint64_t)m, b1_box, BK1) ||
-        !make_map(&mA2, hid, (uint64_t)e * c_max, (uint64_t)h, T2::A_ROWS, BK2) ||
-        !make_map(&mB2, w2, (uint64_t)e * m, (uint64_t)h, T2::B_ROWS, BK2) ||
+        !make_map(&mA2, hid, (uint64_t)e * c_max, (uint64_t)h, T2::A_BOX_ROWS, BK2) ||
+        !make_map(&mB2, w2, (uint64_t)e * m, (uint64_t)h, T2::B_BOX_ROWS, BK2) ||
         !make_map(&mO1, hid, (uint64_t)e * c_max, (uint64_t)h, 32, 32) ||
         !make_map(&mO2, out, (uint64_t)e * c_max, (uint64_t)m, 32, 32))
         return MOE_ERR_CUDA;
     GemmArgs g1{counts, c_dev, st, (const __nv_bfloat16 *)b1, (__nv_bfloat16 *)hid, c_max, e, m, h, h};
     moe_status r;
-    if (swiglu) r = launch_gemm<EPI_SWIGLU, TM1, BK1, PAIR1>(mA1, mB1, mB3, mO1, g1, stream);
+    if (swiglu) r = launch_gemm<EPI_SWIGLU, TM1, BK1, CL1>(mA1, mB1, mB3, mO1, g1, stream);
     else if (act == MOE_ACT_GELU)
-        r = launch_gemm<EPI_GELU, TM1, BK1, PAIR1>(mA1, mB1, mB1, mO1, g1, stream);
-    else r = launch_gemm<EPI_RELU, TM1, BK1, PAIR1>(mA1, mB1, mB1, mO1, g1, stream);
+        r = launch_gemm<EPI_GELU, TM1, BK1, CL1>(mA1, mB1, mB1, mO1, g1, stream);
+    else r = launch_gemm<EPI_RELU, TM1, BK1, CL1>(mA1, mB1, mB1, mO1, g1, stream);
     if (r != MOE_OK) return r;
     GemmArgs g2{counts, c_dev, st, (const __nv_bfloat16 *)b2, (__nv_bfloat16 *)out, c_max, e, h, m, m};
-    return launch_gemm<EPI_BIAS, TM2, BK2, false>(mA2, mB2, mB2, mO2, g2, stream);
+    return launch_gemm<EPI_BIAS, TM2, BK2, 1>(mA2, mB2, mB2, mO2, g2, stream);
 }
 
 }  // namespace moe
