@@ -60,20 +60,24 @@ enum Epi { EPI_GELU = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_BIAS = 3 };
 // CL = 4: two such pairs compute the tiles (m, 2n) and (m, 2n+1), which share
 // their A rows: each CTA loads a quarter of the pair tile's A rows and
 // multicasts it to its counterpart in the other pair, a quarter fewer operand
-// bytes per SM again.
+// bytes per SM again.  TN = 2 (with CL = 2, TM = 1): the pair tile is 256 x 512
+// as two N = 256 MMAs sharing each A tile, one 512-column accumulator per CTA;
+// each SM then fills 48 KB of operands per 1024 MMA cycles instead of 32 KB per
+// 512 (the fill of shared memory, not L2, is what bounds the ring).
 // BK is the K depth of one pipeline stage: 64 bf16 (one 128-byte swizzle row)
 // or 32 (64-byte swizzle); the smaller stage doubles the number of stages in
 // the same shared memory, i.e. more operand bytes in flight to cover L2/HBM
 // latency.
-template <int TM, int BK_, int CL_ = 1>
+template <int TM, int BK_, int CL_ = 1, int TN_ = 1>
 struct Tiling {
+    static constexpr int TN = TN_;                        // N = 256 MMAs per K step (pairs)
     static constexpr int CL = CL_;                        // CTAs per cluster: 1, 2 or 4
     static constexpr bool PAIR = CL > 1;                  // 2-SM MMA on CTA pairs
     static constexpr bool QUAD = CL == 4;                 // two pairs sharing A by multicast
     static constexpr int BK = BK_;
     static constexpr int ROWB = BK * 2;                   // bytes per operand row
     static constexpr int A_ROWS = UM * TM;                // rows of A per CTA and stage
-    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;     // rows of B per CTA and stage
+    static constexpr int B_ROWS = PAIR ? TN * BN / 2 : BN;  // rows of B per CTA and stage
     static constexpr int BMT = A_ROWS * (PAIR ? 2 : 1);   // rows of A per tile
     static constexpr int A_BOX_ROWS = QUAD ? A_ROWS / 4 : A_ROWS / 2;  // rows of one A copy
     static constexpr int B_BOX_ROWS = B_ROWS / 2;                    // rows of one B copy
@@ -81,11 +85,12 @@ struct Tiling {
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = SMEM_RING / STAGE_BYTES;
-    static constexpr int NACC = TM == 1 ? 2 : 1;          // accumulator buffers
-    static constexpr int ACC_COLS = BN * TM;              // TMEM columns per buffer
+    static constexpr int NACC = TM == 1 && TN == 1 ? 2 : 1;  // accumulator buffers
+    static constexpr int ACC_COLS = BN * TM * TN;         // TMEM columns per buffer
     static_assert(BK == 64 || BK == 32, "BK");
     static_assert(CL == 1 || CL == 2 || CL == 4, "cluster size");
     static_assert(!PAIR || TM == 1, "pair tiles use one M=256 MMA");
+    static_assert(TN == 1 || (TN == 2 && CL == 2), "512-column tiles on plain CTA pairs");
     static_assert(STAGES >= 3 && STAGES <= 8, "stages");
 };
 
@@ -494,12 +499,13 @@ __device__ __forceinline__ Tile decode_tile(const int32_t *tile_start, int e, in
     return T;
 }
 
-template <int EPI, int TM, int BK, int CL>
+template <int EPI, int TM, int BK, int CL, int TN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmO,
               const GemmArgs args) {
-    using TL = Tiling<TM, BK, CL>;
+    using TL = Tiling<TM, BK, CL, TN>;
+    static_assert(TN == 1 || EPI != EPI_SWIGLU, "SwiGLU tiles pair W1 and W3 in one N = 256 MMA");
     constexpr bool PAIR = TL::PAIR, QUAD = TL::QUAD;
     constexpr int STAGES = TL::STAGES, BMT = TL::BMT, A_BYTES = TL::A_BYTES;
     constexpr int B_BYTES = TL::B_BYTES, ROWB = TL::ROWB;
@@ -529,7 +535,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     const uint32_t lead = rank & ~1u;    // the pair's MMA-issuing CTA
     const int tile0 = (int)(blockIdx.x / CL);
     const int tile_step = (int)(gridDim.x / CL);
-    constexpr int NOUT_TILE = EPI == EPI_SWIGLU ? BN / 2 : BN;  // output columns per tile
+    constexpr int NOUT_TILE = EPI == EPI_SWIGLU ? BN / 2 : BN * TN;  // output columns per tile
     const int ntn = (args.n_out + NOUT_TILE - 1) / NOUT_TILE;
     const int ntn_t = QUAD ? (ntn + 1) / 2 : ntn;               // N entries of the tile list
     const int nk = (args.K + BK - 1) / BK;
@@ -624,9 +630,12 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             const int a_sub = QUAD ? (int)cpair * 2 + hh : hh;
             const int a_row = (int)((int64_t)T.j * args.c_max + (int64_t)T.mt * BMT +
                                     (int64_t)prank * TL::A_ROWS + (int64_t)a_sub * TL::A_BOX_ROWS);
+            // B rows of this CTA: its half of the (each) N = 256 sub-tile; with
+            // TN = 2 producer hh loads N sub-tile hh
             const int b_row = T.j * args.b_rows + T.nt * NOUT_TILE +
-                              (PAIR && EPI != EPI_SWIGLU ? (int)prank * TL::B_ROWS : 0) +
-                              hh * TL::B_BOX_ROWS;
+                              (TN == 2 ? hh * BN + (int)prank * (BN / 2)
+                                       : (PAIR && EPI != EPI_SWIGLU ? (int)prank * TL::B_ROWS : 0) +
+                                             hh * TL::B_BOX_ROWS);
             for (int kb = 0; kb < nk; kb++) {
                 int ok = 1;
                 if (lane == 0) {
@@ -704,8 +713,11 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
 #pragma unroll
                     for (int kk = 0; kk < BK / UK; kk++) {
                         if (PAIR) {
-                            umma_pair(d, sdesc<ROWB>(a0 + kk * UK * 2), sdesc<ROWB>(b0 + kk * UK * 2),
-                                      (kb | kk) != 0);
+#pragma unroll
+                            for (int tn = 0; tn < TN; tn++)  // N sub-tiles share the A tile
+                                umma_pair(d + (uint32_t)(tn * BN), sdesc<ROWB>(a0 + kk * UK * 2),
+                                          sdesc<ROWB>(b0 + tn * (B_BYTES / TN) + kk * UK * 2),
+                                          (kb | kk) != 0);
                         } else {
 #pragma unroll
                             for (int hm = 0; hm < TM; hm++)  // M halves share the B tile
@@ -938,11 +950,11 @@ int max_clusters(K kern, size_t smem, int cl) {
     return n;
 }
 
-template <int EPI, int TM, int BK, int CL>
+template <int EPI, int TM, int BK, int CL, int TN>
 moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &b3,
                        const CUtensorMap &o, const GemmArgs &args, cudaStream_t stream) {
-    using TL = Tiling<TM, BK, CL>;
-    auto kern = tc_group_gemm<EPI, TM, BK, CL>;
+    using TL = Tiling<TM, BK, CL, TN>;
+    auto kern = tc_group_gemm<EPI, TM, BK, CL, TN>;
     constexpr size_t SMEM = smem_bytes<TL>();
     static int units[64] = {0};  // resident CTAs (CL = 1) or clusters, per device
     int dev = 0;
@@ -955,7 +967,7 @@ moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtenso
         nunits = CL > 1 ? max_clusters(kern, SMEM, CL) : sm_count();
         if (dev >= 0 && dev < 64) units[dev] = nunits;
     }
-    constexpr int NOUT_TILE = EPI == EPI_SWIGLU ? BN / 2 : BN;
+    constexpr int NOUT_TILE = EPI == EPI_SWIGLU ? BN / 2 : BN * TN;
     int64_t ntn = (args.n_out + NOUT_TILE - 1) / NOUT_TILE;
     if (TL::QUAD) ntn = (ntn + 1) / 2;
     int64_t upper = (int64_t)args.e * ((args.c_max + TL::BMT - 1) / TL::BMT) * ntn;
@@ -1001,12 +1013,12 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
                          void *hid, void *out, int32_t *st, cudaStream_t stream) {
     // fc1: 256-row tiles on CTA pairs (2-SM MMA), two pairs per cluster sharing
     // A by multicast, two accumulators per CTA so its activation epilogue
-    // overlaps the next tile's main loop.  fc2 (bias-only epilogue, long K):
-    // 256-row tiles per CTA, 32-deep stages.
-    constexpr int TM1 = 1, BK1 = 64, TM2 = 2, BK2 = 32;
-    constexpr int CL1 = 4;
+    // overlaps the next tile's main loop.  fc2 (bias-only epilogue, long K,
+    // about one tile per pair): 256 x 512 tiles on CTA pairs.
+    constexpr int TM1 = 1, BK1 = 64, TM2 = 1, BK2 = 64;
+    constexpr int CL1 = 4, CL2 = 2, TN2 = 2;
     using T1 = Tiling<TM1, BK1, CL1>;
-    using T2 = Tiling<TM2, BK2, 1>;
+    using T2 = Tiling<TM2, BK2, CL2, TN2>;
     CUtensorMap mA1, mB1, mB3, mA2, mB2, mO1, mO2;
     const bool swiglu = act == MOE_ACT_SWIGLU;
     // one CTA's B box: a pair CTA's half tile, or a 1-SM SwiGLU tile's W1/W3 half
@@ -1022,13 +1034,13 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
         return MOE_ERR_CUDA;
     GemmArgs g1{counts, c_dev, st, (const __nv_bfloat16 *)b1, (__nv_bfloat16 *)hid, c_max, e, m, h, h};
     moe_status r;
-    if (swiglu) r = launch_gemm<EPI_SWIGLU, TM1, BK1, CL1>(mA1, mB1, mB3, mO1, g1, stream);
+    if (swiglu) r = launch_gemm<EPI_SWIGLU, TM1, BK1, CL1, 1>(mA1, mB1, mB3, mO1, g1, stream);
     else if (act == MOE_ACT_GELU)
-        r = launch_gemm<EPI_GELU, TM1, BK1, CL1>(mA1, mB1, mB1, mO1, g1, stream);
-    else r = launch_gemm<EPI_RELU, TM1, BK1, CL1>(mA1, mB1, mB1, mO1, g1, stream);
+        r = launch_gemm<EPI_GELU, TM1, BK1, CL1, 1>(mA1, mB1, mB1, mO1, g1, stream);
+    else r = launch_gemm<EPI_RELU, TM1, BK1, CL1, 1>(mA1, mB1, mB1, mO1, g1, stream);
     if (r != MOE_OK) return r;
     GemmArgs g2{counts, c_dev, st, (const __nv_bfloat16 *)b2, (__nv_bfloat16 *)out, c_max, e, h, m, m};
-    return launch_gemm<EPI_BIAS, TM2, BK2, 1>(mA2, mB2, mB2, mO2, g2, stream);
+    return launch_gemm<EPI_BIAS, TM2, BK2, CL2, TN2>(mA2, mB2, mB2, mO2, g2, stream);
 }
 
 }  // namespace moe
