@@ -1011,12 +1011,14 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
                          const void *w1, const void *b1, const void *w3, const void *w2,
                          const void *b2, moe_act act, int e, int64_t c_max, int m, int h,
                          void *hid, void *out, int32_t *st, cudaStream_t stream) {
-    // fc1: 256-row tiles on CTA pairs (2-SM MMA), two pairs per cluster sharing
-    // A by multicast, two accumulators per CTA so its activation epilogue
-    // overlaps the next tile's main loop.  fc2 (bias-only epilogue, long K,
-    // about one tile per pair): 256 x 512 tiles on CTA pairs.
+    // fc1: 256-row tiles on CTA pairs (2-SM MMA), two accumulators per CTA so
+    // its activation epilogue overlaps the next tile's main loop (clusters of
+    // 4 sharing A by multicast move fewer L2 bytes, but only 36 such clusters
+    // fit against 76 pairs, and the shared-memory fill per SM is unchanged).
+    // fc2 (bias-only epilogue, long K, about one tile per pair): 256 x 512
+    // tiles on CTA pairs.
     constexpr int TM1 = 1, BK1 = 64, TM2 = 1, BK2 = 64;
-    constexpr int CL1 = 4, CL2 = 2, TN2 = 2;
+    constexpr int CL1 = 2, CL2 = 2, TN2 = 2;
     using T1 = Tiling<TM1, BK1, CL1>;
     using T2 = Tiling<TM2, BK2, CL2, TN2>;
     CUtensorMap mA1, mB1, mB3, mA2, mB2, mO1, mO2;
