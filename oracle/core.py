@@ -45,7 +45,7 @@ def _L():
             lib = ctypes.CDLL(build())
             P, I64, I32, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
             sig = {
-                "orc_gate_logits": [P, P, P, I64, I32, I32, P],
+                "orc_gate_logits": [P, P, P, I64, I32, I32, I32, P],
                 "orc_topk": [P, I64, I32, I32, P],
                 "orc_gates": [P, P, I64, I32, I32, I32, P],
                 "orc_locations": [P, I64, I32, I32, P, P],
@@ -96,13 +96,27 @@ def round_bf16(v: float) -> float:
     return float(_L().orc_round_bf16(float(v)))
 
 
-def gate_logits(x, wg, bias=None):
-    """fp32 logits [s, e]; ascending-i fmaf order, then + bias."""
+def gate_chunk(e, x_is_bf16):
+    """The logit summation order the layer uses for e experts: chunk width V of
+    the lane-blocked order (8 for bf16 x, 4 for fp32 x) for e <= 32, else 0 (one
+    sequential accumulator)."""
+    if e > 32:
+        return 0
+    return 8 if x_is_bf16 else 4
+
+
+def gate_logits(x, wg, bias=None, chunk=None):
+    """fp32 logits [s, e] in the layer's summation order (see orc_gate_logits),
+    then + bias.  chunk=None picks the order from e and from x's dtype (bf16 bits
+    given as uint16 -> 8, fp32 -> 4)."""
+    x_is_bf16 = np.asarray(x).dtype == np.uint16
     x, wg, bias = to_f32(x), to_f32(wg), to_f32(bias)
     s, m = x.shape
     e = wg.shape[1]
+    if chunk is None:
+        chunk = gate_chunk(e, x_is_bf16)
     out = np.empty((s, e), np.float32)
-    _L().orc_gate_logits(_p(x), _p(wg), _p(bias), s, m, e, _p(out))
+    _L().orc_gate_logits(_p(x), _p(wg), _p(bias), s, m, e, int(chunk), _p(out))
     return out
 
 

@@ -81,26 +81,60 @@ int orc_get_threads(void)
 /* Gate logits l[t,j] = x[t,:] . wg[:,j] + bias[j]   ([Tutel] gate_type 'top').
  *
  * Precision and order (the reading this build fixes so that top-k is
- * reproducible bit for bit): fp32, one accumulator per (t, j) starting from
- * +0, updated acc = fmaf(x[t,i], wg[i,j], acc) for i = 0, 1, ..., m-1 in
- * ascending order, then one fp32 add of bias[j] (skipped when bias is NULL).
+ * reproducible bit for bit): fp32 with one rounding per fused multiply-add,
+ * then one fp32 add of bias[j] (skipped when bias is NULL).  The summation
+ * order depends on `chunk`:
+ *   chunk = V > 0 (V = 8 for bf16 x, 4 for fp32 x; used for e <= 32): the
+ *     features are cut into chunks of V consecutive elements; chunk c belongs
+ *     to lane (c mod 32).  Each of the 32 lanes keeps one accumulator from +0
+ *     and applies acc = fmaf(x[t,i], wg[i,j], acc) to its features in
+ *     ascending i.  The lanes are then combined by a butterfly: for
+ *     o = 16, 8, 4, 2, 1 every lane l takes acc[l] + acc[l xor o] (one fp32
+ *     add; both partners get the same value), and the logit is lane 0's.
+ *   chunk = 0 (used for e > 32): one accumulator from +0, updated with fmaf
+ *     for i = 0, 1, ..., m-1 in ascending order.
  * x is [s, m] row-major, wg is [m, e] row-major, logits is [s, e]. */
 void orc_gate_logits(const float *x, const float *wg, const float *bias,
-                     int64_t s, int m, int e, float *logits)
+                     int64_t s, int m, int e, int chunk, float *logits)
 {
 #pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < s; t++) {
-        /* acc[j] is logit (t, j)'s single accumulator; the loops visit i in
-         * ascending order for every j (walking wg row by row). */
-        float *acc = logits + t * e;
-        for (int j = 0; j < e; j++) acc[j] = 0.0f;
-        for (int i = 0; i < m; i++) {
-            const float xi = x[t * m + i];
-            const float *wr = wg + (int64_t)i * e;
-            for (int j = 0; j < e; j++) acc[j] = fmaf(xi, wr[j], acc[j]);
+        float *out = logits + t * e;
+        if (chunk <= 0) {
+            /* out[j] is logit (t, j)'s single accumulator; the loops visit i
+             * in ascending order for every j (walking wg row by row). */
+            for (int j = 0; j < e; j++) out[j] = 0.0f;
+            for (int i = 0; i < m; i++) {
+                const float xi = x[t * m + i];
+                const float *wr = wg + (int64_t)i * e;
+                for (int j = 0; j < e; j++) out[j] = fmaf(xi, wr[j], out[j]);
+            }
+        } else {
+            float *lane = (float *)malloc(sizeof(float) * 32 * (size_t)e);
+            float nxt[32];
+            for (int q = 0; q < 32 * e; q++) lane[q] = 0.0f;
+            /* lane[l * e + j]: lane l's accumulator for expert j; features
+             * are visited in ascending order, so each lane's own features
+             * are too. */
+            for (int i = 0; i < m; i++) {
+                const int l = (i / chunk) % 32;
+                const float xi = x[t * m + i];
+                const float *wr = wg + (int64_t)i * e;
+                for (int j = 0; j < e; j++) lane[l * e + j] = fmaf(xi, wr[j], lane[l * e + j]);
+            }
+            for (int j = 0; j < e; j++) {
+                float v[32];
+                for (int l = 0; l < 32; l++) v[l] = lane[l * e + j];
+                for (int o = 16; o >= 1; o >>= 1) {
+                    for (int l = 0; l < 32; l++) nxt[l] = v[l] + v[l ^ o];
+                    for (int l = 0; l < 32; l++) v[l] = nxt[l];
+                }
+                out[j] = v[0];
+            }
+            free(lane);
         }
         if (bias)
-            for (int j = 0; j < e; j++) acc[j] = acc[j] + bias[j];
+            for (int j = 0; j < e; j++) out[j] = out[j] + bias[j];
     }
 }
 

@@ -28,7 +28,7 @@ def test_gate_logit_order_golden(case):
     x = np.array([case["x"]], np.float32)
     wg = np.array(case["wg"], np.float32)
     bias = None if case["bias"] is None else np.array(case["bias"], np.float32)
-    got = oracle.gate_logits(x, wg, bias)[0]
+    got = oracle.gate_logits(x, wg, bias, chunk=case["chunk"])[0]
     want = np.atleast_1d(np.array(case["logit"], np.float32))
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), (got, want)
 
@@ -50,9 +50,36 @@ def test_gate_logits_bf16_inputs_widen_exactly():
 
     xb = synth.normal_host(3, "x", (5, 16), 1.0, "bf16")
     wg = synth.normal_host(3, "wg", (16, 3), 0.25, "f32")
-    a = oracle.gate_logits(xb, wg)               # uint16 bits
-    b = oracle.gate_logits(synth.bf16_bits_to_f32(xb), wg)
+    a = oracle.gate_logits(xb, wg)               # uint16 bits: chunks of 8
+    b = oracle.gate_logits(synth.bf16_bits_to_f32(xb), wg, chunk=8)
     assert np.array_equal(a, b)
+
+
+def test_gate_chunk_follows_expert_count_and_dtype():
+    """The layer's order: lane-blocked chunks of one 16-byte load (8 bf16 or 4
+    fp32 elements) for e <= 32, one sequential accumulator above."""
+    assert oracle.gate_chunk(32, True) == 8 and oracle.gate_chunk(1, False) == 4
+    assert oracle.gate_chunk(33, True) == 0 and oracle.gate_chunk(256, False) == 0
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((3, 96)).astype(np.float32)
+    wg = rng.standard_normal((96, 40)).astype(np.float32)
+    seq = oracle.gate_logits(x, wg, chunk=0)
+    assert np.array_equal(oracle.gate_logits(x, wg), seq)          # e = 40 > 32
+    assert np.array_equal(oracle.gate_logits(x, wg[:, :8]),
+                          oracle.gate_logits(x, wg[:, :8], chunk=4))
+
+
+def test_gate_logits_orders_agree_to_rounding():
+    """Every order sums the same exact products: the two orders differ from the
+    exact (fp64) dot product by at most a few ulp of the sum of |products|."""
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((16, 1024)).astype(np.float32)
+    wg = (rng.standard_normal((1024, 8)) / 32).astype(np.float32)
+    exact = x.astype(np.float64) @ wg.astype(np.float64)
+    scale = np.abs(x.astype(np.float64)) @ np.abs(wg.astype(np.float64))
+    for chunk in (0, 4, 8):
+        got = oracle.gate_logits(x, wg, chunk=chunk).astype(np.float64)
+        assert np.all(np.abs(got - exact) <= 1024 * 2.0 ** -24 * scale), chunk
 
 
 def _brute_topk(v, k):
