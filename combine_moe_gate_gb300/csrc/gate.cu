@@ -4,13 +4,22 @@
 // gate) and the DeepSpeed-MoE vs Tutel blog, section 1.4 (top-k fused into one
 // kernel that emits a dense token-to-expert table instead of a one-hot mask).
 //
-// Logit order (fixed so routing is reproducible bit for bit): each logit has a
-// single fp32 accumulator starting at +0, updated with a fused multiply-add in
-// ascending feature index; the bias is then added once in fp32.  The kernel is
-// a register-blocked SIMT GEMM: every thread owns TT tokens x TE experts, and
-// each of its accumulators walks the features in ascending order, which is
-// exactly that contract.  Tensor cores are not used: their internal
-// accumulation order is unspecified and would make routing irreproducible.
+// Logit order (fixed so routing is reproducible bit for bit; fp32 with one
+// rounding per fused multiply-add, then one fp32 add of the bias):
+//   e <= 32: the features are cut into chunks of one 16-byte load (8 bf16 or 4
+//     fp32 elements); chunk c belongs to lane c mod 32, each lane accumulates
+//     its features from +0 in ascending index, and the 32 lane sums are
+//     combined by an xor butterfly (o = 16, 8, 4, 2, 1; the logit is lane 0's).
+//     gate_lane_kernel is exactly that: lane l of a warp owns chunk l of every
+//     512-byte slice of the feature axis.
+//   e > 32: one accumulator per logit from +0 in ascending feature index.
+//     gate_topk_kernel is a register-blocked SIMT GEMM: every thread owns TT
+//     tokens x TE experts, and each accumulator walks the features in order.
+//     (The lane-blocked order needs 32 live partial sums per logit; with all e
+//     experts of a token in one CTA, as the fused top-k needs, that leaves a
+//     CTA only a handful of tokens for large e.)
+// Tensor cores are not used: their internal accumulation order is unspecified
+// and would make routing irreproducible.
 #include "common.cuh"
 
 namespace moe {
@@ -74,6 +83,7 @@ struct GateCfg {
     static constexpr int LG_BYTES = TOKC * LGS * 4;
     static constexpr int SMEM = MAIN_BYTES > LG_BYTES ? MAIN_BYTES : LG_BYTES;
     static_assert(EP % TE == 0 && NT % EX == 0 && TE % 4 == 0 && STAGES >= 2, "layout");
+    static_assert(EP > 32, "e <= 32 uses the lane-blocked kernel (its logit order)");
 };
 
 template <class C, typename XT>
@@ -206,52 +216,7 @@ gate_topk_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
         }
     __syncthreads();
 
-    if constexpr (C::EP <= 32) {
-        // softmax + top-k, one thread per token: the token's <= 32 logits are read
-        // from the tile; selection scans experts in ascending index with a strict
-        // comparison, so equal logits go to the lower index.
-        for (int tl = tid; tl < C::TOKC; tl += C::NT) {
-            const int64_t t = t0 + tl;
-            if (t >= s) break;
-            float v[C::EP];
-            float mx = -INFINITY;
-#pragma unroll
-            for (int q = 0; q < C::EP; q++) {
-                v[q] = q < e ? lg[tl * C::LGS + q] : -INFINITY;
-                mx = fmaxf(mx, v[q]);
-            }
-            float z = 0.0f;
-#pragma unroll
-            for (int q = 0; q < C::EP; q++)
-                if (q < e) z += expf(v[q] - mx);
-            unsigned taken = 0;
-            float psel = 0.0f;
-            float pr[C::EP];
-#pragma unroll
-            for (int r = 0; r < C::EP; r++) {
-                if (r >= k) break;
-                float bv = -INFINITY;
-                int bj = 0;
-                bool found = false;
-#pragma unroll
-                for (int q = 0; q < C::EP; q++) {
-                    bool cand = q < e && !((taken >> q) & 1u);
-                    if (cand && (!found || v[q] > bv)) { bv = v[q]; bj = q; found = true; }
-                }
-                taken |= 1u << bj;
-                pr[r] = expf(bv - mx);
-                psel += pr[r];
-                idx[(int64_t)r * s + t] = bj;
-            }
-            const float den = normalize ? psel : z;
-#pragma unroll
-            for (int r = 0; r < C::EP; r++) {
-                if (r >= k) break;
-                gates[(int64_t)r * s + t] = pr[r] / den;
-            }
-        }
-        return;
-    } else {
+    {
         // softmax + top-k: one warp per token
         constexpr int NW = C::NT / 32;
         constexpr int QE = (C::EP + 31) / 32;  // experts per lane
@@ -316,143 +281,218 @@ gate_topk_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
 }
 
 // ---------------------------------------------------------------- small e
-// One thread per (token, expert) for e <= 32: the logit's single accumulator
-// walks the features in ascending order (the contract above) with no blocking,
-// so the batch runs as s*e independent chains.  The gate weight [m][e] is copied
-// whole into shared memory (the e threads of a token read consecutive words);
-// x reaches shared memory through a SK-deep cp.async ring of tiles of the CTA's
-// TPB tokens, so that a whole ring of x (not just a few registers per thread) is
-// in flight against HBM latency; the threads of a token read its features with
-// broadcast loads.  Softmax and top-k run on the EP lanes of each token with
-// segmented shuffles.  (KS below: features per tile, 512 bytes of each row.)
-constexpr int SK = 4;    // x tiles in flight
+// e <= 32: the lane-blocked logit order.  Each K tile is a 512-byte slice of
+// the feature axis, i.e. 32 chunks of one 16-byte load (V = 8 bf16 or 4 fp32
+// features); lane l of every warp owns chunk l of every tile, so over the tiles
+// it visits exactly the chunks c with c mod 32 = l, in ascending order.  A warp
+// computes T = 64 / EP tokens x all EP experts (64 accumulators per lane); its
+// lanes' x loads cover 512 contiguous bytes of a token row, and the K tile's
+// weight block is staged as [chunk][feature][expert] with each chunk's block
+// padded by 16 bytes, so the lanes' 16-byte weight loads fall on distinct
+// banks.  x rows and weight blocks stream through an SK-deep cp.async ring.
+// After the last tile an xor butterfly over the lanes finishes every logit,
+// and one lane per token does softmax and top-k.
+constexpr int SK = 4;    // K tiles in flight
+constexpr int LNW = 4;   // warps per CTA
 
 template <int EP, typename XT>
-struct SmallCfg {
-    static constexpr int KS = 512 / (int)sizeof(XT);             // features per x tile (512 B rows)
-    static constexpr int TPB = (256 / 32) * (32 / EP);           // tokens per CTA
-    static constexpr int XROWB = 512 + 16;                       // padded x tile row (bytes)
-    static constexpr int XBYTES = SK * TPB * XROWB;              // x ring
-    static_assert(XBYTES <= 140 * 1024, "x ring");
+struct LaneCfg {
+    static constexpr int V = 16 / (int)sizeof(XT);   // features per chunk (one 16-byte load)
+    static constexpr int KS = 32 * V;                // features per K tile
+    static constexpr int T = 64 / EP;                // tokens per warp
+    static constexpr int TC = LNW * T;               // tokens per CTA
+    static constexpr int XROWB = 512 + 16;           // x tile row (bytes, padded)
+    static constexpr int XB = TC * XROWB;            // x tile bytes
+    static constexpr int WCH = V * EP + 4;           // floats per chunk block of the weight tile
+    static constexpr int WB = 32 * WCH * 4;          // weight tile bytes
+    static constexpr int STAGE = XB + WB;
+    static constexpr int SMEM = SK * STAGE;
+    static_assert(EP >= 4 && EP <= 32 && 64 % EP == 0, "experts per CTA");
+    static_assert(XB % 16 == 0 && WB % 16 == 0, "16-byte stages");
 };
 
+// Feature u (compile-time) of a 16-byte chunk, widened exactly to fp32.
+template <typename XT, int U>
+__device__ __forceinline__ float chunk_elem(const V16 &v) {
+    if constexpr (sizeof(XT) == 2)
+        return (U & 1) ? bf16hi(v.w[U >> 1]) : bf16lo(v.w[U >> 1]);
+    else
+        return __uint_as_float(v.w[U]);
+}
+
+template <typename XT, int EP, int T, int U>
+__device__ __forceinline__ void lane_fma_feature(float (&acc)[T][EP], const V16 (&xv)[T],
+                                                 const float *wu) {
+    float w[EP];
+#pragma unroll
+    for (int q = 0; q < EP / 4; q++) {
+        const float4 w4 = reinterpret_cast<const float4 *>(wu)[q];
+        w[4 * q] = w4.x; w[4 * q + 1] = w4.y; w[4 * q + 2] = w4.z; w[4 * q + 3] = w4.w;
+    }
+#pragma unroll
+    for (int tt = 0; tt < T; tt++) {
+        const float xf = chunk_elem<XT, U>(xv[tt]);
+#pragma unroll
+        for (int jj = 0; jj < EP; jj++) acc[tt][jj] = fmaf(xf, w[jj], acc[tt][jj]);
+    }
+}
+
+template <typename XT, int EP, int T, int U, int V>
+__device__ __forceinline__ void lane_fma_chunk(float (&acc)[T][EP], const V16 (&xv)[T],
+                                               const float *wc) {
+    if constexpr (U < V) {
+        lane_fma_feature<XT, EP, T, U>(acc, xv, wc + U * EP);
+        lane_fma_chunk<XT, EP, T, U + 1, V>(acc, xv, wc);
+    }
+}
+
 template <int EP, typename XT>
-__global__ void __launch_bounds__(256)
-gate_small_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
-                  const float *__restrict__ bias, int64_t s, int m, int e, int k, int normalize,
-                  int32_t *__restrict__ idx, float *__restrict__ gates, int32_t *status) {
+__global__ void __launch_bounds__(LNW * 32)
+gate_lane_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
+                 const float *__restrict__ bias, int64_t s, int m, int e, int k, int normalize,
+                 int32_t *__restrict__ idx, float *__restrict__ gates, int32_t *status) {
     pdl_enter();
     if (status_bad(status)) return;
-    using SC = SmallCfg<EP, XT>;
-    constexpr int VEC = Elt<XT>::VEC, KS = SC::KS;
-    constexpr int CPR = KS / VEC;   // 16-byte chunks per token row per tile
-    extern __shared__ __align__(16) unsigned char smem_small[];
-    unsigned char *xs = smem_small;                          // [SK][TPB][XROWB]
-    float *wt = reinterpret_cast<float *>(smem_small + SC::XBYTES);  // [m][e]
-    const int64_t t0 = (int64_t)blockIdx.x * SC::TPB;
-    const int ntiles = (m + KS - 1) / KS;
-    auto load_x = [&](int tile) {
-        unsigned char *dst = xs + (tile % SK) * SC::TPB * SC::XROWB;
-        for (int q = threadIdx.x; q < SC::TPB * CPR; q += 256) {
-            const int row = q / CPR, ch = q % CPR;
+    using C = LaneCfg<EP, XT>;
+    constexpr int V = C::V, T = C::T, NT = LNW * 32;
+    extern __shared__ __align__(16) unsigned char smem_lane[];
+    const int64_t t0 = (int64_t)blockIdx.x * C::TC;
+    const int ntiles = (m + C::KS - 1) / C::KS;
+    const int nch = m / V;                               // m is a multiple of V
+    const bool wvec = e == EP;                           // whole 16-byte weight rows
+    auto load_tile = [&](int tile) {
+        unsigned char *st = smem_lane + (tile % SK) * C::STAGE;
+        for (int q = threadIdx.x; q < C::TC * 32; q += NT) {   // x: the CTA's rows, 32 chunks
+            const int row = q >> 5, ch = q & 31;
             const int64_t t = t0 + row;
-            const int f = tile * KS + ch * VEC;
+            const int f = tile * C::KS + ch * V;
             const bool ok = t < s && f < m;
-            cp_async16(dst + row * SC::XROWB + ch * 16, ok ? (const void *)(x + t * m + f) : (const void *)x,
-                       ok);
+            cp_async16(st + row * C::XROWB + ch * 16,
+                       ok ? (const void *)(x + t * m + f) : (const void *)x, ok);
+        }
+        float *wt = reinterpret_cast<float *>(st + C::XB);
+        if (wvec) {   // weight rows of EP floats, 16 bytes at a time
+            for (int q = threadIdx.x; q < C::KS * (EP / 4); q += NT) {
+                const int g = q % (EP / 4), r = q / (EP / 4);   // r = chunk * V + feature
+                const int ch = r / V, u = r - ch * V;
+                const int f = tile * C::KS + r;
+                const bool ok = f < m;
+                cp_async16(wt + ch * C::WCH + u * EP + g * 4,
+                           ok ? (const void *)(wg + (int64_t)f * e + g * 4) : (const void *)wg, ok);
+            }
+        } else {      // e < EP: one float at a time, zero for experts >= e
+            for (int q = threadIdx.x; q < C::KS * EP; q += NT) {
+                const int jj = q % EP, r = q / EP;
+                const int ch = r / V, u = r - ch * V;
+                const int f = tile * C::KS + r;
+                const bool ok = f < m && jj < e;
+                cp_async4(wt + ch * C::WCH + u * EP + jj,
+                          ok ? (const void *)(wg + (int64_t)f * e + jj) : (const void *)wg, ok);
+            }
         }
         cp_async_commit();
     };
 #pragma unroll
     for (int p = 0; p < SK - 1; p++) {
-        if (p < ntiles) load_x(p);
+        if (p < ntiles) load_tile(p);
         else cp_async_commit();
-    }
-    {   // the gate weight, [m][e] as in global memory, copied in one go
-        const int total = m * e;
-        if ((e & 3) == 0) {
-            for (int q = threadIdx.x * 4; q < total; q += 256 * 4)
-                cp_async16(wt + q, wg + q, true);
-        } else {
-            for (int q = threadIdx.x; q < total; q += 256) cp_async4(wt + q, wg + q, true);
-        }
-        cp_async_commit();
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    constexpr int TPW = 32 / EP;
-    const int j = lane % EP;
-    const int tl = warp * TPW + lane / EP;       // token within the CTA
-    const int64_t t = t0 + tl;
-    const bool live = t < s;
-    const float *wr = wt + (j < e ? j : 0);
-    float acc = 0.0f;
-    for (int it = 0; it < ntiles; it++) {
-        if (it == 0) cp_async_wait<0>();   // the weight (committed after the x prologue) and tile 0
-        else cp_async_wait<SK - 2>();
-        __syncthreads();   // tile `it` landed (and the weight staged); tile it-1 fully read
-        if (it + SK - 1 < ntiles) load_x(it + SK - 1);
-        else cp_async_commit();
-        const unsigned char *xr = xs + (it % SK) * SC::TPB * SC::XROWB + tl * SC::XROWB;
-        const int nfeat = min(KS, m - it * KS);
-        const float *w = wr + (int64_t)it * KS * e;
-        for (int c = 0; c < nfeat / VEC; c++) {
-            float f[VEC];
-            Elt<XT>::unpack(*reinterpret_cast<const V16 *>(xr + c * 16), f);
+    float acc[T][EP];
 #pragma unroll
-            for (int u = 0; u < VEC; u++) acc = fmaf(f[u], w[(c * VEC + u) * e], acc);
+    for (int tt = 0; tt < T; tt++)
+#pragma unroll
+        for (int jj = 0; jj < EP; jj++) acc[tt][jj] = 0.0f;
+    for (int it = 0; it < ntiles; it++) {
+        cp_async_wait<SK - 2>();
+        __syncthreads();   // tile `it` landed; tile it-1 fully read
+        if (it + SK - 1 < ntiles) load_tile(it + SK - 1);
+        else cp_async_commit();
+        if (it * 32 + lane < nch) {   // this lane's chunk of the tile holds features
+            const unsigned char *st = smem_lane + (it % SK) * C::STAGE;
+            V16 xv[T];
+#pragma unroll
+            for (int tt = 0; tt < T; tt++)
+                xv[tt] = *reinterpret_cast<const V16 *>(st + (warp * T + tt) * C::XROWB + lane * 16);
+            const float *wc = reinterpret_cast<const float *>(st + C::XB) + lane * C::WCH;
+            lane_fma_chunk<XT, EP, T, 0, V>(acc, xv, wc);
         }
     }
     cp_async_wait<0>();
-    float v = -INFINITY;
-    if (j < e) v = bias ? acc + bias[j] : acc;
-    // segmented (EP lanes per token) softmax statistics
-    float mx = v;
+    // xor butterfly over the lanes: every lane ends with every full logit
 #pragma unroll
-    for (int o = EP / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float z = j < e ? expf(v - mx) : 0.0f;
+    for (int o = 16; o >= 1; o >>= 1)
 #pragma unroll
-    for (int o = EP / 2; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-    // top-k: k rounds of segmented arg-max (ties -> lower expert index)
-    bool taken = j >= e;
-    float my_v = 0.0f;
-    int my_j = 0;
-    for (int r = 0; r < k; r++) {
-        float bv = taken ? -INFINITY : v;
-        int bj = taken ? 0x7fffffff : j;
+        for (int tt = 0; tt < T; tt++)
 #pragma unroll
-        for (int o = EP / 2; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
-            if (ov > bv || (ov == bv && oj < bj)) { bv = ov; bj = oj; }
+            for (int jj = 0; jj < EP; jj++)
+                acc[tt][jj] = acc[tt][jj] + __shfl_xor_sync(0xffffffffu, acc[tt][jj], o);
+    if (lane >= T) return;
+    const int64_t t = t0 + warp * T + lane;
+    if (t >= s) return;
+    // lane tt takes token tt's row (a static selection keeps it in registers)
+    float row[EP];
+#pragma unroll
+    for (int jj = 0; jj < EP; jj++) row[jj] = acc[0][jj];
+#pragma unroll
+    for (int tt = 1; tt < T; tt++)
+        if (lane == tt) {
+#pragma unroll
+            for (int jj = 0; jj < EP; jj++) row[jj] = acc[tt][jj];
         }
-        if (bj == j) taken = true;
-        if (j == r) { my_v = bv; my_j = bj; }
-    }
-    const float p = j < k ? expf(my_v - mx) : 0.0f;
-    float sel = p;
+    float mx = -INFINITY;
 #pragma unroll
-    for (int o = EP / 2; o > 0; o >>= 1) sel += __shfl_xor_sync(0xffffffffu, sel, o);
-    if (live && j < k) {
-        idx[(int64_t)j * s + t] = my_j;
-        gates[(int64_t)j * s + t] = p / (normalize ? sel : z);
+    for (int jj = 0; jj < EP; jj++)
+        if (jj < e) {
+            if (bias) row[jj] = row[jj] + bias[jj];
+            mx = fmaxf(mx, row[jj]);
+        }
+    float z = 0.0f;
+#pragma unroll
+    for (int jj = 0; jj < EP; jj++)
+        if (jj < e) z += expf(row[jj] - mx);
+    // top-k: k rounds of arg-max over the experts not yet taken (ties -> lower
+    // index); the first pass sums the selected probabilities, the second repeats
+    // the same selection and writes it
+    float sel = 0.0f;
+    for (int pass = 0; pass < 2; pass++) {
+        uint32_t taken = 0;
+        for (int r = 0; r < k; r++) {
+            int bj = -1;
+            float bv = -INFINITY;
+#pragma unroll
+            for (int jj = 0; jj < EP; jj++) {
+                if (jj < e && !(taken & (1u << jj)) && (bj < 0 || row[jj] > bv)) {
+                    bv = row[jj];
+                    bj = jj;
+                }
+            }
+            taken |= 1u << bj;
+            const float p = expf(bv - mx);
+            if (pass == 0) {
+                sel += p;
+            } else {
+                idx[(int64_t)r * s + t] = bj;
+                gates[(int64_t)r * s + t] = p / (normalize ? sel : z);
+            }
+        }
     }
 }
 
 template <int EP, typename XT>
-moe_status launch_small(const void *x, const float *wg, const float *bias, int64_t s, int m, int e,
-                        int k, int normalize, int32_t *idx, float *gates, int32_t *st,
-                        cudaStream_t stream) {
-    auto kern = gate_small_kernel<EP, XT>;
-    const size_t smem = SmallCfg<EP, XT>::XBYTES + (size_t)m * e * sizeof(float);
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+moe_status launch_lane(const void *x, const float *wg, const float *bias, int64_t s, int m, int e,
+                       int k, int normalize, int32_t *idx, float *gates, int32_t *st,
+                       cudaStream_t stream) {
+    using C = LaneCfg<EP, XT>;
+    auto kern = gate_lane_kernel<EP, XT>;
+    if (C::SMEM > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
             cudaSuccess)
         return MOE_ERR_CUDA;
-    constexpr int TPB = SmallCfg<EP, XT>::TPB;
-    const int64_t grid = (s + TPB - 1) / TPB;
+    const int64_t grid = (s + C::TC - 1) / C::TC;
     if (grid > 0x7fffffff) return MOE_ERR_UNSUPPORTED;
-    return launch_pdl(kern, dim3((unsigned)grid), dim3(256), smem, stream, (const XT *)x, wg, bias, s,
-                      m, e, k, normalize, idx, gates, st);
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(LNW * 32), C::SMEM, stream, (const XT *)x, wg,
+                      bias, s, m, e, k, normalize, idx, gates, st);
 }
 
 template <class C, typename XT>
@@ -471,9 +511,6 @@ moe_status launch_cfg(const void *x, const float *wg, const float *bias, int64_t
                       bias, s, m, e, k, normalize, idx, gates, st);
 }
 
-// Shared memory the small-e kernel may use for the transposed gate weight.
-constexpr size_t SMALL_E_SMEM_MAX = 64 * 1024;
-
 template <typename XT>
 moe_status gate_dispatch(const void *x, const float *wg, const float *bias, int64_t s, int m, int e,
                          int k, int normalize, int32_t *idx, float *gates, int32_t *st,
@@ -482,21 +519,12 @@ moe_status gate_dispatch(const void *x, const float *wg, const float *bias, int6
     if (e <= EPV)                                                                           \
         return launch_cfg<GateCfg<EPV, TEV, TTV, NTV, KTV, STV, XT>, XT>(                   \
             x, wg, bias, s, m, e, k, normalize, idx, gates, st, stream);
-    // small e whose transposed weight fits in shared memory: one chain per thread
-#define MOE_GATE_SMALL(EPV)                                                                  \
-    if (e <= EPV && (size_t)m * e * sizeof(float) <= SMALL_E_SMEM_MAX)                       \
-        return launch_small<EPV, XT>(x, wg, bias, s, m, e, k, normalize, idx, gates, st, stream);
-    MOE_GATE_SMALL(4)
-    MOE_GATE_SMALL(8)
-    MOE_GATE_SMALL(16)
-    MOE_GATE_SMALL(32)
-#undef MOE_GATE_SMALL
-    // otherwise: HBM/latency bound -> few tokens per CTA, long tiles, deep pipeline;
-    // large e: fp32-FMA bound -> register-blocked 8x8 micro-tiles
-    MOE_GATE_CASE(4, 4, 1, 64, 128, 4)
-    MOE_GATE_CASE(8, 4, 1, 64, 128, 4)
-    MOE_GATE_CASE(16, 4, 1, 128, 128, 3)
-    MOE_GATE_CASE(32, 8, 1, 128, 64, 4)
+    // e <= 32: lane-blocked order, all experts of a token in one warp
+    if (e <= 4) return launch_lane<4, XT>(x, wg, bias, s, m, e, k, normalize, idx, gates, st, stream);
+    if (e <= 8) return launch_lane<8, XT>(x, wg, bias, s, m, e, k, normalize, idx, gates, st, stream);
+    if (e <= 16) return launch_lane<16, XT>(x, wg, bias, s, m, e, k, normalize, idx, gates, st, stream);
+    if (e <= 32) return launch_lane<32, XT>(x, wg, bias, s, m, e, k, normalize, idx, gates, st, stream);
+    // e > 32: fp32-FMA bound -> register-blocked 8x8 micro-tiles, sequential order
     MOE_GATE_CASE(64, 8, 8, 128, 32, 3)
     MOE_GATE_CASE(128, 8, 8, 256, 32, 2)
     MOE_GATE_CASE(256, 8, 8, 256, 32, 2)

@@ -72,9 +72,15 @@ typedef enum {
 
 /*
  * Gate ([Tutel] gate_type 'top'; [Blog] 1.4 fused top-k).
- *   logits[t, j] = fp32 dot(x[t, :], wg[:, j]) + bias[j], with one accumulator
- *   from +0 updated by fused multiply-add in ascending feature index, then one
- *   fp32 add of the bias.  This fixed order makes idx reproducible bit for bit.
+ *   logits[t, j] = fp32 dot(x[t, :], wg[:, j]) + bias[j], fused multiply-adds
+ *   (one rounding each) in a fixed order, then one fp32 add of the bias:
+ *     e <= 32: the features are cut into chunks of one 16-byte load (8 bf16 or
+ *       4 fp32 elements); chunk c goes to lane c mod 32; each of the 32 lanes
+ *       accumulates its features from +0 in ascending index; the lane sums are
+ *       combined by an xor butterfly (o = 16, 8, 4, 2, 1: v[l] + v[l xor o]),
+ *       and the logit is lane 0's value.
+ *     e > 32: one accumulator from +0 in ascending feature index.
+ *   This fixed order makes idx reproducible bit for bit.
  *   idx[r, t]: expert at position r when experts are ordered by (logit
  *   descending, index ascending).  gates[r, t]: softmax probability of that
  *   expert over all e logits; with MOE_FLAG_NORMALIZE_GATES divided by the sum
