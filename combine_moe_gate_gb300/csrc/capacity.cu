@@ -136,7 +136,7 @@ cap_assign_kernel(const int32_t *__restrict__ idx, int64_t n, int e, int nblk,
 // its base offsets, then ranks its own chunk stably as cap_assign does.  The
 // last CTA, which has seen every route, writes counts[], c and the overflow
 // status.
-constexpr int CAPS_NT = 256, CAPS_NW = CAPS_NT / 32, CAPS_CH = 1024, CAPS_MAXE = 256;
+constexpr int CAPS_NT = 1024, CAPS_NW = CAPS_NT / 32, CAPS_CH = 1024, CAPS_MAXE = 256;
 constexpr int CAPS_ROUNDS = CAPS_CH / CAPS_NT;   // routes per thread (own chunk)
 constexpr int CAPS_MAXBLK = 16;
 
@@ -151,7 +151,7 @@ cap_small_kernel(const int32_t *__restrict__ idx, int64_t n, int e, int c_fixed,
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int q = tid; q < CAPS_MAXE; q += CAPS_NT) base[q] = 0;
     for (int q = tid; q < CAPS_NW * CAPS_MAXE; q += CAPS_NT) (&wcnt[0][0])[q] = 0;
-    // own chunk: warp w takes routes [w*128, (w+1)*128) of it, 4 rounds of 32
+    // own chunk: warp w takes routes [w*32*R, (w+1)*32*R) of it, R = CAPS_ROUNDS rounds of 32
     const int64_t seg0 = (int64_t)blockIdx.x * CAPS_CH + warp * 32 * CAPS_ROUNDS;
     int32_t val[CAPS_ROUNDS], rank[CAPS_ROUNDS];
 #pragma unroll
