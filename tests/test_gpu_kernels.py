@@ -30,6 +30,9 @@ GATE_CASES = [
     _w(s=129, m=256, e=256, k=8, h=64, skew_alpha=2.0),
     _w(s=77, m=40, e=5, k=5, h=64),
     _w(s=64, m=32, e=3, k=1, h=64, dtype="f32", normalize_gates=False),
+    # several 512-byte feature slices with a ragged last one (lane-blocked order)
+    _w(s=150, m=520, e=7, k=2, h=64, dtype="f32"),
+    _w(s=100, m=1032, e=32, k=4, h=64, skew_alpha=0.5),
 ]
 
 
