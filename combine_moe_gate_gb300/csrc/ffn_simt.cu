@@ -21,10 +21,8 @@ __device__ __forceinline__ float silu(float a) { return a / (1.0f + expf(-a)); }
 
 template <typename T> __device__ __forceinline__ float ldf(const T *p);
 template <> __device__ __forceinline__ float ldf<float>(const float *p) { return *p; }
-template <> __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 template <typename T> __device__ __forceinline__ T stf(float v);
 template <> __device__ __forceinline__ float stf<float>(float v) { return v; }
-template <> __device__ __forceinline__ __nv_bfloat16 stf<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
 
 // A: [e, c_max, K] rows; B, B3: [e, N, K]; bias [e, N]; C: [e, c_max, N].
 template <typename T, int EPI>

@@ -425,36 +425,16 @@ __device__ __forceinline__ void tmem_tie(uint32_t (&r)[32]) {
                    "+r"(r[30]), "+r"(r[31]));
 }
 
-// erfc(x) for x >= 0 by Abramowitz & Stegun, Handbook of Mathematical
-// Functions, formula 7.1.28 (Hastings): erf(x) = 1 - (1 + a1 x + ... + a6 x^6)^-16
-// with |error| <= 3e-7, so erfc(x) = (1 + a1 x + ... + a6 x^6)^-16.  One
-// reciprocal and no exponential, which keeps the fc1 epilogue cheap; the error
-// is three orders of magnitude below the bf16 rounding that follows.
-__device__ __forceinline__ float erfc_as7128(float x) {
-    float p = fmaf(x, 0.0000430638f, 0.0002765672f);
-    p = fmaf(x, p, 0.0001520143f);
-    p = fmaf(x, p, 0.0092705272f);
-    p = fmaf(x, p, 0.0422820123f);
-    p = fmaf(x, p, 0.0705230784f);
-    p = fmaf(x, p, 1.0f);
-    float q = p * p;   // ^2
-    q = q * q;         // ^4
-    q = q * q;         // ^8
-    q = q * q;         // ^16 (overflows to inf for large x: erfc -> 0)
-    float r;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(q));
-    return r;
-}
-
 // GELU, exact erf form: a * Phi(a) with Phi(a) = 0.5 (1 + erf(a / sqrt 2)),
 // evaluated as 1 - erfc/2 for a >= 0 and erfc(|a| / sqrt 2) / 2 for a < 0 so
-// that the negative tail does not cancel.  |GELU error| <= 5e-7.
-__device__ __forceinline__ float gelu_erf(float a) {
-    const float r = 0.5f * erfc_as7128(fabsf(a) * 0.70710678118654752f);
-    return a * (a >= 0.0f ? 1.0f - r : r);
-}
-
-// The same GELU on a pair of values with packed fp32x2 arithmetic.
+// that the negative tail does not cancel.  erfc(x) for x >= 0 by Abramowitz &
+// Stegun, Handbook of Mathematical Functions, formula 7.1.28 (Hastings):
+// erf(x) = 1 - (1 + a1 x + ... + a6 x^6)^-16 with |error| <= 3e-7, so
+// erfc(x) = (1 + a1 x + ... + a6 x^6)^-16: one reciprocal and no exponential,
+// which keeps the fc1 epilogue cheap; |GELU error| <= 5e-7, three orders of
+// magnitude below the bf16 rounding that follows.  Two values at a time with
+// packed fp32x2 arithmetic; the 16th power overflows to inf for large x, where
+// erfc -> 0.
 __device__ __forceinline__ float2 gelu_erf2(float2 a) {
     const float2 x = __fmul2_rn(make_float2(fabsf(a.x), fabsf(a.y)),
                                 make_float2(0.70710678118654752f, 0.70710678118654752f));
