@@ -19,6 +19,7 @@ from .core import (  # noqa: F401
     encode,
     encode_bwd,
     ffn_rows,
+    gate_bwd,
     gate_chunk,
     gate_logits,
     gates,

@@ -46,6 +46,7 @@ def _L():
             P, I64, I32, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
             sig = {
                 "orc_gate_logits": [P, P, P, I64, I32, I32, I32, P],
+                "orc_gate_bwd": [P, P, P, P, P, I64, I32, I32, I32, I32, P, P, P, P],
                 "orc_topk": [P, I64, I32, I32, P],
                 "orc_gates": [P, P, I64, I32, I32, I32, P],
                 "orc_locations": [P, I64, I32, I32, P, P],
@@ -136,6 +137,24 @@ def gates(logits, idx, normalize):
     g = np.empty((k, s), np.float32)
     _L().orc_gates(_p(logits), _p(idx), s, e, k, int(bool(normalize)), _p(g))
     return g
+
+
+def gate_bwd(x, wg, bias, idx, d_gates, normalize, chunk=None):
+    """Backward of the gate values to the logits, the gate weight, its bias and
+    x (float64 arrays d_logits [s, e], d_wg [m, e], d_bias [e], d_x [s, m]);
+    the forward logits are recomputed in the layer's order."""
+    lg = gate_logits(x, wg, bias, chunk)
+    x, wg = to_f32(x), to_f32(wg)
+    idx = np.ascontiguousarray(idx, np.int32)
+    dg = np.ascontiguousarray(d_gates, np.float32)
+    s, m = x.shape
+    e = wg.shape[1]
+    k = idx.shape[0]
+    out = dict(d_logits=np.empty((s, e)), d_wg=np.empty((m, e)), d_bias=np.empty(e),
+               d_x=np.empty((s, m)))
+    _L().orc_gate_bwd(_p(x), _p(wg), _p(lg), _p(idx), _p(dg), s, m, e, k, int(bool(normalize)),
+                      _p(out["d_logits"]), _p(out["d_wg"]), _p(out["d_bias"]), _p(out["d_x"]))
+    return out
 
 
 def locations(idx, e):

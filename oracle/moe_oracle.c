@@ -186,6 +186,69 @@ void orc_gates(const float *logits, const int32_t *idx, int64_t s, int e, int k,
     }
 }
 
+/* Backward of the gate values ([Tutel] gate_type 'top': gates are softmax
+ * probabilities of the k selected experts, renormalised over them when
+ * `normalize`).  Top-k selection is piecewise constant, so gradients flow only
+ * through the softmax.  In double, from the forward's fp32 logits:
+ *   p = softmax(l) over all e experts, A = sum_r dg_r g_r with g_r the gate
+ *   value of route r (recomputed in double);
+ *   normalize:  g_r = p_{i_r} / sum_q p_{i_q};  dl_{i_r} = g_r (dg_r - A), other
+ *               experts 0  (the renormalised gates are a softmax over the
+ *               selected logits alone);
+ *   otherwise:  g_r = p_{i_r};  dl_j = -p_j A + sum_{r: i_r = j} dg_r g_r.
+ * Then through l = x Wg + b:  d_wg[i,j] = sum_t x[t,i] dl[t,j],
+ * d_bias[j] = sum_t dl[t,j],  d_x[t,i] = sum_j dl[t,j] wg[i,j].
+ * Shapes: x [s, m], wg [m, e], logits [s, e], idx / d_gates [k, s];
+ * outputs d_logits [s, e], d_wg [m, e], d_bias [e], d_x [s, m] (double). */
+void orc_gate_bwd(const float *x, const float *wg, const float *logits, const int32_t *idx,
+                  const float *d_gates, int64_t s, int m, int e, int k, int normalize,
+                  double *d_logits, double *d_wg, double *d_bias, double *d_x)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < s; t++) {
+        const float *l = logits + t * e;
+        double *dl = d_logits + t * e;
+        double mx = l[0];
+        for (int j = 1; j < e; j++) if (l[j] > mx) mx = l[j];
+        double z = 0.0;
+        for (int j = 0; j < e; j++) z += exp((double)l[j] - mx);
+        double sel = 0.0;
+        for (int r = 0; r < k; r++) sel += exp((double)l[idx[(int64_t)r * s + t]] - mx) / z;
+        double a = 0.0;
+        for (int r = 0; r < k; r++) {
+            const int j = idx[(int64_t)r * s + t];
+            const double p = exp((double)l[j] - mx) / z;
+            const double g = normalize ? p / sel : p;
+            a += (double)d_gates[(int64_t)r * s + t] * g;
+        }
+        for (int j = 0; j < e; j++) dl[j] = normalize ? 0.0 : -(exp((double)l[j] - mx) / z) * a;
+        for (int r = 0; r < k; r++) {
+            const int j = idx[(int64_t)r * s + t];
+            const double p = exp((double)l[j] - mx) / z;
+            const double g = normalize ? p / sel : p;
+            const double dg = d_gates[(int64_t)r * s + t];
+            dl[j] += normalize ? g * (dg - a) : dg * g;
+        }
+        for (int i = 0; i < m; i++) {
+            double acc = 0.0;
+            for (int j = 0; j < e; j++) acc += dl[j] * (double)wg[(int64_t)i * e + j];
+            d_x[t * m + i] = acc;
+        }
+    }
+    for (int j = 0; j < e; j++) {
+        double acc = 0.0;
+        for (int64_t t = 0; t < s; t++) acc += d_logits[t * e + j];
+        d_bias[j] = acc;
+    }
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < m; i++)
+        for (int j = 0; j < e; j++) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < s; t++) acc += (double)x[t * m + i] * d_logits[t * e + j];
+            d_wg[(int64_t)i * e + j] = acc;
+        }
+}
+
 /* --------------------------------------------------------------- capacity */
 
 /* Slot assignment as a sequential queue ([Blog] 1.4: the cumsum over the
