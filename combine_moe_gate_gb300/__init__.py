@@ -7,7 +7,7 @@ is missing, importing the entry points raises.
 
 Functions keep the C names:
     moe_gate_topk, moe_capacity_locations, moe_encode, moe_expert_ffn,
-    moe_decode, moe_decode_bwd, moe_encode_bwd, moe_layer_forward
+    moe_decode, moe_decode_bwd, moe_encode_bwd, moe_layer_forward, moe_gate_bwd
 plus the size queries and `MoEError`.
 """
 
@@ -47,6 +47,7 @@ def load():
                            ctypes.c_float, ctypes.c_size_t)
     sigs = {
         "moe_gate_topk": (I, [P, I, P, P, I64, I, I, I, U, P, P, P, P]),
+        "moe_gate_bwd": (I, [P, I, P, P, I64, I, I, I, U, P, P, P, P, P, P, P, P, P]),
         "moe_capacity_bound": (I64, [F, I64, I, I]),
         "moe_capacity_workspace_size": (SZ, [I64, I, I]),
         "moe_capacity_locations": (I, [P, I64, I, I, F, I64, P, SZ, P, P, P, P, P]),
@@ -191,6 +192,19 @@ def moe_decode_bwd(dy, out, idx, loc, gates, counts, c_dev, d_out, d_gates, dev_
         _ptr(dy), _ptr(out), _dt(out), _ptr(idx), _ptr(loc), _ptr(gates), _ptr(counts),
         _ptr(c_dev), s, m, e, k, c_max, int(flags), _ptr(d_out), _ptr(d_gates), _ptr(dev_status),
         _stream(stream)), "moe_decode_bwd")
+
+
+def moe_gate_bwd(x, wg, bias, idx, gates, d_gates, d_logits, dev_status, d_wg=None, d_bias=None,
+                 d_x=None, flags=0, stream=None):
+    """Gate backward: d_gates [k, s] fp32 -> d_logits [s, e] and, when given,
+    d_wg [m, e], d_bias [e], d_x [s, m] (all fp32)."""
+    s, m = x.shape
+    e = wg.shape[1]
+    k = idx.shape[0]
+    _check(load().moe_gate_bwd(_ptr(x), _dt(x), _ptr(wg), _ptr(bias), s, m, e, k, int(flags),
+                               _ptr(idx), _ptr(gates), _ptr(d_gates), _ptr(d_logits), _ptr(d_wg),
+                               _ptr(d_bias), _ptr(d_x), _ptr(dev_status), _stream(stream)),
+           "moe_gate_bwd")
 
 
 def moe_encode_bwd(d_buf, idx, loc, c_dev, dx, dev_status, stream=None):

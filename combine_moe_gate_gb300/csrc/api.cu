@@ -12,6 +12,10 @@ void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 moe_status gate_topk_launch(const void *x, moe_dtype xdt, const float *wg, const float *bias,
                             int64_t s, int m, int e, int k, unsigned flags, int32_t *idx,
                             float *gates, int32_t *st, cudaStream_t stream);
+moe_status gate_bwd_launch(const void *x, moe_dtype xdt, const float *wg, const float *bias,
+                           int64_t s, int m, int e, int k, unsigned flags, const int32_t *idx,
+                           const float *gates, const float *d_gates, float *d_logits, float *d_wg,
+                           float *d_bias, float *d_x, int32_t *st, cudaStream_t stream);
 int64_t capacity_bound_host(float f, int64_t s, int e, int k);
 size_t capacity_workspace_bytes(int64_t s, int e, int k);
 moe_status capacity_launch(const int32_t *idx, int64_t s, int e, int k, float f, int64_t c_max,
@@ -95,6 +99,19 @@ moe_status moe_gate_topk(const void *x, moe_dtype xdt, const float *wg, const fl
     if (e > 256) return MOE_ERR_UNSUPPORTED;
     return gate_topk_launch(x, xdt, wg, bias, s, m, e, k, flags, idx, gates, dev_status,
                             as_stream(stream));
+}
+
+moe_status moe_gate_bwd(const void *x, moe_dtype xdt, const float *wg, const float *bias,
+                        int64_t s, int m, int e, int k, unsigned flags, const int32_t *idx,
+                        const float *gates, const float *d_gates, float *d_logits, float *d_wg,
+                        float *d_bias, float *d_x, int32_t *dev_status, void *stream) {
+    if (!routing_shape_ok(s, e, k) || !rows_ok(xdt, m) || !ok16(x) || !ok16(wg) ||
+        !opt16(bias) || !ok4(idx) || !ok4(gates) || !ok4(d_gates) || !ok4(d_logits) ||
+        !opt16(d_wg) || !opt16(d_bias) || !opt16(d_x) || !ok4(dev_status) || (flags & ~3u))
+        return MOE_ERR_INVALID_ARG;
+    if (e > 256) return MOE_ERR_UNSUPPORTED;
+    return gate_bwd_launch(x, xdt, wg, bias, s, m, e, k, flags, idx, gates, d_gates, d_logits,
+                           d_wg, d_bias, d_x, dev_status, as_stream(stream));
 }
 
 int64_t moe_capacity_bound(float capacity_factor, int64_t s, int e, int k) {

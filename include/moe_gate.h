@@ -223,6 +223,28 @@ moe_status moe_encode_bwd(const void *d_buf, moe_dtype dt, const int32_t *idx,
                           const int32_t *loc, const int32_t *c_dev, int64_t s, int m, int e,
                           int k, int64_t c_max, void *dx, int32_t *dev_status, void *stream);
 
+/*
+ * Gate backward ([Tutel] gate_type 'top': the gates are softmax probabilities
+ * of the k selected experts, renormalised over them with
+ * MOE_FLAG_NORMALIZE_GATES).  Top-k selection is piecewise constant, so the
+ * gradient flows through the softmax only.  With A = sum_r dg[r,t] g[r,t]:
+ *   renormalised:  d_logits[t, idx[r,t]] = g (dg - A), other experts 0;
+ *   raw softmax:   d_logits[t, j] = -p_j A + sum over routes r to j of dg g,
+ *                  p = softmax of the logits (recomputed here from x, wg, bias);
+ *   d_wg = x^T d_logits [m, e],  d_bias = sum over t of d_logits [e],
+ *   d_x = d_logits wg^T [s, m].
+ * Inputs: x [s, m] in `xdt`; wg [m, e] fp32; bias [e] fp32 or NULL (used only
+ * to recompute the logits of the raw softmax); idx, gates [k, s] as the gate
+ * wrote them; d_gates [k, s] fp32 (e.g. moe_decode_bwd's).  Outputs, all fp32,
+ * each one sequential fp32 sum: d_logits [s, e] (required), d_wg [m, e],
+ * d_bias [e], d_x [s, m] (each may be NULL).  e <= 256 here.
+ * This entry point extends the pages' forward gate to its backward.
+ */
+moe_status moe_gate_bwd(const void *x, moe_dtype xdt, const float *wg, const float *bias,
+                        int64_t s, int m, int e, int k, unsigned flags, const int32_t *idx,
+                        const float *gates, const float *d_gates, float *d_logits, float *d_wg,
+                        float *d_bias, float *d_x, int32_t *dev_status, void *stream);
+
 /* Bytes of device workspace moe_layer_forward needs. */
 size_t moe_layer_workspace_size(moe_dtype dt, moe_act act, int64_t s, int m, int e, int k,
                                 int64_t c_max, int h);

@@ -1,0 +1,91 @@
+"""GPU gate backward against the oracle (through the C ABI).
+
+The device backward gets the oracle's own idx and gates, so only the backward
+is compared.  Tolerances follow from the arithmetic: d_logits may differ by a
+relative 2e-5 of the token's scale S_t = sum_r |dg g| + |A| (fp32 evaluation
+from fp32 gates), 1e-4 for the raw softmax, whose logits the device recomputes
+in another summation order (m * 2^-24 * sum |x w| stays below 1e-4 here); the
+products add that error times their other factor plus n * 2^-24 * sum |terms|
+for their own fp32 sums of n terms.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import combine_moe_gate_gb300 as M
+import oracle
+import synth
+from synth.workloads import Workload
+
+from gpu_util import to_dev
+
+pytestmark = pytest.mark.gpu
+
+U = 2.0 ** -24
+
+
+def _w(**kw):
+    kw.setdefault("name", "gbwd")
+    kw.setdefault("h", 64)
+    kw.setdefault("act", "gelu")
+    kw.setdefault("capacity_factor", 1.0)
+    return Workload(**kw)
+
+
+CASES = [
+    (_w(s=300, m=136, e=8, k=2), True, "all"),
+    (_w(s=257, m=264, e=32, k=4, skew_alpha=1.0), True, "all"),
+    (_w(s=130, m=512, e=64, k=3, skew_alpha=1.2), True, "all"),
+    (_w(s=256, m=64, e=4, k=1, dtype="f32", normalize_gates=False, skew_alpha=0.5), False, "all"),
+    (_w(s=200, m=96, e=6, k=2, dtype="f32", normalize_gates=False), False, "all"),
+    (_w(s=100, m=40, e=5, k=3), True, "logits_only"),
+    (_w(s=100, m=40, e=5, k=3), True, "bias_only"),
+]
+
+
+@pytest.mark.parametrize("w,normalize,outs", CASES,
+                         ids=lambda v: getattr(v, "name", str(v)) if not isinstance(v, Workload)
+                         else f"s{v.s}_m{v.m}_e{v.e}_k{v.k}_{v.dtype}")
+def test_gate_bwd_matches_oracle(w, normalize, outs):
+    inp = synth.make_inputs_host(w, parts=("x", "wg", "bias"))
+    x, wg, bias = inp["x"], inp["wg"], inp["bias"]
+    lg = oracle.gate_logits(x, wg, bias)
+    idx = oracle.topk(lg, w.k)
+    g = oracle.gates(lg, idx, normalize)
+    dg = synth.normal_host(7, "dg", (w.k, w.s), 1.0, "f32")
+    ref = oracle.gate_bwd(x, wg, bias, idx, dg, normalize)
+
+    s, m, e = w.s, w.m, w.e
+    dev = lambda a: to_dev(a)
+    z = lambda *shape: torch.full(shape, float("nan"), dtype=torch.float32, device="cuda")
+    d_logits = z(s, e)
+    d_wg = z(m, e) if outs == "all" else None
+    d_bias = z(e) if outs in ("all", "bias_only") else None
+    d_x = z(s, m) if outs == "all" else None
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flags = M.MOE_FLAG_NORMALIZE_GATES if normalize else 0
+    M.moe_gate_bwd(dev(x), dev(wg), None if bias is None else dev(bias), dev(idx), dev(g), dev(dg),
+                   d_logits, st, d_wg=d_wg, d_bias=d_bias, d_x=d_x, flags=flags)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+
+    xf = oracle.to_f32(x).astype(np.float64)
+    w64 = wg.astype(np.float64)
+    dl = ref["d_logits"]
+    a = (dg.astype(np.float64) * g.astype(np.float64)).sum(0)                  # [s]
+    scale = np.abs(dg.astype(np.float64) * g.astype(np.float64)).sum(0) + np.abs(a)
+    rel = 2e-5 if normalize else 1e-4
+    tol_dl = rel * scale + 1e-7                                                 # [s]
+
+    got = d_logits.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - dl) <= tol_dl[:, None]), np.abs(got - dl).max()
+    if d_wg is not None:
+        tol = np.abs(xf).T @ tol_dl[:, None] + s * U * (np.abs(xf).T @ np.abs(dl))
+        assert np.all(np.abs(d_wg.cpu().numpy() - ref["d_wg"]) <= tol)
+    if d_bias is not None:
+        tol = tol_dl.sum() + s * U * np.abs(dl).sum(0)
+        assert np.all(np.abs(d_bias.cpu().numpy() - ref["d_bias"]) <= tol)
+    if d_x is not None:
+        tol = tol_dl[:, None] * np.abs(w64).sum(1)[None, :] + e * U * (np.abs(dl) @ np.abs(w64).T)
+        assert np.all(np.abs(d_x.cpu().numpy() - ref["d_x"]) <= tol)
