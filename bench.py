@@ -335,6 +335,37 @@ def run_ours(args, rank, world, local_rank):
         e2e_ms += a.elapsed_time(b)
     e2e_ms /= args.steps
 
+    # ---- gate backward (not part of the step): gradient of the gate values to
+    # the logits, the gate weight, its bias and x, from this batch's routing
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    d_gates = torch.randn((w.k, w.s), generator=gen, device=dev, dtype=torch.float32)
+    d_logits = torch.empty((w.s, w.e), device=dev, dtype=torch.float32)
+    d_wg = torch.empty((w.m, w.e), device=dev, dtype=torch.float32)
+    d_bias = torch.empty((w.e,), device=dev, dtype=torch.float32)
+    d_xg = torch.empty((w.s, w.m), device=dev, dtype=torch.float32)
+
+    def gate_bwd_step():
+        M.moe_gate_bwd(x, wg, gb, bufs.idx, bufs.gates, d_gates, d_logits, bufs.status,
+                       d_wg=d_wg, d_bias=d_bias, d_x=d_xg, flags=flags)
+
+    for _ in range(3):
+        flush.fill_(1)
+        gate_bwd_step()
+    torch.cuda.synchronize()
+    gbwd_ms = 0.0
+    for _ in range(args.steps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        gate_bwd_step()
+        b.record()
+        b.synchronize()
+        gbwd_ms += a.elapsed_time(b)
+    gbwd_ms /= args.steps
+    if int(bufs.status.item()) != 0:
+        raise RuntimeError(f"device status {int(bufs.status.item())}")
+
     # ---- max over ranks
     ms_step, e2e_ms = reduce_max([ms_step, e2e_ms], device=dev)
 
@@ -364,6 +395,10 @@ def run_ours(args, rank, world, local_rank):
             d.update(tflops=tf, tc_frac=tf / pk["bf16"])
         stages[n] = d
     ffn_tf = ffn_flops / (stage_ms["expert_ffn"] * 1e-3) / 1e12
+    # gate backward, timed on its own: fp32 FMAs of d_wg = x^T dl and d_x = dl Wg^T
+    gbwd_flops = 4.0 * w.s * w.m * w.e
+    stages["gate_bwd"] = {"ms": gbwd_ms, "fp32_tflops": gbwd_flops / (gbwd_ms * 1e-3) / 1e12,
+                          "note": "not part of the step: d_logits, d_wg, d_bias, d_x"}
     clocks = clk.summary(t_wall0, t_wall1)
 
     res = {
