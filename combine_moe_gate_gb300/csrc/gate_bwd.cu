@@ -10,7 +10,8 @@
 //                  the selected logits alone);
 //   raw softmax:   dl_j = -p_j A + sum_{r: i_r = j} dg_r g_r, p = softmax(l).
 // Then through l = x Wg + b: d_wg = x^T dl, d_bias = sum_t dl, d_x = dl Wg^T.
-// All in fp32; every output is one sequential fp32 sum (deterministic).
+// All in fp32 and deterministic: every output is an fp32 sum in a fixed order
+// (d_wg and d_bias: per token group in token order, then a fixed tree).
 #include "common.cuh"
 
 namespace moe {
@@ -108,43 +109,131 @@ gate_bwd_dl_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
 }
 
 // ------------------------------------------------------------- d_wg, d_bias
-// d_wg[i, j] = sum_t x[t, i] dl[t, j]: a CTA owns 32 features x 8 experts and
-// walks the tokens in order, 32 at a time through shared memory; thread (ty,
-// tx) accumulates output (i0 + tx, j0 + ty).  The CTAs with i0 == 0 also sum
-// d_bias for their experts.
-constexpr int WG_TI = 32, WG_TJ = 8, WG_TT = 32;
+// d_wg[i, j] = sum_t x[t, i] dl[t, j] and d_bias[j] = sum_t dl[t, j].  A CTA
+// owns WG_F features and WG_EB experts for every token.  Thread (g, q) holds
+// the four features i0 + 4q .. i0 + 4q + 3 (one 16- or 8-byte load; rows are
+// multiples of four features) and sums the tokens g, g + WG_G, g + 2 WG_G, ...
+// with WG_U of them in flight.  The CTA then adds its WG_G token groups'
+// partials in a fixed tree (xor shuffles inside a warp, the warps in order),
+// so every result is independent of scheduling.  The CTAs of the first
+// feature block also sum d_bias.
+constexpr int WG_Q = 2, WG_F = 4 * WG_Q, WG_EB = 8, WG_U = 4;
+constexpr int WG_THREADS = 512, WG_G = WG_THREADS / WG_Q, WG_WARPS = WG_THREADS / 32;
 
-template <typename XT>
-__global__ void __launch_bounds__(WG_TI * WG_TJ)
+__device__ __forceinline__ void ld_x4(const float *p, float (&v)[4]) {
+    const float4 a = *reinterpret_cast<const float4 *>(p);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+}
+__device__ __forceinline__ void ld_x4(const __nv_bfloat16 *p, float (&v)[4]) {
+    // bf16 -> fp32 is exact: the 16 bits become the high half of the word
+    const uint2 a = *reinterpret_cast<const uint2 *>(p);
+    v[0] = __uint_as_float(a.x << 16); v[1] = __uint_as_float(a.x & 0xffff0000u);
+    v[2] = __uint_as_float(a.y << 16); v[3] = __uint_as_float(a.y & 0xffff0000u);
+}
+
+// the n (0, 4 or 8 when VEC) experts of one d_logits row from p; zeros past n
+template <bool VEC>
+__device__ __forceinline__ void ld_dl8(const float *p, int n, float (&v)[WG_EB]) {
+    if (VEC) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+        if (n >= 4) a = *reinterpret_cast<const float4 *>(p);
+        if (n >= 8) b = *reinterpret_cast<const float4 *>(p + 4);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+#pragma unroll
+        for (int jj = 0; jj < WG_EB; jj++) v[jj] = jj < n ? p[jj] : 0.0f;
+    }
+}
+
+template <typename XT, bool DVEC>
+__global__ void __launch_bounds__(WG_THREADS)
 gate_bwd_dwg_kernel(const XT *__restrict__ x, const float *__restrict__ dl, int64_t s, int m,
                     int e, float *__restrict__ d_wg, float *__restrict__ d_bias, int32_t *status) {
     pdl_enter();
     if (status_bad(status)) return;
-    __shared__ float xs[WG_TT][WG_TI + 1];
-    __shared__ float ds[WG_TT][WG_TJ + 1];
-    const int tx = threadIdx.x % WG_TI, ty = threadIdx.x / WG_TI;
-    const int i0 = blockIdx.x * WG_TI, j0 = blockIdx.y * WG_TJ;
-    const int i = i0 + tx, j = j0 + ty;
-    float acc = 0.0f, accb = 0.0f;
-    for (int64_t t0 = 0; t0 < s; t0 += WG_TT) {
-        __syncthreads();
-        for (int q = threadIdx.x; q < WG_TT * WG_TI; q += WG_TI * WG_TJ) {
-            const int tt = q / WG_TI, ii = q % WG_TI;
-            xs[tt][ii] = (t0 + tt < s && i0 + ii < m) ? ldx(x + (t0 + tt) * m + i0 + ii) : 0.0f;
+    __shared__ float red[WG_WARPS][WG_F * WG_EB];
+    __shared__ float redb[WG_WARPS][WG_EB];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int q = threadIdx.x % WG_Q, g = threadIdx.x / WG_Q;
+    const int i0 = blockIdx.x * WG_F, i = i0 + 4 * q;
+    const int j0 = blockIdx.y * WG_EB, nj = min(WG_EB, e - j0);
+    const bool want_wg = d_wg != nullptr;                  // uniform over the CTA
+    const bool want_b = d_bias != nullptr && blockIdx.x == 0;
+    const bool load_x = want_wg && i < m;
+    float acc[4][WG_EB], accb[WG_EB];
+#pragma unroll
+    for (int jj = 0; jj < WG_EB; jj++) {
+        accb[jj] = 0.0f;
+#pragma unroll
+        for (int f = 0; f < 4; f++) acc[f][jj] = 0.0f;
+    }
+    for (int64_t t0 = g; t0 < s; t0 += (int64_t)WG_G * WG_U) {
+        float xv[WG_U][4], dv[WG_U][WG_EB];
+#pragma unroll
+        for (int u = 0; u < WG_U; u++) {
+            const int64_t t = t0 + (int64_t)u * WG_G;
+            const bool in = t < s;
+            ld_dl8<DVEC>(dl + (in ? t : 0) * e + j0, in ? nj : 0, dv[u]);
+            if (in && load_x) {
+                ld_x4(x + t * m + i, xv[u]);
+            } else {
+#pragma unroll
+                for (int f = 0; f < 4; f++) xv[u][f] = 0.0f;
+            }
         }
-        for (int q = threadIdx.x; q < WG_TT * WG_TJ; q += WG_TI * WG_TJ) {
-            const int tt = q / WG_TJ, jj = q % WG_TJ;
-            ds[tt][jj] = (t0 + tt < s && j0 + jj < e) ? dl[(t0 + tt) * e + j0 + jj] : 0.0f;
-        }
-        __syncthreads();
-#pragma unroll 8
-        for (int tt = 0; tt < WG_TT; tt++) {
-            acc = fmaf(xs[tt][tx], ds[tt][ty], acc);
-            accb += ds[tt][ty];
+#pragma unroll
+        for (int u = 0; u < WG_U; u++)
+#pragma unroll
+            for (int jj = 0; jj < WG_EB; jj++) {
+#pragma unroll
+                for (int f = 0; f < 4; f++) acc[f][jj] = fmaf(xv[u][f], dv[u][jj], acc[f][jj]);
+                accb[jj] += dv[u][jj];
+            }
+    }
+    // lanes with the same q: xor over the token-group bits of the lane index
+    if (want_wg) {
+#pragma unroll
+        for (int f = 0; f < 4; f++)
+#pragma unroll
+            for (int jj = 0; jj < WG_EB; jj++) {
+                float v = acc[f][jj];
+#pragma unroll
+                for (int o = WG_Q; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                acc[f][jj] = v;
+            }
+        if (lane < WG_Q) {
+#pragma unroll
+            for (int f = 0; f < 4; f++)
+#pragma unroll
+                for (int jj = 0; jj < WG_EB; jj++) red[warp][(4 * lane + f) * WG_EB + jj] = acc[f][jj];
         }
     }
-    if (d_wg && i < m && j < e) d_wg[(int64_t)i * e + j] = acc;
-    if (d_bias && blockIdx.x == 0 && tx == 0 && j < e) d_bias[j] = accb;
+    if (want_b) {
+#pragma unroll
+        for (int jj = 0; jj < WG_EB; jj++) {
+            float v = accb[jj];
+#pragma unroll
+            for (int o = WG_Q; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) redb[warp][jj] = v;
+        }
+    }
+    __syncthreads();
+    const int o = threadIdx.x;
+    if (want_wg && o < WG_F * WG_EB) {
+        const int ii = i0 + o / WG_EB, jj = o % WG_EB;
+        float sum = 0.0f;
+#pragma unroll
+        for (int w = 0; w < WG_WARPS; w++) sum += red[w][o];
+        if (ii < m && jj < nj) d_wg[(int64_t)ii * e + j0 + jj] = sum;
+    }
+    if (want_b && o >= WG_F * WG_EB && o < WG_F * WG_EB + WG_EB) {
+        const int jj = o - WG_F * WG_EB;
+        float sum = 0.0f;
+#pragma unroll
+        for (int w = 0; w < WG_WARPS; w++) sum += redb[w][jj];
+        if (jj < nj) d_bias[j0 + jj] = sum;
+    }
 }
 
 // --------------------------------------------------------------------- d_x
@@ -190,11 +279,15 @@ moe_status gate_bwd_typed(const void *x, const float *wg, const float *bias, int
                               d_gates, d_logits, st);
     if (r != MOE_OK) return r;
     if (d_wg || d_bias) {
-        // d_bias alone runs only the first feature block's CTAs
-        const unsigned gx = d_wg ? (unsigned)((m + WG_TI - 1) / WG_TI) : 1u;
-        r = launch_pdl(gate_bwd_dwg_kernel<XT>, dim3(gx, (unsigned)((e + WG_TJ - 1) / WG_TJ)),
-                       dim3(WG_TI * WG_TJ), 0, stream, (const XT *)x, (const float *)d_logits, s,
-                       m, e, d_wg, d_bias, st);
+        // d_bias alone runs only the first feature block's CTAs; d_logits rows
+        // load as float4 when they stay 16-byte aligned
+        const unsigned gx = d_wg ? (unsigned)((m + WG_F - 1) / WG_F) : 1u;
+        const dim3 grid(gx, (unsigned)((e + WG_EB - 1) / WG_EB));
+        const bool vec = e % 4 == 0 && aligned16(d_logits);
+        r = vec ? launch_pdl(gate_bwd_dwg_kernel<XT, true>, grid, dim3(WG_THREADS), 0, stream,
+                             (const XT *)x, (const float *)d_logits, s, m, e, d_wg, d_bias, st)
+                : launch_pdl(gate_bwd_dwg_kernel<XT, false>, grid, dim3(WG_THREADS), 0, stream,
+                             (const XT *)x, (const float *)d_logits, s, m, e, d_wg, d_bias, st);
         if (r != MOE_OK) return r;
     }
     if (d_x) {

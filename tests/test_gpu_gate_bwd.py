@@ -39,6 +39,10 @@ CASES = [
     (_w(s=130, m=512, e=64, k=3, skew_alpha=1.2), True, "all"),
     (_w(s=256, m=64, e=4, k=1, dtype="f32", normalize_gates=False, skew_alpha=0.5), False, "all"),
     (_w(s=200, m=96, e=6, k=2, dtype="f32", normalize_gates=False), False, "all"),
+    # several rounds of token groups, expert blocks with a 4-wide tail, a
+    # partly filled last feature block
+    (_w(s=2500, m=48, e=12, k=2), True, "all"),
+    (_w(s=1100, m=36, e=20, k=3, dtype="f32", normalize_gates=False), False, "all"),
     (_w(s=100, m=40, e=5, k=3), True, "logits_only"),
     (_w(s=100, m=40, e=5, k=3), True, "bias_only"),
 ]
