@@ -237,33 +237,65 @@ gate_bwd_dwg_kernel(const XT *__restrict__ x, const float *__restrict__ dl, int6
 }
 
 // --------------------------------------------------------------------- d_x
-// d_x[t, i] = sum_j dl[t, j] wg[i, j]: a CTA owns 32 features (their weight
-// rows staged in shared memory, rows padded by one word) and DX_TOK tokens;
-// lane = feature, warp = token.
-constexpr int DX_WARPS = 8, DX_TOK = 64;
+// d_x[t, i] = sum_j dl[t, j] wg[i, j], summed over j in order.  A CTA owns
+// DX_TOK tokens and DX_F features, whose weights it stages transposed in
+// shared memory (wgs[j][i], rows padded to DX_LD words); lane l of a warp
+// computes features 4l .. 4l + 3 (one float4 store) for DX_U tokens at once.
+constexpr int DX_WARPS = 8, DX_U = 4, DX_TOK = DX_WARPS * DX_U, DX_F = 128, DX_LD = DX_F + 4;
 
+template <bool DVEC>
 __global__ void __launch_bounds__(DX_WARPS * 32)
 gate_bwd_dx_kernel(const float *__restrict__ dl, const float *__restrict__ wg, int64_t s, int m,
                    int e, float *__restrict__ d_x, int32_t *status) {
     pdl_enter();
     if (status_bad(status)) return;
-    extern __shared__ float wgs[];   // [32][e + 1]
+    extern __shared__ float4 wgs4[];   // [e][DX_LD] floats
+    float *wgs = reinterpret_cast<float *>(wgs4);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int i0 = blockIdx.x * 32;
-    for (int q = threadIdx.x; q < 32 * e; q += DX_WARPS * 32) {
+    const int i0 = blockIdx.y * DX_F;
+    for (int q = threadIdx.x; q < DX_F * e; q += DX_WARPS * 32) {
         const int ii = q / e, j = q % e;
-        wgs[ii * (e + 1) + j] = i0 + ii < m ? wg[(int64_t)(i0 + ii) * e + j] : 0.0f;
+        wgs[j * DX_LD + ii] = i0 + ii < m ? wg[(int64_t)(i0 + ii) * e + j] : 0.0f;
     }
     __syncthreads();
-    const float *wr = wgs + lane * (e + 1);
-    const int64_t tb = (int64_t)blockIdx.y * DX_TOK;
-    for (int tt = warp; tt < DX_TOK; tt += DX_WARPS) {
-        const int64_t t = tb + tt;
-        if (t >= s) break;
-        const float *dr = dl + t * e;
-        float acc = 0.0f;
-        for (int j = 0; j < e; j++) acc = fmaf(dr[j], wr[j], acc);
-        if (i0 + lane < m) d_x[t * m + i0 + lane] = acc;
+    const int i = i0 + 4 * lane;
+    const int64_t tb = (int64_t)blockIdx.x * DX_TOK + warp;   // tokens tb + u DX_WARPS
+    float acc[DX_U][4];
+#pragma unroll
+    for (int u = 0; u < DX_U; u++)
+#pragma unroll
+        for (int f = 0; f < 4; f++) acc[u][f] = 0.0f;
+    for (int j0 = 0; j0 < e; j0 += WG_EB) {
+        const int nj = min(WG_EB, e - j0);
+        float dv[DX_U][WG_EB];
+#pragma unroll
+        for (int u = 0; u < DX_U; u++) {
+            const int64_t t = tb + (int64_t)u * DX_WARPS;
+            const bool in = t < s;
+            ld_dl8<DVEC>(dl + (in ? t : 0) * e + j0, in ? nj : 0, dv[u]);
+        }
+#pragma unroll
+        for (int jj = 0; jj < WG_EB; jj++) {
+            if (jj < nj) {
+                const float4 w = *reinterpret_cast<const float4 *>(wgs + (j0 + jj) * DX_LD + 4 * lane);
+#pragma unroll
+                for (int u = 0; u < DX_U; u++) {
+                    acc[u][0] = fmaf(dv[u][jj], w.x, acc[u][0]);
+                    acc[u][1] = fmaf(dv[u][jj], w.y, acc[u][1]);
+                    acc[u][2] = fmaf(dv[u][jj], w.z, acc[u][2]);
+                    acc[u][3] = fmaf(dv[u][jj], w.w, acc[u][3]);
+                }
+            }
+        }
+    }
+    if (i < m) {
+#pragma unroll
+        for (int u = 0; u < DX_U; u++) {
+            const int64_t t = tb + (int64_t)u * DX_WARPS;
+            if (t < s)
+                *reinterpret_cast<float4 *>(d_x + t * m + i) =
+                    make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+        }
     }
 }
 
@@ -291,16 +323,19 @@ moe_status gate_bwd_typed(const void *x, const float *wg, const float *bias, int
         if (r != MOE_OK) return r;
     }
     if (d_x) {
-        const size_t smem = (size_t)32 * (e + 1) * sizeof(float);
-        auto kern = gate_bwd_dx_kernel;
+        // rows of four features (rows are multiples of four); tokens on grid x
+        const size_t smem = (size_t)e * DX_LD * sizeof(float);
+        const bool vec = e % 4 == 0 && aligned16(d_logits);
+        auto kern = vec ? gate_bwd_dx_kernel<true> : gate_bwd_dx_kernel<false>;
         if (smem > 48 * 1024 &&
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
                 cudaSuccess)
             return MOE_ERR_CUDA;
-        const int64_t gy = (s + DX_TOK - 1) / DX_TOK;
-        if (gy > 65535) return MOE_ERR_UNSUPPORTED;
-        r = launch_pdl(kern, dim3((unsigned)((m + 31) / 32), (unsigned)gy), dim3(DX_WARPS * 32),
-                       smem, stream, (const float *)d_logits, wg, s, m, e, d_x, st);
+        const int64_t gx = (s + DX_TOK - 1) / DX_TOK;
+        if (gx > 0x7fffffff || (m + DX_F - 1) / DX_F > 65535) return MOE_ERR_UNSUPPORTED;
+        r = launch_pdl(kern, dim3((unsigned)gx, (unsigned)((m + DX_F - 1) / DX_F)),
+                       dim3(DX_WARPS * 32), smem, stream, (const float *)d_logits, wg, s, m, e,
+                       d_x, st);
     }
     return r;
 }
