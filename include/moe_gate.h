@@ -235,9 +235,11 @@ moe_status moe_encode_bwd(const void *d_buf, moe_dtype dt, const int32_t *idx,
  *   d_x = d_logits wg^T [s, m].
  * Inputs: x [s, m] in `xdt`; wg [m, e] fp32; bias [e] fp32 or NULL (used only
  * to recompute the logits of the raw softmax); idx, gates [k, s] as the gate
- * wrote them; d_gates [k, s] fp32 (e.g. moe_decode_bwd's).  Outputs, all fp32,
- * each one sequential fp32 sum: d_logits [s, e] (required), d_wg [m, e],
- * d_bias [e], d_x [s, m] (each may be NULL).  e <= 256 here.
+ * wrote them; d_gates [k, s] fp32 (e.g. moe_decode_bwd's).  Outputs, all fp32
+ * and deterministic (fixed summation orders: d_x sums the experts in order,
+ * d_wg and d_bias sum tokens per token group, then the groups in a fixed
+ * tree): d_logits [s, e] (required), d_wg [m, e], d_bias [e], d_x [s, m]
+ * (each may be NULL).  e <= 256 here.
  * This entry point extends the pages' forward gate to its backward.
  */
 moe_status moe_gate_bwd(const void *x, moe_dtype xdt, const float *wg, const float *bias,
