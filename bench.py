@@ -349,20 +349,36 @@ def run_ours(args, rank, world, local_rank):
         M.moe_gate_bwd(x, wg, gb, bufs.idx, bufs.gates, d_gates, d_logits, bufs.status,
                        d_wg=d_wg, d_bias=d_bias, d_x=d_xg, flags=flags)
 
-    for _ in range(3):
-        flush.fill_(1)
-        gate_bwd_step()
-    torch.cuda.synchronize()
-    gbwd_ms = 0.0
-    for _ in range(args.steps):
-        flush.fill_(1)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        gate_bwd_step()
-        b.record()
-        b.synchronize()
-        gbwd_ms += a.elapsed_time(b)
-    gbwd_ms /= args.steps
+    def time_alone(fn):
+        """Mean event time of fn over args.steps calls, L2 flushed before each."""
+        for _ in range(3):
+            flush.fill_(1)
+            fn()
+        torch.cuda.synchronize()
+        tot = 0.0
+        for _ in range(args.steps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            tot += a.elapsed_time(b)
+        return tot / args.steps
+
+    gbwd_ms = time_alone(gate_bwd_step)
+
+    # ---- decode and encode backward (not part of the step): dE and dG from a
+    # dY of this batch's shape, then dX from dBuf := dE (the identity-expert chain)
+    dy = torch.randn((w.s, w.m), generator=gen, device=dev, dtype=torch.float32).to(x.dtype)
+    d_out = torch.empty_like(bufs.out)
+    d_gates_dec = torch.empty((w.k, w.s), device=dev, dtype=torch.float32)
+    dx_enc = torch.empty_like(x)
+    dbwd_ms = time_alone(lambda: M.moe_decode_bwd(dy, bufs.out, bufs.idx, bufs.loc, bufs.gates,
+                                                  bufs.counts, bufs.c_dev, d_out, d_gates_dec,
+                                                  bufs.status))
+    ebwd_ms = time_alone(lambda: M.moe_encode_bwd(d_out, bufs.idx, bufs.loc, bufs.c_dev, dx_enc,
+                                                  bufs.status))
     if int(bufs.status.item()) != 0:
         raise RuntimeError(f"device status {int(bufs.status.item())}")
 
@@ -382,6 +398,8 @@ def run_ours(args, rank, world, local_rank):
         "gate": w.s * w.m * b + 4 * w.m * w.e + 8 * w.s * w.k,
         "encode": t1 * w.m * b + R * w.m * b + 8 * w.s * w.k,
         "decode": R * w.m * b + w.s * w.m * b + 12 * w.s * w.k,
+        "decode_bwd": t1 * w.m * b + 2 * R * w.m * b + 16 * w.s * w.k,
+        "encode_bwd": R * w.m * b + w.s * w.m * b + 8 * w.s * w.k,
     }
     pk = peaks()
     stages = {}
@@ -399,6 +417,9 @@ def run_ours(args, rank, world, local_rank):
     gbwd_flops = 4.0 * w.s * w.m * w.e
     stages["gate_bwd"] = {"ms": gbwd_ms, "fp32_tflops": gbwd_flops / (gbwd_ms * 1e-3) / 1e12,
                           "note": "not part of the step: d_logits, d_wg, d_bias, d_x"}
+    for n, ms in (("decode_bwd", dbwd_ms), ("encode_bwd", ebwd_ms)):
+        gbs = bytes_[n] / (ms * 1e-3) / 1e9
+        stages[n] = {"ms": ms, "gbs": gbs, "hbm_frac": gbs / pk["hbm"], "note": "not part of the step"}
     clocks = clk.summary(t_wall0, t_wall1)
 
     res = {
