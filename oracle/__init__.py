@@ -18,6 +18,7 @@ from .core import (  # noqa: F401
     decode_bwd,
     encode,
     encode_bwd,
+    ffn_bwd,
     ffn_rows,
     gate_bwd,
     gate_chunk,

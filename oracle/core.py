@@ -56,6 +56,8 @@ def _L():
                 "orc_decode_bwd": [P, P, P, P, P, I64, I64, I32, I32, I32, I64, I32, P, P],
                 "orc_encode_bwd": [P, P, P, I64, I64, I32, I32, I32, I64, I32, P],
                 "orc_ffn_rows": [P, P, P, P, P, P, I32, I32, I64, I32, I32, I32, P, P, I64, P],
+                "orc_ffn_bwd": [P, P, P, P, P, I32, I32, I64, I32, I32, I32, P, P, P, P, P, P, P,
+                                P],
                 "orc_round_bf16": [D],
                 "orc_set_threads": [I32],
                 "orc_get_threads": [],
@@ -234,6 +236,30 @@ def ffn_rows(buf, w1, b1, w3, w2, b2, act, rows_e, rows_j, bf16):
     out = np.empty((len(re), m), np.float32)
     _L().orc_ffn_rows(_p(buf), _p(w1), _p(b1), _p(w3), _p(w2), _p(b2), ACT[act], e, cmax, m, h,
                       int(bf16), _p(re), _p(rj), len(re), _p(out))
+    return out
+
+
+def ffn_bwd(buf, w1, b1, w3, w2, act, kept, d_out, bf16):
+    """Backward of the expert MLP over the kept rows (row j < kept[e] of expert
+    e) for L = sum <d_out, out>: d_buf [e, cmax, m] (layer dtype, 0 past the
+    kept rows), d_w1 / d_w3 [e, h, m], d_w2 [e, m, h], d_b1 [e, h], d_b2 [e, m]
+    (fp32; d_w3 for SwiGLU only, the biases for ReLU/GELU only)."""
+    buf, w1, b1, w3, w2, d_out = (to_f32(a) for a in (buf, w1, b1, w3, w2, d_out))
+    e, cmax, m = buf.shape
+    h = w1.shape[1]
+    kept = np.ascontiguousarray(kept, np.int64)
+    assert kept.shape == (e,) and np.all((kept >= 0) & (kept <= cmax))
+    swiglu = act == "swiglu"
+    out = dict(d_buf=np.empty((e, cmax, m), np.float32), d_w1=np.empty((e, h, m), np.float32),
+               d_w2=np.empty((e, m, h), np.float32))
+    if swiglu:
+        out["d_w3"] = np.empty((e, h, m), np.float32)
+    else:
+        out["d_b1"] = np.empty((e, h), np.float32)
+        out["d_b2"] = np.empty((e, m), np.float32)
+    _L().orc_ffn_bwd(_p(buf), _p(w1), _p(b1), _p(w3), _p(w2), ACT[act], e, cmax, m, h, int(bf16),
+                     _p(kept), _p(d_out), _p(out["d_buf"]), _p(out["d_w1"]), _p(out.get("d_b1")),
+                     _p(out.get("d_w3")), _p(out["d_w2"]), _p(out.get("d_b2")))
     return out
 
 

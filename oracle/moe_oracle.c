@@ -421,3 +421,120 @@ void orc_ffn_rows(const float *buf, const float *w1, const float *b1, const floa
         free(hid);
     }
 }
+
+/* ---------------------------------------------------- expert FFN backward */
+
+/* Backward of orc_ffn_rows over every kept row (row j < kept[e] of expert e),
+ * for L = sum over kept rows of <d_out, out>.  The forward's roundings are
+ * taken as the identity (their derivative almost everywhere); the hidden
+ * activation fc2 consumed is the rounded one, recomputed exactly as the
+ * forward does.  All sums in double; d_buf is rounded once to the layer
+ * dtype, the weight and bias gradients once to fp32.
+ *   ReLU/GELU: pre = x w1^T + b1, hid = act(pre);
+ *              d_hid = d_out w2, d_pre = d_hid * act'(pre)
+ *              (ReLU' = 1 where pre > 0, else 0; GELU' = Phi(z) + z phi(z));
+ *   SwiGLU:    a = x w1^T, b = x w3^T, hid = silu(a) b;
+ *              d_a = d_hid * b * sigma(a) (1 + a (1 - sigma(a))), d_b = d_hid * silu(a);
+ *   d_w2[e] = sum_rows d_out^T hid,  d_b2[e] = sum_rows d_out,
+ *   d_w1[e] = sum_rows d_pre^T x (d_a for SwiGLU),  d_b1[e] = sum_rows d_pre,
+ *   d_w3[e] = sum_rows d_b^T x,  d_buf = d_pre w1 (+ d_b w3).
+ * Rows of d_buf at or past kept[e] are 0.  SwiGLU has no biases: d_b1, d_b2
+ * are then not written.  Any output may be NULL.  Layouts as orc_ffn_rows;
+ * d_out and d_buf [e, cmax, m]. */
+void orc_ffn_bwd(const float *buf, const float *w1, const float *b1, const float *w3,
+                 const float *w2, int act, int e, int64_t cmax, int m, int h, int bf16,
+                 const int64_t *kept, const float *d_out, float *d_buf, float *d_w1,
+                 float *d_b1, float *d_w3, float *d_w2, float *d_b2)
+{
+    const int swiglu = act == ORC_ACT_SWIGLU;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int ex = 0; ex < e; ex++) {
+        const int64_t rows = kept[ex];
+        double *gw1 = (double *)calloc((size_t)h * m, sizeof(double));
+        double *gw3 = (double *)calloc((size_t)h * m, sizeof(double));
+        double *gw2 = (double *)calloc((size_t)m * h, sizeof(double));
+        double *gb1 = (double *)calloc((size_t)h, sizeof(double));
+        double *gb2 = (double *)calloc((size_t)m, sizeof(double));
+        double *hid = (double *)malloc(sizeof(double) * (size_t)h);
+        double *dp = (double *)malloc(sizeof(double) * (size_t)h);    /* d_pre or d_a */
+        double *dq = (double *)malloc(sizeof(double) * (size_t)h);    /* d_b (SwiGLU) */
+        for (int64_t j = 0; j < cmax; j++) {
+            const float *xr = buf + ((int64_t)ex * cmax + j) * m;
+            const float *gr = d_out + ((int64_t)ex * cmax + j) * m;
+            float *dbr = d_buf ? d_buf + ((int64_t)ex * cmax + j) * m : NULL;
+            if (j >= rows) {
+                if (dbr)
+                    for (int i = 0; i < m; i++) dbr[i] = 0.0f;
+                continue;
+            }
+            /* forward of this row: the derivative factors and the rounded hidden */
+            for (int u = 0; u < h; u++) {
+                const float *w1r = w1 + ((int64_t)ex * h + u) * m;
+                double a = 0.0;
+                for (int i = 0; i < m; i++) a += (double)xr[i] * (double)w1r[i];
+                if (swiglu) {
+                    const float *w3r = w3 + ((int64_t)ex * h + u) * m;
+                    double b = 0.0;
+                    for (int i = 0; i < m; i++) b += (double)xr[i] * (double)w3r[i];
+                    const double sg = 1.0 / (1.0 + exp(-a));
+                    hid[u] = round_to(a * sg * b, bf16);
+                    dp[u] = b * sg * (1.0 + a * (1.0 - sg));   /* d hid / d a */
+                    dq[u] = a * sg;                            /* d hid / d b */
+                } else {
+                    if (b1) a += (double)b1[(int64_t)ex * h + u];
+                    if (act == ORC_ACT_RELU) {
+                        hid[u] = round_to(a > 0.0 ? a : 0.0, bf16);
+                        dp[u] = a > 0.0 ? 1.0 : 0.0;
+                    } else {
+                        const double cdf = 0.5 * (1.0 + erf(a / sqrt(2.0)));
+                        /* standard normal density; 1/sqrt(2 pi) written out */
+                        const double pdf = exp(-0.5 * a * a) * 0.39894228040143267794;
+                        hid[u] = round_to(a * cdf, bf16);
+                        dp[u] = cdf + a * pdf;
+                    }
+                    dq[u] = 0.0;
+                }
+            }
+            /* fc2: d_hid, d_w2, d_b2 */
+            for (int u = 0; u < h; u++) {
+                double dh = 0.0;
+                for (int i = 0; i < m; i++)
+                    dh += (double)gr[i] * (double)w2[((int64_t)ex * m + i) * h + u];
+                dp[u] *= dh;
+                dq[u] *= dh;
+            }
+            for (int i = 0; i < m; i++) {
+                gb2[i] += (double)gr[i];
+                for (int u = 0; u < h; u++) gw2[(int64_t)i * h + u] += (double)gr[i] * hid[u];
+            }
+            /* fc1: d_w1 (d_w3), d_b1, d_buf */
+            for (int u = 0; u < h; u++) {
+                gb1[u] += dp[u];
+                for (int i = 0; i < m; i++) {
+                    gw1[(int64_t)u * m + i] += dp[u] * (double)xr[i];
+                    if (swiglu) gw3[(int64_t)u * m + i] += dq[u] * (double)xr[i];
+                }
+            }
+            if (dbr) {
+                for (int i = 0; i < m; i++) {
+                    double v = 0.0;
+                    for (int u = 0; u < h; u++) {
+                        v += dp[u] * (double)w1[((int64_t)ex * h + u) * m + i];
+                        if (swiglu) v += dq[u] * (double)w3[((int64_t)ex * h + u) * m + i];
+                    }
+                    dbr[i] = round_to(v, bf16);
+                }
+            }
+        }
+        for (int64_t q = 0; q < (int64_t)h * m; q++) {
+            if (d_w1) d_w1[(int64_t)ex * h * m + q] = (float)gw1[q];
+            if (d_w3 && swiglu) d_w3[(int64_t)ex * h * m + q] = (float)gw3[q];
+            if (d_w2) d_w2[(int64_t)ex * m * h + q] = (float)gw2[q];
+        }
+        for (int u = 0; u < h; u++)
+            if (d_b1 && !swiglu) d_b1[(int64_t)ex * h + u] = (float)gb1[u];
+        for (int i = 0; i < m; i++)
+            if (d_b2 && !swiglu) d_b2[(int64_t)ex * m + i] = (float)gb2[i];
+        free(gw1); free(gw3); free(gw2); free(gb1); free(gb2); free(hid); free(dp); free(dq);
+    }
+}
