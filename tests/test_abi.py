@@ -97,4 +97,32 @@ def test_invalid_arguments_are_rejected_before_launch():
     assert dec(A, M.MOE_F32, A, A, A, A, 10, 6, 4, 1, 8, A, A, None) == INV    # m % 4 != 0 (fp32)
     enc = lib.moe_encode
     assert enc(A, M.MOE_BF16, A, A, None, A, 10, 64, 4, 1, 8, M.MOE_FLAG_ZERO_FILL, A, A, None) == INV
+    # gate backward: x, wg, bias, s, m, e, k, flags, idx, gates, d_gates, d_logits,
+    # d_wg, d_bias, d_x, status, stream
+    gbwd = lib.moe_gate_bwd
+    ok = (A, M.MOE_BF16, B, None, 10, 64, 8, 2, 1, A, B, A, B, None, None, None, A, None)
+    def gb(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return gbwd(*a)
+    assert gb(a6=300) == M.MOE_ERR_UNSUPPORTED                   # e > 256
+    assert gb(a7=9) == INV                                       # k > e
+    assert gb(a5=60) == INV                                      # bf16 rows not a multiple of 8
+    assert gb(a8=4) == INV                                       # unknown flag
+    assert gb(a0=odd) == INV and gb(a2=odd) == INV               # misaligned x / wg
+    assert gb(a12=None) == INV                                   # d_logits is required
+    assert gb(a11=None) == INV and gb(a10=None) == INV           # d_gates, gates are required
+    assert gb(a13=odd) == INV and gb(a15=odd) == INV             # misaligned d_wg / d_x
+    assert gb(a3=odd) == INV                                     # misaligned bias
+    dbwd = lib.moe_decode_bwd
+    # dy, out, dt, idx, loc, gates, counts, c_dev, s, m, e, k, c_max, flags, d_out, d_gates, status
+    assert dbwd(A, A, M.MOE_BF16, A, A, A, None, A, 10, 64, 4, 1, 0, 0, A, A, A, None) == INV
+    assert dbwd(A, A, M.MOE_BF16, A, A, A, None, A, 10, 64, 4, 1, 8, M.MOE_FLAG_ZERO_FILL, A, A, A,
+                None) == INV                                     # zero fill needs counts
+    assert dbwd(odd, A, M.MOE_BF16, A, A, A, None, A, 10, 64, 4, 1, 8, 0, A, A, A, None) == INV
+    ebwd = lib.moe_encode_bwd
+    # d_buf, dt, idx, loc, c_dev, s, m, e, k, c_max, dx, status
+    assert ebwd(A, M.MOE_BF16, A, A, A, 10, 64, 4, 5, 8, A, A, None) == INV      # k > e
+    assert ebwd(A, M.MOE_BF16, A, A, A, 10, 64, 4, 1, 8, odd, A, None) == INV    # misaligned dx
     assert M.launch_count() == before
