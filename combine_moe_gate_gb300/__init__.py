@@ -86,8 +86,37 @@ def launch_count() -> int:
     return int(load().moe_launch_count())
 
 
-def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+def _ptr(t, name="tensor", dtype=None, shape=None):
+    """Device address of a contiguous CUDA tensor; checks the dtype and shape
+    when given (a mismatch here would let a kernel read or write out of
+    bounds).  None passes through as NULL."""
+    if t is None:
+        return None
+    if shape is not None and tuple(t.shape) != tuple(int(d) for d in shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if not _on_device(t):
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _on_device(t) -> bool:
+    return t.is_cuda
+
+
+def _i32():
+    import torch
+
+    return torch.int32
+
+
+def _f32():
+    import torch
+
+    return torch.float32
 
 
 def _dt(t):
@@ -141,18 +170,24 @@ def moe_gate_topk(x, wg, bias, k, idx, gates, dev_status, flags=0, stream=None):
     """x [s, m]; wg [m, e] fp32; bias [e] fp32 or None -> idx [k, s] int32, gates [k, s] fp32."""
     s, m = x.shape
     e = wg.shape[1]
-    _check(load().moe_gate_topk(_ptr(x), _dt(x), _ptr(wg), _ptr(bias), s, m, e, int(k),
-                                int(flags), _ptr(idx), _ptr(gates), _ptr(dev_status),
-                                _stream(stream)), "moe_gate_topk")
+    k = int(k)
+    I, F = _i32(), _f32()
+    _check(load().moe_gate_topk(
+        _ptr(x, "x"), _dt(x), _ptr(wg, "wg", F, (m, e)), _ptr(bias, "bias", F, (e,)), s, m, e, k,
+        int(flags), _ptr(idx, "idx", I, (k, s)), _ptr(gates, "gates", F, (k, s)),
+        _ptr(dev_status, "dev_status", I), _stream(stream)), "moe_gate_topk")
 
 
 def moe_capacity_locations(idx, e, capacity_factor, c_max, workspace, loc, counts, c_dev,
                            dev_status, stream=None):
     k, s = idx.shape
+    I = _i32()
     _check(load().moe_capacity_locations(
-        _ptr(idx), s, int(e), k, float(capacity_factor), int(c_max), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _ptr(loc), _ptr(counts), _ptr(c_dev),
-        _ptr(dev_status), _stream(stream)), "moe_capacity_locations")
+        _ptr(idx, "idx", I), s, int(e), k, float(capacity_factor), int(c_max),
+        _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _ptr(loc, "loc", I, (k, s)), _ptr(counts, "counts", I, (int(e),)),
+        _ptr(c_dev, "c_dev", I), _ptr(dev_status, "dev_status", I), _stream(stream)),
+        "moe_capacity_locations")
 
 
 def moe_encode(x, idx, loc, counts, c_dev, buf, dev_status, flags=0, stream=None):
@@ -160,38 +195,50 @@ def moe_encode(x, idx, loc, counts, c_dev, buf, dev_status, flags=0, stream=None
     s, m = x.shape
     k = idx.shape[0]
     e, c_max, _ = buf.shape
-    _check(load().moe_encode(_ptr(x), _dt(x), _ptr(idx), _ptr(loc), _ptr(counts), _ptr(c_dev),
-                             s, m, e, k, c_max, int(flags), _ptr(buf), _ptr(dev_status),
-                             _stream(stream)), "moe_encode")
+    I = _i32()
+    _check(load().moe_encode(
+        _ptr(x, "x"), _dt(x), _ptr(idx, "idx", I, (k, s)), _ptr(loc, "loc", I, (k, s)),
+        _ptr(counts, "counts", I, (e,)), _ptr(c_dev, "c_dev", I), s, m, e, k, c_max, int(flags),
+        _ptr(buf, "buf", x.dtype, (e, c_max, m)), _ptr(dev_status, "dev_status", I),
+        _stream(stream)), "moe_encode")
 
 
 def moe_expert_ffn(buf, counts, c_dev, w1, b1, w3, w2, b2, act, workspace, out, dev_status,
                    stream=None):
     e, c_max, m = buf.shape
     h = w1.shape[1]
+    I, dt = _i32(), buf.dtype
     _check(load().moe_expert_ffn(
-        _ptr(buf), _dt(buf), _ptr(counts), _ptr(c_dev), _ptr(w1), _ptr(b1), _ptr(w3), _ptr(w2),
-        _ptr(b2), _act(act), e, c_max, m, h, _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _ptr(out), _ptr(dev_status),
+        _ptr(buf, "buf"), _dt(buf), _ptr(counts, "counts", I, (e,)), _ptr(c_dev, "c_dev", I),
+        _ptr(w1, "w1", dt, (e, h, m)), _ptr(b1, "b1", dt, (e, h)), _ptr(w3, "w3", dt, (e, h, m)),
+        _ptr(w2, "w2", dt, (e, m, h)), _ptr(b2, "b2", dt, (e, m)), _act(act), e, c_max, m, h,
+        _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _ptr(out, "out", dt, (e, c_max, m)), _ptr(dev_status, "dev_status", I),
         _stream(stream)), "moe_expert_ffn")
 
 
 def moe_decode(out, idx, loc, gates, c_dev, y, dev_status, stream=None):
     e, c_max, m = out.shape
     k, s = idx.shape
-    _check(load().moe_decode(_ptr(out), _dt(out), _ptr(idx), _ptr(loc), _ptr(gates), _ptr(c_dev),
-                             s, m, e, k, c_max, _ptr(y), _ptr(dev_status), _stream(stream)),
-           "moe_decode")
+    I, F = _i32(), _f32()
+    _check(load().moe_decode(
+        _ptr(out, "out"), _dt(out), _ptr(idx, "idx", I), _ptr(loc, "loc", I, (k, s)),
+        _ptr(gates, "gates", F, (k, s)), _ptr(c_dev, "c_dev", I), s, m, e, k, c_max,
+        _ptr(y, "y", out.dtype, (s, m)), _ptr(dev_status, "dev_status", I), _stream(stream)),
+        "moe_decode")
 
 
 def moe_decode_bwd(dy, out, idx, loc, gates, counts, c_dev, d_out, d_gates, dev_status, flags=0,
                    stream=None):
     e, c_max, m = out.shape
     k, s = idx.shape
+    I, F, dt = _i32(), _f32(), out.dtype
     _check(load().moe_decode_bwd(
-        _ptr(dy), _ptr(out), _dt(out), _ptr(idx), _ptr(loc), _ptr(gates), _ptr(counts),
-        _ptr(c_dev), s, m, e, k, c_max, int(flags), _ptr(d_out), _ptr(d_gates), _ptr(dev_status),
-        _stream(stream)), "moe_decode_bwd")
+        _ptr(dy, "dy", dt, (s, m)), _ptr(out, "out"), _dt(out), _ptr(idx, "idx", I),
+        _ptr(loc, "loc", I, (k, s)), _ptr(gates, "gates", F, (k, s)),
+        _ptr(counts, "counts", I, (e,)), _ptr(c_dev, "c_dev", I), s, m, e, k, c_max, int(flags),
+        _ptr(d_out, "d_out", dt, (e, c_max, m)), _ptr(d_gates, "d_gates", F, (k, s)),
+        _ptr(dev_status, "dev_status", I), _stream(stream)), "moe_decode_bwd")
 
 
 def moe_gate_bwd(x, wg, bias, idx, gates, d_gates, d_logits, dev_status, d_wg=None, d_bias=None,
@@ -201,18 +248,24 @@ def moe_gate_bwd(x, wg, bias, idx, gates, d_gates, d_logits, dev_status, d_wg=No
     s, m = x.shape
     e = wg.shape[1]
     k = idx.shape[0]
-    _check(load().moe_gate_bwd(_ptr(x), _dt(x), _ptr(wg), _ptr(bias), s, m, e, k, int(flags),
-                               _ptr(idx), _ptr(gates), _ptr(d_gates), _ptr(d_logits), _ptr(d_wg),
-                               _ptr(d_bias), _ptr(d_x), _ptr(dev_status), _stream(stream)),
-           "moe_gate_bwd")
+    I, F = _i32(), _f32()
+    _check(load().moe_gate_bwd(
+        _ptr(x, "x"), _dt(x), _ptr(wg, "wg", F, (m, e)), _ptr(bias, "bias", F, (e,)), s, m, e, k,
+        int(flags), _ptr(idx, "idx", I, (k, s)), _ptr(gates, "gates", F, (k, s)),
+        _ptr(d_gates, "d_gates", F, (k, s)), _ptr(d_logits, "d_logits", F, (s, e)),
+        _ptr(d_wg, "d_wg", F, (m, e)), _ptr(d_bias, "d_bias", F, (e,)),
+        _ptr(d_x, "d_x", F, (s, m)), _ptr(dev_status, "dev_status", I), _stream(stream)),
+        "moe_gate_bwd")
 
 
 def moe_encode_bwd(d_buf, idx, loc, c_dev, dx, dev_status, stream=None):
     e, c_max, m = d_buf.shape
     k, s = idx.shape
-    _check(load().moe_encode_bwd(_ptr(d_buf), _dt(d_buf), _ptr(idx), _ptr(loc), _ptr(c_dev), s, m,
-                                 e, k, c_max, _ptr(dx), _ptr(dev_status), _stream(stream)),
-           "moe_encode_bwd")
+    I = _i32()
+    _check(load().moe_encode_bwd(
+        _ptr(d_buf, "d_buf"), _dt(d_buf), _ptr(idx, "idx", I), _ptr(loc, "loc", I, (k, s)),
+        _ptr(c_dev, "c_dev", I), s, m, e, k, c_max, _ptr(dx, "dx", d_buf.dtype, (s, m)),
+        _ptr(dev_status, "dev_status", I), _stream(stream)), "moe_encode_bwd")
 
 
 def moe_layer_forward(x, wg, gate_bias, w1, b1, w3, w2, b2, act, k, capacity_factor, flags,
@@ -221,11 +274,17 @@ def moe_layer_forward(x, wg, gate_bias, w1, b1, w3, w2, b2, act, k, capacity_fac
     s, m = x.shape
     e, c_max, _ = buf.shape
     h = w1.shape[1]
+    k = int(k)
+    I, F, dt = _i32(), _f32(), x.dtype
     _check(load().moe_layer_forward(
-        _ptr(x), _dt(x), _ptr(wg), _ptr(gate_bias), _ptr(w1), _ptr(b1), _ptr(w3), _ptr(w2),
-        _ptr(b2), _act(act), s, m, e, int(k), h, float(capacity_factor), c_max, int(flags),
-        _ptr(idx), _ptr(gates), _ptr(loc), _ptr(counts), _ptr(c_dev), _ptr(buf), _ptr(out),
-        _ptr(y), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status),
+        _ptr(x, "x"), _dt(x), _ptr(wg, "wg", F, (m, e)), _ptr(gate_bias, "gate_bias", F, (e,)),
+        _ptr(w1, "w1", dt, (e, h, m)), _ptr(b1, "b1", dt, (e, h)), _ptr(w3, "w3", dt, (e, h, m)),
+        _ptr(w2, "w2", dt, (e, m, h)), _ptr(b2, "b2", dt, (e, m)), _act(act), s, m, e, k, h,
+        float(capacity_factor), c_max, int(flags), _ptr(idx, "idx", I, (k, s)),
+        _ptr(gates, "gates", F, (k, s)), _ptr(loc, "loc", I, (k, s)),
+        _ptr(counts, "counts", I, (e,)), _ptr(c_dev, "c_dev", I), _ptr(buf, "buf", dt, (e, c_max, m)),
+        _ptr(out, "out", dt, (e, c_max, m)), _ptr(y, "y", dt, (s, m)), _ptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status, "dev_status", I),
         _stream(stream)), "moe_layer_forward")
 
 
