@@ -118,3 +118,35 @@ def test_gate_gradient_is_exact_derivative():
             C2 = dense.combine_weights(idx, loc, g2, c, e)
             fd = np.sum((dense.decode(C2, out) - base) * dY)
             assert abs(d_g[r, t] - fd) <= 1e-5 * (1 + abs(fd))
+
+
+def _one_token(vals, gates):
+    """One token whose k routes go to experts 0..k-1, slot 0 each, m = 1."""
+    k = len(vals)
+    out = np.array(vals, np.float32).reshape(k, 1, 1)           # [e = k, c = 1, m = 1]
+    idx = np.arange(k, dtype=np.int32).reshape(k, 1)
+    loc = np.zeros((k, 1), np.int32)
+    g = np.array(gates, np.float32).reshape(k, 1)
+    return out, idx, loc, g
+
+
+def test_decode_accumulates_by_fused_multiply_add_in_route_order():
+    """The combine accumulates in fp32 (the DeepSpeed index-dispatch PR, change
+    3); the reading adopted is one fused multiply-add per kept route, in
+    ascending route order from +0.  Route 0 contributes 1 * (-1), route 1
+    (1 + 2^-12)^2 = 1 + 2^-11 + 2^-24: fused, the low bit survives and y =
+    2^-11 + 2^-24.  A separate multiply rounds the product to 1 + 2^-11 (tie to
+    even) and gives 2^-11; the reverse route order gives 2^-11 as well."""
+    u = 1.0 + 2.0 ** -12
+    out, idx, loc, g = _one_token([-1.0, u], [1.0, u])
+    y = oracle.decode(out, idx, loc, g, 1, False)
+    assert y[0, 0] == np.float32(2.0 ** -11 + 2.0 ** -24)
+
+
+def test_encode_bwd_adds_routes_in_ascending_order():
+    """dX sums the kept routes' rows in fp32 in ascending route order from +0:
+    2^24 + 1 ties to even at 2^24, and - 2^24 then gives 0.  Descending order
+    would give -2^24 + 1 = -16777215 (exact), then + 2^24 = 1."""
+    d_buf, idx, loc, _ = _one_token([2.0 ** 24, 1.0, -(2.0 ** 24)], [1.0, 1.0, 1.0])
+    dx = oracle.encode_bwd(d_buf, idx, loc, 1, False)
+    assert dx[0, 0] == 0.0
