@@ -150,3 +150,32 @@ def test_encode_bwd_adds_routes_in_ascending_order():
     d_buf, idx, loc, _ = _one_token([2.0 ** 24, 1.0, -(2.0 ** 24)], [1.0, 1.0, 1.0])
     dx = oracle.encode_bwd(d_buf, idx, loc, 1, False)
     assert dx[0, 0] == 0.0
+
+
+def _bf16_of_f32(a):
+    return synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(a))
+
+
+def test_bf16_outputs_are_rounded_once():
+    """With bf16 tensors the combine, its K0 twin and dE are rounded to bf16
+    exactly once, after the fp32 accumulation (decode, encode backward) or from
+    the exact product g * dY (decode backward)."""
+    s, m, e, k = 70, 16, 5, 2
+    idx, g, loc, needed, c = _routing(21, s, e, k, 0.8)
+    cmax = c + 2
+    out = _bf16_of_f32(synth.normal_host(21, "out", (e, cmax, m), 1.0, "f32"))
+    dy = _bf16_of_f32(synth.normal_host(21, "dy", (s, m), 1.0, "f32"))
+    y_b = oracle.decode(out, idx, loc, g, c, True)
+    y_f = oracle.decode(out, idx, loc, g, c, False)
+    assert np.array_equal(y_b.view(np.uint32), _bf16_of_f32(y_f).view(np.uint32))
+    dx_b = oracle.encode_bwd(out, idx, loc, c, True)
+    dx_f = oracle.encode_bwd(out, idx, loc, c, False)
+    assert np.array_equal(dx_b.view(np.uint32), _bf16_of_f32(dx_f).view(np.uint32))
+    d_out, _ = oracle.decode_bwd(dy, out, idx, loc, g, c, True)
+    kept = loc < c
+    for r, t in zip(*np.nonzero(kept)):
+        row = d_out[idx[r, t], loc[r, t]].astype(np.float64)
+        exact = np.float64(g[r, t]) * dy[t].astype(np.float64)
+        assert np.all(row.astype(np.float32).view(np.uint32) & 0xFFFF == 0)      # bf16 values
+        # nearest bf16: within half a bf16 step (2^-8 relative) of the exact product
+        assert np.all(np.abs(row - exact) <= np.abs(exact) * 2.0 ** -8)
