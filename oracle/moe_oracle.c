@@ -80,7 +80,7 @@ int orc_get_threads(void)
 
 /* Gate logits l[t,j] = x[t,:] . wg[:,j] + bias[j]   ([Tutel] gate_type 'top').
  *
- * Precision and order (the reading this build fixes so that top-k is
+ * Precision and order (the reading adopted here, so that top-k is
  * reproducible bit for bit): fp32 with one rounding per fused multiply-add,
  * then one fp32 add of bias[j] (skipped when bias is NULL).  The summation
  * order depends on `chunk`:
