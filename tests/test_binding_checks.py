@@ -92,3 +92,59 @@ def test_backward_and_layer_entry_points_check_their_outputs(host_as_device):
                             torch.zeros((e, m, h), **bf), None, "gelu", k, 1.0, 0, idx,
                             torch.zeros((k, s)), loc, counts, c_dev, out, out,
                             torch.zeros((s, m), **bf), torch.zeros(16, dtype=torch.uint8), st)
+
+
+class _StubLib:
+    """Records each call's arguments instead of calling the library."""
+
+    def __init__(self):
+        self.calls = {}
+
+    def __getattr__(self, name):
+        def fn(*args):
+            self.calls[name] = args
+            return 0
+        return fn
+
+
+@pytest.fixture
+def stub(monkeypatch, host_as_device):
+    lib = _StubLib()
+    monkeypatch.setattr(M, "load", lambda: lib)
+    monkeypatch.setattr(M, "_stream", lambda s: None)
+    return lib
+
+
+def test_well_formed_calls_pass_and_marshal_their_sizes(stub):
+    s, m, e, k, h, c_max = 24, 64, 8, 2, 32, 10
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    z = lambda *shape, dtype=f32: torch.zeros(shape, dtype=dtype)
+    x, wg, gb = z(s, m, dtype=bf), z(m, e), z(e)
+    idx, loc, gates = z(k, s, dtype=i32), z(k, s, dtype=i32), z(k, s)
+    counts, c_dev, st = z(e, dtype=i32), z(1, dtype=i32), z(1, dtype=i32)
+    buf, out = z(e, c_max, m, dtype=bf), z(e, c_max, m, dtype=bf)
+    w1, w2, b1, b2 = z(e, h, m, dtype=bf), z(e, m, h, dtype=bf), z(e, h, dtype=bf), z(e, m, dtype=bf)
+    ws = z(4096, dtype=torch.uint8)
+    M.moe_gate_topk(x, wg, gb, k, idx, gates, st, flags=1)
+    M.moe_capacity_locations(idx, e, 1.25, c_max, ws, loc, counts, c_dev, st)
+    M.moe_encode(x, idx, loc, counts, c_dev, buf, st)
+    M.moe_expert_ffn(buf, counts, c_dev, w1, b1, None, w2, b2, "gelu", ws, out, st)
+    M.moe_decode(out, idx, loc, gates, c_dev, z(s, m, dtype=bf), st)
+    M.moe_decode_bwd(z(s, m, dtype=bf), out, idx, loc, gates, counts, c_dev, z(e, c_max, m, dtype=bf),
+                     z(k, s), st)
+    M.moe_encode_bwd(out, idx, loc, c_dev, z(s, m, dtype=bf), st)
+    M.moe_gate_bwd(x, wg, gb, idx, gates, z(k, s), z(s, e), st, d_wg=z(m, e), d_bias=z(e),
+                   d_x=z(s, m))
+    M.moe_layer_forward(x, wg, gb, w1, b1, None, w2, b2, "gelu", k, 1.25, 1, idx, gates, loc,
+                        counts, c_dev, buf, out, z(s, m, dtype=bf), ws, st)
+    c = stub.calls
+    assert c["moe_gate_topk"][4:8] == (s, m, e, k)
+    assert c["moe_capacity_locations"][1:4] == (s, e, k)
+    assert c["moe_encode"][6:11] == (s, m, e, k, c_max)
+    assert c["moe_expert_ffn"][10:14] == (e, c_max, m, h)
+    assert c["moe_decode"][6:11] == (s, m, e, k, c_max)
+    assert c["moe_decode_bwd"][8:13] == (s, m, e, k, c_max)
+    assert c["moe_encode_bwd"][5:10] == (s, m, e, k, c_max)
+    assert c["moe_gate_bwd"][4:8] == (s, m, e, k)
+    assert c["moe_layer_forward"][10:15] == (s, m, e, k, h)
+    assert c["moe_layer_forward"][16] == c_max
