@@ -54,6 +54,9 @@ def load():
         "moe_encode": (I, [P, I, P, P, P, P, I64, I, I, I, I64, U, P, P, P]),
         "moe_expert_ffn_workspace_size": (SZ, [I, I, I, I64, I, I]),
         "moe_expert_ffn": (I, [P, I, P, P, P, P, P, P, P, I, I, I64, I, I, P, SZ, P, P, P]),
+        "moe_expert_ffn_bwd_workspace_size": (SZ, [I, I, I, I64, I, I]),
+        "moe_expert_ffn_bwd": (I, [P, P, I, P, P, P, P, P, P, I, I, I64, I, I, P, P, SZ, P, P, P,
+                                   P, P, P, P, P]),
         "moe_decode": (I, [P, I, P, P, P, P, I64, I, I, I, I64, P, P, P]),
         "moe_decode_bwd": (I, [P, P, I, P, P, P, P, P, I64, I, I, I, I64, U, P, P, P, P]),
         "moe_encode_bwd": (I, [P, I, P, P, P, I64, I, I, I, I64, P, P, P]),
@@ -160,6 +163,11 @@ def moe_expert_ffn_workspace_size(dtype, act, e, c_max, m, h) -> int:
                                                     int(m), int(h)))
 
 
+def moe_expert_ffn_bwd_workspace_size(dtype, act, e, c_max, m, h) -> int:
+    return int(load().moe_expert_ffn_bwd_workspace_size(int(dtype), _act(act), int(e), int(c_max),
+                                                        int(m), int(h)))
+
+
 def moe_layer_workspace_size(dtype, act, s, m, e, k, c_max, h) -> int:
     return int(load().moe_layer_workspace_size(int(dtype), _act(act), int(s), int(m), int(e),
                                                int(k), int(c_max), int(h)))
@@ -215,6 +223,25 @@ def moe_expert_ffn(buf, counts, c_dev, w1, b1, w3, w2, b2, act, workspace, out, 
         _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _ptr(out, "out", dt, (e, c_max, m)), _ptr(dev_status, "dev_status", I),
         _stream(stream)), "moe_expert_ffn")
+
+
+def moe_expert_ffn_bwd(buf, hid, counts, c_dev, w1, b1, w3, w2, act, d_out, workspace, d_buf,
+                       d_w1, d_w3, d_w2, d_b1, d_b2, dev_status, stream=None):
+    """Gradient of moe_expert_ffn over the kept rows (bf16); hid is the
+    forward's hidden (its workspace after the call)."""
+    e, c_max, m = buf.shape
+    h = w1.shape[1]
+    I, dt = _i32(), buf.dtype
+    _check(load().moe_expert_ffn_bwd(
+        _ptr(buf, "buf"), _ptr(hid, "hid", dt, (e, c_max, h)), _dt(buf),
+        _ptr(counts, "counts", I, (e,)), _ptr(c_dev, "c_dev", I), _ptr(w1, "w1", dt, (e, h, m)),
+        _ptr(b1, "b1", dt, (e, h)), _ptr(w3, "w3", dt, (e, h, m)), _ptr(w2, "w2", dt, (e, m, h)),
+        _act(act), e, c_max, m, h, _ptr(d_out, "d_out", dt, (e, c_max, m)),
+        _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _ptr(d_buf, "d_buf", dt, (e, c_max, m)), _ptr(d_w1, "d_w1", dt, (e, h, m)),
+        _ptr(d_w3, "d_w3", dt, (e, h, m)), _ptr(d_w2, "d_w2", dt, (e, m, h)),
+        _ptr(d_b1, "d_b1", dt, (e, h)), _ptr(d_b2, "d_b2", dt, (e, m)),
+        _ptr(dev_status, "dev_status", I), _stream(stream)), "moe_expert_ffn_bwd")
 
 
 def moe_decode(out, idx, loc, gates, c_dev, y, dev_status, stream=None):

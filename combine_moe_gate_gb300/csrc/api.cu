@@ -41,6 +41,12 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
                          const void *w1, const void *b1, const void *w3, const void *w2,
                          const void *b2, moe_act act, int e, int64_t c_max, int m, int h,
                          void *hid, void *out, int32_t *st, cudaStream_t stream);
+size_t ffn_tc_bwd_workspace_bytes(moe_act act, int e, int64_t c_max, int m, int h);
+moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *counts,
+                             const int32_t *c_dev, const void *w1, const void *b1, const void *w3,
+                             const void *w2, moe_act act, int e, int64_t c_max, int m, int h,
+                             const void *d_out, void *ws, void *d_buf, void *d_w1, void *d_w3,
+                             void *d_w2, void *d_b1, void *d_b2, int32_t *st, cudaStream_t stream);
 moe_status ffn_simt_launch(const void *buf, moe_dtype dt, const int32_t *counts,
                            const int32_t *c_dev, const void *w1, const void *b1, const void *w3,
                            const void *w2, const void *b2, moe_act act, int e, int64_t c_max,
@@ -226,6 +232,44 @@ moe_status moe_encode_bwd(const void *d_buf, moe_dtype dt, const int32_t *idx, c
         return MOE_ERR_INVALID_ARG;
     return combine_launch(d_buf, dt, idx, loc, nullptr, c_dev, s, m, e, k, c_max, dx, dev_status,
                           as_stream(stream));
+}
+
+size_t moe_expert_ffn_bwd_workspace_size(moe_dtype dt, moe_act act, int e, int64_t c_max, int m,
+                                         int h) {
+    if (dt != MOE_BF16 || e < 1 || e > kMaxE || c_max < 1 || m < 1 || h < 1) return 0;
+    if (act != MOE_ACT_RELU && act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU) return 0;
+    return ffn_tc_bwd_workspace_bytes(act, e, c_max, m, h);
+}
+
+moe_status moe_expert_ffn_bwd(const void *buf, const void *hid, moe_dtype dt,
+                              const int32_t *counts, const int32_t *c_dev, const void *w1,
+                              const void *b1, const void *w3, const void *w2, moe_act act, int e,
+                              int64_t c_max, int m, int h, const void *d_out, void *workspace,
+                              size_t workspace_bytes, void *d_buf, void *d_w1, void *d_w3,
+                              void *d_w2, void *d_b1, void *d_b2, int32_t *dev_status,
+                              void *stream) {
+    if (!rows_ok(dt, m) || !rows_ok(dt, h) || e < 1 || e > kMaxE || c_max < 1 ||
+        c_max > 0x7fffffff || !ok16(buf) || !ok16(hid) || !ok4(counts) || !ok4(c_dev) ||
+        !ok16(w1) || !ok16(w2) || !opt16(b1) || !ok16(d_out) || !ok16(workspace) ||
+        !ok16(d_buf) || !ok16(d_w1) || !ok16(d_w2) || !opt16(d_b1) || !opt16(d_b2) ||
+        !ok4(dev_status))
+        return MOE_ERR_INVALID_ARG;
+    if (act != MOE_ACT_RELU && act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU)
+        return MOE_ERR_INVALID_ARG;
+    if (act == MOE_ACT_SWIGLU &&
+        (!ok16(w3) || !ok16(d_w3) || b1 != nullptr || d_b1 != nullptr || d_b2 != nullptr))
+        return MOE_ERR_INVALID_ARG;
+    if (dt != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (workspace_bytes < moe_expert_ffn_bwd_workspace_size(dt, act, e, c_max, m, h))
+        return MOE_ERR_INVALID_ARG;
+    const int64_t h2 = act == MOE_ACT_SWIGLU ? 2 * (int64_t)h : h;
+    // every operand of the products within the grouped GEMM's index range
+    if (!ffn_tc_supported(e, c_max, m, h) || !ffn_tc_supported(e, h2, m, h) ||
+        (int64_t)e * h2 >= ((int64_t)1 << 31) || (int64_t)e * ((c_max + 7) / 8 * 8) >= ((int64_t)1 << 31))
+        return MOE_ERR_UNSUPPORTED;
+    return ffn_tc_bwd_launch(buf, hid, counts, c_dev, w1, b1, w3, w2, act, e, c_max, m, h, d_out,
+                             workspace, d_buf, d_w1, d_w3, d_w2, d_b1, d_b2, dev_status,
+                             as_stream(stream));
 }
 
 size_t moe_layer_workspace_size(moe_dtype dt, moe_act act, int64_t s, int m, int e, int k,

@@ -1,0 +1,183 @@
+// SIMT helper kernels of the expert-FFN backward: zero-padded transposes (so
+// that every product runs on the forward's K-major grouped GEMM), the
+// activation derivative, and bias-gradient column sums.
+//
+// Method: the Tutel profile's experts {'type': 'ffn', hidden_size_per_expert,
+// has_fc1_bias, has_fc2_bias}, differentiated: with pre = x w1^T + b1 and
+// hid = act(pre), d_pre = (d_out w2) * act'(pre); SwiGLU (hid = silu(a) b)
+// splits it into d_a = d_hid b silu'(a) and d_b = d_hid silu(a).
+#include "ffn_bwd.cuh"
+
+namespace moe {
+namespace {
+
+// ------------------------------------------------------------- transposes
+constexpr int TP = 32, TP_Y = 8;
+
+__global__ void __launch_bounds__(TP * TP_Y)
+transpose_pad_kernel(const uint16_t *__restrict__ src, int64_t src_batch, int64_t src_pitch,
+                     uint16_t *__restrict__ dst, int64_t dst_batch, int64_t dst_pitch, int rows,
+                     int cols, int dst_cols, const int32_t *__restrict__ counts,
+                     const int32_t *__restrict__ c_dev, int32_t *status) {
+    pdl_enter();
+    if (status_bad(status)) return;
+    __shared__ uint32_t tile[TP][TP + 1];
+    const int b = blockIdx.z;
+    const int r0 = blockIdx.x * TP, c0 = blockIdx.y * TP;
+    int kept = rows;
+    if (counts) kept = max(0, min(min(counts[b], *c_dev), rows));
+    const uint16_t *s = src + (int64_t)b * src_batch;
+    uint16_t *d = dst + (int64_t)b * dst_batch;
+    for (int i = threadIdx.y; i < TP; i += TP_Y) {
+        const int r = r0 + i, c = c0 + (int)threadIdx.x;
+        tile[i][threadIdx.x] = (r < kept && c < cols) ? (uint32_t)s[(int64_t)r * src_pitch + c] : 0u;
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < TP; i += TP_Y) {
+        const int c = c0 + i, r = r0 + (int)threadIdx.x;
+        if (c < cols && r < dst_cols) d[(int64_t)c * dst_pitch + r] = (uint16_t)tile[threadIdx.x][i];
+    }
+}
+
+// ---------------------------------------------------- activation backward
+constexpr int AB_THREADS = 256;
+
+__global__ void __launch_bounds__(AB_THREADS)
+act_bwd_kernel(const __nv_bfloat16 *__restrict__ pa, const __nv_bfloat16 *__restrict__ pb,
+               const __nv_bfloat16 *__restrict__ dh, int act, int e, int64_t c_max, int h,
+               const int32_t *__restrict__ counts, const int32_t *__restrict__ c_dev,
+               __nv_bfloat16 *__restrict__ d_pre, int32_t *status) {
+    pdl_enter();
+    if (status_bad(status)) return;
+    const bool swiglu = act == MOE_ACT_SWIGLU;
+    const int hv = h / 8;                                  // 16-byte chunks per row
+    const int64_t h2 = swiglu ? 2 * (int64_t)h : (int64_t)h;
+    const int64_t n = (int64_t)e * c_max * hv;
+    const int c = *c_dev;
+    for (int64_t q = (int64_t)blockIdx.x * AB_THREADS + threadIdx.x; q < n;
+         q += (int64_t)gridDim.x * AB_THREADS) {
+        const int64_t row = q / hv;
+        const int v = (int)(q % hv);
+        const int j = (int)(row / c_max);
+        const int64_t r = row % c_max;
+        if (r >= (int64_t)min(counts[j], c)) continue;
+        const int64_t off = row * h + (int64_t)v * 8;
+        float a[8], g[8], o[8];
+        Elt<__nv_bfloat16>::unpack(ld_v16(pa + off), a);
+        Elt<__nv_bfloat16>::unpack(ld_v16(dh + off), g);
+        __nv_bfloat16 *dst = d_pre + row * h2 + (int64_t)v * 8;
+        if (swiglu) {
+            float b[8], ob[8];
+            Elt<__nv_bfloat16>::unpack(ld_v16(pb + off), b);
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const float sg = 1.0f / (1.0f + expf(-a[i]));
+                o[i] = g[i] * b[i] * sg * (1.0f + a[i] * (1.0f - sg));   // d_a
+                ob[i] = g[i] * a[i] * sg;                                // d_b
+            }
+            st_v16(dst, Elt<__nv_bfloat16>::pack(o));
+            st_v16(dst + h, Elt<__nv_bfloat16>::pack(ob));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                float dact;
+                if (act == MOE_ACT_RELU) {
+                    dact = a[i] > 0.0f ? 1.0f : 0.0f;
+                } else {
+                    // GELU'(z) = Phi(z) + z phi(z); 0.3989... = 1 / sqrt(2 pi)
+                    dact = normcdff(a[i]) + a[i] * expf(-0.5f * a[i] * a[i]) * 0.3989422804014327f;
+                }
+                o[i] = g[i] * dact;
+            }
+            st_v16(dst, Elt<__nv_bfloat16>::pack(o));
+        }
+    }
+}
+
+// --------------------------------------------------------- column sums
+// A CTA owns 32 columns of one expert (lane = column); its 8 warps take every
+// 8th kept row and the partials are added in warp order.
+constexpr int CS_WARPS = 8;
+
+__global__ void __launch_bounds__(CS_WARPS * 32)
+colsum_kernel(const __nv_bfloat16 *__restrict__ src, int64_t c_max, int cols, int64_t pitch,
+              const int32_t *__restrict__ counts, const int32_t *__restrict__ c_dev,
+              __nv_bfloat16 *__restrict__ out, int32_t *status) {
+    pdl_enter();
+    if (status_bad(status)) return;
+    __shared__ float part[CS_WARPS][33];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int j = blockIdx.y;
+    const int col = blockIdx.x * 32 + lane;
+    const int64_t kept = max(0, min(min(counts[j], *c_dev), (int)min(c_max, (int64_t)0x7fffffff)));
+    float acc = 0.0f;
+    if (col < cols) {
+        const __nv_bfloat16 *s = src + (int64_t)j * c_max * pitch + col;
+#pragma unroll 4
+        for (int64_t r = warp; r < kept; r += CS_WARPS) acc += __bfloat162float(s[r * pitch]);
+    }
+    part[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0 && col < cols) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int w = 0; w < CS_WARPS; w++) sum += part[w][lane];
+        out[(int64_t)j * cols + col] = __float2bfloat16_rn(sum);
+    }
+}
+
+__global__ void fill_i32_kernel(int32_t *p, int n, int32_t v) {
+    pdl_enter();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = v;
+}
+
+}  // namespace
+
+moe_status transpose_pad_launch(const __nv_bfloat16 *src, int64_t src_batch, int64_t src_pitch,
+                                __nv_bfloat16 *dst, int64_t dst_batch, int64_t dst_pitch,
+                                int batches, int rows, int cols, int dst_cols,
+                                const int32_t *counts, const int32_t *c_dev, int32_t *status,
+                                cudaStream_t stream) {
+    if (batches < 1 || batches > 65535 || rows < 0 || cols < 1 || dst_cols < rows)
+        return MOE_ERR_INVALID_ARG;
+    const dim3 grid((unsigned)((dst_cols + TP - 1) / TP), (unsigned)((cols + TP - 1) / TP),
+                    (unsigned)batches);
+    if (grid.y > 65535) return MOE_ERR_UNSUPPORTED;
+    return launch_pdl(transpose_pad_kernel, grid, dim3(TP, TP_Y), 0, stream,
+                      (const uint16_t *)src, src_batch, src_pitch, (uint16_t *)dst, dst_batch,
+                      dst_pitch, rows, cols, dst_cols, counts, c_dev, status);
+}
+
+moe_status act_bwd_launch(const __nv_bfloat16 *pa, const __nv_bfloat16 *pb,
+                          const __nv_bfloat16 *d_hid, moe_act act, int e, int64_t c_max, int h,
+                          const int32_t *counts, const int32_t *c_dev, __nv_bfloat16 *d_pre,
+                          int32_t *status, cudaStream_t stream) {
+    if (h % 8 != 0) return MOE_ERR_INVALID_ARG;
+    const int64_t n = (int64_t)e * c_max * (h / 8);
+    int64_t blocks = (n + AB_THREADS - 1) / AB_THREADS;
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+    if (blocks < 1) blocks = 1;
+    return launch_pdl(act_bwd_kernel, dim3((unsigned)blocks), dim3(AB_THREADS), 0, stream, pa, pb,
+                      d_hid, (int)act, e, c_max, h, counts, c_dev, d_pre, status);
+}
+
+moe_status colsum_launch(const __nv_bfloat16 *src, int e, int64_t c_max, int cols,
+                         int64_t src_pitch, const int32_t *counts, const int32_t *c_dev,
+                         __nv_bfloat16 *out, int32_t *status, cudaStream_t stream) {
+    if (e < 1 || e > 65535 || cols < 1) return MOE_ERR_INVALID_ARG;
+    return launch_pdl(colsum_kernel, dim3((unsigned)((cols + 31) / 32), (unsigned)e),
+                      dim3(CS_WARPS * 32), 0, stream, src, c_max, cols, src_pitch, counts, c_dev,
+                      out, status);
+}
+
+moe_status fill_i32_launch(int32_t *p, int n, int32_t v, cudaStream_t stream) {
+    if (n < 1) return MOE_OK;
+    return launch_pdl(fill_i32_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, stream, p,
+                      n, v);
+}
+
+}  // namespace moe

@@ -29,6 +29,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "ffn_bwd.cuh"
 
 namespace moe {
 namespace {
@@ -1023,6 +1024,142 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
     if (r != MOE_OK) return r;
     GemmArgs g2{counts, c_dev, st, (const __nv_bfloat16 *)b2, (__nv_bfloat16 *)out, c_max, e, h, m, m};
     return launch_gemm<EPI_BIAS, TM2, BK2, CL2, TN2>(mA2, mB2, mB2, mO2, g2, stream);
+}
+
+
+// ---------------------------------------------------------------- backward
+// The expert-FFN backward as bias-epilogue products on the fc2 tiling (the
+// kernel computes out[j] = A[j] B[j]^T over the kept rows of A[j], both
+// operands K-major), with SIMT transposes, activation derivative and bias
+// sums in between:
+//   pre = buf w1^T + b1 (SwiGLU: a = buf w1^T, b = buf w3^T), recomputed;
+//   d_hid = d_out w2                  (B = w2 transposed to [e, h, m]);
+//   d_pre = d_hid * act'(pre)         (SwiGLU: [d_a | d_b]);
+//   d_buf = d_pre w1 (+ d_b w3)       (B = [w1^T | w3^T] [e, m, h or 2h]);
+//   d_w2 = d_out^T hid, d_w1 = d_pre^T buf (d_w3 = d_b^T buf): the kept rows
+//   are the contraction, so A and B are the transposed activations
+//   [e, features, Kp], zero past each expert's kept rows;
+//   d_b1, d_b2: column sums of d_pre, d_out over the kept rows.
+namespace {
+
+constexpr int64_t up256i(int64_t b) { return (b + 255) & ~(int64_t)255; }
+
+struct BwdLayout {
+    int64_t pa, pb, dh, dpre, wT, w2T, doT, hidT, dpT, bufT, ints, total;
+};
+
+BwdLayout bwd_layout(moe_act act, int e, int64_t c_max, int m, int h) {
+    const bool swiglu = act == MOE_ACT_SWIGLU;
+    const int64_t E = e, H2 = swiglu ? 2 * (int64_t)h : h, Kp = (c_max + 7) / 8 * 8;
+    BwdLayout L{};
+    int64_t o = 0;
+    auto take = [&](int64_t bytes) { const int64_t at = o; o += up256i(bytes); return at; };
+    L.pa = take(E * c_max * h * 2);
+    L.pb = take(swiglu ? E * c_max * h * 2 : 0);
+    L.dh = take(E * c_max * h * 2);
+    L.dpre = take(E * c_max * H2 * 2);
+    L.wT = take(E * m * H2 * 2);
+    L.w2T = take(E * h * m * 2);
+    L.doT = take(E * m * Kp * 2);
+    L.hidT = take(E * h * Kp * 2);
+    L.dpT = take((swiglu ? 2 : 1) * E * h * Kp * 2);
+    L.bufT = take(E * m * Kp * 2);
+    L.ints = take((2 * E + 2) * 4);
+    L.total = o;
+    return L;
+}
+
+// out[j] = A[j] B[j]^T (+ bias[j]) over the rows min(counts[j], *c_dev, c_max)
+// of every expert j: A [e * c_max, K], B [e * b_rows, K], out [e, c_max, n_out].
+moe_status gemm_bias(const void *a, const void *b, int b_rows, void *out, const void *bias,
+                     const int32_t *counts, const int32_t *c_dev, int e, int64_t c_max, int K,
+                     int n_out, int32_t *st, cudaStream_t stream) {
+    using T2 = Tiling<1, 64, 2, 2>;
+    CUtensorMap mA, mB, mO;
+    if (!make_map(&mA, a, (uint64_t)e * c_max, (uint64_t)K, T2::A_BOX_ROWS, 64) ||
+        !make_map(&mB, b, (uint64_t)e * b_rows, (uint64_t)K, T2::B_BOX_ROWS, 64) ||
+        !make_map(&mO, out, (uint64_t)e * c_max, (uint64_t)n_out, 32, 32))
+        return MOE_ERR_CUDA;
+    GemmArgs g{counts, c_dev, st, (const __nv_bfloat16 *)bias, (__nv_bfloat16 *)out, c_max, e, K,
+               n_out, b_rows};
+    return launch_gemm<EPI_BIAS, 1, 64, 2, 2>(mA, mB, mB, mO, g, stream);
+}
+
+}  // namespace
+
+size_t ffn_tc_bwd_workspace_bytes(moe_act act, int e, int64_t c_max, int m, int h) {
+    return (size_t)bwd_layout(act, e, c_max, m, h).total;
+}
+
+moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *counts,
+                             const int32_t *c_dev, const void *w1, const void *b1, const void *w3,
+                             const void *w2, moe_act act, int e, int64_t c_max, int m, int h,
+                             const void *d_out, void *ws, void *d_buf, void *d_w1, void *d_w3,
+                             void *d_w2, void *d_b1, void *d_b2, int32_t *st, cudaStream_t stream) {
+    using bf = __nv_bfloat16;
+    const bool swiglu = act == MOE_ACT_SWIGLU;
+    const BwdLayout L = bwd_layout(act, e, c_max, m, h);
+    const int64_t E = e, H2 = swiglu ? 2 * (int64_t)h : h, Kp = (c_max + 7) / 8 * 8;
+    if (Kp > 0x7fffffff || H2 > 0x7fffffff) return MOE_ERR_UNSUPPORTED;
+    char *w = (char *)ws;
+    bf *pa = (bf *)(w + L.pa), *pb = (bf *)(w + L.pb), *dh = (bf *)(w + L.dh);
+    bf *dpre = (bf *)(w + L.dpre), *wT = (bf *)(w + L.wT), *w2T = (bf *)(w + L.w2T);
+    bf *doT = (bf *)(w + L.doT), *hidT = (bf *)(w + L.hidT), *dpT = (bf *)(w + L.dpT);
+    bf *bufT = (bf *)(w + L.bufT);
+    int32_t *cnt_m = (int32_t *)(w + L.ints), *cnt_h = cnt_m + e, *cdev_m = cnt_h + e,
+            *cdev_h = cdev_m + 1;
+    moe_status r;
+#define MOE_TRY(x) \
+    do {           \
+        r = (x);   \
+        if (r != MOE_OK) return r; \
+    } while (0)
+    // row counts of the weight-gradient products: every feature row is kept
+    MOE_TRY(fill_i32_launch(cnt_m, e, m, stream));
+    MOE_TRY(fill_i32_launch(cnt_h, e, h, stream));
+    MOE_TRY(fill_i32_launch(cdev_m, 1, m, stream));
+    MOE_TRY(fill_i32_launch(cdev_h, 1, h, stream));
+    // weights as K-major B operands of the data-gradient products
+    MOE_TRY(transpose_pad_launch((const bf *)w2, (int64_t)m * h, h, w2T, (int64_t)h * m, m, e, m, h,
+                                 m, nullptr, nullptr, st, stream));
+    MOE_TRY(transpose_pad_launch((const bf *)w1, (int64_t)h * m, m, wT, (int64_t)m * H2, H2, e, h, m,
+                                 h, nullptr, nullptr, st, stream));
+    if (swiglu)
+        MOE_TRY(transpose_pad_launch((const bf *)w3, (int64_t)h * m, m, wT + h, (int64_t)m * H2, H2,
+                                     e, h, m, h, nullptr, nullptr, st, stream));
+    // pre-activations, recomputed; then d_hid, d_pre, d_buf
+    MOE_TRY(gemm_bias(buf, w1, h, pa, swiglu ? nullptr : b1, counts, c_dev, e, c_max, m, h, st,
+                      stream));
+    if (swiglu) MOE_TRY(gemm_bias(buf, w3, h, pb, nullptr, counts, c_dev, e, c_max, m, h, st, stream));
+    MOE_TRY(gemm_bias(d_out, w2T, h, dh, nullptr, counts, c_dev, e, c_max, m, h, st, stream));
+    MOE_TRY(act_bwd_launch(pa, swiglu ? pb : nullptr, dh, act, e, c_max, h, counts, c_dev, dpre, st,
+                           stream));
+    MOE_TRY(gemm_bias(dpre, wT, m, d_buf, nullptr, counts, c_dev, e, c_max, (int)H2, m, st, stream));
+    // weight gradients: the kept rows are the contraction
+    MOE_TRY(transpose_pad_launch((const bf *)d_out, c_max * m, m, doT, (int64_t)m * Kp, Kp, e,
+                                 (int)c_max, m, (int)Kp, counts, c_dev, st, stream));
+    MOE_TRY(transpose_pad_launch((const bf *)hid, c_max * h, h, hidT, (int64_t)h * Kp, Kp, e,
+                                 (int)c_max, h, (int)Kp, counts, c_dev, st, stream));
+    MOE_TRY(transpose_pad_launch((const bf *)buf, c_max * m, m, bufT, (int64_t)m * Kp, Kp, e,
+                                 (int)c_max, m, (int)Kp, counts, c_dev, st, stream));
+    MOE_TRY(transpose_pad_launch(dpre, c_max * H2, H2, dpT, (int64_t)h * Kp, Kp, e, (int)c_max, h,
+                                 (int)Kp, counts, c_dev, st, stream));
+    if (swiglu)
+        MOE_TRY(transpose_pad_launch(dpre + h, c_max * H2, H2, dpT + E * h * Kp, (int64_t)h * Kp, Kp,
+                                     e, (int)c_max, h, (int)Kp, counts, c_dev, st, stream));
+    MOE_TRY(gemm_bias(doT, hidT, h, d_w2, nullptr, cnt_m, cdev_m, e, m, (int)Kp, h, st, stream));
+    MOE_TRY(gemm_bias(dpT, bufT, m, d_w1, nullptr, cnt_h, cdev_h, e, h, (int)Kp, m, st, stream));
+    if (swiglu)
+        MOE_TRY(gemm_bias(dpT + E * h * Kp, bufT, m, d_w3, nullptr, cnt_h, cdev_h, e, h, (int)Kp, m,
+                          st, stream));
+    // bias gradients (ReLU / GELU experts)
+    if (!swiglu && d_b1)
+        MOE_TRY(colsum_launch(dpre, e, c_max, h, h, counts, c_dev, (bf *)d_b1, st, stream));
+    if (!swiglu && d_b2)
+        MOE_TRY(colsum_launch((const bf *)d_out, e, c_max, m, m, counts, c_dev, (bf *)d_b2, st,
+                              stream));
+#undef MOE_TRY
+    return MOE_OK;
 }
 
 }  // namespace moe

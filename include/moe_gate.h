@@ -223,6 +223,38 @@ moe_status moe_encode_bwd(const void *d_buf, moe_dtype dt, const int32_t *idx,
                           const int32_t *loc, const int32_t *c_dev, int64_t s, int m, int e,
                           int k, int64_t c_max, void *dx, int32_t *dev_status, void *stream);
 
+/* Bytes of device workspace moe_expert_ffn_bwd needs (0 if unsupported). */
+size_t moe_expert_ffn_bwd_workspace_size(moe_dtype dt, moe_act act, int e, int64_t c_max, int m,
+                                         int h);
+
+/*
+ * Per-expert FFN backward (the gradient of moe_expert_ffn; the pages give
+ * only the forward experts 'ffn' of [Tutel]).  For L = sum over kept rows of
+ * <d_out, out>, with every kept row i < min(counts[j], c) of expert j:
+ *   pre = buf W1^T + b1 (recomputed), d_hid = d_out W2,
+ *   d_pre = d_hid * act'(pre)   (SwiGLU: d_a = d_hid * b * silu'(a),
+ *                                d_b = d_hid * silu(a), a = buf W1^T, b = buf W3^T),
+ *   d_buf = d_pre W1 (+ d_b W3), d_w2 = d_out^T hid, d_b2 = sum d_out,
+ *   d_w1 = d_pre^T buf (d_a for SwiGLU), d_w3 = d_b^T buf, d_b1 = sum d_pre.
+ * Inputs: buf [e, c_max, m] and hid [e, c_max, h] as moe_expert_ffn read and
+ * wrote them (hid is its workspace after the call); w1, w3 [e, h, m];
+ * w2 [e, m, h]; b1 [e, h] or NULL; d_out [e, c_max, m]; counts, c_dev as for
+ * the forward.  Outputs in `dt`: d_buf [e, c_max, m] (rows past the kept
+ * count not written), d_w1, d_w3 [e, h, m], d_w2 [e, m, h], d_b1 [e, h],
+ * d_b2 [e, m].  d_w3 is SwiGLU's only, which takes no biases; d_b1 / d_b2 may
+ * be NULL.  workspace: moe_expert_ffn_bwd_workspace_size() bytes, scratch.
+ * bf16 only (MOE_ERR_UNSUPPORTED for fp32): every product is the forward's
+ * tensor-core grouped GEMM (fp32 accumulation in TMEM); pre-activations and
+ * intermediate gradients are rounded to bf16 between the products.
+ */
+moe_status moe_expert_ffn_bwd(const void *buf, const void *hid, moe_dtype dt,
+                              const int32_t *counts, const int32_t *c_dev, const void *w1,
+                              const void *b1, const void *w3, const void *w2, moe_act act, int e,
+                              int64_t c_max, int m, int h, const void *d_out, void *workspace,
+                              size_t workspace_bytes, void *d_buf, void *d_w1, void *d_w3,
+                              void *d_w2, void *d_b1, void *d_b2, int32_t *dev_status,
+                              void *stream);
+
 /*
  * Gate backward ([Tutel] gate_type 'top': the gates are softmax probabilities
  * of the k selected experts, renormalised over them with

@@ -125,4 +125,20 @@ def test_invalid_arguments_are_rejected_before_launch():
     # d_buf, dt, idx, loc, c_dev, s, m, e, k, c_max, dx, status
     assert ebwd(A, M.MOE_BF16, A, A, A, 10, 64, 4, 5, 8, A, A, None) == INV      # k > e
     assert ebwd(A, M.MOE_BF16, A, A, A, 10, 64, 4, 1, 8, odd, A, None) == INV    # misaligned dx
+    fb = lib.moe_expert_ffn_bwd
+    # buf, hid, dt, counts, c_dev, w1, b1, w3, w2, act, e, c_max, m, h, d_out, ws, ws_bytes,
+    # d_buf, d_w1, d_w3, d_w2, d_b1, d_b2, status, stream
+    fok = [A, B, M.MOE_BF16, A, A, A, None, None, B, 1, 4, 64, 64, 128, A, B, 1 << 40, A, B, None,
+           A, None, None, A, None]
+    def fbc(**kw):
+        a = list(fok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return fb(*a)
+    assert fbc(a2=M.MOE_F32) == M.MOE_ERR_UNSUPPORTED           # bf16 only
+    assert fbc(a9=2) == INV                                      # SwiGLU needs w3 and d_w3
+    assert fbc(a9=2, a7=A, a19=B, a6=A) == INV                   # ... and takes no bias
+    assert fbc(a16=0) == INV                                     # workspace too small
+    assert fbc(a13=100) == INV                                   # h not a multiple of 8
+    assert fbc(a1=odd) == INV and fbc(a17=odd) == INV            # misaligned hid / d_buf
     assert M.launch_count() == before

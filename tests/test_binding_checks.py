@@ -137,7 +137,11 @@ def test_well_formed_calls_pass_and_marshal_their_sizes(stub):
                    d_x=z(s, m))
     M.moe_layer_forward(x, wg, gb, w1, b1, None, w2, b2, "gelu", k, 1.25, 1, idx, gates, loc,
                         counts, c_dev, buf, out, z(s, m, dtype=bf), ws, st)
+    M.moe_expert_ffn_bwd(buf, z(e, c_max, h, dtype=bf), counts, c_dev, w1, b1, None, w2, "gelu",
+                         z(e, c_max, m, dtype=bf), ws, z(e, c_max, m, dtype=bf), z(e, h, m, dtype=bf),
+                         None, z(e, m, h, dtype=bf), z(e, h, dtype=bf), z(e, m, dtype=bf), st)
     c = stub.calls
+    assert c["moe_expert_ffn_bwd"][10:14] == (e, c_max, m, h)
     assert c["moe_gate_topk"][4:8] == (s, m, e, k)
     assert c["moe_capacity_locations"][1:4] == (s, e, k)
     assert c["moe_encode"][6:11] == (s, m, e, k, c_max)

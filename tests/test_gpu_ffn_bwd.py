@@ -1,0 +1,140 @@
+"""GPU expert-FFN backward against the oracle (through the C ABI).
+
+The forward runs on the device first (its workspace is the hidden the
+backward reads); the oracle's backward takes the same buf, weights and d_out.
+
+Tolerance, from the arithmetic: the device rounds the recomputed
+pre-activation, d_hid and d_pre to bf16 between its fp32-accumulated products
+(relative 2^-9 each), evaluates the activation derivative at the rounded
+pre-activation (|act''| <= 0.8 for GELU; SiLU's terms bounded likewise), reads
+the hidden its own forward rounded, and rounds every output to bf16 once.  So
+each d_pre (d_a, d_b) element may be off by E = 2^-7 (|d_pre| + |d_hid| |pre|)
+(SwiGLU: 2^-7 |d_hid| |b| (1 + |a|) and 2^-7 |d_hid| |a|), and an output
+built from it by at most the same product taken over E and absolute values,
+plus half a bf16 step of the value; d_w2 by 2^-8 of |d_out|^T |hid|.  The
+intermediates are evaluated in fp64 from the same inputs for this bound only;
+the expected values are the oracle's.
+
+Not yet run on a GB300: the test is collected with the GPU tests but skipped
+unless MOE_FFN_BWD_GPU=1.
+"""
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import combine_moe_gate_gb300 as M
+import oracle
+import synth
+from synth.workloads import Workload
+
+from gpu_util import to_dev, to_host
+
+pytestmark = [
+    pytest.mark.gpu,
+    pytest.mark.skipif(os.environ.get("MOE_FFN_BWD_GPU") != "1",
+                       reason="FFN backward: not yet run on a GB300 (set MOE_FFN_BWD_GPU=1)"),
+]
+
+
+def _w(**kw):
+    kw.setdefault("name", "ffnbwd")
+    return Workload(**kw)
+
+
+CASES = [
+    _w(s=300, m=64, e=3, k=2, h=128, act="gelu", capacity_factor=0.0),
+    _w(s=333, m=128, e=4, k=2, h=256, act="relu", capacity_factor=1.25),
+    _w(s=300, m=192, e=5, k=2, h=320, act="swiglu", capacity_factor=0.0, skew_alpha=1.0),
+    _w(s=600, m=200, e=3, k=2, h=136, act="gelu", capacity_factor=0.0),
+]
+
+
+def _f64(a):
+    return oracle.to_f32(a).astype(np.float64)
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: f"e{w.e}_m{w.m}_h{w.h}_{w.act}")
+def test_expert_ffn_bwd_matches_oracle(w):
+    inp = synth.make_inputs_host(w)
+    ref = oracle.layer_forward(w, inp)
+    c, e, m, h = ref["c"], w.e, w.m, w.h
+    c_max = c + 3
+    kept = ref["kept"].astype(np.int64)
+    buf_h = np.zeros((e, c_max, m), np.float32)
+    buf_h[:, :c] = ref["buf"][:, :c]
+    d_out_h = synth.bf16_bits_to_f32(synth.normal_host(5, "d_out", (e, c_max, m), 1.0, "bf16"))
+    swiglu = w.act == "swiglu"
+    bf = torch.bfloat16
+    buf = to_dev(buf_h).to(bf)
+    counts = to_dev(ref["needed"].astype(np.int32))
+    c_dev = to_dev(np.array([c], np.int32))
+    w1, w3, w2 = to_dev(inp["w1"]), to_dev(inp["w3"]), to_dev(inp["w2"])
+    b1, b2 = to_dev(inp["b1"]), to_dev(inp["b2"])
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # forward: its workspace holds the hidden the backward reads
+    ws_f = torch.empty(M.moe_expert_ffn_workspace_size(M.MOE_BF16, w.act, e, c_max, m, h),
+                       dtype=torch.uint8, device="cuda")
+    out = torch.empty((e, c_max, m), dtype=bf, device="cuda")
+    M.moe_expert_ffn(buf, counts, c_dev, w1, b1, w3, w2, b2, w.act, ws_f, out, st)
+    hid = ws_f[: e * c_max * h * 2].view(bf).view(e, c_max, h)
+    ws = torch.empty(M.moe_expert_ffn_bwd_workspace_size(M.MOE_BF16, w.act, e, c_max, m, h),
+                     dtype=torch.uint8, device="cuda")
+    d_buf = torch.full((e, c_max, m), 3.0, dtype=bf, device="cuda")
+    d_w1 = torch.empty((e, h, m), dtype=bf, device="cuda")
+    d_w3 = torch.empty((e, h, m), dtype=bf, device="cuda") if swiglu else None
+    d_w2 = torch.empty((e, m, h), dtype=bf, device="cuda")
+    d_b1 = None if swiglu else torch.empty((e, h), dtype=bf, device="cuda")
+    d_b2 = None if swiglu else torch.empty((e, m), dtype=bf, device="cuda")
+    M.moe_expert_ffn_bwd(buf, hid, counts, c_dev, w1, b1, w3, w2, w.act, to_dev(d_out_h).to(bf), ws,
+                         d_buf, d_w1, d_w3, d_w2, d_b1, d_b2, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+
+    want = oracle.ffn_bwd(buf_h, inp["w1"], inp["b1"], inp["w3"], inp["w2"], w.act, kept, d_out_h,
+                          True)
+
+    # error bounds (fp64 intermediates from the same inputs)
+    W1, W2 = _f64(inp["w1"]), _f64(inp["w2"])
+    W3 = _f64(inp["w3"]) if swiglu else None
+    b1f = None if inp["b1"] is None else _f64(inp["b1"])
+    u = 2.0 ** -7
+    for j in range(e):
+        r = int(kept[j])
+        x = buf_h[j, :r].astype(np.float64)
+        g = d_out_h[j, :r].astype(np.float64)
+        dh = g @ W2[j]                                                   # [r, h]
+        a = x @ W1[j].T
+        if swiglu:
+            b = x @ W3[j].T
+            sg = 1.0 / (1.0 + np.exp(-a))
+            hid_abs = np.abs(a * sg * b)
+            ea = u * np.abs(dh) * np.abs(b) * (1.0 + np.abs(a))
+            eb = u * np.abs(dh) * np.abs(a)
+            e_buf = ea @ np.abs(W1[j]) + eb @ np.abs(W3[j])
+        else:
+            pre = a + (b1f[j] if b1f is not None else 0.0)
+            if w.act == "relu":
+                dact, hid_abs = (pre > 0).astype(np.float64), np.maximum(pre, 0.0)
+            else:
+                cdf = 0.5 * (1.0 + np.vectorize(__import__("math").erf)(pre / np.sqrt(2.0)))
+                dact = cdf + pre * np.exp(-0.5 * pre * pre) / np.sqrt(2.0 * np.pi)
+                hid_abs = np.abs(pre * cdf)
+            ea = u * (np.abs(dh * dact) + np.abs(dh) * np.abs(pre))
+            e_buf = ea @ np.abs(W1[j])
+
+        def check(got, ref_v, err, name):
+            tol = 1.5 * err + 2.0 ** -8 * np.abs(ref_v) + 1e-6
+            assert np.all(np.abs(got - ref_v) <= tol), (name, j, np.abs(got - ref_v).max())
+
+        check(to_host(d_buf)[j, :r], want["d_buf"][j, :r], e_buf, "d_buf")
+        check(to_host(d_w1)[j], want["d_w1"][j], ea.T @ np.abs(x), "d_w1")
+        check(to_host(d_w2)[j], want["d_w2"][j], 2.0 ** -8 * (np.abs(g).T @ hid_abs), "d_w2")
+        if swiglu:
+            check(to_host(d_w3)[j], want["d_w3"][j], eb.T @ np.abs(x), "d_w3")
+        else:
+            check(to_host(d_b1)[j], want["d_b1"][j], ea.sum(0), "d_b1")
+            check(to_host(d_b2)[j], want["d_b2"][j], 2.0 ** -9 * np.abs(g).sum(0), "d_b2")
+        assert np.all(to_host(d_buf)[j, r:] == 3.0)        # rows past the kept count untouched
