@@ -188,16 +188,22 @@ def cpu_baseline_dict(w, inp, target_s):
 
 def ffn_traffic_from_profile():
     """DRAM bytes per expert-FFN call from the committed ncu summary, or None when
-    the kernel source has changed since the counters were taken."""
+    the forward GEMM's source has changed since the counters were taken.  The
+    digest covers ffn_tc.cu up to the end of its first `namespace moe` block:
+    the forward kernel and its launcher (the backward's host code follows)."""
     import hashlib
 
     prof = os.path.join(ROOT, "profiles", "expert_ffn_tcgen05_bf16_e8.md")
     src = os.path.join(ROOT, "combine_moe_gate_gb300", "csrc", "ffn_tc.cu")
     try:
         text = open(prof).read()
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        data = open(src, "rb").read()
     except OSError:
         return None
+    end = data.find(b"}  // namespace moe\n")
+    if end < 0:
+        return None
+    digest = hashlib.sha256(data[:end + len(b"}  // namespace moe\n")]).hexdigest()[:16]
     fields = dict(line.split(":", 1) for line in text.splitlines() if line.startswith(
         ("source_sha256_16:", "dram_bytes_per_call:")))
     if fields.get("source_sha256_16", "").split()[0:1] != [digest]:

@@ -29,7 +29,6 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
-#include "ffn_bwd.cuh"
 
 namespace moe {
 namespace {
@@ -1026,6 +1025,13 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
     return launch_gemm<EPI_BIAS, TM2, BK2, CL2, TN2>(mA2, mB2, mB2, mO2, g2, stream);
 }
 
+}  // namespace moe
+
+// The expert-FFN backward, appended after the forward (the code above is
+// the forward GEMM unchanged).
+#include "ffn_bwd.cuh"
+
+namespace moe {
 
 // ---------------------------------------------------------------- backward
 // The expert-FFN backward as bias-epilogue products on the fc2 tiling (the
