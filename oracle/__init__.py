@@ -26,6 +26,7 @@ from .core import (  # noqa: F401
     gates,
     get_threads,
     kept_rows,
+    layer_backward,
     layer_forward,
     locations,
     round_bf16,

@@ -295,3 +295,27 @@ def layer_forward(w, inp, cmax=None, rows=None):
     if full:
         res["y"] = decode(out, idx, loc, g, c, bf16)
     return res
+
+
+def layer_backward(w, inp, fwd, dy):
+    """Backward of the layer forward for L = <dy, y>, from `fwd` =
+    layer_forward(w, inp) (full): decode backward gives d_out (the experts'
+    output gradient) and d_gates; the expert MLP backward over the kept rows
+    gives d_buf and the weight gradients; encode backward turns d_buf into the
+    copy path's d_x, and the gate backward of d_gates gives the gate path's
+    d_x, d_wg and the gate bias gradient.  d_x is the sum of the two paths (in
+    double); routing (top-k, slots, drops) is piecewise constant."""
+    bf16 = w.dtype == "bf16"
+    c = fwd["c"]
+    d_out, d_g = decode_bwd(dy, fwd["out"], fwd["idx"], fwd["loc"], fwd["gates"], c, bf16)
+    ffn = ffn_bwd(fwd["buf"], inp["w1"], inp.get("b1"), inp.get("w3"), inp["w2"], w.act,
+                  fwd["kept"], d_out, bf16)
+    dx_copy = encode_bwd(ffn["d_buf"], fwd["idx"], fwd["loc"], c, bf16)
+    gate = gate_bwd(inp["x"], inp["wg"], inp.get("bias"), fwd["idx"], d_g,
+                    w.normalize_gates and w.k >= 2)
+    res = dict(ffn)
+    res.update(d_out=d_out, d_gates=d_g, d_logits=gate["d_logits"], d_wg=gate["d_wg"],
+               d_gate_bias=gate["d_bias"],
+               d_x=dx_copy.astype(np.float64) + gate["d_x"])
+    return res
+
