@@ -57,10 +57,7 @@ enum Epi { EPI_GELU = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_BIAS = 3 };
 // (cluster of 2) computes a 256 x 256 tile with the 2-SM MMA (M = 256): each
 // CTA loads its 128 rows of A and one half of the B tile, so each SM moves the
 // TM = 2 operand bytes per FLOP while keeping two accumulators for overlap.
-// CL = 4: two such pairs compute the tiles (m, 2n) and (m, 2n+1), which share
-// their A rows: each CTA loads a quarter of the pair tile's A rows and
-// multicasts it to its counterpart in the other pair, a quarter fewer operand
-// bytes per SM again.  TN = 2 (with CL = 2, TM = 1): the pair tile is 256 x 512
+// TN = 2 (with CL = 2, TM = 1): the pair tile is 256 x 512
 // as two N = 256 MMAs sharing each A tile, one 512-column accumulator per CTA;
 // each SM then fills 48 KB of operands per 1024 MMA cycles instead of 32 KB per
 // 512 (the fill of shared memory, not L2, is what bounds the ring).
@@ -71,15 +68,14 @@ enum Epi { EPI_GELU = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_BIAS = 3 };
 template <int TM, int BK_, int CL_ = 1, int TN_ = 1>
 struct Tiling {
     static constexpr int TN = TN_;                        // N = 256 MMAs per K step (pairs)
-    static constexpr int CL = CL_;                        // CTAs per cluster: 1, 2 or 4
+    static constexpr int CL = CL_;                        // CTAs per cluster: 1 or 2
     static constexpr bool PAIR = CL > 1;                  // 2-SM MMA on CTA pairs
-    static constexpr bool QUAD = CL == 4;                 // two pairs sharing A by multicast
     static constexpr int BK = BK_;
     static constexpr int ROWB = BK * 2;                   // bytes per operand row
     static constexpr int A_ROWS = UM * TM;                // rows of A per CTA and stage
     static constexpr int B_ROWS = PAIR ? TN * BN / 2 : BN;  // rows of B per CTA and stage
     static constexpr int BMT = A_ROWS * (PAIR ? 2 : 1);   // rows of A per tile
-    static constexpr int A_BOX_ROWS = QUAD ? A_ROWS / 4 : A_ROWS / 2;  // rows of one A copy
+    static constexpr int A_BOX_ROWS = A_ROWS / 2;                    // rows of one A copy
     static constexpr int B_BOX_ROWS = B_ROWS / 2;                    // rows of one B copy
     static constexpr int A_BYTES = A_ROWS * BK * 2;
     static constexpr int B_BYTES = B_ROWS * BK * 2;
@@ -88,7 +84,7 @@ struct Tiling {
     static constexpr int NACC = TM == 1 && TN == 1 ? 2 : 1;  // accumulator buffers
     static constexpr int ACC_COLS = BN * TM * TN;         // TMEM columns per buffer
     static_assert(BK == 64 || BK == 32, "BK");
-    static_assert(CL == 1 || CL == 2 || CL == 4, "cluster size");
+    static_assert(CL == 1 || CL == 2, "cluster size");
     static_assert(!PAIR || TM == 1, "pair tiles use one M=256 MMA");
     static_assert(TN == 1 || (TN == 2 && CL == 2), "512-column tiles on plain CTA pairs");
     static_assert(STAGES >= 3 && STAGES <= 8, "stages");
@@ -308,18 +304,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-// TMA load of one box into the same shared-memory offset of every CTA in
-// `mask`; for each destination the bytes are counted on the mbarrier at
-// bar_cluster's offset in that destination's pair-leading CTA (even rank).
-__device__ __forceinline__ void tma_load_2d_mcast(void *dst, const CUtensorMap *map, int x, int y,
-                                                  uint32_t bar_cluster, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(su32(dst)),
-        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar_cluster), "h"(mask)
-        : "memory");
-}
-
 // TMA load into this CTA's shared memory whose completion is counted on an
 // mbarrier of either CTA of the pair (cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, int x, int y,
@@ -486,7 +470,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
               const GemmArgs args) {
     using TL = Tiling<TM, BK, CL, TN>;
     static_assert(TN == 1 || EPI != EPI_SWIGLU, "SwiGLU tiles pair W1 and W3 in one N = 256 MMA");
-    constexpr bool PAIR = TL::PAIR, QUAD = TL::QUAD;
+    constexpr bool PAIR = TL::PAIR;
     constexpr int STAGES = TL::STAGES, BMT = TL::BMT, A_BYTES = TL::A_BYTES;
     constexpr int B_BYTES = TL::B_BYTES, ROWB = TL::ROWB;
     __shared__ int32_t s_bad;
@@ -507,17 +491,15 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = args.e;
-    // Clusters: the even CTA of each pair issues the pair's MMAs; tiles are
-    // dealt out per cluster (with CL = 4 a tile index covers two N tiles).
+    // Pairs: the even CTA of each pair issues the pair's MMAs; tiles are
+    // dealt out per cluster.
     const uint32_t rank = PAIR ? cluster_rank() : 0;
     const uint32_t prank = rank & 1u;    // rank within the pair
-    const uint32_t cpair = rank >> 1;    // pair within a cluster of 4
     const uint32_t lead = rank & ~1u;    // the pair's MMA-issuing CTA
     const int tile0 = (int)(blockIdx.x / CL);
     const int tile_step = (int)(gridDim.x / CL);
     constexpr int NOUT_TILE = EPI == EPI_SWIGLU ? BN / 2 : BN * TN;  // output columns per tile
     const int ntn = (args.n_out + NOUT_TILE - 1) / NOUT_TILE;
-    const int ntn_t = QUAD ? (ntn + 1) / 2 : ntn;               // N entries of the tile list
     const int nk = (args.K + BK - 1) / BK;
 
     // ---- setup: per-expert row counts and tile prefix (warp 0), barriers,
@@ -529,7 +511,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             int j = base + lane;
             int rows = j < e ? min(max(args.counts[j], 0), c_eff) : 0;
             if (j < e) kept_rows[j] = rows;
-            const int own = ((rows + BMT - 1) / BMT) * ntn_t;
+            const int own = ((rows + BMT - 1) / BMT) * ntn;
             int v = own;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -546,7 +528,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             // full: one arrival (with its transaction bytes, for a pair those of
             // both CTAs) from each of the four producers of the MMA-issuing CTA
             // empty: released by the MMAs of every pair whose copies write the stage
-            for (int s = 0; s < STAGES; s++) { mbar_init(&ctl->full[s], 4); mbar_init(&ctl->empty[s], QUAD ? 2 : 1); }
+            for (int s = 0; s < STAGES; s++) { mbar_init(&ctl->full[s], 4); mbar_init(&ctl->empty[s], 1); }
             for (int a = 0; a < 2; a++) {
                 mbar_init(&ctl->tfull[a], 1);
                 mbar_init(&ctl->tempty[a], PAIR ? 2 * EPI_WARPS : EPI_WARPS);
@@ -592,24 +574,19 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         // halves of each stage's A tile, 1/3 those of its B tile (lane 0 of each
         // issues).  In a pair both CTAs load their own halves; the copies
         // complete on the pair-leading CTA's full barriers, whose producers
-        // announce the bytes of both.  With CL = 4 the A copies are multicast to
-        // the same rank of the other pair, which loads the other half of them.
+        // announce the bytes of both.
         const int prod = warp == 0 ? 0 : warp - PROD_WARP0 + 1;
         const bool is_a = (prod & 1) == 0;
         const int hh = prod >> 1;   // row half of this producer's boxes
         constexpr int A_BOX_BYTES = TL::A_BOX_ROWS * ROWB, B_BOX_BYTES = TL::B_BOX_ROWS * ROWB;
-        // bytes one producer's copies put into each CTA of its pair per stage
-        constexpr int MY_BYTES_ONE = QUAD ? 2 * A_BOX_BYTES : A_BOX_BYTES;
         int stage = 0;
         uint32_t phase = 0;
         int issued = 0;
         for (int t = tile0; t < total; t += tile_step) {
             Tile T = decode_tile(ctl->tile_start, e, t, BMT, kept_rows);
-            if (QUAD) T.nt = 2 * T.nt + (int)cpair;
-            // A: this CTA's 128 rows; with CL = 4 split in quarters: (pair, half)
-            const int a_sub = QUAD ? (int)cpair * 2 + hh : hh;
+            // A: this CTA's 128 rows, half of them per producer
             const int a_row = (int)((int64_t)T.j * args.c_max + (int64_t)T.mt * BMT +
-                                    (int64_t)prank * TL::A_ROWS + (int64_t)a_sub * TL::A_BOX_ROWS);
+                                    (int64_t)prank * TL::A_ROWS + (int64_t)hh * TL::A_BOX_ROWS);
             // B rows of this CTA: its half of the (each) N = 256 sub-tile; with
             // TN = 2 producer hh loads N sub-tile hh
             const int b_row = T.j * args.b_rows + T.nt * NOUT_TILE +
@@ -623,13 +600,9 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     if (ok && PAIR) {
                         const uint32_t fb = map_to_rank(su32(&ctl->full[stage]), lead);
                         if (is_a) {
-                            if (prank == 0) mbar_expect_tx(&ctl->full[stage], 2 * MY_BYTES_ONE);
-                            if (QUAD)
-                                tma_load_2d_mcast(sA + stage * A_BYTES + a_sub * A_BOX_BYTES, &tmA, kb * BK,
-                                                  a_row, fb, (uint16_t)((1u << prank) | (1u << (prank + 2))));
-                            else
-                                tma_load_2d_pair(sA + stage * A_BYTES + a_sub * A_BOX_BYTES, &tmA, kb * BK,
-                                                 a_row, fb);
+                            if (prank == 0) mbar_expect_tx(&ctl->full[stage], 2 * A_BOX_BYTES);
+                            tma_load_2d_pair(sA + stage * A_BYTES + hh * A_BOX_BYTES, &tmA, kb * BK,
+                                             a_row, fb);
                         } else {
                             // SwiGLU: the first CTA's half of B is W1, the second's W3
                             if (prank == 0) mbar_expect_tx(&ctl->full[stage], 2 * B_BOX_BYTES);
@@ -673,9 +646,8 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------------ MMA issuer
         if (!PAIR || prank == 0) {
-            // the pair's own CTAs, and every CTA whose stages its copies fill
-            const uint16_t pair_mask = (uint16_t)(3u << (2 * cpair));
-            const uint16_t stage_mask = QUAD ? (uint16_t)0xF : pair_mask;
+            // both CTAs of the pair
+            const uint16_t pair_mask = (uint16_t)3u;
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -707,7 +679,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                         }
                     }
                     // stage reusable (in both CTAs of a pair) once these MMAs read it
-                    if (PAIR) umma_commit_pair(&ctl->empty[stage], stage_mask);
+                    if (PAIR) umma_commit_pair(&ctl->empty[stage], pair_mask);
                     else umma_commit(&ctl->empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -740,7 +712,6 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         uint32_t acc_phase = 0;
         for (int t = tile0; t < total; t += tile_step) {
             Tile T = decode_tile(ctl->tile_start, e, t, BMT, kept_rows);
-            if (QUAD) T.nt = 2 * T.nt + (int)cpair;
             if (!mbar_wait<PAIR>(&ctl->tfull[acc], acc_phase, abort_flag, args.status)) break;
             tc_fence_after();
             const int row = T.mt * BMT + row_in_tile;
@@ -948,8 +919,7 @@ moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtenso
         if (dev >= 0 && dev < 64) units[dev] = nunits;
     }
     constexpr int NOUT_TILE = EPI == EPI_SWIGLU ? BN / 2 : BN * TN;
-    int64_t ntn = (args.n_out + NOUT_TILE - 1) / NOUT_TILE;
-    if (TL::QUAD) ntn = (ntn + 1) / 2;
+    const int64_t ntn = (args.n_out + NOUT_TILE - 1) / NOUT_TILE;
     int64_t upper = (int64_t)args.e * ((args.c_max + TL::BMT - 1) / TL::BMT) * ntn;
     int64_t grid = upper < nunits ? upper : nunits;
     if (grid < 1) grid = 1;
@@ -992,9 +962,7 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
                          const void *b2, moe_act act, int e, int64_t c_max, int m, int h,
                          void *hid, void *out, int32_t *st, cudaStream_t stream) {
     // fc1: 256-row tiles on CTA pairs (2-SM MMA), two accumulators per CTA so
-    // its activation epilogue overlaps the next tile's main loop (clusters of
-    // 4 sharing A by multicast move fewer L2 bytes, but only 36 such clusters
-    // fit against 76 pairs, and the shared-memory fill per SM is unchanged).
+    // its activation epilogue overlaps the next tile's main loop.
     // fc2 (bias-only epilogue, long K, about one tile per pair): 256 x 512
     // tiles on CTA pairs.
     constexpr int TM1 = 1, BK1 = 64, TM2 = 1, BK2 = 64;
