@@ -14,12 +14,7 @@ built from it by at most the same product taken over E and absolute values,
 plus half a bf16 step of the value; d_w2 by 2^-8 of |d_out|^T |hid|.  The
 intermediates are evaluated in fp64 from the same inputs for this bound only;
 the expected values are the oracle's.
-
-Not yet run on a GB300: the test is collected with the GPU tests but skipped
-unless MOE_FFN_BWD_GPU=1.
 """
-
-import os
 
 import numpy as np
 import pytest
@@ -32,11 +27,7 @@ from synth.workloads import Workload
 
 from gpu_util import to_dev, to_host
 
-pytestmark = [
-    pytest.mark.gpu,
-    pytest.mark.skipif(os.environ.get("MOE_FFN_BWD_GPU") != "1",
-                       reason="FFN backward: not yet run on a GB300 (set MOE_FFN_BWD_GPU=1)"),
-]
+pytestmark = pytest.mark.gpu
 
 
 def _w(**kw):
