@@ -6,7 +6,8 @@ tensor shapes, the current CUDA stream.  There is no fallback: if the library
 is missing, importing the entry points raises.
 
 Functions keep the C names:
-    moe_gate_topk, moe_capacity_locations, moe_encode, moe_expert_ffn,
+    moe_gate_topk, moe_capacity_locations, moe_capacity_locations_noalloc,
+    moe_encode, moe_expert_ffn,
     moe_decode, moe_decode_bwd, moe_encode_bwd, moe_layer_forward, moe_gate_bwd
 plus the size queries and `MoEError`.
 """
@@ -51,6 +52,7 @@ def load():
         "moe_capacity_bound": (I64, [F, I64, I, I]),
         "moe_capacity_workspace_size": (SZ, [I64, I, I]),
         "moe_capacity_locations": (I, [P, I64, I, I, F, I64, P, SZ, P, P, P, P, P]),
+        "moe_capacity_locations_noalloc": (I, [P, I64, I, I, F, I64, P, P, P, P, P]),
         "moe_encode": (I, [P, I, P, P, P, P, I64, I, I, I, I64, U, P, P, P]),
         "moe_expert_ffn_workspace_size": (SZ, [I, I, I, I64, I, I]),
         "moe_expert_ffn": (I, [P, I, P, P, P, P, P, P, P, I, I, I64, I, I, P, SZ, P, P, P]),
@@ -196,6 +198,19 @@ def moe_capacity_locations(idx, e, capacity_factor, c_max, workspace, loc, count
         _ptr(loc, "loc", I, (k, s)), _ptr(counts, "counts", I, (int(e),)),
         _ptr(c_dev, "c_dev", I), _ptr(dev_status, "dev_status", I), _stream(stream)),
         "moe_capacity_locations")
+
+
+def moe_capacity_locations_noalloc(idx, e, capacity_factor, c_max, loc, counts, c_dev,
+                                   dev_status, stream=None):
+    """moe_capacity_locations with its scratch in the library's fixed device
+    array (for callers that cannot allocate device memory); see the header."""
+    k, s = idx.shape
+    I = _i32()
+    _check(load().moe_capacity_locations_noalloc(
+        _ptr(idx, "idx", I), s, int(e), k, float(capacity_factor), int(c_max),
+        _ptr(loc, "loc", I, (k, s)), _ptr(counts, "counts", I, (int(e),)),
+        _ptr(c_dev, "c_dev", I), _ptr(dev_status, "dev_status", I), _stream(stream)),
+        "moe_capacity_locations_noalloc")
 
 
 def moe_encode(x, idx, loc, counts, c_dev, buf, dev_status, flags=0, stream=None):

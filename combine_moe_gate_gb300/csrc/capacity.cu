@@ -16,7 +16,10 @@
 //      __match_any_sync groups equal experts and popc of the lower lanes gives
 //      the rank), then adds the per-warp prefix.  CTA 0 also forms counts[],
 //      the capacity c and the overflow check.
+#include <cuda.h>
+
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 
@@ -292,24 +295,60 @@ static __device__ __align__(256) int32_t g_cap_scratch[NOALLOC_SCRATCH_BYTES / s
 
 namespace {
 
+// Identity of the CUDA context current on this thread (cuCtxGetId: unique for
+// the life of the process, so a context created after cudaDeviceReset gets a
+// new one).  The driver entry points are fetched through the runtime; false
+// if either is unavailable or no context is current.
+bool current_context_id(unsigned long long *id) {
+    using GetCurrent = CUresult (*)(CUcontext *);
+    using GetId = CUresult (*)(CUcontext, unsigned long long *);
+    static const auto fns = [] {
+        void *a = nullptr, *b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault,
+                                             &qa) != cudaSuccess ||
+            qa != cudaDriverEntryPointSuccess)
+            a = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) !=
+                cudaSuccess ||
+            qb != cudaDriverEntryPointSuccess)
+            b = nullptr;
+        cudaGetLastError();
+        return std::make_pair(reinterpret_cast<GetCurrent>(a), reinterpret_cast<GetId>(b));
+    }();
+    CUcontext ctx = nullptr;
+    if (!fns.first || !fns.second || fns.first(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return fns.second(ctx, id) == CUDA_SUCCESS;
+}
+
 // Device address of g_cap_scratch on the current device.  In host code the
-// symbol name is only a host-side stand-in, so the address is looked up once
-// per device with that device current and cached.
+// symbol name is only a host-side stand-in, so the address is looked up with
+// the device current: once per device and context (the cache is keyed on the
+// context's identity, so a reset device, whose module is loaded again into a
+// new context, gets a fresh lookup), or on every call when the context's
+// identity cannot be read.
 int32_t *cap_scratch_on_current_device() {
     static std::mutex mu;
     static int32_t *addr[64] = {nullptr};
+    static unsigned long long ctx_of[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_cap_scratch) != cudaSuccess || p == nullptr) {
-            cudaGetLastError();
-            return nullptr;
-        }
-        addr[dev] = static_cast<int32_t *>(p);
+    unsigned long long id = 0;
+    if (addr[dev] && current_context_id(&id) && id == ctx_of[dev]) return addr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_cap_scratch) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return nullptr;
     }
-    return addr[dev];
+    // the lookup makes the device's primary context current if none was
+    if (current_context_id(&id)) {
+        addr[dev] = static_cast<int32_t *>(p);
+        ctx_of[dev] = id;
+    } else {
+        addr[dev] = nullptr;
+    }
+    return static_cast<int32_t *>(p);
 }
 
 }  // namespace

@@ -135,9 +135,10 @@ moe_status moe_capacity_locations(const int32_t *idx, int64_t s, int e, int k,
  *     on every GPU that loads the library until the process exits.  Shapes
  *     whose moe_capacity_workspace_size() exceeds it return
  *     MOE_ERR_UNSUPPORTED with nothing launched.
- *   - The first call on a device looks up the array's device address (once per
- *     device, with that device current); make that first call before any
- *     stream capture.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and keeps it for that device's CUDA context; after
+ *     cudaDeviceReset the next call looks it up again.  Make the first call on
+ *     each device (and the first after a reset) before any stream capture.
  *   - All calls share the one array: calls that overlap on the GPU (different
  *     streams without ordering between them) race and give wrong locations.
  *     Calls ordered on one stream are safe; nothing needs clearing in between.

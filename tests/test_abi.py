@@ -88,6 +88,23 @@ def test_invalid_arguments_are_rejected_before_launch():
     assert cap(A, 100, 4, 2, 1.0, 0, A, 1 << 20, A, A, A, A, None) == INV        # c_max = 0
     assert cap(A, 100, 4, 2, 1.0, 50, A, 0, A, A, A, A, None) == INV             # workspace too small
     assert cap(A, 100, 4, 2, float("nan"), 50, A, 1 << 20, A, A, A, A, None) == INV
+    # the allocation-free variant: idx, s, e, k, f, c_max, loc, counts, c_dev, status, stream
+    na = lib.moe_capacity_locations_noalloc
+    nok = (A, 100, 4, 2, 1.0, 50, A, B, A, B, None)
+    def nac(**kw):
+        a = list(nok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return na(*a)
+    assert nac(a5=0) == INV                                      # c_max < 1
+    assert nac(a5=1 << 31) == INV                                # c_max beyond int32
+    assert nac(a4=float("nan")) == INV                           # NaN capacity factor
+    assert nac(a3=5) == INV and nac(a3=0) == INV                 # k > e, k = 0
+    assert nac(a2=0) == INV and nac(a2=2000) == INV              # e = 0, e > 1024
+    assert nac(a1=0) == INV                                      # s = 0
+    for i in (0, 6, 7, 8, 9):                                    # idx, loc, counts, c_dev, status
+        assert nac(**{f"a{i}": None}) == INV
+        assert nac(**{f"a{i}": ctypes.c_void_p(0x30002)}) == INV # not 4-byte aligned
     ffn = lib.moe_expert_ffn
     # SwiGLU takes no biases and needs w3
     assert ffn(A, M.MOE_BF16, A, A, A, B, A, A, None, 2, 4, 64, 64, 64, A, 1 << 30, A, A, None) == INV

@@ -86,6 +86,11 @@ def test_backward_and_layer_entry_points_check_their_outputs(host_as_device):
         M.moe_expert_ffn(out, counts, c_dev, torch.zeros((e, h, m), **bf), None, None,
                          torch.zeros((e, h, m), **bf), None, "gelu", torch.zeros(16, dtype=torch.uint8),
                          torch.zeros((e, c_max, m), **bf), st)
+    with pytest.raises(ValueError, match="counts: shape"):
+        M.moe_capacity_locations_noalloc(idx, e, 1.0, c_max, loc, torch.zeros(e + 1, **i32), c_dev,
+                                         st)
+    with pytest.raises(TypeError, match="loc: dtype"):
+        M.moe_capacity_locations_noalloc(idx, e, 1.0, c_max, torch.zeros((k, s)), counts, c_dev, st)
     with pytest.raises(TypeError, match="b1: dtype"):
         M.moe_layer_forward(torch.zeros((s, m), **bf), torch.zeros((m, e)), None,
                             torch.zeros((e, h, m), **bf), torch.zeros((e, h)), None,
@@ -127,6 +132,7 @@ def test_well_formed_calls_pass_and_marshal_their_sizes(stub):
     ws = z(4096, dtype=torch.uint8)
     M.moe_gate_topk(x, wg, gb, k, idx, gates, st, flags=1)
     M.moe_capacity_locations(idx, e, 1.25, c_max, ws, loc, counts, c_dev, st)
+    M.moe_capacity_locations_noalloc(idx, e, 1.25, c_max, loc, counts, c_dev, st)
     M.moe_encode(x, idx, loc, counts, c_dev, buf, st)
     M.moe_expert_ffn(buf, counts, c_dev, w1, b1, None, w2, b2, "gelu", ws, out, st)
     M.moe_decode(out, idx, loc, gates, c_dev, z(s, m, dtype=bf), st)
@@ -144,6 +150,8 @@ def test_well_formed_calls_pass_and_marshal_their_sizes(stub):
     assert c["moe_expert_ffn_bwd"][10:14] == (e, c_max, m, h)
     assert c["moe_gate_topk"][4:8] == (s, m, e, k)
     assert c["moe_capacity_locations"][1:4] == (s, e, k)
+    assert c["moe_capacity_locations_noalloc"][1:4] == (s, e, k)
+    assert c["moe_capacity_locations_noalloc"][5] == c_max
     assert c["moe_encode"][6:11] == (s, m, e, k, c_max)
     assert c["moe_expert_ffn"][10:14] == (e, c_max, m, h)
     assert c["moe_decode"][6:11] == (s, m, e, k, c_max)
