@@ -458,6 +458,8 @@ void orc_ffn_bwd(const float *buf, const float *w1, const float *b1, const float
         double *hid = (double *)malloc(sizeof(double) * (size_t)h);
         double *dp = (double *)malloc(sizeof(double) * (size_t)h);    /* d_pre or d_a */
         double *dq = (double *)malloc(sizeof(double) * (size_t)h);    /* d_b (SwiGLU) */
+        double *dh = (double *)malloc(sizeof(double) * (size_t)h);    /* d_hid */
+        double *dx = (double *)malloc(sizeof(double) * (size_t)m);    /* d_buf row */
         for (int64_t j = 0; j < cmax; j++) {
             const float *xr = buf + ((int64_t)ex * cmax + j) * m;
             const float *gr = d_out + ((int64_t)ex * cmax + j) * m;
@@ -495,13 +497,17 @@ void orc_ffn_bwd(const float *buf, const float *w1, const float *b1, const float
                     dq[u] = 0.0;
                 }
             }
-            /* fc2: d_hid, d_w2, d_b2 */
+            /* fc2: d_hid[u] = sum over i ascending of d_out[i] w2[i, u] (the
+             * rows of w2 are walked in order; each sum still adds its terms in
+             * ascending i), then d_w2, d_b2 */
+            for (int u = 0; u < h; u++) dh[u] = 0.0;
+            for (int i = 0; i < m; i++) {
+                const float *w2r = w2 + ((int64_t)ex * m + i) * h;
+                for (int u = 0; u < h; u++) dh[u] += (double)gr[i] * (double)w2r[u];
+            }
             for (int u = 0; u < h; u++) {
-                double dh = 0.0;
-                for (int i = 0; i < m; i++)
-                    dh += (double)gr[i] * (double)w2[((int64_t)ex * m + i) * h + u];
-                dp[u] *= dh;
-                dq[u] *= dh;
+                dp[u] *= dh[u];
+                dq[u] *= dh[u];
             }
             for (int i = 0; i < m; i++) {
                 gb2[i] += (double)gr[i];
@@ -516,14 +522,18 @@ void orc_ffn_bwd(const float *buf, const float *w1, const float *b1, const float
                 }
             }
             if (dbr) {
-                for (int i = 0; i < m; i++) {
-                    double v = 0.0;
-                    for (int u = 0; u < h; u++) {
-                        v += dp[u] * (double)w1[((int64_t)ex * h + u) * m + i];
-                        if (swiglu) v += dq[u] * (double)w3[((int64_t)ex * h + u) * m + i];
+                /* d_buf[i] = sum over u ascending of d_pre[u] w1[u, i] (+ d_b[u]
+                 * w3[u, i] after each w1 term), rows of w1 / w3 walked in order */
+                for (int i = 0; i < m; i++) dx[i] = 0.0;
+                for (int u = 0; u < h; u++) {
+                    const float *w1r = w1 + ((int64_t)ex * h + u) * m;
+                    const float *w3r = swiglu ? w3 + ((int64_t)ex * h + u) * m : NULL;
+                    for (int i = 0; i < m; i++) {
+                        dx[i] += dp[u] * (double)w1r[i];
+                        if (swiglu) dx[i] += dq[u] * (double)w3r[i];
                     }
-                    dbr[i] = round_to(v, bf16);
                 }
+                for (int i = 0; i < m; i++) dbr[i] = round_to(dx[i], bf16);
             }
         }
         for (int64_t q = 0; q < (int64_t)h * m; q++) {
@@ -536,5 +546,6 @@ void orc_ffn_bwd(const float *buf, const float *w1, const float *b1, const float
         for (int i = 0; i < m; i++)
             if (d_b2 && !swiglu) d_b2[(int64_t)ex * m + i] = (float)gb2[i];
         free(gw1); free(gw3); free(gw2); free(gb1); free(gb2); free(hid); free(dp); free(dq);
+        free(dh); free(dx);
     }
 }
