@@ -18,11 +18,13 @@ __global__ void __launch_bounds__(TP * TP_Y)
 transpose_pad_kernel(const uint16_t *__restrict__ src, int64_t src_batch, int64_t src_pitch,
                      uint16_t *__restrict__ dst, int64_t dst_batch, int64_t dst_pitch, int rows,
                      int cols, int dst_cols, const int32_t *__restrict__ counts,
-                     const int32_t *__restrict__ c_dev, int32_t *status) {
+                     const int32_t *__restrict__ skip, const int32_t *__restrict__ c_dev,
+                     int32_t *status) {
     pdl_enter();
     if (status_bad(status)) return;
     __shared__ uint32_t tile[TP][TP + 1];
     const int b = blockIdx.z;
+    if (skip && min(skip[b], *c_dev) <= 0) return;   // block-uniform
     const int r0 = blockIdx.x * TP, c0 = blockIdx.y * TP;
     int kept = rows;
     if (counts) kept = max(0, min(min(counts[b], *c_dev), rows));
@@ -126,18 +128,13 @@ colsum_kernel(const __nv_bfloat16 *__restrict__ src, int64_t c_max, int cols, in
     }
 }
 
-__global__ void fill_i32_kernel(int32_t *p, int n, int32_t v) {
-    pdl_enter();
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = v;
-}
-
 }  // namespace
 
 moe_status transpose_pad_launch(const __nv_bfloat16 *src, int64_t src_batch, int64_t src_pitch,
                                 __nv_bfloat16 *dst, int64_t dst_batch, int64_t dst_pitch,
                                 int batches, int rows, int cols, int dst_cols,
-                                const int32_t *counts, const int32_t *c_dev, int32_t *status,
-                                cudaStream_t stream) {
+                                const int32_t *counts, const int32_t *skip, const int32_t *c_dev,
+                                int32_t *status, cudaStream_t stream) {
     if (batches < 1 || batches > 65535 || rows < 0 || cols < 1 || dst_cols < rows)
         return MOE_ERR_INVALID_ARG;
     const dim3 grid((unsigned)((dst_cols + TP - 1) / TP), (unsigned)((cols + TP - 1) / TP),
@@ -145,7 +142,7 @@ moe_status transpose_pad_launch(const __nv_bfloat16 *src, int64_t src_batch, int
     if (grid.y > 65535) return MOE_ERR_UNSUPPORTED;
     return launch_pdl(transpose_pad_kernel, grid, dim3(TP, TP_Y), 0, stream,
                       (const uint16_t *)src, src_batch, src_pitch, (uint16_t *)dst, dst_batch,
-                      dst_pitch, rows, cols, dst_cols, counts, c_dev, status);
+                      dst_pitch, rows, cols, dst_cols, counts, skip, c_dev, status);
 }
 
 moe_status act_bwd_launch(const __nv_bfloat16 *pa, const __nv_bfloat16 *pb,
@@ -172,12 +169,6 @@ moe_status colsum_launch(const __nv_bfloat16 *src, int e, int64_t c_max, int col
     return launch_pdl(colsum_kernel, dim3((unsigned)((cols + 31) / 32), (unsigned)e),
                       dim3(CS_WARPS * 32), 0, stream, src, c_max, cols, src_pitch, counts, c_dev,
                       out, status);
-}
-
-moe_status fill_i32_launch(int32_t *p, int n, int32_t v, cudaStream_t stream) {
-    if (n < 1) return MOE_OK;
-    return launch_pdl(fill_i32_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, stream, p,
-                      n, v);
 }
 
 }  // namespace moe

@@ -7,13 +7,14 @@ namespace moe {
 
 // dst[b][c][r] = src[b][r][c] for r < kept_b, 0 for kept_b <= r < dst_cols,
 // over c < cols and b < batches, bf16.  kept_b = min(counts[b], *c_dev, rows)
-// when counts is given, else rows.  Row pitches are in elements; the batch
-// strides too.
+// when counts is given, else rows.  Batches b with min(skip[b], *c_dev) <= 0
+// are left untouched when skip is given.  Row pitches are in elements; the
+// batch strides too.
 moe_status transpose_pad_launch(const __nv_bfloat16 *src, int64_t src_batch, int64_t src_pitch,
                                 __nv_bfloat16 *dst, int64_t dst_batch, int64_t dst_pitch,
                                 int batches, int rows, int cols, int dst_cols,
-                                const int32_t *counts, const int32_t *c_dev, int32_t *status,
-                                cudaStream_t stream);
+                                const int32_t *counts, const int32_t *skip, const int32_t *c_dev,
+                                int32_t *status, cudaStream_t stream);
 
 // Activation backward over the kept rows of each expert, bf16 in and out:
 //   ReLU / GELU: d_pre[r, u] = d_hid[r, u] * act'(pa[r, u]);
@@ -31,8 +32,5 @@ moe_status act_bwd_launch(const __nv_bfloat16 *pa, const __nv_bfloat16 *pb,
 moe_status colsum_launch(const __nv_bfloat16 *src, int e, int64_t c_max, int cols,
                          int64_t src_pitch, const int32_t *counts, const int32_t *c_dev,
                          __nv_bfloat16 *out, int32_t *status, cudaStream_t stream);
-
-// p[i] = v for i < n.
-moe_status fill_i32_launch(int32_t *p, int n, int32_t v, cudaStream_t stream);
 
 }  // namespace moe

@@ -132,6 +132,13 @@ struct GemmArgs {
     int K;             // contraction length
     int n_out;         // output columns per expert
     int b_rows;        // rows of each B tensor map per expert
+    // Contraction per expert (weight gradients): when set, every expert has
+    // c_max output rows (counts / c_dev unused) and expert j contracts over
+    // its first min(k_counts[j], *k_cdev, K) K columns only; the operands must
+    // be zero from there to the next multiple of BK.  An expert with none
+    // gets a zero output tile and no MMA.
+    const int32_t *k_counts;
+    const int32_t *k_cdev;
 };
 
 // ------------------------------------------------------------- PTX wrappers
@@ -443,11 +450,15 @@ __device__ __forceinline__ float2 gelu_erf2(float2 a) {
 
 __device__ __forceinline__ float silu(float a) { return a / (1.0f + expf(-a)); }
 
-// Tile t -> (expert j, m-tile, n-tile); m-tile varies fastest.
-struct Tile { int j, mt, nt, rows; };
+// Tile t -> (expert j, m-tile, n-tile); m-tile varies fastest.  rows: the
+// expert's output rows; nk: its K blocks.  kept_rows[] holds the output rows
+// per expert, or (uniform_rows > 0: every expert has that many output rows)
+// the K columns per expert.
+struct Tile { int j, mt, nt, rows, nk; };
 
 __device__ __forceinline__ Tile decode_tile(const int32_t *tile_start, int e, int t, int bmt,
-                                            const int32_t *kept_rows) {
+                                            const int32_t *kept_rows, int uniform_rows,
+                                            int nk_all, int bk) {
     int lo = 0, hi = e;  // largest j with tile_start[j] <= t
     while (hi - lo > 1) {
         int mid = (lo + hi) >> 1;
@@ -456,7 +467,8 @@ __device__ __forceinline__ Tile decode_tile(const int32_t *tile_start, int e, in
     Tile T;
     T.j = lo;
     int local = t - tile_start[lo];
-    T.rows = kept_rows[lo];
+    T.rows = uniform_rows > 0 ? uniform_rows : kept_rows[lo];
+    T.nk = uniform_rows > 0 ? (kept_rows[lo] + bk - 1) / bk : nk_all;
     int mtiles = (T.rows + bmt - 1) / bmt;
     T.nt = local / mtiles;
     T.mt = local % mtiles;
@@ -501,16 +513,19 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     constexpr int NOUT_TILE = EPI == EPI_SWIGLU ? BN / 2 : BN * TN;  // output columns per tile
     const int ntn = (args.n_out + NOUT_TILE - 1) / NOUT_TILE;
     const int nk = (args.K + BK - 1) / BK;
+    const bool kmode = args.k_counts != nullptr;           // K per expert
+    const int urows = kmode ? (int)args.c_max : 0;
 
     // ---- setup: per-expert row counts and tile prefix (warp 0), barriers,
     // TMEM allocation (warp 1)
     if (warp == 0) {
-        const int c_eff = (int)min((int64_t)*args.c_dev, args.c_max);
+        const int c_eff = kmode ? 0 : (int)min((int64_t)*args.c_dev, args.c_max);
+        const int k_eff = kmode ? (int)min((int64_t)*args.k_cdev, (int64_t)args.K) : 0;
         int run = 0;
         for (int base = 0; base < e; base += 32) {
             int j = base + lane;
-            int rows = j < e ? min(max(args.counts[j], 0), c_eff) : 0;
-            if (j < e) kept_rows[j] = rows;
+            int rows = j >= e ? 0 : kmode ? urows : min(max(args.counts[j], 0), c_eff);
+            if (j < e) kept_rows[j] = kmode ? min(max(args.k_counts[j], 0), k_eff) : rows;
             const int own = ((rows + BMT - 1) / BMT) * ntn;
             int v = own;
 #pragma unroll
@@ -583,7 +598,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         uint32_t phase = 0;
         int issued = 0;
         for (int t = tile0; t < total; t += tile_step) {
-            Tile T = decode_tile(ctl->tile_start, e, t, BMT, kept_rows);
+            Tile T = decode_tile(ctl->tile_start, e, t, BMT, kept_rows, urows, nk, BK);
             // A: this CTA's 128 rows, half of them per producer
             const int a_row = (int)((int64_t)T.j * args.c_max + (int64_t)T.mt * BMT +
                                     (int64_t)prank * TL::A_ROWS + (int64_t)hh * TL::A_BOX_ROWS);
@@ -593,7 +608,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                               (TN == 2 ? hh * BN + (int)prank * (BN / 2)
                                        : (PAIR && EPI != EPI_SWIGLU ? (int)prank * TL::B_ROWS : 0) +
                                              hh * TL::B_BOX_ROWS);
-            for (int kb = 0; kb < nk; kb++) {
+            for (int kb = 0; kb < T.nk; kb++) {
                 int ok = 1;
                 if (lane == 0) {
                     ok = mbar_wait<PAIR>(&ctl->empty[stage], phase ^ 1u, abort_flag, args.status);
@@ -653,11 +668,12 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             int acc = 0;
             uint32_t acc_phase = 0;
             for (int t = tile0; t < total; t += tile_step) {
+                const int tnk = kmode ? decode_tile(ctl->tile_start, e, t, BMT, kept_rows, urows, nk, BK).nk : nk;
                 if (!mbar_wait<PAIR>(&ctl->tempty[acc], acc_phase ^ 1u, abort_flag, args.status)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(acc * TL::ACC_COLS);
                 bool ok = true;
-                for (int kb = 0; kb < nk; kb++) {
+                for (int kb = 0; kb < tnk; kb++) {
                     if (!mbar_wait<PAIR>(&ctl->full[stage], phase, abort_flag, args.status)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a0 = su32(sA + stage * A_BYTES);
@@ -684,7 +700,8 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                // accumulator ready when all MMAs finish
+                // accumulator ready when all MMAs finish (a tile without K
+                // blocks is published at once; its epilogue writes zeros)
                 if (PAIR) umma_commit_pair(&ctl->tfull[acc], pair_mask);
                 else umma_commit(&ctl->tfull[acc]);
                 if (++acc == TL::NACC) { acc = 0; acc_phase ^= 1u; }
@@ -711,7 +728,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = tile0; t < total; t += tile_step) {
-            Tile T = decode_tile(ctl->tile_start, e, t, BMT, kept_rows);
+            Tile T = decode_tile(ctl->tile_start, e, t, BMT, kept_rows, urows, nk, BK);
             if (!mbar_wait<PAIR>(&ctl->tfull[acc], acc_phase, abort_flag, args.status)) break;
             tc_fence_after();
             const int row = T.mt * BMT + row_in_tile;
@@ -729,10 +746,15 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     const int ocol = col0 + c0;               // column within the tile's output
                     const int gcol = T.nt * NOUT_TILE + ocol; // column within the expert
                     uint32_t r[32], u[32];
-                    tmem_ld32(tbase + (uint32_t)ocol, r);
-                    tmem_ld32(tbase + (uint32_t)(BN / 2 + ocol), u);
-                    tmem_wait_ld(r);
-                    tmem_tie(u);
+                    if (T.nk > 0) {
+                        tmem_ld32(tbase + (uint32_t)ocol, r);
+                        tmem_ld32(tbase + (uint32_t)(BN / 2 + ocol), u);
+                        tmem_wait_ld(r);
+                        tmem_tie(u);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; i++) r[i] = u[i] = 0u;   // empty contraction
+                    }
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; i++)
@@ -761,10 +783,15 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
 #pragma unroll 1
                 for (int c0 = 0; c0 < COLS; c0 += 64) {
                     uint32_t r[2][32];
-                    tmem_ld32(tbase + (uint32_t)(col0 + c0), r[0]);
-                    tmem_ld32(tbase + (uint32_t)(col0 + c0 + 32), r[1]);
-                    tmem_wait_ld(r[0]);
-                    tmem_tie(r[1]);
+                    if (T.nk > 0) {
+                        tmem_ld32(tbase + (uint32_t)(col0 + c0), r[0]);
+                        tmem_ld32(tbase + (uint32_t)(col0 + c0 + 32), r[1]);
+                        tmem_wait_ld(r[0]);
+                        tmem_tie(r[1]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; i++) r[0][i] = r[1][i] = 0u;   // empty contraction
+                    }
 #pragma unroll
                     for (int h2 = 0; h2 < 2; h2++) {
                         const int gcol = T.nt * NOUT_TILE + col0 + c0 + 32 * h2;
@@ -1012,14 +1039,15 @@ namespace moe {
 //   d_buf = d_pre w1 (+ d_b w3)       (B = [w1^T | w3^T] [e, m, h or 2h]);
 //   d_w2 = d_out^T hid, d_w1 = d_pre^T buf (d_w3 = d_b^T buf): the kept rows
 //   are the contraction, so A and B are the transposed activations
-//   [e, features, Kp], zero past each expert's kept rows;
+//   [e, features, Kp], zero past each expert's kept rows, and each expert
+//   contracts over its own kept rows only (an expert with none gets zeros);
 //   d_b1, d_b2: column sums of d_pre, d_out over the kept rows.
 namespace {
 
 constexpr int64_t up256i(int64_t b) { return (b + 255) & ~(int64_t)255; }
 
 struct BwdLayout {
-    int64_t pa, pb, dh, dpre, wT, w2T, doT, hidT, dpT, bufT, ints, total;
+    int64_t pa, pb, dh, dpre, wT, w2T, doT, hidT, dpT, bufT, total;
 };
 
 BwdLayout bwd_layout(moe_act act, int e, int64_t c_max, int m, int h) {
@@ -1038,16 +1066,18 @@ BwdLayout bwd_layout(moe_act act, int e, int64_t c_max, int m, int h) {
     L.hidT = take(E * h * Kp * 2);
     L.dpT = take((swiglu ? 2 : 1) * E * h * Kp * 2);
     L.bufT = take(E * m * Kp * 2);
-    L.ints = take((2 * E + 2) * 4);
     L.total = o;
     return L;
 }
 
 // out[j] = A[j] B[j]^T (+ bias[j]) over the rows min(counts[j], *c_dev, c_max)
 // of every expert j: A [e * c_max, K], B [e * b_rows, K], out [e, c_max, n_out].
+// With k_counts (weight gradients): all c_max rows of every expert, and expert
+// j contracts over its first min(k_counts[j], *k_cdev) columns of K only.
 moe_status gemm_bias(const void *a, const void *b, int b_rows, void *out, const void *bias,
                      const int32_t *counts, const int32_t *c_dev, int e, int64_t c_max, int K,
-                     int n_out, int32_t *st, cudaStream_t stream) {
+                     int n_out, int32_t *st, cudaStream_t stream,
+                     const int32_t *k_counts = nullptr, const int32_t *k_cdev = nullptr) {
     using T2 = Tiling<1, 64, 2, 2>;
     CUtensorMap mA, mB, mO;
     if (!make_map(&mA, a, (uint64_t)e * c_max, (uint64_t)K, T2::A_BOX_ROWS, 64) ||
@@ -1055,7 +1085,7 @@ moe_status gemm_bias(const void *a, const void *b, int b_rows, void *out, const 
         !make_map(&mO, out, (uint64_t)e * c_max, (uint64_t)n_out, 32, 32))
         return MOE_ERR_CUDA;
     GemmArgs g{counts, c_dev, st, (const __nv_bfloat16 *)bias, (__nv_bfloat16 *)out, c_max, e, K,
-               n_out, b_rows};
+               n_out, b_rows, k_counts, k_cdev};
     return launch_gemm<EPI_BIAS, 1, 64, 2, 2>(mA, mB, mB, mO, g, stream);
 }
 
@@ -1080,27 +1110,21 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
     bf *dpre = (bf *)(w + L.dpre), *wT = (bf *)(w + L.wT), *w2T = (bf *)(w + L.w2T);
     bf *doT = (bf *)(w + L.doT), *hidT = (bf *)(w + L.hidT), *dpT = (bf *)(w + L.dpT);
     bf *bufT = (bf *)(w + L.bufT);
-    int32_t *cnt_m = (int32_t *)(w + L.ints), *cnt_h = cnt_m + e, *cdev_m = cnt_h + e,
-            *cdev_h = cdev_m + 1;
     moe_status r;
 #define MOE_TRY(x) \
     do {           \
         r = (x);   \
         if (r != MOE_OK) return r; \
     } while (0)
-    // row counts of the weight-gradient products: every feature row is kept
-    MOE_TRY(fill_i32_launch(cnt_m, e, m, stream));
-    MOE_TRY(fill_i32_launch(cnt_h, e, h, stream));
-    MOE_TRY(fill_i32_launch(cdev_m, 1, m, stream));
-    MOE_TRY(fill_i32_launch(cdev_h, 1, h, stream));
-    // weights as K-major B operands of the data-gradient products
+    // weights as K-major B operands of the data-gradient products (experts
+    // without kept rows are skipped: no tile of theirs reads them)
     MOE_TRY(transpose_pad_launch((const bf *)w2, (int64_t)m * h, h, w2T, (int64_t)h * m, m, e, m, h,
-                                 m, nullptr, nullptr, st, stream));
+                                 m, nullptr, counts, c_dev, st, stream));
     MOE_TRY(transpose_pad_launch((const bf *)w1, (int64_t)h * m, m, wT, (int64_t)m * H2, H2, e, h, m,
-                                 h, nullptr, nullptr, st, stream));
+                                 h, nullptr, counts, c_dev, st, stream));
     if (swiglu)
         MOE_TRY(transpose_pad_launch((const bf *)w3, (int64_t)h * m, m, wT + h, (int64_t)m * H2, H2,
-                                     e, h, m, h, nullptr, nullptr, st, stream));
+                                     e, h, m, h, nullptr, counts, c_dev, st, stream));
     // pre-activations, recomputed; then d_hid, d_pre, d_buf
     MOE_TRY(gemm_bias(buf, w1, h, pa, swiglu ? nullptr : b1, counts, c_dev, e, c_max, m, h, st,
                       stream));
@@ -1109,23 +1133,27 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
     MOE_TRY(act_bwd_launch(pa, swiglu ? pb : nullptr, dh, act, e, c_max, h, counts, c_dev, dpre, st,
                            stream));
     MOE_TRY(gemm_bias(dpre, wT, m, d_buf, nullptr, counts, c_dev, e, c_max, (int)H2, m, st, stream));
-    // weight gradients: the kept rows are the contraction
+    // weight gradients: the kept rows are the contraction, each expert over
+    // its own (zero-padded to a multiple of 8 past them; the GEMM reads the
+    // padding up to its next K block, and past Kp its tensor map fills zeros)
     MOE_TRY(transpose_pad_launch((const bf *)d_out, c_max * m, m, doT, (int64_t)m * Kp, Kp, e,
-                                 (int)c_max, m, (int)Kp, counts, c_dev, st, stream));
+                                 (int)c_max, m, (int)Kp, counts, counts, c_dev, st, stream));
     MOE_TRY(transpose_pad_launch((const bf *)hid, c_max * h, h, hidT, (int64_t)h * Kp, Kp, e,
-                                 (int)c_max, h, (int)Kp, counts, c_dev, st, stream));
+                                 (int)c_max, h, (int)Kp, counts, counts, c_dev, st, stream));
     MOE_TRY(transpose_pad_launch((const bf *)buf, c_max * m, m, bufT, (int64_t)m * Kp, Kp, e,
-                                 (int)c_max, m, (int)Kp, counts, c_dev, st, stream));
+                                 (int)c_max, m, (int)Kp, counts, counts, c_dev, st, stream));
     MOE_TRY(transpose_pad_launch(dpre, c_max * H2, H2, dpT, (int64_t)h * Kp, Kp, e, (int)c_max, h,
-                                 (int)Kp, counts, c_dev, st, stream));
+                                 (int)Kp, counts, counts, c_dev, st, stream));
     if (swiglu)
         MOE_TRY(transpose_pad_launch(dpre + h, c_max * H2, H2, dpT + E * h * Kp, (int64_t)h * Kp, Kp,
-                                     e, (int)c_max, h, (int)Kp, counts, c_dev, st, stream));
-    MOE_TRY(gemm_bias(doT, hidT, h, d_w2, nullptr, cnt_m, cdev_m, e, m, (int)Kp, h, st, stream));
-    MOE_TRY(gemm_bias(dpT, bufT, m, d_w1, nullptr, cnt_h, cdev_h, e, h, (int)Kp, m, st, stream));
+                                     e, (int)c_max, h, (int)Kp, counts, counts, c_dev, st, stream));
+    MOE_TRY(gemm_bias(doT, hidT, h, d_w2, nullptr, nullptr, nullptr, e, m, (int)Kp, h, st, stream,
+                      counts, c_dev));
+    MOE_TRY(gemm_bias(dpT, bufT, m, d_w1, nullptr, nullptr, nullptr, e, h, (int)Kp, m, st, stream,
+                      counts, c_dev));
     if (swiglu)
-        MOE_TRY(gemm_bias(dpT + E * h * Kp, bufT, m, d_w3, nullptr, cnt_h, cdev_h, e, h, (int)Kp, m,
-                          st, stream));
+        MOE_TRY(gemm_bias(dpT + E * h * Kp, bufT, m, d_w3, nullptr, nullptr, nullptr, e, h, (int)Kp,
+                          m, st, stream, counts, c_dev));
     // bias gradients (ReLU / GELU experts)
     if (!swiglu && d_b1)
         MOE_TRY(colsum_launch(dpre, e, c_max, h, h, counts, c_dev, (bf *)d_b1, st, stream));
