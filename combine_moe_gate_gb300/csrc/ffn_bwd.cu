@@ -13,6 +13,7 @@ namespace {
 
 // ------------------------------------------------------------- transposes
 constexpr int TP = 32, TP_Y = 8;
+constexpr int PAD_TO = 64;   // K block of the weight-gradient GEMMs
 
 __global__ void __launch_bounds__(TP * TP_Y)
 transpose_pad_kernel(const uint16_t *__restrict__ src, int64_t src_batch, int64_t src_pitch,
@@ -28,6 +29,10 @@ transpose_pad_kernel(const uint16_t *__restrict__ src, int64_t src_batch, int64_
     const int r0 = blockIdx.x * TP, c0 = blockIdx.y * TP;
     int kept = rows;
     if (counts) kept = max(0, min(min(counts[b], *c_dev), rows));
+    // zeros are written up to the next multiple of PAD_TO past the kept rows
+    // (the consumer reads no further); block-uniform exit past that
+    const int pad_end = counts ? min(dst_cols, (kept + PAD_TO - 1) / PAD_TO * PAD_TO) : dst_cols;
+    if (r0 >= pad_end) return;
     const uint16_t *s = src + (int64_t)b * src_batch;
     uint16_t *d = dst + (int64_t)b * dst_batch;
     for (int i = threadIdx.y; i < TP; i += TP_Y) {
@@ -37,7 +42,7 @@ transpose_pad_kernel(const uint16_t *__restrict__ src, int64_t src_batch, int64_
     __syncthreads();
     for (int i = threadIdx.y; i < TP; i += TP_Y) {
         const int c = c0 + i, r = r0 + (int)threadIdx.x;
-        if (c < cols && r < dst_cols) d[(int64_t)c * dst_pitch + r] = (uint16_t)tile[threadIdx.x][i];
+        if (c < cols && r < pad_end) d[(int64_t)c * dst_pitch + r] = (uint16_t)tile[threadIdx.x][i];
     }
 }
 

@@ -7,7 +7,8 @@ namespace moe {
 
 // dst[b][c][r] = src[b][r][c] for r < kept_b, 0 for kept_b <= r < dst_cols,
 // over c < cols and b < batches, bf16.  kept_b = min(counts[b], *c_dev, rows)
-// when counts is given, else rows.  Batches b with min(skip[b], *c_dev) <= 0
+// when counts is given (then the zeros stop at the next multiple of 64 past
+// kept_b: the grouped GEMM's K blocks read no further), else rows.  Batches b with min(skip[b], *c_dev) <= 0
 // are left untouched when skip is given.  Row pitches are in elements; the
 // batch strides too.
 moe_status transpose_pad_launch(const __nv_bfloat16 *src, int64_t src_batch, int64_t src_pitch,

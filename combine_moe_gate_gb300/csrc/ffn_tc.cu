@@ -1134,8 +1134,8 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
                            stream));
     MOE_TRY(gemm_bias(dpre, wT, m, d_buf, nullptr, counts, c_dev, e, c_max, (int)H2, m, st, stream));
     // weight gradients: the kept rows are the contraction, each expert over
-    // its own (zero-padded to a multiple of 8 past them; the GEMM reads the
-    // padding up to its next K block, and past Kp its tensor map fills zeros)
+    // its own (zero-padded past them up to the GEMM's next 64-deep K block;
+    // past Kp its tensor map fills zeros)
     MOE_TRY(transpose_pad_launch((const bf *)d_out, c_max * m, m, doT, (int64_t)m * Kp, Kp, e,
                                  (int)c_max, m, (int)Kp, counts, counts, c_dev, st, stream));
     MOE_TRY(transpose_pad_launch((const bf *)hid, c_max * h, h, hidT, (int64_t)h * Kp, Kp, e,
