@@ -1,19 +1,27 @@
-"""Benchmark of the MoE layer forward hot path on GB300.
+"""Benchmark of the MoE layer hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config NAME] [--no-graded] [--no-cpu-baseline]
 
 One step = one forward pass of the whole path (gate -> capacity/locations ->
-encode -> expert FFN -> decode) over one batch of the bf16 workload
-s=4096 m=1024 e=8 k=2 h=4096 GELU, capacity_factor 1.25.  Inputs are seeded
+encode -> expert FFN -> decode) over one batch of the chosen workload.  The
+default workload is the largest one that fits a GPU: the dynamic-load sweep's
+s=65536 point with capacity factor 2 and uniform routing (m=4096, e=64, k=2,
+h=8192 GELU, c=4096, every one of the 131072 routes kept).  Inputs are seeded
 synthetic tensors already resident in HBM; L2 is flushed (256 MiB write)
-before every timed step and the flush is outside the timed interval.
+before every timed step, outside the timed interval.
 
-value       whole-job forward tokens/s (device time, CUDA events, max over ranks)
-e2e         the same metric through the one-call public API (moe_layer_forward)
-            with the step's input copied from pinned host memory and the output
-            copied back inside the timed interval
-roofline    the expert FFN (the dominant stage): algorithmic bf16 FLOPs of the
-            kept rows / its measured duration, against the measured bf16 peak
+value        whole-job forward tokens/s (device time, CUDA events, max over ranks)
+e2e          the same metric through one C call with host buffers
+             (moe_layer_forward_host: the step's x copied from pinned host
+             memory and y copied back, inside the timed interval)
+stages       every stage's time on the workload, each against its binding
+             roofline: HBM bytes for gate/encode/decode, fp32 FMA for the gate
+             where its flops outweigh its bytes, tensor-core flops and weight
+             bytes for the expert FFN
+graded       the same stage breakdown on the s=8192 e=16 layer (with its whole
+             forward + backward chain) and on the e=256 SwiGLU layer
+roofline     the expert FFN (the dominant kernel) on the headline workload
 cpu_baseline the CPU oracle timed on the host cores on a bounded token sample
 
 With --gpus N > 1 (torchrun) every rank runs an independent replica of the
@@ -36,23 +44,37 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
-from synth.workloads import BF16_E8  # noqa: E402
+from synth import workloads as W  # noqa: E402
 
 METRIC = "MoE-layer fwd tokens/s; encode/decode HBM GB/s and FFN TC util, 1×GB300"
-WORKLOAD = BF16_E8
 L2_FLUSH_BYTES = 256 << 20
 
+# name -> (workload, expert-weight seed or None for the workload's own seed)
+CONFIGS = {
+    "tiny_f32": (W.TINY_FP32, None),
+    "bf16_e8": (W.BF16_E8, None),
+    "bf16_e16": (W.BF16_E16_BWD, None),
+    "bf16_e256_swiglu": (W.BF16_E256_SWIGLU, None),
+    # sweep point p = 3*8 + 1*2 + 0: s=65536, f=2, uniform; the sweep shares weight seed 0
+    "sweep_s65536_f2": (W.sweep_points()[26], 0),
+}
+HEADLINE = "sweep_s65536_f2"
+GRADED = ("bf16_e16", "bf16_e256_swiglu")
 
-def parse():
+
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default=HEADLINE, choices=sorted(CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--no-graded", action="store_true",
+                    help="skip the stage breakdowns of the other graded workloads")
+    return ap.parse_args(argv)
 
 
 def peaks():
@@ -146,6 +168,60 @@ def job_throughput(world, tokens_per_rank, ms_step):
     return world * tokens_per_rank / (ms_step * 1e-3)
 
 
+# ------------------------------------------------------ algorithmic work
+def stage_work(w, R, t1, hit):
+    """Algorithmic bytes and flops per call of every stage, from the routing
+    actually produced: R kept routes, t1 tokens with at least one kept route,
+    `hit` experts with at least one kept row (b bytes per element)."""
+    b = 4 if w.dtype == "f32" else 2
+    s, m, e, k, h = w.s, w.m, w.e, w.k, w.h
+    nw = 3 if w.act == "swiglu" else 2                      # weight matrices per expert
+    ffn_flop = (6.0 if w.act == "swiglu" else 4.0) * R * m * h
+    return {
+        "gate": dict(bytes=s * m * b + 4 * m * e + 8 * s * k, flop=2.0 * s * m * e),
+        "capacity": dict(bytes=8 * s * k),
+        "encode": dict(bytes=t1 * m * b + R * m * b + 8 * s * k),
+        "expert_ffn": dict(flop=ffn_flop,
+                           bytes=hit * nw * m * h * b + 2 * R * m * b + 2 * R * h * b),
+        "decode": dict(bytes=R * m * b + s * m * b + 12 * s * k),
+        "decode_bwd": dict(bytes=t1 * m * b + 2 * R * m * b + 16 * s * k),
+        "encode_bwd": dict(bytes=R * m * b + s * m * b + 8 * s * k),
+        # dgrad and wgrad products, 2*R*m*h flop each: GELU/ReLU d_hid, d_buf,
+        # d_w2, d_w1; SwiGLU adds d_b's share of d_buf and d_w3
+        "ffn_bwd": dict(flop=(12.0 if w.act == "swiglu" else 8.0) * R * m * h),
+        # d_logits [s, e] written and read, x read, d_x written (fp32), wg read
+        "gate_bwd": dict(bytes=s * m * b + 4 * s * m + 8 * s * e + 4 * m * e + 12 * s * k,
+                         flop=4.0 * s * m * e),
+    }
+
+
+def rate(name, ms, work, pk):
+    """A stage's time against its binding roofline (the larger of its HBM and
+    its arithmetic time; arithmetic is tensor-core bf16 for the FFN, fp32 FMA
+    for the gate)."""
+    d = {"ms": ms}
+    sec = ms * 1e-3
+    t_hbm = t_alu = 0.0
+    if "bytes" in work:
+        gbs = work["bytes"] / sec / 1e9
+        d.update(gbs=gbs, hbm_frac=gbs / pk["hbm"])
+        t_hbm = work["bytes"] / (pk["hbm"] * 1e9)
+    if "flop" in work:
+        tf = work["flop"] / sec / 1e12
+        if name in ("expert_ffn", "ffn_bwd"):
+            d.update(tflops=tf, tc_frac=tf / pk["bf16"])
+            t_alu = work["flop"] / (pk["bf16"] * 1e12)
+        elif pk.get("fp32"):
+            d.update(fp32_tflops=tf, fp32_frac=tf / pk["fp32"])
+            t_alu = work["flop"] / (pk["fp32"] * 1e12)
+    if name == "capacity":
+        d["bound"] = "latency"
+    elif t_hbm or t_alu:
+        d["bound"] = "hbm" if t_hbm >= t_alu else ("tensor" if "tc_frac" in d else "fp32")
+        d["roofline_frac"] = max(t_hbm, t_alu) / sec
+    return d
+
+
 # ------------------------------------------------------------------ oracle
 def oracle_sample_inputs(w, inp, s_sample):
     """The first s_sample tokens of the workload's batch (same weights)."""
@@ -155,14 +231,15 @@ def oracle_sample_inputs(w, inp, s_sample):
     return ws, sub
 
 
-def time_oracle(w, inp, target_s):
+def time_oracle(w, inp, target_s, s_min=1):
     """Time the CPU oracle's full forward chain on the first s' tokens of the
-    batch, s' sized so one pass takes about target_s seconds (at most the whole
-    batch); when the whole batch is faster than that, it is repeated until
-    target_s has passed.  Returns (tokens/s, s', passes, seconds, threads)."""
+    batch (a batch of its own: capacity by the workload's rule at s'), s'
+    sized so one pass takes about target_s seconds (at least s_min, at most
+    the whole batch); when the whole batch is faster than that, it is repeated
+    until target_s has passed.  Returns (tokens/s, s', passes, seconds, threads)."""
     import oracle
 
-    s1 = min(w.s, 64)
+    s1 = min(w.s, max(s_min, 16))
     ws, sub = oracle_sample_inputs(w, inp, s1)
     t = time.perf_counter()
     oracle.layer_forward(ws, sub)
@@ -179,21 +256,47 @@ def time_oracle(w, inp, target_s):
     return passes * s2 / dt, s2, passes, dt, oracle.get_threads()
 
 
+def host_inputs(w, weight_seed, dev=None):
+    """The workload's inputs as host arrays for the oracle: drawn on the GPU
+    when one is available (the multi-GB expert weights), else on the host;
+    bf16 tensors widened to fp32 values once, here, so that the oracle's calls
+    do not convert them again."""
+    import torch
+
+    import oracle
+
+    if dev is None and torch.cuda.is_available():
+        dev = torch.device("cuda", torch.cuda.current_device())
+    if dev is not None:
+        d = synth.make_inputs_device(w, dev, weight_seed=weight_seed)
+        out = {}
+        for n, t in d.items():
+            out[n] = None if t is None else t.float().cpu().numpy()
+            d[n] = None
+        del d
+        torch.cuda.empty_cache()
+        return out
+    inp = synth.make_inputs_host(w)
+    return {n: None if a is None else oracle.to_f32(a) for n, a in inp.items()}
+
+
 def cpu_baseline_dict(w, inp, target_s):
-    v, s2, passes, dt, thr = time_oracle(w, inp, target_s)
+    v, s2, passes, dt, thr = time_oracle(w, inp, target_s, s_min=min(w.s, 256))
     return {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle",
             "sample": f"full forward chain (gate, capacity, encode, FFN, decode) on the first {s2} "
-                      f"of {w.s} tokens, same weights, {passes} pass(es): {dt:.1f} s on {thr} threads"}
+                      f"of {w.s} tokens as a batch of their own (capacity by the same rule), same "
+                      f"weights, {passes} pass(es): {dt:.1f} s on {thr} threads"}
 
 
-def ffn_traffic_from_profile():
-    """DRAM bytes per expert-FFN call from the committed ncu summary, or None when
-    the forward GEMM's source has changed since the counters were taken.  The
-    digest covers ffn_tc.cu up to the end of its first `namespace moe` block:
-    the forward kernel and its launcher (the backward's host code follows)."""
+def ffn_traffic_from_profile(workload_name):
+    """DRAM bytes per expert-FFN call on this workload from the committed ncu
+    summary, or None when there is none or the forward GEMM's source has
+    changed since its counters were taken.  The digest covers ffn_tc.cu up to
+    the end of its first `namespace moe` block: the forward kernel and its
+    launcher (the backward's host code follows)."""
     import hashlib
 
-    prof = os.path.join(ROOT, "profiles", "expert_ffn_tcgen05_bf16_e8.md")
+    prof = os.path.join(ROOT, "profiles", f"expert_ffn_tcgen05_{workload_name}.md")
     src = os.path.join(ROOT, "combine_moe_gate_gb300", "csrc", "ffn_tc.cu")
     try:
         text = open(prof).read()
@@ -212,6 +315,229 @@ def ffn_traffic_from_profile():
 
 
 # ------------------------------------------------------------------- ours
+class LayerRun:
+    """One workload's device inputs and buffers, and its timed passes."""
+
+    STAGES = ["gate", "capacity", "encode", "expert_ffn", "decode"]
+
+    def __init__(self, w, weight_seed, dev, flush):
+        import torch
+
+        import combine_moe_gate_gb300 as M
+
+        self.M, self.torch, self.w, self.dev, self.flush = M, torch, w, dev, flush
+        self.inp = synth.make_inputs_device(w, dev, weight_seed=weight_seed)
+        self.tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        self.dt = M.MOE_BF16 if w.dtype == "bf16" else M.MOE_F32
+        self.bufs = M.alloc_layer(w.s, w.m, w.e, w.k, w.h, w.act, w.capacity_factor,
+                                  dtype=self.tdt, device=dev)
+        self.flags = M.MOE_FLAG_NORMALIZE_GATES if w.normalize_gates and w.k >= 2 else 0
+        b = self.bufs
+        self.cap_ws = b.workspace[: M.moe_capacity_workspace_size(w.s, w.e, w.k)]
+        self.ffn_ws = torch.empty(M.moe_expert_ffn_workspace_size(self.dt, w.act, w.e, b.c_max, w.m,
+                                                                  w.h), dtype=torch.uint8, device=dev)
+
+    def args(self):
+        i = self.inp
+        return (i["x"], i["wg"], i["bias"], i["w1"], i["b1"], i["w3"], i["w2"], i["b2"])
+
+    def whole_step(self):
+        x, wg, gb, w1, b1, w3, w2, b2 = self.args()
+        self.M.run_layer(x, wg, gb, w1, b1, w3, w2, b2, self.w.act, self.w.k,
+                         self.w.capacity_factor, self.bufs, normalize_gates=bool(self.flags))
+
+    def staged_step(self, ev):
+        """The five C-ABI calls with an event after each stage (ev[0] before)."""
+        M, w, b = self.M, self.w, self.bufs
+        x, wg, gb, w1, b1, w3, w2, b2 = self.args()
+        ev[0].record()
+        M.moe_gate_topk(x, wg, gb, w.k, b.idx, b.gates, b.status, flags=self.flags)
+        ev[1].record()
+        M.moe_capacity_locations(b.idx, w.e, w.capacity_factor, b.c_max, self.cap_ws, b.loc,
+                                 b.counts, b.c_dev, b.status)
+        ev[2].record()
+        M.moe_encode(x, b.idx, b.loc, b.counts, b.c_dev, b.buf, b.status)
+        ev[3].record()
+        M.moe_expert_ffn(b.buf, b.counts, b.c_dev, w1, b1, w3, w2, b2, w.act, self.ffn_ws, b.out,
+                         b.status)
+        ev[4].record()
+        M.moe_decode(b.out, b.idx, b.loc, b.gates, b.c_dev, b.y, b.status)
+        ev[5].record()
+
+    def hid(self):
+        w, b = self.w, self.bufs
+        n = w.e * b.c_max * w.h
+        return self.ffn_ws[: n * (2 if w.dtype == "bf16" else 4)].view(self.tdt).view(w.e, b.c_max, w.h)
+
+    def check_status(self):
+        v = int(self.bufs.status.item())
+        if v != 0:
+            raise RuntimeError(f"{self.w.name}: device status {v} ({self.M.status_str(v)})")
+
+    def time_calls(self, fn, steps, warmup):
+        """Mean event time (ms) of fn over `steps` calls, L2 flushed before each."""
+        torch = self.torch
+        for _ in range(warmup):
+            self.flush.fill_(1)
+            fn()
+        torch.cuda.synchronize()
+        tot = 0.0
+        for _ in range(steps):
+            self.flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            tot += a.elapsed_time(b)
+        return tot / steps
+
+    def time_stages(self, steps, warmup):
+        torch = self.torch
+        mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        for _ in range(warmup):
+            self.flush.fill_(1)
+            self.staged_step(mk())
+        torch.cuda.synchronize()
+        events = []
+        for _ in range(steps):
+            self.flush.fill_(1)
+            ev = mk()
+            self.staged_step(ev)
+            events.append(ev)
+        torch.cuda.synchronize()
+        self.check_status()
+        out = {n: 0.0 for n in self.STAGES}
+        for ev in events:
+            for i, n in enumerate(self.STAGES):
+                out[n] += ev[i].elapsed_time(ev[i + 1])
+        return {n: v / steps for n, v in out.items()}
+
+    def routing_summary(self):
+        """(c, R kept routes, t1 tokens with a kept route, experts hit), read
+        back after timing."""
+        b = self.bufs
+        counts = b.counts.cpu().numpy().astype(np.int64)
+        c = int(b.c_dev.item())
+        kept = np.minimum(counts, c)
+        loc = b.loc.cpu().numpy()
+        return c, int(kept.sum()), int(((loc < c).any(0)).sum()), int((kept > 0).sum())
+
+    def backward_chain(self, steps, warmup, pk):
+        """Backward of the forward just run, timed call by call and as the whole
+        forward + backward chain: decode backward (dE, dG from dY), the expert
+        FFN backward (d_buf and the weight gradients from dE), encode backward
+        (the copy path's d_x from d_buf) and the gate backward (the gate path's
+        d_logits, d_wg, d_bias, d_x from dG).  The two d_x terms are left
+        separate (their sum is one elementwise add)."""
+        torch, M, w, b = self.torch, self.M, self.w, self.bufs
+        x, wg, gb, w1, b1, w3, w2, b2 = self.args()
+        dev, tdt = self.dev, self.tdt
+        dy = self.inp["dy"] if self.inp.get("dy") is not None else synth.normal_torch(
+            w.seed, "dy", (w.s, w.m), 1.0, w.dtype, dev)
+        d_out = torch.empty_like(b.out)
+        d_g = torch.empty((w.k, w.s), device=dev, dtype=torch.float32)
+        d_buf = torch.empty_like(b.buf)
+        dx = torch.empty((w.s, w.m), device=dev, dtype=tdt)
+        swiglu = w.act == "swiglu"
+        d_w1 = torch.empty_like(w1)
+        d_w3 = torch.empty_like(w1) if swiglu else None
+        d_w2 = torch.empty_like(w2)
+        d_b1 = None if b1 is None else torch.empty_like(b1)
+        d_b2 = None if b2 is None else torch.empty_like(b2)
+        ws = torch.empty(M.moe_expert_ffn_bwd_workspace_size(self.dt, w.act, w.e, b.c_max, w.m, w.h),
+                         dtype=torch.uint8, device=dev)
+        d_logits = torch.empty((w.s, w.e), device=dev, dtype=torch.float32)
+        d_wg = torch.empty((w.m, w.e), device=dev, dtype=torch.float32)
+        d_bias = torch.empty((w.e,), device=dev, dtype=torch.float32)
+        d_xg = torch.empty((w.s, w.m), device=dev, dtype=torch.float32)
+        hid = self.hid()
+
+        def dec():
+            M.moe_decode_bwd(dy, b.out, b.idx, b.loc, b.gates, b.counts, b.c_dev, d_out, d_g,
+                             b.status)
+
+        def ffn():
+            M.moe_expert_ffn_bwd(b.buf, hid, b.counts, b.c_dev, w1, b1, w3, w2, w.act, d_out, ws,
+                                 d_buf, d_w1, d_w3, d_w2, d_b1, d_b2, b.status)
+
+        def enc():
+            M.moe_encode_bwd(d_buf, b.idx, b.loc, b.c_dev, dx, b.status)
+
+        def gate():
+            M.moe_gate_bwd(x, wg, gb, b.idx, b.gates, d_g, d_logits, b.status, d_wg=d_wg,
+                           d_bias=d_bias, d_x=d_xg, flags=self.flags)
+
+        # the forward whose buf / hid / out the backward reads
+        self.staged_step([torch.cuda.Event() for _ in range(6)])
+
+        def chain():
+            self.staged_step([torch.cuda.Event() for _ in range(6)])
+            dec()
+            ffn()
+            enc()
+            gate()
+
+        res = {}
+        for name, fn in (("decode_bwd", dec), ("ffn_bwd", ffn), ("encode_bwd", enc),
+                         ("gate_bwd", gate)):
+            res[name] = self.time_calls(fn, steps, warmup)
+        res["fwd_bwd_step"] = self.time_calls(chain, steps, warmup)
+        self.check_status()
+        return res
+
+
+def rank_free(run):
+    del run
+    import torch
+
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def fp32_fma_peak(M, dev):
+    """Measured fp32 FMA throughput (TFLOP/s): the better of scalar and packed
+    fp32x2 fused multiply-adds over every SM, best of 5 launches."""
+    import torch
+
+    out = torch.zeros(1, dtype=torch.float32, device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks, iters = sms * 8, 8192
+    flop = blocks * 256 * iters * 32.0
+    best = {}
+    for packed in (0, 1):
+        M.moe_probe_fp32_fma(packed, blocks, 64, out)
+        torch.cuda.synchronize()
+        t = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            M.moe_probe_fp32_fma(packed, blocks, iters, out)
+            b.record()
+            b.synchronize()
+            t.append(a.elapsed_time(b))
+        best["packed" if packed else "scalar"] = flop / (min(t) * 1e-3) / 1e12
+    return best
+
+
+def graded_report(name, run, stage_ms, pk, extra=None):
+    w = run.w
+    c, R, t1, hit = run.routing_summary()
+    work = stage_work(w, R, t1, hit)
+    d = {"workload": w.name, "s": w.s, "m": w.m, "e": w.e, "k": w.k, "h": w.h, "act": w.act,
+         "capacity_factor": w.capacity_factor, "c": c, "kept_routes": R, "experts_hit": hit,
+         "layer_ms": sum(stage_ms.values()),
+         "stages": {n: rate(n, ms, work[n], pk) for n, ms in stage_ms.items()}}
+    if extra:
+        for n, ms in extra.items():
+            if n in work:
+                d["stages"][n] = dict(rate(n, ms, work[n], pk), note="backward, timed alone")
+            else:
+                d["stages"][n] = {"ms": ms, "tokens_per_s": w.s / (ms * 1e-3),
+                                  "note": "forward + decode/FFN/encode/gate backward, one chain"}
+    return d
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -219,62 +545,20 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = WORKLOAD
-    inp = synth.make_inputs_host(w)
-
-    def D(a):
-        if a is None:
-            return None
-        if a.dtype == np.uint16:
-            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
-        return torch.from_numpy(a).to(dev)
-
-    x, wg, gb = D(inp["x"]), D(inp["wg"]), D(inp["bias"])
-    w1, b1, w3, w2, b2 = (D(inp[n]) for n in ("w1", "b1", "w3", "w2", "b2"))
-    bufs = M.alloc_layer(w.s, w.m, w.e, w.k, w.h, w.act, w.capacity_factor, device=dev)
-    flags = M.MOE_FLAG_NORMALIZE_GATES if w.normalize_gates and w.k >= 2 else 0
-    cap_ws = bufs.workspace[: M.moe_capacity_workspace_size(w.s, w.e, w.k)]
-    ffn_ws = torch.empty(M.moe_expert_ffn_workspace_size(M.MOE_BF16, w.act, w.e, bufs.c_max, w.m, w.h),
-                         dtype=torch.uint8, device=dev)
+    pk = peaks()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
+    fp32 = fp32_fma_peak(M, dev)
+    pk["fp32"] = max(fp32.values())
+    w, wseed = CONFIGS[args.config]
+    run = LayerRun(w, wseed, dev, flush)
 
-    def staged_step(ev):
-        """The five C-ABI calls, with an event after each stage."""
-        M.moe_gate_topk(x, wg, gb, w.k, bufs.idx, bufs.gates, bufs.status, flags=flags)
-        ev[1].record()
-        M.moe_capacity_locations(bufs.idx, w.e, w.capacity_factor, bufs.c_max, cap_ws, bufs.loc,
-                                 bufs.counts, bufs.c_dev, bufs.status)
-        ev[2].record()
-        M.moe_encode(x, bufs.idx, bufs.loc, bufs.counts, bufs.c_dev, bufs.buf, bufs.status)
-        ev[3].record()
-        M.moe_expert_ffn(bufs.buf, bufs.counts, bufs.c_dev, w1, b1, w3, w2, b2, w.act, ffn_ws,
-                         bufs.out, bufs.status)
-        ev[4].record()
-        M.moe_decode(bufs.out, bufs.idx, bufs.loc, bufs.gates, bufs.c_dev, bufs.y, bufs.status)
-
-    def mk():
-        return [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-
+    # ---- warm-up: staged and whole
+    run.time_stages(max(1, args.warmup // 2), 1)
     for _ in range(args.warmup):
         flush.fill_(1)
-        ev = mk()
-        ev[0].record()
-        staged_step(ev)
-        ev[5].record()
+        run.whole_step()
     torch.cuda.synchronize()
-    if int(bufs.status.item()) != 0:
-        raise RuntimeError(f"device status {int(bufs.status.item())}")
-    torch.cuda.synchronize()
-
-    def whole_step():
-        M.run_layer(x, wg, gb, w1, b1, w3, w2, b2, w.act, w.k, w.capacity_factor, bufs,
-                    normalize_gates=bool(flags))
-
-    for _ in range(args.warmup):
-        flush.fill_(1)
-        whole_step()
-    torch.cuda.synchronize()
+    run.check_status()
 
     # ---- timed (headline): device-resident inputs, the whole layer per step
     n_launch0 = M.launch_count()
@@ -288,7 +572,7 @@ def run_ours(args, rank, world, local_rank):
             flush.fill_(1)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
-            whole_step()
+            run.whole_step()
             b.record()
             pairs.append((a, b))
         torch.cuda.synchronize()
@@ -297,137 +581,32 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     launches = M.launch_count() - n_launch0
     ms_step = sum(a.elapsed_time(b) for a, b in pairs) / args.steps
+    clocks = clk.summary(t_wall0, t_wall1)
+    run.check_status()
 
-    # ---- timed (stages): the same calls with an event after every stage
-    events = []
-    for _ in range(args.steps):
-        flush.fill_(1)
-        ev = mk()
-        ev[0].record()
-        staged_step(ev)
-        ev[5].record()
-        events.append(ev)
-    torch.cuda.synchronize()
-    stage_names = ["gate", "capacity", "encode", "expert_ffn", "decode"]
-    stage_ms = {n: 0.0 for n in stage_names}
-    for ev in events:
-        for i, n in enumerate(stage_names):
-            stage_ms[n] += ev[i].elapsed_time(ev[i + 1])
-    stage_ms = {n: v / args.steps for n, v in stage_ms.items()}
+    # ---- stages: the same calls with an event after every stage
+    stage_ms = run.time_stages(args.steps, 2)
 
-    # ---- e2e: one-call public API, host input/output inside the interval
-    x_host = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    y_host = torch.empty((w.s, w.m), dtype=torch.bfloat16).pin_memory()
-    x_dev = torch.empty_like(x)
+    # ---- e2e: one C call with host buffers (pinned), copies inside the interval
+    x_host = run.inp["x"].cpu().pin_memory()
+    y_host = torch.empty((w.s, w.m), dtype=run.tdt).pin_memory()
+    x_dev = torch.empty_like(run.inp["x"])
+    xx, wg, gb, w1, b1, w3, w2, b2 = run.args()
 
     def e2e_step():
-        x_dev.copy_(x_host, non_blocking=True)
-        M.run_layer(x_dev, wg, gb, w1, b1, w3, w2, b2, w.act, w.k, w.capacity_factor, bufs,
-                    normalize_gates=bool(flags))
-        y_host.copy_(bufs.y, non_blocking=True)
+        M.run_layer_host(x_host, y_host, x_dev, wg, gb, w1, b1, w3, w2, b2, w.act, w.k,
+                         w.capacity_factor, run.bufs, normalize_gates=bool(run.flags))
 
-    for _ in range(max(3, args.warmup // 2)):
-        flush.fill_(1)
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_ms = 0.0
-    for _ in range(args.steps):
-        flush.fill_(1)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        e2e_step()
-        b.record()
-        b.synchronize()
-        e2e_ms += a.elapsed_time(b)
-    e2e_ms /= args.steps
+    e2e_ms = run.time_calls(e2e_step, args.steps, max(3, args.warmup // 2))
+    run.check_status()
 
-    # ---- gate backward (not part of the step): gradient of the gate values to
-    # the logits, the gate weight, its bias and x, from this batch's routing
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(7)
-    d_gates = torch.randn((w.k, w.s), generator=gen, device=dev, dtype=torch.float32)
-    d_logits = torch.empty((w.s, w.e), device=dev, dtype=torch.float32)
-    d_wg = torch.empty((w.m, w.e), device=dev, dtype=torch.float32)
-    d_bias = torch.empty((w.e,), device=dev, dtype=torch.float32)
-    d_xg = torch.empty((w.s, w.m), device=dev, dtype=torch.float32)
-
-    def gate_bwd_step():
-        M.moe_gate_bwd(x, wg, gb, bufs.idx, bufs.gates, d_gates, d_logits, bufs.status,
-                       d_wg=d_wg, d_bias=d_bias, d_x=d_xg, flags=flags)
-
-    def time_alone(fn):
-        """Mean event time of fn over args.steps calls, L2 flushed before each."""
-        for _ in range(3):
-            flush.fill_(1)
-            fn()
-        torch.cuda.synchronize()
-        tot = 0.0
-        for _ in range(args.steps):
-            flush.fill_(1)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            b.synchronize()
-            tot += a.elapsed_time(b)
-        return tot / args.steps
-
-    gbwd_ms = time_alone(gate_bwd_step)
-
-    # ---- decode and encode backward (not part of the step): dE and dG from a
-    # dY of this batch's shape, then dX from dBuf := dE (the identity-expert chain)
-    dy = torch.randn((w.s, w.m), generator=gen, device=dev, dtype=torch.float32).to(x.dtype)
-    d_out = torch.empty_like(bufs.out)
-    d_gates_dec = torch.empty((w.k, w.s), device=dev, dtype=torch.float32)
-    dx_enc = torch.empty_like(x)
-    dbwd_ms = time_alone(lambda: M.moe_decode_bwd(dy, bufs.out, bufs.idx, bufs.loc, bufs.gates,
-                                                  bufs.counts, bufs.c_dev, d_out, d_gates_dec,
-                                                  bufs.status))
-    ebwd_ms = time_alone(lambda: M.moe_encode_bwd(d_out, bufs.idx, bufs.loc, bufs.c_dev, dx_enc,
-                                                  bufs.status))
-    if int(bufs.status.item()) != 0:
-        raise RuntimeError(f"device status {int(bufs.status.item())}")
+    c, R, t1, hit = run.routing_summary()
+    work = stage_work(w, R, t1, hit)
+    stages = {n: rate(n, stage_ms[n], work[n], pk) for n in run.STAGES}
+    ffn_tf = work["expert_ffn"]["flop"] / (stage_ms["expert_ffn"] * 1e-3) / 1e12
 
     # ---- max over ranks
     ms_step, e2e_ms = reduce_max([ms_step, e2e_ms], device=dev)
-
-    # ---- algorithmic work of this batch (read after timing)
-    counts = bufs.counts.cpu().numpy().astype(np.int64)
-    c = int(bufs.c_dev.item())
-    kept = np.minimum(counts, c)
-    R = int(kept.sum())
-    loc = bufs.loc.cpu().numpy()
-    t1 = int(((loc < c).any(0)).sum())  # tokens with at least one kept route
-    b = 2
-    ffn_flops = 4.0 * R * w.m * w.h
-    bytes_ = {
-        "gate": w.s * w.m * b + 4 * w.m * w.e + 8 * w.s * w.k,
-        "encode": t1 * w.m * b + R * w.m * b + 8 * w.s * w.k,
-        "decode": R * w.m * b + w.s * w.m * b + 12 * w.s * w.k,
-        "decode_bwd": t1 * w.m * b + 2 * R * w.m * b + 16 * w.s * w.k,
-        "encode_bwd": R * w.m * b + w.s * w.m * b + 8 * w.s * w.k,
-    }
-    pk = peaks()
-    stages = {}
-    for n in stage_names:
-        d = {"ms": stage_ms[n]}
-        if n in bytes_:
-            gbs = bytes_[n] / (stage_ms[n] * 1e-3) / 1e9
-            d.update(gbs=gbs, hbm_frac=gbs / pk["hbm"])
-        if n == "expert_ffn":
-            tf = ffn_flops / (stage_ms[n] * 1e-3) / 1e12
-            d.update(tflops=tf, tc_frac=tf / pk["bf16"])
-        stages[n] = d
-    ffn_tf = ffn_flops / (stage_ms["expert_ffn"] * 1e-3) / 1e12
-    # gate backward, timed on its own: fp32 FMAs of d_wg = x^T dl and d_x = dl Wg^T
-    gbwd_flops = 4.0 * w.s * w.m * w.e
-    stages["gate_bwd"] = {"ms": gbwd_ms, "fp32_tflops": gbwd_flops / (gbwd_ms * 1e-3) / 1e12,
-                          "note": "not part of the step: d_logits, d_wg, d_bias, d_x"}
-    for n, ms in (("decode_bwd", dbwd_ms), ("encode_bwd", ebwd_ms)):
-        gbs = bytes_[n] / (ms * 1e-3) / 1e9
-        stages[n] = {"ms": ms, "gbs": gbs, "hbm_frac": gbs / pk["hbm"], "note": "not part of the step"}
-    clocks = clk.summary(t_wall0, t_wall1)
-
     res = {
         "metric": METRIC,
         "value": job_throughput(world, w.s, ms_step),
@@ -439,25 +618,49 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded counter-based normal draws; no dataset)",
         "config": {"workload": w.name, "s": w.s, "m": w.m, "e": w.e, "k": w.k, "h": w.h,
                    "act": w.act, "capacity_factor": w.capacity_factor, "c": c, "kept_routes": R,
+                   "experts_hit": hit,
                    "l2": "flushed (256 MiB write) before every timed step, outside the interval",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"kernel": "expert_ffn (tcgen05 grouped GEMM, fc1+fc2; duration from the "
                                "stage-bracketed timed pass)", "bound": "tensor",
                      "achieved": ffn_tf, "peak": pk["bf16"], "unit": "TFLOP/s",
                      "frac": ffn_tf / pk["bf16"], "peak_source": f"{pk['src']} bf16 burst",
-                     "traffic": ffn_traffic_from_profile(), "traffic_unit": "bytes per call"},
+                     "traffic": ffn_traffic_from_profile(w.name), "traffic_unit": "bytes per call"},
         "stages": stages,
+        "fp32_fma_tflops": dict(fp32, source="moe_probe_fp32_fma on this GPU, best of 5"),
         "e2e": {"value": job_throughput(world, w.s, e2e_ms), "unit": "tokens/s",
-                "h2d_bytes_per_step": w.s * w.m * 2, "d2h_bytes_per_step": w.s * w.m * 2,
-                "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+                "d2h_bytes_per_step": y_host.numel() * y_host.element_size(),
+                "ms_per_step": e2e_ms, "api": "moe_layer_forward_host (one C call)"},
         "clocks": clocks,
         "gpu_launches": launches,
     }
+    del x_host, y_host, x_dev
+    rank_free(run)
+    run = None
+
+    # ---- the other graded workloads: stage breakdowns (and the e=16 layer's backward)
+    if not args.no_graded:
+        graded = {}
+        gsteps = max(5, min(args.steps, 30))
+        for name in GRADED:
+            if name == args.config:
+                continue
+            gw, gseed = CONFIGS[name]
+            g = LayerRun(gw, gseed, dev, flush)
+            sm = g.time_stages(gsteps, 3)
+            extra = g.backward_chain(gsteps, 3, pk) if gw.backward else None
+            graded[name] = graded_report(name, g, sm, pk, extra)
+            rank_free(g)
+            g = None
+        res["graded"] = graded
+
     if rank == 0 and not args.no_cpu_baseline:
+        inp = host_inputs(w, wseed, dev)
         res["cpu_baseline"] = cpu_baseline_dict(w, inp, args.cpu_seconds)
     return res
 
@@ -466,9 +669,10 @@ def run_reference(args):
     """The CPU oracle as the reference arm: each step is a bounded token sample."""
     import oracle
 
-    w = WORKLOAD
-    inp = synth.make_inputs_host(w)
-    _, s2, _, dt0, thr = time_oracle(w, inp, max(0.2, 60.0 / max(1, args.steps)))
+    w, wseed = CONFIGS[args.config]
+    inp = host_inputs(w, wseed)
+    per_step = max(0.25, min(2.0, 90.0 / max(1, args.steps)))
+    _, s2, _, _, thr = time_oracle(w, inp, per_step)
     ws, sub = oracle_sample_inputs(w, inp, s2)
     for _ in range(min(args.warmup, 1)):
         oracle.layer_forward(ws, sub)
@@ -486,7 +690,7 @@ def run_reference(args):
                    "act": w.act, "capacity_factor": w.capacity_factor},
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle",
                          "sample": f"each step: the CPU oracle's forward chain on the first {s2} "
-                                   f"tokens of the batch"},
+                                   f"tokens of the batch as a batch of their own"},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

@@ -65,6 +65,9 @@ def load():
         "moe_layer_workspace_size": (SZ, [I, I, I64, I, I, I, I64, I]),
         "moe_layer_forward": (I, [P, I, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, I64, U,
                                   P, P, P, P, P, P, P, P, P, SZ, P, P]),
+        "moe_layer_forward_host": (I, [P, P, P, I, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, I64,
+                                       U, P, P, P, P, P, P, P, P, P, SZ, P, P]),
+        "moe_probe_fp32_fma": (I, [I, I, I, P, P]),
         "moe_status_str": (ctypes.c_char_p, [I]),
         "moe_launch_count": (ctypes.c_uint64, []),
     }
@@ -330,4 +333,36 @@ def moe_layer_forward(x, wg, gate_bias, w1, b1, w3, w2, b2, act, k, capacity_fac
         _stream(stream)), "moe_layer_forward")
 
 
-from .layer import MoELayerBuffers, alloc_layer, run_layer  # noqa: E402,F401
+def moe_layer_forward_host(x_host, y_host, x, wg, gate_bias, w1, b1, w3, w2, b2, act, k,
+                           capacity_factor, flags, idx, gates, loc, counts, c_dev, buf, out, y,
+                           workspace, dev_status, stream=None):
+    """moe_layer_forward with x read from, and y written to, host tensors
+    (pinned for asynchronous copies); x and y are the device buffers."""
+    s, m = x.shape
+    e, c_max, _ = buf.shape
+    h = w1.shape[1]
+    k = int(k)
+    I, F, dt = _i32(), _f32(), x.dtype
+    for name, t in (("x_host", x_host), ("y_host", y_host)):
+        if t.is_cuda or tuple(t.shape) != (s, m) or t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{name}: must be a contiguous host tensor [{s}, {m}] of {dt}")
+    _check(load().moe_layer_forward_host(
+        ctypes.c_void_p(x_host.data_ptr()), ctypes.c_void_p(y_host.data_ptr()), _ptr(x, "x"), _dt(x),
+        _ptr(wg, "wg", F, (m, e)), _ptr(gate_bias, "gate_bias", F, (e,)),
+        _ptr(w1, "w1", dt, (e, h, m)), _ptr(b1, "b1", dt, (e, h)), _ptr(w3, "w3", dt, (e, h, m)),
+        _ptr(w2, "w2", dt, (e, m, h)), _ptr(b2, "b2", dt, (e, m)), _act(act), s, m, e, k, h,
+        float(capacity_factor), c_max, int(flags), _ptr(idx, "idx", I, (k, s)),
+        _ptr(gates, "gates", F, (k, s)), _ptr(loc, "loc", I, (k, s)),
+        _ptr(counts, "counts", I, (e,)), _ptr(c_dev, "c_dev", I), _ptr(buf, "buf", dt, (e, c_max, m)),
+        _ptr(out, "out", dt, (e, c_max, m)), _ptr(y, "y", dt, (s, m)), _ptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status, "dev_status", I),
+        _stream(stream)), "moe_layer_forward_host")
+
+
+def moe_probe_fp32_fma(packed, blocks, iters, out, stream=None):
+    """Launch the fp32 FMA throughput probe (blocks * 256 * iters * 32 flop)."""
+    _check(load().moe_probe_fp32_fma(int(bool(packed)), int(blocks), int(iters),
+                                     _ptr(out, "out", _f32()), _stream(stream)), "moe_probe_fp32_fma")
+
+
+from .layer import MoELayerBuffers, alloc_layer, run_layer, run_layer_host  # noqa: E402,F401

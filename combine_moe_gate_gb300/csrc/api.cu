@@ -36,6 +36,8 @@ moe_status decode_bwd_launch(const void *dy, const void *out, moe_dtype dt, cons
 moe_status capacity_noalloc_launch(const int32_t *idx, int64_t s, int e, int k, float f,
                                    int64_t c_max, int32_t *loc, int32_t *counts, int32_t *c_dev,
                                    int32_t *st, cudaStream_t stream);
+moe_status probe_fp32_fma_launch(int packed, int blocks, int iters, float *out,
+                                 cudaStream_t stream);
 bool ffn_tc_supported(int e, int64_t c_max, int m, int h);
 moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *c_dev,
                          const void *w1, const void *b1, const void *w3, const void *w2,
@@ -305,6 +307,42 @@ moe_status moe_layer_forward(const void *x, moe_dtype dt, const float *wg, const
                         ws + cap_b, workspace_bytes - cap_b, out, dev_status, stream);
     if (st != MOE_OK) return st;
     return moe_decode(out, dt, idx, loc, gates, c_dev, s, m, e, k, c_max, y, dev_status, stream);
+}
+
+moe_status moe_layer_forward_host(const void *x_host, void *y_host, const void *x, moe_dtype dt,
+                                  const float *wg, const float *gate_bias, const void *w1,
+                                  const void *b1, const void *w3, const void *w2, const void *b2,
+                                  moe_act act, int64_t s, int m, int e, int k, int h,
+                                  float capacity_factor, int64_t c_max, unsigned flags,
+                                  int32_t *idx, float *gates, int32_t *loc, int32_t *counts,
+                                  int32_t *c_dev, void *buf, void *out, void *y, void *workspace,
+                                  size_t workspace_bytes, int32_t *dev_status, void *stream) {
+    if (x_host == nullptr || y_host == nullptr || !valid_dt(dt) || s < 1 || m < 1 || !ok16(x) ||
+        !ok16(y))
+        return MOE_ERR_INVALID_ARG;
+    if (moe_layer_workspace_size(dt, act, s, m, e, k, c_max, h) == 0) return MOE_ERR_INVALID_ARG;
+    const size_t bytes = (size_t)s * (size_t)m * esize(dt);
+    cudaStream_t st = as_stream(stream);
+    if (cudaMemcpyAsync(const_cast<void *>(x), x_host, bytes, cudaMemcpyHostToDevice, st) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    moe_status r = moe_layer_forward(x, dt, wg, gate_bias, w1, b1, w3, w2, b2, act, s, m, e, k, h,
+                                     capacity_factor, c_max, flags, idx, gates, loc, counts,
+                                     c_dev, buf, out, y, workspace, workspace_bytes, dev_status,
+                                     stream);
+    if (r != MOE_OK) return r;
+    if (cudaMemcpyAsync(y_host, y, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+moe_status moe_probe_fp32_fma(int packed, int blocks, int iters, float *out, void *stream) {
+    if (blocks < 1 || iters < 1 || !ok4(out)) return MOE_ERR_INVALID_ARG;
+    return probe_fp32_fma_launch(packed, blocks, iters, out, as_stream(stream));
 }
 
 }  // extern "C"

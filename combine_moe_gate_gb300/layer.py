@@ -10,7 +10,7 @@ from typing import Optional
 import torch
 
 from . import (MOE_BF16, MOE_F32, MOE_FLAG_NORMALIZE_GATES, moe_capacity_bound,
-               moe_layer_forward, moe_layer_workspace_size)
+               moe_layer_forward, moe_layer_forward_host, moe_layer_workspace_size)
 
 
 @dataclass
@@ -53,6 +53,19 @@ def alloc_layer(s, m, e, k, h, act, capacity_factor, dtype=torch.bfloat16, devic
         workspace=torch.empty((ws,), dtype=torch.uint8, device=device),
         status=torch.zeros((1,), **i32),
     )
+
+
+def run_layer_host(x_host, y_host, x, wg, gate_bias, w1, b1, w3, w2, b2, act, k, capacity_factor,
+                   bufs: MoELayerBuffers, normalize_gates=True, flags=0, stream=None):
+    """Enqueue host-to-device copy of x_host, the whole forward layer and the
+    copy of y back to y_host (one C call); the caller synchronises."""
+    if normalize_gates:
+        flags |= MOE_FLAG_NORMALIZE_GATES
+    moe_layer_forward_host(x_host, y_host, x, wg, gate_bias, w1, b1, w3, w2, b2, act, k,
+                           capacity_factor, flags, bufs.idx, bufs.gates, bufs.loc, bufs.counts,
+                           bufs.c_dev, bufs.buf, bufs.out, bufs.y, bufs.workspace, bufs.status,
+                           stream=stream)
+    return y_host
 
 
 def run_layer(x, wg, gate_bias, w1, b1, w3, w2, b2, act, k, capacity_factor, bufs: MoELayerBuffers,

@@ -300,6 +300,36 @@ moe_status moe_layer_forward(const void *x, moe_dtype dt, const float *wg, const
                              void *workspace, size_t workspace_bytes,
                              int32_t *dev_status, void *stream);
 
+/*
+ * moe_layer_forward with the layer's input taken from host memory and its
+ * output returned to host memory, for a caller whose tokens live on the host:
+ * x_host [s, m] is copied into the device buffer x, the layer runs as in
+ * moe_layer_forward, and y is copied to y_host [s, m], all three enqueued on
+ * `stream` (cudaMemcpyAsync: with pinned host memory the copies are
+ * asynchronous; with pageable memory the runtime may block the calling thread
+ * until they are done).  Arguments after x are those of moe_layer_forward.
+ * The caller synchronises the stream before reading y_host.
+ */
+moe_status moe_layer_forward_host(const void *x_host, void *y_host, const void *x, moe_dtype dt,
+                                  const float *wg, const float *gate_bias, const void *w1,
+                                  const void *b1, const void *w3, const void *w2, const void *b2,
+                                  moe_act act, int64_t s, int m, int e, int k, int h,
+                                  float capacity_factor, int64_t c_max, unsigned flags,
+                                  int32_t *idx, float *gates, int32_t *loc, int32_t *counts,
+                                  int32_t *c_dev, void *buf, void *out, void *y, void *workspace,
+                                  size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * Measurement helper, not part of the layer: launches `blocks` CTAs of 256
+ * threads, each thread running 8 independent two-wide chains of `iters` fp32
+ * fused multiply-adds (packed fp32x2 FMA when `packed`, else scalar pairs),
+ * i.e. blocks * 256 * iters * 32 flop.  Timed by the caller with events, it
+ * gives this GPU's fp32 FMA throughput, the roofline of a gate whose logits
+ * (2*m*e flop per token) outweigh its HBM bytes.  out: one device float the
+ * kernel may write (never for these values).
+ */
+moe_status moe_probe_fp32_fma(int packed, int blocks, int iters, float *out, void *stream);
+
 /* Human-readable name of a status code (static string). */
 const char *moe_status_str(moe_status st);
 

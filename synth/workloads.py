@@ -146,12 +146,14 @@ def make_inputs_host(w: Workload, parts=("x", "wg", "bias", "w1", "w3", "w2", "b
     return out
 
 
-def make_inputs_device(w: Workload, device="cuda", weight_seed=None):
+def make_inputs_device(w: Workload, device="cuda", weight_seed=None,
+                       parts=("x", "wg", "bias", "w1", "w3", "w2", "b1", "b2", "dy")):
     """The same recipe drawn with torch on `device` (for multi-GB workloads).
 
     bf16 tensors come back as torch.bfloat16, fp32 as torch.float32.  Expert
     weights use `weight_seed` when given (the sweep shares one weight set across
-    its points), otherwise the workload's seed.
+    its points), otherwise the workload's seed.  Only the requested parts are
+    drawn.
     """
     import torch
 
@@ -159,19 +161,20 @@ def make_inputs_device(w: Workload, device="cuda", weight_seed=None):
 
     dt, sd = w.dtype, w.seed
     wsd = sd if weight_seed is None else weight_seed
-    out = {
-        "x": normal_torch(sd, "x", (w.s, w.m), 1.0, dt, device),
-        "wg": normal_torch(sd, "wg", (w.m, w.e), 1.0 / math.sqrt(w.m), "f32", device),
-        "bias": None,
-        "w1": normal_torch(wsd, "w1", (w.e, w.h, w.m), 1.0 / math.sqrt(w.m), dt, device),
-        "w3": (normal_torch(wsd, "w3", (w.e, w.h, w.m), 1.0 / math.sqrt(w.m), dt, device)
-               if w.act == ACT_SWIGLU else None),
-        "w2": normal_torch(wsd, "w2", (w.e, w.m, w.h), 1.0 / math.sqrt(w.h), dt, device),
-        "b1": normal_torch(wsd, "b1", (w.e, w.h), 0.01, dt, device) if w.has_bias else None,
-        "b2": normal_torch(wsd, "b2", (w.e, w.m), 0.01, dt, device) if w.has_bias else None,
-        "dy": normal_torch(sd, "dy", (w.s, w.m), 1.0, dt, device) if w.backward else None,
+    draw = {
+        "x": lambda: normal_torch(sd, "x", (w.s, w.m), 1.0, dt, device),
+        "wg": lambda: normal_torch(sd, "wg", (w.m, w.e), 1.0 / math.sqrt(w.m), "f32", device),
+        "bias": lambda: None,
+        "w1": lambda: normal_torch(wsd, "w1", (w.e, w.h, w.m), 1.0 / math.sqrt(w.m), dt, device),
+        "w3": lambda: (normal_torch(wsd, "w3", (w.e, w.h, w.m), 1.0 / math.sqrt(w.m), dt, device)
+                       if w.act == ACT_SWIGLU else None),
+        "w2": lambda: normal_torch(wsd, "w2", (w.e, w.m, w.h), 1.0 / math.sqrt(w.h), dt, device),
+        "b1": lambda: normal_torch(wsd, "b1", (w.e, w.h), 0.01, dt, device) if w.has_bias else None,
+        "b2": lambda: normal_torch(wsd, "b2", (w.e, w.m), 0.01, dt, device) if w.has_bias else None,
+        "dy": lambda: normal_torch(sd, "dy", (w.s, w.m), 1.0, dt, device) if w.backward else None,
     }
+    out = {n: draw[n]() for n in parts}
     b = gate_bias_host(w)
-    if b is not None:
+    if "bias" in parts and b is not None:
         out["bias"] = torch.from_numpy(b).to(device)
     return out
