@@ -1,18 +1,23 @@
 """GPU parity on the full-size workloads, through the one-call layer entry point
 (moe_layer_forward) that the bench times.
 
-Inputs are drawn on the device (synth.make_inputs_device) and the slices the
-oracle needs are copied back to the host.  The oracle then checks:
+Inputs are drawn on the device (synth.make_inputs_device) and copied back to
+the host for the oracle.  The oracle then checks:
   * routing over the whole batch: top-k indices, slot locations, per-expert
     counts and capacity bit for bit, gates within the fp32 tolerance;
   * encode over every kept route: the slot row equals the token row bit for bit;
-  * the expert FFN on sampled rows (first, last and random kept rows of a few
-    experts) within the bf16 tolerance;
-  * the layer output y on sampled tokens: the oracle's FFN rows for every kept
-    route of the token, combined by the oracle's decode (bf16 tolerance);
-  * decode alone on sampled tokens with identity experts (the encoded buffer as
-    expert output): bit for bit, both sides accumulate in fp32 in route order;
-  * for the backward workload, decode_bwd and encode_bwd over the whole batch.
+  * the expert FFN output (bf16 / fp32 tolerance against the oracle's MLP of
+    the same slot row): on every kept row for the tiny, e=8 and e=16 layers;
+    on the e=256 layer and the sweep points, on every kept route of 1024
+    sampled tokens plus one row of every 256-row tile of every expert those
+    routes leave uncovered;
+  * the layer output y (the oracle's decode of the oracle's FFN rows): on the
+    whole batch for the tiny, e=8 and e=16 layers, on the 1024 sampled tokens
+    otherwise;
+  * decode alone with identity experts (the encoded buffer as expert output):
+    bit for bit, both sides accumulate in fp32 in route order (whole batch or
+    the sampled tokens);
+  * for the e=16 layer, decode_bwd and encode_bwd over the whole batch.
 """
 
 import numpy as np
@@ -27,6 +32,9 @@ from gpu_util import assert_close, bf16_bits_of_f32, status_ok
 
 pytestmark = pytest.mark.gpu
 
+TILE_ROWS = 256        # output rows of one expert-FFN tile (a CTA pair's M)
+SAMPLE_TOKENS = 1024
+
 
 def _host_bits(t):
     if t is None:
@@ -37,32 +45,79 @@ def _host_bits(t):
 
 
 class _Weights:
-    """Host copies of single experts' weights, fetched on demand."""
+    """Expert weights on the device (drawn once per weight set) and host fp32
+    copies of single experts, fetched on demand; the sweep's 32 points share
+    one weight set."""
 
-    def __init__(self, inp):
-        self.inp = inp
-        self.cache = {}
+    NAMES = ("w1", "w3", "w2", "b1", "b2")
 
-    def get(self, j):
-        if j not in self.cache:
-            sl = lambda n: None if self.inp[n] is None else _host_bits(self.inp[n][j:j + 1])
-            self.cache[j] = {n: sl(n) for n in ("w1", "w3", "w2", "b1", "b2")}
-        return self.cache[j]
+    def __init__(self):
+        self.key = None
+        self.dev = {}
+        self.host = {}
+
+    def get_device(self, w, weight_seed):
+        key = (w.e, w.m, w.h, w.act, w.dtype, w.biases, w.seed if weight_seed is None else weight_seed)
+        if key != self.key:
+            self.key, self.dev, self.host = None, {}, {}
+            torch.cuda.empty_cache()
+            self.dev = synth.make_inputs_device(w, "cuda", weight_seed=weight_seed, parts=self.NAMES)
+            self.key = key
+        return self.dev
+
+    def expert(self, j):
+        if j not in self.host:
+            self.host[j] = {n: None if t is None else oracle.to_f32(_host_bits(t[j:j + 1]))
+                            for n, t in self.dev.items()}
+        return self.host[j]
 
 
-def _ffn_expected(w, wts, x_h, j, rows_tokens):
-    """Oracle FFN outputs of expert j for the listed token rows (in order)."""
-    ww = wts.get(j)
-    buf = x_h[np.asarray(rows_tokens)][None]            # [1, n, m]
-    return oracle.ffn_rows(buf, ww["w1"], ww["b1"], ww["w3"], ww["w2"], ww["b2"], w.act,
-                           np.zeros(len(rows_tokens), np.int32), np.arange(len(rows_tokens)),
-                           w.dtype == "bf16")
+_WEIGHTS = _Weights()
 
 
-def run_and_check(w, weight_seed=None, n_ffn_experts=3, n_tokens=4, rng_seed=0):
+def _ffn_rows_by_slot(w, x_h, slots, slot_tok):
+    """Oracle FFN outputs for the listed (expert, slot) pairs: each slot's row
+    is its token's x row.  Returns {slot: row}."""
+    by_e = {}
+    for (j, l) in slots:
+        by_e.setdefault(j, []).append(l)
+    got = {}
+    for j, ls in sorted(by_e.items()):
+        ww = _WEIGHTS.expert(j)
+        buf = x_h[np.asarray([slot_tok[(j, l)] for l in ls])][None]       # [1, n, m]
+        o = oracle.ffn_rows(buf, ww["w1"], ww["b1"], ww["w3"], ww["w2"], ww["b2"], w.act,
+                            np.zeros(len(ls), np.int32), np.arange(len(ls), dtype=np.int64),
+                            w.dtype == "bf16")
+        for l, row in zip(ls, o):
+            got[(j, l)] = row
+    return got
+
+
+def _compact_decode(w, toks, idx_o, loc_o, kept, g_o, rows):
+    """The oracle's decode of token list `toks` from the slot rows `rows`
+    ({(j, l): row}), as a compact [n, 1, m] expert buffer."""
+    idx_m = np.zeros((w.k, len(toks)), np.int32)
+    loc_m = np.ones((w.k, len(toks)), np.int32)     # loc 1 >= c 1: dropped
+    outs, pos = [], {}
+    for ti, t in enumerate(toks):
+        for r in range(w.k):
+            if kept[r, t]:
+                key = (int(idx_o[r, t]), int(loc_o[r, t]))
+                if key not in pos:
+                    pos[key] = len(outs)
+                    outs.append(rows[key])
+                idx_m[r, ti], loc_m[r, ti] = pos[key], 0
+    if not outs:
+        return np.zeros((len(toks), w.m), np.float32)
+    out_m = np.stack(outs)[:, None, :]
+    return oracle.decode(out_m, idx_m, loc_m, g_o[:, toks], 1, w.dtype == "bf16")
+
+
+def run_and_check(w, weight_seed=None, full=False, rng_seed=0):
     rng = np.random.default_rng(rng_seed)
     torch.cuda.synchronize()
-    inp = synth.make_inputs_device(w, "cuda", weight_seed=weight_seed)
+    inp = dict(_WEIGHTS.get_device(w, weight_seed))
+    inp.update(synth.make_inputs_device(w, "cuda", parts=("x", "wg", "bias", "dy")))
     x_h = _host_bits(inp["x"])
     wg_h = inp["wg"].cpu().numpy()
     bias_h = None if inp["bias"] is None else inp["bias"].cpu().numpy()
@@ -101,101 +156,71 @@ def run_and_check(w, weight_seed=None, n_ffn_experts=3, n_tokens=4, rng_seed=0):
     rows = bufs.buf[torch.from_numpy(j_k).cuda().long(), torch.from_numpy(l_k).cuda().long()]
     assert np.array_equal(_host_bits(rows), x_h[t_k]), "encoded rows"
     del rows
+    slot_tok = {(int(j), int(l)): int(t) for t, j, l in zip(t_k, j_k, l_k)}
 
-    # slot -> token map (oracle's)
-    slot_tok = {}
-    for r, t, j, l in zip(r_k, t_k, j_k, l_k):
-        slot_tok[(int(j), int(l))] = int(t)
-
-    wts = _Weights(inp)
-    # expert FFN: sampled rows of a few experts (most loaded, least loaded, random)
-    live = np.nonzero(kept_o > 0)[0]
-    pick = {int(live[np.argmax(kept_o[live])]), int(live[np.argmin(kept_o[live])])}
-    while len(pick) < min(n_ffn_experts, len(live)):
-        pick.add(int(rng.choice(live)))
-    for j in sorted(pick):
-        kj = int(kept_o[j])
-        rws = sorted({0, kj - 1, int(rng.integers(kj)), int(rng.integers(kj))})
-        want = _ffn_expected(w, wts, x_h, j, [slot_tok[(j, r)] for r in rws])
-        got = bufs.out[j, torch.tensor(rws).cuda()].float().cpu().numpy()
-        assert_close(got, want, w.dtype, f"ffn expert {j}")
-
-    # layer output on sampled tokens: oracle FFN rows of each kept route + oracle decode
-    toks = rng.choice(w.s, size=min(n_tokens, w.s), replace=False)
-    outs, q = [], 0
-    idx_m = np.zeros((w.k, len(toks)), np.int32)
-    loc_m = np.ones((w.k, len(toks)), np.int32)     # loc 1 >= c 1: dropped
-    g_m = np.zeros((w.k, len(toks)), np.float32)
-    for ti, t in enumerate(toks):
-        for r in range(w.k):
-            g_m[r, ti] = g_o[r, t]
-            if kept[r, t]:
-                outs.append(_ffn_expected(w, wts, x_h, int(idx_o[r, t]), [int(t)])[0])
-                idx_m[r, ti], loc_m[r, ti] = q, 0
-                q += 1
-    if outs:
-        out_m = np.stack(outs)[:, None, :]
-        y_want = oracle.decode(out_m, idx_m, loc_m, g_m, 1, bf16)
+    # tokens whose output is checked, and the slots whose FFN rows are checked
+    if full:
+        toks = np.arange(w.s)
+        slots = sorted(slot_tok)
     else:
-        y_want = np.zeros((len(toks), w.m), np.float32)
+        toks = np.sort(rng.choice(w.s, size=min(SAMPLE_TOKENS, w.s), replace=False))
+        slots = {(int(idx_o[r, t]), int(loc_o[r, t])) for t in toks for r in range(w.k) if kept[r, t]}
+        covered = {(j, l // TILE_ROWS) for (j, l) in slots}
+        for j in np.nonzero(kept_o > 0)[0]:
+            for tile in range((int(kept_o[j]) + TILE_ROWS - 1) // TILE_ROWS):
+                if (int(j), tile) not in covered:
+                    lo, hi = tile * TILE_ROWS, min((tile + 1) * TILE_ROWS, int(kept_o[j]))
+                    slots.add((int(j), int(rng.integers(lo, hi))))
+        slots = sorted(slots)
+    ffn_o = _ffn_rows_by_slot(w, x_h, slots, slot_tok)
+
+    # expert FFN output on those slots
+    sj = torch.tensor([j for j, _ in slots], device="cuda", dtype=torch.long)
+    sl = torch.tensor([l for _, l in slots], device="cuda", dtype=torch.long)
+    got = bufs.out[sj, sl].float().cpu().numpy()
+    assert_close(got, np.stack([ffn_o[s_] for s_ in slots]), w.dtype, "expert FFN rows")
+    tiles = {(j, l // TILE_ROWS) for (j, l) in slots}
+    want_tiles = sum((int(kj) + TILE_ROWS - 1) // TILE_ROWS for kj in kept_o)
+    assert len(tiles) == want_tiles, "an FFN tile without a checked row"
+
+    # layer output: the oracle's decode of the oracle's FFN rows
+    y_want = _compact_decode(w, toks, idx_o, loc_o, kept, g_o, ffn_o)
     y_got = bufs.y[torch.from_numpy(toks).cuda().long()].float().cpu().numpy()
     assert_close(y_got, y_want, w.dtype, "layer output y")
 
-    # decode alone, identity experts: decode the encoded buffer; the oracle's slot
-    # rows are the host token rows they hold.  Bit-exact on sampled tokens (both
-    # sides accumulate in fp32 in ascending route order).
-    # (the oracle's gates are fed to the GPU: both sides then multiply identical values)
+    # decode alone, identity experts: decode the encoded buffer with the oracle's
+    # gates (both sides then multiply identical values); bit-exact
     y2 = torch.empty((w.s, w.m), dtype=tdt, device="cuda")
-    g_dev = torch.from_numpy(g_o).cuda()
-    M.moe_decode(bufs.buf, bufs.idx, bufs.loc, g_dev, bufs.c_dev, y2, bufs.status)
+    M.moe_decode(bufs.buf, bufs.idx, bufs.loc, torch.from_numpy(g_o).cuda(), bufs.c_dev, y2,
+                 bufs.status)
     torch.cuda.synchronize()
     status_ok(bufs.status)
-    toks2 = rng.choice(w.s, size=min(64, w.s), replace=False)
-    rows_needed = {}
-    idx_m2 = np.zeros((w.k, len(toks2)), np.int32)
-    loc_m2 = np.ones((w.k, len(toks2)), np.int32)
-    for ti, t in enumerate(toks2):
-        for r in range(w.k):
-            if kept[r, t]:
-                key = (int(idx_o[r, t]), int(loc_o[r, t]))
-                idx_m2[r, ti] = rows_needed.setdefault(key, len(rows_needed))
-                loc_m2[r, ti] = 0
-    keys = sorted(rows_needed, key=rows_needed.get)
-    if keys:
-        out_rows = x_h[np.array([slot_tok[k_] for k_ in keys])][:, None, :]
-        y2_want = oracle.decode(out_rows, idx_m2, loc_m2, g_o[:, toks2], 1, bf16)
-        y2_got = y2[torch.from_numpy(toks2).cuda().long()]
-        want_bits = bf16_bits_of_f32(y2_want) if bf16 else y2_want.view(np.int32)
-        got_bits = (y2_got.view(torch.int16) if bf16 else y2_got.view(torch.int32)).cpu().numpy()
-        assert np.array_equal(got_bits, want_bits), "decode of the encoded buffer"
-    del y2
+    x_rows = {s_: oracle.to_f32(x_h[slot_tok[s_]]) for s_ in slot_tok} if full else None
+    if not full:
+        x_rows = {(int(idx_o[r, t]), int(loc_o[r, t])): oracle.to_f32(x_h[t])
+                  for t in toks for r in range(w.k) if kept[r, t]}
+    y2_want = _compact_decode(w, toks, idx_o, loc_o, kept, g_o, x_rows)
+    y2_got = y2[torch.from_numpy(toks).cuda().long()]
+    want_bits = bf16_bits_of_f32(y2_want) if bf16 else y2_want.view(np.int32)
+    got_bits = (y2_got.view(torch.int16) if bf16 else y2_got.view(torch.int32)).cpu().numpy()
+    assert np.array_equal(got_bits, want_bits), "decode of the encoded buffer"
+    del y2, y2_got
 
     res = dict(idx=idx_o, loc=loc_o, g=g_o, c=c_o, c_max=c_max, need=need_o)
     return inp, bufs, res
 
 
 def test_tiny_fp32_full_layer():
-    w = W.TINY_FP32
-    inp = synth.make_inputs_host(w)
-    ref = oracle.layer_forward(w, inp)
-    run_and_check(w, n_ffn_experts=4, n_tokens=16)
-    # tiny: the whole output checked against the whole oracle chain
-    bufs = M.alloc_layer(w.s, w.m, w.e, w.k, w.h, w.act, w.capacity_factor, dtype=torch.float32)
-    dev = lambda a: None if a is None else torch.from_numpy(a).cuda()
-    M.run_layer(dev(inp["x"]), dev(inp["wg"]), None, dev(inp["w1"]), dev(inp["b1"]), None,
-                dev(inp["w2"]), dev(inp["b2"]), w.act, w.k, w.capacity_factor, bufs,
-                normalize_gates=False)
-    torch.cuda.synchronize()
-    assert_close(bufs.y.cpu().numpy(), ref["y"], "f32", "y")
+    run_and_check(W.TINY_FP32, full=True)
 
 
 def test_bf16_e8_bench_workload():
-    run_and_check(W.BF16_E8, n_ffn_experts=4, n_tokens=8)
+    run_and_check(W.BF16_E8, full=True)
 
 
 def test_bf16_e16_forward_and_backward():
     w = W.BF16_E16_BWD
-    inp, bufs, res = run_and_check(w, n_ffn_experts=4, n_tokens=6)
+    inp, bufs, res = run_and_check(w, full=True)
     # backward of decode and encode over the whole batch
     c, c_max = res["c"], res["c_max"]
     out_in = synth.normal_torch(w.seed + 1000, "out", (w.e, c_max, w.m), 1.0, w.dtype, "cuda")
@@ -224,10 +249,10 @@ def test_bf16_e16_forward_and_backward():
 
 
 def test_bf16_e256_swiglu_skewed():
-    run_and_check(W.BF16_E256_SWIGLU, n_ffn_experts=3, n_tokens=2)
+    run_and_check(W.BF16_E256_SWIGLU)
 
 
 @pytest.mark.parametrize("p", range(32))
 def test_dynamic_load_sweep_point(p):
     w = W.sweep_points()[p]
-    run_and_check(w, weight_seed=0, n_ffn_experts=2, n_tokens=2, rng_seed=p)
+    run_and_check(w, weight_seed=0, rng_seed=p)
