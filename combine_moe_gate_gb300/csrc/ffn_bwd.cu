@@ -12,10 +12,15 @@ namespace moe {
 namespace {
 
 // ------------------------------------------------------------- transposes
-constexpr int TP = 32, TP_Y = 8;
-constexpr int PAD_TO = 64;   // K block of the weight-gradient GEMMs
+// A CTA moves a 64 x 64 tile: 16-byte loads of source rows into shared
+// memory, then each thread gathers 8 elements of a source column and stores
+// them as one 16-byte piece of a destination row.  Row lengths, pitches and
+// offsets are multiples of 8 elements (16 bytes).
+constexpr int TP = 64, TP_THREADS = 256;
+constexpr int TP_PITCH = TP + 8;   // shared row pitch (elements): 144 bytes, conflict-free columns
+constexpr int PAD_TO = 64;         // K block of the weight-gradient GEMMs
 
-__global__ void __launch_bounds__(TP * TP_Y)
+__global__ void __launch_bounds__(TP_THREADS)
 transpose_pad_kernel(const uint16_t *__restrict__ src, int64_t src_batch, int64_t src_pitch,
                      uint16_t *__restrict__ dst, int64_t dst_batch, int64_t dst_pitch, int rows,
                      int cols, int dst_cols, const int32_t *__restrict__ counts,
@@ -23,7 +28,7 @@ transpose_pad_kernel(const uint16_t *__restrict__ src, int64_t src_batch, int64_
                      int32_t *status) {
     pdl_enter();
     if (status_bad(status)) return;
-    __shared__ uint32_t tile[TP][TP + 1];
+    __shared__ __align__(16) uint16_t tile[TP][TP_PITCH];
     const int b = blockIdx.z;
     if (skip && min(skip[b], *c_dev) <= 0) return;   // block-uniform
     const int r0 = blockIdx.x * TP, c0 = blockIdx.y * TP;
@@ -33,21 +38,30 @@ transpose_pad_kernel(const uint16_t *__restrict__ src, int64_t src_batch, int64_
     // (the consumer reads no further); block-uniform exit past that
     const int pad_end = counts ? min(dst_cols, (kept + PAD_TO - 1) / PAD_TO * PAD_TO) : dst_cols;
     if (r0 >= pad_end) return;
-    const uint16_t *s = src + (int64_t)b * src_batch;
-    uint16_t *d = dst + (int64_t)b * dst_batch;
-    for (int i = threadIdx.y; i < TP; i += TP_Y) {
-        const int r = r0 + i, c = c0 + (int)threadIdx.x;
-        tile[i][threadIdx.x] = (r < kept && c < cols) ? (uint32_t)s[(int64_t)r * src_pitch + c] : 0u;
+    const uint16_t *sb = src + (int64_t)b * src_batch;
+    uint16_t *db = dst + (int64_t)b * dst_batch;
+    for (int i = threadIdx.x; i < TP * (TP / 8); i += TP_THREADS) {
+        const int r = i >> 3, c = (i & 7) * 8;
+        V16 v;
+        v.w[0] = v.w[1] = v.w[2] = v.w[3] = 0u;
+        if (r0 + r < kept && c0 + c < cols) v = ld_stream(sb + (int64_t)(r0 + r) * src_pitch + c0 + c);
+        *reinterpret_cast<V16 *>(&tile[r][c]) = v;
     }
     __syncthreads();
-    for (int i = threadIdx.y; i < TP; i += TP_Y) {
-        const int c = c0 + i, r = r0 + (int)threadIdx.x;
-        if (c < cols && r < pad_end) d[(int64_t)c * dst_pitch + r] = (uint16_t)tile[threadIdx.x][i];
+    for (int i = threadIdx.x; i < TP * (TP / 8); i += TP_THREADS) {
+        const int c = i >> 3, r = (i & 7) * 8;   // destination row c0 + c, columns r0 + r ..
+        if (c0 + c >= cols || r0 + r >= pad_end) continue;
+        V16 v;
+#pragma unroll
+        for (int u = 0; u < 4; u++)
+            v.w[u] = (uint32_t)tile[r + 2 * u][c] | ((uint32_t)tile[r + 2 * u + 1][c] << 16);
+        st_v16(db + (int64_t)(c0 + c) * dst_pitch + r0 + r, v);
     }
 }
 
 // ---------------------------------------------------- activation backward
 constexpr int AB_THREADS = 256;
+constexpr int AB_ROWS = 16;   // rows of one expert per CTA
 
 __global__ void __launch_bounds__(AB_THREADS)
 act_bwd_kernel(const __nv_bfloat16 *__restrict__ pa, const __nv_bfloat16 *__restrict__ pb,
@@ -57,25 +71,24 @@ act_bwd_kernel(const __nv_bfloat16 *__restrict__ pa, const __nv_bfloat16 *__rest
     pdl_enter();
     if (status_bad(status)) return;
     const bool swiglu = act == MOE_ACT_SWIGLU;
+    const int j = blockIdx.y;
+    const int64_t kept = min((int64_t)min(counts[j], *c_dev), c_max);
+    const int64_t r0 = (int64_t)blockIdx.x * AB_ROWS;
+    if (r0 >= kept) return;                                // block-uniform
     const int hv = h / 8;                                  // 16-byte chunks per row
     const int64_t h2 = swiglu ? 2 * (int64_t)h : (int64_t)h;
-    const int64_t n = (int64_t)e * c_max * hv;
-    const int c = *c_dev;
-    for (int64_t q = (int64_t)blockIdx.x * AB_THREADS + threadIdx.x; q < n;
-         q += (int64_t)gridDim.x * AB_THREADS) {
-        const int64_t row = q / hv;
+    const int64_t nrow = min((int64_t)AB_ROWS, kept - r0);
+    for (int64_t q = threadIdx.x; q < nrow * hv; q += AB_THREADS) {
+        const int64_t row = (int64_t)j * c_max + r0 + q / hv;
         const int v = (int)(q % hv);
-        const int j = (int)(row / c_max);
-        const int64_t r = row % c_max;
-        if (r >= (int64_t)min(counts[j], c)) continue;
         const int64_t off = row * h + (int64_t)v * 8;
         float a[8], g[8], o[8];
-        Elt<__nv_bfloat16>::unpack(ld_v16(pa + off), a);
-        Elt<__nv_bfloat16>::unpack(ld_v16(dh + off), g);
+        Elt<__nv_bfloat16>::unpack(ld_stream(pa + off), a);
+        Elt<__nv_bfloat16>::unpack(ld_stream(dh + off), g);
         __nv_bfloat16 *dst = d_pre + row * h2 + (int64_t)v * 8;
         if (swiglu) {
             float b[8], ob[8];
-            Elt<__nv_bfloat16>::unpack(ld_v16(pb + off), b);
+            Elt<__nv_bfloat16>::unpack(ld_stream(pb + off), b);
 #pragma unroll
             for (int i = 0; i < 8; i++) {
                 const float sg = 1.0f / (1.0f + expf(-a[i]));
@@ -140,12 +153,14 @@ moe_status transpose_pad_launch(const __nv_bfloat16 *src, int64_t src_batch, int
                                 int batches, int rows, int cols, int dst_cols,
                                 const int32_t *counts, const int32_t *skip, const int32_t *c_dev,
                                 int32_t *status, cudaStream_t stream) {
-    if (batches < 1 || batches > 65535 || rows < 0 || cols < 1 || dst_cols < rows)
+    if (batches < 1 || batches > 65535 || rows < 0 || cols < 1 || dst_cols < rows ||
+        cols % 8 || dst_cols % 8 || src_pitch % 8 || dst_pitch % 8 || src_batch % 8 ||
+        dst_batch % 8 || !aligned16(src) || !aligned16(dst))
         return MOE_ERR_INVALID_ARG;
     const dim3 grid((unsigned)((dst_cols + TP - 1) / TP), (unsigned)((cols + TP - 1) / TP),
                     (unsigned)batches);
     if (grid.y > 65535) return MOE_ERR_UNSUPPORTED;
-    return launch_pdl(transpose_pad_kernel, grid, dim3(TP, TP_Y), 0, stream,
+    return launch_pdl(transpose_pad_kernel, grid, dim3(TP_THREADS), 0, stream,
                       (const uint16_t *)src, src_batch, src_pitch, (uint16_t *)dst, dst_batch,
                       dst_pitch, rows, cols, dst_cols, counts, skip, c_dev, status);
 }
@@ -154,17 +169,11 @@ moe_status act_bwd_launch(const __nv_bfloat16 *pa, const __nv_bfloat16 *pb,
                           const __nv_bfloat16 *d_hid, moe_act act, int e, int64_t c_max, int h,
                           const int32_t *counts, const int32_t *c_dev, __nv_bfloat16 *d_pre,
                           int32_t *status, cudaStream_t stream) {
-    if (h % 8 != 0) return MOE_ERR_INVALID_ARG;
-    const int64_t n = (int64_t)e * c_max * (h / 8);
-    int64_t blocks = (n + AB_THREADS - 1) / AB_THREADS;
-    int sms = 0, dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
-    if (blocks < 1) blocks = 1;
-    return launch_pdl(act_bwd_kernel, dim3((unsigned)blocks), dim3(AB_THREADS), 0, stream, pa, pb,
-                      d_hid, (int)act, e, c_max, h, counts, c_dev, d_pre, status);
+    if (h % 8 != 0 || e < 1 || e > 65535) return MOE_ERR_INVALID_ARG;
+    const int64_t gx = (c_max + AB_ROWS - 1) / AB_ROWS;
+    if (gx > 0x7fffffff) return MOE_ERR_UNSUPPORTED;
+    return launch_pdl(act_bwd_kernel, dim3((unsigned)gx, (unsigned)e), dim3(AB_THREADS), 0, stream,
+                      pa, pb, d_hid, (int)act, e, c_max, h, counts, c_dev, d_pre, status);
 }
 
 moe_status colsum_launch(const __nv_bfloat16 *src, int e, int64_t c_max, int cols,
