@@ -13,11 +13,11 @@
 //     gate_lane_kernel is exactly that: lane l of a warp owns chunk l of every
 //     512-byte slice of the feature axis.
 //   e > 32: one accumulator per logit from +0 in ascending feature index.
-//     gate_topk_kernel is a register-blocked SIMT GEMM: every thread owns TT
-//     tokens x TE experts, and each accumulator walks the features in order.
-//     (The lane-blocked order needs 32 live partial sums per logit; with all e
-//     experts of a token in one CTA, as the fused top-k needs, that leaves a
-//     CTA only a handful of tokens for large e.)
+//     gate_seq_kernel is a persistent register-blocked SIMT GEMM: warps own
+//     expert groups, lanes own tokens, and each accumulator walks the features
+//     in order.  (The lane-blocked order needs 32 live partial sums per logit;
+//     with all e experts of a token in one CTA, as the fused top-k needs, that
+//     leaves a CTA only a handful of tokens for large e.)
 // Tensor cores are not used: their internal accumulation order is unspecified
 // and would make routing irreproducible.
 #include "common.cuh"
@@ -43,241 +43,259 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// N consecutive floats from shared memory; 16-byte loads when N % 4 == 0
-// (callers pass 16-byte aligned addresses in that case).
-template <int N>
-__device__ __forceinline__ void lds_vec(float *dst, const float *src) {
-    if constexpr (N % 4 == 0) {
-#pragma unroll
-        for (int i = 0; i < N / 4; i++) {
-            float4 v = reinterpret_cast<const float4 *>(src)[i];
-            dst[4 * i] = v.x; dst[4 * i + 1] = v.y; dst[4 * i + 2] = v.z; dst[4 * i + 3] = v.w;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < N; i++) dst[i] = src[i];
-    }
+// Feature u (compile-time) of a 16-byte chunk, widened exactly to fp32.
+template <typename XT, int U>
+__device__ __forceinline__ float chunk_elem(const V16 &v) {
+    if constexpr (sizeof(XT) == 2)
+        return (U & 1) ? bf16hi(v.w[U >> 1]) : bf16lo(v.w[U >> 1]);
+    else
+        return __uint_as_float(v.w[U]);
 }
 
-template <int EP_, int TE_, int TT_, int NT_, int KT_, int ST_, typename XT>
-struct GateCfg {
-    static constexpr int KT = KT_;               // features per shared-memory tile
-    static constexpr int STAGES = ST_;           // cp.async pipeline depth
-    static constexpr int EP = EP_;               // experts per CTA (e padded)
-    static constexpr int TE = TE_;               // experts per thread
-    static constexpr int TT = TT_;               // tokens per thread
-    static constexpr int NT = NT_;               // threads per CTA
-    static constexpr int EX = EP / TE;           // threads along experts
-    static constexpr int TY = NT / EX;           // threads along tokens
-    static constexpr int TOKC = TY * TT;         // tokens per CTA
-    static constexpr int VEC = Elt<XT>::VEC;     // x elements per 16-byte chunk
-    static constexpr int XCH = KT / VEC;         // 16-byte chunks per token row per tile
-    static constexpr int XROW = KT * Elt<XT>::BYTES + 16;  // padded raw row (bytes)
-    static constexpr int XFS = TOKC + 4;         // fp32 x tile row stride (floats)
-    static constexpr int LGS = EP + 1;           // logits tile row stride
-    // shared memory (bytes): raw x ring, fp32 x tile, Wg ring
-    static constexpr int RAW_BYTES = STAGES * TOKC * XROW;
-    static constexpr int XF_BYTES = KT * XFS * 4;
-    static constexpr int WS_BYTES = STAGES * KT * EP * 4;
-    static constexpr int MAIN_BYTES = RAW_BYTES + XF_BYTES + WS_BYTES;
+// e > 32: a persistent CTA of NW warps computes chunks of TOKC tokens x all
+// EP experts, chunk after chunk.  The warps form WT token groups x WE expert
+// groups: warp (wt, we) owns experts [we*EW, (we+1)*EW) of the chunk's tokens
+// wt*32*TT + lane + 32*j (j < TT).  Per K tile of KT features the CTA stages
+// the chunk's x rows as they lie in memory (16 bytes = VEC features of one
+// token per load) and the tile's weight rows [KT][EP] in fp32; per feature, a
+// warp's weight loads are the same address in every lane (a broadcast), so
+// shared-memory traffic stays well below what the fp32 pipe consumes.  Two
+// experts' chains advance per packed fp32x2 fused multiply-add (each lane of
+// the pair rounds exactly as fmaf), so issue slots are left for the loads.
+// Every accumulator walks the features in ascending order.  After a chunk's
+// last tile the logits (+ bias) go to shared memory -- into the stage just
+// consumed when they fit there, which the next refill only reaches after the
+// next barrier -- and one warp per token does softmax and top-k, while the
+// next chunk's tiles are already in flight.
+template <int EP_, int EW_, int TT_, int NW_, int KT_, int ST_, typename XT>
+struct SeqCfg {
+    static constexpr int EP = EP_;                       // experts per CTA (e padded)
+    static constexpr int EW = EW_;                       // experts per warp
+    static constexpr int TT = TT_;                       // tokens per lane
+    static constexpr int NW = NW_;                       // warps per CTA
+    static constexpr int KT = KT_;                       // features per K tile
+    static constexpr int ST = ST_;                       // pipeline stages
+    static constexpr int NT = NW * 32;
+    static constexpr int WE = EP / EW;                   // warps along experts
+    static constexpr int WT = NW / WE;                   // warps along tokens
+    static constexpr int TOKC = WT * 32 * TT;            // tokens per chunk
+    static constexpr int VEC = Elt<XT>::VEC;             // features per 16-byte x load
+    static constexpr int XCH = KT / VEC;                 // 16-byte chunks per x row and tile
+    static constexpr int XROW = KT * Elt<XT>::BYTES + 16;  // padded x row (bytes)
+    static constexpr int X_BYTES = TOKC * XROW;
+    static constexpr int W_BYTES = KT * EP * 4;
+    static constexpr int STAGE = X_BYTES + W_BYTES;
+    static constexpr int LGS = EP + 1;                   // logits row stride (floats)
     static constexpr int LG_BYTES = TOKC * LGS * 4;
-    static constexpr int SMEM = MAIN_BYTES > LG_BYTES ? MAIN_BYTES : LG_BYTES;
-    static_assert(EP % TE == 0 && NT % EX == 0 && TE % 4 == 0 && STAGES >= 2, "layout");
-    static_assert(EP > 32, "e <= 32 uses the lane-blocked kernel (its logit order)");
+    static constexpr bool LG_IN_STAGE = LG_BYTES <= STAGE;
+    static constexpr int SMEM = ST * STAGE + (LG_IN_STAGE ? 0 : LG_BYTES);
+    static_assert(EP % EW == 0 && NW % WE == 0 && EW % 4 == 0 && EP > 32, "experts per warp");
+    static_assert(KT % VEC == 0 && X_BYTES % 16 == 0 && W_BYTES % 16 == 0 && ST >= 2, "stages");
 };
 
+// Stage one K tile of one chunk: x rows [t0, t0 + TOKC) x features [k0, k0 + KT)
+// and weight rows [k0, k0 + KT) (zero past s, m and e).
 template <class C, typename XT>
-__device__ __forceinline__ void load_tile(unsigned char *raw, float *ws, const XT *x, const float *wg,
-                                          int64_t s, int m, int e, int64_t t0, int k0, bool wg16) {
-    const int tid = threadIdx.x;
-    // x: TOKC rows x XCH chunks of 16 bytes
-    for (int q = tid; q < C::TOKC * C::XCH; q += C::NT) {
-        int row = q / C::XCH, ch = q % C::XCH;
-        int64_t t = t0 + row;
-        int f = k0 + ch * C::VEC;
-        bool ok = t < s && f < m;
-        const XT *src = ok ? x + t * m + f : x;
-        cp_async16(raw + row * C::XROW + ch * 16, src, ok);
+__device__ __forceinline__ void seq_load(unsigned char *st, const XT *x, const float *wg, int64_t s,
+                                         int m, int e, int64_t t0, int k0, bool wg16) {
+    for (int q = threadIdx.x; q < C::TOKC * C::XCH; q += C::NT) {
+        const int row = q / C::XCH, ch = q % C::XCH;
+        const int64_t t = t0 + row;
+        const int f = k0 + ch * C::VEC;
+        const bool ok = t < s && f < m;
+        cp_async16(st + row * C::XROW + ch * 16, ok ? (const void *)(x + t * m + f) : (const void *)x,
+                   ok);
     }
-    // Wg: KT rows x EP columns (zero beyond m rows / e columns)
-    constexpr int KT = C::KT;
+    float *ws = reinterpret_cast<float *>(st + C::X_BYTES);
     if (wg16) {
-        for (int q = tid; q < KT * (C::EP / 4); q += C::NT) {
-            int kk = q / (C::EP / 4), j = (q % (C::EP / 4)) * 4;
-            bool ok = k0 + kk < m && j < e;
-            const float *src = ok ? wg + (int64_t)(k0 + kk) * e + j : wg;
-            cp_async16(ws + kk * C::EP + j, src, ok);
+        for (int q = threadIdx.x; q < C::KT * (C::EP / 4); q += C::NT) {
+            const int kk = q / (C::EP / 4), j = (q % (C::EP / 4)) * 4;
+            const bool ok = k0 + kk < m && j < e;
+            cp_async16(ws + kk * C::EP + j, ok ? (const void *)(wg + (int64_t)(k0 + kk) * e + j)
+                                               : (const void *)wg, ok);
         }
     } else {
-        for (int q = tid; q < KT * C::EP; q += C::NT) {
-            int kk = q / C::EP, j = q % C::EP;
-            bool ok = k0 + kk < m && j < e;
-            const float *src = ok ? wg + (int64_t)(k0 + kk) * e + j : wg;
-            cp_async4(ws + kk * C::EP + j, src, ok);
+        for (int q = threadIdx.x; q < C::KT * C::EP; q += C::NT) {
+            const int kk = q / C::EP, j = q % C::EP;
+            const bool ok = k0 + kk < m && j < e;
+            cp_async4(ws + kk * C::EP + j, ok ? (const void *)(wg + (int64_t)(k0 + kk) * e + j)
+                                              : (const void *)wg, ok);
         }
     }
     cp_async_commit();
 }
 
+// One feature U (compile-time) of the lane's x chunks: acc[j][i..i+1] +=
+// x[token j][f] * w[f][expert i..i+1] for every token j and expert pair.
+template <class C, typename XT, int U>
+__device__ __forceinline__ void seq_feature(float2 (&acc)[C::TT][C::EW / 2], const V16 (&xv)[C::TT],
+                                            const float *wf) {
+    float2 w2[C::EW / 2];
+#pragma unroll
+    for (int q = 0; q < C::EW / 4; q++) {
+        const float4 w4 = reinterpret_cast<const float4 *>(wf)[q];   // same address in every lane
+        w2[2 * q] = make_float2(w4.x, w4.y);
+        w2[2 * q + 1] = make_float2(w4.z, w4.w);
+    }
+#pragma unroll
+    for (int j = 0; j < C::TT; j++) {
+        const float xf = chunk_elem<XT, U>(xv[j]);
+        const float2 x2 = make_float2(xf, xf);
+#pragma unroll
+        for (int i = 0; i < C::EW / 2; i++) acc[j][i] = __ffma2_rn(x2, w2[i], acc[j][i]);
+    }
+}
+
+template <class C, typename XT, int U>
+__device__ __forceinline__ void seq_group(float2 (&acc)[C::TT][C::EW / 2], const V16 (&xv)[C::TT],
+                                          const float *wg_tile) {
+    if constexpr (U < C::VEC) {
+        seq_feature<C, XT, U>(acc, xv, wg_tile + U * C::EP);
+        seq_group<C, XT, U + 1>(acc, xv, wg_tile);
+    }
+}
+
+// Softmax over the e logits of one token and top-k (ties -> lower index), one
+// warp; lane r < k writes route r.
+__device__ __forceinline__ void softmax_topk_warp(const float *row, int e, int k, int normalize,
+                                                  int64_t t, int64_t s, int32_t *idx, float *gates,
+                                                  int qe) {
+    const int lane = threadIdx.x & 31;
+    constexpr int QMAX = 8;                      // e <= 256
+    float v[QMAX];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < QMAX; q++) {
+        const int ex = lane + 32 * q;
+        v[q] = (q < qe && ex < e) ? row[ex] : -INFINITY;
+        mx = fmaxf(mx, v[q]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float z = 0.0f;
+#pragma unroll
+    for (int q = 0; q < QMAX; q++)
+        if (q < qe && lane + 32 * q < e) z += expf(v[q] - mx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    unsigned taken = 0;  // bit q: expert lane+32q already selected
+    float my_v = 0.0f;   // lane r keeps route r's logit and expert
+    int my_j = 0;
+    for (int r = 0; r < k; r++) {
+        float bv = -INFINITY;
+        int bj = 0x7fffffff;
+#pragma unroll
+        for (int q = 0; q < QMAX; q++) {
+            const int ex = lane + 32 * q;
+            const bool cand = q < qe && ex < e && !((taken >> q) & 1u);
+            if (cand && (v[q] > bv || (v[q] == bv && ex < bj))) { bv = v[q]; bj = ex; }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
+            if (ov > bv || (ov == bv && oj < bj)) { bv = ov; bj = oj; }
+        }
+        if ((bj & 31) == lane) taken |= 1u << (bj >> 5);
+        if (lane == r) { my_v = bv; my_j = bj; }
+    }
+    const float p = lane < k ? expf(my_v - mx) : 0.0f;
+    float g;
+    if (normalize) {
+        float sel = p;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sel += __shfl_xor_sync(0xffffffffu, sel, o);
+        g = p / sel;
+    } else {
+        g = p / z;
+    }
+    if (lane < k) {
+        idx[(int64_t)lane * s + t] = my_j;
+        gates[(int64_t)lane * s + t] = g;
+    }
+}
+
 template <class C, typename XT>
 __global__ void __launch_bounds__(C::NT)
-gate_topk_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
-                 const float *__restrict__ bias, int64_t s, int m, int e, int k, int normalize,
-                 int32_t *__restrict__ idx, float *__restrict__ gates, int32_t *status) {
+gate_seq_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
+                const float *__restrict__ bias, int64_t s, int m, int e, int k, int normalize,
+                int32_t *__restrict__ idx, float *__restrict__ gates, int32_t *status) {
     pdl_enter();
     if (status_bad(status)) return;
-    extern __shared__ __align__(16) unsigned char smem[];
-    unsigned char *raw = smem;                                   // [STAGES][TOKC][XROW]
-    float *xf = (float *)(smem + C::RAW_BYTES);                  // [KT][XFS]
-    float *ws = (float *)(smem + C::RAW_BYTES + C::XF_BYTES);    // [STAGES][KT][EP]
-
-    const int tid = threadIdx.x;
-    const int tx = tid % C::EX, ty = tid / C::EX;
-    const int64_t t0 = (int64_t)blockIdx.x * C::TOKC;
-    const bool wg16 = (e % 4) == 0;  // rows of wg start on 16-byte boundaries
-
-    float acc[C::TT][C::TE];
+    extern __shared__ __align__(16) unsigned char smem_seq[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int we = warp % C::WE, wt = warp / C::WE;   // expert group, token group
+    const int tok0 = wt * 32 * C::TT + lane;          // the lane's first token in a chunk
+    const bool wg16 = (e % 4) == 0;   // rows of wg start on 16-byte boundaries
+    const int ntiles = (m + C::KT - 1) / C::KT;
+    const int64_t nchunks = (s + C::TOKC - 1) / C::TOKC;
+    const int64_t my_chunks =
+        blockIdx.x < nchunks ? (nchunks - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const int64_t total = my_chunks * ntiles;   // (chunk, tile) steps of this CTA, flattened
+    auto issue = [&](int64_t q) {
+        const int64_t chunk = blockIdx.x + (q / ntiles) * (int64_t)gridDim.x;
+        const int kt = (int)(q % ntiles);
+        seq_load<C, XT>(smem_seq + (q % C::ST) * C::STAGE, x, wg, s, m, e, chunk * C::TOKC,
+                        kt * C::KT, wg16);
+    };
 #pragma unroll
-    for (int j = 0; j < C::TT; j++)
-#pragma unroll
-        for (int i = 0; i < C::TE; i++) acc[j][i] = 0.0f;
-
-    constexpr int KT = C::KT, ST = C::STAGES;
-    const int ntiles = (m + KT - 1) / KT;
-    // prologue: tiles 0 .. ST-2 in flight (one commit group per tile, empty groups past the end)
-#pragma unroll
-    for (int p = 0; p < ST - 1; p++) {
-        if (p < ntiles)
-            load_tile<C, XT>(raw + p * C::TOKC * C::XROW, ws + p * KT * C::EP, x, wg, s, m, e, t0,
-                             p * KT, wg16);
-        else
-            cp_async_commit();
+    for (int p = 0; p < C::ST - 1; p++) {
+        if (p < total) issue(p);
+        else cp_async_commit();
     }
-    for (int it = 0; it < ntiles; it++) {
-        const int cur = it % ST;
-        cp_async_wait<ST - 2>();
-        __syncthreads();  // tile `it` landed; everyone finished reading tile it-1 and xf
-        {
-            const int nx = it + ST - 1, nb = nx % ST;
-            if (nx < ntiles)
-                load_tile<C, XT>(raw + nb * C::TOKC * C::XROW, ws + nb * KT * C::EP, x, wg, s, m, e,
-                                 t0, nx * KT, wg16);
-            else
-                cp_async_commit();
+    float2 acc[C::TT][C::EW / 2];
+    const int qe = (e + 31) / 32;
+    for (int64_t q = 0; q < total; q++) {
+        cp_async_wait<C::ST - 2>();
+        __syncthreads();   // step q landed; step q-1 (and the previous softmax) fully read
+        if (q + C::ST - 1 < total) issue(q + C::ST - 1);
+        else cp_async_commit();
+        const int kt = (int)(q % ntiles);
+        if (kt == 0) {
+#pragma unroll
+            for (int j = 0; j < C::TT; j++)
+#pragma unroll
+                for (int i = 0; i < C::EW / 2; i++) acc[j][i] = make_float2(0.0f, 0.0f);
         }
-        // widen the raw x tile to fp32, transposed to [feature][token]
-        const unsigned char *rc = raw + cur * C::TOKC * C::XROW;
-        for (int q = tid; q < C::TOKC * C::XCH; q += C::NT) {
-            int row = q % C::TOKC, ch = q / C::TOKC;
-            V16 v = *(const V16 *)(rc + row * C::XROW + ch * 16);
-            float f[C::VEC];
-            Elt<XT>::unpack(v, f);
+        unsigned char *st = smem_seq + (q % C::ST) * C::STAGE;
+        const float *wtile = reinterpret_cast<const float *>(st + C::X_BYTES) + we * C::EW;
+        const int ngroups = min(C::KT, m - kt * C::KT) / C::VEC;   // m is a multiple of VEC
+#pragma unroll 1
+        for (int g = 0; g < ngroups; g++) {
+            V16 xv[C::TT];
 #pragma unroll
-            for (int u = 0; u < C::VEC; u++) xf[(ch * C::VEC + u) * C::XFS + row] = f[u];
+            for (int j = 0; j < C::TT; j++)
+                xv[j] = *reinterpret_cast<const V16 *>(st + (tok0 + 32 * j) * C::XROW + g * 16);
+            seq_group<C, XT, 0>(acc, xv, wtile + g * C::VEC * C::EP);
         }
-        __syncthreads();
-        const float *wc = ws + cur * KT * C::EP;
-        const int klim = min(KT, m - it * KT);
-        if (klim == KT) {
-#pragma unroll 4
-            for (int kk = 0; kk < KT; kk++) {
-                float xv[C::TT], wv[C::TE];
-                lds_vec<C::TT>(xv, xf + kk * C::XFS + ty * C::TT);
-                lds_vec<C::TE>(wv, wc + kk * C::EP + tx * C::TE);
+        if (kt == ntiles - 1) {
+            // the chunk's logits (+ bias: one fp32 add after the chain), in the
+            // stage just read once every warp is done with it
+            float *lg = reinterpret_cast<float *>(C::LG_IN_STAGE ? st : smem_seq + C::ST * C::STAGE);
+            if (C::LG_IN_STAGE) __syncthreads();
 #pragma unroll
-                for (int j = 0; j < C::TT; j++)
+            for (int j = 0; j < C::TT; j++)
 #pragma unroll
-                    for (int i = 0; i < C::TE; i++) acc[j][i] = fmaf(xv[j], wv[i], acc[j][i]);
-            }
-        } else {
-            for (int kk = 0; kk < klim; kk++) {
-                float xv[C::TT], wv[C::TE];
-                lds_vec<C::TT>(xv, xf + kk * C::XFS + ty * C::TT);
-                lds_vec<C::TE>(wv, wc + kk * C::EP + tx * C::TE);
-#pragma unroll
-                for (int j = 0; j < C::TT; j++)
-#pragma unroll
-                    for (int i = 0; i < C::TE; i++) acc[j][i] = fmaf(xv[j], wv[i], acc[j][i]);
+                for (int i = 0; i < C::EW / 2; i++) {
+                    const int ex = we * C::EW + 2 * i;
+                    float a = acc[j][i].x, b = acc[j][i].y;
+                    if (bias) {
+                        if (ex < e) a = a + bias[ex];
+                        if (ex + 1 < e) b = b + bias[ex + 1];
+                    }
+                    lg[(tok0 + 32 * j) * C::LGS + ex] = a;
+                    lg[(tok0 + 32 * j) * C::LGS + ex + 1] = b;
+                }
+            __syncthreads();
+            const int64_t t0 = (blockIdx.x + (q / ntiles) * (int64_t)gridDim.x) * C::TOKC;
+            for (int tl = warp; tl < C::TOKC; tl += C::NW) {
+                const int64_t t = t0 + tl;
+                if (t >= s) break;
+                softmax_topk_warp(lg + tl * C::LGS, e, k, normalize, t, s, idx, gates, qe);
             }
         }
     }
     cp_async_wait<0>();
-    __syncthreads();  // all reads of the tiles done before the logits overwrite them
-
-    float *lg = (float *)smem;  // [TOKC][LGS]
-#pragma unroll
-    for (int j = 0; j < C::TT; j++)
-#pragma unroll
-        for (int i = 0; i < C::TE; i++) {
-            int ex = tx * C::TE + i;
-            float v = acc[j][i];
-            if (bias && ex < e) v = v + bias[ex];
-            lg[(ty * C::TT + j) * C::LGS + ex] = v;
-        }
-    __syncthreads();
-
-    {
-        // softmax + top-k: one warp per token
-        constexpr int NW = C::NT / 32;
-        constexpr int QE = (C::EP + 31) / 32;  // experts per lane
-        const int lane = tid & 31, warp = tid >> 5;
-        for (int tl = warp; tl < C::TOKC; tl += NW) {
-            const int64_t t = t0 + tl;
-            if (t >= s) break;
-            float v[QE];
-            float mx = -INFINITY;
-#pragma unroll
-            for (int q = 0; q < QE; q++) {
-                int ex = lane + 32 * q;
-                v[q] = ex < e ? lg[tl * C::LGS + ex] : -INFINITY;
-                mx = fmaxf(mx, v[q]);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            float z = 0.0f;
-#pragma unroll
-            for (int q = 0; q < QE; q++)
-                if (lane + 32 * q < e) z += expf(v[q] - mx);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-
-            unsigned taken = 0;  // bit q: expert lane+32q already selected
-            float my_v = 0.0f;   // lane r keeps route r's logit and expert
-            int my_j = 0;
-            for (int r = 0; r < k; r++) {
-                float bv = -INFINITY;
-                int bj = 0x7fffffff;
-#pragma unroll
-                for (int q = 0; q < QE; q++) {
-                    int ex = lane + 32 * q;
-                    bool cand = ex < e && !((taken >> q) & 1u);
-                    if (cand && (v[q] > bv || (v[q] == bv && ex < bj))) { bv = v[q]; bj = ex; }
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                    int oj = __shfl_xor_sync(0xffffffffu, bj, o);
-                    if (ov > bv || (ov == bv && oj < bj)) { bv = ov; bj = oj; }
-                }
-                if ((bj & 31) == lane) taken |= 1u << (bj >> 5);
-                if (lane == r) { my_v = bv; my_j = bj; }
-            }
-            float p = lane < k ? expf(my_v - mx) : 0.0f;
-            float g;
-            if (normalize) {
-                float sel = p;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) sel += __shfl_xor_sync(0xffffffffu, sel, o);
-                g = p / sel;
-            } else {
-                g = p / z;
-            }
-            if (lane < k) {
-                idx[(int64_t)lane * s + t] = my_j;
-                gates[(int64_t)lane * s + t] = g;
-            }
-        }
-    }
 }
 
 // ---------------------------------------------------------------- small e
@@ -310,15 +328,6 @@ struct LaneCfg {
     static_assert(EP >= 4 && EP <= 32 && 64 % EP == 0, "experts per CTA");
     static_assert(XB % 16 == 0 && WB % 16 == 0, "16-byte stages");
 };
-
-// Feature u (compile-time) of a 16-byte chunk, widened exactly to fp32.
-template <typename XT, int U>
-__device__ __forceinline__ float chunk_elem(const V16 &v) {
-    if constexpr (sizeof(XT) == 2)
-        return (U & 1) ? bf16hi(v.w[U >> 1]) : bf16lo(v.w[U >> 1]);
-    else
-        return __uint_as_float(v.w[U]);
-}
 
 template <typename XT, int EP, int T, int U>
 __device__ __forceinline__ void lane_fma_feature(float (&acc)[T][EP], const V16 (&xv)[T],
@@ -479,10 +488,223 @@ gate_lane_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
     }
 }
 
+// The same lane-blocked order with the whole gate weight resident in shared
+// memory (when it fits): a persistent CTA loads Wg once, staged as
+// [tile][chunk][feature][expert] with every chunk block padded by 16 bytes,
+// and each warp then takes T-token groups in turn.  Each lane streams its own
+// 16-byte x chunks through a private RD-deep cp.async ring in shared memory
+// (a lane only ever reads what it copied itself, so no lane waits on another),
+// which keeps RD K tiles of every warp's tokens in flight.  The lane sums are
+// combined by a reduce-scatter form of the xor butterfly: at offset o a lane
+// keeps the half of its values selected by lane bit o and adds the partner's
+// copy of that half, so every logit is the same sum v[l] + v[l ^ o] at every
+// level as in the full butterfly, with a fifth of the shuffles; lane l ends
+// with the flattened (token, expert) values 2l and 2l + 1.
+constexpr int RW_MAX = 8;                 // warps per CTA (at most)
+constexpr int RD = 4;                     // K tiles of x in flight per warp
+constexpr size_t RES_SMEM_MAX = 220 * 1024;
+
+template <int EP, typename XT>
+struct ResCfg {
+    static constexpr int V = 16 / (int)sizeof(XT);
+    static constexpr int KS = 32 * V;
+    static constexpr int T = 64 / EP;
+    static constexpr int WCH = V * EP + 4;           // floats per chunk block (16-byte pad)
+    static constexpr int TILE_FLOATS = 32 * WCH;
+    static constexpr int RING_BYTES = RD * T * 32 * 16;   // per warp
+    static size_t smem(int m, int nw) {
+        return (size_t)((m + KS - 1) / KS) * TILE_FLOATS * 4 + (size_t)nw * (RING_BYTES + 64 * 4);
+    }
+};
+
+// Reduce-scatter step: n values -> n/2, lane bit `o` picks the kept half.
+template <int N, int O>
+__device__ __forceinline__ void rs_step(float (&v)[64], int lane) {
+    const bool hi = (lane & O) != 0;
+#pragma unroll
+    for (int i = 0; i < N / 2; i++) {
+        const float keep = hi ? v[N / 2 + i] : v[i];
+        const float give = hi ? v[i] : v[N / 2 + i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, give, O);
+    }
+}
+
+template <int EP, typename XT>
+__global__ void __launch_bounds__(RW_MAX * 32, 1)
+gate_lane_res_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
+                     const float *__restrict__ bias, int64_t s, int m, int e, int k, int normalize,
+                     int32_t *__restrict__ idx, float *__restrict__ gates, int32_t *status) {
+    pdl_enter();
+    if (status_bad(status)) return;
+    using C = ResCfg<EP, XT>;
+    constexpr int V = C::V, T = C::T;
+    const int nw = blockDim.x >> 5, nt = blockDim.x;
+    extern __shared__ __align__(16) unsigned char smem_res[];
+    float *wres = reinterpret_cast<float *>(smem_res);
+    const int ntiles = (m + C::KS - 1) / C::KS;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const size_t w_bytes = (size_t)ntiles * C::TILE_FLOATS * 4;
+    unsigned char *ring = smem_res + w_bytes + (size_t)warp * C::RING_BYTES;
+    float *lg = reinterpret_cast<float *>(smem_res + w_bytes + (size_t)nw * C::RING_BYTES) + warp * 64;
+    const int nch = m / V;                                       // m is a multiple of V
+    // the whole weight, zero past m features and e experts
+    if (e == EP) {
+        for (int q = threadIdx.x; q < ntiles * C::KS * (EP / 4); q += nt) {
+            const int g = q % (EP / 4), r = q / (EP / 4);          // r = feature
+            const int tile = r / C::KS, rr = r - tile * C::KS, ch = rr / V, u = rr - ch * V;
+            const bool ok = r < m;
+            cp_async16(wres + (size_t)tile * C::TILE_FLOATS + ch * C::WCH + u * EP + g * 4,
+                       ok ? (const void *)(wg + (int64_t)r * e + g * 4) : (const void *)wg, ok);
+        }
+    } else {
+        for (int q = threadIdx.x; q < ntiles * C::KS * EP; q += nt) {
+            const int jj = q % EP, r = q / EP;
+            const int tile = r / C::KS, rr = r - tile * C::KS, ch = rr / V, u = rr - ch * V;
+            const bool ok = r < m && jj < e;
+            cp_async4(wres + (size_t)tile * C::TILE_FLOATS + ch * C::WCH + u * EP + jj,
+                      ok ? (const void *)(wg + (int64_t)r * e + jj) : (const void *)wg, ok);
+        }
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+    const int64_t groups = (s + T - 1) / T;
+    const int64_t gstride = (int64_t)gridDim.x * nw;
+    const int64_t g0 = (int64_t)blockIdx.x * nw + warp;
+    const int64_t my_groups = g0 < groups ? (groups - g0 + gstride - 1) / gstride : 0;
+    const int64_t total = my_groups * ntiles;   // (group, tile) steps of this warp, flattened
+    // this lane's x chunks of step q: its chunk of the step's tile, every token of the group
+    auto issue = [&](int64_t q) {
+        const int64_t t0 = (g0 + (q / ntiles) * gstride) * T;
+        const int ch = (int)(q % ntiles) * 32 + lane;
+        unsigned char *slot = ring + (q % RD) * (T * 32 * 16);
+#pragma unroll
+        for (int tt = 0; tt < T; tt++) {
+            const bool ok = t0 + tt < s && ch < nch;
+            cp_async16(slot + (tt * 32 + lane) * 16,
+                       ok ? (const void *)(x + (t0 + tt) * m + (int64_t)ch * V) : (const void *)x, ok);
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int p = 0; p < RD - 1; p++) {
+        if (p < total) issue(p);
+        else cp_async_commit();
+    }
+    float acc[T][EP];
+    for (int64_t q = 0; q < total; q++) {
+        if (q + RD - 1 < total) issue(q + RD - 1);
+        else cp_async_commit();
+        cp_async_wait<RD - 1>();   // this lane's copies of step q have landed
+        const int tile = (int)(q % ntiles);
+        if (tile == 0) {
+#pragma unroll
+            for (int tt = 0; tt < T; tt++)
+#pragma unroll
+                for (int jj = 0; jj < EP; jj++) acc[tt][jj] = 0.0f;
+        }
+        if (tile * 32 + lane < nch) {   // this lane's chunk of the tile holds features
+            const unsigned char *slot = ring + (q % RD) * (T * 32 * 16);
+            V16 cur[T];
+#pragma unroll
+            for (int tt = 0; tt < T; tt++)
+                cur[tt] = *reinterpret_cast<const V16 *>(slot + (tt * 32 + lane) * 16);
+            lane_fma_chunk<XT, EP, T, 0, V>(acc, cur,
+                                            wres + (size_t)tile * C::TILE_FLOATS + lane * C::WCH);
+        }
+        if (tile != ntiles - 1) continue;
+        const int64_t t0 = (g0 + (q / ntiles) * gstride) * T;
+        // reduce-scatter over the lanes: lane l ends with flattened values 2l, 2l+1
+        float v[64];
+#pragma unroll
+        for (int tt = 0; tt < T; tt++)
+#pragma unroll
+            for (int jj = 0; jj < EP; jj++) v[tt * EP + jj] = acc[tt][jj];
+        rs_step<64, 16>(v, lane);
+        rs_step<32, 8>(v, lane);
+        rs_step<16, 4>(v, lane);
+        rs_step<8, 2>(v, lane);
+        rs_step<4, 1>(v, lane);
+        lg[2 * lane] = v[0];
+        lg[2 * lane + 1] = v[1];
+        __syncwarp();
+        if (lane < T && t0 + lane < s) {
+            const int64_t t = t0 + lane;
+            float row[EP];
+#pragma unroll
+            for (int jj = 0; jj < EP; jj++) row[jj] = lg[lane * EP + jj];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int jj = 0; jj < EP; jj++)
+                if (jj < e) {
+                    if (bias) row[jj] = row[jj] + bias[jj];
+                    mx = fmaxf(mx, row[jj]);
+                }
+            float z = 0.0f;
+#pragma unroll
+            for (int jj = 0; jj < EP; jj++)
+                if (jj < e) z += expf(row[jj] - mx);
+            float sel = 0.0f;
+            for (int pass = 0; pass < 2; pass++) {
+                uint32_t taken = 0;
+                for (int r = 0; r < k; r++) {
+                    int bj = -1;
+                    float bv = -INFINITY;
+#pragma unroll
+                    for (int jj = 0; jj < EP; jj++) {
+                        if (jj < e && !(taken & (1u << jj)) && (bj < 0 || row[jj] > bv)) {
+                            bv = row[jj];
+                            bj = jj;
+                        }
+                    }
+                    taken |= 1u << bj;
+                    const float p = expf(bv - mx);
+                    if (pass == 0) {
+                        sel += p;
+                    } else {
+                        idx[(int64_t)r * s + t] = bj;
+                        gates[(int64_t)r * s + t] = p / (normalize ? sel : z);
+                    }
+                }
+            }
+        }
+        __syncwarp();   // the warp's logits row is reused by its next group
+    }
+    cp_async_wait<0>();
+}
+
 template <int EP, typename XT>
 moe_status launch_lane(const void *x, const float *wg, const float *bias, int64_t s, int m, int e,
                        int k, int normalize, int32_t *idx, float *gates, int32_t *st,
                        cudaStream_t stream) {
+    // the gate weight resident in shared memory when it fits
+    {
+        using R = ResCfg<EP, XT>;
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (sms < 1) sms = 1;
+        const int64_t groups = (s + R::T - 1) / R::T;
+        // warps per CTA: enough to spread the groups over every SM, at most RW_MAX
+        int64_t nw = (groups + sms - 1) / sms;
+        nw = nw < 1 ? 1 : (nw > RW_MAX ? RW_MAX : nw);
+        const size_t res_smem = R::smem(m, (int)nw);
+        if (res_smem <= RES_SMEM_MAX) {
+            auto kern = gate_lane_res_kernel<EP, XT>;
+            static int smem_set[64] = {0};
+            if (dev >= 0 && dev < 64 && !smem_set[dev]) {
+                if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)RES_SMEM_MAX) != cudaSuccess)
+                    return MOE_ERR_CUDA;
+                smem_set[dev] = 1;
+            }
+            const int64_t want = (groups + nw - 1) / nw;
+            const int64_t grid = want < sms ? want : sms;
+            return launch_pdl(kern, dim3((unsigned)grid), dim3((unsigned)(nw * 32)), res_smem, stream,
+                              (const XT *)x, wg, bias, s, m, e, k, normalize, idx, gates, st);
+        }
+    }
     using C = LaneCfg<EP, XT>;
     auto kern = gate_lane_kernel<EP, XT>;
     if (C::SMEM > 48 * 1024 &&
@@ -496,17 +718,29 @@ moe_status launch_lane(const void *x, const float *wg, const float *bias, int64_
 }
 
 template <class C, typename XT>
-moe_status launch_cfg(const void *x, const float *wg, const float *bias, int64_t s, int m, int e,
+moe_status launch_seq(const void *x, const float *wg, const float *bias, int64_t s, int m, int e,
                       int k, int normalize, int32_t *idx, float *gates, int32_t *st,
                       cudaStream_t stream) {
-    auto kern = gate_topk_kernel<C, XT>;
-    if (C::SMEM > 48 * 1024) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
-            cudaSuccess)
+    auto kern = gate_seq_kernel<C, XT>;
+    static int slots[64] = {0};   // resident CTAs per device (persistent grid)
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    int nslot = dev >= 0 && dev < 64 ? slots[dev] : 0;
+    if (!nslot) {
+        if (C::SMEM > 48 * 1024 &&
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+                cudaSuccess)
             return MOE_ERR_CUDA;
+        int per_sm = 0, sms = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::NT, C::SMEM) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        nslot = (per_sm > 0 ? per_sm : 1) * (sms > 0 ? sms : 1);
+        if (dev >= 0 && dev < 64) slots[dev] = nslot;
     }
-    int64_t grid = (s + C::TOKC - 1) / C::TOKC;
-    if (grid > 0x7fffffff) return MOE_ERR_UNSUPPORTED;
+    const int64_t nchunks = (s + C::TOKC - 1) / C::TOKC;
+    const int64_t grid = nchunks < nslot ? nchunks : nslot;
     return launch_pdl(kern, dim3((unsigned)grid), dim3(C::NT), C::SMEM, stream, (const XT *)x, wg,
                       bias, s, m, e, k, normalize, idx, gates, st);
 }
@@ -515,19 +749,19 @@ template <typename XT>
 moe_status gate_dispatch(const void *x, const float *wg, const float *bias, int64_t s, int m, int e,
                          int k, int normalize, int32_t *idx, float *gates, int32_t *st,
                          cudaStream_t stream) {
-#define MOE_GATE_CASE(EPV, TEV, TTV, NTV, KTV, STV)                                        \
+#define MOE_GATE_CASE(EPV, EWV, TTV, NWV, KTV, STV)                                          \
     if (e <= EPV)                                                                           \
-        return launch_cfg<GateCfg<EPV, TEV, TTV, NTV, KTV, STV, XT>, XT>(                   \
+        return launch_seq<SeqCfg<EPV, EWV, TTV, NWV, KTV, STV, XT>, XT>(                    \
             x, wg, bias, s, m, e, k, normalize, idx, gates, st, stream);
     // e <= 32: lane-blocked order, all experts of a token in one warp
     if (e <= 4) return launch_lane<4, XT>(x, wg, bias, s, m, e, k, normalize, idx, gates, st, stream);
     if (e <= 8) return launch_lane<8, XT>(x, wg, bias, s, m, e, k, normalize, idx, gates, st, stream);
     if (e <= 16) return launch_lane<16, XT>(x, wg, bias, s, m, e, k, normalize, idx, gates, st, stream);
     if (e <= 32) return launch_lane<32, XT>(x, wg, bias, s, m, e, k, normalize, idx, gates, st, stream);
-    // e > 32: fp32-FMA bound -> register-blocked 8x8 micro-tiles, sequential order
-    MOE_GATE_CASE(64, 8, 8, 128, 32, 3)
-    MOE_GATE_CASE(128, 8, 8, 256, 32, 2)
-    MOE_GATE_CASE(256, 8, 8, 256, 32, 2)
+    // e > 32: fp32-FMA bound, sequential order; experts per warp x tokens per lane
+    MOE_GATE_CASE(64, 16, 2, 4, 64, 3)
+    MOE_GATE_CASE(128, 16, 2, 8, 64, 3)
+    MOE_GATE_CASE(256, 16, 4, 16, 32, 2)
 #undef MOE_GATE_CASE
     return MOE_ERR_UNSUPPORTED;
 }
