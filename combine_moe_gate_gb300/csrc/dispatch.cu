@@ -19,7 +19,6 @@ namespace moe {
 namespace {
 
 constexpr int DNT = 256;  // threads per CTA (8 token-warps)
-constexpr int UNR = 4;    // 16-byte chunks per lane per batch (decode backward)
 constexpr int SL = 128;   // 16-byte chunks of a row per warp in encode: 4 per lane
 
 struct Routes {
@@ -28,26 +27,49 @@ struct Routes {
     float g;         // lane r: route r's gate
 };
 
-__device__ __forceinline__ Routes load_routes(const int32_t *idx, const int32_t *loc,
-                                              const float *gates, int64_t s, int64_t t, int m,
-                                              int e, int k, int c_eff, int64_t c_max,
-                                              int32_t *status) {
+// Route entries of token t as stored (lane r < k holds route r's), not yet
+// checked; a separate step so that the next item's entries can be in flight
+// while the current item's rows move.
+struct RawRoute {
+    int ex, l;
+    float g;
+};
+
+__device__ __forceinline__ RawRoute fetch_route(const int32_t *idx, const int32_t *loc,
+                                                const float *gates, int64_t s, int64_t t, int k) {
+    const int lane = threadIdx.x & 31;
+    RawRoute q{-1, -1, 0.0f};
+    if (lane < k && t < s) {
+        q.ex = idx[(int64_t)lane * s + t];
+        q.l = loc[(int64_t)lane * s + t];
+        if (gates) q.g = gates[(int64_t)lane * s + t];
+    }
+    return q;
+}
+
+__device__ __forceinline__ Routes decide_routes(const RawRoute &q, int m, int e, int k, int c_eff,
+                                                int64_t c_max, int32_t *status) {
     const int lane = threadIdx.x & 31;
     Routes R{0u, 0, 0.0f};
     bool kept = false;
     if (lane < k) {
-        int ex = idx[(int64_t)lane * s + t];
-        int l = loc[(int64_t)lane * s + t];
-        if ((unsigned)ex >= (unsigned)e || l < 0) {
+        if ((unsigned)q.ex >= (unsigned)e || q.l < 0) {
             set_status(status, MOE_ERR_INVALID_ARG);
-        } else if (l < c_eff) {
+        } else if (q.l < c_eff) {
             kept = true;
-            R.row = ((int64_t)ex * c_max + l) * m;
-            if (gates) R.g = gates[(int64_t)lane * s + t];
+            R.row = ((int64_t)q.ex * c_max + q.l) * m;
+            R.g = q.g;
         }
     }
     R.kept = __ballot_sync(0xffffffffu, kept);
     return R;
+}
+
+__device__ __forceinline__ Routes load_routes(const int32_t *idx, const int32_t *loc,
+                                              const float *gates, int64_t s, int64_t t, int m,
+                                              int e, int k, int c_eff, int64_t c_max,
+                                              int32_t *status) {
+    return decide_routes(fetch_route(idx, loc, gates, s, t, k), m, e, k, c_eff, c_max, status);
 }
 
 __device__ __forceinline__ int read_c(const int32_t *c_dev, int64_t c_max) {
@@ -134,11 +156,15 @@ combine_kernel(const T *__restrict__ src, const int32_t *__restrict__ idx,
     const int nsl = (nch + SLU - 1) / SLU;
     const int64_t items = s * nsl;
     const int64_t nw = (int64_t)gridDim.x * (DNT / 32);
-    for (int64_t it = blockIdx.x * (DNT / 32) + (threadIdx.x >> 5); it < items; it += nw) {
+    int64_t it = blockIdx.x * (DNT / 32) + (threadIdx.x >> 5);
+    RawRoute nxt = fetch_route(idx, loc, WEIGHTED ? gates : nullptr, s, it / nsl, k);
+    for (; it < items; it += nw) {
         const int64_t t = it / nsl;
         const int c0 = (int)(it % nsl) * SLU + lane;
-        Routes R = load_routes(idx, loc, WEIGHTED ? gates : nullptr, s, t, m, e, k, c_eff, c_max,
-                               status);
+        const RawRoute cur = nxt;
+        // the next item's route entries travel while this item's rows move
+        nxt = fetch_route(idx, loc, WEIGHTED ? gates : nullptr, s, (it + nw) / nsl, k);
+        Routes R = decide_routes(cur, m, e, k, c_eff, c_max, status);
         V16 *dst = reinterpret_cast<V16 *>(y + t * m);
         float acc[ONE ? 1 : U][VEC];
         if (!ONE) {
@@ -229,8 +255,33 @@ template <> struct ScaleRound<__nv_bfloat16> {
 };
 
 // -------------------------------------------- decode backward (K1 bwd + K2)
+// One warp per (token, route) pair, token-major (a token's routes are
+// neighbouring items, so its dY row is re-read from cache): dG of the route is
+// a dot product over the whole row kept in one warp, so its summation order is
+// fixed (each lane sums its chunks in row order, then an xor butterfly), and
+// dE = g*dY is stored as the row goes by.  The row is walked in stretches of
+// 32*DU chunks, the next stretch's dY and expert-output chunks loaded before
+// the current one is used; the next item's route entry is fetched while this
+// item's rows move.
+constexpr int DU = 2;   // 16-byte chunks per lane per stretch
+
+struct DbStretch {
+    V16 dv[DU];
+    V16 ov[DU];
+};
+
+__device__ __forceinline__ void db_load(DbStretch &b, const V16 *dyp, const V16 *op, int q0,
+                                        int nch) {
+#pragma unroll
+    for (int u = 0; u < DU; u++)
+        if (q0 + 32 * u < nch) {
+            b.dv[u] = ld_v16(dyp + q0 + 32 * u);   // kept in cache for the token's other routes
+            b.ov[u] = ld_stream(op + q0 + 32 * u);
+        }
+}
+
 template <typename T>
-__global__ void __launch_bounds__(DNT)
+__global__ void __launch_bounds__(DNT, 4)
 decode_bwd_kernel(const T *__restrict__ dy, const T *__restrict__ out,
                   const int32_t *__restrict__ idx, const int32_t *__restrict__ loc,
                   const float *__restrict__ gates, const int32_t *__restrict__ c_dev, int64_t s,
@@ -239,46 +290,69 @@ decode_bwd_kernel(const T *__restrict__ dy, const T *__restrict__ out,
     pdl_enter();
     if (status_bad(status)) return;
     constexpr int VEC = Elt<T>::VEC;
+    constexpr int SW = 32 * DU;   // chunks per stretch
     const int c_eff = read_c(c_dev, c_max);
     const int lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * (DNT / 32);
     const int nch = m / VEC;
-    for (int64_t t = blockIdx.x * (DNT / 32) + (threadIdx.x >> 5); t < s; t += nw) {
-        Routes R = load_routes(idx, loc, gates, s, t, m, e, k, c_eff, c_max, status);
-        if (lane < k && !((R.kept >> lane) & 1u)) d_gates[(int64_t)lane * s + t] = 0.0f;
-        if (!R.kept) continue;
-        const V16 *dyp = reinterpret_cast<const V16 *>(dy + t * m);
-        for (unsigned km = R.kept; km; km &= km - 1) {
-            int r = __ffs(km) - 1;
-            int64_t row = __shfl_sync(0xffffffffu, R.row, r);
-            float g = __shfl_sync(0xffffffffu, R.g, r);
-            const V16 *op = reinterpret_cast<const V16 *>(out + row);
-            V16 *dp = reinterpret_cast<V16 *>(d_out + row);
-            float part = 0.0f;
-            for (int base = 0; base < nch; base += 32 * UNR) {
-                const int q0 = base + lane;
-                V16 dv[UNR], ov[UNR];
-#pragma unroll
-                for (int u = 0; u < UNR; u++)
-                    if (q0 + 32 * u < nch) {
-                        dv[u] = ld_v16(dyp + q0 + 32 * u);  // re-read per route: keep in L1
-                        ov[u] = ld_stream(op + q0 + 32 * u);
-                    }
-#pragma unroll
-                for (int u = 0; u < UNR; u++)
-                    if (q0 + 32 * u < nch) {
-                        float a[VEC], b[VEC];
-                        Elt<T>::unpack(dv[u], a);
-                        Elt<T>::unpack(ov[u], b);
-#pragma unroll
-                        for (int i = 0; i < VEC; i++) part = __fmaf_rn(a[i], b[i], part);
-                        st_v16(dp + q0 + 32 * u, ScaleRound<T>::apply(g, dv[u]));
-                    }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-            if (lane == 0) d_gates[(int64_t)r * s + t] = part;
+    const int64_t items = s * k;
+    // item q = (token q / k, route q % k); lane 0 fetches the route's entry
+    auto fetch = [&](int64_t q, int &ex, int &l, float &g) {
+        ex = -1; l = -1; g = 0.0f;
+        if (lane == 0 && q < items) {
+            const int64_t off = (q % k) * s + q / k;
+            ex = idx[off];
+            l = loc[off];
+            g = gates[off];
         }
+    };
+    int64_t q = blockIdx.x * (DNT / 32) + (threadIdx.x >> 5);
+    int nex, nl;
+    float ng;
+    fetch(q, nex, nl, ng);
+    for (; q < items; q += nw) {
+        const int64_t t = q / k;
+        const int r = (int)(q % k);
+        int ex = __shfl_sync(0xffffffffu, nex, 0), l = __shfl_sync(0xffffffffu, nl, 0);
+        const float g = __shfl_sync(0xffffffffu, ng, 0);
+        fetch(q + nw, nex, nl, ng);   // the next item's entry travels meanwhile
+        if ((unsigned)ex >= (unsigned)e || l < 0) {
+            if (lane == 0) set_status(status, MOE_ERR_INVALID_ARG);
+            continue;
+        }
+        if (l >= c_eff) {   // dropped: no gradient
+            if (lane == 0) d_gates[(int64_t)r * s + t] = 0.0f;
+            continue;
+        }
+        const int64_t row = ((int64_t)ex * c_max + l) * m;
+        const V16 *dyp = reinterpret_cast<const V16 *>(dy + t * m);
+        const V16 *op = reinterpret_cast<const V16 *>(out + row);
+        V16 *dp = reinterpret_cast<V16 *>(d_out + row);
+        float part = 0.0f;
+        auto use = [&](const DbStretch &b, int q0) {
+#pragma unroll
+            for (int u = 0; u < DU; u++)
+                if (q0 + 32 * u < nch) {
+                    float a[VEC], bb[VEC];
+                    Elt<T>::unpack(b.dv[u], a);
+                    Elt<T>::unpack(b.ov[u], bb);
+#pragma unroll
+                    for (int i = 0; i < VEC; i++) part = __fmaf_rn(a[i], bb[i], part);
+                    st_v16(dp + q0 + 32 * u, ScaleRound<T>::apply(g, b.dv[u]));
+                }
+        };
+        // two named stretch buffers, the loop unrolled by two
+        DbStretch b0, b1;
+        db_load(b0, dyp, op, lane, nch);
+        for (int base = 0; base < nch; base += 2 * SW) {
+            if (base + SW < nch) db_load(b1, dyp, op, base + SW + lane, nch);
+            use(b0, base + lane);
+            if (base + 2 * SW < nch) db_load(b0, dyp, op, base + 2 * SW + lane, nch);
+            if (base + SW < nch) use(b1, base + SW + lane);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) d_gates[(int64_t)r * s + t] = part;
     }
 }
 
@@ -303,7 +377,6 @@ int grid_for_items(int64_t items) {
     return (int)(want < 1 ? 1 : (want < cap ? want : cap));
 }
 
-int grid_for_tokens(int64_t s) { return grid_for_items(s); }
 
 int64_t row_slices(int m, moe_dtype dt) {
     const int nch = m / (dt == MOE_BF16 ? 8 : 4);
@@ -354,6 +427,11 @@ moe_status combine_typed(const void *src, const int32_t *idx, const int32_t *loc
         return launch_pdl(combine_kernel<T, W, 4, 2, true>, dim3(grid_for_items(items)), b, 0, stream,
                           sp, idx, loc, gates, c_dev, s, m, e, k, c_max, yp, st);
     }
+    if (k <= 4) {  // all routes in one group: 2 chunks per lane, 8 live accumulators
+        const int64_t items = s * ((nch + 63) / 64);
+        return launch_pdl(combine_kernel<T, W, 2, 4, true>, dim3(grid_for_items(items)), b, 0, stream,
+                          sp, idx, loc, gates, c_dev, s, m, e, k, c_max, yp, st);
+    }
     const int64_t items = s * ((nch + 63) / 64);
     return launch_pdl(combine_kernel<T, W, 2, 4, false>, dim3(grid_for_items(items)), b, 0, stream,
                       sp, idx, loc, gates, c_dev, s, m, e, k, c_max, yp, st);
@@ -387,7 +465,7 @@ moe_status decode_bwd_launch(const void *dy, const void *out, moe_dtype dt, cons
                            m, (float *)d_out, st);
         if (r != MOE_OK) return r;
     }
-    const int grid = grid_for_tokens(s);
+    const int grid = grid_for_items(s * k);
     if (dt == MOE_BF16)
         return launch_pdl(decode_bwd_kernel<__nv_bfloat16>, dim3(grid), dim3(DNT), 0, stream,
                           (const __nv_bfloat16 *)dy, (const __nv_bfloat16 *)out, idx, loc, gates,
