@@ -59,6 +59,9 @@ CONFIGS = {
     "bf16_e256_swiglu": (W.BF16_E256_SWIGLU, None),
     # sweep point p = 3*8 + 1*2 + 0: s=65536, f=2, uniform; the sweep shares weight seed 0
     "sweep_s65536_f2": (W.sweep_points()[26], 0),
+    # the same expert shape (m=4096, h=8192, about 2048 rows per expert) with 8 experts:
+    # the s=65536 layer's kernels at 1/8 of the work, small enough for multi-pass profiling
+    "sweep_shape_e8": (W.sweep_points()[26].with_(s=8192, e=8), 0),
 }
 HEADLINE = "sweep_s65536_f2"
 GRADED = ("bf16_e16", "bf16_e256_swiglu")
@@ -76,6 +79,9 @@ def parse(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graded", action="store_true",
                     help="skip the stage breakdowns of the other graded workloads")
+    ap.add_argument("--only", choices=["gate"],
+                    help="time one stage alone on the config's inputs (its own JSON line, not the "
+                         "layer's): only the tensors that stage reads are drawn")
     return ap.parse_args(argv)
 
 
@@ -724,6 +730,43 @@ def run_ours(args, rank, world, local_rank):
     return res
 
 
+def run_only_gate(args):
+    """The gate alone on the config's x, gate weight and bias: mean event time
+    over args.steps calls, L2 flushed before each."""
+    import torch
+
+    import combine_moe_gate_gb300 as M
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w, _ = CONFIGS[args.config]
+    inp = synth.make_inputs_device(w, dev, parts=("x", "wg", "bias"))
+    idx = torch.empty((w.k, w.s), dtype=torch.int32, device=dev)
+    g = torch.empty((w.k, w.s), dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flags = M.MOE_FLAG_NORMALIZE_GATES if w.normalize_gates and w.k >= 2 else 0
+    fn = lambda: M.moe_gate_topk(inp["x"], inp["wg"], inp["bias"], w.k, idx, g, st, flags=flags)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        fn()
+    torch.cuda.synchronize()
+    tot = 0.0
+    for _ in range(args.steps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        tot += a.elapsed_time(b)
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+    ms = tot / args.steps
+    return {"stage": "gate", "workload": w.name, "ms": ms, "steps": args.steps,
+            "fp32_tflops": 2.0 * w.s * w.m * w.e / (ms * 1e-3) / 1e12}
+
+
 def run_reference(args):
     """The CPU oracle as the reference arm: each step is a bounded token sample."""
     import oracle
@@ -764,6 +807,10 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)))
+        return
+    if args.only == "gate":
+        if rank == 0:
+            print(json.dumps(run_only_gate(args)))
         return
     if world > 1:
         import torch
