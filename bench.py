@@ -431,6 +431,27 @@ class LayerRun:
         loc = b.loc.cpu().numpy()
         return c, int(kept.sum()), int(((loc < c).any(0)).sum()), int((kept > 0).sum())
 
+    def pipelined(self, chunks_list, steps, warmup):
+        """The forward with the capacity dimension cut into d chunks (encode of
+        chunk i+1 on a side stream overlapping the FFN of chunk i), d in
+        chunks_list: mean ms per call, L2 flushed before each."""
+        torch, M, w, b = self.torch, self.M, self.w, self.bufs
+        aux = torch.cuda.Stream(device=self.dev)
+        x, wg, gb, w1, b1, w3, w2, b2 = self.args()
+        res = {}
+        for d in chunks_list:
+            events = [torch.cuda.Event() for _ in range(d + 1)]
+
+            def fn():
+                M.moe_layer_forward_pipelined(x, wg, gb, w1, b1, w3, w2, b2, w.act, w.k,
+                                              w.capacity_factor, self.flags, b.idx, b.gates, b.loc,
+                                              b.counts, b.c_dev, b.buf, b.out, b.y, b.workspace,
+                                              b.status, d, aux, events)
+
+            res[str(d)] = self.time_calls(fn, steps, warmup)
+        self.check_status()
+        return res
+
     def dispatch_backward(self, steps, warmup):
         """decode backward (dE, dG from dY) and encode backward (dX from dBuf
         := dE) on the forward just timed, each alone."""
@@ -660,6 +681,8 @@ def run_ours(args, rank, world, local_rank):
     # ---- decode and encode backward on this workload (timed alone, not part of
     # the step): dE and dG from a dY of the batch's shape, then dX from dBuf := dE
     bw = run.dispatch_backward(args.steps, 3)
+    # ---- capacity-dimension pipelining (not the headline: the same layer, chunked)
+    pipe = run.pipelined([2, 4, 8], max(5, min(args.steps, 30)), 3)
 
     c, R, t1, hit = run.routing_summary()
     work = stage_work(w, R, t1, hit)
@@ -695,6 +718,9 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": ffn_traffic_from_profile(w.name), "traffic_unit": "bytes per call"},
         "stages": stages,
         "fp32_fma_tflops": dict(fp32, source="moe_probe_fp32_fma on this GPU, best of 5"),
+        "pipelining": dict({"single_pass_ms": ms_step}, **{f"chunks_{d}_ms": v for d, v in pipe.items()},
+                           note="moe_layer_forward_pipelined: encode of capacity chunk i+1 on a side "
+                                "stream overlaps the FFN of chunk i; results bit-identical"),
         "e2e": {"value": job_throughput(world, w.s, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": y_hosts[0].numel() * y_hosts[0].element_size(),
@@ -720,6 +746,11 @@ def run_ours(args, rank, world, local_rank):
             sm = g.time_stages(gsteps, 3)
             extra = g.backward_chain(gsteps, 3, pk) if gw.backward else None
             graded[name] = graded_report(name, g, sm, pk, extra)
+            if gw.backward:
+                single = g.time_calls(g.whole_step, gsteps, 3)
+                graded[name]["pipelining"] = dict({"single_pass_ms": single},
+                                                  **{f"chunks_{d}_ms": v for d, v in
+                                                     g.pipelined([2, 4, 8], gsteps, 3).items()})
             rank_free(g)
             g = None
         res["graded"] = graded

@@ -67,6 +67,8 @@ def load():
                                   P, P, P, P, P, P, P, P, P, SZ, P, P]),
         "moe_layer_forward_host": (I, [P, P, P, I, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, I64,
                                        U, P, P, P, P, P, P, P, P, P, SZ, P, P]),
+        "moe_layer_forward_pipelined": (I, [P, I, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, I64,
+                                            U, P, P, P, P, P, P, P, P, P, SZ, P, I, P, P, P]),
         "moe_probe_fp32_fma": (I, [I, I, I, P, P]),
         "moe_status_str": (ctypes.c_char_p, [I]),
         "moe_launch_count": (ctypes.c_uint64, []),
@@ -357,6 +359,42 @@ def moe_layer_forward_host(x_host, y_host, x, wg, gate_bias, w1, b1, w3, w2, b2,
         _ptr(out, "out", dt, (e, c_max, m)), _ptr(y, "y", dt, (s, m)), _ptr(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _ptr(dev_status, "dev_status", I),
         _stream(stream)), "moe_layer_forward_host")
+
+
+def moe_layer_forward_pipelined(x, wg, gate_bias, w1, b1, w3, w2, b2, act, k, capacity_factor,
+                                flags, idx, gates, loc, counts, c_dev, buf, out, y, workspace,
+                                dev_status, chunks, aux_stream, events, stream=None):
+    """moe_layer_forward with encode of capacity chunk i+1 (on aux_stream)
+    overlapping the FFN of chunk i (on stream); events: 1 + chunks
+    torch.cuda.Event objects."""
+    s, m = x.shape
+    e, c_max, _ = buf.shape
+    h = w1.shape[1]
+    k, chunks = int(k), int(chunks)
+    if len(events) < chunks + 1:
+        raise ValueError(f"events: need {chunks + 1}, got {len(events)}")
+    for ev in events[:chunks + 1]:   # the handles exist once the events are recorded or created
+        if getattr(ev, "cuda_event", 0) == 0:
+            ev.record(torch_current_stream())
+    handles = (ctypes.c_void_p * (chunks + 1))(*[ctypes.c_void_p(ev.cuda_event) for ev in
+                                                 events[:chunks + 1]])
+    I, F, dt = _i32(), _f32(), x.dtype
+    _check(load().moe_layer_forward_pipelined(
+        _ptr(x, "x"), _dt(x), _ptr(wg, "wg", F, (m, e)), _ptr(gate_bias, "gate_bias", F, (e,)),
+        _ptr(w1, "w1", dt, (e, h, m)), _ptr(b1, "b1", dt, (e, h)), _ptr(w3, "w3", dt, (e, h, m)),
+        _ptr(w2, "w2", dt, (e, m, h)), _ptr(b2, "b2", dt, (e, m)), _act(act), s, m, e, k, h,
+        float(capacity_factor), c_max, int(flags), _ptr(idx, "idx", I, (k, s)),
+        _ptr(gates, "gates", F, (k, s)), _ptr(loc, "loc", I, (k, s)),
+        _ptr(counts, "counts", I, (e,)), _ptr(c_dev, "c_dev", I), _ptr(buf, "buf", dt, (e, c_max, m)),
+        _ptr(out, "out", dt, (e, c_max, m)), _ptr(y, "y", dt, (s, m)), _ptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status, "dev_status", I), chunks,
+        _stream(stream), _stream(aux_stream), handles), "moe_layer_forward_pipelined")
+
+
+def torch_current_stream():
+    import torch
+
+    return torch.cuda.current_stream()
 
 
 def moe_probe_fp32_fma(packed, blocks, iters, out, stream=None):

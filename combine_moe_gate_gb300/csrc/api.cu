@@ -24,7 +24,7 @@ moe_status capacity_launch(const int32_t *idx, int64_t s, int e, int k, float f,
 moe_status encode_launch(const void *x, moe_dtype dt, const int32_t *idx, const int32_t *loc,
                          const int32_t *counts, const int32_t *c_dev, int64_t s, int m, int e,
                          int k, int64_t c_max, unsigned flags, void *buf, int32_t *st,
-                         cudaStream_t stream);
+                         cudaStream_t stream, int lo, int hi);
 moe_status combine_launch(const void *src, moe_dtype dt, const int32_t *idx, const int32_t *loc,
                           const float *gates, const int32_t *c_dev, int64_t s, int m, int e, int k,
                           int64_t c_max, void *y, int32_t *st, cudaStream_t stream);
@@ -42,7 +42,8 @@ bool ffn_tc_supported(int e, int64_t c_max, int m, int h);
 moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *c_dev,
                          const void *w1, const void *b1, const void *w3, const void *w2,
                          const void *b2, moe_act act, int e, int64_t c_max, int m, int h,
-                         void *hid, void *out, int32_t *st, cudaStream_t stream);
+                         void *hid, void *out, int32_t *st, cudaStream_t stream, int row_lo,
+                         int row_hi);
 size_t ffn_tc_bwd_workspace_bytes(moe_act act, int e, int64_t c_max, int m, int h);
 moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *counts,
                              const int32_t *c_dev, const void *w1, const void *b1, const void *w3,
@@ -166,7 +167,7 @@ moe_status moe_encode(const void *x, moe_dtype dt, const int32_t *idx, const int
         (flags & ~3u) || ((flags & MOE_FLAG_ZERO_FILL) && !ok4(counts)))
         return MOE_ERR_INVALID_ARG;
     return encode_launch(x, dt, idx, loc, counts, c_dev, s, m, e, k, c_max, flags, buf, dev_status,
-                         as_stream(stream));
+                         as_stream(stream), 0, 0x7fffffff);
 }
 
 size_t moe_expert_ffn_workspace_size(moe_dtype dt, moe_act act, int e, int64_t c_max, int m,
@@ -195,7 +196,7 @@ moe_status moe_expert_ffn(const void *buf, moe_dtype dt, const int32_t *counts,
     if (dt == MOE_BF16) {
         if (!ffn_tc_supported(e, c_max, m, h)) return MOE_ERR_UNSUPPORTED;
         return ffn_tc_launch(buf, counts, c_dev, w1, b1, w3, w2, b2, act, e, c_max, m, h,
-                             workspace, out, dev_status, as_stream(stream));
+                             workspace, out, dev_status, as_stream(stream), 0, 0);
     }
     return ffn_simt_launch(buf, dt, counts, c_dev, w1, b1, w3, w2, b2, act, e, c_max, m, h,
                            workspace, out, dev_status, as_stream(stream));
@@ -338,6 +339,72 @@ moe_status moe_layer_forward_host(const void *x_host, void *y_host, const void *
         return MOE_ERR_CUDA;
     }
     return MOE_OK;
+}
+
+moe_status moe_layer_forward_pipelined(const void *x, moe_dtype dt, const float *wg,
+                                       const float *gate_bias, const void *w1, const void *b1,
+                                       const void *w3, const void *w2, const void *b2, moe_act act,
+                                       int64_t s, int m, int e, int k, int h, float capacity_factor,
+                                       int64_t c_max, unsigned flags, int32_t *idx, float *gates,
+                                       int32_t *loc, int32_t *counts, int32_t *c_dev, void *buf,
+                                       void *out, void *y, void *workspace, size_t workspace_bytes,
+                                       int32_t *dev_status, int chunks, void *stream,
+                                       void *aux_stream, void *const *events) {
+    if (chunks < 1 || chunks > 64 || events == nullptr) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i <= chunks; i++)
+        if (events[i] == nullptr) return MOE_ERR_INVALID_ARG;
+    if (dt != MOE_BF16 || chunks == 1)
+        return moe_layer_forward(x, dt, wg, gate_bias, w1, b1, w3, w2, b2, act, s, m, e, k, h,
+                                 capacity_factor, c_max, flags, idx, gates, loc, counts, c_dev, buf,
+                                 out, y, workspace, workspace_bytes, dev_status, stream);
+    size_t need = moe_layer_workspace_size(dt, act, s, m, e, k, c_max, h);
+    if (need == 0 || workspace_bytes < need || !ok16(workspace)) return MOE_ERR_INVALID_ARG;
+    // every stage's own checks, by the calls below, before anything is launched
+    if (!routing_shape_ok(s, e, k) || !rows_ok(dt, m) || !rows_ok(dt, h) || c_max < 1 ||
+        c_max > 0x7fffffff || !ok16(x) || !ok16(wg) || !opt16(gate_bias) || !ok4(idx) ||
+        !ok4(gates) || !ok4(loc) || !ok4(counts) || !ok4(c_dev) || !ok16(buf) || !ok16(out) ||
+        !ok16(y) || !ok4(dev_status) || !ok16(w1) || !ok16(w2) || !opt16(b1) || !opt16(b2) ||
+        (flags & ~3u) || (act != MOE_ACT_RELU && act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU) ||
+        (act == MOE_ACT_SWIGLU && (!ok16(w3) || b1 != nullptr || b2 != nullptr)))
+        return MOE_ERR_INVALID_ARG;
+    if (e > 256 || !ffn_tc_supported(e, c_max, m, h)) return MOE_ERR_UNSUPPORTED;
+    const size_t cap_b = up256(moe_capacity_workspace_size(s, e, k));
+    char *ws = (char *)workspace;
+    cudaStream_t st = as_stream(stream), aux = as_stream(aux_stream);
+    cudaEvent_t *ev = (cudaEvent_t *)events;
+    moe_status r;
+    r = moe_gate_topk(x, dt, wg, gate_bias, s, m, e, k, flags & MOE_FLAG_NORMALIZE_GATES, idx, gates,
+                      dev_status, stream);
+    if (r != MOE_OK) return r;
+    r = moe_capacity_locations(idx, s, e, k, capacity_factor, c_max, ws, cap_b, loc, counts, c_dev,
+                               dev_status, stream);
+    if (r != MOE_OK) return r;
+    if (cudaEventRecord(ev[0], st) != cudaSuccess || cudaStreamWaitEvent(aux, ev[0], 0) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    // slot chunks [lo, hi) of the expert buffer, in whole 256-row FFN tiles
+    const int64_t step = ((c_max + chunks - 1) / chunks + 255) / 256 * 256;
+    for (int i = 0; i < chunks; i++) {
+        const int64_t lo = (int64_t)i * step, hi = lo + step;
+        if (lo >= c_max) break;
+        const int ihi = hi >= c_max ? 0x7fffffff : (int)hi;
+        // encode of chunk i on the side stream (zero fill, if asked, with the first)
+        r = encode_launch(x, dt, idx, loc, counts, c_dev, s, m, e, k, c_max,
+                          i == 0 ? (flags & MOE_FLAG_ZERO_FILL) : 0u, buf, dev_status, aux, (int)lo,
+                          ihi);
+        if (r != MOE_OK) return r;
+        if (cudaEventRecord(ev[1 + i], aux) != cudaSuccess ||
+            cudaStreamWaitEvent(st, ev[1 + i], 0) != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+        // the FFN of chunk i on the main stream, while chunk i+1 is encoded
+        r = ffn_tc_launch(buf, counts, c_dev, w1, b1, w3, w2, b2, act, e, c_max, m, h, ws + cap_b,
+                          out, dev_status, st, (int)lo, hi >= c_max ? 0 : (int)hi);
+        if (r != MOE_OK) return r;
+    }
+    return moe_decode(out, dt, idx, loc, gates, c_dev, s, m, e, k, c_max, y, dev_status, stream);
 }
 
 moe_status moe_probe_fp32_fma(int packed, int blocks, int iters, float *out, void *stream) {

@@ -48,14 +48,15 @@ __device__ __forceinline__ RawRoute fetch_route(const int32_t *idx, const int32_
 }
 
 __device__ __forceinline__ Routes decide_routes(const RawRoute &q, int m, int e, int k, int c_eff,
-                                                int64_t c_max, int32_t *status) {
+                                                int64_t c_max, int32_t *status, int lo = 0,
+                                                int hi = 0x7fffffff) {
     const int lane = threadIdx.x & 31;
     Routes R{0u, 0, 0.0f};
     bool kept = false;
     if (lane < k) {
         if ((unsigned)q.ex >= (unsigned)e || q.l < 0) {
             set_status(status, MOE_ERR_INVALID_ARG);
-        } else if (q.l < c_eff) {
+        } else if (q.l < c_eff && q.l >= lo && q.l < hi) {
             kept = true;
             R.row = ((int64_t)q.ex * c_max + q.l) * m;
             R.g = q.g;
@@ -68,8 +69,9 @@ __device__ __forceinline__ Routes decide_routes(const RawRoute &q, int m, int e,
 __device__ __forceinline__ Routes load_routes(const int32_t *idx, const int32_t *loc,
                                               const float *gates, int64_t s, int64_t t, int m,
                                               int e, int k, int c_eff, int64_t c_max,
-                                              int32_t *status) {
-    return decide_routes(fetch_route(idx, loc, gates, s, t, k), m, e, k, c_eff, c_max, status);
+                                              int32_t *status, int lo = 0, int hi = 0x7fffffff) {
+    return decide_routes(fetch_route(idx, loc, gates, s, t, k), m, e, k, c_eff, c_max, status, lo,
+                         hi);
 }
 
 __device__ __forceinline__ int read_c(const int32_t *c_dev, int64_t c_max) {
@@ -85,7 +87,8 @@ template <typename T>
 __global__ void __launch_bounds__(DNT, 4)
 encode_kernel(const T *__restrict__ x, const int32_t *__restrict__ idx,
               const int32_t *__restrict__ loc, const int32_t *__restrict__ c_dev, int64_t s,
-              int m, int e, int k, int64_t c_max, T *__restrict__ buf, int32_t *status) {
+              int m, int e, int k, int64_t c_max, T *__restrict__ buf, int32_t *status, int lo,
+              int hi) {
     pdl_enter();
     if (status_bad(status)) return;
     const int c_eff = read_c(c_dev, c_max);
@@ -102,7 +105,7 @@ encode_kernel(const T *__restrict__ x, const int32_t *__restrict__ idx,
 #pragma unroll
         for (int u = 0; u < SL / 32; u++)
             if (c0 + 32 * u < nch) v[u] = ld_stream(src + c0 + 32 * u);
-        Routes R = load_routes(idx, loc, nullptr, s, t, m, e, k, c_eff, c_max, status);
+        Routes R = load_routes(idx, loc, nullptr, s, t, m, e, k, c_eff, c_max, status, lo, hi);
         for (unsigned km = R.kept; km; km &= km - 1) {
             const int r = __ffs(km) - 1;
             const int64_t row = __shfl_sync(0xffffffffu, R.row, r);
@@ -388,16 +391,16 @@ int64_t row_slices(int m, moe_dtype dt) {
 moe_status encode_launch(const void *x, moe_dtype dt, const int32_t *idx, const int32_t *loc,
                          const int32_t *counts, const int32_t *c_dev, int64_t s, int m, int e,
                          int k, int64_t c_max, unsigned flags, void *buf, int32_t *st,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, int lo, int hi) {
     const int grid = grid_for_items(s * row_slices(m, dt));
     moe_status r;
     if (dt == MOE_BF16)
         r = launch_pdl(encode_kernel<__nv_bfloat16>, dim3(grid), dim3(DNT), 0, stream,
                        (const __nv_bfloat16 *)x, idx, loc, c_dev, s, m, e, k, c_max,
-                       (__nv_bfloat16 *)buf, st);
+                       (__nv_bfloat16 *)buf, st, lo, hi);
     else
         r = launch_pdl(encode_kernel<float>, dim3(grid), dim3(DNT), 0, stream, (const float *)x, idx,
-                       loc, c_dev, s, m, e, k, c_max, (float *)buf, st);
+                       loc, c_dev, s, m, e, k, c_max, (float *)buf, st, lo, hi);
     if (r != MOE_OK) return r;
     if (flags & MOE_FLAG_ZERO_FILL) {
         int64_t gx = (c_max + (DNT / 32) - 1) / (DNT / 32);

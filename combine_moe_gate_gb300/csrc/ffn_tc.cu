@@ -139,6 +139,10 @@ struct GemmArgs {
     // gets a zero output tile and no MMA.
     const int32_t *k_counts;
     const int32_t *k_cdev;
+    // Row range (forward only): expert rows [row_lo, row_hi) of the kept rows
+    // are computed (row_hi = 0: no upper end); rows are addressed from row_lo.
+    int row_lo;
+    int row_hi;
 };
 
 // ------------------------------------------------------------- PTX wrappers
@@ -525,6 +529,10 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         for (int base = 0; base < e; base += 32) {
             int j = base + lane;
             int rows = j >= e ? 0 : kmode ? urows : min(max(args.counts[j], 0), c_eff);
+            if (!kmode && j < e) {   // the kept rows inside [row_lo, row_hi)
+                const int hi = args.row_hi > 0 ? min(rows, args.row_hi) : rows;
+                rows = max(0, hi - args.row_lo);
+            }
             if (j < e) kept_rows[j] = kmode ? min(max(args.k_counts[j], 0), k_eff) : rows;
             const int own = ((rows + BMT - 1) / BMT) * ntn;
             int v = own;
@@ -600,7 +608,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         for (int t = tile0; t < total; t += tile_step) {
             Tile T = decode_tile(ctl->tile_start, e, t, BMT, kept_rows, urows, nk, BK);
             // A: this CTA's 128 rows, half of them per producer
-            const int a_row = (int)((int64_t)T.j * args.c_max + (int64_t)T.mt * BMT +
+            const int a_row = (int)((int64_t)T.j * args.c_max + args.row_lo + (int64_t)T.mt * BMT +
                                     (int64_t)prank * TL::A_ROWS + (int64_t)hh * TL::A_BOX_ROWS);
             // B rows of this CTA: its half of the (each) N = 256 sub-tile; with
             // TN = 2 producer hh loads N sub-tile hh
@@ -734,9 +742,9 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             const int row = T.mt * BMT + row_in_tile;
             const bool valid = row < T.rows;
             const bool all_kept = row - lane + 31 < T.rows;  // the warp's 32 rows
-            const int64_t grow0 = (int64_t)T.j * args.c_max + row - lane;
+            const int64_t grow0 = (int64_t)T.j * args.c_max + args.row_lo + row - lane;
             __nv_bfloat16 *orow =
-                args.out + ((int64_t)T.j * args.c_max + row) * (int64_t)args.n_out;
+                args.out + ((int64_t)T.j * args.c_max + args.row_lo + row) * (int64_t)args.n_out;
             const __nv_bfloat16 *brow = args.bias ? args.bias + (int64_t)T.j * args.n_out : nullptr;
             const uint32_t tbase = tmem + ((uint32_t)(sub * 32) << 16) +
                                    (uint32_t)(acc * TL::ACC_COLS + (TM == 2 ? half * BN : 0));
@@ -987,7 +995,8 @@ bool ffn_tc_supported(int e, int64_t c_max, int m, int h) {
 moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *c_dev,
                          const void *w1, const void *b1, const void *w3, const void *w2,
                          const void *b2, moe_act act, int e, int64_t c_max, int m, int h,
-                         void *hid, void *out, int32_t *st, cudaStream_t stream) {
+                         void *hid, void *out, int32_t *st, cudaStream_t stream, int row_lo,
+                         int row_hi) {
     // fc1: 256-row tiles on CTA pairs (2-SM MMA), two accumulators per CTA so
     // its activation epilogue overlaps the next tile's main loop.
     // fc2 (bias-only epilogue, long K, about one tile per pair): 256 x 512
@@ -1009,14 +1018,16 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
         !make_map(&mO1, hid, (uint64_t)e * c_max, (uint64_t)h, 32, 32) ||
         !make_map(&mO2, out, (uint64_t)e * c_max, (uint64_t)m, 32, 32))
         return MOE_ERR_CUDA;
-    GemmArgs g1{counts, c_dev, st, (const __nv_bfloat16 *)b1, (__nv_bfloat16 *)hid, c_max, e, m, h, h};
+    GemmArgs g1{counts, c_dev, st, (const __nv_bfloat16 *)b1, (__nv_bfloat16 *)hid, c_max, e, m, h, h,
+                nullptr, nullptr, row_lo, row_hi};
     moe_status r;
     if (swiglu) r = launch_gemm<EPI_SWIGLU, TM1, BK1, CL1, 1>(mA1, mB1, mB3, mO1, g1, stream);
     else if (act == MOE_ACT_GELU)
         r = launch_gemm<EPI_GELU, TM1, BK1, CL1, 1>(mA1, mB1, mB1, mO1, g1, stream);
     else r = launch_gemm<EPI_RELU, TM1, BK1, CL1, 1>(mA1, mB1, mB1, mO1, g1, stream);
     if (r != MOE_OK) return r;
-    GemmArgs g2{counts, c_dev, st, (const __nv_bfloat16 *)b2, (__nv_bfloat16 *)out, c_max, e, h, m, m};
+    GemmArgs g2{counts, c_dev, st, (const __nv_bfloat16 *)b2, (__nv_bfloat16 *)out, c_max, e, h, m, m,
+                nullptr, nullptr, row_lo, row_hi};
     return launch_gemm<EPI_BIAS, TM2, BK2, CL2, TN2>(mA2, mB2, mB2, mO2, g2, stream);
 }
 
@@ -1085,7 +1096,7 @@ moe_status gemm_bias(const void *a, const void *b, int b_rows, void *out, const 
         !make_map(&mO, out, (uint64_t)e * c_max, (uint64_t)n_out, 32, 32))
         return MOE_ERR_CUDA;
     GemmArgs g{counts, c_dev, st, (const __nv_bfloat16 *)bias, (__nv_bfloat16 *)out, c_max, e, K,
-               n_out, b_rows, k_counts, k_cdev};
+               n_out, b_rows, k_counts, k_cdev, 0, 0};
     return launch_gemm<EPI_BIAS, 1, 64, 2, 2>(mA, mB, mB, mO, g, stream);
 }
 

@@ -320,6 +320,30 @@ moe_status moe_layer_forward_host(const void *x_host, void *y_host, const void *
                                   size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
+ * moe_layer_forward with the capacity dimension cut into `chunks` pieces so
+ * that encoding one piece overlaps the expert FFN of the previous one (the
+ * one-GPU form of the adaptive pipelining in [Blog] 3.4, which overlaps
+ * all-to-all with expert computation by splitting the capacity dimension):
+ * gate and capacity run on `stream`; slot rows [i*q, (i+1)*q) of every expert
+ * (q = c_max / chunks rounded up to 256 rows) are encoded on `aux_stream` and
+ * run through the FFN on `stream` once their encode is done; decode follows
+ * on `stream` (a token's routes may fall in different pieces).  Results are
+ * bit-identical to moe_layer_forward.  events: 1 + chunks cudaEvent_t handles
+ * (passed as void*) created by the caller, used for the cross-stream order;
+ * aux_stream may equal stream (no overlap).  bf16 only (fp32, or chunks = 1:
+ * the single pass).  1 <= chunks <= 64.  The caller synchronises `stream`.
+ */
+moe_status moe_layer_forward_pipelined(const void *x, moe_dtype dt, const float *wg,
+                                       const float *gate_bias, const void *w1, const void *b1,
+                                       const void *w3, const void *w2, const void *b2, moe_act act,
+                                       int64_t s, int m, int e, int k, int h, float capacity_factor,
+                                       int64_t c_max, unsigned flags, int32_t *idx, float *gates,
+                                       int32_t *loc, int32_t *counts, int32_t *c_dev, void *buf,
+                                       void *out, void *y, void *workspace, size_t workspace_bytes,
+                                       int32_t *dev_status, int chunks, void *stream,
+                                       void *aux_stream, void *const *events);
+
+/*
  * Measurement helper, not part of the layer: launches `blocks` CTAs of 256
  * threads, each thread running 8 independent two-wide chains of `iters` fp32
  * fused multiply-adds (packed fp32x2 FMA when `packed`, else scalar pairs),

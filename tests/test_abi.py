@@ -105,6 +105,21 @@ def test_invalid_arguments_are_rejected_before_launch():
     for i in (0, 6, 7, 8, 9):                                    # idx, loc, counts, c_dev, status
         assert nac(**{f"a{i}": None}) == INV
         assert nac(**{f"a{i}": ctypes.c_void_p(0x30002)}) == INV # not 4-byte aligned
+    # the pipelined layer: ..., dev_status, chunks, stream, aux_stream, events
+    pl = lib.moe_layer_forward_pipelined
+    ev = (ctypes.c_void_p * 3)(A, B, A)
+    pok = [A, M.MOE_BF16, B, None, A, None, None, A, None, 1, 64, 64, 8, 2, 128, 1.0, 16, 0,
+           A, B, A, B, A, A, B, A, A, 1 << 30, A, 2, None, None, ev]
+    def plc(**kw):
+        a = list(pok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return pl(*a)
+    assert plc(a29=0) == INV and plc(a29=65) == INV             # chunks outside [1, 64]
+    assert plc(a32=None) == INV                                  # events required
+    assert plc(a32=(ctypes.c_void_p * 3)(A, None, A)) == INV     # every event required
+    assert plc(a27=0) == INV                                     # workspace too small
+    assert plc(a0=odd) == INV and plc(a25=odd) == INV            # misaligned x / y
     ffn = lib.moe_expert_ffn
     # SwiGLU takes no biases and needs w3
     assert ffn(A, M.MOE_BF16, A, A, A, B, A, A, None, 2, 4, 64, 64, 64, A, 1 << 30, A, A, None) == INV

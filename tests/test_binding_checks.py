@@ -143,6 +143,12 @@ def test_well_formed_calls_pass_and_marshal_their_sizes(stub):
                    d_x=z(s, m))
     M.moe_layer_forward(x, wg, gb, w1, b1, None, w2, b2, "gelu", k, 1.25, 1, idx, gates, loc,
                         counts, c_dev, buf, out, z(s, m, dtype=bf), ws, st)
+    class _Ev:
+        cuda_event = 1
+
+    M.moe_layer_forward_pipelined(x, wg, gb, w1, b1, None, w2, b2, "gelu", k, 1.25, 1, idx, gates,
+                                  loc, counts, c_dev, buf, out, z(s, m, dtype=bf), ws, st, 3, None,
+                                  [_Ev()] * 4)
     M.moe_expert_ffn_bwd(buf, z(e, c_max, h, dtype=bf), counts, c_dev, w1, b1, None, w2, "gelu",
                          z(e, c_max, m, dtype=bf), ws, z(e, c_max, m, dtype=bf), z(e, h, m, dtype=bf),
                          None, z(e, m, h, dtype=bf), z(e, h, dtype=bf), z(e, m, dtype=bf), st)
@@ -160,3 +166,9 @@ def test_well_formed_calls_pass_and_marshal_their_sizes(stub):
     assert c["moe_gate_bwd"][4:8] == (s, m, e, k)
     assert c["moe_layer_forward"][10:15] == (s, m, e, k, h)
     assert c["moe_layer_forward"][16] == c_max
+    assert c["moe_layer_forward_pipelined"][10:15] == (s, m, e, k, h)
+    assert c["moe_layer_forward_pipelined"][16] == c_max and c["moe_layer_forward_pipelined"][29] == 3
+    with pytest.raises(ValueError, match="events: need 4"):
+        M.moe_layer_forward_pipelined(x, wg, gb, w1, b1, None, w2, b2, "gelu", k, 1.25, 1, idx,
+                                      gates, loc, counts, c_dev, buf, out, z(s, m, dtype=bf), ws, st,
+                                      3, None, [_Ev()] * 3)
