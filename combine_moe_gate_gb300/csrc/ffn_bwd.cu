@@ -15,10 +15,17 @@ namespace {
 // A CTA moves a 64 x 64 tile: 16-byte loads of source rows into shared
 // memory, then each thread gathers 8 elements of a source column and stores
 // them as one 16-byte piece of a destination row.  Row lengths, pitches and
-// offsets are multiples of 8 elements (16 bytes).
+// offsets are multiples of 8 elements (16 bytes).  In shared memory the
+// 16-byte chunks of tile row r are permuted by chunk ^ ((r / 8) % 8), so the
+// column gathers of eight lanes, from rows 8 apart, fall in eight different
+// banks.
 constexpr int TP = 64, TP_THREADS = 256;
-constexpr int TP_PITCH = TP + 8;   // shared row pitch (elements): 144 bytes, conflict-free columns
 constexpr int PAD_TO = 64;         // K block of the weight-gradient GEMMs
+constexpr int TP_GRID_X = 16;      // CTAs per (column block, batch) striding over row blocks
+
+__device__ __forceinline__ int tp_col(int r, int c) {   // shared column of tile element (r, c)
+    return ((((c >> 3) ^ (r >> 3)) & 7) << 3) | (c & 7);
+}
 
 __global__ void __launch_bounds__(TP_THREADS)
 transpose_pad_kernel(const uint16_t *__restrict__ src, int64_t src_batch, int64_t src_pitch,
@@ -28,40 +35,79 @@ transpose_pad_kernel(const uint16_t *__restrict__ src, int64_t src_batch, int64_
                      int32_t *status) {
     pdl_enter();
     if (status_bad(status)) return;
-    __shared__ __align__(16) uint16_t tile[TP][TP_PITCH];
+    __shared__ __align__(16) uint16_t tile[TP][TP];
     const int b = blockIdx.z;
     if (skip && min(skip[b], *c_dev) <= 0) return;   // block-uniform
-    const int r0 = blockIdx.x * TP, c0 = blockIdx.y * TP;
+    const int c0 = blockIdx.y * TP;
     int kept = rows;
     if (counts) kept = max(0, min(min(counts[b], *c_dev), rows));
     // zeros are written up to the next multiple of PAD_TO past the kept rows
-    // (the consumer reads no further); block-uniform exit past that
+    // (the consumer reads no further); the CTAs of a batch stride over the row
+    // blocks up to there (the grid is sized for c_max rows, most of which are
+    // usually not kept)
     const int pad_end = counts ? min(dst_cols, (kept + PAD_TO - 1) / PAD_TO * PAD_TO) : dst_cols;
-    if (r0 >= pad_end) return;
     const uint16_t *sb = src + (int64_t)b * src_batch;
     uint16_t *db = dst + (int64_t)b * dst_batch;
-    for (int i = threadIdx.x; i < TP * (TP / 8); i += TP_THREADS) {
-        const int r = i >> 3, c = (i & 7) * 8;
-        V16 v;
-        v.w[0] = v.w[1] = v.w[2] = v.w[3] = 0u;
-        if (r0 + r < kept && c0 + c < cols) v = ld_stream(sb + (int64_t)(r0 + r) * src_pitch + c0 + c);
-        *reinterpret_cast<V16 *>(&tile[r][c]) = v;
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < TP * (TP / 8); i += TP_THREADS) {
-        const int c = i >> 3, r = (i & 7) * 8;   // destination row c0 + c, columns r0 + r ..
-        if (c0 + c >= cols || r0 + r >= pad_end) continue;
-        V16 v;
+    for (int r0 = blockIdx.x * TP; r0 < pad_end; r0 += gridDim.x * TP) {
+        __syncthreads();   // the previous block's gathers are done with the tile
+        for (int i = threadIdx.x; i < TP * (TP / 8); i += TP_THREADS) {
+            const int r = i >> 3, c = (i & 7) * 8;
+            V16 v;
+            v.w[0] = v.w[1] = v.w[2] = v.w[3] = 0u;
+            if (r0 + r < kept && c0 + c < cols) v = ld_stream(sb + (int64_t)(r0 + r) * src_pitch + c0 + c);
+            *reinterpret_cast<V16 *>(&tile[r][tp_col(r, c)]) = v;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < TP * (TP / 8); i += TP_THREADS) {
+            const int c = i >> 3, r = (i & 7) * 8;   // destination row c0 + c, columns r0 + r ..
+            if (c0 + c >= cols || r0 + r >= pad_end) continue;
+            V16 v;
 #pragma unroll
-        for (int u = 0; u < 4; u++)
-            v.w[u] = (uint32_t)tile[r + 2 * u][c] | ((uint32_t)tile[r + 2 * u + 1][c] << 16);
-        st_v16(db + (int64_t)(c0 + c) * dst_pitch + r0 + r, v);
+            for (int u = 0; u < 4; u++)
+                v.w[u] = (uint32_t)tile[r + 2 * u][tp_col(r + 2 * u, c)] |
+                         ((uint32_t)tile[r + 2 * u + 1][tp_col(r + 2 * u + 1, c)] << 16);
+            st_v16(db + (int64_t)(c0 + c) * dst_pitch + r0 + r, v);
+        }
     }
 }
 
 // ---------------------------------------------------- activation backward
 constexpr int AB_THREADS = 256;
 constexpr int AB_ROWS = 16;   // rows of one expert per CTA
+constexpr int AB_U = 4;       // 16-byte chunks per thread in flight together
+constexpr int AB_GRID_X = 32; // CTAs per expert
+
+__device__ __forceinline__ void act_bwd_chunk(const V16 &pa, const V16 &pb, const V16 &dh, int act,
+                                              __nv_bfloat16 *dst, int h) {
+    float a[8], g[8], o[8];
+    Elt<__nv_bfloat16>::unpack(pa, a);
+    Elt<__nv_bfloat16>::unpack(dh, g);
+    if (act == MOE_ACT_SWIGLU) {
+        float b[8], ob[8];
+        Elt<__nv_bfloat16>::unpack(pb, b);
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const float sg = 1.0f / (1.0f + expf(-a[i]));
+            o[i] = g[i] * b[i] * sg * (1.0f + a[i] * (1.0f - sg));   // d_a
+            ob[i] = g[i] * a[i] * sg;                                // d_b
+        }
+        st_v16(dst, Elt<__nv_bfloat16>::pack(o));
+        st_v16(dst + h, Elt<__nv_bfloat16>::pack(ob));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            float dact;
+            if (act == MOE_ACT_RELU) {
+                dact = a[i] > 0.0f ? 1.0f : 0.0f;
+            } else {
+                // GELU'(z) = Phi(z) + z phi(z); 0.3989... = 1 / sqrt(2 pi)
+                dact = normcdff(a[i]) + a[i] * expf(-0.5f * a[i] * a[i]) * 0.3989422804014327f;
+            }
+            o[i] = g[i] * dact;
+        }
+        st_v16(dst, Elt<__nv_bfloat16>::pack(o));
+    }
+}
 
 __global__ void __launch_bounds__(AB_THREADS)
 act_bwd_kernel(const __nv_bfloat16 *__restrict__ pa, const __nv_bfloat16 *__restrict__ pb,
@@ -73,43 +119,34 @@ act_bwd_kernel(const __nv_bfloat16 *__restrict__ pa, const __nv_bfloat16 *__rest
     const bool swiglu = act == MOE_ACT_SWIGLU;
     const int j = blockIdx.y;
     const int64_t kept = min((int64_t)min(counts[j], *c_dev), c_max);
-    const int64_t r0 = (int64_t)blockIdx.x * AB_ROWS;
-    if (r0 >= kept) return;                                // block-uniform
     const int hv = h / 8;                                  // 16-byte chunks per row
     const int64_t h2 = swiglu ? 2 * (int64_t)h : (int64_t)h;
-    const int64_t nrow = min((int64_t)AB_ROWS, kept - r0);
-    for (int64_t q = threadIdx.x; q < nrow * hv; q += AB_THREADS) {
-        const int64_t row = (int64_t)j * c_max + r0 + q / hv;
-        const int v = (int)(q % hv);
-        const int64_t off = row * h + (int64_t)v * 8;
-        float a[8], g[8], o[8];
-        Elt<__nv_bfloat16>::unpack(ld_stream(pa + off), a);
-        Elt<__nv_bfloat16>::unpack(ld_stream(dh + off), g);
-        __nv_bfloat16 *dst = d_pre + row * h2 + (int64_t)v * 8;
-        if (swiglu) {
-            float b[8], ob[8];
-            Elt<__nv_bfloat16>::unpack(ld_stream(pb + off), b);
+    // the CTAs of an expert stride over its kept rows, AB_ROWS at a time
+    for (int64_t r0 = (int64_t)blockIdx.x * AB_ROWS; r0 < kept;
+         r0 += (int64_t)gridDim.x * AB_ROWS) {
+        const int64_t nrow = min((int64_t)AB_ROWS, kept - r0);
+        const int64_t n = nrow * hv;
+        for (int64_t q0 = threadIdx.x; q0 < n; q0 += (int64_t)AB_THREADS * AB_U) {
+            V16 va[AB_U], vb[AB_U], vg[AB_U];
+            // every load of the batch in flight before any arithmetic
 #pragma unroll
-            for (int i = 0; i < 8; i++) {
-                const float sg = 1.0f / (1.0f + expf(-a[i]));
-                o[i] = g[i] * b[i] * sg * (1.0f + a[i] * (1.0f - sg));   // d_a
-                ob[i] = g[i] * a[i] * sg;                                // d_b
-            }
-            st_v16(dst, Elt<__nv_bfloat16>::pack(o));
-            st_v16(dst + h, Elt<__nv_bfloat16>::pack(ob));
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; i++) {
-                float dact;
-                if (act == MOE_ACT_RELU) {
-                    dact = a[i] > 0.0f ? 1.0f : 0.0f;
-                } else {
-                    // GELU'(z) = Phi(z) + z phi(z); 0.3989... = 1 / sqrt(2 pi)
-                    dact = normcdff(a[i]) + a[i] * expf(-0.5f * a[i] * a[i]) * 0.3989422804014327f;
+            for (int u = 0; u < AB_U; u++) {
+                const int64_t q = q0 + (int64_t)u * AB_THREADS;
+                if (q < n) {
+                    const int64_t off = ((int64_t)j * c_max + r0 + q / hv) * h + (q % hv) * 8;
+                    va[u] = ld_stream(pa + off);
+                    vg[u] = ld_stream(dh + off);
+                    if (swiglu) vb[u] = ld_stream(pb + off);
                 }
-                o[i] = g[i] * dact;
             }
-            st_v16(dst, Elt<__nv_bfloat16>::pack(o));
+#pragma unroll
+            for (int u = 0; u < AB_U; u++) {
+                const int64_t q = q0 + (int64_t)u * AB_THREADS;
+                if (q < n) {
+                    const int64_t row = (int64_t)j * c_max + r0 + q / hv;
+                    act_bwd_chunk(va[u], vb[u], vg[u], act, d_pre + row * h2 + (q % hv) * 8, h);
+                }
+            }
         }
     }
 }
@@ -157,8 +194,9 @@ moe_status transpose_pad_launch(const __nv_bfloat16 *src, int64_t src_batch, int
         cols % 8 || dst_cols % 8 || src_pitch % 8 || dst_pitch % 8 || src_batch % 8 ||
         dst_batch % 8 || !aligned16(src) || !aligned16(dst))
         return MOE_ERR_INVALID_ARG;
-    const dim3 grid((unsigned)((dst_cols + TP - 1) / TP), (unsigned)((cols + TP - 1) / TP),
-                    (unsigned)batches);
+    const int rblocks = (dst_cols + TP - 1) / TP;
+    const dim3 grid((unsigned)(rblocks < TP_GRID_X ? rblocks : TP_GRID_X),
+                    (unsigned)((cols + TP - 1) / TP), (unsigned)batches);
     if (grid.y > 65535) return MOE_ERR_UNSUPPORTED;
     return launch_pdl(transpose_pad_kernel, grid, dim3(TP_THREADS), 0, stream,
                       (const uint16_t *)src, src_batch, src_pitch, (uint16_t *)dst, dst_batch,
@@ -170,8 +208,8 @@ moe_status act_bwd_launch(const __nv_bfloat16 *pa, const __nv_bfloat16 *pb,
                           const int32_t *counts, const int32_t *c_dev, __nv_bfloat16 *d_pre,
                           int32_t *status, cudaStream_t stream) {
     if (h % 8 != 0 || e < 1 || e > 65535) return MOE_ERR_INVALID_ARG;
-    const int64_t gx = (c_max + AB_ROWS - 1) / AB_ROWS;
-    if (gx > 0x7fffffff) return MOE_ERR_UNSUPPORTED;
+    int64_t gx = (c_max + AB_ROWS - 1) / AB_ROWS;
+    if (gx > AB_GRID_X) gx = AB_GRID_X;   // CTAs per expert; they stride over the kept rows
     return launch_pdl(act_bwd_kernel, dim3((unsigned)gx, (unsigned)e), dim3(AB_THREADS), 0, stream,
                       pa, pb, d_hid, (int)act, e, c_max, h, counts, c_dev, d_pre, status);
 }
