@@ -79,7 +79,7 @@ def parse(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graded", action="store_true",
                     help="skip the stage breakdowns of the other graded workloads")
-    ap.add_argument("--only", choices=["gate"],
+    ap.add_argument("--only", choices=["gate", "gate_bwd"],
                     help="time one stage alone on the config's inputs (its own JSON line, not the "
                          "layer's): only the tensors that stage reads are drawn")
     return ap.parse_args(argv)
@@ -762,8 +762,10 @@ def run_ours(args, rank, world, local_rank):
 
 
 def run_only_gate(args):
-    """The gate alone on the config's x, gate weight and bias: mean event time
-    over args.steps calls, L2 flushed before each."""
+    """The gate (or, with --only gate_bwd, the gate backward: d_logits, d_wg,
+    d_bias and d_x from unit-normal d_gates) alone on the config's x, gate
+    weight and bias: mean event time over args.steps calls, L2 flushed before
+    each."""
     import torch
 
     import combine_moe_gate_gb300 as M
@@ -778,6 +780,17 @@ def run_only_gate(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flags = M.MOE_FLAG_NORMALIZE_GATES if w.normalize_gates and w.k >= 2 else 0
     fn = lambda: M.moe_gate_topk(inp["x"], inp["wg"], inp["bias"], w.k, idx, g, st, flags=flags)
+    flop = 2.0 * w.s * w.m * w.e
+    if args.only == "gate_bwd":
+        fn()
+        d_g = synth.normal_torch(w.seed, "d_gates", (w.k, w.s), 1.0, "f32", dev)
+        d_logits = torch.empty((w.s, w.e), device=dev, dtype=torch.float32)
+        d_wg = torch.empty((w.m, w.e), device=dev, dtype=torch.float32)
+        d_bias = torch.empty((w.e,), device=dev, dtype=torch.float32)
+        d_x = torch.empty((w.s, w.m), device=dev, dtype=torch.float32)
+        fn = lambda: M.moe_gate_bwd(inp["x"], inp["wg"], inp["bias"], idx, g, d_g, d_logits, st,
+                                    d_wg=d_wg, d_bias=d_bias, d_x=d_x, flags=flags)
+        flop *= 2.0
     for _ in range(args.warmup):
         flush.fill_(1)
         fn()
@@ -794,8 +807,8 @@ def run_only_gate(args):
     if int(st.item()) != 0:
         raise RuntimeError(f"device status {int(st.item())}")
     ms = tot / args.steps
-    return {"stage": "gate", "workload": w.name, "ms": ms, "steps": args.steps,
-            "fp32_tflops": 2.0 * w.s * w.m * w.e / (ms * 1e-3) / 1e12}
+    return {"stage": args.only, "workload": w.name, "ms": ms, "steps": args.steps,
+            "fp32_tflops": flop / (ms * 1e-3) / 1e12}
 
 
 def run_reference(args):
@@ -839,7 +852,7 @@ def main():
         if rank == 0:
             print(json.dumps(run_reference(args)))
         return
-    if args.only == "gate":
+    if args.only:
         if rank == 0:
             print(json.dumps(run_only_gate(args)))
         return

@@ -44,6 +44,34 @@ moe_status launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem
     return MOE_OK;
 }
 
+// launch_pdl for a kernel launched in clusters of `cl` CTAs along x
+// (gridDim.x a multiple of cl).
+template <typename... KArgs, typename... Args>
+moe_status launch_cluster_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, int cl,
+                              cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cl;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t err = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+    note_launch();
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
 // Wait until the previous kernel in the stream has completed and its writes
 // are visible (no-op when launched without programmatic serialization), then
 // let the next kernel start its own launch early.
@@ -51,6 +79,15 @@ __device__ __forceinline__ void pdl_enter() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+
+// The two halves of pdl_enter, for a kernel that reads nothing its
+// predecessor writes: it lets its successor launch at once, runs alongside
+// its predecessor, and waits for it (pdl_wait) before it exits, so that its
+// own completion still implies its predecessor's.
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ------------------------------------------------------------ device status
 
@@ -91,6 +128,27 @@ __device__ __forceinline__ void st_v16_cs(void *p, const V16 &v) {
     asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
                  :: "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]) : "memory");
 }
+
+// Asynchronous global -> shared copies (cp.async): `valid` false copies
+// nothing and zero-fills the destination (gmem must still be a valid address).
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool valid) {
+    unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    int n = valid ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(n)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem, bool valid) {
+    unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    int n = valid ? 4 : 0;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(s), "l"(gmem), "r"(n)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// This thread's copies of all but the newest N committed groups have landed.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // bf16 <-> fp32.  Widening is exact (bit shift).
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }

@@ -25,24 +25,6 @@
 namespace moe {
 namespace {
 
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool valid) {
-    unsigned s = (unsigned)__cvta_generic_to_shared(smem);
-    int n = valid ? 16 : 0;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(n)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async4(void *smem, const void *gmem, bool valid) {
-    unsigned s = (unsigned)__cvta_generic_to_shared(smem);
-    int n = valid ? 4 : 0;
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(s), "l"(gmem), "r"(n)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
 // Feature u (compile-time) of a 16-byte chunk, widened exactly to fp32.
 template <typename XT, int U>
 __device__ __forceinline__ float chunk_elem(const V16 &v) {

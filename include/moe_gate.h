@@ -20,6 +20,7 @@
  * Conventions shared by every call:
  *   - Every pointer argument is caller-owned memory.  Device pointers must be
  *     16-byte aligned.  Tensors are dense row-major with the shapes given.
+ *     Outputs overlap neither the inputs nor each other.
  *   - No call allocates, frees or synchronises.  Work is enqueued on `stream`
  *     (a cudaStream_t passed as void*; NULL = the legacy default stream).
  *   - Routing tables are route-major [k, s]: entry (r, t) is at r*s + t.

@@ -43,6 +43,10 @@ CASES = [
     # partly filled last feature block
     (_w(s=2500, m=48, e=12, k=2), True, "all"),
     (_w(s=1100, m=36, e=20, k=3, dtype="f32", normalize_gates=False), False, "all"),
+    # many ring stages per warp; wide expert counts (d_x in 4-token warp tiles)
+    (_w(s=5000, m=200, e=64, k=4, skew_alpha=0.8), True, "all"),
+    (_w(s=700, m=264, e=256, k=8), True, "all"),
+    (_w(s=530, m=132, e=130, k=6, dtype="f32", normalize_gates=False), False, "all"),
     (_w(s=100, m=40, e=5, k=3), True, "logits_only"),
     (_w(s=100, m=40, e=5, k=3), True, "bias_only"),
 ]
@@ -93,3 +97,47 @@ def test_gate_bwd_matches_oracle(w, normalize, outs):
     if d_x is not None:
         tol = tol_dl[:, None] * np.abs(w64).sum(1)[None, :] + e * U * (np.abs(dl) @ np.abs(w64).T)
         assert np.all(np.abs(d_x.cpu().numpy() - ref["d_x"]) <= tol)
+
+
+def _bwd_inputs(w, normalize):
+    inp = synth.make_inputs_host(w, parts=("x", "wg", "bias"))
+    lg = oracle.gate_logits(inp["x"], inp["wg"], inp["bias"])
+    idx = oracle.topk(lg, w.k)
+    g = oracle.gates(lg, idx, normalize)
+    dg = synth.normal_host(7, "dg", (w.k, w.s), 1.0, "f32")
+    return [to_dev(a) for a in (inp["x"], inp["wg"], inp["bias"], idx, g, dg)]
+
+
+def _run_bwd(w, args, normalize, st):
+    x, wg, bias, idx, g, dg = args
+    out = [torch.full(sh, float("nan"), dtype=torch.float32, device="cuda")
+           for sh in ((w.s, w.e), (w.m, w.e), (w.e,), (w.s, w.m))]
+    M.moe_gate_bwd(x, wg, bias, idx, g, dg, out[0], st, d_wg=out[1], d_bias=out[2], d_x=out[3],
+                   flags=M.MOE_FLAG_NORMALIZE_GATES if normalize else 0)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("w", [_w(s=8192, m=2048, e=16, k=3), _w(s=3000, m=520, e=256, k=8)],
+                         ids=lambda w: f"s{w.s}_m{w.m}_e{w.e}")
+def test_gate_bwd_is_deterministic(w):
+    """The split sums (token slices, warps, cluster ranks) add in a fixed
+    order: two calls give bit-identical outputs."""
+    args = _bwd_inputs(w, True)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a = _run_bwd(w, args, True, st)
+    b = _run_bwd(w, args, True, st)
+    assert int(st.item()) == 0
+    for u, v in zip(a, b):
+        assert torch.equal(u.view(torch.int32), v.view(torch.int32))
+
+
+def test_gate_bwd_skips_after_error():
+    """With the status word already set every kernel skips its stores."""
+    w = _w(s=600, m=136, e=24, k=2)
+    args = _bwd_inputs(w, True)
+    st = torch.full((1,), 3, dtype=torch.int32, device="cuda")
+    out = _run_bwd(w, args, True, st)
+    assert int(st.item()) == 3
+    for o in out:
+        assert torch.isnan(o).all()
