@@ -270,10 +270,12 @@ moe_status moe_expert_ffn_bwd(const void *buf, const void *hid, moe_dtype dt,
  * Inputs: x [s, m] in `xdt`; wg [m, e] fp32; bias [e] fp32 or NULL (used only
  * to recompute the logits of the raw softmax); idx, gates [k, s] as the gate
  * wrote them; d_gates [k, s] fp32 (e.g. moe_decode_bwd's).  Outputs, all fp32
- * and deterministic (fixed summation orders: d_x sums the experts in order,
- * d_wg and d_bias sum tokens per token group, then the groups in a fixed
- * tree): d_logits [s, e] (required), d_wg [m, e], d_bias [e], d_x [s, m]
- * (each may be NULL).  e <= 256 here.
+ * and deterministic: d_logits [s, e] (required), d_wg [m, e], d_bias [e],
+ * d_x [s, m] (each may be NULL).  Fixed summation orders: A sums the routes in
+ * route order; d_wg and d_bias sum each of 64 contiguous token slices in token
+ * order, then the slices in order; d_x sums, per token, the experts in order
+ * (raw softmax) or its k routes in route order (renormalised gates, where the
+ * other experts' d_logits are zero).  e <= 256 here.
  * This entry point extends the pages' forward gate to its backward.
  */
 moe_status moe_gate_bwd(const void *x, moe_dtype xdt, const float *wg, const float *bias,
