@@ -214,32 +214,39 @@ gate_seq_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
     const int64_t my_chunks =
         blockIdx.x < nchunks ? (nchunks - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     const int64_t total = my_chunks * ntiles;   // (chunk, tile) steps of this CTA, flattened
-    auto issue = [&](int64_t q) {
-        const int64_t chunk = blockIdx.x + (q / ntiles) * (int64_t)gridDim.x;
-        const int kt = (int)(q % ntiles);
-        seq_load<C, XT>(smem_seq + (q % C::ST) * C::STAGE, x, wg, s, m, e, chunk * C::TOKC,
-                        kt * C::KT, wg16);
+    // the step being issued (ST - 1 ahead of the one computed): chunk, tile, stage
+    int64_t ichunk = blockIdx.x;
+    int ikt = 0, ist = 0;
+    auto issue_next = [&]() {
+        seq_load<C, XT>(smem_seq + ist * C::STAGE, x, wg, s, m, e, ichunk * C::TOKC, ikt * C::KT,
+                        wg16);
+        ist = ist + 1 == C::ST ? 0 : ist + 1;
+        if (++ikt == ntiles) {
+            ikt = 0;
+            ichunk += gridDim.x;
+        }
     };
 #pragma unroll
     for (int p = 0; p < C::ST - 1; p++) {
-        if (p < total) issue(p);
+        if (p < total) issue_next();
         else cp_async_commit();
     }
     float2 acc[C::TT][C::EW / 2];
     const int qe = (e + 31) / 32;
+    int kt = 0, st_q = 0;
+    int64_t chunk = blockIdx.x;   // the computed step's chunk
     for (int64_t q = 0; q < total; q++) {
         cp_async_wait<C::ST - 2>();
         __syncthreads();   // step q landed; step q-1 (and the previous softmax) fully read
-        if (q + C::ST - 1 < total) issue(q + C::ST - 1);
+        if (q + C::ST - 1 < total) issue_next();
         else cp_async_commit();
-        const int kt = (int)(q % ntiles);
         if (kt == 0) {
 #pragma unroll
             for (int j = 0; j < C::TT; j++)
 #pragma unroll
                 for (int i = 0; i < C::EW / 2; i++) acc[j][i] = make_float2(0.0f, 0.0f);
         }
-        unsigned char *st = smem_seq + (q % C::ST) * C::STAGE;
+        unsigned char *st = smem_seq + st_q * C::STAGE;
         const float *wtile = reinterpret_cast<const float *>(st + C::X_BYTES) + we * C::EW;
         const int ngroups = min(C::KT, m - kt * C::KT) / C::VEC;   // m is a multiple of VEC
 #pragma unroll 1
@@ -269,12 +276,17 @@ gate_seq_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
                     lg[(tok0 + 32 * j) * C::LGS + ex + 1] = b;
                 }
             __syncthreads();
-            const int64_t t0 = (blockIdx.x + (q / ntiles) * (int64_t)gridDim.x) * C::TOKC;
+            const int64_t t0 = chunk * C::TOKC;
             for (int tl = warp; tl < C::TOKC; tl += C::NW) {
                 const int64_t t = t0 + tl;
                 if (t >= s) break;
                 softmax_topk_warp(lg + tl * C::LGS, e, k, normalize, t, s, idx, gates, qe);
             }
+        }
+        st_q = st_q + 1 == C::ST ? 0 : st_q + 1;
+        if (++kt == ntiles) {
+            kt = 0;
+            chunk += gridDim.x;
         }
     }
     cp_async_wait<0>();
@@ -555,11 +567,11 @@ gate_lane_res_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
     const int64_t g0 = (int64_t)blockIdx.x * nw + warp;
     const int64_t my_groups = g0 < groups ? (groups - g0 + gstride - 1) / gstride : 0;
     const int64_t total = my_groups * ntiles;   // (group, tile) steps of this warp, flattened
-    // this lane's x chunks of step q: its chunk of the step's tile, every token of the group
-    auto issue = [&](int64_t q) {
-        const int64_t t0 = (g0 + (q / ntiles) * gstride) * T;
-        const int ch = (int)(q % ntiles) * 32 + lane;
-        unsigned char *slot = ring + (q % RD) * (T * 32 * 16);
+    // this lane's x chunks of one step: its chunk of tile `it`, every token of
+    // the group starting at token t0, into ring slot `slot`
+    auto issue = [&](int64_t t0, int it, int slot_i) {
+        const int ch = it * 32 + lane;
+        unsigned char *slot = ring + slot_i * (T * 32 * 16);
 #pragma unroll
         for (int tt = 0; tt < T; tt++) {
             const bool ok = t0 + tt < s && ch < nch;
@@ -568,17 +580,29 @@ gate_lane_res_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
         }
         cp_async_commit();
     };
+    // the step being issued (RD - 1 ahead of the one computed): token, tile, slot
+    int64_t it0 = g0 * T;
+    int itile = 0, islot = 0;
+    auto issue_next = [&]() {
+        issue(it0, itile, islot);
+        islot = islot + 1 == RD ? 0 : islot + 1;
+        if (++itile == ntiles) {
+            itile = 0;
+            it0 += gstride * T;
+        }
+    };
 #pragma unroll
     for (int p = 0; p < RD - 1; p++) {
-        if (p < total) issue(p);
+        if (p < total) issue_next();
         else cp_async_commit();
     }
     float acc[T][EP];
+    int tile = 0, slot_q = 0;
+    int64_t t0 = g0 * T;   // the computed step's group
     for (int64_t q = 0; q < total; q++) {
-        if (q + RD - 1 < total) issue(q + RD - 1);
+        if (q + RD - 1 < total) issue_next();
         else cp_async_commit();
         cp_async_wait<RD - 1>();   // this lane's copies of step q have landed
-        const int tile = (int)(q % ntiles);
         if (tile == 0) {
 #pragma unroll
             for (int tt = 0; tt < T; tt++)
@@ -586,7 +610,7 @@ gate_lane_res_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
                 for (int jj = 0; jj < EP; jj++) acc[tt][jj] = 0.0f;
         }
         if (tile * 32 + lane < nch) {   // this lane's chunk of the tile holds features
-            const unsigned char *slot = ring + (q % RD) * (T * 32 * 16);
+            const unsigned char *slot = ring + slot_q * (T * 32 * 16);
             V16 cur[T];
 #pragma unroll
             for (int tt = 0; tt < T; tt++)
@@ -594,8 +618,9 @@ gate_lane_res_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
             lane_fma_chunk<XT, EP, T, 0, V>(acc, cur,
                                             wres + (size_t)tile * C::TILE_FLOATS + lane * C::WCH);
         }
-        if (tile != ntiles - 1) continue;
-        const int64_t t0 = (g0 + (q / ntiles) * gstride) * T;
+        slot_q = slot_q + 1 == RD ? 0 : slot_q + 1;
+        if (++tile != ntiles) continue;
+        tile = 0;
         // reduce-scatter over the lanes: lane l ends with flattened values 2l, 2l+1
         float v[64];
 #pragma unroll
@@ -651,6 +676,7 @@ gate_lane_res_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
             }
         }
         __syncwarp();   // the warp's logits row is reused by its next group
+        t0 += gstride * T;
     }
     cp_async_wait<0>();
 }
@@ -743,7 +769,7 @@ moe_status gate_dispatch(const void *x, const float *wg, const float *bias, int6
     // e > 32: fp32-FMA bound, sequential order; experts per warp x tokens per lane
     MOE_GATE_CASE(64, 16, 2, 4, 64, 3)
     MOE_GATE_CASE(128, 16, 2, 8, 64, 3)
-    MOE_GATE_CASE(256, 16, 4, 16, 32, 2)
+    MOE_GATE_CASE(256, 32, 4, 8, 32, 2)
 #undef MOE_GATE_CASE
     return MOE_ERR_UNSUPPORTED;
 }
