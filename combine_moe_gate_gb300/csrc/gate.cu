@@ -340,6 +340,36 @@ __device__ __forceinline__ void lane_fma_feature(float (&acc)[T][EP], const V16 
     }
 }
 
+// The same with packed fp32x2 FMAs over expert pairs (each half rounds exactly
+// as fmaf, so the sums are the same bits): acc[tt][i] holds experts 2i, 2i + 1.
+template <typename XT, int EP, int T, int U>
+__device__ __forceinline__ void lane_fma2_feature(float2 (&acc)[T][EP / 2], const V16 (&xv)[T],
+                                                  const float *wu) {
+    float2 w[EP / 2];
+#pragma unroll
+    for (int q = 0; q < EP / 4; q++) {
+        const float4 w4 = reinterpret_cast<const float4 *>(wu)[q];
+        w[2 * q] = make_float2(w4.x, w4.y);
+        w[2 * q + 1] = make_float2(w4.z, w4.w);
+    }
+#pragma unroll
+    for (int tt = 0; tt < T; tt++) {
+        const float xf = chunk_elem<XT, U>(xv[tt]);
+        const float2 x2 = make_float2(xf, xf);
+#pragma unroll
+        for (int i = 0; i < EP / 2; i++) acc[tt][i] = __ffma2_rn(x2, w[i], acc[tt][i]);
+    }
+}
+
+template <typename XT, int EP, int T, int U, int V>
+__device__ __forceinline__ void lane_fma2_chunk(float2 (&acc)[T][EP / 2], const V16 (&xv)[T],
+                                                const float *wc) {
+    if constexpr (U < V) {
+        lane_fma2_feature<XT, EP, T, U>(acc, xv, wc + U * EP);
+        lane_fma2_chunk<XT, EP, T, U + 1, V>(acc, xv, wc);
+    }
+}
+
 template <typename XT, int EP, int T, int U, int V>
 __device__ __forceinline__ void lane_fma_chunk(float (&acc)[T][EP], const V16 (&xv)[T],
                                                const float *wc) {
@@ -485,17 +515,21 @@ gate_lane_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
 // The same lane-blocked order with the whole gate weight resident in shared
 // memory (when it fits): a persistent CTA loads Wg once, staged as
 // [tile][chunk][feature][expert] with every chunk block padded by 16 bytes,
-// and each warp then takes T-token groups in turn.  Each lane streams its own
-// 16-byte x chunks through a private RD-deep cp.async ring in shared memory
-// (a lane only ever reads what it copied itself, so no lane waits on another),
-// which keeps RD K tiles of every warp's tokens in flight.  The lane sums are
-// combined by a reduce-scatter form of the xor butterfly: at offset o a lane
-// keeps the half of its values selected by lane bit o and adds the partner's
-// copy of that half, so every logit is the same sum v[l] + v[l ^ o] at every
-// level as in the full butterfly, with a fifth of the shuffles; lane l ends
-// with the flattened (token, expert) values 2l and 2l + 1.
-constexpr int RW_MAX = 8;                 // warps per CTA (at most)
-constexpr int RD = 4;                     // K tiles of x in flight per warp
+// and takes one contiguous range of the T-token groups, dealt to its warps in
+// turn.  Each lane streams its own 16-byte x chunks through a private RD-deep
+// cp.async ring in shared memory (a lane only ever reads what it copied
+// itself, so no lane waits on another).  The lane sums are combined by a
+// reduce-scatter form of the xor butterfly: at offset o a lane keeps the half
+// of its values selected by lane bit o and adds the partner's copy of that
+// half, so every logit is the same sum v[l] + v[l ^ o] at every level as in
+// the full butterfly, with a fifth of the shuffles; lane l ends with the
+// flattened (token, expert) values 2l and 2l + 1, so token tt's EP logits sit
+// in the EP / 2 lanes from tt * EP / 2 on, which then do its softmax and
+// top-k together with shuffles inside that lane segment.
+constexpr int RW_MAX = 16;                // warps per CTA (at most)
+// fewer warps (more registers a lane) the more tokens a warp holds
+template <int EP> constexpr int res_warps_max() { return EP >= 32 ? RW_MAX : EP == 16 ? 12 : 8; }
+constexpr int RD = 3;                     // K tiles of x in flight per warp
 constexpr size_t RES_SMEM_MAX = 220 * 1024;
 
 template <int EP, typename XT>
@@ -507,7 +541,7 @@ struct ResCfg {
     static constexpr int TILE_FLOATS = 32 * WCH;
     static constexpr int RING_BYTES = RD * T * 32 * 16;   // per warp
     static size_t smem(int m, int nw) {
-        return (size_t)((m + KS - 1) / KS) * TILE_FLOATS * 4 + (size_t)nw * (RING_BYTES + 64 * 4);
+        return (size_t)((m + KS - 1) / KS) * TILE_FLOATS * 4 + (size_t)nw * RING_BYTES;
     }
 };
 
@@ -523,8 +557,62 @@ __device__ __forceinline__ void rs_step(float (&v)[64], int lane) {
     }
 }
 
+// Softmax and top-k of one token whose logits a and b (experts j0, j0 + 1)
+// are spread over a segment of S = EP / 2 lanes: max and sum by xor shuffles
+// inside the segment, then k rounds of segment arg-max over the experts not
+// yet taken (ties -> lower index).  Route r is written by the segment's lane
+// r mod S; its gate divides by the selected probabilities summed in route
+// order (renormalised) or by the softmax sum.
+template <int S>
+__device__ __forceinline__ void segment_topk(float a, float b, int j0, int e, int k, int normalize,
+                                             int64_t t, int64_t s, int32_t *idx, float *gates,
+                                             int lane) {
+    const bool va = j0 < e, vb = j0 + 1 < e;
+    float mx = fmaxf(va ? a : -INFINITY, vb ? b : -INFINITY);
+#pragma unroll
+    for (int o = S / 2; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float z = (va ? expf(a - mx) : 0.0f) + (vb ? expf(b - mx) : 0.0f);
+#pragma unroll
+    for (int o = S / 2; o >= 1; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    const int ls = lane % S;
+    bool ta = !va, tb = !vb;   // taken (or not an expert)
+    float sel = 0.0f, rp0 = 0.0f, rp1 = 0.0f;
+    int rj0 = 0, rj1 = 0;
+    for (int r = 0; r < k; r++) {
+        float cv = -INFINITY;
+        int cj = 0x7fffffff;
+        if (!ta) { cv = a; cj = j0; }
+        if (!tb && (cj == 0x7fffffff || b > cv)) { cv = b; cj = j0 + 1; }
+#pragma unroll
+        for (int o = S / 2; o >= 1; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, cv, o);
+            const int oj = __shfl_xor_sync(0xffffffffu, cj, o);
+            if (oj != 0x7fffffff && (cj == 0x7fffffff || ov > cv || (ov == cv && oj < cj))) {
+                cv = ov;
+                cj = oj;
+            }
+        }
+        ta = ta || cj == j0;
+        tb = tb || cj == j0 + 1;
+        const float p = expf(cv - mx);
+        sel += p;
+        if (r == ls) { rj0 = cj; rp0 = p; }
+        if (r == ls + S) { rj1 = cj; rp1 = p; }
+    }
+    if (t >= s) return;
+    const float den = normalize ? sel : z;
+    if (ls < k) {
+        idx[(int64_t)ls * s + t] = rj0;
+        gates[(int64_t)ls * s + t] = rp0 / den;
+    }
+    if (ls + S < k) {
+        idx[(int64_t)(ls + S) * s + t] = rj1;
+        gates[(int64_t)(ls + S) * s + t] = rp1 / den;
+    }
+}
+
 template <int EP, typename XT>
-__global__ void __launch_bounds__(RW_MAX * 32, 1)
+__global__ void __launch_bounds__(res_warps_max<EP>() * 32, 1)
 gate_lane_res_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
                      const float *__restrict__ bias, int64_t s, int m, int e, int k, int normalize,
                      int32_t *__restrict__ idx, float *__restrict__ gates, int32_t *status) {
@@ -539,7 +627,6 @@ gate_lane_res_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const size_t w_bytes = (size_t)ntiles * C::TILE_FLOATS * 4;
     unsigned char *ring = smem_res + w_bytes + (size_t)warp * C::RING_BYTES;
-    float *lg = reinterpret_cast<float *>(smem_res + w_bytes + (size_t)nw * C::RING_BYTES) + warp * 64;
     const int nch = m / V;                                       // m is a multiple of V
     // the whole weight, zero past m features and e experts
     if (e == EP) {
@@ -559,14 +646,13 @@ gate_lane_res_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
                       ok ? (const void *)(wg + (int64_t)r * e + jj) : (const void *)wg, ok);
         }
     }
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
+    cp_async_commit();   // the oldest group: waited for below, after the x prologue
+    // this CTA's contiguous range of groups, warp w takes lo + w, lo + w + nw, ...
     const int64_t groups = (s + T - 1) / T;
-    const int64_t gstride = (int64_t)gridDim.x * nw;
-    const int64_t g0 = (int64_t)blockIdx.x * nw + warp;
-    const int64_t my_groups = g0 < groups ? (groups - g0 + gstride - 1) / gstride : 0;
+    const int64_t lo = groups * blockIdx.x / gridDim.x, hi = groups * (blockIdx.x + 1) / gridDim.x;
+    const int64_t my_groups = lo + warp < hi ? (hi - lo - warp + nw - 1) / nw : 0;
     const int64_t total = my_groups * ntiles;   // (group, tile) steps of this warp, flattened
+    const int64_t gstride_t = (int64_t)nw * T;  // tokens between this warp's groups
     // this lane's x chunks of one step: its chunk of tile `it`, every token of
     // the group starting at token t0, into ring slot `slot`
     auto issue = [&](int64_t t0, int it, int slot_i) {
@@ -581,14 +667,14 @@ gate_lane_res_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
         cp_async_commit();
     };
     // the step being issued (RD - 1 ahead of the one computed): token, tile, slot
-    int64_t it0 = g0 * T;
+    int64_t it0 = (lo + warp) * T;
     int itile = 0, islot = 0;
     auto issue_next = [&]() {
         issue(it0, itile, islot);
         islot = islot + 1 == RD ? 0 : islot + 1;
         if (++itile == ntiles) {
             itile = 0;
-            it0 += gstride * T;
+            it0 += gstride_t;
         }
     };
 #pragma unroll
@@ -596,9 +682,11 @@ gate_lane_res_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
         if (p < total) issue_next();
         else cp_async_commit();
     }
-    float acc[T][EP];
+    cp_async_wait<RD - 1>();   // the weight (this thread's copies) ...
+    __syncthreads();           // ... and every thread's
+    float2 acc[T][EP / 2];
     int tile = 0, slot_q = 0;
-    int64_t t0 = g0 * T;   // the computed step's group
+    int64_t t0 = (lo + warp) * T;   // the computed step's group
     for (int64_t q = 0; q < total; q++) {
         if (q + RD - 1 < total) issue_next();
         else cp_async_commit();
@@ -607,7 +695,7 @@ gate_lane_res_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
 #pragma unroll
             for (int tt = 0; tt < T; tt++)
 #pragma unroll
-                for (int jj = 0; jj < EP; jj++) acc[tt][jj] = 0.0f;
+                for (int i = 0; i < EP / 2; i++) acc[tt][i] = make_float2(0.0f, 0.0f);
         }
         if (tile * 32 + lane < nch) {   // this lane's chunk of the tile holds features
             const unsigned char *slot = ring + slot_q * (T * 32 * 16);
@@ -615,8 +703,8 @@ gate_lane_res_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
 #pragma unroll
             for (int tt = 0; tt < T; tt++)
                 cur[tt] = *reinterpret_cast<const V16 *>(slot + (tt * 32 + lane) * 16);
-            lane_fma_chunk<XT, EP, T, 0, V>(acc, cur,
-                                            wres + (size_t)tile * C::TILE_FLOATS + lane * C::WCH);
+            lane_fma2_chunk<XT, EP, T, 0, V>(acc, cur,
+                                             wres + (size_t)tile * C::TILE_FLOATS + lane * C::WCH);
         }
         slot_q = slot_q + 1 == RD ? 0 : slot_q + 1;
         if (++tile != ntiles) continue;
@@ -626,57 +714,23 @@ gate_lane_res_kernel(const XT *__restrict__ x, const float *__restrict__ wg,
 #pragma unroll
         for (int tt = 0; tt < T; tt++)
 #pragma unroll
-            for (int jj = 0; jj < EP; jj++) v[tt * EP + jj] = acc[tt][jj];
+            for (int i = 0; i < EP / 2; i++) {
+                v[tt * EP + 2 * i] = acc[tt][i].x;
+                v[tt * EP + 2 * i + 1] = acc[tt][i].y;
+            }
         rs_step<64, 16>(v, lane);
         rs_step<32, 8>(v, lane);
         rs_step<16, 4>(v, lane);
         rs_step<8, 2>(v, lane);
         rs_step<4, 1>(v, lane);
-        lg[2 * lane] = v[0];
-        lg[2 * lane + 1] = v[1];
-        __syncwarp();
-        if (lane < T && t0 + lane < s) {
-            const int64_t t = t0 + lane;
-            float row[EP];
-#pragma unroll
-            for (int jj = 0; jj < EP; jj++) row[jj] = lg[lane * EP + jj];
-            float mx = -INFINITY;
-#pragma unroll
-            for (int jj = 0; jj < EP; jj++)
-                if (jj < e) {
-                    if (bias) row[jj] = row[jj] + bias[jj];
-                    mx = fmaxf(mx, row[jj]);
-                }
-            float z = 0.0f;
-#pragma unroll
-            for (int jj = 0; jj < EP; jj++)
-                if (jj < e) z += expf(row[jj] - mx);
-            float sel = 0.0f;
-            for (int pass = 0; pass < 2; pass++) {
-                uint32_t taken = 0;
-                for (int r = 0; r < k; r++) {
-                    int bj = -1;
-                    float bv = -INFINITY;
-#pragma unroll
-                    for (int jj = 0; jj < EP; jj++) {
-                        if (jj < e && !(taken & (1u << jj)) && (bj < 0 || row[jj] > bv)) {
-                            bv = row[jj];
-                            bj = jj;
-                        }
-                    }
-                    taken |= 1u << bj;
-                    const float p = expf(bv - mx);
-                    if (pass == 0) {
-                        sel += p;
-                    } else {
-                        idx[(int64_t)r * s + t] = bj;
-                        gates[(int64_t)r * s + t] = p / (normalize ? sel : z);
-                    }
-                }
-            }
+        const int j0 = (2 * lane) % EP;
+        float a = v[0], b = v[1];
+        if (bias) {   // one fp32 add after the chain
+            if (j0 < e) a = a + bias[j0];
+            if (j0 + 1 < e) b = b + bias[j0 + 1];
         }
-        __syncwarp();   // the warp's logits row is reused by its next group
-        t0 += gstride * T;
+        segment_topk<EP / 2>(a, b, j0, e, k, normalize, t0 + (2 * lane) / EP, s, idx, gates, lane);
+        t0 += gstride_t;
     }
     cp_async_wait<0>();
 }
@@ -696,7 +750,9 @@ moe_status launch_lane(const void *x, const float *wg, const float *bias, int64_
         const int64_t groups = (s + R::T - 1) / R::T;
         // warps per CTA: enough to spread the groups over every SM, at most RW_MAX
         int64_t nw = (groups + sms - 1) / sms;
-        nw = nw < 1 ? 1 : (nw > RW_MAX ? RW_MAX : nw);
+        nw = nw < 1 ? 1 : (nw > res_warps_max<EP>() ? res_warps_max<EP>() : nw);
+        // fewer warps when their rings would not fit beside the weight
+        while (nw > 4 && R::smem(m, (int)nw) > RES_SMEM_MAX) nw--;
         const size_t res_smem = R::smem(m, (int)nw);
         if (res_smem <= RES_SMEM_MAX) {
             auto kern = gate_lane_res_kernel<EP, XT>;
