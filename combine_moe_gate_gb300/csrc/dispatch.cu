@@ -35,6 +35,41 @@ struct RawRoute {
     float g;
 };
 
+// Position of a work item it = row * parts + part that steps by a fixed stride:
+// one division at the start, none in the loop.
+struct ItemIter {
+    int64_t row, drow;
+    int part, dpart, parts;
+    __device__ __forceinline__ ItemIter(int64_t it, int64_t stride, int parts_) : parts(parts_) {
+        row = it / parts_;
+        part = (int)(it - row * parts_);
+        drow = stride / parts_;
+        dpart = (int)(stride - drow * parts_);
+    }
+    __device__ __forceinline__ void next() {
+        row += drow;
+        part += dpart;
+        if (part >= parts) {
+            part -= parts;
+            row++;
+        }
+    }
+};
+
+// (row, part) of work item it = row * parts + part: a 32-bit division when
+// every item index fits (`small`, uniform over the grid), else a 64-bit one.
+__device__ __forceinline__ void split_item(int64_t it, int parts, bool small, int64_t &row,
+                                           int &part) {
+    if (small) {
+        const uint32_t u = (uint32_t)it, r = u / (uint32_t)parts;
+        row = r;
+        part = (int)(u - r * (uint32_t)parts);
+    } else {
+        row = it / parts;
+        part = (int)(it - row * parts);
+    }
+}
+
 __device__ __forceinline__ RawRoute fetch_route(const int32_t *idx, const int32_t *loc,
                                                 const float *gates, int64_t s, int64_t t, int k) {
     const int lane = threadIdx.x & 31;
@@ -97,9 +132,11 @@ encode_kernel(const T *__restrict__ x, const int32_t *__restrict__ idx,
     const int nsl = (nch + SL - 1) / SL;
     const int64_t items = s * nsl;
     const int64_t nw = (int64_t)gridDim.x * (DNT / 32);
-    for (int64_t it = blockIdx.x * (DNT / 32) + (threadIdx.x >> 5); it < items; it += nw) {
-        const int64_t t = it / nsl;
-        const int c0 = (int)(it % nsl) * SL + lane;
+    const int64_t it0 = blockIdx.x * (DNT / 32) + (threadIdx.x >> 5);
+    ItemIter pos(it0, nw, nsl);
+    for (int64_t it = it0; it < items; it += nw, pos.next()) {
+        const int64_t t = pos.row;
+        const int c0 = pos.part * SL + lane;
         const V16 *src = reinterpret_cast<const V16 *>(x + t * m);
         V16 v[SL / 32];
 #pragma unroll
@@ -160,13 +197,22 @@ combine_kernel(const T *__restrict__ src, const int32_t *__restrict__ idx,
     const int64_t items = s * nsl;
     const int64_t nw = (int64_t)gridDim.x * (DNT / 32);
     int64_t it = blockIdx.x * (DNT / 32) + (threadIdx.x >> 5);
-    RawRoute nxt = fetch_route(idx, loc, WEIGHTED ? gates : nullptr, s, it / nsl, k);
+    const bool small = items + nw <= 0x7fffffff;
+    int64_t t;
+    int part;
+    split_item(it, nsl, small, t, part);
+    RawRoute nxt = fetch_route(idx, loc, WEIGHTED ? gates : nullptr, s, t, k);
     for (; it < items; it += nw) {
-        const int64_t t = it / nsl;
-        const int c0 = (int)(it % nsl) * SLU + lane;
+        split_item(it, nsl, small, t, part);
+        const int c0 = part * SLU + lane;
         const RawRoute cur = nxt;
         // the next item's route entries travel while this item's rows move
-        nxt = fetch_route(idx, loc, WEIGHTED ? gates : nullptr, s, (it + nw) / nsl, k);
+        {
+            int64_t tn;
+            int pn;
+            split_item(it + nw, nsl, small, tn, pn);
+            nxt = fetch_route(idx, loc, WEIGHTED ? gates : nullptr, s, tn, k);
+        }
         Routes R = decide_routes(cur, m, e, k, c_eff, c_max, status);
         V16 *dst = reinterpret_cast<V16 *>(y + t * m);
         float acc[ONE ? 1 : U][VEC];
@@ -224,18 +270,24 @@ combine_kernel(const T *__restrict__ src, const int32_t *__restrict__ idx,
     }
 }
 
-// g * d correctly rounded to bf16 (one rounding of the exact product): the
-// fp32 product p is exact to within the error term err = fma(g, d, -p); only
-// when p sits exactly halfway between two bf16 values does err decide.
-__device__ __forceinline__ uint32_t mul_round_bf16(float g, float d) {
-    float p = __fmul_rn(g, d);
-    float err = __fmaf_rn(g, d, -p);
+// g * d (fp32 times a bf16 value) correctly rounded to bf16, one rounding of
+// the exact product, by round to odd: the product truncated to fp32 with its
+// last bit set when it was inexact keeps 16 bits beyond bf16's precision, so
+// rounding that to bf16 (nearest even) rounds the exact product once.  err is
+// the exact remainder g*d - p (at most 8 significant bits).  Infinities and
+// NaNs keep their bits.
+__device__ __forceinline__ float mul_round_odd(float g, float d) {
+    const float p = __fmul_rz(g, d);
+    const float err = __fmaf_rn(g, d, -p);
     uint32_t u = __float_as_uint(p);
-    if ((u & 0xFFFFu) == 0x8000u && err != 0.0f && (u & 0x7F800000u) != 0x7F800000u) {
-        bool away = (err > 0.0f) == (p > 0.0f);
-        return (u >> 16) + (away ? 1u : 0u);
-    }
-    return f2bf(p);
+    if (err != 0.0f && (u & 0x7F800000u) != 0x7F800000u) u |= 1u;
+    return __uint_as_float(u);
+}
+
+// Two of them, packed (lo in the low half).
+__device__ __forceinline__ uint32_t mul_round_bf16x2(float g, float lo, float hi) {
+    const __nv_bfloat162 r = __floats2bfloat162_rn(mul_round_odd(g, lo), mul_round_odd(g, hi));
+    return *reinterpret_cast<const uint32_t *>(&r);
 }
 
 template <typename T> struct ScaleRound;
@@ -251,8 +303,7 @@ template <> struct ScaleRound<__nv_bfloat16> {
     __device__ __forceinline__ static V16 apply(float g, const V16 &d) {
         V16 o;
 #pragma unroll
-        for (int i = 0; i < 4; i++)
-            o.w[i] = mul_round_bf16(g, bf16lo(d.w[i])) | (mul_round_bf16(g, bf16hi(d.w[i])) << 16);
+        for (int i = 0; i < 4; i++) o.w[i] = mul_round_bf16x2(g, bf16lo(d.w[i]), bf16hi(d.w[i]));
         return o;
     }
 };
@@ -300,10 +351,14 @@ decode_bwd_kernel(const T *__restrict__ dy, const T *__restrict__ out,
     const int nch = m / VEC;
     const int64_t items = s * k;
     // item q = (token q / k, route q % k); lane 0 fetches the route's entry
+    const bool small = items + nw <= 0x7fffffff;
     auto fetch = [&](int64_t q, int &ex, int &l, float &g) {
         ex = -1; l = -1; g = 0.0f;
         if (lane == 0 && q < items) {
-            const int64_t off = (q % k) * s + q / k;
+            int64_t tq;
+            int rq;
+            split_item(q, k, small, tq, rq);
+            const int64_t off = (int64_t)rq * s + tq;
             ex = idx[off];
             l = loc[off];
             g = gates[off];
@@ -314,8 +369,9 @@ decode_bwd_kernel(const T *__restrict__ dy, const T *__restrict__ out,
     float ng;
     fetch(q, nex, nl, ng);
     for (; q < items; q += nw) {
-        const int64_t t = q / k;
-        const int r = (int)(q % k);
+        int64_t t;
+        int r;
+        split_item(q, k, small, t, r);
         int ex = __shfl_sync(0xffffffffu, nex, 0), l = __shfl_sync(0xffffffffu, nl, 0);
         const float g = __shfl_sync(0xffffffffu, ng, 0);
         fetch(q + nw, nex, nl, ng);   // the next item's entry travels meanwhile
