@@ -77,6 +77,29 @@ constexpr int AB_ROWS = 16;   // rows of one expert per CTA
 constexpr int AB_U = 4;       // 16-byte chunks per thread in flight together
 constexpr int AB_GRID_X = 32; // CTAs per expert
 
+// GELU'(z) = Phi(z) + z phi(z), Phi(z) = 0.5 (1 + erf(z / sqrt 2)), phi the
+// normal density.  Phi as in the forward GELU: erfc(x) = (1 + a1 x + ... +
+// a6 x^6)^-16 for x = |z| / sqrt 2 (Abramowitz & Stegun, Handbook of
+// Mathematical Functions, 7.1.28, |error| <= 3e-7), Phi = 1 - erfc / 2 for
+// z >= 0 and erfc / 2 below, so the negative tail does not cancel.
+__device__ __forceinline__ float gelu_grad(float z) {
+    const float x = fabsf(z) * 0.70710678118654752f;
+    float p = fmaf(x, 0.0000430638f, 0.0002765672f);
+    p = fmaf(x, p, 0.0001520143f);
+    p = fmaf(x, p, 0.0092705272f);
+    p = fmaf(x, p, 0.0422820123f);
+    p = fmaf(x, p, 0.0705230784f);
+    p = fmaf(x, p, 1.0f);
+    p = p * p;
+    p = p * p;
+    p = p * p;
+    p = p * p;   // overflows to inf for large x, where erfc -> 0
+    const float half_erfc = 0.5f * __frcp_rn(p);
+    const float phi_cdf = z >= 0.0f ? 1.0f - half_erfc : half_erfc;
+    // 0.3989... = 1 / sqrt(2 pi)
+    return phi_cdf + z * __expf(-0.5f * z * z) * 0.3989422804014327f;
+}
+
 __device__ __forceinline__ void act_bwd_chunk(const V16 &pa, const V16 &pb, const V16 &dh, int act,
                                               __nv_bfloat16 *dst, int h) {
     float a[8], g[8], o[8];
@@ -100,8 +123,7 @@ __device__ __forceinline__ void act_bwd_chunk(const V16 &pa, const V16 &pb, cons
             if (act == MOE_ACT_RELU) {
                 dact = a[i] > 0.0f ? 1.0f : 0.0f;
             } else {
-                // GELU'(z) = Phi(z) + z phi(z); 0.3989... = 1 / sqrt(2 pi)
-                dact = normcdff(a[i]) + a[i] * expf(-0.5f * a[i] * a[i]) * 0.3989422804014327f;
+                dact = gelu_grad(a[i]);
             }
             o[i] = g[i] * dact;
         }
@@ -124,16 +146,20 @@ act_bwd_kernel(const __nv_bfloat16 *__restrict__ pa, const __nv_bfloat16 *__rest
     // the CTAs of an expert stride over its kept rows, AB_ROWS at a time
     for (int64_t r0 = (int64_t)blockIdx.x * AB_ROWS; r0 < kept;
          r0 += (int64_t)gridDim.x * AB_ROWS) {
-        const int64_t nrow = min((int64_t)AB_ROWS, kept - r0);
-        const int64_t n = nrow * hv;
-        for (int64_t q0 = threadIdx.x; q0 < n; q0 += (int64_t)AB_THREADS * AB_U) {
+        const int nrow = (int)min((int64_t)AB_ROWS, kept - r0);
+        const int n = nrow * hv;   // chunks of this row block (AB_ROWS * h / 8 fits an int)
+        const int64_t row0 = (int64_t)j * c_max + r0;
+        for (int q0 = threadIdx.x; q0 < n; q0 += AB_THREADS * AB_U) {
             V16 va[AB_U], vb[AB_U], vg[AB_U];
+            int rr[AB_U], cc[AB_U];   // row in the block, chunk in the row
             // every load of the batch in flight before any arithmetic
 #pragma unroll
             for (int u = 0; u < AB_U; u++) {
-                const int64_t q = q0 + (int64_t)u * AB_THREADS;
+                const int q = q0 + u * AB_THREADS;
+                rr[u] = q / hv;
+                cc[u] = q - rr[u] * hv;
                 if (q < n) {
-                    const int64_t off = ((int64_t)j * c_max + r0 + q / hv) * h + (q % hv) * 8;
+                    const int64_t off = (row0 + rr[u]) * h + cc[u] * 8;
                     va[u] = ld_stream(pa + off);
                     vg[u] = ld_stream(dh + off);
                     if (swiglu) vb[u] = ld_stream(pb + off);
@@ -141,20 +167,20 @@ act_bwd_kernel(const __nv_bfloat16 *__restrict__ pa, const __nv_bfloat16 *__rest
             }
 #pragma unroll
             for (int u = 0; u < AB_U; u++) {
-                const int64_t q = q0 + (int64_t)u * AB_THREADS;
-                if (q < n) {
-                    const int64_t row = (int64_t)j * c_max + r0 + q / hv;
-                    act_bwd_chunk(va[u], vb[u], vg[u], act, d_pre + row * h2 + (q % hv) * 8, h);
-                }
+                if (q0 + u * AB_THREADS < n)
+                    act_bwd_chunk(va[u], vb[u], vg[u], act, d_pre + (row0 + rr[u]) * h2 + cc[u] * 8,
+                                  h);
             }
         }
     }
 }
 
 // --------------------------------------------------------- column sums
-// A CTA owns 32 columns of one expert (lane = column); its 8 warps take every
-// 8th kept row and the partials are added in warp order.
-constexpr int CS_WARPS = 8;
+// A CTA owns CS_COLS columns of one expert, lane l columns 8l .. 8l + 7 (one
+// 16-byte load a row); its 16 warps take every 16th kept row, CS_U rows in
+// flight, and the partials are added in warp order.
+constexpr int CS_WARPS = 16, CS_COLS = 256, CS_U = 4;
+static_assert(CS_COLS == 32 * 8 && CS_WARPS * 32 >= CS_COLS, "8 columns a lane, a thread a column");
 
 __global__ void __launch_bounds__(CS_WARPS * 32)
 colsum_kernel(const __nv_bfloat16 *__restrict__ src, int64_t c_max, int cols, int64_t pitch,
@@ -162,23 +188,43 @@ colsum_kernel(const __nv_bfloat16 *__restrict__ src, int64_t c_max, int cols, in
               __nv_bfloat16 *__restrict__ out, int32_t *status) {
     pdl_enter();
     if (status_bad(status)) return;
-    __shared__ float part[CS_WARPS][33];
+    __shared__ float part[CS_WARPS][CS_COLS];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int j = blockIdx.y;
-    const int col = blockIdx.x * 32 + lane;
+    const int c0 = blockIdx.x * CS_COLS + 8 * lane;
     const int64_t kept = max(0, min(min(counts[j], *c_dev), (int)min(c_max, (int64_t)0x7fffffff)));
-    float acc = 0.0f;
-    if (col < cols) {
-        const __nv_bfloat16 *s = src + (int64_t)j * c_max * pitch + col;
-#pragma unroll 4
-        for (int64_t r = warp; r < kept; r += CS_WARPS) acc += __bfloat162float(s[r * pitch]);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) acc[i] = 0.0f;
+    if (c0 < cols) {
+        const __nv_bfloat16 *sp = src + (int64_t)j * c_max * pitch + c0;
+        for (int64_t r0 = warp; r0 < kept; r0 += (int64_t)CS_WARPS * CS_U) {
+            V16 v[CS_U];
+#pragma unroll
+            for (int u = 0; u < CS_U; u++) {
+                const int64_t r = r0 + (int64_t)u * CS_WARPS;
+                if (r < kept) v[u] = ld_stream(sp + r * pitch);
+            }
+#pragma unroll
+            for (int u = 0; u < CS_U; u++) {
+                if (r0 + (int64_t)u * CS_WARPS < kept) {
+                    float f[8];
+                    Elt<__nv_bfloat16>::unpack(v[u], f);
+#pragma unroll
+                    for (int i = 0; i < 8; i++) acc[i] += f[i];
+                }
+            }
+        }
     }
-    part[warp][lane] = acc;
+#pragma unroll
+    for (int i = 0; i < 8; i++) part[warp][8 * lane + i] = acc[i];
     __syncthreads();
-    if (warp == 0 && col < cols) {
+    // threads 0 .. CS_COLS - 1 finish one column each
+    const int col = blockIdx.x * CS_COLS + threadIdx.x;
+    if (threadIdx.x < CS_COLS && col < cols) {
         float sum = 0.0f;
 #pragma unroll
-        for (int w = 0; w < CS_WARPS; w++) sum += part[w][lane];
+        for (int w = 0; w < CS_WARPS; w++) sum += part[w][threadIdx.x];
         out[(int64_t)j * cols + col] = __float2bfloat16_rn(sum);
     }
 }
@@ -217,8 +263,10 @@ moe_status act_bwd_launch(const __nv_bfloat16 *pa, const __nv_bfloat16 *pb,
 moe_status colsum_launch(const __nv_bfloat16 *src, int e, int64_t c_max, int cols,
                          int64_t src_pitch, const int32_t *counts, const int32_t *c_dev,
                          __nv_bfloat16 *out, int32_t *status, cudaStream_t stream) {
-    if (e < 1 || e > 65535 || cols < 1) return MOE_ERR_INVALID_ARG;
-    return launch_pdl(colsum_kernel, dim3((unsigned)((cols + 31) / 32), (unsigned)e),
+    // rows of whole 16-byte chunks
+    if (e < 1 || e > 65535 || cols < 1 || cols % 8 || src_pitch % 8 || !aligned16(src))
+        return MOE_ERR_INVALID_ARG;
+    return launch_pdl(colsum_kernel, dim3((unsigned)((cols + CS_COLS - 1) / CS_COLS), (unsigned)e),
                       dim3(CS_WARPS * 32), 0, stream, src, c_max, cols, src_pitch, counts, c_dev,
                       out, status);
 }
