@@ -77,11 +77,31 @@ constexpr int AB_ROWS = 16;   // rows of one expert per CTA
 constexpr int AB_U = 4;       // 16-byte chunks per thread in flight together
 constexpr int AB_GRID_X = 32; // CTAs per expert
 
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ float exp2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// Two floats to packed bf16 (nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+    const __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
 // GELU'(z) = Phi(z) + z phi(z), Phi(z) = 0.5 (1 + erf(z / sqrt 2)), phi the
 // normal density.  Phi as in the forward GELU: erfc(x) = (1 + a1 x + ... +
 // a6 x^6)^-16 for x = |z| / sqrt 2 (Abramowitz & Stegun, Handbook of
 // Mathematical Functions, 7.1.28, |error| <= 3e-7), Phi = 1 - erfc / 2 for
-// z >= 0 and erfc / 2 below, so the negative tail does not cancel.
+// z >= 0 and erfc / 2 below, so the negative tail does not cancel; phi(z) =
+// 2^(-z^2 log2(e) / 2) / sqrt(2 pi).  Approximate reciprocal and power of two
+// (relative error ~2^-22), far below the bf16 rounding that follows.
 __device__ __forceinline__ float gelu_grad(float z) {
     const float x = fabsf(z) * 0.70710678118654752f;
     float p = fmaf(x, 0.0000430638f, 0.0002765672f);
@@ -94,18 +114,20 @@ __device__ __forceinline__ float gelu_grad(float z) {
     p = p * p;
     p = p * p;
     p = p * p;   // overflows to inf for large x, where erfc -> 0
-    const float half_erfc = 0.5f * __frcp_rn(p);
-    const float phi_cdf = z >= 0.0f ? 1.0f - half_erfc : half_erfc;
-    // 0.3989... = 1 / sqrt(2 pi)
-    return phi_cdf + z * __expf(-0.5f * z * z) * 0.3989422804014327f;
+    const float half_erfc = 0.5f * rcp_approx(p);
+    const float cdf = z >= 0.0f ? 1.0f - half_erfc : half_erfc;
+    // -log2(e) / 2 and 1 / sqrt(2 pi)
+    const float dens = exp2_approx((z * z) * -0.72134752044448170f);
+    return fmaf(z * 0.3989422804014327f, dens, cdf);
 }
 
-__device__ __forceinline__ void act_bwd_chunk(const V16 &pa, const V16 &pb, const V16 &dh, int act,
+template <int ACT>
+__device__ __forceinline__ void act_bwd_chunk(const V16 &pa, const V16 &pb, const V16 &dh,
                                               __nv_bfloat16 *dst, int h) {
     float a[8], g[8], o[8];
     Elt<__nv_bfloat16>::unpack(pa, a);
     Elt<__nv_bfloat16>::unpack(dh, g);
-    if (act == MOE_ACT_SWIGLU) {
+    if constexpr (ACT == MOE_ACT_SWIGLU) {
         float b[8], ob[8];
         Elt<__nv_bfloat16>::unpack(pb, b);
 #pragma unroll
@@ -118,27 +140,24 @@ __device__ __forceinline__ void act_bwd_chunk(const V16 &pa, const V16 &pb, cons
         st_v16(dst + h, Elt<__nv_bfloat16>::pack(ob));
     } else {
 #pragma unroll
-        for (int i = 0; i < 8; i++) {
-            float dact;
-            if (act == MOE_ACT_RELU) {
-                dact = a[i] > 0.0f ? 1.0f : 0.0f;
-            } else {
-                dact = gelu_grad(a[i]);
-            }
-            o[i] = g[i] * dact;
-        }
-        st_v16(dst, Elt<__nv_bfloat16>::pack(o));
+        for (int i = 0; i < 8; i++)
+            o[i] = g[i] * (ACT == MOE_ACT_RELU ? (a[i] > 0.0f ? 1.0f : 0.0f) : gelu_grad(a[i]));
+        V16 v;
+#pragma unroll
+        for (int i = 0; i < 4; i++) v.w[i] = pack2_bf16(o[2 * i], o[2 * i + 1]);
+        st_v16(dst, v);
     }
 }
 
+template <int ACT>
 __global__ void __launch_bounds__(AB_THREADS)
 act_bwd_kernel(const __nv_bfloat16 *__restrict__ pa, const __nv_bfloat16 *__restrict__ pb,
-               const __nv_bfloat16 *__restrict__ dh, int act, int e, int64_t c_max, int h,
+               const __nv_bfloat16 *__restrict__ dh, int e, int64_t c_max, int h,
                const int32_t *__restrict__ counts, const int32_t *__restrict__ c_dev,
                __nv_bfloat16 *__restrict__ d_pre, int32_t *status) {
     pdl_enter();
     if (status_bad(status)) return;
-    const bool swiglu = act == MOE_ACT_SWIGLU;
+    constexpr bool swiglu = ACT == MOE_ACT_SWIGLU;
     const int j = blockIdx.y;
     const int64_t kept = min((int64_t)min(counts[j], *c_dev), c_max);
     const int hv = h / 8;                                  // 16-byte chunks per row
@@ -168,8 +187,8 @@ act_bwd_kernel(const __nv_bfloat16 *__restrict__ pa, const __nv_bfloat16 *__rest
 #pragma unroll
             for (int u = 0; u < AB_U; u++) {
                 if (q0 + u * AB_THREADS < n)
-                    act_bwd_chunk(va[u], vb[u], vg[u], act, d_pre + (row0 + rr[u]) * h2 + cc[u] * 8,
-                                  h);
+                    act_bwd_chunk<ACT>(va[u], vb[u], vg[u], d_pre + (row0 + rr[u]) * h2 + cc[u] * 8,
+                                       h);
             }
         }
     }
@@ -256,8 +275,15 @@ moe_status act_bwd_launch(const __nv_bfloat16 *pa, const __nv_bfloat16 *pb,
     if (h % 8 != 0 || e < 1 || e > 65535) return MOE_ERR_INVALID_ARG;
     int64_t gx = (c_max + AB_ROWS - 1) / AB_ROWS;
     if (gx > AB_GRID_X) gx = AB_GRID_X;   // CTAs per expert; they stride over the kept rows
-    return launch_pdl(act_bwd_kernel, dim3((unsigned)gx, (unsigned)e), dim3(AB_THREADS), 0, stream,
-                      pa, pb, d_hid, (int)act, e, c_max, h, counts, c_dev, d_pre, status);
+    const dim3 grid((unsigned)gx, (unsigned)e);
+    if (act == MOE_ACT_SWIGLU)
+        return launch_pdl(act_bwd_kernel<MOE_ACT_SWIGLU>, grid, dim3(AB_THREADS), 0, stream, pa, pb,
+                          d_hid, e, c_max, h, counts, c_dev, d_pre, status);
+    if (act == MOE_ACT_RELU)
+        return launch_pdl(act_bwd_kernel<MOE_ACT_RELU>, grid, dim3(AB_THREADS), 0, stream, pa, pb,
+                          d_hid, e, c_max, h, counts, c_dev, d_pre, status);
+    return launch_pdl(act_bwd_kernel<MOE_ACT_GELU>, grid, dim3(AB_THREADS), 0, stream, pa, pb, d_hid,
+                      e, c_max, h, counts, c_dev, d_pre, status);
 }
 
 moe_status colsum_launch(const __nv_bfloat16 *src, int e, int64_t c_max, int cols,
