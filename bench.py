@@ -79,7 +79,7 @@ def parse(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graded", action="store_true",
                     help="skip the stage breakdowns of the other graded workloads")
-    ap.add_argument("--only", choices=["gate", "gate_bwd"],
+    ap.add_argument("--only", choices=["gate", "gate_bwd", "backward"],
                     help="time one stage alone on the config's inputs (its own JSON line, not the "
                          "layer's): only the tensors that stage reads are drawn")
     return ap.parse_args(argv)
@@ -776,6 +776,22 @@ def run_ours(args, rank, world, local_rank):
     return res
 
 
+def run_only_backward(args):
+    """The backward chain alone on the config's layer (one forward first):
+    decode backward, expert FFN backward, encode backward and gate backward,
+    each timed call by call (L2 flushed before each), plus the whole forward +
+    backward chain."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w, wseed = CONFIGS[args.config]
+    run = LayerRun(w, wseed, dev, L2Flush(torch, dev))
+    ms = run.backward_chain(args.steps, args.warmup, None)
+    return {"stage": "backward", "workload": w.name, "steps": args.steps,
+            "ms": {k: round(v, 5) for k, v in ms.items()}}
+
+
 def run_only_gate(args):
     """The gate (or, with --only gate_bwd, the gate backward: d_logits, d_wg,
     d_bias and d_x from unit-normal d_gates) alone on the config's x, gate
@@ -869,7 +885,8 @@ def main():
         return
     if args.only:
         if rank == 0:
-            print(json.dumps(run_only_gate(args)))
+            print(json.dumps(run_only_backward(args) if args.only == "backward" else
+                             run_only_gate(args)))
         return
     if world > 1:
         import torch
