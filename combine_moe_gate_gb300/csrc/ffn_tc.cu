@@ -48,7 +48,9 @@ constexpr int MAX_E = 1024;
 constexpr unsigned long long WAIT_NS = 1000000000ull;  // 1 s per wait
 constexpr int SMEM_RING = 192 * 1024;   // operand ring per CTA
 
-enum Epi { EPI_GELU = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_BIAS = 3 };
+// EPI_BIAS_BMN: the bias epilogue with B read MN-major, straight from a
+// row-major [K, N] tensor (the weights of the data-gradient products).
+enum Epi { EPI_GELU = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_BIAS = 3, EPI_BIAS_BMN = 4 };
 
 // Tile shape.  TM = 1: 128 x 256 tiles, two 256-column accumulators in TMEM so
 // the epilogue of one tile overlaps the main loop of the next.  TM = 2:
@@ -97,6 +99,8 @@ constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >
 // The same for the 2-SM MMA: M = 256 over the CTA pair (128 rows per CTA).
 constexpr uint32_t IDESC_PAIR = (1u << 4) | (1u << 7) | (1u << 10) |
                                 ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((2 * UM) >> 4) << 24);
+// ... with B MN-major (bit 16).
+constexpr uint32_t IDESC_PAIR_BMN = IDESC_PAIR | (1u << 16);
 
 template <int STAGES>
 struct Ctl {  // control block in shared memory
@@ -344,6 +348,15 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
            ((uint64_t)((ROWB * 8) >> 4) << 32) | ((uint64_t)1 << 46) | (mode << 61);
 }
 
+// Shared-memory matrix descriptor of an MN-major operand in the 128-byte
+// swizzled layout TMA writes for boxes of 64 elements along M/N by BK rows
+// along K: 8-row groups along K 1024 bytes apart (stride byte offset), the
+// 64-element blocks along M/N `lbo` bytes apart (leading byte offset).
+__device__ __forceinline__ uint64_t sdesc_mn(uint32_t saddr, uint32_t lbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
 __device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -355,13 +368,14 @@ __device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, ui
 
 // 2-SM MMA, issued by the pair's first CTA: A and B descriptors name the same
 // shared-memory offsets in both CTAs; each CTA's TMEM receives its 128 rows.
+template <uint32_t ID = IDESC_PAIR>
 __device__ __forceinline__ void umma_pair(uint32_t tmem_d, uint64_t a, uint64_t b,
                                           uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(a), "l"(b), "r"(IDESC_PAIR), "r"(accumulate)
+        "l"(a), "l"(b), "r"(ID), "r"(accumulate)
         : "memory");
 }
 
@@ -486,6 +500,8 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
               const GemmArgs args) {
     using TL = Tiling<TM, BK, CL, TN>;
     static_assert(TN == 1 || EPI != EPI_SWIGLU, "SwiGLU tiles pair W1 and W3 in one N = 256 MMA");
+    constexpr bool BMN = EPI == EPI_BIAS_BMN;   // B MN-major: [K, N] rows, boxes of 64 columns
+    static_assert(!BMN || (CL == 2 && TN == 2 && BK == 64), "MN-major B on 256 x 512 pair tiles");
     constexpr bool PAIR = TL::PAIR;
     constexpr int STAGES = TL::STAGES, BMT = TL::BMT, A_BYTES = TL::A_BYTES;
     constexpr int B_BYTES = TL::B_BYTES, ROWB = TL::ROWB;
@@ -626,6 +642,17 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                             if (prank == 0) mbar_expect_tx(&ctl->full[stage], 2 * A_BOX_BYTES);
                             tma_load_2d_pair(sA + stage * A_BYTES + hh * A_BOX_BYTES, &tmA, kb * BK,
                                              a_row, fb);
+                        } else if (BMN) {
+                            // this CTA's 128 columns of N sub-tile hh, K rows kb*BK ..:
+                            // two boxes of 64 columns (b_row - j * b_rows is the column)
+                            if (prank == 0) mbar_expect_tx(&ctl->full[stage], 2 * B_BOX_BYTES);
+                            const int n_col = b_row - T.j * args.b_rows;
+                            const int k_row = T.j * args.b_rows + kb * BK;
+#pragma unroll
+                            for (int i = 0; i < 2; i++)
+                                tma_load_2d_pair(sB + stage * B_BYTES + hh * B_BOX_BYTES +
+                                                     i * (B_BOX_BYTES / 2),
+                                                 &tmB, n_col + 64 * i, k_row, fb);
                         } else {
                             // SwiGLU: the first CTA's half of B is W1, the second's W3
                             if (prank == 0) mbar_expect_tx(&ctl->full[stage], 2 * B_BOX_BYTES);
@@ -688,7 +715,17 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     const uint32_t b0 = su32(sB + stage * B_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < BK / UK; kk++) {
-                        if (PAIR) {
+                        if (BMN) {
+                            // B: K rows of 128 bytes, kk * UK rows in; blocks of 64
+                            // columns (B_BYTES / TN / 2 bytes) apart
+#pragma unroll
+                            for (int tn = 0; tn < TN; tn++)
+                                umma_pair<IDESC_PAIR_BMN>(
+                                    d + (uint32_t)(tn * BN), sdesc<ROWB>(a0 + kk * UK * 2),
+                                    sdesc_mn(b0 + tn * (B_BYTES / TN) + kk * UK * 128,
+                                             B_BYTES / TN / 2),
+                                    (kb | kk) != 0);
+                        } else if (PAIR) {
 #pragma unroll
                             for (int tn = 0; tn < TN; tn++)  // N sub-tiles share the A tile
                                 umma_pair(d + (uint32_t)(tn * BN), sdesc<ROWB>(a0 + kk * UK * 2),
@@ -1058,7 +1095,7 @@ namespace {
 constexpr int64_t up256i(int64_t b) { return (b + 255) & ~(int64_t)255; }
 
 struct BwdLayout {
-    int64_t pa, pb, dh, dpre, wT, w2T, doT, hidT, dpT, bufT, total;
+    int64_t pa, pb, dh, dpre, wT, doT, hidT, dpT, bufT, total;
 };
 
 BwdLayout bwd_layout(moe_act act, int e, int64_t c_max, int m, int h) {
@@ -1071,8 +1108,7 @@ BwdLayout bwd_layout(moe_act act, int e, int64_t c_max, int m, int h) {
     L.pb = take(swiglu ? E * c_max * h * 2 : 0);
     L.dh = take(E * c_max * h * 2);
     L.dpre = take(E * c_max * H2 * 2);
-    L.wT = take(E * m * H2 * 2);
-    L.w2T = take(E * h * m * 2);
+    L.wT = take(swiglu ? E * m * H2 * 2 : 0);   // [W1 | W3] transposed (SwiGLU only)
     L.doT = take(E * m * Kp * 2);
     L.hidT = take(E * h * Kp * 2);
     L.dpT = take((swiglu ? 2 : 1) * E * h * Kp * 2);
@@ -1100,6 +1136,22 @@ moe_status gemm_bias(const void *a, const void *b, int b_rows, void *out, const 
     return launch_gemm<EPI_BIAS, 1, 64, 2, 2>(mA, mB, mB, mO, g, stream);
 }
 
+// The same with B MN-major: out[j] = A[j] B[j] with B [e * K, n_out] row-major
+// (K rows per expert; rows past an expert's K meet zero columns of A).
+moe_status gemm_bias_bmn(const void *a, const void *b, void *out, const int32_t *counts,
+                         const int32_t *c_dev, int e, int64_t c_max, int K, int n_out, int32_t *st,
+                         cudaStream_t stream) {
+    using T2 = Tiling<1, 64, 2, 2>;
+    CUtensorMap mA, mB, mO;
+    if (!make_map(&mA, a, (uint64_t)e * c_max, (uint64_t)K, T2::A_BOX_ROWS, 64) ||
+        !make_map(&mB, b, (uint64_t)e * K, (uint64_t)n_out, 64, 64) ||
+        !make_map(&mO, out, (uint64_t)e * c_max, (uint64_t)n_out, 32, 32))
+        return MOE_ERR_CUDA;
+    GemmArgs g{counts, c_dev, st, nullptr, (__nv_bfloat16 *)out, c_max, e, K, n_out, K, nullptr,
+               nullptr, 0, 0};
+    return launch_gemm<EPI_BIAS_BMN, 1, 64, 2, 2>(mA, mB, mB, mO, g, stream);
+}
+
 }  // namespace
 
 size_t ffn_tc_bwd_workspace_bytes(moe_act act, int e, int64_t c_max, int m, int h) {
@@ -1118,7 +1170,7 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
     if (Kp > 0x7fffffff || H2 > 0x7fffffff) return MOE_ERR_UNSUPPORTED;
     char *w = (char *)ws;
     bf *pa = (bf *)(w + L.pa), *pb = (bf *)(w + L.pb), *dh = (bf *)(w + L.dh);
-    bf *dpre = (bf *)(w + L.dpre), *wT = (bf *)(w + L.wT), *w2T = (bf *)(w + L.w2T);
+    bf *dpre = (bf *)(w + L.dpre), *wT = (bf *)(w + L.wT);
     bf *doT = (bf *)(w + L.doT), *hidT = (bf *)(w + L.hidT), *dpT = (bf *)(w + L.dpT);
     bf *bufT = (bf *)(w + L.bufT);
     moe_status r;
@@ -1127,23 +1179,26 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
         r = (x);   \
         if (r != MOE_OK) return r; \
     } while (0)
-    // weights as K-major B operands of the data-gradient products (experts
-    // without kept rows are skipped: no tile of theirs reads them)
-    MOE_TRY(transpose_pad_launch((const bf *)w2, (int64_t)m * h, h, w2T, (int64_t)h * m, m, e, m, h,
-                                 m, nullptr, counts, c_dev, st, stream));
-    MOE_TRY(transpose_pad_launch((const bf *)w1, (int64_t)h * m, m, wT, (int64_t)m * H2, H2, e, h, m,
-                                 h, nullptr, counts, c_dev, st, stream));
-    if (swiglu)
+    // the data-gradient products read W2 (and W1 for ReLU / GELU) MN-major in
+    // place; SwiGLU's [W1 | W3] contraction reads one K-major transposed copy
+    // (experts without kept rows are skipped: no tile of theirs reads them)
+    if (swiglu) {
+        MOE_TRY(transpose_pad_launch((const bf *)w1, (int64_t)h * m, m, wT, (int64_t)m * H2, H2, e,
+                                     h, m, h, nullptr, counts, c_dev, st, stream));
         MOE_TRY(transpose_pad_launch((const bf *)w3, (int64_t)h * m, m, wT + h, (int64_t)m * H2, H2,
                                      e, h, m, h, nullptr, counts, c_dev, st, stream));
+    }
     // pre-activations, recomputed; then d_hid, d_pre, d_buf
     MOE_TRY(gemm_bias(buf, w1, h, pa, swiglu ? nullptr : b1, counts, c_dev, e, c_max, m, h, st,
                       stream));
     if (swiglu) MOE_TRY(gemm_bias(buf, w3, h, pb, nullptr, counts, c_dev, e, c_max, m, h, st, stream));
-    MOE_TRY(gemm_bias(d_out, w2T, h, dh, nullptr, counts, c_dev, e, c_max, m, h, st, stream));
+    MOE_TRY(gemm_bias_bmn(d_out, w2, dh, counts, c_dev, e, c_max, m, h, st, stream));
     MOE_TRY(act_bwd_launch(pa, swiglu ? pb : nullptr, dh, act, e, c_max, h, counts, c_dev, dpre, st,
                            stream));
-    MOE_TRY(gemm_bias(dpre, wT, m, d_buf, nullptr, counts, c_dev, e, c_max, (int)H2, m, st, stream));
+    if (swiglu)
+        MOE_TRY(gemm_bias(dpre, wT, m, d_buf, nullptr, counts, c_dev, e, c_max, (int)H2, m, st, stream));
+    else
+        MOE_TRY(gemm_bias_bmn(dpre, w1, d_buf, counts, c_dev, e, c_max, h, m, st, stream));
     // weight gradients: the kept rows are the contraction, each expert over
     // its own (zero-padded past them up to the GEMM's next 64-deep K block;
     // past Kp its tensor map fills zeros)
