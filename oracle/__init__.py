@@ -18,8 +18,11 @@ from .core import (  # noqa: F401
     decode_bwd,
     encode,
     encode_bwd,
+    fc_fp8,
     ffn_bwd,
     ffn_rows,
+    fp8_decode,
+    fp8_encode,
     gate_bwd,
     gate_chunk,
     gate_logits,
@@ -29,6 +32,7 @@ from .core import (  # noqa: F401
     layer_backward,
     layer_forward,
     locations,
+    quantize_rows_fp8,
     round_bf16,
     set_threads,
     to_f32,

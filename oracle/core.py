@@ -59,6 +59,10 @@ def _L():
                 "orc_ffn_bwd": [P, P, P, P, P, I32, I32, I64, I32, I32, I32, P, P, P, P, P, P, P,
                                 P],
                 "orc_round_bf16": [D],
+                "orc_quantize_rows_fp8": [P, I64, I32, P, P],
+                "orc_fc_fp8": [P, P, P, P, P, I32, I64, I32, I32, P],
+                "orc_fp8_decode": [ctypes.c_uint8],
+                "orc_fp8_encode": [ctypes.c_float],
                 "orc_set_threads": [I32],
                 "orc_get_threads": [],
             }
@@ -68,6 +72,8 @@ def _L():
                 fn.restype = None
             lib.orc_capacity.restype = I64
             lib.orc_round_bf16.restype = ctypes.c_float
+            lib.orc_fp8_decode.restype = ctypes.c_float
+            lib.orc_fp8_encode.restype = ctypes.c_uint8
             lib.orc_get_threads.restype = I32
             _lib = lib
     return _lib
@@ -319,3 +325,43 @@ def layer_backward(w, inp, fwd, dy):
                d_x=dx_copy.astype(np.float64) + gate["d_x"])
     return res
 
+
+
+# ----------------------------------------------------------- FP8 experts
+FP8_ACT = {None: -1, "none": -1, "relu": 0, "gelu": 1}
+
+
+def fp8_decode(code: int) -> float:
+    """The value of one e4m3 code (NaN for 0x7F / 0xFF)."""
+    return float(_L().orc_fp8_decode(int(code) & 0xFF))
+
+
+def fp8_encode(v: float) -> int:
+    """e4m3 code of v: nearest, ties to even, saturating to +-448."""
+    return int(_L().orc_fp8_encode(float(v)))
+
+
+def quantize_rows_fp8(x):
+    """Row-wise e4m3 quantisation of a 2-D array (fp32 values or bf16 bits):
+    (codes uint8 [rows, cols], scales fp32 [rows]), scale = amax / 448."""
+    x = np.ascontiguousarray(to_f32(x))
+    rows, cols = x.shape
+    q = np.empty((rows, cols), np.uint8)
+    sc = np.empty(rows, np.float32)
+    _L().orc_quantize_rows_fp8(_p(x), rows, cols, _p(q), _p(sc))
+    return q, sc
+
+
+def fc_fp8(qa, sa, qw, sw, bias, act):
+    """act(sa[r] sw[n] sum_k a[r, k] w[n, k] + bias[n]) rounded to bf16, a and w
+    e4m3 codes [rows, K] and [N, K]: [rows, N] float32 holding bf16 values."""
+    qa = np.ascontiguousarray(qa, np.uint8)
+    qw = np.ascontiguousarray(qw, np.uint8)
+    sa = np.ascontiguousarray(sa, np.float32)
+    sw = np.ascontiguousarray(sw, np.float32)
+    bias = None if bias is None else np.ascontiguousarray(to_f32(bias))
+    rows, K = qa.shape
+    N = qw.shape[0]
+    out = np.empty((rows, N), np.float32)
+    _L().orc_fc_fp8(_p(qa), _p(sa), _p(qw), _p(sw), _p(bias), FP8_ACT[act], rows, K, N, _p(out))
+    return out

@@ -549,3 +549,88 @@ void orc_ffn_bwd(const float *buf, const float *w1, const float *b1, const float
         free(dh); free(dx);
     }
 }
+
+/* ------------------------------------------------- FP8 (e4m3) experts */
+
+/* Low-precision experts ([Tutel] profile, "notes" and "highlights": the
+ * inference formats FP8 / blockwise FP8).  The pages name the formats but no
+ * block size; this restatement scales every row of an operand by one fp32
+ * factor (one per token row of the activations, one per output channel of the
+ * weights), so that the factors apply once, after the contraction.
+ *
+ * e4m3 (the OCP FP8 E4M3 format): sign, 4 exponent bits with bias 7, 3
+ * mantissa bits; exponent field 0 holds the subnormals m * 2^-9; no
+ * infinities; exponent field 15 with mantissa 7 is NaN, so the largest finite
+ * magnitude is 1.75 * 2^8 = 448.  Encoding rounds to nearest, ties to even,
+ * and saturates finite values beyond 448 to +-448. */
+float orc_fp8_decode(uint8_t c)
+{
+    int s = c >> 7, ef = (c >> 3) & 15, mf = c & 7;
+    double v;
+    if (ef == 15 && mf == 7) return NAN;
+    if (ef == 0) v = ldexp((double)mf, -9);
+    else v = ldexp(1.0 + mf / 8.0, ef - 7);
+    return (float)(s ? -v : v);
+}
+
+uint8_t orc_fp8_encode(float x)
+{
+    if (isnan(x)) return 0x7F;
+    uint8_t sgn = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0) return sgn | 0x7E;
+    if (a < ldexp(1.0, -6)) {                       /* subnormal range: quantum 2^-9 */
+        double r = nearbyint(ldexp(a, 9));          /* ties to even */
+        return sgn | (uint8_t)r;                    /* r = 8 is the smallest normal */
+    }
+    int ex;
+    frexp(a, &ex);                                  /* a in [2^(ex-1), 2^ex) */
+    int E = ex - 1;                                 /* unbiased exponent, >= -6 */
+    double r = nearbyint(ldexp(a, 3 - E));          /* in [8, 16], ties to even */
+    if (r == 16.0) { E += 1; r = 8.0; }
+    if (E > 8 || (E == 8 && r > 14.0)) return sgn | 0x7E;   /* past 448: saturate */
+    return sgn | (uint8_t)(((E + 7) << 3) | ((int)r - 8));
+}
+
+/* Row quantisation: for each of `rows` rows of `cols` values, amax = max |x|,
+ * scale = amax / 448 (fp32 division; 1 for an all-zero row), and every value
+ * x / scale (fp32 division) encoded as e4m3. */
+void orc_quantize_rows_fp8(const float *x, int64_t rows, int cols, uint8_t *q, float *scale)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; r++) {
+        const float *xr = x + r * cols;
+        float amax = 0.0f;
+        for (int i = 0; i < cols; i++) {
+            float v = fabsf(xr[i]);
+            if (v > amax) amax = v;
+        }
+        float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+        scale[r] = s;
+        for (int i = 0; i < cols; i++) q[r * cols + i] = orc_fp8_encode(xr[i] / s);
+    }
+}
+
+/* One e4m3 product layer: out[r, n] = act(sa[r] * sw[n] * sum_k a[r, k] w[n, k]
+ * + bias[n]) with a and w the decoded e4m3 codes, the sum in double, rounded
+ * once to bf16.  act: -1 none, ORC_ACT_RELU, ORC_ACT_GELU (exact erf).  a
+ * [rows, K], w [N, K], bias [N] or NULL, out [rows, N]. */
+void orc_fc_fp8(const uint8_t *qa, const float *sa, const uint8_t *qw, const float *sw,
+                const float *bias, int act, int64_t rows, int K, int N, float *out)
+{
+    float dec[256];
+    for (int c = 0; c < 256; c++) dec[c] = orc_fp8_decode((uint8_t)c);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; r++) {
+        for (int n = 0; n < N; n++) {
+            double acc = 0.0;
+            for (int k = 0; k < K; k++)
+                acc += (double)dec[qa[r * K + k]] * (double)dec[qw[(int64_t)n * K + k]];
+            double v = (double)sa[r] * (double)sw[n] * acc;
+            if (bias) v += (double)bias[n];
+            if (act == ORC_ACT_RELU) v = v > 0.0 ? v : 0.0;
+            else if (act == ORC_ACT_GELU) v = 0.5 * v * (1.0 + erf(v / sqrt(2.0)));
+            out[r * N + n] = round_bf16(v);
+        }
+    }
+}
