@@ -70,6 +70,9 @@ def load():
         "moe_layer_forward_pipelined": (I, [P, I, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, I64,
                                             U, P, P, P, P, P, P, P, P, P, SZ, P, I, P, P, P]),
         "moe_probe_fp32_fma": (I, [I, I, I, P, P]),
+        "moe_quantize_rows_fp8": (I, [P, I64, I64, I, P, P, P, P, P, P]),
+        "moe_expert_ffn_fp8_workspace_size": (SZ, [I, I64, I, I]),
+        "moe_expert_ffn_fp8": (I, [P, P, P, P, P, P, P, P, P, P, I, I, I64, I, I, P, SZ, P, P, P]),
         "moe_status_str": (ctypes.c_char_p, [I]),
         "moe_launch_count": (ctypes.c_uint64, []),
     }
@@ -243,6 +246,46 @@ def moe_expert_ffn(buf, counts, c_dev, w1, b1, w3, w2, b2, act, workspace, out, 
         _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _ptr(out, "out", dt, (e, c_max, m)), _ptr(dev_status, "dev_status", I),
         _stream(stream)), "moe_expert_ffn")
+
+
+def moe_expert_ffn_fp8_workspace_size(e, c_max, m, h) -> int:
+    return int(load().moe_expert_ffn_fp8_workspace_size(int(e), int(c_max), int(m), int(h)))
+
+
+def moe_quantize_rows_fp8(src, q, scale, dev_status, counts=None, c_dev=None, stream=None):
+    """e4m3 codes (uint8, src's shape) and per-row fp32 scales of a bf16 tensor
+    [rows, cols] or [batches, rows, cols]; with counts / c_dev only the kept
+    rows of each batch."""
+    import torch
+
+    shape = tuple(src.shape) if src.dim() == 3 else (1,) + tuple(src.shape)
+    b, r, c = shape
+    I = _i32()
+    _check(load().moe_quantize_rows_fp8(
+        _ptr(src, "src", torch.bfloat16), b, r, c,
+        _ptr(counts, "counts", I, (b,)) if counts is not None else None,
+        _ptr(c_dev, "c_dev", I) if c_dev is not None else None,
+        _ptr(q, "q", torch.uint8, tuple(src.shape)),
+        _ptr(scale, "scale", _f32(), tuple(src.shape[:-1])), _ptr(dev_status, "dev_status", I),
+        _stream(stream)), "moe_quantize_rows_fp8")
+
+
+def moe_expert_ffn_fp8(buf_q, buf_scale, counts, c_dev, w1_q, w1_scale, b1, w2_q, w2_scale, b2,
+                       act, workspace, out, dev_status, stream=None):
+    import torch
+
+    e, c_max, m = buf_q.shape
+    h = w1_q.shape[1]
+    I, F, U8, bf = _i32(), _f32(), torch.uint8, torch.bfloat16
+    _check(load().moe_expert_ffn_fp8(
+        _ptr(buf_q, "buf_q", U8), _ptr(buf_scale, "buf_scale", F, (e, c_max)),
+        _ptr(counts, "counts", I, (e,)), _ptr(c_dev, "c_dev", I),
+        _ptr(w1_q, "w1_q", U8, (e, h, m)), _ptr(w1_scale, "w1_scale", F, (e, h)),
+        _ptr(b1, "b1", bf, (e, h)), _ptr(w2_q, "w2_q", U8, (e, m, h)),
+        _ptr(w2_scale, "w2_scale", F, (e, m)), _ptr(b2, "b2", bf, (e, m)), _act(act), e, c_max,
+        m, h, _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _ptr(out, "out", bf, (e, c_max, m)), _ptr(dev_status, "dev_status", I), _stream(stream)),
+        "moe_expert_ffn_fp8")
 
 
 def moe_expert_ffn_bwd(buf, hid, counts, c_dev, w1, b1, w3, w2, act, d_out, workspace, d_buf,

@@ -45,6 +45,15 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
                          void *hid, void *out, int32_t *st, cudaStream_t stream, int row_lo,
                          int row_hi);
 size_t ffn_tc_bwd_workspace_bytes(moe_act act, int e, int64_t c_max, int m, int h);
+moe_status quantize_rows_fp8_launch(const void *src, int64_t batches, int64_t rows_per_batch,
+                                    int cols, const int32_t *counts, const int32_t *c_dev,
+                                    void *q, float *scale, int32_t *st, cudaStream_t stream);
+moe_status ffn_tc_fp8_launch(const void *buf_q, const float *buf_scale, const int32_t *counts,
+                             const int32_t *c_dev, const void *w1_q, const float *w1_scale,
+                             const void *b1, const void *w2_q, const float *w2_scale,
+                             const void *b2, moe_act act, int e, int64_t c_max, int m, int h,
+                             void *hid, void *hid_q, float *hid_scale, void *out, int32_t *st,
+                             cudaStream_t stream);
 moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *counts,
                              const int32_t *c_dev, const void *w1, const void *b1, const void *w3,
                              const void *w2, moe_act act, int e, int64_t c_max, int m, int h,
@@ -405,6 +414,48 @@ moe_status moe_layer_forward_pipelined(const void *x, moe_dtype dt, const float 
         if (r != MOE_OK) return r;
     }
     return moe_decode(out, dt, idx, loc, gates, c_dev, s, m, e, k, c_max, y, dev_status, stream);
+}
+
+size_t moe_expert_ffn_fp8_workspace_size(int e, int64_t c_max, int m, int h) {
+    if (e < 1 || e > kMaxE || c_max < 1 || m < 16 || h < 16 || m % 16 || h % 16) return 0;
+    const int64_t rows = (int64_t)e * c_max;
+    return up256((size_t)rows * h * 2) + up256((size_t)rows * h) + up256((size_t)rows * 4);
+}
+
+moe_status moe_quantize_rows_fp8(const void *src, int64_t batches, int64_t rows_per_batch,
+                                 int cols, const int32_t *counts, const int32_t *c_dev, void *q,
+                                 float *scale, int32_t *dev_status, void *stream) {
+    if (batches < 1 || batches > 0x7fffffff || rows_per_batch < 1 || cols < 16 || cols % 16 ||
+        batches * rows_per_batch > ((int64_t)1 << 40) || !ok16(src) || !ok16(q) || !ok4(scale) ||
+        !ok4(dev_status) || (counts == nullptr) != (c_dev == nullptr) ||
+        (counts && (!ok4(counts) || !ok4(c_dev))))
+        return MOE_ERR_INVALID_ARG;
+    return quantize_rows_fp8_launch(src, batches, rows_per_batch, cols, counts, c_dev, q, scale,
+                                    dev_status, as_stream(stream));
+}
+
+moe_status moe_expert_ffn_fp8(const void *buf_q, const float *buf_scale, const int32_t *counts,
+                              const int32_t *c_dev, const void *w1_q, const float *w1_scale,
+                              const void *b1, const void *w2_q, const float *w2_scale,
+                              const void *b2, moe_act act, int e, int64_t c_max, int m, int h,
+                              void *workspace, size_t workspace_bytes, void *out,
+                              int32_t *dev_status, void *stream) {
+    const size_t need = moe_expert_ffn_fp8_workspace_size(e, c_max, m, h);
+    if (need == 0 || c_max > 0x7fffffff || !ok16(buf_q) || !ok4(buf_scale) || !ok4(counts) ||
+        !ok4(c_dev) || !ok16(w1_q) || !ok16(w1_scale) || !opt16(b1) || !ok16(w2_q) ||
+        !ok16(w2_scale) || !opt16(b2) || !ok16(workspace) || workspace_bytes < need ||
+        !ok16(out) || !ok4(dev_status))
+        return MOE_ERR_INVALID_ARG;
+    if (act != MOE_ACT_RELU && act != MOE_ACT_GELU) return MOE_ERR_UNSUPPORTED;
+    if (!ffn_tc_supported(e, c_max, m, h)) return MOE_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)e * c_max;
+    char *w = (char *)workspace;
+    void *hid = w;
+    void *hid_q = w + up256((size_t)rows * h * 2);
+    float *hid_scale = (float *)(w + up256((size_t)rows * h * 2) + up256((size_t)rows * h));
+    return ffn_tc_fp8_launch(buf_q, buf_scale, counts, c_dev, w1_q, w1_scale, b1, w2_q, w2_scale, b2,
+                             act, e, c_max, m, h, hid, hid_q, hid_scale, out, dev_status,
+                             as_stream(stream));
 }
 
 moe_status moe_probe_fp32_fma(int packed, int blocks, int iters, float *out, void *stream) {

@@ -67,25 +67,26 @@ enum Epi { EPI_GELU = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_BIAS = 3, EPI_BIAS_BM
 // or 32 (64-byte swizzle); the smaller stage doubles the number of stages in
 // the same shared memory, i.e. more operand bytes in flight to cover L2/HBM
 // latency.
-template <int TM, int BK_, int CL_ = 1, int TN_ = 1>
+template <int TM, int BK_, int CL_ = 1, int TN_ = 1, int EB_ = 2>
 struct Tiling {
+    static constexpr int EB = EB_;                        // bytes per operand element (2 bf16, 1 e4m3)
     static constexpr int TN = TN_;                        // N = 256 MMAs per K step (pairs)
     static constexpr int CL = CL_;                        // CTAs per cluster: 1 or 2
     static constexpr bool PAIR = CL > 1;                  // 2-SM MMA on CTA pairs
     static constexpr int BK = BK_;
-    static constexpr int ROWB = BK * 2;                   // bytes per operand row
+    static constexpr int ROWB = BK * EB;                  // bytes per operand row
     static constexpr int A_ROWS = UM * TM;                // rows of A per CTA and stage
     static constexpr int B_ROWS = PAIR ? TN * BN / 2 : BN;  // rows of B per CTA and stage
     static constexpr int BMT = A_ROWS * (PAIR ? 2 : 1);   // rows of A per tile
     static constexpr int A_BOX_ROWS = A_ROWS / 2;                    // rows of one A copy
     static constexpr int B_BOX_ROWS = B_ROWS / 2;                    // rows of one B copy
-    static constexpr int A_BYTES = A_ROWS * BK * 2;
-    static constexpr int B_BYTES = B_ROWS * BK * 2;
+    static constexpr int A_BYTES = A_ROWS * ROWB;
+    static constexpr int B_BYTES = B_ROWS * ROWB;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = SMEM_RING / STAGE_BYTES;
     static constexpr int NACC = TM == 1 && TN == 1 ? 2 : 1;  // accumulator buffers
     static constexpr int ACC_COLS = BN * TM * TN;         // TMEM columns per buffer
-    static_assert(BK == 64 || BK == 32, "BK");
+    static_assert(ROWB == 128 || ROWB == 64, "BK");
     static_assert(CL == 1 || CL == 2, "cluster size");
     static_assert(!PAIR || TM == 1, "pair tiles use one M=256 MMA");
     static_assert(TN == 1 || (TN == 2 && CL == 2), "512-column tiles on plain CTA pairs");
@@ -101,6 +102,10 @@ constexpr uint32_t IDESC_PAIR = (1u << 4) | (1u << 7) | (1u << 10) |
                                 ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((2 * UM) >> 4) << 24);
 // ... with B MN-major (bit 16).
 constexpr uint32_t IDESC_PAIR_BMN = IDESC_PAIR | (1u << 16);
+// kind::f8f6f4 with A and B e4m3 (format 0), D fp32, both K-major; the 2-SM
+// MMA, K = 32 elements (32 bytes, as kind::f16's 16 elements).
+constexpr uint32_t IDESC_PAIR_F8 = (1u << 4) | ((uint32_t)(BN >> 3) << 17) |
+                                   ((uint32_t)((2 * UM) >> 4) << 24);
 
 template <int STAGES>
 struct Ctl {  // control block in shared memory
@@ -147,6 +152,11 @@ struct GemmArgs {
     // are computed (row_hi = 0: no upper end); rows are addressed from row_lo.
     int row_lo;
     int row_hi;
+    // e4m3 operands: the fp32 scale of every A row ([e * c_max]) and of every
+    // B row, i.e. output column ([e * n_out]); the epilogue forms
+    // acc * (a_scale * b_scale) + bias.  NULL for bf16.
+    const float *a_scale;
+    const float *b_scale;
 };
 
 // ------------------------------------------------------------- PTX wrappers
@@ -379,6 +389,16 @@ __device__ __forceinline__ void umma_pair(uint32_t tmem_d, uint64_t a, uint64_t 
         : "memory");
 }
 
+__device__ __forceinline__ void umma_pair_f8(uint32_t tmem_d, uint64_t a, uint64_t b,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(IDESC_PAIR_F8), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -493,13 +513,15 @@ __device__ __forceinline__ Tile decode_tile(const int32_t *tile_start, int e, in
     return T;
 }
 
-template <int EPI, int TM, int BK, int CL, int TN>
+template <int EPI, int TM, int BK, int CL, int TN, int EB = 2>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmO,
               const GemmArgs args) {
-    using TL = Tiling<TM, BK, CL, TN>;
+    using TL = Tiling<TM, BK, CL, TN, EB>;
     static_assert(TN == 1 || EPI != EPI_SWIGLU, "SwiGLU tiles pair W1 and W3 in one N = 256 MMA");
+    constexpr bool F8 = EB == 1;   // e4m3 operands (kind::f8f6f4), scaled epilogue
+    static_assert(!F8 || (CL == 2 && EPI != EPI_SWIGLU && EPI != EPI_BIAS_BMN), "e4m3 pair tiles");
     constexpr bool BMN = EPI == EPI_BIAS_BMN;   // B MN-major: [K, N] rows, boxes of 64 columns
     static_assert(!BMN || (CL == 2 && TN == 2 && BK == 64), "MN-major B on 256 x 512 pair tiles");
     constexpr bool PAIR = TL::PAIR;
@@ -714,8 +736,14 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     const uint32_t a0 = su32(sA + stage * A_BYTES);
                     const uint32_t b0 = su32(sB + stage * B_BYTES);
 #pragma unroll
-                    for (int kk = 0; kk < BK / UK; kk++) {
-                        if (BMN) {
+                    for (int kk = 0; kk < ROWB / 32; kk++) {   // one MMA per 32 bytes of K
+                        if (F8) {
+#pragma unroll
+                            for (int tn = 0; tn < TN; tn++)
+                                umma_pair_f8(d + (uint32_t)(tn * BN), sdesc<ROWB>(a0 + kk * 32),
+                                             sdesc<ROWB>(b0 + tn * (B_BYTES / TN) + kk * 32),
+                                             (kb | kk) != 0);
+                        } else if (BMN) {
                             // B: K rows of 128 bytes, kk * UK rows in; blocks of 64
                             // columns (B_BYTES / TN / 2 bytes) apart
 #pragma unroll
@@ -825,6 +853,9 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     reinterpret_cast<float4 *>(bsl + lane * 8)[1] = make_float4(b8[4], b8[5], b8[6], b8[7]);
                 }
                 __syncwarp();
+                // e4m3: this lane's row scale (its output row)
+                const float sa = F8 && valid ? args.a_scale[grow0 + lane] : 0.0f;
+                const float *bsc = F8 ? args.b_scale + (int64_t)T.j * args.n_out : nullptr;
 #pragma unroll 1
                 for (int c0 = 0; c0 < COLS; c0 += 64) {
                     uint32_t r[2][32];
@@ -847,11 +878,23 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                             const float4 bl = bp[0], bh = bp[1];
                             const float2 bb[4] = {make_float2(bl.x, bl.y), make_float2(bl.z, bl.w),
                                                   make_float2(bh.x, bh.y), make_float2(bh.z, bh.w)};
+                            float sc[8];   // e4m3: a_scale * b_scale of the 8 columns
+                            if (F8) {
+                                const int g8 = gcol + q * 8;
+                                float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+                                if (g8 < args.n_out) {   // n_out is a multiple of 16
+                                    lo = reinterpret_cast<const float4 *>(bsc + g8)[0];
+                                    hi = reinterpret_cast<const float4 *>(bsc + g8)[1];
+                                }
+                                sc[0] = sa * lo.x; sc[1] = sa * lo.y; sc[2] = sa * lo.z; sc[3] = sa * lo.w;
+                                sc[4] = sa * hi.x; sc[5] = sa * hi.y; sc[6] = sa * hi.z; sc[7] = sa * hi.w;
+                            }
 #pragma unroll
                             for (int i = 0; i < 4; i++) {
-                                float2 a = __fadd2_rn(make_float2(__uint_as_float(r[h2][q * 8 + 2 * i]),
-                                                                  __uint_as_float(r[h2][q * 8 + 2 * i + 1])),
-                                                      bb[i]);
+                                const float2 acc2 = make_float2(__uint_as_float(r[h2][q * 8 + 2 * i]),
+                                                                __uint_as_float(r[h2][q * 8 + 2 * i + 1]));
+                                float2 a = F8 ? __ffma2_rn(acc2, make_float2(sc[2 * i], sc[2 * i + 1]), bb[i])
+                                              : __fadd2_rn(acc2, bb[i]);
                                 if (EPI == EPI_GELU) a = gelu_erf2(a);
                                 else if (EPI == EPI_RELU) a = make_float2(fmaxf(a.x, 0.0f), fmaxf(a.y, 0.0f));
                                 pk[q * 4 + i] = pack_bf16(a.x, a.y);
@@ -938,6 +981,21 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, 
     return r == CUDA_SUCCESS;
 }
 
+// The same over an e4m3 (byte) matrix, box box_rows x 128 (128-byte swizzle).
+bool make_map_u8(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int sm_count() {
     static int cached[64] = {0};
     int dev = 0;
@@ -973,11 +1031,11 @@ int max_clusters(K kern, size_t smem, int cl) {
     return n;
 }
 
-template <int EPI, int TM, int BK, int CL, int TN>
+template <int EPI, int TM, int BK, int CL, int TN, int EB = 2>
 moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &b3,
                        const CUtensorMap &o, const GemmArgs &args, cudaStream_t stream) {
-    using TL = Tiling<TM, BK, CL, TN>;
-    auto kern = tc_group_gemm<EPI, TM, BK, CL, TN>;
+    using TL = Tiling<TM, BK, CL, TN, EB>;
+    auto kern = tc_group_gemm<EPI, TM, BK, CL, TN, EB>;
     constexpr size_t SMEM = smem_bytes<TL>();
     static int units[64] = {0};  // resident CTAs (CL = 1) or clusters, per device
     int dev = 0;
@@ -1066,6 +1124,44 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
     GemmArgs g2{counts, c_dev, st, (const __nv_bfloat16 *)b2, (__nv_bfloat16 *)out, c_max, e, h, m, m,
                 nullptr, nullptr, row_lo, row_hi};
     return launch_gemm<EPI_BIAS, TM2, BK2, CL2, TN2>(mA2, mB2, mB2, mO2, g2, stream);
+}
+
+moe_status quantize_rows_fp8_launch(const void *src, int64_t batches, int64_t rows_per_batch,
+                                    int cols, const int32_t *counts, const int32_t *c_dev,
+                                    void *q, float *scale, int32_t *st, cudaStream_t stream);
+
+// The expert FFN on e4m3 operands with one fp32 scale per row: fc1 on the
+// quantised rows and W1 (the same pair tiles as bf16, 128-element K blocks,
+// kind::f8f6f4), the scales, bias and activation in the epilogue, bf16 hidden;
+// the hidden rows quantised; fc2 likewise into bf16 out.  ReLU / GELU only.
+moe_status ffn_tc_fp8_launch(const void *buf_q, const float *buf_scale, const int32_t *counts,
+                             const int32_t *c_dev, const void *w1_q, const float *w1_scale,
+                             const void *b1, const void *w2_q, const float *w2_scale,
+                             const void *b2, moe_act act, int e, int64_t c_max, int m, int h,
+                             void *hid, void *hid_q, float *hid_scale, void *out, int32_t *st,
+                             cudaStream_t stream) {
+    constexpr int BKF = 128;   // e4m3 elements per K block (128 bytes)
+    using T1 = Tiling<1, BKF, 2, 1, 1>;
+    using T2 = Tiling<1, BKF, 2, 2, 1>;
+    CUtensorMap mA1, mB1, mO1, mA2, mB2, mO2;
+    if (!make_map_u8(&mA1, buf_q, (uint64_t)e * c_max, (uint64_t)m, T1::A_BOX_ROWS) ||
+        !make_map_u8(&mB1, w1_q, (uint64_t)e * h, (uint64_t)m, T1::B_BOX_ROWS) ||
+        !make_map(&mO1, hid, (uint64_t)e * c_max, (uint64_t)h, 32, 32) ||
+        !make_map_u8(&mA2, hid_q, (uint64_t)e * c_max, (uint64_t)h, T2::A_BOX_ROWS) ||
+        !make_map_u8(&mB2, w2_q, (uint64_t)e * m, (uint64_t)h, T2::B_BOX_ROWS) ||
+        !make_map(&mO2, out, (uint64_t)e * c_max, (uint64_t)m, 32, 32))
+        return MOE_ERR_CUDA;
+    GemmArgs g1{counts, c_dev, st, (const __nv_bfloat16 *)b1, (__nv_bfloat16 *)hid, c_max, e, m, h, h,
+                nullptr, nullptr, 0, 0, buf_scale, w1_scale};
+    moe_status r = act == MOE_ACT_GELU
+                       ? launch_gemm<EPI_GELU, 1, BKF, 2, 1, 1>(mA1, mB1, mB1, mO1, g1, stream)
+                       : launch_gemm<EPI_RELU, 1, BKF, 2, 1, 1>(mA1, mB1, mB1, mO1, g1, stream);
+    if (r != MOE_OK) return r;
+    r = quantize_rows_fp8_launch(hid, e, c_max, h, counts, c_dev, hid_q, hid_scale, st, stream);
+    if (r != MOE_OK) return r;
+    GemmArgs g2{counts, c_dev, st, (const __nv_bfloat16 *)b2, (__nv_bfloat16 *)out, c_max, e, h, m, m,
+                nullptr, nullptr, 0, 0, hid_scale, w2_scale};
+    return launch_gemm<EPI_BIAS, 1, BKF, 2, 2, 1>(mA2, mB2, mB2, mO2, g2, stream);
 }
 
 }  // namespace moe

@@ -283,6 +283,54 @@ moe_status moe_gate_bwd(const void *x, moe_dtype xdt, const float *wg, const flo
                         const float *gates, const float *d_gates, float *d_logits, float *d_wg,
                         float *d_bias, float *d_x, int32_t *dev_status, void *stream);
 
+/*
+ * Low-precision experts ([Tutel] profile, notes and highlights: FP8 among its
+ * inference formats, "blockwise FP8" without a block size).  Here an operand
+ * is e4m3 (OCP FP8 E4M3: 4 exponent bits, bias 7, 3 mantissa bits, largest
+ * finite 448) with one fp32 scale per row, so the scales apply once, after
+ * the contraction:
+ *   q[r, i] = e4m3(x[r, i] / scale[r]),  scale[r] = amax_i |x[r, i]| / 448
+ * (fp32 divisions, nearest-even, saturating at +-448; scale 1 for a zero row).
+ *
+ * moe_quantize_rows_fp8: src [batches, rows_per_batch, cols] bf16 -> q (same
+ * shape, one byte per code) and scale [batches, rows_per_batch] fp32.  With
+ * counts [batches] and c_dev (both or neither), only the rows r <
+ * min(counts[b], *c_dev, rows_per_batch) of batch b are written (the kept
+ * rows of an expert buffer); else every row (e.g. weights [e, rows, cols]).
+ * cols a multiple of 16.  Deterministic; the codes match an exact-arithmetic
+ * reference bit for bit.  This entry point extends the pages' expert FFN to
+ * the FP8 format.
+ */
+moe_status moe_quantize_rows_fp8(const void *src, int64_t batches, int64_t rows_per_batch,
+                                 int cols, const int32_t *counts, const int32_t *c_dev, void *q,
+                                 float *scale, int32_t *dev_status, void *stream);
+
+/* Bytes of device workspace moe_expert_ffn_fp8 needs (0: bad shape). */
+size_t moe_expert_ffn_fp8_workspace_size(int e, int64_t c_max, int m, int h);
+
+/*
+ * The expert FFN (ReLU / GELU) on e4m3 operands: buf_q [e, c_max, m] with
+ * buf_scale [e, c_max] (moe_quantize_rows_fp8 of the encoded buffer's kept
+ * rows), w1_q [e, h, m] with w1_scale [e, h], w2_q [e, m, h] with w2_scale
+ * [e, m] (weights quantised per output channel), b1 [e, h], b2 [e, m] bf16 or
+ * NULL.  For the kept rows of every expert:
+ *   hid = bf16(act(s_x s_w1 (x_q . w1_q^T) + b1));  hid quantised per row;
+ *   out = bf16(s_h s_w2 (hid_q . w2_q^T) + b2)
+ * with fp32 accumulation (tcgen05 kind::f8f6f4 on CTA pairs).  out [e, c_max,
+ * m] bf16.  m and h multiples of 16.  Workspace (moe_expert_ffn_fp8_workspace
+ * _size() bytes): the bf16 hidden [e, c_max, h] at offset 0, its codes [e,
+ * c_max, h] and its scales [e, c_max] fp32 after it, each starting on a
+ * 256-byte boundary; a caller may read them after the call.  SwiGLU returns
+ * MOE_ERR_UNSUPPORTED.  This entry point extends the pages' expert FFN to the
+ * FP8 format.
+ */
+moe_status moe_expert_ffn_fp8(const void *buf_q, const float *buf_scale, const int32_t *counts,
+                              const int32_t *c_dev, const void *w1_q, const float *w1_scale,
+                              const void *b1, const void *w2_q, const float *w2_scale,
+                              const void *b2, moe_act act, int e, int64_t c_max, int m, int h,
+                              void *workspace, size_t workspace_bytes, void *out,
+                              int32_t *dev_status, void *stream);
+
 /* Bytes of device workspace moe_layer_forward needs. */
 size_t moe_layer_workspace_size(moe_dtype dt, moe_act act, int64_t s, int m, int e, int k,
                                 int64_t c_max, int h);

@@ -173,4 +173,33 @@ def test_invalid_arguments_are_rejected_before_launch():
     assert fbc(a16=0) == INV                                     # workspace too small
     assert fbc(a13=100) == INV                                   # h not a multiple of 8
     assert fbc(a1=odd) == INV and fbc(a17=odd) == INV            # misaligned hid / d_buf
+    # e4m3 row quantisation: src, batches, rows_per_batch, cols, counts, c_dev, q, scale, status
+    qr = lib.moe_quantize_rows_fp8
+    qok = [A, 2, 8, 64, None, None, B, A, B, None]
+    def qrc(**kw):
+        a = list(qok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return qr(*a)
+    assert qrc(a3=40) == INV and qrc(a3=0) == INV                # cols not a multiple of 16
+    assert qrc(a1=0) == INV and qrc(a2=0) == INV                 # no rows
+    assert qrc(a4=A) == INV                                      # counts without c_dev
+    assert qrc(a0=odd) == INV and qrc(a6=odd) == INV             # misaligned src / codes
+    assert qrc(a7=None) == INV                                   # scales required
+    # e4m3 experts: buf_q, buf_scale, counts, c_dev, w1_q, w1_scale, b1, w2_q, w2_scale, b2,
+    # act, e, c_max, m, h, ws, ws_bytes, out, status, stream
+    f8 = lib.moe_expert_ffn_fp8
+    f8ok = [A, A, A, A, B, A, None, B, A, None, 1, 4, 64, 64, 128, A, 1 << 40, B, A, None]
+    def f8c(**kw):
+        a = list(f8ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f8(*a)
+    assert f8c(a10=2) == M.MOE_ERR_UNSUPPORTED                  # SwiGLU
+    assert f8c(a13=72) == INV and f8c(a14=40) == INV             # m, h not multiples of 16
+    assert f8c(a16=0) == INV                                     # workspace too small
+    assert f8c(a0=odd) == INV and f8c(a17=odd) == INV            # misaligned codes / out
+    assert f8c(a5=odd) == INV                                    # misaligned weight scales
+    assert M.moe_expert_ffn_fp8_workspace_size(4, 64, 64, 128) >= 4 * 64 * 128 * 3 + 4 * 64 * 4
+    assert M.moe_expert_ffn_fp8_workspace_size(4, 64, 72, 128) == 0
     assert M.launch_count() == before
