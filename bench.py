@@ -387,6 +387,49 @@ class LayerRun:
         M.moe_decode(b.out, b.idx, b.loc, b.gates, b.c_dev, b.y, b.status)
         ev[5].record()
 
+    def fp8_experts(self, steps, warmup):
+        """The layer with e4m3 experts (ReLU / GELU): the weights quantised per
+        output channel once (untimed), then per call the encoded buffer's
+        kept rows quantised and the e4m3 FFN, timed alone (L2 flushed before
+        each call), and the whole e4m3 layer step (gate, capacity, encode,
+        quantise, FFN, decode) through the same C calls."""
+        torch, M, w, b = self.torch, self.M, self.w, self.bufs
+        x, wg, gb, w1, b1, w3, w2, b2 = self.args()
+        dev = self.dev
+        if w.act not in ("relu", "gelu") or w.m % 16 or w.h % 16 or w.dtype != "bf16":
+            return None
+        st = b.status
+        w1q = torch.empty(w1.shape, dtype=torch.uint8, device=dev)
+        w2q = torch.empty(w2.shape, dtype=torch.uint8, device=dev)
+        w1s = torch.empty(w1.shape[:-1], dtype=torch.float32, device=dev)
+        w2s = torch.empty(w2.shape[:-1], dtype=torch.float32, device=dev)
+        M.moe_quantize_rows_fp8(w1, w1q, w1s, st)
+        M.moe_quantize_rows_fp8(w2, w2q, w2s, st)
+        bq = torch.empty(b.buf.shape, dtype=torch.uint8, device=dev)
+        bs = torch.empty(b.buf.shape[:-1], dtype=torch.float32, device=dev)
+        ws = torch.empty(M.moe_expert_ffn_fp8_workspace_size(w.e, b.c_max, w.m, w.h),
+                         dtype=torch.uint8, device=dev)
+        out8 = torch.empty_like(b.out)
+
+        def ffn():
+            M.moe_quantize_rows_fp8(b.buf, bq, bs, st, counts=b.counts, c_dev=b.c_dev)
+            M.moe_expert_ffn_fp8(bq, bs, b.counts, b.c_dev, w1q, w1s, b1, w2q, w2s, b2, w.act, ws,
+                                 out8, st)
+
+        def layer():
+            M.moe_gate_topk(x, wg, gb, w.k, b.idx, b.gates, st, flags=self.flags)
+            M.moe_capacity_locations(b.idx, w.e, w.capacity_factor, b.c_max, self.cap_ws, b.loc,
+                                     b.counts, b.c_dev, st)
+            M.moe_encode(x, b.idx, b.loc, b.counts, b.c_dev, b.buf, st)
+            ffn()
+            M.moe_decode(out8, b.idx, b.loc, b.gates, b.c_dev, b.y, st)
+
+        layer()   # the buffer the timed FFN calls read
+        res = {"expert_ffn_ms": self.time_calls(ffn, steps, warmup),
+               "layer_ms": self.time_calls(layer, steps, warmup)}
+        self.check_status()
+        return res
+
     def hid(self):
         w, b = self.w, self.bufs
         n = w.e * b.c_max * w.h
@@ -698,6 +741,8 @@ def run_ours(args, rank, world, local_rank):
     bw = run.dispatch_backward(args.steps, 3)
     # ---- capacity-dimension pipelining (not the headline: the same layer, chunked)
     pipe = run.pipelined([2, 4, 8], max(5, min(args.steps, 30)), 3)
+    # ---- e4m3 experts on the same layer (not the headline: another expert format)
+    f8 = run.fp8_experts(max(5, min(args.steps, 20)), 3)
 
     c, R, t1, hit = run.routing_summary()
     work = stage_work(w, R, t1, hit)
@@ -733,6 +778,15 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": ffn_traffic_from_profile(w.name), "traffic_unit": "bytes per call"},
         "stages": stages,
         "fp32_fma_tflops": dict(fp32, source="moe_probe_fp32_fma on this GPU, best of 5"),
+        "fp8_experts": None if f8 is None else {
+            "expert_ffn_ms": f8["expert_ffn_ms"],
+            "expert_ffn_tflops": work["expert_ffn"]["flop"] / (f8["expert_ffn_ms"] * 1e-3) / 1e12,
+            "fp8_peak_tflops": 2 * pk["bf16"],
+            "tc_frac": work["expert_ffn"]["flop"] / (f8["expert_ffn_ms"] * 1e-3) / 1e12 / (2 * pk["bf16"]),
+            "layer_ms": f8["layer_ms"], "tokens_per_s": w.s / (f8["layer_ms"] * 1e-3),
+            "note": "e4m3 operands, one fp32 scale per row (moe_quantize_rows_fp8 + "
+                    "moe_expert_ffn_fp8, the buffer's quantisation included in the FFN time); "
+                    "fp8 peak = 2 x the measured bf16 burst peak (dense e4m3 : bf16 = 2 : 1)"},
         "pipelining": dict({"single_pass_ms": ms_step}, **{f"chunks_{d}_ms": v for d, v in pipe.items()},
                            note="moe_layer_forward_pipelined: encode of capacity chunk i+1 on a side "
                                 "stream overlaps the FFN of chunk i; results bit-identical"),
