@@ -79,7 +79,7 @@ def parse(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graded", action="store_true",
                     help="skip the stage breakdowns of the other graded workloads")
-    ap.add_argument("--only", choices=["gate", "gate_bwd", "backward"],
+    ap.add_argument("--only", choices=["gate", "gate_bwd", "backward", "fp8"],
                     help="time one stage alone on the config's inputs (its own JSON line, not the "
                          "layer's): only the tensors that stage reads are drawn")
     return ap.parse_args(argv)
@@ -846,6 +846,28 @@ def run_only_backward(args):
             "ms": {k: round(v, 5) for k, v in ms.items()}}
 
 
+def run_only_fp8(args):
+    """The config's layer with e4m3 experts (ReLU / GELU) alone: one whole
+    e4m3 layer step first (its tensor-core GEMM launches are the first two),
+    then the e4m3 FFN call by call (buffer quantisation, fc1, hidden
+    quantisation, fc2; L2 flushed before each), then the whole e4m3 layer."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w, wseed = CONFIGS[args.config]
+    run = LayerRun(w, wseed, dev, L2Flush(torch, dev))
+    r = run.fp8_experts(args.steps, args.warmup)
+    if r is None:
+        return {"stage": "fp8", "workload": w.name, "unsupported": "e4m3 experts: ReLU / GELU only"}
+    R = int(torch.clamp(run.bufs.counts, max=int(run.bufs.c_dev.item())).sum())
+    flop = 4.0 * R * w.m * w.h
+    return {"stage": "fp8", "workload": w.name, "steps": args.steps, "kept_rows": R,
+            "expert_ffn_ms": r["expert_ffn_ms"], "layer_ms": r["layer_ms"],
+            "expert_ffn_tflops": flop / (r["expert_ffn_ms"] * 1e-3) / 1e12,
+            "tokens_per_s": w.s / (r["layer_ms"] * 1e-3)}
+
+
 def run_only_gate(args):
     """The gate (or, with --only gate_bwd, the gate backward: d_logits, d_wg,
     d_bias and d_x from unit-normal d_gates) alone on the config's x, gate
@@ -940,7 +962,7 @@ def main():
     if args.only:
         if rank == 0:
             print(json.dumps(run_only_backward(args) if args.only == "backward" else
-                             run_only_gate(args)))
+                             run_only_fp8(args) if args.only == "fp8" else run_only_gate(args)))
         return
     if world > 1:
         import torch

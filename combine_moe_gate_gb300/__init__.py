@@ -75,6 +75,7 @@ def load():
         "moe_expert_ffn_fp8": (I, [P, P, P, P, P, P, P, P, P, P, I, I, I64, I, I, P, SZ, P, P, P]),
         "moe_status_str": (ctypes.c_char_p, [I]),
         "moe_launch_count": (ctypes.c_uint64, []),
+        "moe_debug_stall_gemms": (I, [I]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -97,6 +98,13 @@ def status_str(code) -> str:
 
 def launch_count() -> int:
     return int(load().moe_launch_count())
+
+
+def moe_debug_stall_gemms(n):
+    """Error-path test hook: the next n tensor-core GEMM launches issue no
+    operand copies, so each times out after about a second with
+    MOE_ERR_TIMEOUT in its status word (n = 0 cancels)."""
+    _check(load().moe_debug_stall_gemms(int(n)), "moe_debug_stall_gemms")
 
 
 def _ptr(t, name="tensor", dtype=None, shape=None):

@@ -8,6 +8,14 @@ namespace moe {
 static std::atomic<uint64_t> g_launches{0};
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+static std::atomic<int32_t> g_gemm_stalls{0};
+bool take_gemm_stall() {
+    int32_t n = g_gemm_stalls.load(std::memory_order_relaxed);
+    while (n > 0 && !g_gemm_stalls.compare_exchange_weak(n, n - 1, std::memory_order_relaxed)) {
+    }
+    return n > 0;
+}
+
 // kernels (one translation unit each)
 moe_status gate_topk_launch(const void *x, moe_dtype xdt, const float *wg, const float *bias,
                             int64_t s, int m, int e, int k, unsigned flags, int32_t *idx,
@@ -107,6 +115,12 @@ const char *moe_status_str(moe_status st) {
 }
 
 uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+moe_status moe_debug_stall_gemms(int32_t n) {
+    if (n < 0) return MOE_ERR_INVALID_ARG;
+    g_gemm_stalls.store(n, std::memory_order_relaxed);
+    return MOE_OK;
+}
 
 moe_status moe_gate_topk(const void *x, moe_dtype xdt, const float *wg, const float *bias,
                          int64_t s, int m, int e, int k, unsigned flags, int32_t *idx,

@@ -14,6 +14,10 @@ namespace moe {
 // Count of kernels launched by this library (exported by moe_launch_count).
 void note_launch();
 
+// True (and one fewer pending) while moe_debug_stall_gemms has stalls pending:
+// the tensor-core GEMM launch being prepared then issues no operand copies.
+bool take_gemm_stall();
+
 inline moe_status launch_status() {
     cudaError_t err = cudaGetLastError();
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

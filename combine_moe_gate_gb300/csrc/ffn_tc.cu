@@ -157,6 +157,9 @@ struct GemmArgs {
     // acc * (a_scale * b_scale) + bias.  NULL for bf16.
     const float *a_scale;
     const float *b_scale;
+    // Error-path test: the producers issue no copies, so the MMA issuer's
+    // bounded wait on the first stage runs out (MOE_ERR_TIMEOUT).
+    int32_t stall;
 };
 
 // ------------------------------------------------------------- PTX wrappers
@@ -643,7 +646,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         int stage = 0;
         uint32_t phase = 0;
         int issued = 0;
-        for (int t = tile0; t < total; t += tile_step) {
+        for (int t = tile0; t < total && !args.stall; t += tile_step) {
             Tile T = decode_tile(ctl->tile_start, e, t, BMT, kept_rows, urows, nk, BK);
             // A: this CTA's 128 rows, half of them per producer
             const int a_row = (int)((int64_t)T.j * args.c_max + args.row_lo + (int64_t)T.mt * BMT +
@@ -1033,8 +1036,10 @@ int max_clusters(K kern, size_t smem, int cl) {
 
 template <int EPI, int TM, int BK, int CL, int TN, int EB = 2>
 moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &b3,
-                       const CUtensorMap &o, const GemmArgs &args, cudaStream_t stream) {
+                       const CUtensorMap &o, const GemmArgs &args_in, cudaStream_t stream) {
     using TL = Tiling<TM, BK, CL, TN, EB>;
+    GemmArgs args = args_in;
+    args.stall = take_gemm_stall() ? 1 : 0;
     auto kern = tc_group_gemm<EPI, TM, BK, CL, TN, EB>;
     constexpr size_t SMEM = smem_bytes<TL>();
     static int units[64] = {0};  // resident CTAs (CL = 1) or clusters, per device

@@ -411,6 +411,20 @@ const char *moe_status_str(moe_status st);
 /* Number of kernels this library has launched in this process (monotonic). */
 uint64_t moe_launch_count(void);
 
+/*
+ * Error-path test hook, not for production use.  The next n launches of the
+ * tensor-core grouped GEMM in this process (moe_expert_ffn, _fp8, _bwd and the
+ * layer calls all use it; fc1 and fc2 are one launch each) issue no operand
+ * copies, so the MMA issuer's bounded wait on its first stage runs out after
+ * about one second: the launch sets MOE_ERR_TIMEOUT in the call's status
+ * word, drains, releases its tensor memory and returns, and every later
+ * kernel that reads that status word writes nothing.  The context stays
+ * usable.  n = 0 cancels pending stalls.  The count is process-wide: calls
+ * made meanwhile from other threads may take the stalls.
+ * Errors: MOE_ERR_INVALID_ARG for n < 0.
+ */
+moe_status moe_debug_stall_gemms(int32_t n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -34,6 +34,16 @@ def test_status_strings():
     assert M.status_str(99) == "unknown status"
 
 
+def test_debug_stall_hook_arguments():
+    lib = M.load()
+    assert lib.moe_debug_stall_gemms(-1) == M.MOE_ERR_INVALID_ARG
+    assert lib.moe_debug_stall_gemms(3) == M.MOE_OK
+    assert lib.moe_debug_stall_gemms(0) == M.MOE_OK   # cancels: no GEMM launch stalls after this
+    with pytest.raises(M.MoEError):
+        M.moe_debug_stall_gemms(-2)
+    assert "timed out" in M.status_str(M.MOE_ERR_TIMEOUT)
+
+
 def test_capacity_bound_matches_closed_forms():
     with open(os.path.join(GOLD, "capacity.json")) as f:
         cap = json.load(f)
