@@ -315,8 +315,8 @@ def ffn_traffic_from_profile(workload_name):
     """DRAM bytes per expert-FFN call on this workload from the committed ncu
     summary, or None when there is none or the forward GEMM's source has
     changed since its counters were taken.  The digest covers ffn_tc.cu up to
-    the end of its first `namespace moe` block: the forward kernel and its
-    launcher (the backward's host code follows)."""
+    its e4m3-forward marker: the GEMM kernel and the bf16 forward launcher
+    (the e4m3 launcher and the backward's host code follow)."""
     import hashlib
 
     prof = os.path.join(ROOT, "profiles", f"expert_ffn_tcgen05_{workload_name}.md")
@@ -326,10 +326,10 @@ def ffn_traffic_from_profile(workload_name):
         data = open(src, "rb").read()
     except OSError:
         return None
-    end = data.find(b"}  // namespace moe\n")
+    end = data.find(b"// ------------------------------------------------------------ e4m3 forward\n")
     if end < 0:
         return None
-    digest = hashlib.sha256(data[:end + len(b"}  // namespace moe\n")]).hexdigest()[:16]
+    digest = hashlib.sha256(data[:end]).hexdigest()[:16]
     fields = dict(line.split(":", 1) for line in text.splitlines() if line.startswith(
         ("source_sha256_16:", "dram_bytes_per_call:")))
     if fields.get("source_sha256_16", "").split()[0:1] != [digest]:

@@ -1131,6 +1131,7 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
     return launch_gemm<EPI_BIAS, TM2, BK2, CL2, TN2>(mA2, mB2, mB2, mO2, g2, stream);
 }
 
+// ------------------------------------------------------------ e4m3 forward
 moe_status quantize_rows_fp8_launch(const void *src, int64_t batches, int64_t rows_per_batch,
                                     int cols, const int32_t *counts, const int32_t *c_dev,
                                     void *q, float *scale, int32_t *st, cudaStream_t stream);
@@ -1138,7 +1139,10 @@ moe_status quantize_rows_fp8_launch(const void *src, int64_t batches, int64_t ro
 // The expert FFN on e4m3 operands with one fp32 scale per row: fc1 on the
 // quantised rows and W1 (the same pair tiles as bf16, 128-element K blocks,
 // kind::f8f6f4), the scales, bias and activation in the epilogue, bf16 hidden;
-// the hidden rows quantised; fc2 likewise into bf16 out.  ReLU / GELU only.
+// the hidden rows quantised; fc2 likewise into bf16 out, on 256 x 256 pair
+// tiles with two accumulators (with 128-element K blocks the main loop is
+// short enough for the epilogue to show; measured 4% faster than 256 x 512
+// on 8 experts, the same on 64).  ReLU / GELU only.
 moe_status ffn_tc_fp8_launch(const void *buf_q, const float *buf_scale, const int32_t *counts,
                              const int32_t *c_dev, const void *w1_q, const float *w1_scale,
                              const void *b1, const void *w2_q, const float *w2_scale,
@@ -1147,7 +1151,7 @@ moe_status ffn_tc_fp8_launch(const void *buf_q, const float *buf_scale, const in
                              cudaStream_t stream) {
     constexpr int BKF = 128;   // e4m3 elements per K block (128 bytes)
     using T1 = Tiling<1, BKF, 2, 1, 1>;
-    using T2 = Tiling<1, BKF, 2, 2, 1>;
+    using T2 = Tiling<1, BKF, 2, 1, 1>;
     CUtensorMap mA1, mB1, mO1, mA2, mB2, mO2;
     if (!make_map_u8(&mA1, buf_q, (uint64_t)e * c_max, (uint64_t)m, T1::A_BOX_ROWS) ||
         !make_map_u8(&mB1, w1_q, (uint64_t)e * h, (uint64_t)m, T1::B_BOX_ROWS) ||
@@ -1166,7 +1170,7 @@ moe_status ffn_tc_fp8_launch(const void *buf_q, const float *buf_scale, const in
     if (r != MOE_OK) return r;
     GemmArgs g2{counts, c_dev, st, (const __nv_bfloat16 *)b2, (__nv_bfloat16 *)out, c_max, e, h, m, m,
                 nullptr, nullptr, 0, 0, hid_scale, w2_scale};
-    return launch_gemm<EPI_BIAS, 1, BKF, 2, 2, 1>(mA2, mB2, mB2, mO2, g2, stream);
+    return launch_gemm<EPI_BIAS, 1, BKF, 2, 1, 1>(mA2, mB2, mB2, mO2, g2, stream);
 }
 
 }  // namespace moe

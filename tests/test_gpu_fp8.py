@@ -37,7 +37,11 @@ def _bits(t):
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-@pytest.mark.parametrize("rows,cols", [(1, 16), (37, 80), (600, 4096)])
+# row widths for each register layout of the kernel (one, two, four or eight
+# warps per row; a chunk count just past a layout's capacity) and the loop
+# form beyond 16384 columns
+@pytest.mark.parametrize("rows,cols", [(1, 16), (37, 80), (600, 4096), (5, 2064), (9, 8192),
+                                       (3, 16384), (2, 16400)])
 def test_quantize_rows_fp8_is_bit_exact(rows, cols):
     x = _bf16((rows, cols), 21, f"q{rows}", 3.0)
     x[0] = 0                                   # an all-zero row: scale 1
@@ -50,9 +54,10 @@ def test_quantize_rows_fp8_is_bit_exact(rows, cols):
     assert np.array_equal(q.cpu().numpy(), qo)
 
 
-def test_quantize_rows_fp8_writes_kept_rows_only():
-    e, c_max, m = 3, 50, 64
-    x = _bf16((e, c_max, m), 22, "qk")
+@pytest.mark.parametrize("m", [64, 4096])
+def test_quantize_rows_fp8_writes_kept_rows_only(m):
+    e, c_max = 3, 50
+    x = _bf16((e, c_max, m), 22, f"qk{m}")
     counts = torch.tensor([50, 0, 17], dtype=torch.int32, device="cuda")
     c_dev = torch.tensor([40], dtype=torch.int32, device="cuda")
     q, sc = _q(x, counts, c_dev)
