@@ -286,6 +286,43 @@ moe_status act_bwd_launch(const __nv_bfloat16 *pa, const __nv_bfloat16 *pb,
                       e, c_max, h, counts, c_dev, d_pre, status);
 }
 
+// ------------------------------------------------------------ tail rows
+namespace {
+
+constexpr int TR_WARPS = 8;   // one warp per row, 64 / TR_WARPS CTAs per expert
+
+__global__ void __launch_bounds__(TR_WARPS * 32)
+tail_rows_kernel(const __nv_bfloat16 *__restrict__ src, int64_t src_pitch, int64_t c_max, int cols,
+                 const int32_t *__restrict__ counts, const int32_t *__restrict__ c_dev,
+                 __nv_bfloat16 *__restrict__ dst, int32_t *status) {
+    pdl_enter();
+    if (status_bad(status)) return;
+    const int j = blockIdx.y;
+    const int64_t kept = min((int64_t)max(counts[j], 0), min((int64_t)*c_dev, c_max));
+    const int nvalid = (int)(kept & 63);
+    if (nvalid == 0) return;
+    const int r = blockIdx.x * TR_WARPS + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    const __nv_bfloat16 *srow = src + ((int64_t)j * c_max + (kept - nvalid) + r) * src_pitch;
+    __nv_bfloat16 *drow = dst + ((int64_t)j * 64 + r) * cols;
+    for (int c = lane * 8; c < cols; c += 32 * 8) {
+        V16 v{};
+        if (r < nvalid) v = ld_v16(srow + c);
+        st_v16(drow + c, v);
+    }
+}
+
+}  // namespace
+
+moe_status tail_rows_launch(const __nv_bfloat16 *src, int64_t src_pitch, int64_t c_max, int cols,
+                            int e, const int32_t *counts, const int32_t *c_dev, __nv_bfloat16 *dst,
+                            int32_t *status, cudaStream_t stream) {
+    if (e < 1 || e > 65535 || c_max < 1 || cols < 8 || cols % 8 || src_pitch % 8 || !aligned16(src) ||
+        !aligned16(dst))
+        return MOE_ERR_INVALID_ARG;
+    return launch_pdl(tail_rows_kernel, dim3(64 / TR_WARPS, (unsigned)e), dim3(TR_WARPS * 32), 0,
+                      stream, src, src_pitch, c_max, cols, counts, c_dev, dst, status);
+}
+
 moe_status colsum_launch(const __nv_bfloat16 *src, int e, int64_t c_max, int cols,
                          int64_t src_pitch, const int32_t *counts, const int32_t *c_dev,
                          __nv_bfloat16 *out, int32_t *status, cudaStream_t stream) {

@@ -34,4 +34,15 @@ moe_status colsum_launch(const __nv_bfloat16 *src, int e, int64_t c_max, int col
                          int64_t src_pitch, const int32_t *counts, const int32_t *c_dev,
                          __nv_bfloat16 *out, int32_t *status, cudaStream_t stream);
 
+// The partly kept last 64-row block of every expert, for the MN-major weight
+// gradients: with kept_b = min(counts[b], *c_dev, c_max) and r0 = kept_b
+// rounded down to a multiple of 64, dst[b][r] = src[b][r0 + r] for
+// r < kept_b - r0 and 0 for the rest of the 64 rows; experts whose kept rows
+// end on a block boundary are left untouched (nothing reads them).  src rows
+// of `cols` columns at row pitch src_pitch, c_max rows per expert; dst
+// [e, 64, cols] dense.
+moe_status tail_rows_launch(const __nv_bfloat16 *src, int64_t src_pitch, int64_t c_max, int cols,
+                            int e, const int32_t *counts, const int32_t *c_dev, __nv_bfloat16 *dst,
+                            int32_t *status, cudaStream_t stream);
+
 }  // namespace moe

@@ -50,7 +50,14 @@ constexpr int SMEM_RING = 192 * 1024;   // operand ring per CTA
 
 // EPI_BIAS_BMN: the bias epilogue with B read MN-major, straight from a
 // row-major [K, N] tensor (the weights of the data-gradient products).
-enum Epi { EPI_GELU = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_BIAS = 3, EPI_BIAS_BMN = 4 };
+// EPI_WGRAD_MN: the weight-gradient products out[j] = A[j]^T B[j] with both
+// operands read MN-major from row-major activations [e * b_rows, M or N]
+// (b_rows rows per expert): expert j contracts over its first k_counts[j]
+// rows; a last K block that is only partly kept is read from the tail maps
+// instead ([e * BK, M or N]: those rows copied, zeros after them), so no
+// row past an expert's kept rows is ever read.
+enum Epi { EPI_GELU = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_BIAS = 3, EPI_BIAS_BMN = 4,
+           EPI_WGRAD_MN = 5 };
 
 // Tile shape.  TM = 1: 128 x 256 tiles, two 256-column accumulators in TMEM so
 // the epilogue of one tile overlaps the main loop of the next.  TM = 2:
@@ -100,8 +107,9 @@ constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >
 // The same for the 2-SM MMA: M = 256 over the CTA pair (128 rows per CTA).
 constexpr uint32_t IDESC_PAIR = (1u << 4) | (1u << 7) | (1u << 10) |
                                 ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((2 * UM) >> 4) << 24);
-// ... with B MN-major (bit 16).
+// ... with B MN-major (bit 16); with A and B MN-major (bits 15 and 16).
 constexpr uint32_t IDESC_PAIR_BMN = IDESC_PAIR | (1u << 16);
+constexpr uint32_t IDESC_PAIR_MN = IDESC_PAIR | (1u << 15) | (1u << 16);
 // kind::f8f6f4 with A and B e4m3 (format 0), D fp32, both K-major; the 2-SM
 // MMA, K = 32 elements (32 bytes, as kind::f16's 16 elements).
 constexpr uint32_t IDESC_PAIR_F8 = (1u << 4) | ((uint32_t)(BN >> 3) << 17) |
@@ -520,12 +528,14 @@ template <int EPI, int TM, int BK, int CL, int TN, int EB = 2>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmO,
+              const __grid_constant__ CUtensorMap tmAt, const __grid_constant__ CUtensorMap tmBt,
               const GemmArgs args) {
     using TL = Tiling<TM, BK, CL, TN, EB>;
     static_assert(TN == 1 || EPI != EPI_SWIGLU, "SwiGLU tiles pair W1 and W3 in one N = 256 MMA");
     constexpr bool F8 = EB == 1;   // e4m3 operands (kind::f8f6f4), scaled epilogue
     static_assert(!F8 || (CL == 2 && EPI != EPI_SWIGLU && EPI != EPI_BIAS_BMN), "e4m3 pair tiles");
-    constexpr bool BMN = EPI == EPI_BIAS_BMN;   // B MN-major: [K, N] rows, boxes of 64 columns
+    constexpr bool AMN = EPI == EPI_WGRAD_MN;   // A MN-major as well, tail blocks from tmAt / tmBt
+    constexpr bool BMN = EPI == EPI_BIAS_BMN || AMN;   // B MN-major: [K, N] rows, boxes of 64 columns
     static_assert(!BMN || (CL == 2 && TN == 2 && BK == 64), "MN-major B on 256 x 512 pair tiles");
     constexpr bool PAIR = TL::PAIR;
     constexpr int STAGES = TL::STAGES, BMT = TL::BMT, A_BYTES = TL::A_BYTES;
@@ -657,11 +667,33 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                               (TN == 2 ? hh * BN + (int)prank * (BN / 2)
                                        : (PAIR && EPI != EPI_SWIGLU ? (int)prank * TL::B_ROWS : 0) +
                                              hh * TL::B_BOX_ROWS);
+            // MN-major weight gradients: a last K block only partly kept
+            // comes from the tail maps (rows j * BK ..)
+            const bool part_tail = AMN && (kept_rows[T.j] % BK) != 0;
             for (int kb = 0; kb < T.nk; kb++) {
                 int ok = 1;
                 if (lane == 0) {
                     ok = mbar_wait<PAIR>(&ctl->empty[stage], phase ^ 1u, abort_flag, args.status);
-                    if (ok && PAIR) {
+                    const bool tail = part_tail && kb == T.nk - 1;
+                    const int k_row = tail ? T.j * BK : T.j * args.b_rows + kb * BK;
+                    if (ok && PAIR && AMN) {
+                        const uint32_t fb = map_to_rank(su32(&ctl->full[stage]), lead);
+                        if (is_a) {
+                            // this CTA's 128 output rows = A columns, block hh of 64
+                            if (prank == 0) mbar_expect_tx(&ctl->full[stage], 2 * A_BOX_BYTES);
+                            tma_load_2d_pair(sA + stage * A_BYTES + hh * A_BOX_BYTES,
+                                             tail ? &tmAt : &tmA,
+                                             T.mt * BMT + (int)prank * TL::A_ROWS + hh * 64, k_row, fb);
+                        } else {
+                            if (prank == 0) mbar_expect_tx(&ctl->full[stage], 2 * B_BOX_BYTES);
+                            const int n_col = b_row - T.j * args.b_rows;
+#pragma unroll
+                            for (int i = 0; i < 2; i++)
+                                tma_load_2d_pair(sB + stage * B_BYTES + hh * B_BOX_BYTES +
+                                                     i * (B_BOX_BYTES / 2),
+                                                 tail ? &tmBt : &tmB, n_col + 64 * i, k_row, fb);
+                        }
+                    } else if (ok && PAIR) {
                         const uint32_t fb = map_to_rank(su32(&ctl->full[stage]), lead);
                         if (is_a) {
                             if (prank == 0) mbar_expect_tx(&ctl->full[stage], 2 * A_BOX_BYTES);
@@ -672,7 +704,6 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                             // two boxes of 64 columns (b_row - j * b_rows is the column)
                             if (prank == 0) mbar_expect_tx(&ctl->full[stage], 2 * B_BOX_BYTES);
                             const int n_col = b_row - T.j * args.b_rows;
-                            const int k_row = T.j * args.b_rows + kb * BK;
 #pragma unroll
                             for (int i = 0; i < 2; i++)
                                 tma_load_2d_pair(sB + stage * B_BYTES + hh * B_BOX_BYTES +
@@ -746,6 +777,16 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                                 umma_pair_f8(d + (uint32_t)(tn * BN), sdesc<ROWB>(a0 + kk * 32),
                                              sdesc<ROWB>(b0 + tn * (B_BYTES / TN) + kk * 32),
                                              (kb | kk) != 0);
+                        } else if (AMN) {
+                            // A and B: K rows of 128 bytes, kk * UK rows in; A's two
+                            // 64-column blocks A_BYTES / 2 apart, B's as below
+#pragma unroll
+                            for (int tn = 0; tn < TN; tn++)
+                                umma_pair<IDESC_PAIR_MN>(
+                                    d + (uint32_t)(tn * BN), sdesc_mn(a0 + kk * UK * 128, A_BYTES / 2),
+                                    sdesc_mn(b0 + tn * (B_BYTES / TN) + kk * UK * 128,
+                                             B_BYTES / TN / 2),
+                                    (kb | kk) != 0);
                         } else if (BMN) {
                             // B: K rows of 128 bytes, kk * UK rows in; blocks of 64
                             // columns (B_BYTES / TN / 2 bytes) apart
@@ -968,11 +1009,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // (bk = 64: 128-byte swizzle; bk = 32: 64-byte swizzle, also the epilogue's
 // output staging; bk = 16: 32-byte swizzle).
 bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
-              int bk) {
+              int bk, uint64_t pitch = 0) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
+    cuuint64_t strides[1] = {(pitch ? pitch : cols) * 2};   // row pitch in bytes
     cuuint32_t box[2] = {(cuuint32_t)bk, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
@@ -1036,7 +1077,8 @@ int max_clusters(K kern, size_t smem, int cl) {
 
 template <int EPI, int TM, int BK, int CL, int TN, int EB = 2>
 moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &b3,
-                       const CUtensorMap &o, const GemmArgs &args_in, cudaStream_t stream) {
+                       const CUtensorMap &o, const GemmArgs &args_in, cudaStream_t stream,
+                       const CUtensorMap *a_tail = nullptr, const CUtensorMap *b_tail = nullptr) {
     using TL = Tiling<TM, BK, CL, TN, EB>;
     GemmArgs args = args_in;
     args.stall = take_gemm_stall() ? 1 : 0;
@@ -1060,7 +1102,7 @@ moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtenso
     if (grid < 1) grid = 1;
     if (CL == 1)
         return launch_pdl(kern, dim3((unsigned)grid), dim3(NUM_THREADS), SMEM, stream, a, b, b3, o,
-                          args);
+                          a_tail ? *a_tail : a, b_tail ? *b_tail : b, args);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(CL * grid));
     cfg.blockDim = dim3(NUM_THREADS);
@@ -1075,7 +1117,8 @@ moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtenso
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t err = cudaLaunchKernelEx(&cfg, kern, a, b, b3, o, args);
+    cudaError_t err = cudaLaunchKernelEx(&cfg, kern, a, b, b3, o, a_tail ? *a_tail : a,
+                                         b_tail ? *b_tail : b, args);
     note_launch();
     if (err != cudaSuccess) {
         cudaGetLastError();
@@ -1182,30 +1225,29 @@ moe_status ffn_tc_fp8_launch(const void *buf_q, const float *buf_scale, const in
 namespace moe {
 
 // ---------------------------------------------------------------- backward
-// The expert-FFN backward as bias-epilogue products on the fc2 tiling (the
-// kernel computes out[j] = A[j] B[j]^T over the kept rows of A[j], both
-// operands K-major), with SIMT transposes, activation derivative and bias
-// sums in between:
+// The expert-FFN backward as products on the 256 x 512 pair tiling, with the
+// SIMT activation derivative, tail copies and bias sums in between:
 //   pre = buf w1^T + b1 (SwiGLU: a = buf w1^T, b = buf w3^T), recomputed;
-//   d_hid = d_out w2                  (B = w2 transposed to [e, h, m]);
+//   d_hid = d_out w2                  (B = w2 read MN-major in place);
 //   d_pre = d_hid * act'(pre)         (SwiGLU: [d_a | d_b]);
-//   d_buf = d_pre w1 (+ d_b w3)       (B = [w1^T | w3^T] [e, m, h or 2h]);
+//   d_buf = d_pre w1                  (B = w1 MN-major in place; SwiGLU:
+//                                      d_pre [w1^T | w3^T], one K-major copy);
 //   d_w2 = d_out^T hid, d_w1 = d_pre^T buf (d_w3 = d_b^T buf): the kept rows
-//   are the contraction, so A and B are the transposed activations
-//   [e, features, Kp], zero past each expert's kept rows, and each expert
-//   contracts over its own kept rows only (an expert with none gets zeros);
+//   are the contraction, each expert over its own (an expert with none gets
+//   zeros), both operands read MN-major in place and each expert's partly
+//   kept last 64-row block from a zero-padded copy;
 //   d_b1, d_b2: column sums of d_pre, d_out over the kept rows.
 namespace {
 
 constexpr int64_t up256i(int64_t b) { return (b + 255) & ~(int64_t)255; }
 
 struct BwdLayout {
-    int64_t pa, pb, dh, dpre, wT, doT, hidT, dpT, bufT, total;
+    int64_t pa, pb, dh, dpre, wT, tDo, tHid, tDp, tBuf, total;
 };
 
 BwdLayout bwd_layout(moe_act act, int e, int64_t c_max, int m, int h) {
     const bool swiglu = act == MOE_ACT_SWIGLU;
-    const int64_t E = e, H2 = swiglu ? 2 * (int64_t)h : h, Kp = (c_max + 7) / 8 * 8;
+    const int64_t E = e, H2 = swiglu ? 2 * (int64_t)h : h;
     BwdLayout L{};
     int64_t o = 0;
     auto take = [&](int64_t bytes) { const int64_t at = o; o += up256i(bytes); return at; };
@@ -1214,22 +1256,20 @@ BwdLayout bwd_layout(moe_act act, int e, int64_t c_max, int m, int h) {
     L.dh = take(E * c_max * h * 2);
     L.dpre = take(E * c_max * H2 * 2);
     L.wT = take(swiglu ? E * m * H2 * 2 : 0);   // [W1 | W3] transposed (SwiGLU only)
-    L.doT = take(E * m * Kp * 2);
-    L.hidT = take(E * h * Kp * 2);
-    L.dpT = take((swiglu ? 2 : 1) * E * h * Kp * 2);
-    L.bufT = take(E * m * Kp * 2);
+    // the partly kept last 64-row block of each expert's d_out, hid, d_pre, buf
+    L.tDo = take(E * 64 * m * 2);
+    L.tHid = take(E * 64 * h * 2);
+    L.tDp = take(E * 64 * H2 * 2);
+    L.tBuf = take(E * 64 * m * 2);
     L.total = o;
     return L;
 }
 
 // out[j] = A[j] B[j]^T (+ bias[j]) over the rows min(counts[j], *c_dev, c_max)
 // of every expert j: A [e * c_max, K], B [e * b_rows, K], out [e, c_max, n_out].
-// With k_counts (weight gradients): all c_max rows of every expert, and expert
-// j contracts over its first min(k_counts[j], *k_cdev) columns of K only.
 moe_status gemm_bias(const void *a, const void *b, int b_rows, void *out, const void *bias,
                      const int32_t *counts, const int32_t *c_dev, int e, int64_t c_max, int K,
-                     int n_out, int32_t *st, cudaStream_t stream,
-                     const int32_t *k_counts = nullptr, const int32_t *k_cdev = nullptr) {
+                     int n_out, int32_t *st, cudaStream_t stream) {
     using T2 = Tiling<1, 64, 2, 2>;
     CUtensorMap mA, mB, mO;
     if (!make_map(&mA, a, (uint64_t)e * c_max, (uint64_t)K, T2::A_BOX_ROWS, 64) ||
@@ -1237,7 +1277,7 @@ moe_status gemm_bias(const void *a, const void *b, int b_rows, void *out, const 
         !make_map(&mO, out, (uint64_t)e * c_max, (uint64_t)n_out, 32, 32))
         return MOE_ERR_CUDA;
     GemmArgs g{counts, c_dev, st, (const __nv_bfloat16 *)bias, (__nv_bfloat16 *)out, c_max, e, K,
-               n_out, b_rows, k_counts, k_cdev, 0, 0};
+               n_out, b_rows, nullptr, nullptr, 0, 0};
     return launch_gemm<EPI_BIAS, 1, 64, 2, 2>(mA, mB, mB, mO, g, stream);
 }
 
@@ -1257,6 +1297,28 @@ moe_status gemm_bias_bmn(const void *a, const void *b, void *out, const int32_t 
     return launch_gemm<EPI_BIAS_BMN, 1, 64, 2, 2>(mA, mB, mB, mO, g, stream);
 }
 
+// Weight gradients out[j] = A[j]^T B[j] over the first min(counts[j], *c_dev,
+// c_max) rows of expert j, both operands read MN-major in place: A rows of
+// a_cols columns at pitch a_pitch, B rows of b_cols at pitch b_pitch, c_max
+// rows per expert; a_tail / b_tail [e, 64, *] (pitches a_tpitch / b_tpitch)
+// hold each expert's partly kept last 64-row block (tail_rows_launch);
+// out [e, a_cols, b_cols].
+moe_status gemm_wgrad_mn(const void *a, int64_t a_pitch, int a_cols, const void *a_tail,
+                         int64_t a_tpitch, const void *b, int64_t b_pitch, int b_cols,
+                         const void *b_tail, int64_t b_tpitch, void *out, const int32_t *counts,
+                         const int32_t *c_dev, int e, int64_t c_max, int32_t *st, cudaStream_t stream) {
+    CUtensorMap mA, mAt, mB, mBt, mO;
+    if (!make_map(&mA, a, (uint64_t)e * c_max, (uint64_t)a_cols, 64, 64, (uint64_t)a_pitch) ||
+        !make_map(&mAt, a_tail, (uint64_t)e * 64, (uint64_t)a_cols, 64, 64, (uint64_t)a_tpitch) ||
+        !make_map(&mB, b, (uint64_t)e * c_max, (uint64_t)b_cols, 64, 64, (uint64_t)b_pitch) ||
+        !make_map(&mBt, b_tail, (uint64_t)e * 64, (uint64_t)b_cols, 64, 64, (uint64_t)b_tpitch) ||
+        !make_map(&mO, out, (uint64_t)e * a_cols, (uint64_t)b_cols, 32, 32))
+        return MOE_ERR_CUDA;
+    GemmArgs g{nullptr, nullptr, st, nullptr, (__nv_bfloat16 *)out, a_cols, e, (int)c_max, b_cols,
+               (int)c_max, counts, c_dev, 0, 0};
+    return launch_gemm<EPI_WGRAD_MN, 1, 64, 2, 2>(mA, mB, mB, mO, g, stream, &mAt, &mBt);
+}
+
 }  // namespace
 
 size_t ffn_tc_bwd_workspace_bytes(moe_act act, int e, int64_t c_max, int m, int h) {
@@ -1271,13 +1333,13 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
     using bf = __nv_bfloat16;
     const bool swiglu = act == MOE_ACT_SWIGLU;
     const BwdLayout L = bwd_layout(act, e, c_max, m, h);
-    const int64_t E = e, H2 = swiglu ? 2 * (int64_t)h : h, Kp = (c_max + 7) / 8 * 8;
-    if (Kp > 0x7fffffff || H2 > 0x7fffffff) return MOE_ERR_UNSUPPORTED;
+    const int64_t H2 = swiglu ? 2 * (int64_t)h : h;
+    if (c_max > 0x7fffffff || H2 > 0x7fffffff) return MOE_ERR_UNSUPPORTED;
     char *w = (char *)ws;
     bf *pa = (bf *)(w + L.pa), *pb = (bf *)(w + L.pb), *dh = (bf *)(w + L.dh);
     bf *dpre = (bf *)(w + L.dpre), *wT = (bf *)(w + L.wT);
-    bf *doT = (bf *)(w + L.doT), *hidT = (bf *)(w + L.hidT), *dpT = (bf *)(w + L.dpT);
-    bf *bufT = (bf *)(w + L.bufT);
+    bf *tDo = (bf *)(w + L.tDo), *tHid = (bf *)(w + L.tHid), *tDp = (bf *)(w + L.tDp);
+    bf *tBuf = (bf *)(w + L.tBuf);
     moe_status r;
 #define MOE_TRY(x) \
     do {           \
@@ -1305,26 +1367,19 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
     else
         MOE_TRY(gemm_bias_bmn(dpre, w1, d_buf, counts, c_dev, e, c_max, h, m, st, stream));
     // weight gradients: the kept rows are the contraction, each expert over
-    // its own (zero-padded past them up to the GEMM's next 64-deep K block;
-    // past Kp its tensor map fills zeros)
-    MOE_TRY(transpose_pad_launch((const bf *)d_out, c_max * m, m, doT, (int64_t)m * Kp, Kp, e,
-                                 (int)c_max, m, (int)Kp, counts, counts, c_dev, st, stream));
-    MOE_TRY(transpose_pad_launch((const bf *)hid, c_max * h, h, hidT, (int64_t)h * Kp, Kp, e,
-                                 (int)c_max, h, (int)Kp, counts, counts, c_dev, st, stream));
-    MOE_TRY(transpose_pad_launch((const bf *)buf, c_max * m, m, bufT, (int64_t)m * Kp, Kp, e,
-                                 (int)c_max, m, (int)Kp, counts, counts, c_dev, st, stream));
-    MOE_TRY(transpose_pad_launch(dpre, c_max * H2, H2, dpT, (int64_t)h * Kp, Kp, e, (int)c_max, h,
-                                 (int)Kp, counts, counts, c_dev, st, stream));
+    // its own; both operands are read MN-major in place, the partly kept last
+    // 64-row block of each expert from a zero-padded copy
+    MOE_TRY(tail_rows_launch((const bf *)d_out, m, c_max, m, e, counts, c_dev, tDo, st, stream));
+    MOE_TRY(tail_rows_launch((const bf *)hid, h, c_max, h, e, counts, c_dev, tHid, st, stream));
+    MOE_TRY(tail_rows_launch(dpre, H2, c_max, (int)H2, e, counts, c_dev, tDp, st, stream));
+    MOE_TRY(tail_rows_launch((const bf *)buf, m, c_max, m, e, counts, c_dev, tBuf, st, stream));
+    MOE_TRY(gemm_wgrad_mn(d_out, m, m, tDo, m, hid, h, h, tHid, h, d_w2, counts, c_dev, e, c_max, st,
+                          stream));
+    MOE_TRY(gemm_wgrad_mn(dpre, H2, h, tDp, H2, buf, m, m, tBuf, m, d_w1, counts, c_dev, e, c_max,
+                          st, stream));
     if (swiglu)
-        MOE_TRY(transpose_pad_launch(dpre + h, c_max * H2, H2, dpT + E * h * Kp, (int64_t)h * Kp, Kp,
-                                     e, (int)c_max, h, (int)Kp, counts, counts, c_dev, st, stream));
-    MOE_TRY(gemm_bias(doT, hidT, h, d_w2, nullptr, nullptr, nullptr, e, m, (int)Kp, h, st, stream,
-                      counts, c_dev));
-    MOE_TRY(gemm_bias(dpT, bufT, m, d_w1, nullptr, nullptr, nullptr, e, h, (int)Kp, m, st, stream,
-                      counts, c_dev));
-    if (swiglu)
-        MOE_TRY(gemm_bias(dpT + E * h * Kp, bufT, m, d_w3, nullptr, nullptr, nullptr, e, h, (int)Kp,
-                          m, st, stream, counts, c_dev));
+        MOE_TRY(gemm_wgrad_mn(dpre + h, H2, h, tDp + h, H2, buf, m, m, tBuf, m, d_w3, counts, c_dev,
+                              e, c_max, st, stream));
     // bias gradients (ReLU / GELU experts)
     if (!swiglu && d_b1)
         MOE_TRY(colsum_launch(dpre, e, c_max, h, h, counts, c_dev, (bf *)d_b1, st, stream));

@@ -65,16 +65,43 @@ def test_expert_ffn_bwd_matches_oracle(w):
     inp = synth.make_inputs_host(w)
     # routing and the encoded buffer (the forward's expert rows are not needed)
     ref = oracle.layer_forward(w, inp, rows=(np.zeros(1, np.int32), np.zeros(1, np.int64)))
-    c, e, m, h = ref["c"], w.e, w.m, w.h
+    c, e, m = ref["c"], w.e, w.m
     c_max = c + 3
     kept = ref["kept"].astype(np.int64)
-    buf_h = np.zeros((e, c_max, m), np.float32)
-    buf_h[:, :c] = ref["buf"][:, :c]
+    # rows past each expert's kept rows hold large values: none may reach a gradient
+    buf_h = synth.bf16_bits_to_f32(synth.normal_host(6, "stale", (e, c_max, m), 50.0, "bf16"))
+    for j in range(e):
+        buf_h[j, :kept[j]] = ref["buf"][j, :kept[j]]
     d_out_h = synth.bf16_bits_to_f32(synth.normal_host(5, "d_out", (e, c_max, m), 1.0, "bf16"))
+    _check_bwd(w, inp, buf_h, d_out_h, ref["needed"], kept, c, c_max)
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_expert_ffn_bwd_block_edges(act):
+    """Kept rows chosen at the weight gradients' 64-row block edges: exactly
+    one block, none, a block plus a few rows, a single row, and a count above
+    c (kept = c = 200, past three full blocks), with large values in every row
+    past the kept ones."""
+    w = _w(s=64, m=192, e=5, k=1, h=320, act=act, capacity_factor=0.0)
+    inp = synth.make_inputs_host(w)
+    e, m = w.e, w.m
+    needed = np.array([64, 0, 135, 1, 230], np.int32)
+    c, c_max = 200, 208
+    kept = np.minimum(needed, c).astype(np.int64)
+    buf_h = synth.bf16_bits_to_f32(synth.normal_host(7, "buf_e", (e, c_max, m), 1.0, "bf16"))
+    stale = synth.bf16_bits_to_f32(synth.normal_host(8, "stale_e", (e, c_max, m), 50.0, "bf16"))
+    d_out_h = synth.bf16_bits_to_f32(synth.normal_host(9, "d_out_e", (e, c_max, m), 1.0, "bf16"))
+    for j in range(e):
+        buf_h[j, kept[j]:] = stale[j, kept[j]:]
+    _check_bwd(w, inp, buf_h, d_out_h, needed, kept, c, c_max)
+
+
+def _check_bwd(w, inp, buf_h, d_out_h, needed, kept, c, c_max):
+    e, m, h = w.e, w.m, w.h
     swiglu = w.act == "swiglu"
     bf = torch.bfloat16
     buf = to_dev(buf_h).to(bf)
-    counts = to_dev(ref["needed"].astype(np.int32))
+    counts = to_dev(np.asarray(needed).astype(np.int32))
     c_dev = to_dev(np.array([c], np.int32))
     w1, w3, w2 = to_dev(inp["w1"]), to_dev(inp["w3"]), to_dev(inp["w2"])
     b1, b2 = to_dev(inp["b1"]), to_dev(inp["b2"])
