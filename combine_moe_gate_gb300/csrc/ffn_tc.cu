@@ -56,8 +56,11 @@ constexpr int SMEM_RING = 192 * 1024;   // operand ring per CTA
 // rows; a last K block that is only partly kept is read from the tail maps
 // instead ([e * BK, M or N]: those rows copied, zeros after them), so no
 // row past an expert's kept rows is ever read.
+// EPI_DGELU / EPI_DRELU: the activation backward fused into the recomputed
+// pre-activation: out = d_hid * act'(acc + bias) with d_hid (GemmArgs::aux)
+// laid out like out; the pre-activation itself is never stored.
 enum Epi { EPI_GELU = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_BIAS = 3, EPI_BIAS_BMN = 4,
-           EPI_WGRAD_MN = 5 };
+           EPI_WGRAD_MN = 5, EPI_DGELU = 6, EPI_DRELU = 7 };
 
 // Tile shape.  TM = 1: 128 x 256 tiles, two 256-column accumulators in TMEM so
 // the epilogue of one tile overlaps the main loop of the next.  TM = 2:
@@ -165,6 +168,8 @@ struct GemmArgs {
     // acc * (a_scale * b_scale) + bias.  NULL for bf16.
     const float *a_scale;
     const float *b_scale;
+    // EPI_DGELU / EPI_DRELU: d_hid [e * c_max, n_out], the rows of out.
+    const __nv_bfloat16 *aux;
     // Error-path test: the producers issue no copies, so the MMA issuer's
     // bounded wait on the first stage runs out (MOE_ERR_TIMEOUT).
     int32_t stall;
@@ -497,6 +502,35 @@ __device__ __forceinline__ float2 gelu_erf2(float2 a) {
     return __fmul2_rn(a, phi);
 }
 
+// GELU'(z) = Phi(z) + z phi(z), two values at a time: Phi as in gelu_erf2
+// (A&S 7.1.28 erfc, 1 - erfc/2 above zero, erfc/2 below); phi(z) =
+// 2^(-z^2 log2(e) / 2) / sqrt(2 pi) with the approximate power of two
+// (relative error ~2^-22, far below the bf16 rounding that follows).
+__device__ __forceinline__ float2 gelu_grad2(float2 z) {
+    const float2 x = __fmul2_rn(make_float2(fabsf(z.x), fabsf(z.y)),
+                                make_float2(0.70710678118654752f, 0.70710678118654752f));
+    float2 p = __ffma2_rn(x, make_float2(0.0000430638f, 0.0000430638f),
+                          make_float2(0.0002765672f, 0.0002765672f));
+    p = __ffma2_rn(x, p, make_float2(0.0001520143f, 0.0001520143f));
+    p = __ffma2_rn(x, p, make_float2(0.0092705272f, 0.0092705272f));
+    p = __ffma2_rn(x, p, make_float2(0.0422820123f, 0.0422820123f));
+    p = __ffma2_rn(x, p, make_float2(0.0705230784f, 0.0705230784f));
+    p = __ffma2_rn(x, p, make_float2(1.0f, 1.0f));
+    float2 q = __fmul2_rn(p, p);
+    q = __fmul2_rn(q, q);
+    q = __fmul2_rn(q, q);
+    q = __fmul2_rn(q, q);
+    float2 r, d;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.x) : "f"(q.x));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.y) : "f"(q.y));
+    r = __fmul2_rn(r, make_float2(0.5f, 0.5f));
+    const float2 cdf = make_float2(z.x >= 0.0f ? 1.0f - r.x : r.x, z.y >= 0.0f ? 1.0f - r.y : r.y);
+    const float2 t = __fmul2_rn(__fmul2_rn(z, z), make_float2(-0.72134752044448170f, -0.72134752044448170f));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(d.x) : "f"(t.x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(d.y) : "f"(t.y));
+    return __ffma2_rn(__fmul2_rn(z, make_float2(0.3989422804014327f, 0.3989422804014327f)), d, cdf);
+}
+
 __device__ __forceinline__ float silu(float a) { return a / (1.0f + expf(-a)); }
 
 // Tile t -> (expert j, m-tile, n-tile); m-tile varies fastest.  rows: the
@@ -535,6 +569,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     constexpr bool F8 = EB == 1;   // e4m3 operands (kind::f8f6f4), scaled epilogue
     static_assert(!F8 || (CL == 2 && EPI != EPI_SWIGLU && EPI != EPI_BIAS_BMN), "e4m3 pair tiles");
     constexpr bool AMN = EPI == EPI_WGRAD_MN;   // A MN-major as well, tail blocks from tmAt / tmBt
+    constexpr bool DACT = EPI == EPI_DGELU || EPI == EPI_DRELU;   // activation backward epilogue
     constexpr bool BMN = EPI == EPI_BIAS_BMN || AMN;   // B MN-major: [K, N] rows, boxes of 64 columns
     static_assert(!BMN || (CL == 2 && TN == 2 && BK == 64), "MN-major B on 256 x 512 pair tiles");
     constexpr bool PAIR = TL::PAIR;
@@ -899,6 +934,9 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 __syncwarp();
                 // e4m3: this lane's row scale (its output row)
                 const float sa = F8 && valid ? args.a_scale[grow0 + lane] : 0.0f;
+                const __nv_bfloat16 *drow =
+                    DACT ? args.aux + ((int64_t)T.j * args.c_max + args.row_lo + row) * (int64_t)args.n_out
+                         : nullptr;
                 const float *bsc = F8 ? args.b_scale + (int64_t)T.j * args.n_out : nullptr;
 #pragma unroll 1
                 for (int c0 = 0; c0 < COLS; c0 += 64) {
@@ -916,6 +954,16 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     for (int h2 = 0; h2 < 2; h2++) {
                         const int gcol = T.nt * NOUT_TILE + col0 + c0 + 32 * h2;
                         uint32_t pk[16];
+                        uint32_t dv[16];   // activation backward: this row's d_hid, 32 columns
+                        if (DACT) {
+#pragma unroll
+                            for (int q = 0; q < 4; q++) {
+                                V16 v{};
+                                if (valid && gcol + q * 8 < args.n_out) v = ld_v16(drow + gcol + q * 8);
+                                dv[q * 4 + 0] = v.w[0]; dv[q * 4 + 1] = v.w[1];
+                                dv[q * 4 + 2] = v.w[2]; dv[q * 4 + 3] = v.w[3];
+                            }
+                        }
 #pragma unroll
                         for (int q = 0; q < 4; q++) {
                             const float4 *bp = reinterpret_cast<const float4 *>(bsl + c0 + 32 * h2 + q * 8);
@@ -941,6 +989,16 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                                               : __fadd2_rn(acc2, bb[i]);
                                 if (EPI == EPI_GELU) a = gelu_erf2(a);
                                 else if (EPI == EPI_RELU) a = make_float2(fmaxf(a.x, 0.0f), fmaxf(a.y, 0.0f));
+                                if (DACT) {
+                                    const uint32_t g2 = dv[q * 4 + i];
+                                    const float2 g = make_float2(__uint_as_float(g2 << 16),
+                                                                 __uint_as_float(g2 & 0xFFFF0000u));
+                                    const float2 da = EPI == EPI_DGELU
+                                                          ? gelu_grad2(a)
+                                                          : make_float2(a.x > 0.0f ? 1.0f : 0.0f,
+                                                                        a.y > 0.0f ? 1.0f : 0.0f);
+                                    a = __fmul2_rn(g, da);
+                                }
                                 pk[q * 4 + i] = pack_bf16(a.x, a.y);
                             }
                         }
@@ -1227,9 +1285,11 @@ namespace moe {
 // ---------------------------------------------------------------- backward
 // The expert-FFN backward as products on the 256 x 512 pair tiling, with the
 // SIMT activation derivative, tail copies and bias sums in between:
-//   pre = buf w1^T + b1 (SwiGLU: a = buf w1^T, b = buf w3^T), recomputed;
 //   d_hid = d_out w2                  (B = w2 read MN-major in place);
-//   d_pre = d_hid * act'(pre)         (SwiGLU: [d_a | d_b]);
+//   d_pre = d_hid * act'(buf w1^T + b1), the pre-activation recomputed in
+//                                      the product's epilogue (SwiGLU: a =
+//                                      buf w1^T and b = buf w3^T recomputed
+//                                      and stored, then [d_a | d_b]);
 //   d_buf = d_pre w1                  (B = w1 MN-major in place; SwiGLU:
 //                                      d_pre [w1^T | w3^T], one K-major copy);
 //   d_w2 = d_out^T hid, d_w1 = d_pre^T buf (d_w3 = d_b^T buf): the kept rows
@@ -1251,7 +1311,7 @@ BwdLayout bwd_layout(moe_act act, int e, int64_t c_max, int m, int h) {
     BwdLayout L{};
     int64_t o = 0;
     auto take = [&](int64_t bytes) { const int64_t at = o; o += up256i(bytes); return at; };
-    L.pa = take(E * c_max * h * 2);
+    L.pa = take(swiglu ? E * c_max * h * 2 : 0);   // SwiGLU's recomputed a and b
     L.pb = take(swiglu ? E * c_max * h * 2 : 0);
     L.dh = take(E * c_max * h * 2);
     L.dpre = take(E * c_max * H2 * 2);
@@ -1295,6 +1355,24 @@ moe_status gemm_bias_bmn(const void *a, const void *b, void *out, const int32_t 
     GemmArgs g{counts, c_dev, st, nullptr, (__nv_bfloat16 *)out, c_max, e, K, n_out, K, nullptr,
                nullptr, 0, 0};
     return launch_gemm<EPI_BIAS_BMN, 1, 64, 2, 2>(mA, mB, mB, mO, g, stream);
+}
+
+// d_pre = d_hid * act'(buf w1^T + b1) over the kept rows (ReLU / GELU): the
+// pre-activation recomputed on the fc1 tiling and differentiated in the
+// epilogue, never stored.
+moe_status gemm_dact(const void *buf, const void *w1, const void *b1, const void *d_hid, moe_act act,
+                     void *d_pre, const int32_t *counts, const int32_t *c_dev, int e, int64_t c_max,
+                     int m, int h, int32_t *st, cudaStream_t stream) {
+    using T1 = Tiling<1, 64, 2, 1>;
+    CUtensorMap mA, mB, mO;
+    if (!make_map(&mA, buf, (uint64_t)e * c_max, (uint64_t)m, T1::A_BOX_ROWS, 64) ||
+        !make_map(&mB, w1, (uint64_t)e * h, (uint64_t)m, T1::B_BOX_ROWS, 64) ||
+        !make_map(&mO, d_pre, (uint64_t)e * c_max, (uint64_t)h, 32, 32))
+        return MOE_ERR_CUDA;
+    GemmArgs g{counts, c_dev, st, (const __nv_bfloat16 *)b1, (__nv_bfloat16 *)d_pre, c_max, e, m, h, h,
+               nullptr, nullptr, 0, 0, nullptr, nullptr, (const __nv_bfloat16 *)d_hid};
+    return act == MOE_ACT_GELU ? launch_gemm<EPI_DGELU, 1, 64, 2, 1>(mA, mB, mB, mO, g, stream)
+                               : launch_gemm<EPI_DRELU, 1, 64, 2, 1>(mA, mB, mB, mO, g, stream);
 }
 
 // Weight gradients out[j] = A[j]^T B[j] over the first min(counts[j], *c_dev,
@@ -1355,13 +1433,17 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
         MOE_TRY(transpose_pad_launch((const bf *)w3, (int64_t)h * m, m, wT + h, (int64_t)m * H2, H2,
                                      e, h, m, h, nullptr, counts, c_dev, st, stream));
     }
-    // pre-activations, recomputed; then d_hid, d_pre, d_buf
-    MOE_TRY(gemm_bias(buf, w1, h, pa, swiglu ? nullptr : b1, counts, c_dev, e, c_max, m, h, st,
-                      stream));
-    if (swiglu) MOE_TRY(gemm_bias(buf, w3, h, pb, nullptr, counts, c_dev, e, c_max, m, h, st, stream));
+    // d_hid; then d_pre (ReLU / GELU: the pre-activation recomputed and
+    // differentiated in one product; SwiGLU: a and b recomputed, then the
+    // activation backward); then d_buf
     MOE_TRY(gemm_bias_bmn(d_out, w2, dh, counts, c_dev, e, c_max, m, h, st, stream));
-    MOE_TRY(act_bwd_launch(pa, swiglu ? pb : nullptr, dh, act, e, c_max, h, counts, c_dev, dpre, st,
-                           stream));
+    if (swiglu) {
+        MOE_TRY(gemm_bias(buf, w1, h, pa, nullptr, counts, c_dev, e, c_max, m, h, st, stream));
+        MOE_TRY(gemm_bias(buf, w3, h, pb, nullptr, counts, c_dev, e, c_max, m, h, st, stream));
+        MOE_TRY(act_bwd_launch(pa, pb, dh, act, e, c_max, h, counts, c_dev, dpre, st, stream));
+    } else {
+        MOE_TRY(gemm_dact(buf, w1, b1, dh, act, dpre, counts, c_dev, e, c_max, m, h, st, stream));
+    }
     if (swiglu)
         MOE_TRY(gemm_bias(dpre, wT, m, d_buf, nullptr, counts, c_dev, e, c_max, (int)H2, m, st, stream));
     else
