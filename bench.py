@@ -369,8 +369,10 @@ class LayerRun:
         self.M.run_layer(x, wg, gb, w1, b1, w3, w2, b2, self.w.act, self.w.k,
                          self.w.capacity_factor, self.bufs, normalize_gates=bool(self.flags))
 
-    def staged_step(self, ev):
-        """The five C-ABI calls with an event after each stage (ev[0] before)."""
+    def staged_step(self, ev, pre=None):
+        """The five C-ABI calls with an event after each stage (ev[0] before);
+        with `pre`, the expert FFN is the training forward that also keeps its
+        pre-activation there."""
         M, w, b = self.M, self.w, self.bufs
         x, wg, gb, w1, b1, w3, w2, b2 = self.args()
         ev[0].record()
@@ -381,8 +383,12 @@ class LayerRun:
         ev[2].record()
         M.moe_encode(x, b.idx, b.loc, b.counts, b.c_dev, b.buf, b.status)
         ev[3].record()
-        M.moe_expert_ffn(b.buf, b.counts, b.c_dev, w1, b1, w3, w2, b2, w.act, self.ffn_ws, b.out,
-                         b.status)
+        if pre is None:
+            M.moe_expert_ffn(b.buf, b.counts, b.c_dev, w1, b1, w3, w2, b2, w.act, self.ffn_ws, b.out,
+                             b.status)
+        else:
+            M.moe_expert_ffn_train(b.buf, b.counts, b.c_dev, w1, b1, w2, b2, w.act, self.ffn_ws,
+                                   b.out, pre, b.status)
         ev[4].record()
         M.moe_decode(b.out, b.idx, b.loc, b.gates, b.c_dev, b.y, b.status)
         ev[5].record()
@@ -534,7 +540,10 @@ class LayerRun:
         FFN backward (d_buf and the weight gradients from dE), encode backward
         (the copy path's d_x from d_buf) and the gate backward (the gate path's
         d_logits, d_wg, d_bias, d_x from dG).  The two d_x terms are left
-        separate (their sum is one elementwise add)."""
+        separate (their sum is one elementwise add).  For bf16 ReLU / GELU
+        experts the chain's forward is the training forward, which keeps the
+        pre-activation, and the FFN backward reads it (moe_expert_ffn_bwd_saved);
+        the backward that recomputes it is timed alone as well."""
         torch, M, w, b = self.torch, self.M, self.w, self.bufs
         x, wg, gb, w1, b1, w3, w2, b2 = self.args()
         dev, tdt = self.dev, self.tdt
@@ -557,14 +566,23 @@ class LayerRun:
         d_bias = torch.empty((w.e,), device=dev, dtype=torch.float32)
         d_xg = torch.empty((w.s, w.m), device=dev, dtype=torch.float32)
         hid = self.hid()
+        saved = w.dtype == "bf16" and w.act in ("relu", "gelu")
+        pre = torch.empty((w.e, b.c_max, w.h), device=dev, dtype=tdt) if saved else None
 
         def dec():
             M.moe_decode_bwd(dy, b.out, b.idx, b.loc, b.gates, b.counts, b.c_dev, d_out, d_g,
                              b.status)
 
-        def ffn():
+        def ffn_recompute():
             M.moe_expert_ffn_bwd(b.buf, hid, b.counts, b.c_dev, w1, b1, w3, w2, w.act, d_out, ws,
                                  d_buf, d_w1, d_w3, d_w2, d_b1, d_b2, b.status)
+
+        def ffn():
+            if pre is None:
+                ffn_recompute()
+            else:
+                M.moe_expert_ffn_bwd_saved(b.buf, hid, pre, b.counts, b.c_dev, w1, w2, w.act, d_out,
+                                           ws, d_buf, d_w1, d_w2, d_b1, d_b2, b.status)
 
         def enc():
             M.moe_encode_bwd(d_buf, b.idx, b.loc, b.c_dev, dx, b.status)
@@ -573,11 +591,11 @@ class LayerRun:
             M.moe_gate_bwd(x, wg, gb, b.idx, b.gates, d_g, d_logits, b.status, d_wg=d_wg,
                            d_bias=d_bias, d_x=d_xg, flags=self.flags)
 
-        # the forward whose buf / hid / out the backward reads
-        self.staged_step([torch.cuda.Event() for _ in range(6)])
+        # the forward whose buf / hid / out (/ pre) the backward reads
+        self.staged_step([torch.cuda.Event() for _ in range(6)], pre)
 
         def chain():
-            self.staged_step([torch.cuda.Event() for _ in range(6)])
+            self.staged_step([torch.cuda.Event() for _ in range(6)], pre)
             dec()
             ffn()
             enc()
@@ -587,6 +605,8 @@ class LayerRun:
         for name, fn in (("decode_bwd", dec), ("ffn_bwd", ffn), ("encode_bwd", enc),
                          ("gate_bwd", gate)):
             res[name] = self.time_calls(fn, steps, warmup)
+        if pre is not None:
+            res["ffn_bwd_recompute"] = self.time_calls(ffn_recompute, steps, warmup)
         res["fwd_bwd_step"] = self.time_calls(chain, steps, warmup)
         self.check_status()
         return res
@@ -634,9 +654,15 @@ def graded_report(name, run, stage_ms, pk, extra=None):
          "layer_ms": sum(stage_ms.values()),
          "stages": {n: rate(n, ms, work[n], pk) for n, ms in stage_ms.items()}}
     if extra:
+        saved = "ffn_bwd_recompute" in extra
         for n, ms in extra.items():
-            if n in work:
-                d["stages"][n] = dict(rate(n, ms, work[n], pk), note="backward, timed alone")
+            base = "ffn_bwd" if n == "ffn_bwd_recompute" else n
+            if base in work:
+                note = "backward, timed alone"
+                if base == "ffn_bwd" and saved:
+                    note += ("; recomputes the pre-activation" if n != base else
+                             "; reads the pre-activation the training forward kept")
+                d["stages"][n] = dict(rate(base, ms, work[base], pk), note=note)
             else:
                 d["stages"][n] = {"ms": ms, "tokens_per_s": w.s / (ms * 1e-3),
                                   "note": "forward + decode/FFN/encode/gate backward, one chain"}

@@ -51,7 +51,7 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
                          const void *w1, const void *b1, const void *w3, const void *w2,
                          const void *b2, moe_act act, int e, int64_t c_max, int m, int h,
                          void *hid, void *out, int32_t *st, cudaStream_t stream, int row_lo,
-                         int row_hi);
+                         int row_hi, void *pre = nullptr);
 size_t ffn_tc_bwd_workspace_bytes(moe_act act, int e, int64_t c_max, int m, int h);
 moe_status quantize_rows_fp8_launch(const void *src, int64_t batches, int64_t rows_per_batch,
                                     int cols, const int32_t *counts, const int32_t *c_dev,
@@ -66,7 +66,8 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
                              const int32_t *c_dev, const void *w1, const void *b1, const void *w3,
                              const void *w2, moe_act act, int e, int64_t c_max, int m, int h,
                              const void *d_out, void *ws, void *d_buf, void *d_w1, void *d_w3,
-                             void *d_w2, void *d_b1, void *d_b2, int32_t *st, cudaStream_t stream);
+                             void *d_w2, void *d_b1, void *d_b2, int32_t *st, cudaStream_t stream,
+                             const void *pre = nullptr);
 moe_status ffn_simt_launch(const void *buf, moe_dtype dt, const int32_t *counts,
                            const int32_t *c_dev, const void *w1, const void *b1, const void *w3,
                            const void *w2, const void *b2, moe_act act, int e, int64_t c_max,
@@ -201,11 +202,11 @@ size_t moe_expert_ffn_workspace_size(moe_dtype dt, moe_act act, int e, int64_t c
     return up256((size_t)e * (size_t)c_max * (size_t)h * esize(dt));
 }
 
-moe_status moe_expert_ffn(const void *buf, moe_dtype dt, const int32_t *counts,
-                          const int32_t *c_dev, const void *w1, const void *b1, const void *w3,
-                          const void *w2, const void *b2, moe_act act, int e, int64_t c_max, int m,
-                          int h, void *workspace, size_t workspace_bytes, void *out,
-                          int32_t *dev_status, void *stream) {
+static moe_status expert_ffn(const void *buf, moe_dtype dt, const int32_t *counts,
+                             const int32_t *c_dev, const void *w1, const void *b1, const void *w3,
+                             const void *w2, const void *b2, moe_act act, int e, int64_t c_max,
+                             int m, int h, void *workspace, size_t workspace_bytes, void *out,
+                             void *pre, int32_t *dev_status, void *stream) {
     if (!rows_ok(dt, m) || !rows_ok(dt, h) || e < 1 || e > kMaxE || c_max < 1 ||
         c_max > 0x7fffffff || !ok16(buf) || !ok4(counts) || !ok4(c_dev) || !ok16(w1) ||
         !ok16(w2) || !opt16(b1) || !opt16(b2) || !ok16(out) || !ok4(dev_status) ||
@@ -216,13 +217,34 @@ moe_status moe_expert_ffn(const void *buf, moe_dtype dt, const int32_t *counts,
         return MOE_ERR_INVALID_ARG;
     if (act == MOE_ACT_SWIGLU && (!ok16(w3) || b1 != nullptr || b2 != nullptr))
         return MOE_ERR_INVALID_ARG;
+    if (pre && (dt != MOE_BF16 || act == MOE_ACT_SWIGLU)) return MOE_ERR_UNSUPPORTED;
+    if (pre && !ok16(pre)) return MOE_ERR_INVALID_ARG;
     if (dt == MOE_BF16) {
         if (!ffn_tc_supported(e, c_max, m, h)) return MOE_ERR_UNSUPPORTED;
         return ffn_tc_launch(buf, counts, c_dev, w1, b1, w3, w2, b2, act, e, c_max, m, h,
-                             workspace, out, dev_status, as_stream(stream), 0, 0);
+                             workspace, out, dev_status, as_stream(stream), 0, 0, pre);
     }
     return ffn_simt_launch(buf, dt, counts, c_dev, w1, b1, w3, w2, b2, act, e, c_max, m, h,
                            workspace, out, dev_status, as_stream(stream));
+}
+
+moe_status moe_expert_ffn(const void *buf, moe_dtype dt, const int32_t *counts,
+                          const int32_t *c_dev, const void *w1, const void *b1, const void *w3,
+                          const void *w2, const void *b2, moe_act act, int e, int64_t c_max, int m,
+                          int h, void *workspace, size_t workspace_bytes, void *out,
+                          int32_t *dev_status, void *stream) {
+    return expert_ffn(buf, dt, counts, c_dev, w1, b1, w3, w2, b2, act, e, c_max, m, h, workspace,
+                      workspace_bytes, out, nullptr, dev_status, stream);
+}
+
+moe_status moe_expert_ffn_train(const void *buf, moe_dtype dt, const int32_t *counts,
+                                const int32_t *c_dev, const void *w1, const void *b1,
+                                const void *w2, const void *b2, moe_act act, int e, int64_t c_max,
+                                int m, int h, void *workspace, size_t workspace_bytes, void *out,
+                                void *pre, int32_t *dev_status, void *stream) {
+    if (!pre) return MOE_ERR_INVALID_ARG;
+    return expert_ffn(buf, dt, counts, c_dev, w1, b1, nullptr, w2, b2, act, e, c_max, m, h,
+                      workspace, workspace_bytes, out, pre, dev_status, stream);
 }
 
 moe_status moe_decode(const void *out, moe_dtype dt, const int32_t *idx, const int32_t *loc,
@@ -267,13 +289,13 @@ size_t moe_expert_ffn_bwd_workspace_size(moe_dtype dt, moe_act act, int e, int64
     return ffn_tc_bwd_workspace_bytes(act, e, c_max, m, h);
 }
 
-moe_status moe_expert_ffn_bwd(const void *buf, const void *hid, moe_dtype dt,
-                              const int32_t *counts, const int32_t *c_dev, const void *w1,
-                              const void *b1, const void *w3, const void *w2, moe_act act, int e,
-                              int64_t c_max, int m, int h, const void *d_out, void *workspace,
-                              size_t workspace_bytes, void *d_buf, void *d_w1, void *d_w3,
-                              void *d_w2, void *d_b1, void *d_b2, int32_t *dev_status,
-                              void *stream) {
+static moe_status expert_ffn_bwd(const void *buf, const void *hid, const void *pre, moe_dtype dt,
+                                 const int32_t *counts, const int32_t *c_dev, const void *w1,
+                                 const void *b1, const void *w3, const void *w2, moe_act act, int e,
+                                 int64_t c_max, int m, int h, const void *d_out, void *workspace,
+                                 size_t workspace_bytes, void *d_buf, void *d_w1, void *d_w3,
+                                 void *d_w2, void *d_b1, void *d_b2, int32_t *dev_status,
+                                 void *stream) {
     if (!rows_ok(dt, m) || !rows_ok(dt, h) || e < 1 || e > kMaxE || c_max < 1 ||
         c_max > 0x7fffffff || !ok16(buf) || !ok16(hid) || !ok4(counts) || !ok4(c_dev) ||
         !ok16(w1) || !ok16(w2) || !opt16(b1) || !ok16(d_out) || !ok16(workspace) ||
@@ -293,9 +315,35 @@ moe_status moe_expert_ffn_bwd(const void *buf, const void *hid, moe_dtype dt,
     if (!ffn_tc_supported(e, c_max, m, h) || !ffn_tc_supported(e, h2, m, h) ||
         (int64_t)e * h2 >= ((int64_t)1 << 31) || (int64_t)e * ((c_max + 7) / 8 * 8) >= ((int64_t)1 << 31))
         return MOE_ERR_UNSUPPORTED;
+    if (pre && (act == MOE_ACT_SWIGLU || !ok16(pre))) return MOE_ERR_INVALID_ARG;
     return ffn_tc_bwd_launch(buf, hid, counts, c_dev, w1, b1, w3, w2, act, e, c_max, m, h, d_out,
                              workspace, d_buf, d_w1, d_w3, d_w2, d_b1, d_b2, dev_status,
-                             as_stream(stream));
+                             as_stream(stream), pre);
+}
+
+moe_status moe_expert_ffn_bwd(const void *buf, const void *hid, moe_dtype dt,
+                              const int32_t *counts, const int32_t *c_dev, const void *w1,
+                              const void *b1, const void *w3, const void *w2, moe_act act, int e,
+                              int64_t c_max, int m, int h, const void *d_out, void *workspace,
+                              size_t workspace_bytes, void *d_buf, void *d_w1, void *d_w3,
+                              void *d_w2, void *d_b1, void *d_b2, int32_t *dev_status,
+                              void *stream) {
+    return expert_ffn_bwd(buf, hid, nullptr, dt, counts, c_dev, w1, b1, w3, w2, act, e, c_max, m, h,
+                          d_out, workspace, workspace_bytes, d_buf, d_w1, d_w3, d_w2, d_b1, d_b2,
+                          dev_status, stream);
+}
+
+moe_status moe_expert_ffn_bwd_saved(const void *buf, const void *hid, const void *pre,
+                                    moe_dtype dt, const int32_t *counts, const int32_t *c_dev,
+                                    const void *w1, const void *w2, moe_act act, int e,
+                                    int64_t c_max, int m, int h, const void *d_out,
+                                    void *workspace, size_t workspace_bytes, void *d_buf,
+                                    void *d_w1, void *d_w2, void *d_b1, void *d_b2,
+                                    int32_t *dev_status, void *stream) {
+    if (!pre) return MOE_ERR_INVALID_ARG;
+    return expert_ffn_bwd(buf, hid, pre, dt, counts, c_dev, w1, nullptr, nullptr, w2, act, e, c_max,
+                          m, h, d_out, workspace, workspace_bytes, d_buf, d_w1, nullptr, d_w2, d_b1,
+                          d_b2, dev_status, stream);
 }
 
 size_t moe_layer_workspace_size(moe_dtype dt, moe_act act, int64_t s, int m, int e, int k,

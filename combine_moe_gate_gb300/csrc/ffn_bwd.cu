@@ -199,18 +199,34 @@ act_bwd_kernel(const __nv_bfloat16 *__restrict__ pa, const __nv_bfloat16 *__rest
 // 16-byte load a row); its 16 warps take every 16th kept row, CS_U rows in
 // flight, and the partials are added in warp order.
 constexpr int CS_WARPS = 16, CS_COLS = 256, CS_U = 4;
+
+struct ColsumOp {
+    const __nv_bfloat16 *src;
+    int cols;
+    int64_t pitch;
+    __nv_bfloat16 *out;
+};
+struct ColsumOps {
+    ColsumOp op[2];
+};
 static_assert(CS_COLS == 32 * 8 && CS_WARPS * 32 >= CS_COLS, "8 columns a lane, a thread a column");
 
 __global__ void __launch_bounds__(CS_WARPS * 32)
-colsum_kernel(const __nv_bfloat16 *__restrict__ src, int64_t c_max, int cols, int64_t pitch,
-              const int32_t *__restrict__ counts, const int32_t *__restrict__ c_dev,
-              __nv_bfloat16 *__restrict__ out, int32_t *status) {
+colsum_kernel(ColsumOps ops, int64_t c_max, const int32_t *__restrict__ counts,
+              const int32_t *__restrict__ c_dev, int32_t *status) {
     pdl_enter();
     if (status_bad(status)) return;
     __shared__ float part[CS_WARPS][CS_COLS];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int j = blockIdx.y;
-    const int c0 = blockIdx.x * CS_COLS + 8 * lane;
+    // the column blocks of op 0, then those of op 1
+    const int nb0 = (ops.op[0].cols + CS_COLS - 1) / CS_COLS;
+    const ColsumOp &o = ops.op[(int)blockIdx.x < nb0 ? 0 : 1];
+    const int bx = (int)blockIdx.x < nb0 ? (int)blockIdx.x : (int)blockIdx.x - nb0;
+    const __nv_bfloat16 *__restrict__ src = o.src;
+    const int cols = o.cols;
+    const int64_t pitch = o.pitch;
+    const int c0 = bx * CS_COLS + 8 * lane;
     const int64_t kept = max(0, min(min(counts[j], *c_dev), (int)min(c_max, (int64_t)0x7fffffff)));
     float acc[8];
 #pragma unroll
@@ -239,12 +255,12 @@ colsum_kernel(const __nv_bfloat16 *__restrict__ src, int64_t c_max, int cols, in
     for (int i = 0; i < 8; i++) part[warp][8 * lane + i] = acc[i];
     __syncthreads();
     // threads 0 .. CS_COLS - 1 finish one column each
-    const int col = blockIdx.x * CS_COLS + threadIdx.x;
+    const int col = bx * CS_COLS + threadIdx.x;
     if (threadIdx.x < CS_COLS && col < cols) {
         float sum = 0.0f;
 #pragma unroll
         for (int w = 0; w < CS_WARPS; w++) sum += part[w][threadIdx.x];
-        out[(int64_t)j * cols + col] = __float2bfloat16_rn(sum);
+        o.out[(int64_t)j * cols + col] = __float2bfloat16_rn(sum);
     }
 }
 
@@ -289,14 +305,18 @@ moe_status act_bwd_launch(const __nv_bfloat16 *pa, const __nv_bfloat16 *pb,
 // ------------------------------------------------------------ tail rows
 namespace {
 
-constexpr int TR_WARPS = 8;   // one warp per row, 64 / TR_WARPS CTAs per expert
+constexpr int TR_WARPS = 8;   // one warp per row, 64 / TR_WARPS CTAs per expert and operand
 
 __global__ void __launch_bounds__(TR_WARPS * 32)
-tail_rows_kernel(const __nv_bfloat16 *__restrict__ src, int64_t src_pitch, int64_t c_max, int cols,
-                 const int32_t *__restrict__ counts, const int32_t *__restrict__ c_dev,
-                 __nv_bfloat16 *__restrict__ dst, int32_t *status) {
+tail_rows_kernel(TailOps ops, int64_t c_max, const int32_t *__restrict__ counts,
+                 const int32_t *__restrict__ c_dev, int32_t *status) {
     pdl_enter();
     if (status_bad(status)) return;
+    const TailOp &o = ops.op[blockIdx.z];
+    const __nv_bfloat16 *__restrict__ src = o.src;
+    __nv_bfloat16 *__restrict__ dst = o.dst;
+    const int64_t src_pitch = o.pitch;
+    const int cols = o.cols;
     const int j = blockIdx.y;
     const int64_t kept = min((int64_t)max(counts[j], 0), min((int64_t)*c_dev, c_max));
     const int nvalid = (int)(kept & 63);
@@ -313,25 +333,35 @@ tail_rows_kernel(const __nv_bfloat16 *__restrict__ src, int64_t src_pitch, int64
 
 }  // namespace
 
-moe_status tail_rows_launch(const __nv_bfloat16 *src, int64_t src_pitch, int64_t c_max, int cols,
-                            int e, const int32_t *counts, const int32_t *c_dev, __nv_bfloat16 *dst,
-                            int32_t *status, cudaStream_t stream) {
-    if (e < 1 || e > 65535 || c_max < 1 || cols < 8 || cols % 8 || src_pitch % 8 || !aligned16(src) ||
-        !aligned16(dst))
-        return MOE_ERR_INVALID_ARG;
-    return launch_pdl(tail_rows_kernel, dim3(64 / TR_WARPS, (unsigned)e), dim3(TR_WARPS * 32), 0,
-                      stream, src, src_pitch, c_max, cols, counts, c_dev, dst, status);
+moe_status tail_rows_launch(const TailOps &ops, int nops, int64_t c_max, int e,
+                            const int32_t *counts, const int32_t *c_dev, int32_t *status,
+                            cudaStream_t stream) {
+    if (nops < 1 || nops > TAIL_MAX_OPS || e < 1 || e > 65535 || c_max < 1) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < nops; i++) {
+        const TailOp &o = ops.op[i];
+        if (o.cols < 8 || o.cols % 8 || o.pitch % 8 || !aligned16(o.src) || !aligned16(o.dst))
+            return MOE_ERR_INVALID_ARG;
+    }
+    return launch_pdl(tail_rows_kernel, dim3(64 / TR_WARPS, (unsigned)e, (unsigned)nops),
+                      dim3(TR_WARPS * 32), 0, stream, ops, c_max, counts, c_dev, status);
 }
 
 moe_status colsum_launch(const __nv_bfloat16 *src, int e, int64_t c_max, int cols,
                          int64_t src_pitch, const int32_t *counts, const int32_t *c_dev,
-                         __nv_bfloat16 *out, int32_t *status, cudaStream_t stream) {
+                         __nv_bfloat16 *out, int32_t *status, cudaStream_t stream,
+                         const __nv_bfloat16 *src2, int cols2, int64_t src2_pitch,
+                         __nv_bfloat16 *out2) {
     // rows of whole 16-byte chunks
     if (e < 1 || e > 65535 || cols < 1 || cols % 8 || src_pitch % 8 || !aligned16(src))
         return MOE_ERR_INVALID_ARG;
-    return launch_pdl(colsum_kernel, dim3((unsigned)((cols + CS_COLS - 1) / CS_COLS), (unsigned)e),
-                      dim3(CS_WARPS * 32), 0, stream, src, c_max, cols, src_pitch, counts, c_dev,
-                      out, status);
+    if (src2 && (cols2 < 1 || cols2 % 8 || src2_pitch % 8 || !aligned16(src2)))
+        return MOE_ERR_INVALID_ARG;
+    ColsumOps ops{};
+    ops.op[0] = ColsumOp{src, cols, src_pitch, out};
+    ops.op[1] = src2 ? ColsumOp{src2, cols2, src2_pitch, out2} : ColsumOp{src, 0, src_pitch, out};
+    const int nb = (cols + CS_COLS - 1) / CS_COLS + (src2 ? (cols2 + CS_COLS - 1) / CS_COLS : 0);
+    return launch_pdl(colsum_kernel, dim3((unsigned)nb, (unsigned)e), dim3(CS_WARPS * 32), 0, stream,
+                      ops, c_max, counts, c_dev, status);
 }
 
 }  // namespace moe

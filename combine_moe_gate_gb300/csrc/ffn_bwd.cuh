@@ -29,20 +29,33 @@ moe_status act_bwd_launch(const __nv_bfloat16 *pa, const __nv_bfloat16 *pb,
 
 // out[b][c] = sum over the kept rows r of src[b][r][c] (fp32 sum in a fixed
 // order, one rounding to bf16); src rows of `cols` columns at row pitch
-// src_pitch, batch stride c_max * src_pitch.
+// src_pitch, batch stride c_max * src_pitch.  With src2, the same for a
+// second matrix (cols2, src2_pitch, out2) in the same launch.
 moe_status colsum_launch(const __nv_bfloat16 *src, int e, int64_t c_max, int cols,
                          int64_t src_pitch, const int32_t *counts, const int32_t *c_dev,
-                         __nv_bfloat16 *out, int32_t *status, cudaStream_t stream);
+                         __nv_bfloat16 *out, int32_t *status, cudaStream_t stream,
+                         const __nv_bfloat16 *src2 = nullptr, int cols2 = 0,
+                         int64_t src2_pitch = 0, __nv_bfloat16 *out2 = nullptr);
 
 // The partly kept last 64-row block of every expert, for the MN-major weight
-// gradients: with kept_b = min(counts[b], *c_dev, c_max) and r0 = kept_b
-// rounded down to a multiple of 64, dst[b][r] = src[b][r0 + r] for
-// r < kept_b - r0 and 0 for the rest of the 64 rows; experts whose kept rows
-// end on a block boundary are left untouched (nothing reads them).  src rows
-// of `cols` columns at row pitch src_pitch, c_max rows per expert; dst
-// [e, 64, cols] dense.
-moe_status tail_rows_launch(const __nv_bfloat16 *src, int64_t src_pitch, int64_t c_max, int cols,
-                            int e, const int32_t *counts, const int32_t *c_dev, __nv_bfloat16 *dst,
-                            int32_t *status, cudaStream_t stream);
+// gradients, for up to TAIL_MAX_OPS operands in one launch: with kept_b =
+// min(counts[b], *c_dev, c_max) and r0 = kept_b rounded down to a multiple of
+// 64, dst[b][r] = src[b][r0 + r] for r < kept_b - r0 and 0 for the rest of
+// the 64 rows; experts whose kept rows end on a block boundary are left
+// untouched (nothing reads them).  src rows of `cols` columns at row pitch
+// `pitch`, c_max rows per expert; dst [e, 64, cols] dense.
+constexpr int TAIL_MAX_OPS = 4;
+struct TailOp {
+    const __nv_bfloat16 *src;
+    int64_t pitch;
+    int cols;
+    __nv_bfloat16 *dst;
+};
+struct TailOps {
+    TailOp op[TAIL_MAX_OPS];
+};
+moe_status tail_rows_launch(const TailOps &ops, int nops, int64_t c_max, int e,
+                            const int32_t *counts, const int32_t *c_dev, int32_t *status,
+                            cudaStream_t stream);
 
 }  // namespace moe

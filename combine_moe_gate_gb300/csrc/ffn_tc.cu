@@ -59,8 +59,13 @@ constexpr int SMEM_RING = 192 * 1024;   // operand ring per CTA
 // EPI_DGELU / EPI_DRELU: the activation backward fused into the recomputed
 // pre-activation: out = d_hid * act'(acc + bias) with d_hid (GemmArgs::aux)
 // laid out like out; the pre-activation itself is never stored.
+// EPI_GELU_SAVE / EPI_RELU_SAVE: fc1 that also stores the pre-activation
+// acc + bias (bf16) to GemmArgs::aux_out, laid out like out.
+// EPI_DGELU_BMN / EPI_DRELU_BMN: d_hid = acc (B MN-major) times act'(pre)
+// with the saved pre-activation (GemmArgs::aux) laid out like out.
 enum Epi { EPI_GELU = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_BIAS = 3, EPI_BIAS_BMN = 4,
-           EPI_WGRAD_MN = 5, EPI_DGELU = 6, EPI_DRELU = 7 };
+           EPI_WGRAD_MN = 5, EPI_DGELU = 6, EPI_DRELU = 7, EPI_GELU_SAVE = 8, EPI_RELU_SAVE = 9,
+           EPI_DGELU_BMN = 10, EPI_DRELU_BMN = 11 };
 
 // Tile shape.  TM = 1: 128 x 256 tiles, two 256-column accumulators in TMEM so
 // the epilogue of one tile overlaps the main loop of the next.  TM = 2:
@@ -168,8 +173,11 @@ struct GemmArgs {
     // acc * (a_scale * b_scale) + bias.  NULL for bf16.
     const float *a_scale;
     const float *b_scale;
-    // EPI_DGELU / EPI_DRELU: d_hid [e * c_max, n_out], the rows of out.
+    // EPI_DGELU / EPI_DRELU: d_hid [e * c_max, n_out], the rows of out;
+    // EPI_DGELU_BMN / EPI_DRELU_BMN: the saved pre-activation, likewise.
     const __nv_bfloat16 *aux;
+    // EPI_GELU_SAVE / EPI_RELU_SAVE: where the pre-activation goes, likewise.
+    __nv_bfloat16 *aux_out;
     // Error-path test: the producers issue no copies, so the MMA issuer's
     // bounded wait on the first stage runs out (MOE_ERR_TIMEOUT).
     int32_t stall;
@@ -570,7 +578,12 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     static_assert(!F8 || (CL == 2 && EPI != EPI_SWIGLU && EPI != EPI_BIAS_BMN), "e4m3 pair tiles");
     constexpr bool AMN = EPI == EPI_WGRAD_MN;   // A MN-major as well, tail blocks from tmAt / tmBt
     constexpr bool DACT = EPI == EPI_DGELU || EPI == EPI_DRELU;   // activation backward epilogue
-    constexpr bool BMN = EPI == EPI_BIAS_BMN || AMN;   // B MN-major: [K, N] rows, boxes of 64 columns
+    constexpr bool DACTP = EPI == EPI_DGELU_BMN || EPI == EPI_DRELU_BMN;   // act' of a saved pre
+    constexpr bool DGELU = EPI == EPI_DGELU || EPI == EPI_DGELU_BMN;
+    constexpr bool SAVE = EPI == EPI_GELU_SAVE || EPI == EPI_RELU_SAVE;   // fc1 keeping its pre-activation
+    constexpr bool GELU = EPI == EPI_GELU || EPI == EPI_GELU_SAVE;
+    constexpr bool RELU = EPI == EPI_RELU || EPI == EPI_RELU_SAVE;
+    constexpr bool BMN = EPI == EPI_BIAS_BMN || AMN || DACTP;   // B MN-major: [K, N] rows, 64-column boxes
     static_assert(!BMN || (CL == 2 && TN == 2 && BK == 64), "MN-major B on 256 x 512 pair tiles");
     constexpr bool PAIR = TL::PAIR;
     constexpr int STAGES = TL::STAGES, BMT = TL::BMT, A_BYTES = TL::A_BYTES;
@@ -935,7 +948,11 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 // e4m3: this lane's row scale (its output row)
                 const float sa = F8 && valid ? args.a_scale[grow0 + lane] : 0.0f;
                 const __nv_bfloat16 *drow =
-                    DACT ? args.aux + ((int64_t)T.j * args.c_max + args.row_lo + row) * (int64_t)args.n_out
+                    DACT || DACTP
+                        ? args.aux + ((int64_t)T.j * args.c_max + args.row_lo + row) * (int64_t)args.n_out
+                        : nullptr;
+                __nv_bfloat16 *prow =
+                    SAVE ? args.aux_out + ((int64_t)T.j * args.c_max + args.row_lo + row) * (int64_t)args.n_out
                          : nullptr;
                 const float *bsc = F8 ? args.b_scale + (int64_t)T.j * args.n_out : nullptr;
 #pragma unroll 1
@@ -954,8 +971,8 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     for (int h2 = 0; h2 < 2; h2++) {
                         const int gcol = T.nt * NOUT_TILE + col0 + c0 + 32 * h2;
                         uint32_t pk[16];
-                        uint32_t dv[16];   // activation backward: this row's d_hid, 32 columns
-                        if (DACT) {
+                        uint32_t dv[16];   // activation backward: this row's d_hid or pre, 32 columns
+                        if (DACT || DACTP) {
 #pragma unroll
                             for (int q = 0; q < 4; q++) {
                                 V16 v{};
@@ -966,6 +983,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                         }
 #pragma unroll
                         for (int q = 0; q < 4; q++) {
+                            uint32_t pp[4];   // fc1 keeping its pre-activation: 8 packed columns
                             const float4 *bp = reinterpret_cast<const float4 *>(bsl + c0 + 32 * h2 + q * 8);
                             const float4 bl = bp[0], bh = bp[1];
                             const float2 bb[4] = {make_float2(bl.x, bl.y), make_float2(bl.z, bl.w),
@@ -987,19 +1005,28 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                                                                 __uint_as_float(r[h2][q * 8 + 2 * i + 1]));
                                 float2 a = F8 ? __ffma2_rn(acc2, make_float2(sc[2 * i], sc[2 * i + 1]), bb[i])
                                               : __fadd2_rn(acc2, bb[i]);
-                                if (EPI == EPI_GELU) a = gelu_erf2(a);
-                                else if (EPI == EPI_RELU) a = make_float2(fmaxf(a.x, 0.0f), fmaxf(a.y, 0.0f));
-                                if (DACT) {
-                                    const uint32_t g2 = dv[q * 4 + i];
-                                    const float2 g = make_float2(__uint_as_float(g2 << 16),
-                                                                 __uint_as_float(g2 & 0xFFFF0000u));
-                                    const float2 da = EPI == EPI_DGELU
-                                                          ? gelu_grad2(a)
-                                                          : make_float2(a.x > 0.0f ? 1.0f : 0.0f,
-                                                                        a.y > 0.0f ? 1.0f : 0.0f);
+                                if (SAVE) pp[i] = pack_bf16(a.x, a.y);
+                                if (GELU) a = gelu_erf2(a);
+                                else if (RELU) a = make_float2(fmaxf(a.x, 0.0f), fmaxf(a.y, 0.0f));
+                                if (DACT || DACTP) {
+                                    // DACT: aux is d_hid, a the pre-activation; DACTP: aux is
+                                    // the saved pre-activation, a = d_hid
+                                    const uint32_t u2 = dv[q * 4 + i];
+                                    const float2 u = make_float2(__uint_as_float(u2 << 16),
+                                                                 __uint_as_float(u2 & 0xFFFF0000u));
+                                    const float2 z = DACT ? a : u, g = DACT ? u : a;
+                                    const float2 da = DGELU ? gelu_grad2(z)
+                                                            : make_float2(z.x > 0.0f ? 1.0f : 0.0f,
+                                                                          z.y > 0.0f ? 1.0f : 0.0f);
                                     a = __fmul2_rn(g, da);
                                 }
                                 pk[q * 4 + i] = pack_bf16(a.x, a.y);
+                            }
+                            if (SAVE && valid && gcol + q * 8 < args.n_out) {
+                                // this lane's row of the pre-activation, 8 columns
+                                V16 o;
+                                o.w[0] = pp[0]; o.w[1] = pp[1]; o.w[2] = pp[2]; o.w[3] = pp[3];
+                                st_v16(prow + gcol + q * 8, o);
                             }
                         }
                         epi_store32(&tmO, stg, pk, all_kept, valid, lane, grow0, gcol,
@@ -1197,7 +1224,7 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
                          const void *w1, const void *b1, const void *w3, const void *w2,
                          const void *b2, moe_act act, int e, int64_t c_max, int m, int h,
                          void *hid, void *out, int32_t *st, cudaStream_t stream, int row_lo,
-                         int row_hi) {
+                         int row_hi, void *pre) {
     // fc1: 256-row tiles on CTA pairs (2-SM MMA), two accumulators per CTA so
     // its activation epilogue overlaps the next tile's main loop.
     // fc2 (bias-only epilogue, long K, about one tile per pair): 256 x 512
@@ -1221,11 +1248,18 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
         return MOE_ERR_CUDA;
     GemmArgs g1{counts, c_dev, st, (const __nv_bfloat16 *)b1, (__nv_bfloat16 *)hid, c_max, e, m, h, h,
                 nullptr, nullptr, row_lo, row_hi};
+    g1.aux_out = (__nv_bfloat16 *)pre;   // training: fc1 also keeps its pre-activation
     moe_status r;
-    if (swiglu) r = launch_gemm<EPI_SWIGLU, TM1, BK1, CL1, 1>(mA1, mB1, mB3, mO1, g1, stream);
-    else if (act == MOE_ACT_GELU)
-        r = launch_gemm<EPI_GELU, TM1, BK1, CL1, 1>(mA1, mB1, mB1, mO1, g1, stream);
-    else r = launch_gemm<EPI_RELU, TM1, BK1, CL1, 1>(mA1, mB1, mB1, mO1, g1, stream);
+    if (swiglu) {
+        if (pre) return MOE_ERR_UNSUPPORTED;
+        r = launch_gemm<EPI_SWIGLU, TM1, BK1, CL1, 1>(mA1, mB1, mB3, mO1, g1, stream);
+    } else if (act == MOE_ACT_GELU) {
+        r = pre ? launch_gemm<EPI_GELU_SAVE, TM1, BK1, CL1, 1>(mA1, mB1, mB1, mO1, g1, stream)
+                : launch_gemm<EPI_GELU, TM1, BK1, CL1, 1>(mA1, mB1, mB1, mO1, g1, stream);
+    } else {
+        r = pre ? launch_gemm<EPI_RELU_SAVE, TM1, BK1, CL1, 1>(mA1, mB1, mB1, mO1, g1, stream)
+                : launch_gemm<EPI_RELU, TM1, BK1, CL1, 1>(mA1, mB1, mB1, mO1, g1, stream);
+    }
     if (r != MOE_OK) return r;
     GemmArgs g2{counts, c_dev, st, (const __nv_bfloat16 *)b2, (__nv_bfloat16 *)out, c_max, e, h, m, m,
                 nullptr, nullptr, row_lo, row_hi};
@@ -1289,7 +1323,10 @@ namespace moe {
 //   d_pre = d_hid * act'(buf w1^T + b1), the pre-activation recomputed in
 //                                      the product's epilogue (SwiGLU: a =
 //                                      buf w1^T and b = buf w3^T recomputed
-//                                      and stored, then [d_a | d_b]);
+//                                      and stored, then [d_a | d_b]); with
+//                                      the forward's saved pre-activation,
+//                                      d_pre = (d_out w2) * act'(pre) in one
+//                                      product's epilogue instead;
 //   d_buf = d_pre w1                  (B = w1 MN-major in place; SwiGLU:
 //                                      d_pre [w1^T | w3^T], one K-major copy);
 //   d_w2 = d_out^T hid, d_w1 = d_pre^T buf (d_w3 = d_b^T buf): the kept rows
@@ -1375,6 +1412,24 @@ moe_status gemm_dact(const void *buf, const void *w1, const void *b1, const void
                                : launch_gemm<EPI_DRELU, 1, 64, 2, 1>(mA, mB, mB, mO, g, stream);
 }
 
+// d_pre = (d_out w2) * act'(pre) over the kept rows (ReLU / GELU) with the
+// forward's saved pre-activation: the data-gradient product reads w2
+// MN-major and its epilogue applies the derivative; d_hid is never stored.
+moe_status gemm_dact_bmn(const void *d_out, const void *w2, const void *pre, moe_act act, void *d_pre,
+                         const int32_t *counts, const int32_t *c_dev, int e, int64_t c_max, int m,
+                         int h, int32_t *st, cudaStream_t stream) {
+    using T2 = Tiling<1, 64, 2, 2>;
+    CUtensorMap mA, mB, mO;
+    if (!make_map(&mA, d_out, (uint64_t)e * c_max, (uint64_t)m, T2::A_BOX_ROWS, 64) ||
+        !make_map(&mB, w2, (uint64_t)e * m, (uint64_t)h, 64, 64) ||
+        !make_map(&mO, d_pre, (uint64_t)e * c_max, (uint64_t)h, 32, 32))
+        return MOE_ERR_CUDA;
+    GemmArgs g{counts, c_dev, st, nullptr, (__nv_bfloat16 *)d_pre, c_max, e, m, h, m, nullptr,
+               nullptr, 0, 0, nullptr, nullptr, (const __nv_bfloat16 *)pre};
+    return act == MOE_ACT_GELU ? launch_gemm<EPI_DGELU_BMN, 1, 64, 2, 2>(mA, mB, mB, mO, g, stream)
+                               : launch_gemm<EPI_DRELU_BMN, 1, 64, 2, 2>(mA, mB, mB, mO, g, stream);
+}
+
 // Weight gradients out[j] = A[j]^T B[j] over the first min(counts[j], *c_dev,
 // c_max) rows of expert j, both operands read MN-major in place: A rows of
 // a_cols columns at pitch a_pitch, B rows of b_cols at pitch b_pitch, c_max
@@ -1407,7 +1462,8 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
                              const int32_t *c_dev, const void *w1, const void *b1, const void *w3,
                              const void *w2, moe_act act, int e, int64_t c_max, int m, int h,
                              const void *d_out, void *ws, void *d_buf, void *d_w1, void *d_w3,
-                             void *d_w2, void *d_b1, void *d_b2, int32_t *st, cudaStream_t stream) {
+                             void *d_w2, void *d_b1, void *d_b2, int32_t *st, cudaStream_t stream,
+                             const void *pre) {
     using bf = __nv_bfloat16;
     const bool swiglu = act == MOE_ACT_SWIGLU;
     const BwdLayout L = bwd_layout(act, e, c_max, m, h);
@@ -1436,12 +1492,17 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
     // d_hid; then d_pre (ReLU / GELU: the pre-activation recomputed and
     // differentiated in one product; SwiGLU: a and b recomputed, then the
     // activation backward); then d_buf
-    MOE_TRY(gemm_bias_bmn(d_out, w2, dh, counts, c_dev, e, c_max, m, h, st, stream));
-    if (swiglu) {
+    if (pre) {
+        // the forward's saved pre-activation: one product, d_hid never stored
+        if (swiglu) return MOE_ERR_UNSUPPORTED;
+        MOE_TRY(gemm_dact_bmn(d_out, w2, pre, act, dpre, counts, c_dev, e, c_max, m, h, st, stream));
+    } else if (swiglu) {
+        MOE_TRY(gemm_bias_bmn(d_out, w2, dh, counts, c_dev, e, c_max, m, h, st, stream));
         MOE_TRY(gemm_bias(buf, w1, h, pa, nullptr, counts, c_dev, e, c_max, m, h, st, stream));
         MOE_TRY(gemm_bias(buf, w3, h, pb, nullptr, counts, c_dev, e, c_max, m, h, st, stream));
         MOE_TRY(act_bwd_launch(pa, pb, dh, act, e, c_max, h, counts, c_dev, dpre, st, stream));
     } else {
+        MOE_TRY(gemm_bias_bmn(d_out, w2, dh, counts, c_dev, e, c_max, m, h, st, stream));
         MOE_TRY(gemm_dact(buf, w1, b1, dh, act, dpre, counts, c_dev, e, c_max, m, h, st, stream));
     }
     if (swiglu)
@@ -1451,10 +1512,14 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
     // weight gradients: the kept rows are the contraction, each expert over
     // its own; both operands are read MN-major in place, the partly kept last
     // 64-row block of each expert from a zero-padded copy
-    MOE_TRY(tail_rows_launch((const bf *)d_out, m, c_max, m, e, counts, c_dev, tDo, st, stream));
-    MOE_TRY(tail_rows_launch((const bf *)hid, h, c_max, h, e, counts, c_dev, tHid, st, stream));
-    MOE_TRY(tail_rows_launch(dpre, H2, c_max, (int)H2, e, counts, c_dev, tDp, st, stream));
-    MOE_TRY(tail_rows_launch((const bf *)buf, m, c_max, m, e, counts, c_dev, tBuf, st, stream));
+    {
+        TailOps tails{};
+        tails.op[0] = TailOp{(const bf *)d_out, m, m, tDo};
+        tails.op[1] = TailOp{(const bf *)hid, h, h, tHid};
+        tails.op[2] = TailOp{dpre, H2, (int)H2, tDp};
+        tails.op[3] = TailOp{(const bf *)buf, m, m, tBuf};
+        MOE_TRY(tail_rows_launch(tails, 4, c_max, e, counts, c_dev, st, stream));
+    }
     MOE_TRY(gemm_wgrad_mn(d_out, m, m, tDo, m, hid, h, h, tHid, h, d_w2, counts, c_dev, e, c_max, st,
                           stream));
     MOE_TRY(gemm_wgrad_mn(dpre, H2, h, tDp, H2, buf, m, m, tBuf, m, d_w1, counts, c_dev, e, c_max,
@@ -1462,10 +1527,13 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
     if (swiglu)
         MOE_TRY(gemm_wgrad_mn(dpre + h, H2, h, tDp + h, H2, buf, m, m, tBuf, m, d_w3, counts, c_dev,
                               e, c_max, st, stream));
-    // bias gradients (ReLU / GELU experts)
-    if (!swiglu && d_b1)
+    // bias gradients (ReLU / GELU experts), both in one launch
+    if (!swiglu && d_b1 && d_b2)
+        MOE_TRY(colsum_launch(dpre, e, c_max, h, h, counts, c_dev, (bf *)d_b1, st, stream,
+                              (const bf *)d_out, m, m, (bf *)d_b2));
+    else if (!swiglu && d_b1)
         MOE_TRY(colsum_launch(dpre, e, c_max, h, h, counts, c_dev, (bf *)d_b1, st, stream));
-    if (!swiglu && d_b2)
+    else if (!swiglu && d_b2)
         MOE_TRY(colsum_launch((const bf *)d_out, e, c_max, m, m, counts, c_dev, (bf *)d_b2, st,
                               stream));
 #undef MOE_TRY

@@ -191,6 +191,20 @@ moe_status moe_expert_ffn(const void *buf, moe_dtype dt, const int32_t *counts,
                           int32_t *dev_status, void *stream);
 
 /*
+ * moe_expert_ffn for training (bf16, ReLU / GELU): the same outputs, and fc1
+ * also stores its pre-activation buf W1^T + b1 (fp32 sum rounded once to
+ * bf16) to pre [e, c_max, h] for the kept rows (other rows not written), so
+ * that moe_expert_ffn_bwd_saved need not recompute it.  Errors: as
+ * moe_expert_ffn; MOE_ERR_INVALID_ARG for a NULL or misaligned pre;
+ * MOE_ERR_UNSUPPORTED for fp32 or SwiGLU.
+ */
+moe_status moe_expert_ffn_train(const void *buf, moe_dtype dt, const int32_t *counts,
+                                const int32_t *c_dev, const void *w1, const void *b1,
+                                const void *w2, const void *b2, moe_act act, int e, int64_t c_max,
+                                int m, int h, void *workspace, size_t workspace_bytes, void *out,
+                                void *pre, int32_t *dev_status, void *stream);
+
+/*
  * Fast decode ([Blog] 3.5, K0 forward; [PR8195] change 3, fp32 combine).
  *   y[t, :] = sum over kept routes r of gates[r,t] * out[idx[r,t], loc[r,t], :],
  *   accumulated in fp32 with fused multiply-add in ascending r from +0 and
@@ -246,8 +260,10 @@ size_t moe_expert_ffn_bwd_workspace_size(moe_dtype dt, moe_act act, int e, int64
  * d_b2 [e, m].  d_w3 is SwiGLU's only, which takes no biases; d_b1 / d_b2 may
  * be NULL.  workspace: moe_expert_ffn_bwd_workspace_size() bytes, scratch.
  * bf16 only (MOE_ERR_UNSUPPORTED for fp32): every product is the forward's
- * tensor-core grouped GEMM (fp32 accumulation in TMEM); pre-activations and
- * intermediate gradients are rounded to bf16 between the products.
+ * tensor-core grouped GEMM (fp32 accumulation in TMEM); d_hid and d_pre (and
+ * SwiGLU's recomputed a and b) are rounded to bf16 between the products, the
+ * ReLU / GELU pre-activation is recomputed in fp32 inside the product that
+ * forms d_pre.
  */
 moe_status moe_expert_ffn_bwd(const void *buf, const void *hid, moe_dtype dt,
                               const int32_t *counts, const int32_t *c_dev, const void *w1,
@@ -256,6 +272,23 @@ moe_status moe_expert_ffn_bwd(const void *buf, const void *hid, moe_dtype dt,
                               size_t workspace_bytes, void *d_buf, void *d_w1, void *d_w3,
                               void *d_w2, void *d_b1, void *d_b2, int32_t *dev_status,
                               void *stream);
+
+/*
+ * moe_expert_ffn_bwd with the pre-activation moe_expert_ffn_train saved
+ * (ReLU / GELU): d_pre = (d_out W2) * act'(pre) is formed in one product's
+ * epilogue (d_hid is neither rounded nor stored, and nothing is recomputed);
+ * the other outputs as moe_expert_ffn_bwd.  pre [e, c_max, h] in `dt`;
+ * workspace: moe_expert_ffn_bwd_workspace_size() bytes.  Errors: as
+ * moe_expert_ffn_bwd; MOE_ERR_INVALID_ARG for a NULL or misaligned pre or
+ * for SwiGLU.
+ */
+moe_status moe_expert_ffn_bwd_saved(const void *buf, const void *hid, const void *pre,
+                                    moe_dtype dt, const int32_t *counts, const int32_t *c_dev,
+                                    const void *w1, const void *w2, moe_act act, int e,
+                                    int64_t c_max, int m, int h, const void *d_out,
+                                    void *workspace, size_t workspace_bytes, void *d_buf,
+                                    void *d_w1, void *d_w2, void *d_b1, void *d_b2,
+                                    int32_t *dev_status, void *stream);
 
 /*
  * Gate backward ([Tutel] gate_type 'top': the gates are softmax probabilities

@@ -60,8 +60,14 @@ def _f64(a):
     return oracle.to_f32(a).astype(np.float64)
 
 
+@pytest.mark.parametrize("saved", [False, True], ids=["recompute", "saved_pre"])
 @pytest.mark.parametrize("w", CASES, ids=lambda w: f"e{w.e}_m{w.m}_h{w.h}_{w.act}")
-def test_expert_ffn_bwd_matches_oracle(w):
+def test_expert_ffn_bwd_matches_oracle(w, saved):
+    """saved: the forward is moe_expert_ffn_train (its out and hidden must be
+    the plain forward's bit for bit, its pre-activation within one bf16
+    rounding of the fp64 one) and the backward moe_expert_ffn_bwd_saved."""
+    if saved and w.act == "swiglu":
+        pytest.skip("the saved pre-activation is ReLU / GELU only")
     inp = synth.make_inputs_host(w)
     # routing and the encoded buffer (the forward's expert rows are not needed)
     ref = oracle.layer_forward(w, inp, rows=(np.zeros(1, np.int32), np.zeros(1, np.int64)))
@@ -73,11 +79,11 @@ def test_expert_ffn_bwd_matches_oracle(w):
     for j in range(e):
         buf_h[j, :kept[j]] = ref["buf"][j, :kept[j]]
     d_out_h = synth.bf16_bits_to_f32(synth.normal_host(5, "d_out", (e, c_max, m), 1.0, "bf16"))
-    _check_bwd(w, inp, buf_h, d_out_h, ref["needed"], kept, c, c_max)
+    _check_bwd(w, inp, buf_h, d_out_h, ref["needed"], kept, c, c_max, saved)
 
 
-@pytest.mark.parametrize("act", ["gelu", "swiglu"])
-def test_expert_ffn_bwd_block_edges(act):
+@pytest.mark.parametrize("act,saved", [("gelu", False), ("swiglu", False), ("relu", True)])
+def test_expert_ffn_bwd_block_edges(act, saved):
     """Kept rows chosen at the weight gradients' 64-row block edges: exactly
     one block, none, a block plus a few rows, a single row, and a count above
     c (kept = c = 200, past three full blocks), with large values in every row
@@ -93,10 +99,10 @@ def test_expert_ffn_bwd_block_edges(act):
     d_out_h = synth.bf16_bits_to_f32(synth.normal_host(9, "d_out_e", (e, c_max, m), 1.0, "bf16"))
     for j in range(e):
         buf_h[j, kept[j]:] = stale[j, kept[j]:]
-    _check_bwd(w, inp, buf_h, d_out_h, needed, kept, c, c_max)
+    _check_bwd(w, inp, buf_h, d_out_h, needed, kept, c, c_max, saved)
 
 
-def _check_bwd(w, inp, buf_h, d_out_h, needed, kept, c, c_max):
+def _check_bwd(w, inp, buf_h, d_out_h, needed, kept, c, c_max, saved=False):
     e, m, h = w.e, w.m, w.h
     swiglu = w.act == "swiglu"
     bf = torch.bfloat16
@@ -112,6 +118,24 @@ def _check_bwd(w, inp, buf_h, d_out_h, needed, kept, c, c_max):
     out = torch.empty((e, c_max, m), dtype=bf, device="cuda")
     M.moe_expert_ffn(buf, counts, c_dev, w1, b1, w3, w2, b2, w.act, ws_f, out, st)
     hid = ws_f[: e * c_max * h * 2].view(bf).view(e, c_max, h)
+    if saved:
+        ws_t = torch.empty_like(ws_f)
+        out_t = torch.empty_like(out)
+        pre = torch.empty((e, c_max, h), dtype=bf, device="cuda")
+        M.moe_expert_ffn_train(buf, counts, c_dev, w1, b1, w2, b2, w.act, ws_t, out_t, pre, st)
+        torch.cuda.synchronize()
+        hid_t = ws_t[: e * c_max * h * 2].view(bf).view(e, c_max, h)
+        for j in range(e):
+            r = int(kept[j])
+            assert torch.equal(out_t[j, :r].view(torch.int16), out[j, :r].view(torch.int16)), j
+            assert torch.equal(hid_t[j, :r].view(torch.int16), hid[j, :r].view(torch.int16)), j
+            x = buf_h[j, :r].astype(np.float64)
+            pre64 = x @ _f64(inp["w1"])[j].T + (_f64(inp["b1"])[j] if inp["b1"] is not None else 0.0)
+            got = to_host(pre[j, :r]).astype(np.float64)
+            # one bf16 rounding of the fp32-accumulated sum
+            tol = 2.0 ** -8 * np.abs(pre64) + 2 * m * 2.0 ** -24 * (np.abs(x) @ np.abs(_f64(inp["w1"])[j].T)) + 1e-6
+            assert np.all(np.abs(got - pre64) <= tol), j
+        hid = hid_t
     ws = torch.empty(M.moe_expert_ffn_bwd_workspace_size(M.MOE_BF16, w.act, e, c_max, m, h),
                      dtype=torch.uint8, device="cuda")
     d_buf = torch.full((e, c_max, m), 3.0, dtype=bf, device="cuda")
@@ -120,8 +144,12 @@ def _check_bwd(w, inp, buf_h, d_out_h, needed, kept, c, c_max):
     d_w2 = torch.empty((e, m, h), dtype=bf, device="cuda")
     d_b1 = None if swiglu else torch.empty((e, h), dtype=bf, device="cuda")
     d_b2 = None if swiglu else torch.empty((e, m), dtype=bf, device="cuda")
-    M.moe_expert_ffn_bwd(buf, hid, counts, c_dev, w1, b1, w3, w2, w.act, to_dev(d_out_h).to(bf), ws,
-                         d_buf, d_w1, d_w3, d_w2, d_b1, d_b2, st)
+    if saved:
+        M.moe_expert_ffn_bwd_saved(buf, hid, pre, counts, c_dev, w1, w2, w.act,
+                                   to_dev(d_out_h).to(bf), ws, d_buf, d_w1, d_w2, d_b1, d_b2, st)
+    else:
+        M.moe_expert_ffn_bwd(buf, hid, counts, c_dev, w1, b1, w3, w2, w.act, to_dev(d_out_h).to(bf),
+                             ws, d_buf, d_w1, d_w3, d_w2, d_b1, d_b2, st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
 
