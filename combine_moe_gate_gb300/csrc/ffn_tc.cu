@@ -584,7 +584,8 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     constexpr bool GELU = EPI == EPI_GELU || EPI == EPI_GELU_SAVE;
     constexpr bool RELU = EPI == EPI_RELU || EPI == EPI_RELU_SAVE;
     constexpr bool BMN = EPI == EPI_BIAS_BMN || AMN || DACTP;   // B MN-major: [K, N] rows, 64-column boxes
-    static_assert(!BMN || (CL == 2 && TN == 2 && BK == 64), "MN-major B on 256 x 512 pair tiles");
+    static_assert(!BMN || (CL == 2 && BK == 64 && (TN == 2 || !AMN)),
+                  "MN-major B on pair tiles (MN-major A on 256 x 512 ones)");
     constexpr bool PAIR = TL::PAIR;
     constexpr int STAGES = TL::STAGES, BMT = TL::BMT, A_BYTES = TL::A_BYTES;
     constexpr int B_BYTES = TL::B_BYTES, ROWB = TL::ROWB;
@@ -736,9 +737,9 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                             if (prank == 0) mbar_expect_tx(&ctl->full[stage], 2 * B_BOX_BYTES);
                             const int n_col = b_row - T.j * args.b_rows;
 #pragma unroll
-                            for (int i = 0; i < 2; i++)
+                            for (int i = 0; i < TN; i++)   // TN boxes of 64 columns
                                 tma_load_2d_pair(sB + stage * B_BYTES + hh * B_BOX_BYTES +
-                                                     i * (B_BOX_BYTES / 2),
+                                                     i * (B_BOX_BYTES / TN),
                                                  tail ? &tmBt : &tmB, n_col + 64 * i, k_row, fb);
                         }
                     } else if (ok && PAIR) {
@@ -753,9 +754,9 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                             if (prank == 0) mbar_expect_tx(&ctl->full[stage], 2 * B_BOX_BYTES);
                             const int n_col = b_row - T.j * args.b_rows;
 #pragma unroll
-                            for (int i = 0; i < 2; i++)
+                            for (int i = 0; i < TN; i++)   // TN boxes of 64 columns
                                 tma_load_2d_pair(sB + stage * B_BYTES + hh * B_BOX_BYTES +
-                                                     i * (B_BOX_BYTES / 2),
+                                                     i * (B_BOX_BYTES / TN),
                                                  &tmB, n_col + 64 * i, k_row, fb);
                         } else {
                             // SwiGLU: the first CTA's half of B is W1, the second's W3
@@ -1418,7 +1419,10 @@ moe_status gemm_dact(const void *buf, const void *w1, const void *b1, const void
 moe_status gemm_dact_bmn(const void *d_out, const void *w2, const void *pre, moe_act act, void *d_pre,
                          const int32_t *counts, const int32_t *c_dev, int e, int64_t c_max, int m,
                          int h, int32_t *st, cudaStream_t stream) {
-    using T2 = Tiling<1, 64, 2, 2>;
+    // 256 x 256 pair tiles with two accumulators: the derivative epilogue
+    // (a load of the pre-activation and the GELU derivative per element)
+    // overlaps the next tile's main loop
+    using T2 = Tiling<1, 64, 2, 1>;
     CUtensorMap mA, mB, mO;
     if (!make_map(&mA, d_out, (uint64_t)e * c_max, (uint64_t)m, T2::A_BOX_ROWS, 64) ||
         !make_map(&mB, w2, (uint64_t)e * m, (uint64_t)h, 64, 64) ||
@@ -1426,8 +1430,8 @@ moe_status gemm_dact_bmn(const void *d_out, const void *w2, const void *pre, moe
         return MOE_ERR_CUDA;
     GemmArgs g{counts, c_dev, st, nullptr, (__nv_bfloat16 *)d_pre, c_max, e, m, h, m, nullptr,
                nullptr, 0, 0, nullptr, nullptr, (const __nv_bfloat16 *)pre};
-    return act == MOE_ACT_GELU ? launch_gemm<EPI_DGELU_BMN, 1, 64, 2, 2>(mA, mB, mB, mO, g, stream)
-                               : launch_gemm<EPI_DRELU_BMN, 1, 64, 2, 2>(mA, mB, mB, mO, g, stream);
+    return act == MOE_ACT_GELU ? launch_gemm<EPI_DGELU_BMN, 1, 64, 2, 1>(mA, mB, mB, mO, g, stream)
+                               : launch_gemm<EPI_DRELU_BMN, 1, 64, 2, 1>(mA, mB, mB, mO, g, stream);
 }
 
 // Weight gradients out[j] = A[j]^T B[j] over the first min(counts[j], *c_dev,
