@@ -584,8 +584,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     constexpr bool GELU = EPI == EPI_GELU || EPI == EPI_GELU_SAVE;
     constexpr bool RELU = EPI == EPI_RELU || EPI == EPI_RELU_SAVE;
     constexpr bool BMN = EPI == EPI_BIAS_BMN || AMN || DACTP;   // B MN-major: [K, N] rows, 64-column boxes
-    static_assert(!BMN || (CL == 2 && BK == 64 && (TN == 2 || !AMN)),
-                  "MN-major B on pair tiles (MN-major A on 256 x 512 ones)");
+    static_assert(!BMN || (CL == 2 && BK == 64), "MN-major operands on pair tiles");
     constexpr bool PAIR = TL::PAIR;
     constexpr int STAGES = TL::STAGES, BMT = TL::BMT, A_BYTES = TL::A_BYTES;
     constexpr int B_BYTES = TL::B_BYTES, ROWB = TL::ROWB;
@@ -1318,8 +1317,11 @@ moe_status ffn_tc_fp8_launch(const void *buf_q, const float *buf_scale, const in
 namespace moe {
 
 // ---------------------------------------------------------------- backward
-// The expert-FFN backward as products on the 256 x 512 pair tiling, with the
-// SIMT activation derivative, tail copies and bias sums in between:
+// The expert-FFN backward as products on 256 x 256 pair tiles with two
+// accumulators (each tile's epilogue overlaps the next tile's main loop, and
+// a backward product has twice the tiles of a 256 x 512 tiling, so its last
+// wave over the SM pairs is less empty), with the SIMT tail copies, bias sums
+// and (SwiGLU) activation derivative in between:
 //   d_hid = d_out w2                  (B = w2 read MN-major in place);
 //   d_pre = d_hid * act'(buf w1^T + b1), the pre-activation recomputed in
 //                                      the product's epilogue (SwiGLU: a =
@@ -1368,7 +1370,7 @@ BwdLayout bwd_layout(moe_act act, int e, int64_t c_max, int m, int h) {
 moe_status gemm_bias(const void *a, const void *b, int b_rows, void *out, const void *bias,
                      const int32_t *counts, const int32_t *c_dev, int e, int64_t c_max, int K,
                      int n_out, int32_t *st, cudaStream_t stream) {
-    using T2 = Tiling<1, 64, 2, 2>;
+    using T2 = Tiling<1, 64, 2, 1>;
     CUtensorMap mA, mB, mO;
     if (!make_map(&mA, a, (uint64_t)e * c_max, (uint64_t)K, T2::A_BOX_ROWS, 64) ||
         !make_map(&mB, b, (uint64_t)e * b_rows, (uint64_t)K, T2::B_BOX_ROWS, 64) ||
@@ -1376,7 +1378,7 @@ moe_status gemm_bias(const void *a, const void *b, int b_rows, void *out, const 
         return MOE_ERR_CUDA;
     GemmArgs g{counts, c_dev, st, (const __nv_bfloat16 *)bias, (__nv_bfloat16 *)out, c_max, e, K,
                n_out, b_rows, nullptr, nullptr, 0, 0};
-    return launch_gemm<EPI_BIAS, 1, 64, 2, 2>(mA, mB, mB, mO, g, stream);
+    return launch_gemm<EPI_BIAS, 1, 64, 2, 1>(mA, mB, mB, mO, g, stream);
 }
 
 // The same with B MN-major: out[j] = A[j] B[j] with B [e * K, n_out] row-major
@@ -1384,7 +1386,7 @@ moe_status gemm_bias(const void *a, const void *b, int b_rows, void *out, const 
 moe_status gemm_bias_bmn(const void *a, const void *b, void *out, const int32_t *counts,
                          const int32_t *c_dev, int e, int64_t c_max, int K, int n_out, int32_t *st,
                          cudaStream_t stream) {
-    using T2 = Tiling<1, 64, 2, 2>;
+    using T2 = Tiling<1, 64, 2, 1>;
     CUtensorMap mA, mB, mO;
     if (!make_map(&mA, a, (uint64_t)e * c_max, (uint64_t)K, T2::A_BOX_ROWS, 64) ||
         !make_map(&mB, b, (uint64_t)e * K, (uint64_t)n_out, 64, 64) ||
@@ -1392,7 +1394,7 @@ moe_status gemm_bias_bmn(const void *a, const void *b, void *out, const int32_t 
         return MOE_ERR_CUDA;
     GemmArgs g{counts, c_dev, st, nullptr, (__nv_bfloat16 *)out, c_max, e, K, n_out, K, nullptr,
                nullptr, 0, 0};
-    return launch_gemm<EPI_BIAS_BMN, 1, 64, 2, 2>(mA, mB, mB, mO, g, stream);
+    return launch_gemm<EPI_BIAS_BMN, 1, 64, 2, 1>(mA, mB, mB, mO, g, stream);
 }
 
 // d_pre = d_hid * act'(buf w1^T + b1) over the kept rows (ReLU / GELU): the
@@ -1453,7 +1455,7 @@ moe_status gemm_wgrad_mn(const void *a, int64_t a_pitch, int a_cols, const void 
         return MOE_ERR_CUDA;
     GemmArgs g{nullptr, nullptr, st, nullptr, (__nv_bfloat16 *)out, a_cols, e, (int)c_max, b_cols,
                (int)c_max, counts, c_dev, 0, 0};
-    return launch_gemm<EPI_WGRAD_MN, 1, 64, 2, 2>(mA, mB, mB, mO, g, stream, &mAt, &mBt);
+    return launch_gemm<EPI_WGRAD_MN, 1, 64, 2, 1>(mA, mB, mB, mO, g, stream, &mAt, &mBt);
 }
 
 }  // namespace
