@@ -33,6 +33,11 @@ GATE_CASES = [
     # several 512-byte feature slices with a ragged last one (lane-blocked order)
     _w(s=150, m=520, e=7, k=2, h=64, dtype="f32"),
     _w(s=100, m=1032, e=32, k=4, h=64, skew_alpha=0.5),
+    # e <= 32 batches large enough for the resident kernel's 64 / e tokens per
+    # warp group (smaller ones take 32 / e: twice the groups)
+    _w(s=16400, m=64, e=16, k=2, h=64),
+    _w(s=12000, m=72, e=32, k=4, h=64, skew_alpha=0.5),
+    _w(s=20000, m=48, e=8, k=2, h=64),
 ]
 
 
