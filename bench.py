@@ -584,6 +584,14 @@ class LayerRun:
                 M.moe_expert_ffn_bwd_saved(b.buf, hid, pre, b.counts, b.c_dev, w1, w2, w.act, d_out,
                                            ws, d_buf, d_w1, d_w2, d_b1, d_b2, b.status)
 
+        # the same with the weight and bias gradients kept in fp32
+        g32 = None if pre is None else [torch.empty(t.shape, device=dev, dtype=torch.float32)
+                                        if t is not None else None for t in (d_w1, d_w2, d_b1, d_b2)]
+
+        def ffn_f32():
+            M.moe_expert_ffn_bwd_saved(b.buf, hid, pre, b.counts, b.c_dev, w1, w2, w.act, d_out, ws,
+                                       d_buf, *g32, b.status)
+
         def enc():
             M.moe_encode_bwd(d_buf, b.idx, b.loc, b.c_dev, dx, b.status)
 
@@ -607,6 +615,7 @@ class LayerRun:
             res[name] = self.time_calls(fn, steps, warmup)
         if pre is not None:
             res["ffn_bwd_recompute"] = self.time_calls(ffn_recompute, steps, warmup)
+            res["ffn_bwd_fp32_wgrad"] = self.time_calls(ffn_f32, steps, warmup)
         res["fwd_bwd_step"] = self.time_calls(chain, steps, warmup)
         self.check_status()
         return res
@@ -656,12 +665,14 @@ def graded_report(name, run, stage_ms, pk, extra=None):
     if extra:
         saved = "ffn_bwd_recompute" in extra
         for n, ms in extra.items():
-            base = "ffn_bwd" if n == "ffn_bwd_recompute" else n
+            base = "ffn_bwd" if n.startswith("ffn_bwd") else n
             if base in work:
                 note = "backward, timed alone"
                 if base == "ffn_bwd" and saved:
-                    note += ("; recomputes the pre-activation" if n != base else
-                             "; reads the pre-activation the training forward kept")
+                    note += {"ffn_bwd_recompute": "; recomputes the pre-activation",
+                             "ffn_bwd_fp32_wgrad": "; reads the kept pre-activation, weight and bias "
+                                                   "gradients stored in fp32"}.get(
+                        n, "; reads the pre-activation the training forward kept")
                 d["stages"][n] = dict(rate(base, ms, work[base], pk), note=note)
             else:
                 d["stages"][n] = {"ms": ms, "tokens_per_s": w.s / (ms * 1e-3),

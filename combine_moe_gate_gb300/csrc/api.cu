@@ -67,7 +67,7 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
                              const void *w2, moe_act act, int e, int64_t c_max, int m, int h,
                              const void *d_out, void *ws, void *d_buf, void *d_w1, void *d_w3,
                              void *d_w2, void *d_b1, void *d_b2, int32_t *st, cudaStream_t stream,
-                             const void *pre = nullptr);
+                             const void *pre = nullptr, bool wgrad_f32 = false);
 moe_status ffn_simt_launch(const void *buf, moe_dtype dt, const int32_t *counts,
                            const int32_t *c_dev, const void *w1, const void *b1, const void *w3,
                            const void *w2, const void *b2, moe_act act, int e, int64_t c_max,
@@ -293,9 +293,10 @@ static moe_status expert_ffn_bwd(const void *buf, const void *hid, const void *p
                                  const int32_t *counts, const int32_t *c_dev, const void *w1,
                                  const void *b1, const void *w3, const void *w2, moe_act act, int e,
                                  int64_t c_max, int m, int h, const void *d_out, void *workspace,
-                                 size_t workspace_bytes, void *d_buf, void *d_w1, void *d_w3,
-                                 void *d_w2, void *d_b1, void *d_b2, int32_t *dev_status,
-                                 void *stream) {
+                                 size_t workspace_bytes, void *d_buf, moe_dtype wgrad_dt,
+                                 void *d_w1, void *d_w3, void *d_w2, void *d_b1, void *d_b2,
+                                 int32_t *dev_status, void *stream) {
+    if (wgrad_dt != MOE_BF16 && wgrad_dt != MOE_F32) return MOE_ERR_INVALID_ARG;
     if (!rows_ok(dt, m) || !rows_ok(dt, h) || e < 1 || e > kMaxE || c_max < 1 ||
         c_max > 0x7fffffff || !ok16(buf) || !ok16(hid) || !ok4(counts) || !ok4(c_dev) ||
         !ok16(w1) || !ok16(w2) || !opt16(b1) || !ok16(d_out) || !ok16(workspace) ||
@@ -318,7 +319,7 @@ static moe_status expert_ffn_bwd(const void *buf, const void *hid, const void *p
     if (pre && (act == MOE_ACT_SWIGLU || !ok16(pre))) return MOE_ERR_INVALID_ARG;
     return ffn_tc_bwd_launch(buf, hid, counts, c_dev, w1, b1, w3, w2, act, e, c_max, m, h, d_out,
                              workspace, d_buf, d_w1, d_w3, d_w2, d_b1, d_b2, dev_status,
-                             as_stream(stream), pre);
+                             as_stream(stream), pre, wgrad_dt == MOE_F32);
 }
 
 moe_status moe_expert_ffn_bwd(const void *buf, const void *hid, moe_dtype dt,
@@ -329,7 +330,7 @@ moe_status moe_expert_ffn_bwd(const void *buf, const void *hid, moe_dtype dt,
                               void *d_w2, void *d_b1, void *d_b2, int32_t *dev_status,
                               void *stream) {
     return expert_ffn_bwd(buf, hid, nullptr, dt, counts, c_dev, w1, b1, w3, w2, act, e, c_max, m, h,
-                          d_out, workspace, workspace_bytes, d_buf, d_w1, d_w3, d_w2, d_b1, d_b2,
+                          d_out, workspace, workspace_bytes, d_buf, dt, d_w1, d_w3, d_w2, d_b1, d_b2,
                           dev_status, stream);
 }
 
@@ -338,12 +339,12 @@ moe_status moe_expert_ffn_bwd_saved(const void *buf, const void *hid, const void
                                     const void *w1, const void *w2, moe_act act, int e,
                                     int64_t c_max, int m, int h, const void *d_out,
                                     void *workspace, size_t workspace_bytes, void *d_buf,
-                                    void *d_w1, void *d_w2, void *d_b1, void *d_b2,
-                                    int32_t *dev_status, void *stream) {
+                                    moe_dtype wgrad_dt, void *d_w1, void *d_w2, void *d_b1,
+                                    void *d_b2, int32_t *dev_status, void *stream) {
     if (!pre) return MOE_ERR_INVALID_ARG;
     return expert_ffn_bwd(buf, hid, pre, dt, counts, c_dev, w1, nullptr, nullptr, w2, act, e, c_max,
-                          m, h, d_out, workspace, workspace_bytes, d_buf, d_w1, nullptr, d_w2, d_b1,
-                          d_b2, dev_status, stream);
+                          m, h, d_out, workspace, workspace_bytes, d_buf, wgrad_dt, d_w1, nullptr,
+                          d_w2, d_b1, d_b2, dev_status, stream);
 }
 
 size_t moe_layer_workspace_size(moe_dtype dt, moe_act act, int64_t s, int m, int e, int k,

@@ -204,7 +204,7 @@ struct ColsumOp {
     const __nv_bfloat16 *src;
     int cols;
     int64_t pitch;
-    __nv_bfloat16 *out;
+    void *out;   // bf16, or fp32 when the launch says so
 };
 struct ColsumOps {
     ColsumOp op[2];
@@ -213,7 +213,7 @@ static_assert(CS_COLS == 32 * 8 && CS_WARPS * 32 >= CS_COLS, "8 columns a lane, 
 
 __global__ void __launch_bounds__(CS_WARPS * 32)
 colsum_kernel(ColsumOps ops, int64_t c_max, const int32_t *__restrict__ counts,
-              const int32_t *__restrict__ c_dev, int32_t *status) {
+              const int32_t *__restrict__ c_dev, int out_f32, int32_t *status) {
     pdl_enter();
     if (status_bad(status)) return;
     __shared__ float part[CS_WARPS][CS_COLS];
@@ -260,7 +260,8 @@ colsum_kernel(ColsumOps ops, int64_t c_max, const int32_t *__restrict__ counts,
         float sum = 0.0f;
 #pragma unroll
         for (int w = 0; w < CS_WARPS; w++) sum += part[w][threadIdx.x];
-        o.out[(int64_t)j * cols + col] = __float2bfloat16_rn(sum);
+        if (out_f32) static_cast<float *>(o.out)[(int64_t)j * cols + col] = sum;
+        else static_cast<__nv_bfloat16 *>(o.out)[(int64_t)j * cols + col] = __float2bfloat16_rn(sum);
     }
 }
 
@@ -348,9 +349,8 @@ moe_status tail_rows_launch(const TailOps &ops, int nops, int64_t c_max, int e,
 
 moe_status colsum_launch(const __nv_bfloat16 *src, int e, int64_t c_max, int cols,
                          int64_t src_pitch, const int32_t *counts, const int32_t *c_dev,
-                         __nv_bfloat16 *out, int32_t *status, cudaStream_t stream,
-                         const __nv_bfloat16 *src2, int cols2, int64_t src2_pitch,
-                         __nv_bfloat16 *out2) {
+                         void *out, int32_t *status, cudaStream_t stream, bool out_f32,
+                         const __nv_bfloat16 *src2, int cols2, int64_t src2_pitch, void *out2) {
     // rows of whole 16-byte chunks
     if (e < 1 || e > 65535 || cols < 1 || cols % 8 || src_pitch % 8 || !aligned16(src))
         return MOE_ERR_INVALID_ARG;
@@ -361,7 +361,7 @@ moe_status colsum_launch(const __nv_bfloat16 *src, int e, int64_t c_max, int col
     ops.op[1] = src2 ? ColsumOp{src2, cols2, src2_pitch, out2} : ColsumOp{src, 0, src_pitch, out};
     const int nb = (cols + CS_COLS - 1) / CS_COLS + (src2 ? (cols2 + CS_COLS - 1) / CS_COLS : 0);
     return launch_pdl(colsum_kernel, dim3((unsigned)nb, (unsigned)e), dim3(CS_WARPS * 32), 0, stream,
-                      ops, c_max, counts, c_dev, status);
+                      ops, c_max, counts, c_dev, out_f32 ? 1 : 0, status);
 }
 
 }  // namespace moe

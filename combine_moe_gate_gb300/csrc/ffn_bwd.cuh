@@ -30,12 +30,13 @@ moe_status act_bwd_launch(const __nv_bfloat16 *pa, const __nv_bfloat16 *pb,
 // out[b][c] = sum over the kept rows r of src[b][r][c] (fp32 sum in a fixed
 // order, one rounding to bf16); src rows of `cols` columns at row pitch
 // src_pitch, batch stride c_max * src_pitch.  With src2, the same for a
-// second matrix (cols2, src2_pitch, out2) in the same launch.
+// second matrix (cols2, src2_pitch, out2) in the same launch.  out_f32: the
+// sums are stored in fp32 (not rounded to bf16).
 moe_status colsum_launch(const __nv_bfloat16 *src, int e, int64_t c_max, int cols,
                          int64_t src_pitch, const int32_t *counts, const int32_t *c_dev,
-                         __nv_bfloat16 *out, int32_t *status, cudaStream_t stream,
+                         void *out, int32_t *status, cudaStream_t stream, bool out_f32 = false,
                          const __nv_bfloat16 *src2 = nullptr, int cols2 = 0,
-                         int64_t src2_pitch = 0, __nv_bfloat16 *out2 = nullptr);
+                         int64_t src2_pitch = 0, void *out2 = nullptr);
 
 // The partly kept last 64-row block of every expert, for the MN-major weight
 // gradients, for up to TAIL_MAX_OPS operands in one launch: with kept_b =

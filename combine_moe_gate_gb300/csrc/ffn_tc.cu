@@ -63,9 +63,10 @@ constexpr int SMEM_RING = 192 * 1024;   // operand ring per CTA
 // acc + bias (bf16) to GemmArgs::aux_out, laid out like out.
 // EPI_DGELU_BMN / EPI_DRELU_BMN: d_hid = acc (B MN-major) times act'(pre)
 // with the saved pre-activation (GemmArgs::aux) laid out like out.
+// EPI_WGRAD_MN_F32: EPI_WGRAD_MN writing fp32 to GemmArgs::out_f32.
 enum Epi { EPI_GELU = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_BIAS = 3, EPI_BIAS_BMN = 4,
            EPI_WGRAD_MN = 5, EPI_DGELU = 6, EPI_DRELU = 7, EPI_GELU_SAVE = 8, EPI_RELU_SAVE = 9,
-           EPI_DGELU_BMN = 10, EPI_DRELU_BMN = 11 };
+           EPI_DGELU_BMN = 10, EPI_DRELU_BMN = 11, EPI_WGRAD_MN_F32 = 12 };
 
 // Tile shape.  TM = 1: 128 x 256 tiles, two 256-column accumulators in TMEM so
 // the epilogue of one tile overlaps the main loop of the next.  TM = 2:
@@ -178,6 +179,8 @@ struct GemmArgs {
     const __nv_bfloat16 *aux;
     // EPI_GELU_SAVE / EPI_RELU_SAVE: where the pre-activation goes, likewise.
     __nv_bfloat16 *aux_out;
+    // EPI_WGRAD_MN_F32: the result in fp32 [e * c_max, n_out] (out unused).
+    float *out_f32;
     // Error-path test: the producers issue no copies, so the MMA issuer's
     // bounded wait on the first stage runs out (MOE_ERR_TIMEOUT).
     int32_t stall;
@@ -576,7 +579,8 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     static_assert(TN == 1 || EPI != EPI_SWIGLU, "SwiGLU tiles pair W1 and W3 in one N = 256 MMA");
     constexpr bool F8 = EB == 1;   // e4m3 operands (kind::f8f6f4), scaled epilogue
     static_assert(!F8 || (CL == 2 && EPI != EPI_SWIGLU && EPI != EPI_BIAS_BMN), "e4m3 pair tiles");
-    constexpr bool AMN = EPI == EPI_WGRAD_MN;   // A MN-major as well, tail blocks from tmAt / tmBt
+    constexpr bool F32OUT = EPI == EPI_WGRAD_MN_F32;   // fp32 result, stored from registers
+    constexpr bool AMN = EPI == EPI_WGRAD_MN || F32OUT;   // A MN-major as well, tail blocks from tmAt / tmBt
     constexpr bool DACT = EPI == EPI_DGELU || EPI == EPI_DRELU;   // activation backward epilogue
     constexpr bool DACTP = EPI == EPI_DGELU_BMN || EPI == EPI_DRELU_BMN;   // act' of a saved pre
     constexpr bool DGELU = EPI == EPI_DGELU || EPI == EPI_DGELU_BMN;
@@ -971,6 +975,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     for (int h2 = 0; h2 < 2; h2++) {
                         const int gcol = T.nt * NOUT_TILE + col0 + c0 + 32 * h2;
                         uint32_t pk[16];
+                        float of[32];   // weight gradients in fp32: this row's 32 columns
                         uint32_t dv[16];   // activation backward: this row's d_hid or pre, 32 columns
                         if (DACT || DACTP) {
 #pragma unroll
@@ -1020,7 +1025,12 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                                                                           z.y > 0.0f ? 1.0f : 0.0f);
                                     a = __fmul2_rn(g, da);
                                 }
-                                pk[q * 4 + i] = pack_bf16(a.x, a.y);
+                                if constexpr (F32OUT) {
+                                    of[q * 8 + 2 * i] = a.x;
+                                    of[q * 8 + 2 * i + 1] = a.y;
+                                } else {
+                                    pk[q * 4 + i] = pack_bf16(a.x, a.y);
+                                }
                             }
                             if (SAVE && valid && gcol + q * 8 < args.n_out) {
                                 // this lane's row of the pre-activation, 8 columns
@@ -1029,8 +1039,20 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                                 st_v16(prow + gcol + q * 8, o);
                             }
                         }
-                        epi_store32(&tmO, stg, pk, all_kept, valid, lane, grow0, gcol,
-                                    args.n_out, orow);
+                        if constexpr (F32OUT) {   // fp32 weight gradients: this lane's row, 128 bytes
+                            if (valid) {
+                                float *frow = args.out_f32 + (grow0 + lane) * (int64_t)args.n_out + gcol;
+#pragma unroll
+                                for (int q = 0; q < 8; q++)
+                                    if (gcol + 4 * q < args.n_out)
+                                        *reinterpret_cast<float4 *>(frow + 4 * q) =
+                                            make_float4(of[4 * q], of[4 * q + 1], of[4 * q + 2],
+                                                        of[4 * q + 3]);
+                            }
+                        } else {
+                            epi_store32(&tmO, stg, pk, all_kept, valid, lane, grow0, gcol,
+                                        args.n_out, orow);
+                        }
                     }
                 }
                 __syncwarp();   // slice reused for the next tile
@@ -1441,11 +1463,12 @@ moe_status gemm_dact_bmn(const void *d_out, const void *w2, const void *pre, moe
 // a_cols columns at pitch a_pitch, B rows of b_cols at pitch b_pitch, c_max
 // rows per expert; a_tail / b_tail [e, 64, *] (pitches a_tpitch / b_tpitch)
 // hold each expert's partly kept last 64-row block (tail_rows_launch);
-// out [e, a_cols, b_cols].
+// out [e, a_cols, b_cols], bf16, or fp32 when out_f32.
 moe_status gemm_wgrad_mn(const void *a, int64_t a_pitch, int a_cols, const void *a_tail,
                          int64_t a_tpitch, const void *b, int64_t b_pitch, int b_cols,
                          const void *b_tail, int64_t b_tpitch, void *out, const int32_t *counts,
-                         const int32_t *c_dev, int e, int64_t c_max, int32_t *st, cudaStream_t stream) {
+                         const int32_t *c_dev, int e, int64_t c_max, int32_t *st, cudaStream_t stream,
+                         bool out_f32 = false) {
     CUtensorMap mA, mAt, mB, mBt, mO;
     if (!make_map(&mA, a, (uint64_t)e * c_max, (uint64_t)a_cols, 64, 64, (uint64_t)a_pitch) ||
         !make_map(&mAt, a_tail, (uint64_t)e * 64, (uint64_t)a_cols, 64, 64, (uint64_t)a_tpitch) ||
@@ -1455,6 +1478,10 @@ moe_status gemm_wgrad_mn(const void *a, int64_t a_pitch, int a_cols, const void 
         return MOE_ERR_CUDA;
     GemmArgs g{nullptr, nullptr, st, nullptr, (__nv_bfloat16 *)out, a_cols, e, (int)c_max, b_cols,
                (int)c_max, counts, c_dev, 0, 0};
+    if (out_f32) {   // the output map is not used: the epilogue stores fp32 from registers
+        g.out_f32 = (float *)out;
+        return launch_gemm<EPI_WGRAD_MN_F32, 1, 64, 2, 1>(mA, mB, mB, mO, g, stream, &mAt, &mBt);
+    }
     return launch_gemm<EPI_WGRAD_MN, 1, 64, 2, 1>(mA, mB, mB, mO, g, stream, &mAt, &mBt);
 }
 
@@ -1469,7 +1496,7 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
                              const void *w2, moe_act act, int e, int64_t c_max, int m, int h,
                              const void *d_out, void *ws, void *d_buf, void *d_w1, void *d_w3,
                              void *d_w2, void *d_b1, void *d_b2, int32_t *st, cudaStream_t stream,
-                             const void *pre) {
+                             const void *pre, bool wgrad_f32) {
     using bf = __nv_bfloat16;
     const bool swiglu = act == MOE_ACT_SWIGLU;
     const BwdLayout L = bwd_layout(act, e, c_max, m, h);
@@ -1527,21 +1554,21 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
         MOE_TRY(tail_rows_launch(tails, 4, c_max, e, counts, c_dev, st, stream));
     }
     MOE_TRY(gemm_wgrad_mn(d_out, m, m, tDo, m, hid, h, h, tHid, h, d_w2, counts, c_dev, e, c_max, st,
-                          stream));
+                          stream, wgrad_f32));
     MOE_TRY(gemm_wgrad_mn(dpre, H2, h, tDp, H2, buf, m, m, tBuf, m, d_w1, counts, c_dev, e, c_max,
-                          st, stream));
+                          st, stream, wgrad_f32));
     if (swiglu)
         MOE_TRY(gemm_wgrad_mn(dpre + h, H2, h, tDp + h, H2, buf, m, m, tBuf, m, d_w3, counts, c_dev,
-                              e, c_max, st, stream));
+                              e, c_max, st, stream, wgrad_f32));
     // bias gradients (ReLU / GELU experts), both in one launch
     if (!swiglu && d_b1 && d_b2)
-        MOE_TRY(colsum_launch(dpre, e, c_max, h, h, counts, c_dev, (bf *)d_b1, st, stream,
-                              (const bf *)d_out, m, m, (bf *)d_b2));
+        MOE_TRY(colsum_launch(dpre, e, c_max, h, h, counts, c_dev, d_b1, st, stream, wgrad_f32,
+                              (const bf *)d_out, m, m, d_b2));
     else if (!swiglu && d_b1)
-        MOE_TRY(colsum_launch(dpre, e, c_max, h, h, counts, c_dev, (bf *)d_b1, st, stream));
+        MOE_TRY(colsum_launch(dpre, e, c_max, h, h, counts, c_dev, d_b1, st, stream, wgrad_f32));
     else if (!swiglu && d_b2)
-        MOE_TRY(colsum_launch((const bf *)d_out, e, c_max, m, m, counts, c_dev, (bf *)d_b2, st,
-                              stream));
+        MOE_TRY(colsum_launch((const bf *)d_out, e, c_max, m, m, counts, c_dev, d_b2, st, stream,
+                              wgrad_f32));
 #undef MOE_TRY
     return MOE_OK;
 }

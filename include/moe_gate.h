@@ -278,17 +278,20 @@ moe_status moe_expert_ffn_bwd(const void *buf, const void *hid, moe_dtype dt,
  * (ReLU / GELU): d_pre = (d_out W2) * act'(pre) is formed in one product's
  * epilogue (d_hid is neither rounded nor stored, and nothing is recomputed);
  * the other outputs as moe_expert_ffn_bwd.  pre [e, c_max, h] in `dt`;
+ * d_w1, d_w2, d_b1, d_b2 in `wgrad_dt`: MOE_BF16, or MOE_F32 for weight and
+ * bias gradients kept in fp32 (the products' fp32 sums stored unrounded, as
+ * an optimiser with fp32 master weights wants them); d_buf in `dt`.
  * workspace: moe_expert_ffn_bwd_workspace_size() bytes.  Errors: as
- * moe_expert_ffn_bwd; MOE_ERR_INVALID_ARG for a NULL or misaligned pre or
- * for SwiGLU.
+ * moe_expert_ffn_bwd; MOE_ERR_INVALID_ARG for a NULL or misaligned pre, for
+ * SwiGLU, or for another wgrad_dt.
  */
 moe_status moe_expert_ffn_bwd_saved(const void *buf, const void *hid, const void *pre,
                                     moe_dtype dt, const int32_t *counts, const int32_t *c_dev,
                                     const void *w1, const void *w2, moe_act act, int e,
                                     int64_t c_max, int m, int h, const void *d_out,
                                     void *workspace, size_t workspace_bytes, void *d_buf,
-                                    void *d_w1, void *d_w2, void *d_b1, void *d_b2,
-                                    int32_t *dev_status, void *stream);
+                                    moe_dtype wgrad_dt, void *d_w1, void *d_w2, void *d_b1,
+                                    void *d_b2, int32_t *dev_status, void *stream);
 
 /*
  * Gate backward ([Tutel] gate_type 'top': the gates are softmax probabilities

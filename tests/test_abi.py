@@ -184,10 +184,10 @@ def test_invalid_arguments_are_rejected_before_launch():
     assert fbc(a13=100) == INV                                   # h not a multiple of 8
     assert fbc(a1=odd) == INV and fbc(a17=odd) == INV            # misaligned hid / d_buf
     # the saved-pre backward: buf, hid, pre, dt, counts, c_dev, w1, w2, act, e, c_max, m, h, d_out,
-    # ws, ws_bytes, d_buf, d_w1, d_w2, d_b1, d_b2, status, stream
+    # ws, ws_bytes, d_buf, wgrad_dt, d_w1, d_w2, d_b1, d_b2, status, stream
     fs = lib.moe_expert_ffn_bwd_saved
-    sok = [A, B, A, M.MOE_BF16, A, A, A, B, 1, 4, 64, 64, 128, A, B, 1 << 40, A, B, A, None, None,
-           A, None]
+    sok = [A, B, A, M.MOE_BF16, A, A, A, B, 1, 4, 64, 64, 128, A, B, 1 << 40, A, M.MOE_F32, B, A,
+           None, None, A, None]
     def fsc(**kw):
         a = list(sok)
         for i, v in kw.items():
@@ -197,6 +197,8 @@ def test_invalid_arguments_are_rejected_before_launch():
     assert fsc(a8=2) == INV                                      # no SwiGLU
     assert fsc(a3=M.MOE_F32) == M.MOE_ERR_UNSUPPORTED
     assert fsc(a15=0) == INV                                     # workspace too small
+    assert fsc(a17=7) == INV                                     # weight gradients bf16 or fp32
+    assert fsc(a18=odd) == INV                                   # misaligned d_w1
     # the training forward: buf, dt, counts, c_dev, w1, b1, w2, b2, act, e, c_max, m, h, ws,
     # ws_bytes, out, pre, status, stream
     ft = lib.moe_expert_ffn_train

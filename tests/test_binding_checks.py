@@ -156,11 +156,12 @@ def test_well_formed_calls_pass_and_marshal_their_sizes(stub):
                            z(e, c_max, h, dtype=bf), st)
     M.moe_expert_ffn_bwd_saved(buf, z(e, c_max, h, dtype=bf), z(e, c_max, h, dtype=bf), counts, c_dev,
                                w1, w2, "relu", z(e, c_max, m, dtype=bf), ws, z(e, c_max, m, dtype=bf),
-                               z(e, h, m, dtype=bf), z(e, m, h, dtype=bf), None, None, st)
+                               z(e, h, m), z(e, m, h), z(e, h), z(e, m), st)
     c = stub.calls
     assert c["moe_expert_ffn_bwd"][10:14] == (e, c_max, m, h)
     assert c["moe_expert_ffn_train"][9:13] == (e, c_max, m, h)
     assert c["moe_expert_ffn_bwd_saved"][9:13] == (e, c_max, m, h)
+    assert c["moe_expert_ffn_bwd_saved"][17] == M.MOE_F32   # fp32 weight gradients
     assert c["moe_gate_topk"][4:8] == (s, m, e, k)
     assert c["moe_capacity_locations"][1:4] == (s, e, k)
     assert c["moe_capacity_locations_noalloc"][1:4] == (s, e, k)

@@ -60,12 +60,13 @@ def _f64(a):
     return oracle.to_f32(a).astype(np.float64)
 
 
-@pytest.mark.parametrize("saved", [False, True], ids=["recompute", "saved_pre"])
+@pytest.mark.parametrize("saved", [False, True, "f32"], ids=["recompute", "saved_pre", "saved_pre_f32"])
 @pytest.mark.parametrize("w", CASES, ids=lambda w: f"e{w.e}_m{w.m}_h{w.h}_{w.act}")
 def test_expert_ffn_bwd_matches_oracle(w, saved):
     """saved: the forward is moe_expert_ffn_train (its out and hidden must be
     the plain forward's bit for bit, its pre-activation within one bf16
-    rounding of the fp64 one) and the backward moe_expert_ffn_bwd_saved."""
+    rounding of the fp64 one) and the backward moe_expert_ffn_bwd_saved;
+    "f32": with the weight and bias gradients stored in fp32."""
     if saved and w.act == "swiglu":
         pytest.skip("the saved pre-activation is ReLU / GELU only")
     inp = synth.make_inputs_host(w)
@@ -139,11 +140,12 @@ def _check_bwd(w, inp, buf_h, d_out_h, needed, kept, c, c_max, saved=False):
     ws = torch.empty(M.moe_expert_ffn_bwd_workspace_size(M.MOE_BF16, w.act, e, c_max, m, h),
                      dtype=torch.uint8, device="cuda")
     d_buf = torch.full((e, c_max, m), 3.0, dtype=bf, device="cuda")
-    d_w1 = torch.empty((e, h, m), dtype=bf, device="cuda")
+    gdt = torch.float32 if saved == "f32" else bf   # weight and bias gradients
+    d_w1 = torch.empty((e, h, m), dtype=gdt, device="cuda")
     d_w3 = torch.empty((e, h, m), dtype=bf, device="cuda") if swiglu else None
-    d_w2 = torch.empty((e, m, h), dtype=bf, device="cuda")
-    d_b1 = None if swiglu else torch.empty((e, h), dtype=bf, device="cuda")
-    d_b2 = None if swiglu else torch.empty((e, m), dtype=bf, device="cuda")
+    d_w2 = torch.empty((e, m, h), dtype=gdt, device="cuda")
+    d_b1 = None if swiglu else torch.empty((e, h), dtype=gdt, device="cuda")
+    d_b2 = None if swiglu else torch.empty((e, m), dtype=gdt, device="cuda")
     if saved:
         M.moe_expert_ffn_bwd_saved(buf, hid, pre, counts, c_dev, w1, w2, w.act,
                                    to_dev(d_out_h).to(bf), ws, d_buf, d_w1, d_w2, d_b1, d_b2, st)
