@@ -329,6 +329,37 @@ __device__ __forceinline__ void epi_store32(const CUtensorMap *map, uint8_t *stg
     }
 }
 
+// The same for 16 fp32 columns (64-byte rows: the same staging pattern and
+// swizzle), with a 16 x 32 fp32 output map; the fallback stores this lane's
+// row directly.
+__device__ __forceinline__ void epi_store16f(const CUtensorMap *map, uint8_t *stg, const float *v,
+                                             bool all_kept, bool kept, int lane, int64_t grow0,
+                                             int gcol, int n_out, float *frow) {
+    if (all_kept) {
+        if (gcol >= n_out) return;  // warp-uniform
+        if (lane == 0) bulk_wait_read<0>();  // the previous store has read the buffer
+        __syncwarp();
+        const int sw = (lane >> 1) & 3;
+#pragma unroll
+        for (int c = 0; c < 4; c++)
+            st_shared_v4(stg + lane * 64 + ((c ^ sw) << 4), __float_as_uint(v[4 * c]),
+                         __float_as_uint(v[4 * c + 1]), __float_as_uint(v[4 * c + 2]),
+                         __float_as_uint(v[4 * c + 3]));
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(map, gcol, (int)grow0, stg);
+            bulk_commit();
+        }
+    } else if (kept) {
+#pragma unroll
+        for (int q = 0; q < 4; q++)
+            if (gcol + 4 * q < n_out)
+                *reinterpret_cast<float4 *>(frow + gcol + 4 * q) =
+                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    }
+}
+
 // ------------------------------------------------------- CTA-pair helpers
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -1039,16 +1070,12 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                                 st_v16(prow + gcol + q * 8, o);
                             }
                         }
-                        if constexpr (F32OUT) {   // fp32 weight gradients: this lane's row, 128 bytes
-                            if (valid) {
-                                float *frow = args.out_f32 + (grow0 + lane) * (int64_t)args.n_out + gcol;
-#pragma unroll
-                                for (int q = 0; q < 8; q++)
-                                    if (gcol + 4 * q < args.n_out)
-                                        *reinterpret_cast<float4 *>(frow + 4 * q) =
-                                            make_float4(of[4 * q], of[4 * q + 1], of[4 * q + 2],
-                                                        of[4 * q + 3]);
-                            }
+                        if constexpr (F32OUT) {   // fp32 weight gradients: two 16-column boxes
+                            float *frow = args.out_f32 + (grow0 + lane) * (int64_t)args.n_out;
+                            epi_store16f(&tmO, stg, of, all_kept, valid, lane, grow0, gcol, args.n_out,
+                                         frow);
+                            epi_store16f(&tmO, stg, of + 16, all_kept, valid, lane, grow0, gcol + 16,
+                                         args.n_out, frow);
                         } else {
                             epi_store32(&tmO, stg, pk, all_kept, valid, lane, grow0, gcol,
                                         args.n_out, orow);
@@ -1128,6 +1155,21 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, 
                     bk == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
                     : bk == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
                                : CU_TENSOR_MAP_SWIZZLE_32B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// An fp32 output map over a row-major [rows, cols] matrix, boxes of 32 rows
+// x 16 columns (64-byte swizzle, the epilogue's staging pattern).
+bool make_map_f32_out(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 4};
+    cuuint32_t box[2] = {16, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -1474,11 +1516,12 @@ moe_status gemm_wgrad_mn(const void *a, int64_t a_pitch, int a_cols, const void 
         !make_map(&mAt, a_tail, (uint64_t)e * 64, (uint64_t)a_cols, 64, 64, (uint64_t)a_tpitch) ||
         !make_map(&mB, b, (uint64_t)e * c_max, (uint64_t)b_cols, 64, 64, (uint64_t)b_pitch) ||
         !make_map(&mBt, b_tail, (uint64_t)e * 64, (uint64_t)b_cols, 64, 64, (uint64_t)b_tpitch) ||
-        !make_map(&mO, out, (uint64_t)e * a_cols, (uint64_t)b_cols, 32, 32))
+        !(out_f32 ? make_map_f32_out(&mO, out, (uint64_t)e * a_cols, (uint64_t)b_cols)
+                  : make_map(&mO, out, (uint64_t)e * a_cols, (uint64_t)b_cols, 32, 32)))
         return MOE_ERR_CUDA;
     GemmArgs g{nullptr, nullptr, st, nullptr, (__nv_bfloat16 *)out, a_cols, e, (int)c_max, b_cols,
                (int)c_max, counts, c_dev, 0, 0};
-    if (out_f32) {   // the output map is not used: the epilogue stores fp32 from registers
+    if (out_f32) {   // fp32 boxes of 32 rows x 16 columns
         g.out_f32 = (float *)out;
         return launch_gemm<EPI_WGRAD_MN_F32, 1, 64, 2, 1>(mA, mB, mB, mO, g, stream, &mAt, &mBt);
     }
