@@ -78,18 +78,18 @@ def normal_host(seed: int, name: str, shape, scale: float = 1.0, dtype: str = "f
     """
     shape = tuple(int(d) for d in shape)
     count = int(np.prod(shape, dtype=np.int64)) if shape else 1
+    if dtype not in ("f32", "bf16"):
+        raise ValueError(f"unknown dtype {dtype!r}")
     key = stream_key(seed, name)
-    out = np.empty(count, dtype=np.float32)
+    # converted chunk by chunk, so that a multi-GB tensor needs no full-size temporaries
+    out = np.empty(count, dtype=np.float32 if dtype == "f32" else np.uint16)
     for c0 in range(0, count, _CHUNK):
         c1 = min(count, c0 + _CHUNK)
         u = uniform_host(key, 2 * (start + c0), 2 * (c1 - c0))
         z = np.sqrt(-2.0 * np.log(u[0::2])) * np.cos(2.0 * math.pi * u[1::2])
-        out[c0:c1] = (scale * z).astype(np.float32)
-    if dtype == "f32":
-        return out.reshape(shape)
-    if dtype == "bf16":
-        return f32_to_bf16_bits(out).reshape(shape)
-    raise ValueError(f"unknown dtype {dtype!r}")
+        v = (scale * z).astype(np.float32)
+        out[c0:c1] = v if dtype == "f32" else f32_to_bf16_bits(v)
+    return out.reshape(shape)
 
 
 def _signed(c: int) -> int:
