@@ -1,4 +1,4 @@
-// Expert FFN on the 5th-generation tensor cores (bf16 layers).
+// Expert FFN and its backward on the 5th-generation tensor cores (bf16 and e4m3 layers).
 //
 // Method: the Tutel profile's experts {'type': 'ffn', hidden_size_per_expert,
 // has_fc1_bias, has_fc2_bias} and the DeepSpeed-MoE vs Tutel blog, section 3.5
@@ -11,20 +11,27 @@
 //   fc1:  hid[j] = act(buf[j] W1[j]^T + b1[j])        (SwiGLU: silu(buf W1^T) * (buf W3^T))
 //   fc2:  out[j] = hid[j] W2[j]^T + b2[j]
 //
-// One persistent kernel per GEMM, one CTA per SM (~200 KB shared memory):
-//   warps 0, 10 TMA producers (A tiles, B tiles): an A tile of 128 (or 256) rows
-//               and a 256-row B tile per stage, swizzled, a ring of stages
-//               guarded by full/empty mbarriers;
-//   warp 1      allocates all 512 TMEM columns; one lane issues tcgen05.mma
-//               (kind::f16, bf16 x bf16 -> fp32, M=128 N=256 K=16; two per K step
-//               for 256-row tiles, sharing the B tile) and tcgen05.commit to
-//               release stages and to publish a finished accumulator;
-//   warps 2-9   epilogue: tcgen05.ld 32 lanes x 32 columns, bias + activation in
-//               fp32, one rounding to bf16, 16-byte stores of the valid rows.
-// With 128-row tiles the two 128x256 accumulators let the epilogue of tile i
-// overlap the main loop of tile i+1; 256-row tiles use both as one.  Every wait is bounded: after ~1 s a role sets
-// MOE_ERR_TIMEOUT, raises a CTA-wide abort flag and leaves its loop; the CTA
-// then drains its outstanding copies and MMAs (bounded) and frees TMEM.
+// One persistent kernel per GEMM on CTA pairs (clusters of 2), one CTA per SM
+// (~218 KB of shared memory, 416 threads):
+//   warps 0, 10, 11, 12  TMA producers: each stage's A and B tiles arrive as
+//               four boxes (128-byte swizzle) into a ring guarded by full/empty
+//               mbarriers; a pair's copies complete on the even CTA's barriers;
+//   warp 1      allocates all 512 TMEM columns in both CTAs; in the even CTA
+//               one lane issues the 2-SM tcgen05.mma (M = 256 over the pair,
+//               N = 256; kind::f16 for bf16, kind::f8f6f4 for e4m3) and
+//               tcgen05.commit to release stages and publish accumulators;
+//   warps 2-9   epilogue: tcgen05.ld 32 lanes x 32 columns, then the mode's
+//               arithmetic in fp32 (bias, activation, e4m3 scales, or an
+//               activation derivative), one rounding, and TMA stores of 32 x 32
+//               bf16 (or 32 x 16 fp32) boxes staged in shared memory.
+// Tiles are 256 x 256 with two accumulators (a tile's epilogue overlaps the
+// next tile's main loop) or 256 x 512 with one (TN = 2: two N = 256 MMAs
+// share each A tile).  Operands are K-major, or MN-major (row-major [K, N]
+// weights and activations read in place, for the backward products), and a
+// per-expert-K mode contracts each expert over its own kept rows (the weight
+// gradients).  Every wait is bounded: after ~1 s a role sets MOE_ERR_TIMEOUT,
+// raises a CTA-wide abort flag and leaves its loop; the CTA then drains its
+// outstanding copies and MMAs (bounded) and frees TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
