@@ -387,7 +387,7 @@ class LayerRun:
             M.moe_expert_ffn(b.buf, b.counts, b.c_dev, w1, b1, w3, w2, b2, w.act, self.ffn_ws, b.out,
                              b.status)
         else:
-            M.moe_expert_ffn_train(b.buf, b.counts, b.c_dev, w1, b1, w2, b2, w.act, self.ffn_ws,
+            M.moe_expert_ffn_train(b.buf, b.counts, b.c_dev, w1, b1, w3, w2, b2, w.act, self.ffn_ws,
                                    b.out, pre, b.status)
         ev[4].record()
         M.moe_decode(b.out, b.idx, b.loc, b.gates, b.c_dev, b.y, b.status)
@@ -540,10 +540,11 @@ class LayerRun:
         FFN backward (d_buf and the weight gradients from dE), encode backward
         (the copy path's d_x from d_buf) and the gate backward (the gate path's
         d_logits, d_wg, d_bias, d_x from dG).  The two d_x terms are left
-        separate (their sum is one elementwise add).  For bf16 ReLU / GELU
-        experts the chain's forward is the training forward, which keeps the
-        pre-activation, and the FFN backward reads it (moe_expert_ffn_bwd_saved);
-        the backward that recomputes it is timed alone as well."""
+        separate (their sum is one elementwise add).  For bf16 experts the
+        chain's forward is the training forward, which keeps the pre-activation
+        (SwiGLU: a and b), and the FFN backward reads it
+        (moe_expert_ffn_bwd_saved); the backward that recomputes it, and the
+        one that keeps the weight gradients in fp32, are timed alone as well."""
         torch, M, w, b = self.torch, self.M, self.w, self.bufs
         x, wg, gb, w1, b1, w3, w2, b2 = self.args()
         dev, tdt = self.dev, self.tdt
@@ -566,8 +567,9 @@ class LayerRun:
         d_bias = torch.empty((w.e,), device=dev, dtype=torch.float32)
         d_xg = torch.empty((w.s, w.m), device=dev, dtype=torch.float32)
         hid = self.hid()
-        saved = w.dtype == "bf16" and w.act in ("relu", "gelu")
-        pre = torch.empty((w.e, b.c_max, w.h), device=dev, dtype=tdt) if saved else None
+        saved = w.dtype == "bf16"
+        pre = (torch.empty((w.e, b.c_max, 2 * w.h if swiglu else w.h), device=dev, dtype=tdt)
+               if saved else None)
 
         def dec():
             M.moe_decode_bwd(dy, b.out, b.idx, b.loc, b.gates, b.counts, b.c_dev, d_out, d_g,
@@ -581,16 +583,17 @@ class LayerRun:
             if pre is None:
                 ffn_recompute()
             else:
-                M.moe_expert_ffn_bwd_saved(b.buf, hid, pre, b.counts, b.c_dev, w1, w2, w.act, d_out,
-                                           ws, d_buf, d_w1, d_w2, d_b1, d_b2, b.status)
+                M.moe_expert_ffn_bwd_saved(b.buf, hid, pre, b.counts, b.c_dev, w1, w3, w2, w.act, d_out,
+                                           ws, d_buf, d_w1, d_w3, d_w2, d_b1, d_b2, b.status)
 
         # the same with the weight and bias gradients kept in fp32
         g32 = None if pre is None else [torch.empty(t.shape, device=dev, dtype=torch.float32)
-                                        if t is not None else None for t in (d_w1, d_w2, d_b1, d_b2)]
+                                        if t is not None else None
+                                        for t in (d_w1, d_w3, d_w2, d_b1, d_b2)]
 
         def ffn_f32():
-            M.moe_expert_ffn_bwd_saved(b.buf, hid, pre, b.counts, b.c_dev, w1, w2, w.act, d_out, ws,
-                                       d_buf, *g32, b.status)
+            M.moe_expert_ffn_bwd_saved(b.buf, hid, pre, b.counts, b.c_dev, w1, w3, w2, w.act, d_out,
+                                       ws, d_buf, *g32, b.status)
 
         def enc():
             M.moe_encode_bwd(d_buf, b.idx, b.loc, b.c_dev, dx, b.status)

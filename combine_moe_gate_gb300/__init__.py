@@ -56,12 +56,12 @@ def load():
         "moe_encode": (I, [P, I, P, P, P, P, I64, I, I, I, I64, U, P, P, P]),
         "moe_expert_ffn_workspace_size": (SZ, [I, I, I, I64, I, I]),
         "moe_expert_ffn": (I, [P, I, P, P, P, P, P, P, P, I, I, I64, I, I, P, SZ, P, P, P]),
-        "moe_expert_ffn_train": (I, [P, I, P, P, P, P, P, P, I, I, I64, I, I, P, SZ, P, P, P, P]),
+        "moe_expert_ffn_train": (I, [P, I, P, P, P, P, P, P, P, I, I, I64, I, I, P, SZ, P, P, P, P]),
         "moe_expert_ffn_bwd_workspace_size": (SZ, [I, I, I, I64, I, I]),
         "moe_expert_ffn_bwd": (I, [P, P, I, P, P, P, P, P, P, I, I, I64, I, I, P, P, SZ, P, P, P,
                                    P, P, P, P, P]),
-        "moe_expert_ffn_bwd_saved": (I, [P, P, P, I, P, P, P, P, I, I, I64, I, I, P, P, SZ, P, I, P,
-                                         P, P, P, P, P]),
+        "moe_expert_ffn_bwd_saved": (I, [P, P, P, I, P, P, P, P, P, I, I, I64, I, I, P, P, SZ, P, I,
+                                         P, P, P, P, P, P, P]),
         "moe_decode": (I, [P, I, P, P, P, P, I64, I, I, I, I64, P, P, P]),
         "moe_decode_bwd": (I, [P, P, I, P, P, P, P, P, I64, I, I, I, I64, U, P, P, P, P]),
         "moe_encode_bwd": (I, [P, I, P, P, P, I64, I, I, I, I64, P, P, P]),
@@ -259,19 +259,21 @@ def moe_expert_ffn(buf, counts, c_dev, w1, b1, w3, w2, b2, act, workspace, out, 
         _stream(stream)), "moe_expert_ffn")
 
 
-def moe_expert_ffn_train(buf, counts, c_dev, w1, b1, w2, b2, act, workspace, out, pre, dev_status,
-                         stream=None):
-    """moe_expert_ffn (bf16, ReLU / GELU) that also stores fc1's pre-activation
-    [e, c_max, h] for moe_expert_ffn_bwd_saved."""
+def moe_expert_ffn_train(buf, counts, c_dev, w1, b1, w3, w2, b2, act, workspace, out, pre,
+                         dev_status, stream=None):
+    """moe_expert_ffn (bf16) that also keeps what moe_expert_ffn_bwd_saved
+    needs: the pre-activation [e, c_max, h] (ReLU / GELU) or [a | b]
+    [e, c_max, 2h] (SwiGLU)."""
     e, c_max, m = buf.shape
     h = w1.shape[1]
     I, dt = _i32(), buf.dtype
+    hp = 2 * h if _act(act) == ACT["swiglu"] else h
     _check(load().moe_expert_ffn_train(
         _ptr(buf, "buf"), _dt(buf), _ptr(counts, "counts", I, (e,)), _ptr(c_dev, "c_dev", I),
-        _ptr(w1, "w1", dt, (e, h, m)), _ptr(b1, "b1", dt, (e, h)), _ptr(w2, "w2", dt, (e, m, h)),
-        _ptr(b2, "b2", dt, (e, m)), _act(act), e, c_max, m, h,
+        _ptr(w1, "w1", dt, (e, h, m)), _ptr(b1, "b1", dt, (e, h)), _ptr(w3, "w3", dt, (e, h, m)),
+        _ptr(w2, "w2", dt, (e, m, h)), _ptr(b2, "b2", dt, (e, m)), _act(act), e, c_max, m, h,
         _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
-        _ptr(out, "out", dt, (e, c_max, m)), _ptr(pre, "pre", dt, (e, c_max, h)),
+        _ptr(out, "out", dt, (e, c_max, m)), _ptr(pre, "pre", dt, (e, c_max, hp)),
         _ptr(dev_status, "dev_status", I), _stream(stream)), "moe_expert_ffn_train")
 
 
@@ -334,26 +336,29 @@ def moe_expert_ffn_bwd(buf, hid, counts, c_dev, w1, b1, w3, w2, act, d_out, work
         _ptr(dev_status, "dev_status", I), _stream(stream)), "moe_expert_ffn_bwd")
 
 
-def moe_expert_ffn_bwd_saved(buf, hid, pre, counts, c_dev, w1, w2, act, d_out, workspace, d_buf,
-                             d_w1, d_w2, d_b1, d_b2, dev_status, stream=None):
-    """moe_expert_ffn_bwd with the pre-activation moe_expert_ffn_train saved
-    (ReLU / GELU): nothing is recomputed.  d_w1, d_w2, d_b1, d_b2 are all bf16
-    or all fp32 (weight gradients kept in fp32)."""
+def moe_expert_ffn_bwd_saved(buf, hid, pre, counts, c_dev, w1, w3, w2, act, d_out, workspace,
+                             d_buf, d_w1, d_w3, d_w2, d_b1, d_b2, dev_status, stream=None):
+    """moe_expert_ffn_bwd with what moe_expert_ffn_train kept: nothing is
+    recomputed.  The weight and bias gradients are all bf16 or all fp32
+    (kept in fp32); w3 / d_w3 for SwiGLU only."""
     import torch
 
     e, c_max, m = buf.shape
     h = w1.shape[1]
     I, dt = _i32(), buf.dtype
+    hp = 2 * h if _act(act) == ACT["swiglu"] else h
     gdt = d_w1.dtype
     if gdt not in (torch.bfloat16, torch.float32):
         raise ValueError(f"d_w1: dtype {gdt}, expected bfloat16 or float32")
     _check(load().moe_expert_ffn_bwd_saved(
-        _ptr(buf, "buf"), _ptr(hid, "hid", dt, (e, c_max, h)), _ptr(pre, "pre", dt, (e, c_max, h)),
-        _dt(buf), _ptr(counts, "counts", I, (e,)), _ptr(c_dev, "c_dev", I),
-        _ptr(w1, "w1", dt, (e, h, m)), _ptr(w2, "w2", dt, (e, m, h)), _act(act), e, c_max, m, h,
+        _ptr(buf, "buf"), _ptr(hid, "hid", dt, (e, c_max, h)),
+        _ptr(pre, "pre", dt, (e, c_max, hp)), _dt(buf), _ptr(counts, "counts", I, (e,)),
+        _ptr(c_dev, "c_dev", I), _ptr(w1, "w1", dt, (e, h, m)), _ptr(w3, "w3", dt, (e, h, m)),
+        _ptr(w2, "w2", dt, (e, m, h)), _act(act), e, c_max, m, h,
         _ptr(d_out, "d_out", dt, (e, c_max, m)),
         _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _ptr(d_buf, "d_buf", dt, (e, c_max, m)), _dt(d_w1), _ptr(d_w1, "d_w1", gdt, (e, h, m)),
+        _ptr(d_w3, "d_w3", gdt, (e, h, m)),
         _ptr(d_w2, "d_w2", gdt, (e, m, h)), _ptr(d_b1, "d_b1", gdt, (e, h)),
         _ptr(d_b2, "d_b2", gdt, (e, m)), _ptr(dev_status, "dev_status", I), _stream(stream)),
         "moe_expert_ffn_bwd_saved")

@@ -217,7 +217,7 @@ static moe_status expert_ffn(const void *buf, moe_dtype dt, const int32_t *count
         return MOE_ERR_INVALID_ARG;
     if (act == MOE_ACT_SWIGLU && (!ok16(w3) || b1 != nullptr || b2 != nullptr))
         return MOE_ERR_INVALID_ARG;
-    if (pre && (dt != MOE_BF16 || act == MOE_ACT_SWIGLU)) return MOE_ERR_UNSUPPORTED;
+    if (pre && dt != MOE_BF16) return MOE_ERR_UNSUPPORTED;
     if (pre && !ok16(pre)) return MOE_ERR_INVALID_ARG;
     if (dt == MOE_BF16) {
         if (!ffn_tc_supported(e, c_max, m, h)) return MOE_ERR_UNSUPPORTED;
@@ -239,12 +239,13 @@ moe_status moe_expert_ffn(const void *buf, moe_dtype dt, const int32_t *counts,
 
 moe_status moe_expert_ffn_train(const void *buf, moe_dtype dt, const int32_t *counts,
                                 const int32_t *c_dev, const void *w1, const void *b1,
-                                const void *w2, const void *b2, moe_act act, int e, int64_t c_max,
-                                int m, int h, void *workspace, size_t workspace_bytes, void *out,
-                                void *pre, int32_t *dev_status, void *stream) {
+                                const void *w3, const void *w2, const void *b2, moe_act act, int e,
+                                int64_t c_max, int m, int h, void *workspace,
+                                size_t workspace_bytes, void *out, void *pre, int32_t *dev_status,
+                                void *stream) {
     if (!pre) return MOE_ERR_INVALID_ARG;
-    return expert_ffn(buf, dt, counts, c_dev, w1, b1, nullptr, w2, b2, act, e, c_max, m, h,
-                      workspace, workspace_bytes, out, pre, dev_status, stream);
+    return expert_ffn(buf, dt, counts, c_dev, w1, b1, w3, w2, b2, act, e, c_max, m, h, workspace,
+                      workspace_bytes, out, pre, dev_status, stream);
 }
 
 moe_status moe_decode(const void *out, moe_dtype dt, const int32_t *idx, const int32_t *loc,
@@ -316,7 +317,7 @@ static moe_status expert_ffn_bwd(const void *buf, const void *hid, const void *p
     if (!ffn_tc_supported(e, c_max, m, h) || !ffn_tc_supported(e, h2, m, h) ||
         (int64_t)e * h2 >= ((int64_t)1 << 31) || (int64_t)e * ((c_max + 7) / 8 * 8) >= ((int64_t)1 << 31))
         return MOE_ERR_UNSUPPORTED;
-    if (pre && (act == MOE_ACT_SWIGLU || !ok16(pre))) return MOE_ERR_INVALID_ARG;
+    if (pre && !ok16(pre)) return MOE_ERR_INVALID_ARG;
     return ffn_tc_bwd_launch(buf, hid, counts, c_dev, w1, b1, w3, w2, act, e, c_max, m, h, d_out,
                              workspace, d_buf, d_w1, d_w3, d_w2, d_b1, d_b2, dev_status,
                              as_stream(stream), pre, wgrad_dt == MOE_F32);
@@ -336,15 +337,15 @@ moe_status moe_expert_ffn_bwd(const void *buf, const void *hid, moe_dtype dt,
 
 moe_status moe_expert_ffn_bwd_saved(const void *buf, const void *hid, const void *pre,
                                     moe_dtype dt, const int32_t *counts, const int32_t *c_dev,
-                                    const void *w1, const void *w2, moe_act act, int e,
-                                    int64_t c_max, int m, int h, const void *d_out,
+                                    const void *w1, const void *w3, const void *w2, moe_act act,
+                                    int e, int64_t c_max, int m, int h, const void *d_out,
                                     void *workspace, size_t workspace_bytes, void *d_buf,
-                                    moe_dtype wgrad_dt, void *d_w1, void *d_w2, void *d_b1,
-                                    void *d_b2, int32_t *dev_status, void *stream) {
+                                    moe_dtype wgrad_dt, void *d_w1, void *d_w3, void *d_w2,
+                                    void *d_b1, void *d_b2, int32_t *dev_status, void *stream) {
     if (!pre) return MOE_ERR_INVALID_ARG;
-    return expert_ffn_bwd(buf, hid, pre, dt, counts, c_dev, w1, nullptr, nullptr, w2, act, e, c_max,
-                          m, h, d_out, workspace, workspace_bytes, d_buf, wgrad_dt, d_w1, nullptr,
-                          d_w2, d_b1, d_b2, dev_status, stream);
+    return expert_ffn_bwd(buf, hid, pre, dt, counts, c_dev, w1, nullptr, w3, w2, act, e, c_max, m, h,
+                          d_out, workspace, workspace_bytes, d_buf, wgrad_dt, d_w1, d_w3, d_w2, d_b1,
+                          d_b2, dev_status, stream);
 }
 
 size_t moe_layer_workspace_size(moe_dtype dt, moe_act act, int64_t s, int m, int e, int k,

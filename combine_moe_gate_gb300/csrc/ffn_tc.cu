@@ -71,9 +71,17 @@ constexpr int SMEM_RING = 192 * 1024;   // operand ring per CTA
 // EPI_DGELU_BMN / EPI_DRELU_BMN: d_hid = acc (B MN-major) times act'(pre)
 // with the saved pre-activation (GemmArgs::aux) laid out like out.
 // EPI_WGRAD_MN_F32: EPI_WGRAD_MN writing fp32 to GemmArgs::out_f32.
+// EPI_SWIGLU_SAVE: the SwiGLU fc1 that also stores a = buf W1^T and
+// b = buf W3^T (bf16) to GemmArgs::aux_out, rows of 2 * n_out: a, then b.
+// EPI_DSWIGLU_BMN: d_hid = acc (B MN-major) and the saved [a | b] rows
+// (GemmArgs::aux, 2 * n_out a row) give d_a = d_hid * b * silu'(a) into out
+// and d_b = d_hid * silu(a) into out + n_out, out rows of GemmArgs::out_pitch.
 enum Epi { EPI_GELU = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_BIAS = 3, EPI_BIAS_BMN = 4,
            EPI_WGRAD_MN = 5, EPI_DGELU = 6, EPI_DRELU = 7, EPI_GELU_SAVE = 8, EPI_RELU_SAVE = 9,
-           EPI_DGELU_BMN = 10, EPI_DRELU_BMN = 11, EPI_WGRAD_MN_F32 = 12 };
+           EPI_DGELU_BMN = 10, EPI_DRELU_BMN = 11, EPI_WGRAD_MN_F32 = 12, EPI_SWIGLU_SAVE = 13,
+           EPI_DSWIGLU_BMN = 14 };
+// The SwiGLU fc1 modes (W1 and W3 rows paired in one N = 256 MMA).
+__host__ __device__ constexpr bool is_swiglu(int epi) { return epi == EPI_SWIGLU || epi == EPI_SWIGLU_SAVE; }
 
 // Tile shape.  TM = 1: 128 x 256 tiles, two 256-column accumulators in TMEM so
 // the epilogue of one tile overlaps the main loop of the next.  TM = 2:
@@ -188,6 +196,8 @@ struct GemmArgs {
     __nv_bfloat16 *aux_out;
     // EPI_WGRAD_MN_F32: the result in fp32 [e * c_max, n_out] (out unused).
     float *out_f32;
+    // Elements between rows of out (0: n_out).
+    int64_t out_pitch;
     // Error-path test: the producers issue no copies, so the MMA issuer's
     // bounded wait on the first stage runs out (MOE_ERR_TIMEOUT).
     int32_t stall;
@@ -614,13 +624,14 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
               const __grid_constant__ CUtensorMap tmAt, const __grid_constant__ CUtensorMap tmBt,
               const GemmArgs args) {
     using TL = Tiling<TM, BK, CL, TN, EB>;
-    static_assert(TN == 1 || EPI != EPI_SWIGLU, "SwiGLU tiles pair W1 and W3 in one N = 256 MMA");
+    static_assert(TN == 1 || !is_swiglu(EPI), "SwiGLU tiles pair W1 and W3 in one N = 256 MMA");
     constexpr bool F8 = EB == 1;   // e4m3 operands (kind::f8f6f4), scaled epilogue
-    static_assert(!F8 || (CL == 2 && EPI != EPI_SWIGLU && EPI != EPI_BIAS_BMN), "e4m3 pair tiles");
+    static_assert(!F8 || (CL == 2 && !is_swiglu(EPI) && EPI != EPI_BIAS_BMN), "e4m3 pair tiles");
     constexpr bool F32OUT = EPI == EPI_WGRAD_MN_F32;   // fp32 result, stored from registers
     constexpr bool AMN = EPI == EPI_WGRAD_MN || F32OUT;   // A MN-major as well, tail blocks from tmAt / tmBt
     constexpr bool DACT = EPI == EPI_DGELU || EPI == EPI_DRELU;   // activation backward epilogue
-    constexpr bool DACTP = EPI == EPI_DGELU_BMN || EPI == EPI_DRELU_BMN;   // act' of a saved pre
+    constexpr bool DSWI = EPI == EPI_DSWIGLU_BMN;   // SwiGLU derivative of a saved [a | b]
+    constexpr bool DACTP = EPI == EPI_DGELU_BMN || EPI == EPI_DRELU_BMN || DSWI;   // act' of a saved pre
     constexpr bool DGELU = EPI == EPI_DGELU || EPI == EPI_DGELU_BMN;
     constexpr bool SAVE = EPI == EPI_GELU_SAVE || EPI == EPI_RELU_SAVE;   // fc1 keeping its pre-activation
     constexpr bool GELU = EPI == EPI_GELU || EPI == EPI_GELU_SAVE;
@@ -655,7 +666,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     const uint32_t lead = rank & ~1u;    // the pair's MMA-issuing CTA
     const int tile0 = (int)(blockIdx.x / CL);
     const int tile_step = (int)(gridDim.x / CL);
-    constexpr int NOUT_TILE = EPI == EPI_SWIGLU ? BN / 2 : BN * TN;  // output columns per tile
+    constexpr int NOUT_TILE = is_swiglu(EPI) ? BN / 2 : BN * TN;  // output columns per tile
     const int ntn = (args.n_out + NOUT_TILE - 1) / NOUT_TILE;
     const int nk = (args.K + BK - 1) / BK;
     const bool kmode = args.k_counts != nullptr;           // K per expert
@@ -755,7 +766,7 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             // TN = 2 producer hh loads N sub-tile hh
             const int b_row = T.j * args.b_rows + T.nt * NOUT_TILE +
                               (TN == 2 ? hh * BN + (int)prank * (BN / 2)
-                                       : (PAIR && EPI != EPI_SWIGLU ? (int)prank * TL::B_ROWS : 0) +
+                                       : (PAIR && !is_swiglu(EPI) ? (int)prank * TL::B_ROWS : 0) +
                                              hh * TL::B_BOX_ROWS);
             // MN-major weight gradients: a last K block only partly kept
             // comes from the tail maps (rows j * BK ..)
@@ -803,13 +814,13 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                             // SwiGLU: the first CTA's half of B is W1, the second's W3
                             if (prank == 0) mbar_expect_tx(&ctl->full[stage], 2 * B_BOX_BYTES);
                             tma_load_2d_pair(sB + stage * B_BYTES + hh * B_BOX_BYTES,
-                                             EPI == EPI_SWIGLU && prank ? &tmB3 : &tmB, kb * BK, b_row, fb);
+                                             is_swiglu(EPI) && prank ? &tmB3 : &tmB, kb * BK, b_row, fb);
                         }
                     } else if (ok && is_a) {
                         mbar_expect_tx(&ctl->full[stage], A_BOX_BYTES);
                         tma_load_2d(sA + stage * A_BYTES + hh * A_BOX_BYTES, &tmA, kb * BK, a_row,
                                     &ctl->full[stage]);
-                    } else if (ok && EPI == EPI_SWIGLU) {
+                    } else if (ok && is_swiglu(EPI)) {
                         // W1 rows in the first half of the B tile, W3 rows in the second
                         mbar_expect_tx(&ctl->full[stage], B_BOX_BYTES);
                         tma_load_2d(sB + stage * B_BYTES + hh * B_BOX_BYTES, hh ? &tmB3 : &tmB, kb * BK,
@@ -943,11 +954,12 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             const bool all_kept = row - lane + 31 < T.rows;  // the warp's 32 rows
             const int64_t grow0 = (int64_t)T.j * args.c_max + args.row_lo + row - lane;
             __nv_bfloat16 *orow =
-                args.out + ((int64_t)T.j * args.c_max + args.row_lo + row) * (int64_t)args.n_out;
+                args.out + ((int64_t)T.j * args.c_max + args.row_lo + row) *
+                               (args.out_pitch ? args.out_pitch : (int64_t)args.n_out);
             const __nv_bfloat16 *brow = args.bias ? args.bias + (int64_t)T.j * args.n_out : nullptr;
             const uint32_t tbase = tmem + ((uint32_t)(sub * 32) << 16) +
                                    (uint32_t)(acc * TL::ACC_COLS + (TM == 2 ? half * BN : 0));
-            if (EPI == EPI_SWIGLU) {
+            if (is_swiglu(EPI)) {
 #pragma unroll 1
                 for (int c0 = 0; c0 < COLS; c0 += 32) {
                     const int ocol = col0 + c0;               // column within the tile's output
@@ -970,6 +982,25 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                                               __uint_as_float(u[2 * i + 1]));
                     epi_store32(&tmO, stg, pk, all_kept, valid, lane, grow0, gcol, args.n_out,
                                 orow);
+                    if (EPI == EPI_SWIGLU_SAVE && valid) {   // this lane's row of a, then of b
+                        __nv_bfloat16 *arow = args.aux_out + ((int64_t)T.j * args.c_max + args.row_lo +
+                                                              row) * (2 * (int64_t)args.n_out);
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            if (gcol + 8 * q < args.n_out) {
+                                V16 oa, ob;
+#pragma unroll
+                                for (int i = 0; i < 4; i++) {
+                                    oa.w[i] = pack_bf16(__uint_as_float(r[8 * q + 2 * i]),
+                                                        __uint_as_float(r[8 * q + 2 * i + 1]));
+                                    ob.w[i] = pack_bf16(__uint_as_float(u[8 * q + 2 * i]),
+                                                        __uint_as_float(u[8 * q + 2 * i + 1]));
+                                }
+                                st_v16(arow + gcol + 8 * q, oa);
+                                st_v16(arow + args.n_out + gcol + 8 * q, ob);
+                            }
+                        }
+                    }
                 }
             } else {
                 // this warp's bias columns, widened to fp32 in shared memory once per tile
@@ -991,7 +1022,8 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 const float sa = F8 && valid ? args.a_scale[grow0 + lane] : 0.0f;
                 const __nv_bfloat16 *drow =
                     DACT || DACTP
-                        ? args.aux + ((int64_t)T.j * args.c_max + args.row_lo + row) * (int64_t)args.n_out
+                        ? args.aux + ((int64_t)T.j * args.c_max + args.row_lo + row) *
+                                         ((DSWI ? 2 : 1) * (int64_t)args.n_out)
                         : nullptr;
                 __nv_bfloat16 *prow =
                     SAVE ? args.aux_out + ((int64_t)T.j * args.c_max + args.row_lo + row) * (int64_t)args.n_out
@@ -1014,19 +1046,27 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                         const int gcol = T.nt * NOUT_TILE + col0 + c0 + 32 * h2;
                         uint32_t pk[16];
                         float of[32];   // weight gradients in fp32: this row's 32 columns
-                        uint32_t dv[16];   // activation backward: this row's d_hid or pre, 32 columns
+                        uint32_t dv[16];   // activation backward: this row's d_hid or pre (SwiGLU: a), 32 columns
+                        uint32_t db[16];   // SwiGLU backward: this row's b, 32 columns
                         if (DACT || DACTP) {
 #pragma unroll
                             for (int q = 0; q < 4; q++) {
-                                V16 v{};
-                                if (valid && gcol + q * 8 < args.n_out) v = ld_v16(drow + gcol + q * 8);
-                                dv[q * 4 + 0] = v.w[0]; dv[q * 4 + 1] = v.w[1];
-                                dv[q * 4 + 2] = v.w[2]; dv[q * 4 + 3] = v.w[3];
+                                V16 v{}, w{};
+                                if (valid && gcol + q * 8 < args.n_out) {
+                                    v = ld_v16(drow + gcol + q * 8);
+                                    if (DSWI) w = ld_v16(drow + args.n_out + gcol + q * 8);
+                                }
+#pragma unroll
+                                for (int i = 0; i < 4; i++) {
+                                    dv[q * 4 + i] = v.w[i];
+                                    db[q * 4 + i] = w.w[i];
+                                }
                             }
                         }
 #pragma unroll
                         for (int q = 0; q < 4; q++) {
                             uint32_t pp[4];   // fc1 keeping its pre-activation: 8 packed columns
+                            uint32_t pb[4];   // SwiGLU backward: d_b, 8 packed columns
                             const float4 *bp = reinterpret_cast<const float4 *>(bsl + c0 + 32 * h2 + q * 8);
                             const float4 bl = bp[0], bh = bp[1];
                             const float2 bb[4] = {make_float2(bl.x, bl.y), make_float2(bl.z, bl.w),
@@ -1051,7 +1091,18 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                                 if (SAVE) pp[i] = pack_bf16(a.x, a.y);
                                 if (GELU) a = gelu_erf2(a);
                                 else if (RELU) a = make_float2(fmaxf(a.x, 0.0f), fmaxf(a.y, 0.0f));
-                                if (DACT || DACTP) {
+                                if constexpr (DSWI) {
+                                    // a = d_hid; the saved a and b of these two columns
+                                    const float2 av = make_float2(__uint_as_float(dv[q * 4 + i] << 16),
+                                                                  __uint_as_float(dv[q * 4 + i] & 0xFFFF0000u));
+                                    const float2 bv = make_float2(__uint_as_float(db[q * 4 + i] << 16),
+                                                                  __uint_as_float(db[q * 4 + i] & 0xFFFF0000u));
+                                    const float sx = 1.0f / (1.0f + expf(-av.x));
+                                    const float sy = 1.0f / (1.0f + expf(-av.y));
+                                    pb[i] = pack_bf16(a.x * av.x * sx, a.y * av.y * sy);   // d_b
+                                    a = make_float2(a.x * bv.x * sx * (1.0f + av.x * (1.0f - sx)),
+                                                    a.y * bv.y * sy * (1.0f + av.y * (1.0f - sy)));   // d_a
+                                } else if (DACT || DACTP) {
                                     // DACT: aux is d_hid, a the pre-activation; DACTP: aux is
                                     // the saved pre-activation, a = d_hid
                                     const uint32_t u2 = dv[q * 4 + i];
@@ -1075,6 +1126,14 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                                 V16 o;
                                 o.w[0] = pp[0]; o.w[1] = pp[1]; o.w[2] = pp[2]; o.w[3] = pp[3];
                                 st_v16(prow + gcol + q * 8, o);
+                            }
+                            if constexpr (DSWI) {
+                                if (valid && gcol + q * 8 < args.n_out) {
+                                    // d_b: the second half of this lane's output row, 8 columns
+                                    V16 o;
+                                    o.w[0] = pb[0]; o.w[1] = pb[1]; o.w[2] = pb[2]; o.w[3] = pb[3];
+                                    st_v16(orow + args.n_out + gcol + q * 8, o);
+                                }
                             }
                         }
                         if constexpr (F32OUT) {   // fp32 weight gradients: two 16-column boxes
@@ -1251,7 +1310,7 @@ moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtenso
         nunits = CL > 1 ? max_clusters(kern, SMEM, CL) : sm_count();
         if (dev >= 0 && dev < 64) units[dev] = nunits;
     }
-    constexpr int NOUT_TILE = EPI == EPI_SWIGLU ? BN / 2 : BN * TN;
+    constexpr int NOUT_TILE = is_swiglu(EPI) ? BN / 2 : BN * TN;
     const int64_t ntn = (args.n_out + NOUT_TILE - 1) / NOUT_TILE;
     int64_t upper = (int64_t)args.e * ((args.c_max + TL::BMT - 1) / TL::BMT) * ntn;
     int64_t grid = upper < nunits ? upper : nunits;
@@ -1322,8 +1381,8 @@ moe_status ffn_tc_launch(const void *buf, const int32_t *counts, const int32_t *
     g1.aux_out = (__nv_bfloat16 *)pre;   // training: fc1 also keeps its pre-activation
     moe_status r;
     if (swiglu) {
-        if (pre) return MOE_ERR_UNSUPPORTED;
-        r = launch_gemm<EPI_SWIGLU, TM1, BK1, CL1, 1>(mA1, mB1, mB3, mO1, g1, stream);
+        r = pre ? launch_gemm<EPI_SWIGLU_SAVE, TM1, BK1, CL1, 1>(mA1, mB1, mB3, mO1, g1, stream)
+                : launch_gemm<EPI_SWIGLU, TM1, BK1, CL1, 1>(mA1, mB1, mB3, mO1, g1, stream);
     } else if (act == MOE_ACT_GELU) {
         r = pre ? launch_gemm<EPI_GELU_SAVE, TM1, BK1, CL1, 1>(mA1, mB1, mB1, mO1, g1, stream)
                 : launch_gemm<EPI_GELU, TM1, BK1, CL1, 1>(mA1, mB1, mB1, mO1, g1, stream);
@@ -1507,6 +1566,24 @@ moe_status gemm_dact_bmn(const void *d_out, const void *w2, const void *pre, moe
                                : launch_gemm<EPI_DRELU_BMN, 1, 64, 2, 1>(mA, mB, mB, mO, g, stream);
 }
 
+// SwiGLU with the forward's saved [a | b] rows: d_hid = d_out w2 (w2 read
+// MN-major) and, in the epilogue, d_pre = [d_hid * b * silu'(a) | d_hid *
+// silu(a)] ([e, c_max, 2h]); d_hid is never stored.
+moe_status gemm_dswiglu_bmn(const void *d_out, const void *w2, const void *ab, void *d_pre,
+                            const int32_t *counts, const int32_t *c_dev, int e, int64_t c_max, int m,
+                            int h, int32_t *st, cudaStream_t stream) {
+    using T2 = Tiling<1, 64, 2, 1>;
+    CUtensorMap mA, mB, mO;
+    if (!make_map(&mA, d_out, (uint64_t)e * c_max, (uint64_t)m, T2::A_BOX_ROWS, 64) ||
+        !make_map(&mB, w2, (uint64_t)e * m, (uint64_t)h, 64, 64) ||
+        !make_map(&mO, d_pre, (uint64_t)e * c_max, 2 * (uint64_t)h, 32, 32))
+        return MOE_ERR_CUDA;
+    GemmArgs g{counts, c_dev, st, nullptr, (__nv_bfloat16 *)d_pre, c_max, e, m, h, m, nullptr,
+               nullptr, 0, 0, nullptr, nullptr, (const __nv_bfloat16 *)ab};
+    g.out_pitch = 2 * (int64_t)h;
+    return launch_gemm<EPI_DSWIGLU_BMN, 1, 64, 2, 1>(mA, mB, mB, mO, g, stream);
+}
+
 // Weight gradients out[j] = A[j]^T B[j] over the first min(counts[j], *c_dev,
 // c_max) rows of expert j, both operands read MN-major in place: A rows of
 // a_cols columns at pitch a_pitch, B rows of b_cols at pitch b_pitch, c_max
@@ -1575,9 +1652,11 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
     // d_hid; then d_pre (ReLU / GELU: the pre-activation recomputed and
     // differentiated in one product; SwiGLU: a and b recomputed, then the
     // activation backward); then d_buf
-    if (pre) {
+    if (pre && swiglu) {
+        // the forward's saved [a | b]: one product, d_hid never stored
+        MOE_TRY(gemm_dswiglu_bmn(d_out, w2, pre, dpre, counts, c_dev, e, c_max, m, h, st, stream));
+    } else if (pre) {
         // the forward's saved pre-activation: one product, d_hid never stored
-        if (swiglu) return MOE_ERR_UNSUPPORTED;
         MOE_TRY(gemm_dact_bmn(d_out, w2, pre, act, dpre, counts, c_dev, e, c_max, m, h, st, stream));
     } else if (swiglu) {
         MOE_TRY(gemm_bias_bmn(d_out, w2, dh, counts, c_dev, e, c_max, m, h, st, stream));

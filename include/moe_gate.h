@@ -191,18 +191,20 @@ moe_status moe_expert_ffn(const void *buf, moe_dtype dt, const int32_t *counts,
                           int32_t *dev_status, void *stream);
 
 /*
- * moe_expert_ffn for training (bf16, ReLU / GELU): the same outputs, and fc1
- * also stores its pre-activation buf W1^T + b1 (fp32 sum rounded once to
- * bf16) to pre [e, c_max, h] for the kept rows (other rows not written), so
- * that moe_expert_ffn_bwd_saved need not recompute it.  Errors: as
- * moe_expert_ffn; MOE_ERR_INVALID_ARG for a NULL or misaligned pre;
- * MOE_ERR_UNSUPPORTED for fp32 or SwiGLU.
+ * moe_expert_ffn for training (bf16): the same outputs, and fc1 also stores
+ * what moe_expert_ffn_bwd_saved needs instead of recomputing it, for the kept
+ * rows (other rows not written), rounded once to bf16 from the fp32 sums:
+ *   ReLU / GELU: the pre-activation buf W1^T + b1, pre [e, c_max, h];
+ *   SwiGLU:      a = buf W1^T and b = buf W3^T, pre [e, c_max, 2h] (a, then b).
+ * Errors: as moe_expert_ffn; MOE_ERR_INVALID_ARG for a NULL or misaligned
+ * pre; MOE_ERR_UNSUPPORTED for fp32.
  */
 moe_status moe_expert_ffn_train(const void *buf, moe_dtype dt, const int32_t *counts,
                                 const int32_t *c_dev, const void *w1, const void *b1,
-                                const void *w2, const void *b2, moe_act act, int e, int64_t c_max,
-                                int m, int h, void *workspace, size_t workspace_bytes, void *out,
-                                void *pre, int32_t *dev_status, void *stream);
+                                const void *w3, const void *w2, const void *b2, moe_act act, int e,
+                                int64_t c_max, int m, int h, void *workspace,
+                                size_t workspace_bytes, void *out, void *pre, int32_t *dev_status,
+                                void *stream);
 
 /*
  * Fast decode ([Blog] 3.5, K0 forward; [PR8195] change 3, fp32 combine).
@@ -274,24 +276,27 @@ moe_status moe_expert_ffn_bwd(const void *buf, const void *hid, moe_dtype dt,
                               void *stream);
 
 /*
- * moe_expert_ffn_bwd with the pre-activation moe_expert_ffn_train saved
- * (ReLU / GELU): d_pre = (d_out W2) * act'(pre) is formed in one product's
- * epilogue (d_hid is neither rounded nor stored, and nothing is recomputed);
- * the other outputs as moe_expert_ffn_bwd.  pre [e, c_max, h] in `dt`;
- * d_w1, d_w2, d_b1, d_b2 in `wgrad_dt`: MOE_BF16, or MOE_F32 for weight and
- * bias gradients kept in fp32 (the products' fp32 sums stored unrounded, as
- * an optimiser with fp32 master weights wants them); d_buf in `dt`.
- * workspace: moe_expert_ffn_bwd_workspace_size() bytes.  Errors: as
- * moe_expert_ffn_bwd; MOE_ERR_INVALID_ARG for a NULL or misaligned pre, for
- * SwiGLU, or for another wgrad_dt.
+ * moe_expert_ffn_bwd with what moe_expert_ffn_train kept (pre): d_pre is
+ * formed in the epilogue of the product d_out W2, so d_hid is neither rounded
+ * nor stored and nothing is recomputed:
+ *   ReLU / GELU: d_pre = (d_out W2) * act'(pre), pre [e, c_max, h];
+ *   SwiGLU:      [d_a | d_b] = (d_out W2) * [b silu'(a) | silu(a)],
+ *                pre = [a | b] [e, c_max, 2h].
+ * The other outputs as moe_expert_ffn_bwd (w3 and d_w3 for SwiGLU only, NULL
+ * otherwise; d_b1 / d_b2 for ReLU / GELU only, or NULL).  d_w1, d_w3, d_w2,
+ * d_b1, d_b2 in `wgrad_dt`: MOE_BF16, or MOE_F32 for gradients kept in fp32
+ * (the products' fp32 sums stored unrounded, as an optimiser with fp32 master
+ * weights wants them); d_buf in `dt`.  workspace:
+ * moe_expert_ffn_bwd_workspace_size() bytes.  Errors: as moe_expert_ffn_bwd;
+ * MOE_ERR_INVALID_ARG for a NULL or misaligned pre or another wgrad_dt.
  */
 moe_status moe_expert_ffn_bwd_saved(const void *buf, const void *hid, const void *pre,
                                     moe_dtype dt, const int32_t *counts, const int32_t *c_dev,
-                                    const void *w1, const void *w2, moe_act act, int e,
-                                    int64_t c_max, int m, int h, const void *d_out,
+                                    const void *w1, const void *w3, const void *w2, moe_act act,
+                                    int e, int64_t c_max, int m, int h, const void *d_out,
                                     void *workspace, size_t workspace_bytes, void *d_buf,
-                                    moe_dtype wgrad_dt, void *d_w1, void *d_w2, void *d_b1,
-                                    void *d_b2, int32_t *dev_status, void *stream);
+                                    moe_dtype wgrad_dt, void *d_w1, void *d_w3, void *d_w2,
+                                    void *d_b1, void *d_b2, int32_t *dev_status, void *stream);
 
 /*
  * Gate backward ([Tutel] gate_type 'top': the gates are softmax probabilities

@@ -183,35 +183,35 @@ def test_invalid_arguments_are_rejected_before_launch():
     assert fbc(a16=0) == INV                                     # workspace too small
     assert fbc(a13=100) == INV                                   # h not a multiple of 8
     assert fbc(a1=odd) == INV and fbc(a17=odd) == INV            # misaligned hid / d_buf
-    # the saved-pre backward: buf, hid, pre, dt, counts, c_dev, w1, w2, act, e, c_max, m, h, d_out,
-    # ws, ws_bytes, d_buf, wgrad_dt, d_w1, d_w2, d_b1, d_b2, status, stream
+    # the saved-pre backward: buf, hid, pre, dt, counts, c_dev, w1, w3, w2, act, e, c_max, m, h,
+    # d_out, ws, ws_bytes, d_buf, wgrad_dt, d_w1, d_w3, d_w2, d_b1, d_b2, status, stream
     fs = lib.moe_expert_ffn_bwd_saved
-    sok = [A, B, A, M.MOE_BF16, A, A, A, B, 1, 4, 64, 64, 128, A, B, 1 << 40, A, M.MOE_F32, B, A,
-           None, None, A, None]
+    sok = [A, B, A, M.MOE_BF16, A, A, A, None, B, 1, 4, 64, 64, 128, A, B, 1 << 40, A, M.MOE_F32,
+           B, None, A, None, None, A, None]
     def fsc(**kw):
         a = list(sok)
         for i, v in kw.items():
             a[int(i[1:])] = v
         return fs(*a)
     assert fsc(a2=None) == INV and fsc(a2=odd) == INV            # pre required, aligned
-    assert fsc(a8=2) == INV                                      # no SwiGLU
+    assert fsc(a9=2) == INV                                      # SwiGLU needs w3 and d_w3
     assert fsc(a3=M.MOE_F32) == M.MOE_ERR_UNSUPPORTED
-    assert fsc(a15=0) == INV                                     # workspace too small
-    assert fsc(a17=7) == INV                                     # weight gradients bf16 or fp32
-    assert fsc(a18=odd) == INV                                   # misaligned d_w1
-    # the training forward: buf, dt, counts, c_dev, w1, b1, w2, b2, act, e, c_max, m, h, ws,
+    assert fsc(a16=0) == INV                                     # workspace too small
+    assert fsc(a18=7) == INV                                     # weight gradients bf16 or fp32
+    assert fsc(a19=odd) == INV                                   # misaligned d_w1
+    # the training forward: buf, dt, counts, c_dev, w1, b1, w3, w2, b2, act, e, c_max, m, h, ws,
     # ws_bytes, out, pre, status, stream
     ft = lib.moe_expert_ffn_train
-    tok = [A, M.MOE_BF16, A, A, A, None, B, None, 1, 4, 64, 64, 128, A, 1 << 40, B, A, A, None]
+    tok = [A, M.MOE_BF16, A, A, A, None, None, B, None, 1, 4, 64, 64, 128, A, 1 << 40, B, A, A, None]
     def ftc(**kw):
         a = list(tok)
         for i, v in kw.items():
             a[int(i[1:])] = v
         return ft(*a)
-    assert ftc(a16=None) == INV and ftc(a16=odd) == INV          # pre required, aligned
-    assert ftc(a8=2) == INV                                      # SwiGLU needs w3 (none here)
+    assert ftc(a17=None) == INV and ftc(a17=odd) == INV          # pre required, aligned
+    assert ftc(a9=2) == INV                                      # SwiGLU needs w3 (none here)
     assert ftc(a1=M.MOE_F32) == M.MOE_ERR_UNSUPPORTED            # bf16 only
-    assert ftc(a14=0) == INV                                     # workspace too small
+    assert ftc(a15=0) == INV                                     # workspace too small
     # e4m3 row quantisation: src, batches, rows_per_batch, cols, counts, c_dev, q, scale, status
     qr = lib.moe_quantize_rows_fp8
     qok = [A, 2, 8, 64, None, None, B, A, B, None]

@@ -152,16 +152,17 @@ def test_well_formed_calls_pass_and_marshal_their_sizes(stub):
     M.moe_expert_ffn_bwd(buf, z(e, c_max, h, dtype=bf), counts, c_dev, w1, b1, None, w2, "gelu",
                          z(e, c_max, m, dtype=bf), ws, z(e, c_max, m, dtype=bf), z(e, h, m, dtype=bf),
                          None, z(e, m, h, dtype=bf), z(e, h, dtype=bf), z(e, m, dtype=bf), st)
-    M.moe_expert_ffn_train(buf, counts, c_dev, w1, b1, w2, b2, "gelu", ws, out,
+    M.moe_expert_ffn_train(buf, counts, c_dev, w1, b1, None, w2, b2, "gelu", ws, out,
                            z(e, c_max, h, dtype=bf), st)
-    M.moe_expert_ffn_bwd_saved(buf, z(e, c_max, h, dtype=bf), z(e, c_max, h, dtype=bf), counts, c_dev,
-                               w1, w2, "relu", z(e, c_max, m, dtype=bf), ws, z(e, c_max, m, dtype=bf),
-                               z(e, h, m), z(e, m, h), z(e, h), z(e, m), st)
+    M.moe_expert_ffn_bwd_saved(buf, z(e, c_max, h, dtype=bf), z(e, c_max, 2 * h, dtype=bf), counts,
+                               c_dev, w1, w1, w2, "swiglu", z(e, c_max, m, dtype=bf), ws,
+                               z(e, c_max, m, dtype=bf), z(e, h, m), z(e, h, m), z(e, m, h), None, None,
+                               st)
     c = stub.calls
     assert c["moe_expert_ffn_bwd"][10:14] == (e, c_max, m, h)
-    assert c["moe_expert_ffn_train"][9:13] == (e, c_max, m, h)
-    assert c["moe_expert_ffn_bwd_saved"][9:13] == (e, c_max, m, h)
-    assert c["moe_expert_ffn_bwd_saved"][17] == M.MOE_F32   # fp32 weight gradients
+    assert c["moe_expert_ffn_train"][10:14] == (e, c_max, m, h)
+    assert c["moe_expert_ffn_bwd_saved"][10:14] == (e, c_max, m, h)
+    assert c["moe_expert_ffn_bwd_saved"][18] == M.MOE_F32   # fp32 weight gradients
     assert c["moe_gate_topk"][4:8] == (s, m, e, k)
     assert c["moe_capacity_locations"][1:4] == (s, e, k)
     assert c["moe_capacity_locations_noalloc"][1:4] == (s, e, k)

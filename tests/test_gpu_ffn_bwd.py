@@ -64,11 +64,10 @@ def _f64(a):
 @pytest.mark.parametrize("w", CASES, ids=lambda w: f"e{w.e}_m{w.m}_h{w.h}_{w.act}")
 def test_expert_ffn_bwd_matches_oracle(w, saved):
     """saved: the forward is moe_expert_ffn_train (its out and hidden must be
-    the plain forward's bit for bit, its pre-activation within one bf16
-    rounding of the fp64 one) and the backward moe_expert_ffn_bwd_saved;
-    "f32": with the weight and bias gradients stored in fp32."""
-    if saved and w.act == "swiglu":
-        pytest.skip("the saved pre-activation is ReLU / GELU only")
+    the plain forward's bit for bit, its kept pre-activation -- SwiGLU: a and
+    b -- within one bf16 rounding of the fp64 one) and the backward
+    moe_expert_ffn_bwd_saved; "f32": with the weight and bias gradients
+    stored in fp32."""
     inp = synth.make_inputs_host(w)
     # routing and the encoded buffer (the forward's expert rows are not needed)
     ref = oracle.layer_forward(w, inp, rows=(np.zeros(1, np.int32), np.zeros(1, np.int64)))
@@ -83,7 +82,8 @@ def test_expert_ffn_bwd_matches_oracle(w, saved):
     _check_bwd(w, inp, buf_h, d_out_h, ref["needed"], kept, c, c_max, saved)
 
 
-@pytest.mark.parametrize("act,saved", [("gelu", False), ("swiglu", False), ("relu", True)])
+@pytest.mark.parametrize("act,saved", [("gelu", False), ("swiglu", False), ("relu", True),
+                                       ("swiglu", True)])
 def test_expert_ffn_bwd_block_edges(act, saved):
     """Kept rows chosen at the weight gradients' 64-row block edges: exactly
     one block, none, a block plus a few rows, a single row, and a count above
@@ -122,8 +122,8 @@ def _check_bwd(w, inp, buf_h, d_out_h, needed, kept, c, c_max, saved=False):
     if saved:
         ws_t = torch.empty_like(ws_f)
         out_t = torch.empty_like(out)
-        pre = torch.empty((e, c_max, h), dtype=bf, device="cuda")
-        M.moe_expert_ffn_train(buf, counts, c_dev, w1, b1, w2, b2, w.act, ws_t, out_t, pre, st)
+        pre = torch.empty((e, c_max, 2 * h if swiglu else h), dtype=bf, device="cuda")
+        M.moe_expert_ffn_train(buf, counts, c_dev, w1, b1, w3, w2, b2, w.act, ws_t, out_t, pre, st)
         torch.cuda.synchronize()
         hid_t = ws_t[: e * c_max * h * 2].view(bf).view(e, c_max, h)
         for j in range(e):
@@ -131,24 +131,27 @@ def _check_bwd(w, inp, buf_h, d_out_h, needed, kept, c, c_max, saved=False):
             assert torch.equal(out_t[j, :r].view(torch.int16), out[j, :r].view(torch.int16)), j
             assert torch.equal(hid_t[j, :r].view(torch.int16), hid[j, :r].view(torch.int16)), j
             x = buf_h[j, :r].astype(np.float64)
-            pre64 = x @ _f64(inp["w1"])[j].T + (_f64(inp["b1"])[j] if inp["b1"] is not None else 0.0)
-            got = to_host(pre[j, :r]).astype(np.float64)
-            # one bf16 rounding of the fp32-accumulated sum
-            tol = 2.0 ** -8 * np.abs(pre64) + 2 * m * 2.0 ** -24 * (np.abs(x) @ np.abs(_f64(inp["w1"])[j].T)) + 1e-6
-            assert np.all(np.abs(got - pre64) <= tol), j
+            mats = [inp["w1"], inp["w3"]] if swiglu else [inp["w1"]]
+            for q, wm in enumerate(mats):   # SwiGLU: a, then b
+                pre64 = x @ _f64(wm)[j].T + (_f64(inp["b1"])[j] if inp["b1"] is not None else 0.0)
+                got = to_host(pre[j, :r, q * h:(q + 1) * h]).astype(np.float64)
+                # one bf16 rounding of the fp32-accumulated sum
+                tol = (2.0 ** -8 * np.abs(pre64) + 2 * m * 2.0 ** -24 * (np.abs(x) @ np.abs(_f64(wm)[j].T))
+                       + 1e-6)
+                assert np.all(np.abs(got - pre64) <= tol), (j, q)
         hid = hid_t
     ws = torch.empty(M.moe_expert_ffn_bwd_workspace_size(M.MOE_BF16, w.act, e, c_max, m, h),
                      dtype=torch.uint8, device="cuda")
     d_buf = torch.full((e, c_max, m), 3.0, dtype=bf, device="cuda")
     gdt = torch.float32 if saved == "f32" else bf   # weight and bias gradients
     d_w1 = torch.empty((e, h, m), dtype=gdt, device="cuda")
-    d_w3 = torch.empty((e, h, m), dtype=bf, device="cuda") if swiglu else None
+    d_w3 = torch.empty((e, h, m), dtype=gdt, device="cuda") if swiglu else None
     d_w2 = torch.empty((e, m, h), dtype=gdt, device="cuda")
     d_b1 = None if swiglu else torch.empty((e, h), dtype=gdt, device="cuda")
     d_b2 = None if swiglu else torch.empty((e, m), dtype=gdt, device="cuda")
     if saved:
-        M.moe_expert_ffn_bwd_saved(buf, hid, pre, counts, c_dev, w1, w2, w.act,
-                                   to_dev(d_out_h).to(bf), ws, d_buf, d_w1, d_w2, d_b1, d_b2, st)
+        M.moe_expert_ffn_bwd_saved(buf, hid, pre, counts, c_dev, w1, w3, w2, w.act,
+                                   to_dev(d_out_h).to(bf), ws, d_buf, d_w1, d_w3, d_w2, d_b1, d_b2, st)
     else:
         M.moe_expert_ffn_bwd(buf, hid, counts, c_dev, w1, b1, w3, w2, w.act, to_dev(d_out_h).to(bf),
                              ws, d_buf, d_w1, d_w3, d_w2, d_b1, d_b2, st)
