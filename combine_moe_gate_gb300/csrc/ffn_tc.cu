@@ -1576,7 +1576,9 @@ moe_status gemm_dswiglu_bmn(const void *d_out, const void *w2, const void *ab, v
     CUtensorMap mA, mB, mO;
     if (!make_map(&mA, d_out, (uint64_t)e * c_max, (uint64_t)m, T2::A_BOX_ROWS, 64) ||
         !make_map(&mB, w2, (uint64_t)e * m, (uint64_t)h, 64, 64) ||
-        !make_map(&mO, d_pre, (uint64_t)e * c_max, 2 * (uint64_t)h, 32, 32))
+        // d_a: the first h columns of each 2h-wide row (the map's extent clips a
+        // box at h, so d_b's columns are never written by it)
+        !make_map(&mO, d_pre, (uint64_t)e * c_max, (uint64_t)h, 32, 32, 2 * (uint64_t)h))
         return MOE_ERR_CUDA;
     GemmArgs g{counts, c_dev, st, nullptr, (__nv_bfloat16 *)d_pre, c_max, e, m, h, m, nullptr,
                nullptr, 0, 0, nullptr, nullptr, (const __nv_bfloat16 *)ab};

@@ -82,14 +82,14 @@ def test_expert_ffn_bwd_matches_oracle(w, saved):
     _check_bwd(w, inp, buf_h, d_out_h, ref["needed"], kept, c, c_max, saved)
 
 
-@pytest.mark.parametrize("act,saved", [("gelu", False), ("swiglu", False), ("relu", True),
-                                       ("swiglu", True)])
-def test_expert_ffn_bwd_block_edges(act, saved):
+@pytest.mark.parametrize("act,saved,h", [("gelu", False, 320), ("swiglu", False, 320), ("relu", True, 320),
+                                         ("swiglu", True, 320), ("swiglu", True, 200), ("gelu", True, 200)])
+def test_expert_ffn_bwd_block_edges(act, saved, h):
     """Kept rows chosen at the weight gradients' 64-row block edges: exactly
     one block, none, a block plus a few rows, a single row, and a count above
     c (kept = c = 200, past three full blocks), with large values in every row
     past the kept ones."""
-    w = _w(s=64, m=192, e=5, k=1, h=320, act=act, capacity_factor=0.0)
+    w = _w(s=64, m=192, e=5, k=1, h=h, act=act, capacity_factor=0.0)   # h = 200: a partial 32-column box
     inp = synth.make_inputs_host(w)
     e, m = w.e, w.m
     needed = np.array([64, 0, 135, 1, 230], np.int32)
