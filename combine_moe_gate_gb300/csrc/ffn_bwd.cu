@@ -347,6 +347,41 @@ moe_status tail_rows_launch(const TailOps &ops, int nops, int64_t c_max, int e,
                       dim3(TR_WARPS * 32), 0, stream, ops, c_max, counts, c_dev, status);
 }
 
+// ------------------------------------------------------- zero empty experts
+namespace {
+
+constexpr int ZE_THREADS = 256, ZE_BLOCKS = 64;   // CTAs per (expert, matrix)
+
+__global__ void __launch_bounds__(ZE_THREADS)
+zero_empty_experts_kernel(ZeroOps ops, int64_t c_max, const int32_t *__restrict__ counts,
+                          const int32_t *__restrict__ c_dev, int32_t *status) {
+    pdl_enter();
+    if (status_bad(status)) return;
+    const int j = blockIdx.y;
+    const int64_t kept = min((int64_t)max(counts[j], 0), min((int64_t)*c_dev, c_max));
+    if (kept > 0) return;
+    const ZeroOp &o = ops.op[blockIdx.z];
+    V16 *dst = reinterpret_cast<V16 *>(static_cast<char *>(o.ptr) + (int64_t)j * o.bytes);
+    const int64_t n = o.bytes / 16;
+    V16 z{};
+    for (int64_t i = (int64_t)blockIdx.x * ZE_THREADS + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * ZE_THREADS)
+        st_v16(dst + i, z);
+}
+
+}  // namespace
+
+moe_status zero_empty_experts_launch(const ZeroOps &ops, int nops, int64_t c_max, int e,
+                                     const int32_t *counts, const int32_t *c_dev, int32_t *status,
+                                     cudaStream_t stream) {
+    if (nops < 1 || nops > 3 || e < 1 || e > 65535 || c_max < 1) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < nops; i++)
+        if (!ops.op[i].ptr || ops.op[i].bytes < 16 || ops.op[i].bytes % 16 || !aligned16(ops.op[i].ptr))
+            return MOE_ERR_INVALID_ARG;
+    return launch_pdl(zero_empty_experts_kernel, dim3(ZE_BLOCKS, (unsigned)e, (unsigned)nops),
+                      dim3(ZE_THREADS), 0, stream, ops, c_max, counts, c_dev, status);
+}
+
 moe_status colsum_launch(const __nv_bfloat16 *src, int e, int64_t c_max, int cols,
                          int64_t src_pitch, const int32_t *counts, const int32_t *c_dev,
                          void *out, int32_t *status, cudaStream_t stream, bool out_f32,

@@ -59,4 +59,19 @@ moe_status tail_rows_launch(const TailOps &ops, int nops, int64_t c_max, int e,
                             const int32_t *counts, const int32_t *c_dev, int32_t *status,
                             cudaStream_t stream);
 
+// Zero the `bytes` of slab b (of up to 3 matrices [e, ...], slab b of matrix i
+// at op[i].ptr + b * op[i].bytes) for every expert b without kept rows
+// (min(counts[b], *c_dev, c_max) == 0); other slabs untouched.  16-byte
+// stores; bytes a multiple of 16, pointers 16-byte aligned.
+struct ZeroOp {
+    void *ptr;
+    int64_t bytes;
+};
+struct ZeroOps {
+    ZeroOp op[3];
+};
+moe_status zero_empty_experts_launch(const ZeroOps &ops, int nops, int64_t c_max, int e,
+                                     const int32_t *counts, const int32_t *c_dev, int32_t *status,
+                                     cudaStream_t stream);
+
 }  // namespace moe

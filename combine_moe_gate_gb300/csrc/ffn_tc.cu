@@ -198,6 +198,11 @@ struct GemmArgs {
     float *out_f32;
     // Elements between rows of out (0: n_out).
     int64_t out_pitch;
+    // MN-major B stacked along K from two maps (SwiGLU's [W1; W3]): K rows from
+    // k_split on come from tmB3, k_split rows earlier (0: tmB only).
+    int32_t k_split;
+    // Per-expert K: experts without K rows get no tiles (nothing written).
+    int32_t skip_empty;
     // Error-path test: the producers issue no copies, so the MMA issuer's
     // bounded wait on the first stage runs out (MOE_ERR_TIMEOUT).
     int32_t stall;
@@ -686,6 +691,9 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 rows = max(0, hi - args.row_lo);
             }
             if (j < e) kept_rows[j] = kmode ? min(max(args.k_counts[j], 0), k_eff) : rows;
+            // per-expert K: an expert without any K rows gets no tiles when asked
+            // (its zero output is written elsewhere)
+            if (kmode && args.skip_empty && j < e && kept_rows[j] == 0) rows = 0;
             const int own = ((rows + BMT - 1) / BMT) * ntn;
             int v = own;
 #pragma unroll
@@ -805,11 +813,13 @@ tc_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                             // two boxes of 64 columns (b_row - j * b_rows is the column)
                             if (prank == 0) mbar_expect_tx(&ctl->full[stage], 2 * B_BOX_BYTES);
                             const int n_col = b_row - T.j * args.b_rows;
+                            const bool second = args.k_split > 0 && kb * BK >= args.k_split;
 #pragma unroll
                             for (int i = 0; i < TN; i++)   // TN boxes of 64 columns
                                 tma_load_2d_pair(sB + stage * B_BYTES + hh * B_BOX_BYTES +
                                                      i * (B_BOX_BYTES / TN),
-                                                 &tmB, n_col + 64 * i, k_row, fb);
+                                                 second ? &tmB3 : &tmB, n_col + 64 * i,
+                                                 second ? k_row - args.k_split : k_row, fb);
                         } else {
                             // SwiGLU: the first CTA's half of B is W1, the second's W3
                             if (prank == 0) mbar_expect_tx(&ctl->full[stage], 2 * B_BOX_BYTES);
@@ -1461,7 +1471,9 @@ namespace moe {
 //                                      d_pre = (d_out w2) * act'(pre) in one
 //                                      product's epilogue instead;
 //   d_buf = d_pre w1                  (B = w1 MN-major in place; SwiGLU:
-//                                      d_pre [w1^T | w3^T], one K-major copy);
+//                                      [d_a | d_b] [w1; w3], both read MN-major
+//                                      in place when h is a multiple of 64,
+//                                      else against one K-major copy);
 //   d_w2 = d_out^T hid, d_w1 = d_pre^T buf (d_w3 = d_b^T buf): the kept rows
 //   are the contraction, each expert over its own (an expert with none gets
 //   zeros), both operands read MN-major in place and each expert's partly
@@ -1525,6 +1537,25 @@ moe_status gemm_bias_bmn(const void *a, const void *b, void *out, const int32_t 
     GemmArgs g{counts, c_dev, st, nullptr, (__nv_bfloat16 *)out, c_max, e, K, n_out, K, nullptr,
                nullptr, 0, 0};
     return launch_gemm<EPI_BIAS_BMN, 1, 64, 2, 1>(mA, mB, mB, mO, g, stream);
+}
+
+// SwiGLU's d_buf = [d_a | d_b] [w1; w3]: A [e * c_max, 2h], B read MN-major
+// from w1 for the first h K rows and from w3 for the next h (h a multiple of
+// the 64-row K block, so no block straddles the two).
+moe_status gemm_bias_bmn2(const void *a, const void *b1, const void *b3, void *out,
+                          const int32_t *counts, const int32_t *c_dev, int e, int64_t c_max, int h,
+                          int n_out, int32_t *st, cudaStream_t stream) {
+    using T2 = Tiling<1, 64, 2, 1>;
+    CUtensorMap mA, mB, mB3, mO;
+    if (!make_map(&mA, a, (uint64_t)e * c_max, 2 * (uint64_t)h, T2::A_BOX_ROWS, 64) ||
+        !make_map(&mB, b1, (uint64_t)e * h, (uint64_t)n_out, 64, 64) ||
+        !make_map(&mB3, b3, (uint64_t)e * h, (uint64_t)n_out, 64, 64) ||
+        !make_map(&mO, out, (uint64_t)e * c_max, (uint64_t)n_out, 32, 32))
+        return MOE_ERR_CUDA;
+    GemmArgs g{counts, c_dev, st, nullptr, (__nv_bfloat16 *)out, c_max, e, 2 * h, n_out, h, nullptr,
+               nullptr, 0, 0};
+    g.k_split = h;
+    return launch_gemm<EPI_BIAS_BMN, 1, 64, 2, 1>(mA, mB, mB3, mO, g, stream);
 }
 
 // d_pre = d_hid * act'(buf w1^T + b1) over the kept rows (ReLU / GELU): the
@@ -1591,7 +1622,9 @@ moe_status gemm_dswiglu_bmn(const void *d_out, const void *w2, const void *ab, v
 // a_cols columns at pitch a_pitch, B rows of b_cols at pitch b_pitch, c_max
 // rows per expert; a_tail / b_tail [e, 64, *] (pitches a_tpitch / b_tpitch)
 // hold each expert's partly kept last 64-row block (tail_rows_launch);
-// out [e, a_cols, b_cols], bf16, or fp32 when out_f32.
+// out [e, a_cols, b_cols], bf16, or fp32 when out_f32.  Experts without kept
+// rows are not written (their zero gradients come from
+// zero_empty_experts_launch).
 moe_status gemm_wgrad_mn(const void *a, int64_t a_pitch, int a_cols, const void *a_tail,
                          int64_t a_tpitch, const void *b, int64_t b_pitch, int b_cols,
                          const void *b_tail, int64_t b_tpitch, void *out, const int32_t *counts,
@@ -1607,6 +1640,7 @@ moe_status gemm_wgrad_mn(const void *a, int64_t a_pitch, int a_cols, const void 
         return MOE_ERR_CUDA;
     GemmArgs g{nullptr, nullptr, st, nullptr, (__nv_bfloat16 *)out, a_cols, e, (int)c_max, b_cols,
                (int)c_max, counts, c_dev, 0, 0};
+    g.skip_empty = 1;   // the zero gradients of experts without kept rows: zero_empty_experts_launch
     if (out_f32) {   // fp32 boxes of 32 rows x 16 columns
         g.out_f32 = (float *)out;
         return launch_gemm<EPI_WGRAD_MN_F32, 1, 64, 2, 1>(mA, mB, mB, mO, g, stream, &mAt, &mBt);
@@ -1645,7 +1679,8 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
     // the data-gradient products read W2 (and W1 for ReLU / GELU) MN-major in
     // place; SwiGLU's [W1 | W3] contraction reads one K-major transposed copy
     // (experts without kept rows are skipped: no tile of theirs reads them)
-    if (swiglu) {
+    const bool swiglu_mn = swiglu && h % 64 == 0;   // [W1; W3] read MN-major in place
+    if (swiglu && !swiglu_mn) {
         MOE_TRY(transpose_pad_launch((const bf *)w1, (int64_t)h * m, m, wT, (int64_t)m * H2, H2, e,
                                      h, m, h, nullptr, counts, c_dev, st, stream));
         MOE_TRY(transpose_pad_launch((const bf *)w3, (int64_t)h * m, m, wT + h, (int64_t)m * H2, H2,
@@ -1669,7 +1704,9 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
         MOE_TRY(gemm_bias_bmn(d_out, w2, dh, counts, c_dev, e, c_max, m, h, st, stream));
         MOE_TRY(gemm_dact(buf, w1, b1, dh, act, dpre, counts, c_dev, e, c_max, m, h, st, stream));
     }
-    if (swiglu)
+    if (swiglu_mn)
+        MOE_TRY(gemm_bias_bmn2(dpre, w1, w3, d_buf, counts, c_dev, e, c_max, h, m, st, stream));
+    else if (swiglu)
         MOE_TRY(gemm_bias(dpre, wT, m, d_buf, nullptr, counts, c_dev, e, c_max, (int)H2, m, st, stream));
     else
         MOE_TRY(gemm_bias_bmn(dpre, w1, d_buf, counts, c_dev, e, c_max, h, m, st, stream));
@@ -1683,6 +1720,14 @@ moe_status ffn_tc_bwd_launch(const void *buf, const void *hid, const int32_t *co
         tails.op[2] = TailOp{dpre, H2, (int)H2, tDp};
         tails.op[3] = TailOp{(const bf *)buf, m, m, tBuf};
         MOE_TRY(tail_rows_launch(tails, 4, c_max, e, counts, c_dev, st, stream));
+        // the weight gradients of experts without kept rows are zero: plain
+        // stores at the HBM rate instead of the products' zero tiles
+        const int64_t gb = wgrad_f32 ? 4 : 2;
+        ZeroOps zo{};
+        zo.op[0] = ZeroOp{d_w1, (int64_t)h * m * gb};
+        zo.op[1] = ZeroOp{d_w2, (int64_t)m * h * gb};
+        zo.op[2] = ZeroOp{d_w3, (int64_t)h * m * gb};
+        MOE_TRY(zero_empty_experts_launch(zo, swiglu ? 3 : 2, c_max, e, counts, c_dev, st, stream));
     }
     MOE_TRY(gemm_wgrad_mn(d_out, m, m, tDo, m, hid, h, h, tHid, h, d_w2, counts, c_dev, e, c_max, st,
                           stream, wgrad_f32));
